@@ -1,0 +1,494 @@
+// mac_host.cu -- the C ABI of libmac_gb300 (declared in include/mac.h):
+// argument checks, workspace layouts, the per-ring event pair that orders
+// the rectify-append on the aux stream, and the kernel launch sequences.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "mac_common.cuh"
+
+namespace mac {
+cudaError_t launch_attend_bf16(const AttendParams &p, int G, int grid, cudaStream_t s);
+cudaError_t launch_attend_f32(const AttendParams &p, int G, int grid, cudaStream_t s);
+int attend_occupancy_bf16(int G, bool paged, int n_units);
+int attend_occupancy_f32(int G, bool paged, int n_units);
+}  // namespace mac
+
+using namespace mac;
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int elem_size(const mac_config *c) { return c->dtype == MAC_F32 ? 4 : 2; }
+
+int validate(const mac_config *c) {
+  if (!c) return MAC_ERR_INVALID_ARG;
+  if (c->batch < 1 || c->n_q_heads < 1 || c->n_kv_heads < 1 || c->ring_k < 1 || c->band_r < 0 ||
+      c->max_context < 1 || c->min_context < 0 || !(c->rope_base > 0.0) || !isfinite(c->tau))
+    return MAC_ERR_INVALID_ARG;
+  if (c->n_q_heads % c->n_kv_heads != 0) return MAC_ERR_INVALID_ARG;
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4) return MAC_ERR_UNSUPPORTED;
+  if (c->head_dim != kHeadDim) return MAC_ERR_UNSUPPORTED;
+  if (c->dtype != MAC_BF16 && c->dtype != MAC_F32) return MAC_ERR_INVALID_ARG;
+  if (c->page_size != 0 && c->page_size != 16) return MAC_ERR_UNSUPPORTED;
+  if (c->thr_mode != MAC_THR_ONE_MINUS_TAU && c->thr_mode != MAC_THR_TAU) return MAC_ERR_INVALID_ARG;
+  if (c->rope_mode < MAC_ROPE_HALF || c->rope_mode > MAC_ROPE_NONE) return MAC_ERR_INVALID_ARG;
+  if ((int64_t)c->batch * c->n_kv_heads > kMaxUnits) return MAC_ERR_UNSUPPORTED;
+  if (c->max_context > 0x7fffffffLL - 1) return MAC_ERR_UNSUPPORTED;
+  return MAC_OK;
+}
+
+mac_ring_layout ring_layout(const mac_config *c) {
+  const size_t B = c->batch, H = c->n_q_heads, K = c->ring_k, d = c->head_dim;
+  const size_t es = elem_size(c);
+  mac_ring_layout L;
+  size_t off = 0;
+  L.pos = off;       off = align_up(off + B * K * 4, 256);
+  L.q = off;         off = align_up(off + B * H * K * d * es, 256);
+  L.o = off;         off = align_up(off + B * H * K * d * 4, 256);
+  L.lse = off;       off = align_up(off + B * H * K * 4, 256);
+  L.stage_q = off;   off = align_up(off + B * H * d * es, 256);
+  L.stage_o = off;   off = align_up(off + B * H * d * 4, 256);
+  L.stage_lse = off; off = align_up(off + B * H * 4, 256);
+  L.total = off;
+  return L;
+}
+
+ScratchLayout scratch_layout(const mac_config *c) {
+  const size_t B = c->batch, H = c->n_q_heads, U = (size_t)c->batch * c->n_kv_heads,
+               d = c->head_dim;
+  const size_t G = c->n_q_heads / c->n_kv_heads;
+  ScratchLayout S;
+  S.max_items = (int64_t)U * max_items_per_unit(c->max_context, c->band_r);
+  size_t off = 0;
+  S.ctl = off;        off = align_up(off + 64 * 4, 256);
+  S.match_part = off; off = align_up(off + B * H * kMaxSplits * 8, 256);
+  S.match_cnt = off;  off = align_up(off + U * 4, 256);
+  S.head_info = off;  off = align_up(off + B * H * 8, 256);
+  S.unit_s = off;     off = align_up(off + U * 4, 256);
+  S.q_rot = off;      off = align_up(off + B * H * d * 4, 256);
+  S.unit_done = off;  off = align_up(off + U * 4, 256);
+  S.seed_pos = off;   off = align_up(off + B * 4, 256);
+  S.seed_len = off;   off = align_up(off + B * 4, 256);
+  S.partials = off;   off = align_up(off + (size_t)S.max_items * G * kPartStride * 4, 256);
+  S.total = off;
+  return S;
+}
+
+float threshold_sq(const mac_config *c) {
+  const double f = (c->thr_mode == MAC_THR_TAU) ? c->tau : (1.0 - c->tau);
+  const double thr = f * sqrt(2.0 * (double)c->head_dim);
+  return (float)(thr * thr);
+}
+
+void rope_table(const mac_config *c, double *w) {
+  for (int j = 0; j < kHeadDim / 2; ++j)
+    w[j] = pow(c->rope_base, -2.0 * (double)j / (double)c->head_dim);
+}
+
+float q_scale(const mac_config *c) { return (float)(1.4426950408889634 / sqrt((double)c->head_dim)); }
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_kv(const mac_config *c, const mac_kv *kv) {
+  if (!kv || !kv->k || !kv->v || !aligned16(kv->k) || !aligned16(kv->v)) return MAC_ERR_INVALID_ARG;
+  if (c->page_size == 0) {
+    if (kv->capacity < 1) return MAC_ERR_INVALID_ARG;
+  } else {
+    if (!kv->page_table || kv->max_pages < 1 || kv->n_pages < 1) return MAC_ERR_INVALID_ARG;
+  }
+  return MAC_OK;
+}
+
+KvView kv_view(const mac_config *c, const mac_kv *kv) {
+  KvView v;
+  v.k = kv->k;
+  v.v = kv->v;
+  v.page_table = kv->page_table;
+  v.paged = c->page_size != 0;
+  v.capacity = v.paged ? (int64_t)kv->max_pages * c->page_size : kv->capacity;
+  v.max_pages = kv->max_pages;
+  v.n_pages = kv->n_pages;
+  return v;
+}
+
+// Largest length the kernels accept: within the cache and within the
+// max_context the scratch was sized for.
+int64_t max_len(const mac_config *c, const KvView &v) {
+  return v.capacity < c->max_context ? v.capacity : c->max_context;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int match_splits(const mac_config *c) {
+  const int units = c->batch * c->n_kv_heads;
+  const int sms = num_sms() > 0 ? num_sms() : 148;
+  int max_s = c->ring_k / 32;
+  if (max_s < 1) max_s = 1;
+  if (max_s > kMaxSplits) max_s = kMaxSplits;
+  int s = (2 * sms + units - 1) / units;
+  if (s > max_s) s = max_s;
+  if (s < 1) s = 1;
+  return s;
+}
+
+int attend_grid_size(const mac_config *c) {
+  const int G = c->n_q_heads / c->n_kv_heads;
+  const int units = c->batch * c->n_kv_heads;
+  const bool paged = c->page_size != 0;
+  int per_sm = c->dtype == MAC_F32 ? attend_occupancy_f32(G, paged, units)
+                                   : attend_occupancy_bf16(G, paged, units);
+  if (per_sm < 1) per_sm = 1;
+  return num_sms() * per_sm;
+}
+
+cudaError_t launch_attend(const AttendParams &p, const mac_config *c, cudaStream_t s) {
+  const int G = c->n_q_heads / c->n_kv_heads;
+  const int grid = attend_grid_size(c);
+  if (grid < 1) return cudaErrorInvalidValue;
+  return c->dtype == MAC_F32 ? launch_attend_f32(p, G, grid, s) : launch_attend_bf16(p, G, grid, s);
+}
+
+// ---- per-ring events: the append of step n on stream_aux must finish before
+// step n+1 on the same ring reads or rewrites the rings ([MAC] K3 runs on an
+// auxiliary stream with a single event dependency).
+struct RingEvents {
+  cudaEvent_t main_done = nullptr, aux_done = nullptr;
+  bool pending = false;
+  unsigned long long capture_id = 0;
+  int device = -1;
+};
+std::mutex g_mu;
+std::unordered_map<void *, RingEvents> g_rings;
+
+unsigned long long capture_id_of(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  unsigned long long id = 0;
+  if (cudaStreamGetCaptureInfo(s, &st, &id) != cudaSuccess) return 0;
+  return st == cudaStreamCaptureStatusActive ? id : 0;
+}
+
+int ctl_check(cudaError_t e) { return e == cudaSuccess ? MAC_OK : MAC_ERR_CUDA; }
+
+AttendParams attend_params(const mac_config *c, const ScratchLayout &S, uint8_t *scratch,
+                           const mac_kv *kv, int mode) {
+  AttendParams a;
+  memset(&a, 0, sizeof a);
+  a.mode = mode;
+  a.check_len = 1;
+  a.B = c->batch;
+  a.Hq = c->n_q_heads;
+  a.Hkv = c->n_kv_heads;
+  a.d = c->head_dim;
+  a.K = c->ring_k;
+  a.r = c->band_r;
+  a.kv = kv_view(c, kv);
+  a.max_len = max_len(c, a.kv);
+  a.q_rot = (const float *)(scratch + S.q_rot);
+  a.ctl = (int32_t *)(scratch + S.ctl);
+  a.unit_done = (int32_t *)(scratch + S.unit_done);
+  a.partials = (float *)(scratch + S.partials);
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mac_workspace_size(const mac_config *cfg, size_t *ring_bytes, size_t *scratch_bytes) {
+  int v = validate(cfg);
+  if (v != MAC_OK) return v;
+  if (ring_bytes) *ring_bytes = ring_layout(cfg).total;
+  if (scratch_bytes) *scratch_bytes = scratch_layout(cfg).total;
+  return MAC_OK;
+}
+
+int mac_ring_layout_of(const mac_config *cfg, mac_ring_layout *layout) {
+  int v = validate(cfg);
+  if (v != MAC_OK) return v;
+  if (!layout) return MAC_ERR_INVALID_ARG;
+  *layout = ring_layout(cfg);
+  return MAC_OK;
+}
+
+float mac_threshold_sq(const mac_config *cfg) {
+  if (validate(cfg) != MAC_OK) return NAN;
+  return threshold_sq(cfg);
+}
+
+const char *mac_status_string(int code) {
+  switch (code) {
+    case MAC_OK: return "ok";
+    case MAC_ERR_INVALID_ARG: return "invalid argument";
+    case MAC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MAC_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int mac_init_rings(const mac_config *cfg, void *ring_ws, void *scratch_ws, const void *q_seed,
+                   const int32_t *prompt_len, int32_t n_seed, const mac_kv *kv, void *stream) {
+  int v = validate(cfg);
+  if (v != MAC_OK) return v;
+  if (!ring_ws || !scratch_ws || !aligned16(ring_ws) || !aligned16(scratch_ws))
+    return MAC_ERR_INVALID_ARG;
+  if (q_seed && (!prompt_len || !kv || n_seed < 1 || n_seed > cfg->ring_k || !aligned16(q_seed)))
+    return MAC_ERR_INVALID_ARG;
+  if (q_seed && (v = check_kv(cfg, kv)) != MAC_OK) return v;
+  cudaStream_t s = (cudaStream_t)stream;
+  const mac_ring_layout R = ring_layout(cfg);
+  const ScratchLayout S = scratch_layout(cfg);
+  uint8_t *ring = (uint8_t *)ring_ws, *scr = (uint8_t *)scratch_ws;
+  if (cudaMemsetAsync(ring + R.pos, 0, (size_t)cfg->batch * cfg->ring_k * 4, s) != cudaSuccess ||
+      cudaMemsetAsync(scr, 0, S.partials, s) != cudaSuccess)
+    return MAC_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_rings.find(ring_ws);
+    if (it != g_rings.end()) it->second.pending = false;
+  }
+  if (!q_seed) return ctl_check(cudaGetLastError());
+
+  RopeParams rp;
+  memset(&rp, 0, sizeof rp);
+  rp.B = cfg->batch;
+  rp.Hq = cfg->n_q_heads;
+  rp.d = cfg->head_dim;
+  rp.r = cfg->band_r;
+  rp.rope_mode = cfg->rope_mode;
+  rp.n_seed = n_seed;
+  rp.q_scale = q_scale(cfg);
+  rp.q = q_seed;
+  rp.pos_base = prompt_len;
+  rp.q_rot = (float *)(scr + S.q_rot);
+  rp.seed_pos = (int32_t *)(scr + S.seed_pos);
+  rp.seed_len = (int32_t *)(scr + S.seed_len);
+  rp.ctl = (int32_t *)(scr + S.ctl);
+  rope_table(cfg, rp.rope_w);
+
+  AttendParams ap = attend_params(cfg, S, scr, kv, MODE_FULL);
+  ap.check_len = 0;  // summary lengths p - r may be < 1 (empty summaries)
+  ap.len = rp.seed_len;
+  ap.out = (float *)(ring + R.stage_o);
+  ap.out_lse = (float *)(ring + R.stage_lse);
+
+  AppendParams qp;
+  memset(&qp, 0, sizeof qp);
+  qp.B = cfg->batch;
+  qp.Hq = cfg->n_q_heads;
+  qp.d = cfg->head_dim;
+  qp.K = cfg->ring_k;
+  qp.n_seed = n_seed;
+  qp.pos = rp.seed_pos;
+  qp.capacity = max_len(cfg, kv_view(cfg, kv));
+  qp.q_src = q_seed;
+  qp.src_o = ap.out;
+  qp.src_lse = ap.out_lse;
+  qp.ring_pos = (int32_t *)(ring + R.pos);
+  qp.ring_q = ring + R.q;
+  qp.ring_o = (float *)(ring + R.o);
+  qp.ring_lse = (float *)(ring + R.lse);
+
+  for (int i = 0; i < n_seed; ++i) {
+    rp.seed_index = i;
+    rp.pos_add = -n_seed + 1 + i;
+    qp.seed_index = i;
+    cudaError_t e = launch_rope(rp, cfg->dtype, s);
+    if (e == cudaSuccess) e = launch_attend(ap, cfg, s);
+    if (e == cudaSuccess) e = launch_append(qp, cfg->dtype, s);
+    if (e != cudaSuccess) return MAC_ERR_CUDA;
+  }
+  return MAC_OK;
+}
+
+int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, const void *q_pre,
+                    const int32_t *seq_len, const mac_kv *kv, float *out, int32_t *match_pos,
+                    void *stream_main, void *stream_aux) {
+  int v = validate(cfg);
+  if (v != MAC_OK) return v;
+  if (!ring_ws || !scratch_ws || !q_pre || !seq_len || !out || !aligned16(ring_ws) ||
+      !aligned16(scratch_ws) || !aligned16(q_pre) || !aligned16(out))
+    return MAC_ERR_INVALID_ARG;
+  if ((v = check_kv(cfg, kv)) != MAC_OK) return v;
+  cudaStream_t sm = (cudaStream_t)stream_main;
+  cudaStream_t sa = stream_aux ? (cudaStream_t)stream_aux : sm;
+  const bool use_aux = sa != sm;
+  const mac_ring_layout R = ring_layout(cfg);
+  const ScratchLayout S = scratch_layout(cfg);
+  uint8_t *ring = (uint8_t *)ring_ws, *scr = (uint8_t *)scratch_ws;
+  const unsigned long long cap_id = capture_id_of(sm);
+
+  RingEvents *ev = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    RingEvents &e = g_rings[ring_ws];
+    if (use_aux && !e.main_done) {
+      cudaGetDevice(&e.device);
+      if (cudaEventCreateWithFlags(&e.main_done, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&e.aux_done, cudaEventDisableTiming) != cudaSuccess)
+        return MAC_ERR_CUDA;
+    }
+    if (e.pending && e.capture_id == cap_id) {
+      if (cudaStreamWaitEvent(sm, e.aux_done, 0) != cudaSuccess) return MAC_ERR_CUDA;
+    }
+    e.pending = false;
+    ev = &e;
+  }
+
+  MatchParams mp;
+  memset(&mp, 0, sizeof mp);
+  mp.B = cfg->batch;
+  mp.Hq = cfg->n_q_heads;
+  mp.Hkv = cfg->n_kv_heads;
+  mp.G = cfg->n_q_heads / cfg->n_kv_heads;
+  mp.d = cfg->head_dim;
+  mp.K = cfg->ring_k;
+  mp.r = cfg->band_r;
+  mp.min_context = cfg->min_context;
+  mp.n_splits = match_splits(cfg);
+  mp.thr2 = threshold_sq(cfg);
+  mp.q_scale = q_scale(cfg);
+  mp.rope_mode = cfg->rope_mode;
+  mp.q_pre = q_pre;
+  mp.seq_len = seq_len;
+  mp.capacity = max_len(cfg, kv_view(cfg, kv));
+  mp.ring_pos = (const int32_t *)(ring + R.pos);
+  mp.ring_q = ring + R.q;
+  mp.stage_q = ring + R.stage_q;
+  mp.ctl = (int32_t *)(scr + S.ctl);
+  mp.match_part = (int2 *)(scr + S.match_part);
+  mp.match_cnt = (int32_t *)(scr + S.match_cnt);
+  mp.head_info = (int2 *)(scr + S.head_info);
+  mp.unit_s = (int32_t *)(scr + S.unit_s);
+  mp.q_rot = (float *)(scr + S.q_rot);
+  mp.match_pos_out = match_pos;
+  rope_table(cfg, mp.rope_w);
+  if (launch_match(mp, cfg->dtype, sm) != cudaSuccess) return MAC_ERR_CUDA;
+
+  AttendParams ap = attend_params(cfg, S, scr, kv, MODE_DECODE);
+  ap.check_len = 0;  // the match kernel already flagged bad lengths
+  ap.len = seq_len;
+  ap.head_info = mp.head_info;
+  ap.unit_s = mp.unit_s;
+  ap.ring_o = (const float *)(ring + R.o);
+  ap.ring_lse = (const float *)(ring + R.lse);
+  ap.as_o = (float *)(ring + R.stage_o);
+  ap.as_lse = (float *)(ring + R.stage_lse);
+  ap.out = out;
+  if (launch_attend(ap, cfg, sm) != cudaSuccess) return MAC_ERR_CUDA;
+
+  AppendParams qp;
+  memset(&qp, 0, sizeof qp);
+  qp.B = cfg->batch;
+  qp.Hq = cfg->n_q_heads;
+  qp.d = cfg->head_dim;
+  qp.K = cfg->ring_k;
+  qp.pos = seq_len;
+  qp.capacity = mp.capacity;
+  qp.q_src = ring + R.stage_q;
+  qp.src_o = ap.as_o;
+  qp.src_lse = ap.as_lse;
+  qp.ring_pos = (int32_t *)(ring + R.pos);
+  qp.ring_q = ring + R.q;
+  qp.ring_o = (float *)(ring + R.o);
+  qp.ring_lse = (float *)(ring + R.lse);
+  if (use_aux) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (cudaEventRecord(ev->main_done, sm) != cudaSuccess ||
+        cudaStreamWaitEvent(sa, ev->main_done, 0) != cudaSuccess)
+      return MAC_ERR_CUDA;
+    if (launch_append(qp, cfg->dtype, sa) != cudaSuccess) return MAC_ERR_CUDA;
+    if (cudaEventRecord(ev->aux_done, sa) != cudaSuccess) return MAC_ERR_CUDA;
+    ev->pending = true;
+    ev->capture_id = cap_id;
+  } else {
+    if (launch_append(qp, cfg->dtype, sm) != cudaSuccess) return MAC_ERR_CUDA;
+  }
+  return MAC_OK;
+}
+
+int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pre,
+                       const int32_t *seq_len, const mac_kv *kv, float *out, float *lse,
+                       void *stream) {
+  int v = validate(cfg);
+  if (v != MAC_OK) return v;
+  if (!scratch_ws || !q_pre || !seq_len || !out || !aligned16(scratch_ws) || !aligned16(q_pre) ||
+      !aligned16(out))
+    return MAC_ERR_INVALID_ARG;
+  if ((v = check_kv(cfg, kv)) != MAC_OK) return v;
+  cudaStream_t s = (cudaStream_t)stream;
+  const ScratchLayout S = scratch_layout(cfg);
+  uint8_t *scr = (uint8_t *)scratch_ws;
+
+  RopeParams rp;
+  memset(&rp, 0, sizeof rp);
+  rp.B = cfg->batch;
+  rp.Hq = cfg->n_q_heads;
+  rp.d = cfg->head_dim;
+  rp.r = cfg->band_r;
+  rp.rope_mode = cfg->rope_mode;
+  rp.q_scale = q_scale(cfg);
+  rp.q = q_pre;
+  rp.pos_base = seq_len;
+  rp.q_rot = (float *)(scr + S.q_rot);
+  rp.ctl = (int32_t *)(scr + S.ctl);
+  rope_table(cfg, rp.rope_w);
+  if (launch_rope(rp, cfg->dtype, s) != cudaSuccess) return MAC_ERR_CUDA;
+
+  AttendParams ap = attend_params(cfg, S, scr, kv, MODE_FULL);
+  ap.len = seq_len;
+  ap.out = out;
+  ap.out_lse = lse;
+  if (launch_attend(ap, cfg, s) != cudaSuccess) return MAC_ERR_CUDA;
+  return MAC_OK;
+}
+
+int mac_join_aux(void *ring_ws, void *stream_main) {
+  if (!ring_ws) return MAC_ERR_INVALID_ARG;
+  cudaStream_t sm = (cudaStream_t)stream_main;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_rings.find(ring_ws);
+  if (it == g_rings.end() || !it->second.pending) return MAC_OK;
+  if (it->second.capture_id == capture_id_of(sm)) {
+    if (cudaStreamWaitEvent(sm, it->second.aux_done, 0) != cudaSuccess) return MAC_ERR_CUDA;
+  }
+  it->second.pending = false;
+  return MAC_OK;
+}
+
+int mac_release_ring(void *ring_ws) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_rings.find(ring_ws);
+  if (it == g_rings.end()) return MAC_OK;
+  if (it->second.main_done) cudaEventDestroy(it->second.main_done);
+  if (it->second.aux_done) cudaEventDestroy(it->second.aux_done);
+  g_rings.erase(it);
+  return MAC_OK;
+}
+
+int mac_last_status(const mac_config *cfg, void *scratch_ws, int32_t *device_status, void *stream) {
+  int v = validate(cfg);
+  if (v != MAC_OK) return v;
+  if (!scratch_ws || !device_status) return MAC_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const ScratchLayout S = scratch_layout(cfg);
+  int32_t *ctl = (int32_t *)((uint8_t *)scratch_ws + S.ctl);
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, ctl, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess || cudaMemsetAsync(ctl, 0, sizeof host, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MAC_ERR_CUDA;
+  *device_status = host;
+  return MAC_OK;
+}
+
+}  // extern "C"

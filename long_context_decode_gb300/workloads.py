@@ -248,3 +248,68 @@ def paginate(k: np.ndarray, v: np.ndarray, page_size: int, rng: np.random.Genera
         kp[table[b]] = kb
         vp[table[b]] = vb
     return kp, vp, table
+
+
+# --------------------------------------------------------------------------
+# device-side K/V (large caches: drawn on the GPU with a seeded generator)
+# --------------------------------------------------------------------------
+
+def device_kv(w: Workload, capacity: int, device, seed_offset: int = 0):
+    """Contiguous K, V [B, Hkv, capacity, d] drawn on ``device`` (torch
+    generator seeded from the workload), key structure applied, stored in the
+    workload dtype (torch.bfloat16 or torch.float32)."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(w.seed) * 1000 + 17 + seed_offset)
+    shape = (w.batch, w.n_kv_heads, capacity, w.head_dim)
+    dt = torch.bfloat16 if w.dtype == BF16 else torch.float32
+    k = torch.empty(shape, dtype=dt, device=device)
+    v = torch.empty(shape, dtype=dt, device=device)
+    pos = np.arange(1, capacity + 1)
+    for b in range(w.batch):
+        for g in range(w.n_kv_heads):
+            kb = torch.randn((capacity, w.head_dim), generator=gen, device=device)
+            vb = torch.randn((capacity, w.head_dim), generator=gen, device=device)
+            if w.keys == "recency":
+                sc = torch.from_numpy(w.key_scale(b, pos).astype(np.float32)).to(device)
+                kb *= sc[:, None]
+            if w.keys == "heavy_hitters":
+                hh = torch.from_numpy(w.heavy_hitters(b)[g] - 1).to(device)
+                kb[hh] *= 4.0
+            k[b, g] = kb.to(dt)
+            v[b, g] = vb.to(dt)
+    return k, v
+
+
+def device_paged_kv(w: Workload, extra_steps: int, device, page_seed: int = 5):
+    """Paged K, V [n_pages, Hkv, 16, d] on ``device`` holding each request's
+    own ceil((L_b + steps)/16) pages at shuffled physical ids, and the page
+    table [B, max_pages] (int32, -1 past a request's last page)."""
+    import torch
+
+    ps = 16
+    need = [(L + w.n_steps + extra_steps + ps - 1) // ps for L in w.contexts]
+    total, max_pages = sum(need), max(need)
+    perm = np.random.default_rng([page_seed, w.seed]).permutation(total).astype(np.int32)
+    table = np.full((w.batch, max_pages), -1, np.int32)
+    off = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[off:off + n]
+        off += n
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(w.seed) * 1000 + 29)
+    dt = torch.bfloat16 if w.dtype == BF16 else torch.float32
+    shape = (total, w.n_kv_heads, ps, w.head_dim)
+    kp = torch.empty(shape, dtype=dt, device=device)
+    vp = torch.empty(shape, dtype=dt, device=device)
+    for b, n in enumerate(need):
+        ids = torch.from_numpy(table[b, :n].astype(np.int64)).to(device)
+        for g in range(w.n_kv_heads):
+            kb = torch.randn((n * ps, w.head_dim), generator=gen, device=device)
+            vb = torch.randn((n * ps, w.head_dim), generator=gen, device=device)
+            if w.keys == "heavy_hitters":
+                kb[torch.from_numpy(w.heavy_hitters(b)[g] - 1).to(device)] *= 4.0
+            kp[ids, g] = kb.view(n, ps, w.head_dim).to(dt)
+            vp[ids, g] = vb.view(n, ps, w.head_dim).to(dt)
+    return kp, vp, table

@@ -261,6 +261,8 @@ def flags(res: dict, thr2: float, rel: float = 1e-6) -> np.ndarray:
     ``rel`` of the threshold, or a runner-up within ``rel`` of the minimum."""
     dmin, dsec = res["dmin"], res["dsecond"]
     fin = np.isfinite(dmin)
-    near_thr = fin & (np.abs(dmin - thr2) <= rel * thr2)
-    near_tie = fin & np.isfinite(dsec) & ((dsec - dmin) <= rel * dmin)
+    both = fin & np.isfinite(dsec)
+    near_thr = fin & (np.abs(np.where(fin, dmin, 0.0) - thr2) <= rel * thr2)
+    gap = np.where(both, dsec, 0.0) - np.where(both, dmin, 0.0)
+    near_tie = both & (gap <= rel * np.where(both, dmin, 0.0))
     return near_thr | near_tie

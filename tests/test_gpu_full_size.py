@@ -1,0 +1,47 @@
+"""Parity at the benchmark workloads' full sizes (32K, 4 x 128K, 256K, 16
+mixed paged requests of 8K-128K), with the kernels' production launch
+configuration: trajectories from empty rings, every (request, head)
+decision compared every step, outputs compared on a seeded sample of heads
+(the oracle computes those heads' attention; the match runs for all)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+from harness import TOL, Problem, compare, gpu_trajectory, oracle_trajectory  # noqa: E402
+from long_context_decode_gb300 import mac  # noqa: E402
+from long_context_decode_gb300.workloads import WORKLOADS  # noqa: E402
+from oracle import mac_oracle as O  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_decode_gb300 import build as b
+    b.build()
+    mac.load()
+
+
+@pytest.mark.parametrize("name,steps,sample", [
+    ("llama8b-32k", 40, 12),
+    ("long-128k", 24, 12),
+    ("verylong-256k", 24, 8),
+    ("mixed-paged", 12, 12),
+])
+def test_full_size_workload(name, steps, sample):
+    w = WORKLOADS[name].with_(n_steps=steps)
+    P = Problem(w, device_generated=True, native_paged=w.page_size > 0)
+    rng = np.random.default_rng(123)
+    mask = np.zeros((w.batch, w.n_q_heads), np.uint8)
+    flat = rng.choice(w.batch * w.n_q_heads, size=min(sample, w.batch * w.n_q_heads), replace=False)
+    mask.reshape(-1)[flat] = 1
+    gpu, st, layer = gpu_trajectory(P, steps)
+    ref = oracle_trajectory(P, steps, head_mask=mask)
+    c = compare(gpu, ref, O.threshold_sq(128, w.tau), head_mask=mask)
+    assert st == 0
+    assert c["mismatched"] == 0, c
+    assert c["max_err"] <= TOL, c
+    assert c["hits"] > 0
+    layer.release()
