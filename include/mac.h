@@ -173,6 +173,14 @@ int mac_release_ring(void *ring_ws);
 int mac_last_status(const mac_config *cfg, void *scratch_ws, int32_t *device_status,
                     void *stream);
 
+/* Profiling hook (no counterpart on the pages): the next mac_decode_step
+ * issued by the calling thread records these CUDA events (cudaEvent_t
+ * handles, each may be NULL) on stream_main: before the match kernel, after
+ * it, and after the attend kernel; then the hook clears itself.  Lets a
+ * caller time the kernels on the stream they run on, also inside a captured
+ * graph. */
+int mac_set_phase_events(void *before_match, void *after_match, void *after_attend);
+
 /* Static string for a MAC_OK / MAC_ERR_* code. */
 const char *mac_status_string(int code);
 

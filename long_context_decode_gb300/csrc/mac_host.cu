@@ -179,6 +179,23 @@ unsigned long long capture_id_of(cudaStream_t s) {
 
 int ctl_check(cudaError_t e) { return e == cudaSuccess ? MAC_OK : MAC_ERR_CUDA; }
 
+// events armed by mac_set_phase_events for this thread's next decode step
+thread_local cudaEvent_t t_phase[3] = {nullptr, nullptr, nullptr};
+
+// Inside a stream capture the record becomes an event-record node of the
+// graph (timestamped at replay), not a capture-time dependency marker.
+cudaError_t record_phase(int i, cudaStream_t s) {
+  if (!t_phase[i]) return cudaSuccess;
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &st);
+  if (e == cudaSuccess)
+    e = st == cudaStreamCaptureStatusActive
+            ? cudaEventRecordWithFlags(t_phase[i], s, cudaEventRecordExternal)
+            : cudaEventRecord(t_phase[i], s);
+  t_phase[i] = nullptr;
+  return e;
+}
+
 AttendParams attend_params(const mac_config *c, const ScratchLayout &S, uint8_t *scratch,
                            const mac_kv *kv, int mode) {
   AttendParams a;
@@ -372,7 +389,9 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
   mp.q_rot = (float *)(scr + S.q_rot);
   mp.match_pos_out = match_pos;
   rope_table(cfg, mp.rope_w);
+  if (record_phase(0, sm) != cudaSuccess) return MAC_ERR_CUDA;
   if (launch_match(mp, cfg->dtype, sm) != cudaSuccess) return MAC_ERR_CUDA;
+  if (record_phase(1, sm) != cudaSuccess) return MAC_ERR_CUDA;
 
   AttendParams ap = attend_params(cfg, S, scr, kv, MODE_DECODE);
   ap.check_len = 0;  // the match kernel already flagged bad lengths
@@ -385,6 +404,7 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
   ap.as_lse = (float *)(ring + R.stage_lse);
   ap.out = out;
   if (launch_attend(ap, cfg, sm) != cudaSuccess) return MAC_ERR_CUDA;
+  if (record_phase(2, sm) != cudaSuccess) return MAC_ERR_CUDA;
 
   AppendParams qp;
   memset(&qp, 0, sizeof qp);
@@ -462,6 +482,13 @@ int mac_join_aux(void *ring_ws, void *stream_main) {
     if (cudaStreamWaitEvent(sm, it->second.aux_done, 0) != cudaSuccess) return MAC_ERR_CUDA;
   }
   it->second.pending = false;
+  return MAC_OK;
+}
+
+int mac_set_phase_events(void *before_match, void *after_match, void *after_attend) {
+  t_phase[0] = (cudaEvent_t)before_match;
+  t_phase[1] = (cudaEvent_t)after_match;
+  t_phase[2] = (cudaEvent_t)after_attend;
   return MAC_OK;
 }
 

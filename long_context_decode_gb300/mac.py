@@ -21,7 +21,7 @@ MAC_ROPE_HALF, MAC_ROPE_INTERLEAVED, MAC_ROPE_NONE = 0, 1, 2
 # every function the header declares (checked against include/mac.h by the tests)
 EXPORTS = ("mac_workspace_size", "mac_ring_layout_of", "mac_init_rings", "mac_decode_step",
            "mac_full_attention", "mac_join_aux", "mac_release_ring", "mac_last_status",
-           "mac_status_string", "mac_threshold_sq")
+           "mac_set_phase_events", "mac_status_string", "mac_threshold_sq")
 
 
 class mac_config(ctypes.Structure):
@@ -76,6 +76,7 @@ def load() -> ctypes.CDLL:
     L.mac_join_aux.argtypes = [vp, vp]
     L.mac_release_ring.argtypes = [vp]
     L.mac_last_status.argtypes = [P(mac_config), vp, P(i32), vp]
+    L.mac_set_phase_events.argtypes = [vp, vp, vp]
     L.mac_status_string.argtypes = [ctypes.c_int]
     L.mac_status_string.restype = ctypes.c_char_p
     L.mac_threshold_sq.argtypes = [P(mac_config)]
@@ -158,6 +159,17 @@ def mac_last_status(cfg, scratch, stream=None) -> int:
     _check(load().mac_last_status(ctypes.byref(cfg), _ptr(scratch), ctypes.byref(st), _stream(stream)),
            "mac_last_status")
     return st.value
+
+
+def mac_set_phase_events(before_match=None, after_match=None, after_attend=None):
+    """Arm the next mac_decode_step on this thread to record these
+    torch.cuda.Event objects (or raw cudaEvent_t handles)."""
+    def h(e):
+        if e is None or isinstance(e, int):
+            return e
+        return e.cuda_event
+    _check(load().mac_set_phase_events(h(before_match), h(after_match), h(after_attend)),
+           "mac_set_phase_events")
 
 
 def mac_status_string(code: int) -> str:

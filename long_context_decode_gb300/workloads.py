@@ -282,6 +282,49 @@ def device_kv(w: Workload, capacity: int, device, seed_offset: int = 0):
     return k, v
 
 
+def device_queries(w: Workload, n_pos: int, device, stream_seed: int = 0):
+    """[B, Hq, n_pos, d] pre-RoPE queries drawn on ``device`` with the
+    workload's query process (same processes as ``Workload.queries``, drawn
+    with a torch generator), stored in the workload dtype."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(w.seed) * 7919 + 101 + int(stream_seed))
+    H, d = w.batch * w.n_q_heads, w.head_dim
+    f32 = dict(device=device, dtype=torch.float32)
+    if w.query == "clustered":
+        cent = torch.randn((H, 16, d), generator=gen, **f32)
+        switch = torch.rand((H, n_pos), generator=gen, **f32) < 0.01
+        switch[:, 0] = True
+        newz = torch.randint(0, 16, (H, n_pos), generator=gen, device=device)
+        t = torch.arange(n_pos, device=device).expand(H, n_pos)
+        last = torch.cummax(torch.where(switch, t, torch.zeros_like(t)), dim=1).values
+        z = newz.gather(1, last)
+        q = cent[torch.arange(H, device=device)[:, None], z]
+        q += 0.05 * torch.randn((H, n_pos, d), generator=gen, **f32)
+    else:
+        if w.query == "ar1_jump":
+            rho, sigma, jp = 0.95, 0.31, torch.full((H,), 1.0 / 8.0, **f32)
+        elif w.query == "ar1_098":
+            rho, sigma, jp = 0.98, float(np.sqrt(1 - 0.98 ** 2)), torch.zeros((H,), **f32)
+        elif w.query == "ar1_skew":
+            per = torch.tensor([0.1, 0.3, 0.5, 0.7], **f32)
+            jp = per[torch.arange(w.n_q_heads, device=device) % w.group % 4].repeat(w.batch)
+            rho, sigma = 0.95, 0.31
+        else:
+            raise ValueError(w.query)
+        q = torch.empty((H, n_pos, d), **f32)
+        cur = torch.randn((H, d), generator=gen, **f32)
+        q[:, 0] = cur
+        for i in range(1, n_pos):
+            nxt = rho * cur + sigma * torch.randn((H, d), generator=gen, **f32)
+            jump = torch.rand((H,), generator=gen, **f32) < jp
+            cur = torch.where(jump[:, None], torch.randn((H, d), generator=gen, **f32), nxt)
+            q[:, i] = cur
+    dt = torch.bfloat16 if w.dtype == BF16 else torch.float32
+    return q.view(w.batch, w.n_q_heads, n_pos, d).to(dt)
+
+
 def device_paged_kv(w: Workload, extra_steps: int, device, page_seed: int = 5):
     """Paged K, V [n_pages, Hkv, 16, d] on ``device`` holding each request's
     own ceil((L_b + steps)/16) pages at shuffled physical ids, and the page
