@@ -160,6 +160,34 @@ int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pr
                        const int32_t *seq_len, const mac_kv *kv, float *out, float *lse,
                        void *stream);
 
+/* Largest scratch workspace mac_full_attention_noalloc can use (32 MiB). */
+#define MAC_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* mac_full_attention without a caller-provided scratch workspace.  (The
+ * pages have no counterpart; this is a packaging variant.)  For callers that
+ * cannot allocate device memory: code whose device memory is owned by
+ * another allocator it may not call into, code that must not trigger the
+ * device-wide synchronisation cudaMalloc can cause, or code running under a
+ * fixed memory budget decided at start-up.  The scratch lives in a 32 MiB
+ * array compiled into this library (MAC_NOALLOC_SCRATCH_BYTES); every GPU
+ * that loads the library holds that array until the process exits.
+ *   - Same arguments and results as mac_full_attention, minus scratch_ws.
+ *   - Returns MAC_ERR_UNSUPPORTED, without enqueueing anything, when the
+ *     configuration's scratch (mac_workspace_size) exceeds
+ *     MAC_NOALLOC_SCRATCH_BYTES.
+ *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
+ *     call.  The first call on a device looks up the array's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array.  Each call clears the
+ *     array's counters on its stream before launching, so calls on one
+ *     stream are fine; calls that overlap on the GPU (different streams, or
+ *     different host threads without ordering) race on the array and give
+ *     wrong results.  The device status word of these calls is cleared by
+ *     the next call and is not readable through mac_last_status. */
+int mac_full_attention_noalloc(const mac_config *cfg, const void *q_pre, const int32_t *seq_len,
+                               const mac_kv *kv, float *out, float *lse, void *stream);
+
 /* Make stream_main wait for the last append enqueued on ring_ws (no-op if
  * none is pending).  Needed before ending a stream capture that used a
  * separate aux stream. */

@@ -179,6 +179,28 @@ unsigned long long capture_id_of(cudaStream_t s) {
 
 int ctl_check(cudaError_t e) { return e == cudaSuccess ? MAC_OK : MAC_ERR_CUDA; }
 
+// Scratch of mac_full_attention_noalloc: a fixed array inside the library,
+// for callers that cannot allocate device memory.  Host code must not pass
+// the symbol itself to a kernel (on the host it names a host-side stand-in);
+// noalloc_scratch() returns its device address.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MAC_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[256] = {nullptr};  // per device, looked up once
+
+// Device address of g_noalloc_scratch on the current device (nullptr on error).
+void *noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
 // events armed by mac_set_phase_events for this thread's next decode step
 thread_local cudaEvent_t t_phase[3] = {nullptr, nullptr, nullptr};
 
@@ -470,6 +492,22 @@ int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pr
   ap.out_lse = lse;
   if (launch_attend(ap, cfg, s) != cudaSuccess) return MAC_ERR_CUDA;
   return MAC_OK;
+}
+
+int mac_full_attention_noalloc(const mac_config *cfg, const void *q_pre, const int32_t *seq_len,
+                               const mac_kv *kv, float *out, float *lse, void *stream) {
+  int v = validate(cfg);
+  if (v != MAC_OK) return v;
+  if (scratch_layout(cfg).total > MAC_NOALLOC_SCRATCH_BYTES) return MAC_ERR_UNSUPPORTED;
+  if (!q_pre || !seq_len || !out || !aligned16(q_pre) || !aligned16(out)) return MAC_ERR_INVALID_ARG;
+  if ((v = check_kv(cfg, kv)) != MAC_OK) return v;
+  void *scratch = noalloc_scratch();
+  if (!scratch) return MAC_ERR_CUDA;
+  // the previous call left its counters and status in the array: clear the
+  // control part (everything before the partials) on this call's stream
+  if (cudaMemsetAsync(scratch, 0, scratch_layout(cfg).partials, (cudaStream_t)stream) != cudaSuccess)
+    return MAC_ERR_CUDA;
+  return mac_full_attention(cfg, scratch, q_pre, seq_len, kv, out, lse, stream);
 }
 
 int mac_join_aux(void *ring_ws, void *stream_main) {

@@ -20,8 +20,9 @@ MAC_ROPE_HALF, MAC_ROPE_INTERLEAVED, MAC_ROPE_NONE = 0, 1, 2
 
 # every function the header declares (checked against include/mac.h by the tests)
 EXPORTS = ("mac_workspace_size", "mac_ring_layout_of", "mac_init_rings", "mac_decode_step",
-           "mac_full_attention", "mac_join_aux", "mac_release_ring", "mac_last_status",
-           "mac_set_phase_events", "mac_status_string", "mac_threshold_sq")
+           "mac_full_attention", "mac_full_attention_noalloc", "mac_join_aux", "mac_release_ring",
+           "mac_last_status", "mac_set_phase_events", "mac_status_string", "mac_threshold_sq")
+MAC_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class mac_config(ctypes.Structure):
@@ -73,6 +74,7 @@ def load() -> ctypes.CDLL:
     L.mac_init_rings.argtypes = [P(mac_config), vp, vp, vp, vp, i32, P(mac_kv), vp]
     L.mac_decode_step.argtypes = [P(mac_config), vp, vp, vp, vp, P(mac_kv), vp, vp, vp, vp]
     L.mac_full_attention.argtypes = [P(mac_config), vp, vp, vp, P(mac_kv), vp, vp, vp]
+    L.mac_full_attention_noalloc.argtypes = [P(mac_config), vp, vp, P(mac_kv), vp, vp, vp]
     L.mac_join_aux.argtypes = [vp, vp]
     L.mac_release_ring.argtypes = [vp]
     L.mac_last_status.argtypes = [P(mac_config), vp, P(i32), vp]
@@ -144,6 +146,14 @@ def mac_full_attention(cfg, scratch, q_pre, seq_len, kv: mac_kv, out, lse=None, 
     _check(load().mac_full_attention(ctypes.byref(cfg), _ptr(scratch), _ptr(q_pre), _ptr(seq_len),
                                      ctypes.byref(kv), _ptr(out), _ptr(lse), _stream(stream)),
            "mac_full_attention")
+
+
+def mac_full_attention_noalloc(cfg, q_pre, seq_len, kv: mac_kv, out, lse=None, stream=None):
+    """mac_full_attention with its scratch in the library's fixed array
+    (for callers that cannot allocate device memory; see include/mac.h)."""
+    _check(load().mac_full_attention_noalloc(ctypes.byref(cfg), _ptr(q_pre), _ptr(seq_len),
+                                             ctypes.byref(kv), _ptr(out), _ptr(lse), _stream(stream)),
+           "mac_full_attention_noalloc")
 
 
 def mac_join_aux(ring, stream_main=None):
