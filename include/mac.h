@@ -203,11 +203,20 @@ int mac_last_status(const mac_config *cfg, void *scratch_ws, int32_t *device_sta
 
 /* Profiling hook (no counterpart on the pages): the next mac_decode_step
  * issued by the calling thread records these CUDA events (cudaEvent_t
- * handles, each may be NULL) on stream_main: before the match kernel, after
- * it, and after the attend kernel; then the hook clears itself.  Lets a
- * caller time the kernels on the stream they run on, also inside a captured
- * graph. */
-int mac_set_phase_events(void *before_match, void *after_match, void *after_attend);
+ * handles, each may be NULL): before and after the step kernel (match and
+ * attention) on stream_main, and after the append kernel on the stream it
+ * runs on; then the hook clears itself.  Lets a caller time the kernels on
+ * the stream they run on, also inside a captured graph. */
+int mac_set_phase_events(void *before_step, void *after_step, void *after_append);
+
+/* Profiling hook (no counterpart on the pages): the next step kernel
+ * launched by the calling thread (decode step or full attention) writes, per
+ * CTA, 8 uint64 %globaltimer stamps (ns) into device_buffer
+ * [grid][8]: start, end of the match, after the first grid barrier, after
+ * laying out the chunks, end of the attention, after the second grid
+ * barrier, end; unused stamps are left as they were.  The buffer must hold
+ * 8 * (number of SMs) uint64.  The hook clears itself. */
+int mac_set_trace(void *device_buffer);
 
 /* Static string for a MAC_OK / MAC_ERR_* code. */
 const char *mac_status_string(int code);

@@ -19,18 +19,20 @@ namespace mac {
 // ---------------------------------------------------------------------------
 // work decomposition constants
 // ---------------------------------------------------------------------------
-constexpr int kHeadDim = 128;          // supported head dimension
-constexpr int kThreads = 256;          // threads per CTA (match and attend)
+constexpr int kHeadDim = 128;           // supported head dimension
+constexpr int kThreads = 256;           // threads per CTA (8 warps; thread 0 also issues the copies)
+constexpr int kConsumers = kThreads;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTile = 32;              // tokens per K/V tile (two 16-token pages)
-constexpr int kTailChunk = 128;        // tokens per tail chunk (the last r positions)
-constexpr int kBandChunkMin = 128;     // band chunk size grows from here ...
-constexpr int kBandChunkMax = 2048;    // ... up to here, so that a unit has at most
-constexpr int kBandChunksTarget = 64;  //     kBandChunksTarget band chunks when possible
+constexpr int kStages = 5;              // stage buffers in the TMA ring
+constexpr int kStageBytes = 32768;      // bytes per stage (K+V tile, or ring rows)
+constexpr int kTailChunk = 128;         // tokens per tail chunk (the last r positions)
+constexpr int kBandChunkMin = 128;      // band chunk size grows from here ...
+constexpr int kBandChunkMax = 1024;     // ... up to here, so that a unit has at most
+constexpr int kBandChunksTarget = 128;  //     kBandChunksTarget band chunks when possible
 constexpr int kPartStride = kHeadDim + 4;  // floats per (item, head) partial: o[d], m, l, 0, 0
-constexpr int kMaxUnits = 4096;        // B * Hkv
-constexpr int kMaxSplits = 64;         // match splits per (request, kv-head) unit
-constexpr int kStages = 4;             // TMA pipeline depth (tiles in flight per CTA)
+constexpr int kMaxUnits = 1024;         // B * Hkv
+constexpr int kMaxHeads = 4096;         // B * Hq
+constexpr int kTracePoints = 8;         // timestamps per CTA in a phase trace
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -39,16 +41,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 // scratch workspace (shared by the kernels of one stream)
 // ---------------------------------------------------------------------------
 struct ScratchLayout {
-  size_t ctl;        // int32[64]: [0] status word, [1] work counter, [2] exit counter
-  size_t match_part; // int2 [B][Hq][kMaxSplits]: {bits of D, position}
-  size_t match_cnt;  // int32 [B*Hkv]: CTAs of the match finished per unit
+  size_t ctl;        // uint32[64]: [0] status word, [1] grid-barrier counter
+  size_t best;       // uint64 [B][Hq]: ~(dist bits << 32 | ~pos) of the best candidate, 0 = none
+  size_t match_cnt;  // int32 [B*Hkv]: CTAs whose match slice covered the unit and finished
   size_t head_info;  // int2 [B][Hq]: {matched position or -1, first fresh token lo}
   size_t unit_s;     // int32 [B*Hkv]: first token any head of the unit reads
-  size_t q_rot;      // f32 [B][Hq][d]: R(m) q~ scaled by log2(e)/sqrt(d)
-  size_t unit_done;  // int32 [B*Hkv]: items of the unit finished
-  size_t seed_pos;   // int32 [B]: position being seeded
-  size_t seed_len;   // int32 [B]: its summary length p - r
-  size_t partials;   // f32 [max_items][G][kPartStride]
+  size_t tail_part;  // f32 [B*Hkv][n_tail][G][kPartStride]: tail chunk partials
+  size_t partials;   // f32 [max_items][G][kPartStride]: band chunk partials
   size_t total;
   int64_t max_items;
 };
@@ -58,73 +57,58 @@ struct ScratchLayout {
 // ---------------------------------------------------------------------------
 // The fresh range of a unit is [s, m] (s = first token any head of the group
 // needs).  It is cut at m-r: band chunks cover [s, m-r] and end on m-r,
-// tail chunks cover [m-r+1, m] in kTailChunk pieces aligned on m-r.  Every
-// chunk lies wholly on one side of m-r, so per head the band chunks (plus
-// the cached summary) give the rectified summary AS_{1:m-r} and the tail
-// chunks complete the output ([MAC] K2/K3).  The same plan with s = 1 is the
-// exact full attention, which makes a miss bitwise equal to it.
-struct UnitPlan {
-  int64_t m, s, t_start;
-  int32_t cb, nb, j0, nt, n_items;
+// tail chunks (tail_range) cover [m-r+1, m] in kTailChunk pieces aligned on
+// m-r.  Every chunk lies wholly on one side of m-r, so per head the band
+// chunks (plus the cached summary) give the rectified summary AS_{1:m-r} and
+// the tail chunks complete the output ([MAC] K2/K3).  The same plan with
+// s = 1 is the exact full attention, which makes a miss bitwise equal to it.
+struct BandPlan {
+  int64_t m, s;
+  int32_t cb, nb;  // chunk size and number of band chunks
 };
 
-__host__ __device__ inline UnitPlan plan_unit(int64_t m, int64_t s, int r) {
-  UnitPlan u;
+__host__ __device__ inline BandPlan plan_band(int64_t m, int64_t s, int r) {
+  BandPlan u;
   u.m = m;
   u.s = s;
-  int64_t band_len = (m - r) - s + 1;
+  const int64_t band_len = (m - r) - s + 1;
   u.cb = kBandChunkMin;
-  if (band_len > 0) {
+  u.nb = 0;
+  if (m >= 1 && band_len > 0) {
     while (u.cb < kBandChunkMax && (band_len + u.cb - 1) / u.cb > kBandChunksTarget) u.cb <<= 1;
     u.nb = (int32_t)((band_len + u.cb - 1) / u.cb);
-  } else {
-    u.nb = 0;
   }
-  int64_t tail_lo = m - r + 1;
-  u.t_start = s > tail_lo ? s : tail_lo;
-  int32_t n_tail = (r + kTailChunk - 1) / kTailChunk;
-  if (m >= 1 && u.t_start <= m && n_tail > 0) {
-    u.j0 = (int32_t)((u.t_start - tail_lo) / kTailChunk);
-    u.nt = n_tail - u.j0;
-  } else {
-    u.j0 = 0;
-    u.nt = 0;
-  }
-  u.n_items = u.nb + u.nt > 0 ? u.nb + u.nt : 1;  // an empty unit keeps one empty item
   return u;
 }
 
-// Token range [lo, hi] of item i of the unit; band says it lies at or below m-r.
-__host__ __device__ inline void item_range(const UnitPlan &u, int r, int i, int64_t *lo,
-                                           int64_t *hi, bool *band) {
-  if (u.nb + u.nt == 0) {
-    *lo = 1;
-    *hi = 0;
-    *band = true;
-    return;
-  }
-  if (i < u.nb) {
-    int64_t top = (u.m - r) - (int64_t)(u.nb - 1 - i) * u.cb;
-    int64_t bot = top - u.cb + 1;
-    *lo = bot > u.s ? bot : u.s;
-    *hi = top;
-    *band = true;
-  } else {
-    int64_t base = u.m - r + 1 + (int64_t)(u.j0 + (i - u.nb)) * kTailChunk;
-    *lo = base > u.t_start ? base : u.t_start;
-    int64_t top = base + kTailChunk - 1;
-    *hi = top < u.m ? top : u.m;
-    *band = false;
-  }
+// Token range [lo, hi] of band chunk i of the unit.
+__host__ __device__ inline void band_range(const BandPlan &u, int r, int i, int64_t *lo,
+                                           int64_t *hi) {
+  const int64_t top = (u.m - r) - (int64_t)(u.nb - 1 - i) * u.cb;
+  const int64_t bot = top - u.cb + 1;
+  *lo = bot > u.s ? bot : u.s;
+  *hi = top;
 }
 
-// Worst-case items per unit for contexts up to max_context.
-__host__ inline int64_t max_items_per_unit(int64_t max_context, int r) {
+// Worst-case band chunks per unit for contexts up to max_context.
+__host__ inline int64_t max_band_items_per_unit(int64_t max_context) {
   int64_t nb = kBandChunksTarget;
   int64_t by_max = (max_context + kBandChunkMax - 1) / kBandChunkMax;
   if (by_max > nb) nb = by_max;
-  int64_t nt = (r + kTailChunk - 1) / kTailChunk;
-  return nb + nt + 1;
+  return nb + 1;
+}
+
+// Number of tail chunks of a unit (the last r tokens in kTailChunk pieces).
+__host__ __device__ inline int n_tail_chunks(int r) { return (r + kTailChunk - 1) / kTailChunk; }
+
+// Token range of tail chunk j of a request at length m: the chunks are
+// aligned on m-r and clipped to [1, m] (empty when lo > hi).  They do not
+// depend on the match: every head's band start lies at or before m-r+1.
+__host__ __device__ inline void tail_range(int64_t m, int r, int j, int64_t *lo, int64_t *hi) {
+  const int64_t base = m - r + 1 + (int64_t)j * kTailChunk;
+  *lo = base > 1 ? base : 1;
+  const int64_t top = base + kTailChunk - 1;
+  *hi = top < m ? top : m;
 }
 
 // ---------------------------------------------------------------------------
@@ -137,68 +121,56 @@ struct KvView {
   int32_t max_pages, n_pages, paged;
 };
 
-struct MatchParams {
-  int B, Hq, Hkv, G, d, K, r, min_context, n_splits;
-  float thr2;
+enum { MODE_DECODE = 0, MODE_FULL = 1 };
+
+// One launch of the step kernel.  Positions and lengths of request b:
+//   pos = pos_base[b] + pos_add      (the query's position: RoPE angle pos-1)
+//   m   = pos - len_sub              (attention over [1, m]; decode/full: 0)
+struct StepParams {
+  int mode;
+  int check_len;             // flag lengths outside [1, max_len] (MAC_DEV_BAD_SEQ_LEN)
+  int B, Hq, Hkv, G, K, r, min_context;
+  int n_tail;                // tail chunks per unit, n_tail_chunks(r)
+  float thr2;                // squared match threshold (fp32)
   float q_scale;             // log2(e)/sqrt(d)
   int rope_mode;
-  const void *q_pre;         // [B][Hq][d]
-  const int32_t *seq_len;    // [B]
-  int64_t capacity;          // max valid m: min(cache capacity, max_context)
+  const int32_t *pos_base;
+  int pos_add, len_sub;
+  int64_t max_len;           // lengths above min(capacity, max_context) are rejected
+  KvView kv;
+  const void *q;             // query of (b, h) at element (b*Hq + h) * q_stride + q_offset
+  int64_t q_stride, q_offset;
+  // decode only
   const int32_t *ring_pos;   // [B][K]
   const void *ring_q;        // [B][Hq][K][d]
-  void *stage_q;             // [B][Hq][d]
-  int32_t *ctl;
-  int2 *match_part;
+  const float *ring_o;       // [B][Hq][K][d]
+  const float *ring_lse;     // [B][Hq][K]
+  void *stage_q;             // [B][Hq][d]: copy of the step's query for the append
+  float *as_o;               // [B][Hq][d]: AS_{1:m-r}
+  float *as_lse;             // [B][Hq]
+  int32_t *match_pos_out;    // [B][Hq] or null
+  // outputs
+  float *out;                // [B][Hq][d]
+  float *out_lse;            // [B][Hq] or null
+  // scratch
+  uint32_t *ctl;
+  unsigned long long *best;
   int32_t *match_cnt;
   int2 *head_info;
   int32_t *unit_s;
-  float *q_rot;
-  int32_t *match_pos_out;    // [B][Hq] or null
-  double rope_w[kHeadDim / 2];
-};
-
-enum { MODE_DECODE = 0, MODE_FULL = 1 };
-
-struct AttendParams {
-  int mode;
-  int check_len;             // flag lengths outside [1, capacity] (MAC_DEV_BAD_SEQ_LEN)
-  int B, Hq, Hkv, d, K, r;
-  const int32_t *len;        // [B]: m (decode/full) or p - r (seeding)
-  int64_t max_len;           // lengths above min(capacity, max_context) are rejected
-  KvView kv;
-  const float *q_rot;        // [B][Hq][d]
-  const int2 *head_info;     // decode: [B][Hq]
-  const int32_t *unit_s;     // decode: [B*Hkv]
-  const float *ring_o;       // decode: cached summaries [B][Hq][K][d]
-  const float *ring_lse;     // decode: [B][Hq][K]
-  float *as_o;               // decode: AS_{1:m-r} [B][Hq][d] (may be null)
-  float *as_lse;             // decode: [B][Hq] (may be null)
-  float *out;                // [B][Hq][d]
-  float *out_lse;            // [B][Hq] or null
-  int32_t *ctl;
-  int32_t *unit_done;
+  float *tail_part;
   float *partials;
-};
-
-struct RopeParams {
-  int B, Hq, d, r, rope_mode, n_seed, seed_index;
-  float q_scale;
-  const void *q;             // full: [B][Hq][d]; seed: [B][Hq][n_seed][d]
-  const int32_t *pos_base;   // [B]
-  int pos_add;               // position = pos_base[b] + pos_add
-  float *q_rot;
-  int32_t *seed_pos;         // seed only: position, or 0 when < 1
-  int32_t *seed_len;         // seed only: p - r
-  int32_t *ctl;
+  unsigned long long *trace;  // optional: [grid][kTracePoints] %globaltimer stamps
   double rope_w[kHeadDim / 2];
 };
 
 struct AppendParams {
-  int B, Hq, d, K, seed_index, n_seed;
-  const int32_t *pos;        // [B]: position to append
+  int B, Hq, K;
+  const int32_t *pos_base;   // position appended for request b: pos_base[b] + pos_add
+  int pos_add;
   int64_t capacity;          // max valid position
-  const void *q_src;         // decode: stage_q [B][Hq][d]; seed: q_seed [B][Hq][n_seed][d]
+  const void *q_src;         // query of (b, h) at element (b*Hq + h) * q_stride + q_offset
+  int64_t q_stride, q_offset;
   const float *src_o;        // [B][Hq][d]
   const float *src_lse;      // [B][Hq]
   int32_t *ring_pos;
@@ -210,8 +182,10 @@ struct AppendParams {
 // ---------------------------------------------------------------------------
 // launchers (defined in the .cu files)
 // ---------------------------------------------------------------------------
-cudaError_t launch_match(const MatchParams &p, int dtype, cudaStream_t s);
-cudaError_t launch_rope(const RopeParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_step_bf16(const StepParams &p, int grid, cudaStream_t s);
+cudaError_t launch_step_f32(const StepParams &p, int grid, cudaStream_t s);
+int step_occupancy_bf16(int G, bool paged, int n_units);
+int step_occupancy_f32(int G, bool paged, int n_units);
 cudaError_t launch_append(const AppendParams &p, int dtype, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
@@ -252,14 +226,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for a phase of an mbarrier, giving up after ~2^31 clock cycles (about a
-// second); returns false (and the caller reports MAC_DEV_WAIT_TIMEOUT) if the
-// phase never completed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Non-blocking test of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of parity `parity` of an mbarrier, giving up after
+// ~2^31 clock cycles (about a second) or as soon as *abort is set; returns
+// false when it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
+  const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > (1LL << 31)) return false;
+    if (*abort || clock64() - t0 > (1LL << 31)) return false;
   }
   return true;
 }
@@ -278,6 +266,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
+// Barrier of the CTA's consumer threads (all of them).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -288,14 +281,12 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ void set_status(int32_t *ctl, int bits) {
-  atomicOr(reinterpret_cast<int *>(ctl), bits);
-}
+__device__ __forceinline__ void set_status(uint32_t *ctl, uint32_t bits) { atomicOr(ctl, bits); }
 
-// Total order used by every argmin of the match: smaller distance first,
-// equal distances prefer the more recent position.
-__device__ __forceinline__ bool better(float d_a, int p_a, float d_b, int p_b) {
-  return d_a < d_b || (d_a == d_b && p_a > p_b);
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 
 // Query rotation for one 2x2 block: angle (pos-1) w computed in fp64 and
@@ -323,11 +314,24 @@ __device__ __forceinline__ float elem_f32<float>(const void *base, int64_t i) {
   return reinterpret_cast<const float *>(base)[i];
 }
 
-// q_rot[pair j] = R(pos) q~ scaled by `scale`, for the head whose pre-RoPE
+// 16 bytes of elements -> floats (8 bf16 or 4 fp32).
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4 &u, float *f);
+template <>
+__device__ __forceinline__ void unpack16<uint16_t>(const uint4 &u, float *f) {
+  f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+  f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+}
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4 &u, float *f) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+
+// dst[pair j] = R(pos) q~ scaled by `scale`, for the head whose pre-RoPE
 // query starts at element `src` of `q` and whose output starts at `dst`.
 // Explicitly rounded operations keep the result bitwise identical wherever
-// it is computed (the match kernel for decode steps, the RoPE kernel for
-// full attention), so a decode miss and a full-attention call see the same
+// it is computed, so a decode miss and a full-attention call see the same
 // query.  Returns false for a non-finite input.
 template <typename T>
 __device__ __forceinline__ bool rope_rotate_pair(const void *q, int64_t src, float *dst, int j,

@@ -9,13 +9,6 @@
 
 #include "mac_common.cuh"
 
-namespace mac {
-cudaError_t launch_attend_bf16(const AttendParams &p, int G, int grid, cudaStream_t s);
-cudaError_t launch_attend_f32(const AttendParams &p, int G, int grid, cudaStream_t s);
-int attend_occupancy_bf16(int G, bool paged, int n_units);
-int attend_occupancy_f32(int G, bool paged, int n_units);
-}  // namespace mac
-
 using namespace mac;
 
 namespace {
@@ -59,21 +52,18 @@ mac_ring_layout ring_layout(const mac_config *c) {
 }
 
 ScratchLayout scratch_layout(const mac_config *c) {
-  const size_t B = c->batch, H = c->n_q_heads, U = (size_t)c->batch * c->n_kv_heads,
-               d = c->head_dim;
+  const size_t B = c->batch, H = c->n_q_heads, U = (size_t)c->batch * c->n_kv_heads;
   const size_t G = c->n_q_heads / c->n_kv_heads;
   ScratchLayout S;
-  S.max_items = (int64_t)U * max_items_per_unit(c->max_context, c->band_r);
+  S.max_items = (int64_t)U * max_band_items_per_unit(c->max_context);
+  const size_t n_tail = (size_t)n_tail_chunks(c->band_r);
   size_t off = 0;
   S.ctl = off;        off = align_up(off + 64 * 4, 256);
-  S.match_part = off; off = align_up(off + B * H * kMaxSplits * 8, 256);
+  S.best = off;       off = align_up(off + B * H * 8, 256);
   S.match_cnt = off;  off = align_up(off + U * 4, 256);
   S.head_info = off;  off = align_up(off + B * H * 8, 256);
   S.unit_s = off;     off = align_up(off + U * 4, 256);
-  S.q_rot = off;      off = align_up(off + B * H * d * 4, 256);
-  S.unit_done = off;  off = align_up(off + U * 4, 256);
-  S.seed_pos = off;   off = align_up(off + B * 4, 256);
-  S.seed_len = off;   off = align_up(off + B * 4, 256);
+  S.tail_part = off;  off = align_up(off + U * n_tail * G * kPartStride * 4, 256);
   S.partials = off;   off = align_up(off + (size_t)S.max_items * G * kPartStride * 4, 256);
   S.total = off;
   return S;
@@ -83,11 +73,6 @@ float threshold_sq(const mac_config *c) {
   const double f = (c->thr_mode == MAC_THR_TAU) ? c->tau : (1.0 - c->tau);
   const double thr = f * sqrt(2.0 * (double)c->head_dim);
   return (float)(thr * thr);
-}
-
-void rope_table(const mac_config *c, double *w) {
-  for (int j = 0; j < kHeadDim / 2; ++j)
-    w[j] = pow(c->rope_base, -2.0 * (double)j / (double)c->head_dim);
 }
 
 float q_scale(const mac_config *c) { return (float)(1.4426950408889634 / sqrt((double)c->head_dim)); }
@@ -129,33 +114,70 @@ int num_sms() {
   return n;
 }
 
-int match_splits(const mac_config *c) {
-  const int units = c->batch * c->n_kv_heads;
-  const int sms = num_sms() > 0 ? num_sms() : 148;
-  int max_s = c->ring_k / 32;
-  if (max_s < 1) max_s = 1;
-  if (max_s > kMaxSplits) max_s = kMaxSplits;
-  int s = (2 * sms + units - 1) / units;
-  if (s > max_s) s = max_s;
-  if (s < 1) s = 1;
-  return s;
-}
-
-int attend_grid_size(const mac_config *c) {
+// Persistent grid: as many CTAs as can be resident at once (one per SM).
+int step_grid(const mac_config *c) {
   const int G = c->n_q_heads / c->n_kv_heads;
   const int units = c->batch * c->n_kv_heads;
   const bool paged = c->page_size != 0;
-  int per_sm = c->dtype == MAC_F32 ? attend_occupancy_f32(G, paged, units)
-                                   : attend_occupancy_bf16(G, paged, units);
-  if (per_sm < 1) per_sm = 1;
+  int per_sm = c->dtype == MAC_F32 ? step_occupancy_f32(G, paged, units)
+                                   : step_occupancy_bf16(G, paged, units);
+  if (per_sm < 1) return 0;
   return num_sms() * per_sm;
 }
 
-cudaError_t launch_attend(const AttendParams &p, const mac_config *c, cudaStream_t s) {
-  const int G = c->n_q_heads / c->n_kv_heads;
-  const int grid = attend_grid_size(c);
-  if (grid < 1) return cudaErrorInvalidValue;
-  return c->dtype == MAC_F32 ? launch_attend_f32(p, G, grid, s) : launch_attend_bf16(p, G, grid, s);
+cudaError_t launch_step(StepParams p, const mac_config *c, cudaStream_t s);
+
+// Common part of every step launch: shapes, constants, K/V, scratch.
+StepParams step_params(const mac_config *c, const ScratchLayout &S, uint8_t *scratch,
+                       const mac_kv *kv, int mode) {
+  StepParams a;
+  memset(&a, 0, sizeof a);
+  a.mode = mode;
+  a.check_len = 1;
+  a.B = c->batch;
+  a.Hq = c->n_q_heads;
+  a.Hkv = c->n_kv_heads;
+  a.G = c->n_q_heads / c->n_kv_heads;
+  a.K = c->ring_k;
+  a.r = c->band_r;
+  a.n_tail = n_tail_chunks(c->band_r);
+  a.min_context = c->min_context;
+  a.thr2 = threshold_sq(c);
+  a.q_scale = q_scale(c);
+  a.rope_mode = c->rope_mode;
+  a.kv = kv_view(c, kv);
+  a.max_len = max_len(c, a.kv);
+  a.q_stride = c->head_dim;
+  for (int j = 0; j < kHeadDim / 2; ++j)
+    a.rope_w[j] = pow(c->rope_base, -2.0 * (double)j / (double)c->head_dim);
+  a.ctl = (uint32_t *)(scratch + S.ctl);
+  a.best = (unsigned long long *)(scratch + S.best);
+  a.match_cnt = (int32_t *)(scratch + S.match_cnt);
+  a.head_info = (int2 *)(scratch + S.head_info);
+  a.unit_s = (int32_t *)(scratch + S.unit_s);
+  a.tail_part = (float *)(scratch + S.tail_part);
+  a.partials = (float *)(scratch + S.partials);
+  return a;
+}
+
+AppendParams append_params(const mac_config *c, const mac_ring_layout &R, uint8_t *ring,
+                           const StepParams &sp) {
+  AppendParams q;
+  memset(&q, 0, sizeof q);
+  q.B = c->batch;
+  q.Hq = c->n_q_heads;
+  q.K = c->ring_k;
+  q.pos_base = sp.pos_base;
+  q.pos_add = sp.pos_add;
+  q.capacity = sp.max_len;
+  q.q_stride = c->head_dim;
+  q.src_o = (const float *)(ring + R.stage_o);
+  q.src_lse = (const float *)(ring + R.stage_lse);
+  q.ring_pos = (int32_t *)(ring + R.pos);
+  q.ring_q = ring + R.q;
+  q.ring_o = (float *)(ring + R.o);
+  q.ring_lse = (float *)(ring + R.lse);
+  return q;
 }
 
 // ---- per-ring events: the append of step n on stream_aux must finish before
@@ -176,8 +198,6 @@ unsigned long long capture_id_of(cudaStream_t s) {
   if (cudaStreamGetCaptureInfo(s, &st, &id) != cudaSuccess) return 0;
   return st == cudaStreamCaptureStatusActive ? id : 0;
 }
-
-int ctl_check(cudaError_t e) { return e == cudaSuccess ? MAC_OK : MAC_ERR_CUDA; }
 
 // Scratch of mac_full_attention_noalloc: a fixed array inside the library,
 // for callers that cannot allocate device memory.  Host code must not pass
@@ -203,6 +223,16 @@ void *noalloc_scratch() {
 
 // events armed by mac_set_phase_events for this thread's next decode step
 thread_local cudaEvent_t t_phase[3] = {nullptr, nullptr, nullptr};
+// trace buffer armed by mac_set_trace for this thread's next step kernel
+thread_local unsigned long long *t_trace = nullptr;
+
+cudaError_t launch_step(StepParams p, const mac_config *c, cudaStream_t s) {
+  const int grid = step_grid(c);
+  if (grid < 1) return cudaErrorInvalidValue;
+  p.trace = t_trace;
+  t_trace = nullptr;
+  return c->dtype == MAC_F32 ? launch_step_f32(p, grid, s) : launch_step_bf16(p, grid, s);
+}
 
 // Inside a stream capture the record becomes an event-record node of the
 // graph (timestamped at replay), not a capture-time dependency marker.
@@ -216,27 +246,6 @@ cudaError_t record_phase(int i, cudaStream_t s) {
             : cudaEventRecord(t_phase[i], s);
   t_phase[i] = nullptr;
   return e;
-}
-
-AttendParams attend_params(const mac_config *c, const ScratchLayout &S, uint8_t *scratch,
-                           const mac_kv *kv, int mode) {
-  AttendParams a;
-  memset(&a, 0, sizeof a);
-  a.mode = mode;
-  a.check_len = 1;
-  a.B = c->batch;
-  a.Hq = c->n_q_heads;
-  a.Hkv = c->n_kv_heads;
-  a.d = c->head_dim;
-  a.K = c->ring_k;
-  a.r = c->band_r;
-  a.kv = kv_view(c, kv);
-  a.max_len = max_len(c, a.kv);
-  a.q_rot = (const float *)(scratch + S.q_rot);
-  a.ctl = (int32_t *)(scratch + S.ctl);
-  a.unit_done = (int32_t *)(scratch + S.unit_done);
-  a.partials = (float *)(scratch + S.partials);
-  return a;
 }
 
 }  // namespace
@@ -295,56 +304,27 @@ int mac_init_rings(const mac_config *cfg, void *ring_ws, void *scratch_ws, const
     auto it = g_rings.find(ring_ws);
     if (it != g_rings.end()) it->second.pending = false;
   }
-  if (!q_seed) return ctl_check(cudaGetLastError());
+  if (!q_seed) return MAC_OK;
 
-  RopeParams rp;
-  memset(&rp, 0, sizeof rp);
-  rp.B = cfg->batch;
-  rp.Hq = cfg->n_q_heads;
-  rp.d = cfg->head_dim;
-  rp.r = cfg->band_r;
-  rp.rope_mode = cfg->rope_mode;
-  rp.n_seed = n_seed;
-  rp.q_scale = q_scale(cfg);
-  rp.q = q_seed;
-  rp.pos_base = prompt_len;
-  rp.q_rot = (float *)(scr + S.q_rot);
-  rp.seed_pos = (int32_t *)(scr + S.seed_pos);
-  rp.seed_len = (int32_t *)(scr + S.seed_len);
-  rp.ctl = (int32_t *)(scr + S.ctl);
-  rope_table(cfg, rp.rope_w);
-
-  AttendParams ap = attend_params(cfg, S, scr, kv, MODE_FULL);
-  ap.check_len = 0;  // summary lengths p - r may be < 1 (empty summaries)
-  ap.len = rp.seed_len;
-  ap.out = (float *)(ring + R.stage_o);
-  ap.out_lse = (float *)(ring + R.stage_lse);
-
-  AppendParams qp;
-  memset(&qp, 0, sizeof qp);
-  qp.B = cfg->batch;
-  qp.Hq = cfg->n_q_heads;
-  qp.d = cfg->head_dim;
-  qp.K = cfg->ring_k;
-  qp.n_seed = n_seed;
-  qp.pos = rp.seed_pos;
-  qp.capacity = max_len(cfg, kv_view(cfg, kv));
-  qp.q_src = q_seed;
-  qp.src_o = ap.out;
-  qp.src_lse = ap.out_lse;
-  qp.ring_pos = (int32_t *)(ring + R.pos);
-  qp.ring_q = ring + R.q;
-  qp.ring_o = (float *)(ring + R.o);
-  qp.ring_lse = (float *)(ring + R.lse);
-
+  // seed i: position p = L - n_seed + 1 + i, exact summary over [1, p - r]
+  // of R(p) q_seed[.., i, ..] (the full-attention path), then appended
+  StepParams sp = step_params(cfg, S, scr, kv, MODE_FULL);
+  sp.check_len = 0;  // summary lengths p - r may be < 1 (empty summaries)
+  sp.pos_base = prompt_len;
+  sp.len_sub = cfg->band_r;
+  sp.q = q_seed;
+  sp.q_stride = (int64_t)n_seed * cfg->head_dim;
+  sp.out = (float *)(ring + R.stage_o);
+  sp.out_lse = (float *)(ring + R.stage_lse);
   for (int i = 0; i < n_seed; ++i) {
-    rp.seed_index = i;
-    rp.pos_add = -n_seed + 1 + i;
-    qp.seed_index = i;
-    cudaError_t e = launch_rope(rp, cfg->dtype, s);
-    if (e == cudaSuccess) e = launch_attend(ap, cfg, s);
-    if (e == cudaSuccess) e = launch_append(qp, cfg->dtype, s);
-    if (e != cudaSuccess) return MAC_ERR_CUDA;
+    sp.pos_add = -n_seed + 1 + i;
+    sp.q_offset = (int64_t)i * cfg->head_dim;
+    AppendParams ap = append_params(cfg, R, ring, sp);
+    ap.q_src = q_seed;
+    ap.q_stride = sp.q_stride;
+    ap.q_offset = sp.q_offset;
+    if (launch_step(sp, cfg, s) != cudaSuccess || launch_append(ap, cfg->dtype, s) != cudaSuccess)
+      return MAC_ERR_CUDA;
   }
   return MAC_OK;
 }
@@ -383,77 +363,37 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
     ev = &e;
   }
 
-  MatchParams mp;
-  memset(&mp, 0, sizeof mp);
-  mp.B = cfg->batch;
-  mp.Hq = cfg->n_q_heads;
-  mp.Hkv = cfg->n_kv_heads;
-  mp.G = cfg->n_q_heads / cfg->n_kv_heads;
-  mp.d = cfg->head_dim;
-  mp.K = cfg->ring_k;
-  mp.r = cfg->band_r;
-  mp.min_context = cfg->min_context;
-  mp.n_splits = match_splits(cfg);
-  mp.thr2 = threshold_sq(cfg);
-  mp.q_scale = q_scale(cfg);
-  mp.rope_mode = cfg->rope_mode;
-  mp.q_pre = q_pre;
-  mp.seq_len = seq_len;
-  mp.capacity = max_len(cfg, kv_view(cfg, kv));
-  mp.ring_pos = (const int32_t *)(ring + R.pos);
-  mp.ring_q = ring + R.q;
-  mp.stage_q = ring + R.stage_q;
-  mp.ctl = (int32_t *)(scr + S.ctl);
-  mp.match_part = (int2 *)(scr + S.match_part);
-  mp.match_cnt = (int32_t *)(scr + S.match_cnt);
-  mp.head_info = (int2 *)(scr + S.head_info);
-  mp.unit_s = (int32_t *)(scr + S.unit_s);
-  mp.q_rot = (float *)(scr + S.q_rot);
-  mp.match_pos_out = match_pos;
-  rope_table(cfg, mp.rope_w);
-  if (record_phase(0, sm) != cudaSuccess) return MAC_ERR_CUDA;
-  if (launch_match(mp, cfg->dtype, sm) != cudaSuccess) return MAC_ERR_CUDA;
-  if (record_phase(1, sm) != cudaSuccess) return MAC_ERR_CUDA;
+  StepParams sp = step_params(cfg, S, scr, kv, MODE_DECODE);
+  sp.pos_base = seq_len;
+  sp.q = q_pre;
+  sp.ring_pos = (const int32_t *)(ring + R.pos);
+  sp.ring_q = ring + R.q;
+  sp.ring_o = (const float *)(ring + R.o);
+  sp.ring_lse = (const float *)(ring + R.lse);
+  sp.stage_q = ring + R.stage_q;
+  sp.as_o = (float *)(ring + R.stage_o);
+  sp.as_lse = (float *)(ring + R.stage_lse);
+  sp.match_pos_out = match_pos;
+  sp.out = out;
+  if (record_phase(0, sm) != cudaSuccess || launch_step(sp, cfg, sm) != cudaSuccess ||
+      record_phase(1, sm) != cudaSuccess)
+    return MAC_ERR_CUDA;
 
-  AttendParams ap = attend_params(cfg, S, scr, kv, MODE_DECODE);
-  ap.check_len = 0;  // the match kernel already flagged bad lengths
-  ap.len = seq_len;
-  ap.head_info = mp.head_info;
-  ap.unit_s = mp.unit_s;
-  ap.ring_o = (const float *)(ring + R.o);
-  ap.ring_lse = (const float *)(ring + R.lse);
-  ap.as_o = (float *)(ring + R.stage_o);
-  ap.as_lse = (float *)(ring + R.stage_lse);
-  ap.out = out;
-  if (launch_attend(ap, cfg, sm) != cudaSuccess) return MAC_ERR_CUDA;
-  if (record_phase(2, sm) != cudaSuccess) return MAC_ERR_CUDA;
-
-  AppendParams qp;
-  memset(&qp, 0, sizeof qp);
-  qp.B = cfg->batch;
-  qp.Hq = cfg->n_q_heads;
-  qp.d = cfg->head_dim;
-  qp.K = cfg->ring_k;
-  qp.pos = seq_len;
-  qp.capacity = mp.capacity;
-  qp.q_src = ring + R.stage_q;
-  qp.src_o = ap.as_o;
-  qp.src_lse = ap.as_lse;
-  qp.ring_pos = (int32_t *)(ring + R.pos);
-  qp.ring_q = ring + R.q;
-  qp.ring_o = (float *)(ring + R.o);
-  qp.ring_lse = (float *)(ring + R.lse);
+  AppendParams ap = append_params(cfg, R, ring, sp);
+  ap.q_src = ring + R.stage_q;
   if (use_aux) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (cudaEventRecord(ev->main_done, sm) != cudaSuccess ||
         cudaStreamWaitEvent(sa, ev->main_done, 0) != cudaSuccess)
       return MAC_ERR_CUDA;
-    if (launch_append(qp, cfg->dtype, sa) != cudaSuccess) return MAC_ERR_CUDA;
+    if (launch_append(ap, cfg->dtype, sa) != cudaSuccess || record_phase(2, sa) != cudaSuccess)
+      return MAC_ERR_CUDA;
     if (cudaEventRecord(ev->aux_done, sa) != cudaSuccess) return MAC_ERR_CUDA;
     ev->pending = true;
     ev->capture_id = cap_id;
   } else {
-    if (launch_append(qp, cfg->dtype, sm) != cudaSuccess) return MAC_ERR_CUDA;
+    if (launch_append(ap, cfg->dtype, sm) != cudaSuccess || record_phase(2, sm) != cudaSuccess)
+      return MAC_ERR_CUDA;
   }
   return MAC_OK;
 }
@@ -467,30 +407,13 @@ int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pr
       !aligned16(out))
     return MAC_ERR_INVALID_ARG;
   if ((v = check_kv(cfg, kv)) != MAC_OK) return v;
-  cudaStream_t s = (cudaStream_t)stream;
   const ScratchLayout S = scratch_layout(cfg);
-  uint8_t *scr = (uint8_t *)scratch_ws;
-
-  RopeParams rp;
-  memset(&rp, 0, sizeof rp);
-  rp.B = cfg->batch;
-  rp.Hq = cfg->n_q_heads;
-  rp.d = cfg->head_dim;
-  rp.r = cfg->band_r;
-  rp.rope_mode = cfg->rope_mode;
-  rp.q_scale = q_scale(cfg);
-  rp.q = q_pre;
-  rp.pos_base = seq_len;
-  rp.q_rot = (float *)(scr + S.q_rot);
-  rp.ctl = (int32_t *)(scr + S.ctl);
-  rope_table(cfg, rp.rope_w);
-  if (launch_rope(rp, cfg->dtype, s) != cudaSuccess) return MAC_ERR_CUDA;
-
-  AttendParams ap = attend_params(cfg, S, scr, kv, MODE_FULL);
-  ap.len = seq_len;
-  ap.out = out;
-  ap.out_lse = lse;
-  if (launch_attend(ap, cfg, s) != cudaSuccess) return MAC_ERR_CUDA;
+  StepParams sp = step_params(cfg, S, (uint8_t *)scratch_ws, kv, MODE_FULL);
+  sp.pos_base = seq_len;
+  sp.q = q_pre;
+  sp.out = out;
+  sp.out_lse = lse;
+  if (launch_step(sp, cfg, (cudaStream_t)stream) != cudaSuccess) return MAC_ERR_CUDA;
   return MAC_OK;
 }
 
@@ -523,10 +446,15 @@ int mac_join_aux(void *ring_ws, void *stream_main) {
   return MAC_OK;
 }
 
-int mac_set_phase_events(void *before_match, void *after_match, void *after_attend) {
-  t_phase[0] = (cudaEvent_t)before_match;
-  t_phase[1] = (cudaEvent_t)after_match;
-  t_phase[2] = (cudaEvent_t)after_attend;
+int mac_set_phase_events(void *before_step, void *after_step, void *after_append) {
+  t_phase[0] = (cudaEvent_t)before_step;
+  t_phase[1] = (cudaEvent_t)after_step;
+  t_phase[2] = (cudaEvent_t)after_append;
+  return MAC_OK;
+}
+
+int mac_set_trace(void *device_buffer) {
+  t_trace = (unsigned long long *)device_buffer;
   return MAC_OK;
 }
 

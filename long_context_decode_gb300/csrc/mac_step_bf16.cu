@@ -1,0 +1,9 @@
+// bf16 instantiations of the step kernel.
+#include "mac_step_launch.cuh"
+
+namespace mac {
+cudaError_t launch_step_bf16(const StepParams &p, int grid, cudaStream_t s) {
+  return launch_step_t<uint16_t>(p, grid, s);
+}
+int step_occupancy_bf16(int G, bool paged, int n_units) { return occupancy_t<uint16_t>(G, paged, n_units); }
+}  // namespace mac

@@ -1,0 +1,9 @@
+// fp32 instantiations of the step kernel.
+#include "mac_step_launch.cuh"
+
+namespace mac {
+cudaError_t launch_step_f32(const StepParams &p, int grid, cudaStream_t s) {
+  return launch_step_t<float>(p, grid, s);
+}
+int step_occupancy_f32(int G, bool paged, int n_units) { return occupancy_t<float>(G, paged, n_units); }
+}  // namespace mac

@@ -1,0 +1,77 @@
+// Launch helpers of the step kernel, instantiated once per element type in
+// mac_step_bf16.cu and mac_step_f32.cu (one translation unit each, so the
+// builds run in parallel).
+#pragma once
+
+#include "mac_step.cuh"
+
+namespace mac {
+
+template <typename T, int G, bool PAGED>
+static cudaError_t prepare_step(int n_units, size_t *smem) {
+  using S = Step<T, G, PAGED>;
+  *smem = S::smem_bytes(n_units);
+  static size_t configured[64] = {0};  // per device: dynamic shared memory limit already set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && configured[dev] >= *smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(step_kernel<T, G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)S::smem_bytes(kMaxUnits));
+  if (e == cudaSuccess && dev < 64) configured[dev] = S::smem_bytes(kMaxUnits);
+  return e;
+}
+
+// Cooperative launch: the grid (one CTA per SM) is guaranteed co-resident,
+// which the grid barrier between the match and the attention relies on.
+template <typename T, int G, bool PAGED>
+static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) {
+  size_t smem = 0;
+  cudaError_t e = prepare_step<T, G, PAGED>(p.B * p.Hkv, &smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, step_kernel<T, G, PAGED>, p);
+}
+
+template <typename T, int G, bool PAGED>
+static int occupancy_g(int n_units) {
+  size_t smem = 0;
+  if (prepare_step<T, G, PAGED>(n_units, &smem) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<T, G, PAGED>, kThreads, smem) !=
+      cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <typename T>
+static cudaError_t launch_step_t(const StepParams &p, int grid, cudaStream_t s) {
+  const bool paged = p.kv.paged != 0;
+  switch (p.G) {
+    case 1: return paged ? launch_step_g<T, 1, true>(p, grid, s) : launch_step_g<T, 1, false>(p, grid, s);
+    case 2: return paged ? launch_step_g<T, 2, true>(p, grid, s) : launch_step_g<T, 2, false>(p, grid, s);
+    case 4: return paged ? launch_step_g<T, 4, true>(p, grid, s) : launch_step_g<T, 4, false>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+static int occupancy_t(int G, bool paged, int n_units) {
+  switch (G) {
+    case 1: return paged ? occupancy_g<T, 1, true>(n_units) : occupancy_g<T, 1, false>(n_units);
+    case 2: return paged ? occupancy_g<T, 2, true>(n_units) : occupancy_g<T, 2, false>(n_units);
+    case 4: return paged ? occupancy_g<T, 4, true>(n_units) : occupancy_g<T, 4, false>(n_units);
+    default: return 0;
+  }
+}
+
+}  // namespace mac

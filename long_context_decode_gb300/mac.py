@@ -21,7 +21,8 @@ MAC_ROPE_HALF, MAC_ROPE_INTERLEAVED, MAC_ROPE_NONE = 0, 1, 2
 # every function the header declares (checked against include/mac.h by the tests)
 EXPORTS = ("mac_workspace_size", "mac_ring_layout_of", "mac_init_rings", "mac_decode_step",
            "mac_full_attention", "mac_full_attention_noalloc", "mac_join_aux", "mac_release_ring",
-           "mac_last_status", "mac_set_phase_events", "mac_status_string", "mac_threshold_sq")
+           "mac_last_status", "mac_set_phase_events", "mac_set_trace", "mac_status_string",
+           "mac_threshold_sq")
 MAC_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -79,6 +80,7 @@ def load() -> ctypes.CDLL:
     L.mac_release_ring.argtypes = [vp]
     L.mac_last_status.argtypes = [P(mac_config), vp, P(i32), vp]
     L.mac_set_phase_events.argtypes = [vp, vp, vp]
+    L.mac_set_trace.argtypes = [vp]
     L.mac_status_string.argtypes = [ctypes.c_int]
     L.mac_status_string.restype = ctypes.c_char_p
     L.mac_threshold_sq.argtypes = [P(mac_config)]
@@ -180,6 +182,12 @@ def mac_set_phase_events(before_match=None, after_match=None, after_attend=None)
         return e.cuda_event
     _check(load().mac_set_phase_events(h(before_match), h(after_match), h(after_attend)),
            "mac_set_phase_events")
+
+
+def mac_set_trace(buffer):
+    """Arm the next step kernel on this thread to write per-CTA phase
+    timestamps into ``buffer`` (a torch uint64/int64 tensor of >= 8 * SMs)."""
+    _check(load().mac_set_trace(_ptr(buffer)), "mac_set_trace")
 
 
 def mac_status_string(code: int) -> str:
