@@ -106,9 +106,10 @@ typedef struct {
 /* Workspace sizes for cfg.  ring_bytes: one per layer (the two per-request
  * rings of capacity K, [MAC] "Paper version: K1/K2/K3": a pre-RoPE query
  * ring and a rectified-summary ring with its ln-LSE, plus a small staging
- * area).  scratch_bytes: shared by all calls on one stream (match partials,
- * split-K partials, counters, device status word); it must be zero-filled
- * before its first use (mac_init_rings does it).  Either pointer may be NULL.
+ * area).  scratch_bytes: shared by all calls on one stream (per-head match
+ * minima, split-K piece partials, grid-barrier counter, device status word);
+ * it must be zero-filled before its first use (mac_init_rings does it).  Its
+ * size does not depend on the context length.  Either pointer may be NULL.
  * Returns MAC_ERR_INVALID_ARG / MAC_ERR_UNSUPPORTED for a bad cfg. */
 int mac_workspace_size(const mac_config *cfg, size_t *ring_bytes, size_t *scratch_bytes);
 
@@ -160,15 +161,15 @@ int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pr
                        const int32_t *seq_len, const mac_kv *kv, float *out, float *lse,
                        void *stream);
 
-/* Largest scratch workspace mac_full_attention_noalloc can use (32 MiB). */
-#define MAC_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+/* Largest scratch workspace mac_full_attention_noalloc can use (4 MiB). */
+#define MAC_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 
 /* mac_full_attention without a caller-provided scratch workspace.  (The
  * pages have no counterpart; this is a packaging variant.)  For callers that
  * cannot allocate device memory: code whose device memory is owned by
  * another allocator it may not call into, code that must not trigger the
  * device-wide synchronisation cudaMalloc can cause, or code running under a
- * fixed memory budget decided at start-up.  The scratch lives in a 32 MiB
+ * fixed memory budget decided at start-up.  The scratch lives in a 4 MiB
  * array compiled into this library (MAC_NOALLOC_SCRATCH_BYTES); every GPU
  * that loads the library holds that array until the process exits.
  *   - Same arguments and results as mac_full_attention, minus scratch_ws.

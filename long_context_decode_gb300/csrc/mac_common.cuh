@@ -20,19 +20,18 @@ namespace mac {
 // work decomposition constants
 // ---------------------------------------------------------------------------
 constexpr int kHeadDim = 128;           // supported head dimension
-constexpr int kThreads = 256;           // threads per CTA (8 warps; thread 0 also issues the copies)
+constexpr int kThreads = 256;           // threads per CTA (8 warps)
 constexpr int kConsumers = kThreads;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStages = 5;              // stage buffers in the TMA ring
+constexpr int kStages = 4;              // stage buffers in the TMA ring
 constexpr int kStageBytes = 32768;      // bytes per stage (K+V tile, or ring rows)
-constexpr int kTailChunk = 128;         // tokens per tail chunk (the last r positions)
-constexpr int kBandChunkMin = 128;      // band chunk size grows from here ...
-constexpr int kBandChunkMax = 1024;     // ... up to here, so that a unit has at most
-constexpr int kBandChunksTarget = 128;  //     kBandChunksTarget band chunks when possible
-constexpr int kPartStride = kHeadDim + 4;  // floats per (item, head) partial: o[d], m, l, 0, 0
+constexpr int kPartStride = kHeadDim + 4;  // floats per (piece, head) partial: o[d], m, l, 0, 0
 constexpr int kMaxUnits = 1024;         // B * Hkv
 constexpr int kMaxHeads = 4096;         // B * Hq
+constexpr int kMaxGrid = 256;           // CTAs of the step grid (one per SM)
+constexpr int kPosStage = 4096;         // ring positions staged in shared memory for the match
 constexpr int kTracePoints = 8;         // timestamps per CTA in a phase trace
+constexpr size_t kMaxSmem = 232448;     // dynamic shared memory per CTA (227 KiB)
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -40,76 +39,19 @@ constexpr float kLn2 = 0.6931471805599453f;
 // ---------------------------------------------------------------------------
 // scratch workspace (shared by the kernels of one stream)
 // ---------------------------------------------------------------------------
+// The tail tokens of all units, laid end to end in unit order, are split
+// into one contiguous span per CTA, and so are the band tokens; a CTA's span
+// meets a few units, each meeting is a piece with its own partial summary.
+// Piece (unit u, CTA c) goes to slot u + c: the CTAs meeting a unit form a
+// run that starts at or after the last CTA of the previous unit, so the
+// slots of different pieces never coincide and B*Hkv + grid - 1 suffice.
 struct ScratchLayout {
-  size_t ctl;        // uint32[64]: [0] status word, [1] grid-barrier counter
+  size_t ctl;        // uint32[64]: [0] status word, [2..3] grid-barrier counter (u64)
   size_t best;       // uint64 [B][Hq]: ~(dist bits << 32 | ~pos) of the best candidate, 0 = none
-  size_t match_cnt;  // int32 [B*Hkv]: CTAs whose match slice covered the unit and finished
-  size_t head_info;  // int2 [B][Hq]: {matched position or -1, first fresh token lo}
-  size_t unit_s;     // int32 [B*Hkv]: first token any head of the unit reads
-  size_t tail_part;  // f32 [B*Hkv][n_tail][G][kPartStride]: tail chunk partials
-  size_t partials;   // f32 [max_items][G][kPartStride]: band chunk partials
+  size_t part_a;     // f32 [B*Hkv + kMaxGrid][G][kPartStride]: tail pieces
+  size_t part_b;     // f32 [B*Hkv + kMaxGrid][G][kPartStride]: band pieces
   size_t total;
-  int64_t max_items;
 };
-
-// ---------------------------------------------------------------------------
-// per-(request, kv-head) chunk plan
-// ---------------------------------------------------------------------------
-// The fresh range of a unit is [s, m] (s = first token any head of the group
-// needs).  It is cut at m-r: band chunks cover [s, m-r] and end on m-r,
-// tail chunks (tail_range) cover [m-r+1, m] in kTailChunk pieces aligned on
-// m-r.  Every chunk lies wholly on one side of m-r, so per head the band
-// chunks (plus the cached summary) give the rectified summary AS_{1:m-r} and
-// the tail chunks complete the output ([MAC] K2/K3).  The same plan with
-// s = 1 is the exact full attention, which makes a miss bitwise equal to it.
-struct BandPlan {
-  int64_t m, s;
-  int32_t cb, nb;  // chunk size and number of band chunks
-};
-
-__host__ __device__ inline BandPlan plan_band(int64_t m, int64_t s, int r) {
-  BandPlan u;
-  u.m = m;
-  u.s = s;
-  const int64_t band_len = (m - r) - s + 1;
-  u.cb = kBandChunkMin;
-  u.nb = 0;
-  if (m >= 1 && band_len > 0) {
-    while (u.cb < kBandChunkMax && (band_len + u.cb - 1) / u.cb > kBandChunksTarget) u.cb <<= 1;
-    u.nb = (int32_t)((band_len + u.cb - 1) / u.cb);
-  }
-  return u;
-}
-
-// Token range [lo, hi] of band chunk i of the unit.
-__host__ __device__ inline void band_range(const BandPlan &u, int r, int i, int64_t *lo,
-                                           int64_t *hi) {
-  const int64_t top = (u.m - r) - (int64_t)(u.nb - 1 - i) * u.cb;
-  const int64_t bot = top - u.cb + 1;
-  *lo = bot > u.s ? bot : u.s;
-  *hi = top;
-}
-
-// Worst-case band chunks per unit for contexts up to max_context.
-__host__ inline int64_t max_band_items_per_unit(int64_t max_context) {
-  int64_t nb = kBandChunksTarget;
-  int64_t by_max = (max_context + kBandChunkMax - 1) / kBandChunkMax;
-  if (by_max > nb) nb = by_max;
-  return nb + 1;
-}
-
-// Number of tail chunks of a unit (the last r tokens in kTailChunk pieces).
-__host__ __device__ inline int n_tail_chunks(int r) { return (r + kTailChunk - 1) / kTailChunk; }
-
-// Token range of tail chunk j of a request at length m: the chunks are
-// aligned on m-r and clipped to [1, m] (empty when lo > hi).  They do not
-// depend on the match: every head's band start lies at or before m-r+1.
-__host__ __device__ inline void tail_range(int64_t m, int r, int j, int64_t *lo, int64_t *hi) {
-  const int64_t base = m - r + 1 + (int64_t)j * kTailChunk;
-  *lo = base > 1 ? base : 1;
-  const int64_t top = base + kTailChunk - 1;
-  *hi = top < m ? top : m;
-}
 
 // ---------------------------------------------------------------------------
 // kernel parameter blocks
@@ -130,7 +72,6 @@ struct StepParams {
   int mode;
   int check_len;             // flag lengths outside [1, max_len] (MAC_DEV_BAD_SEQ_LEN)
   int B, Hq, Hkv, G, K, r, min_context;
-  int n_tail;                // tail chunks per unit, n_tail_chunks(r)
   float thr2;                // squared match threshold (fp32)
   float q_scale;             // log2(e)/sqrt(d)
   int rope_mode;
@@ -155,11 +96,8 @@ struct StepParams {
   // scratch
   uint32_t *ctl;
   unsigned long long *best;
-  int32_t *match_cnt;
-  int2 *head_info;
-  int32_t *unit_s;
-  float *tail_part;
-  float *partials;
+  float *part_a;             // tail pieces
+  float *part_b;             // band pieces
   unsigned long long *trace;  // optional: [grid][kTracePoints] %globaltimer stamps
   double rope_w[kHeadDim / 2];
 };
@@ -184,8 +122,8 @@ struct AppendParams {
 // ---------------------------------------------------------------------------
 cudaError_t launch_step_bf16(const StepParams &p, int grid, cudaStream_t s);
 cudaError_t launch_step_f32(const StepParams &p, int grid, cudaStream_t s);
-int step_occupancy_bf16(int G, bool paged, int n_units);
-int step_occupancy_f32(int G, bool paged, int n_units);
+int step_occupancy_bf16(int G, bool paged, int n_heads, int n_units, int K);
+int step_occupancy_f32(int G, bool paged, int n_heads, int n_units, int K);
 cudaError_t launch_append(const AppendParams &p, int dtype, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
@@ -237,6 +175,15 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Acquire-release add on a shared-memory counter (CTA scope); returns the
+// old value.
+__device__ __forceinline__ uint32_t atom_add_acqrel_shared(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v)
+               : "memory");
+  return old;
 }
 
 // Wait for the phase of parity `parity` of an mbarrier, giving up after
@@ -326,30 +273,6 @@ template <>
 __device__ __forceinline__ void unpack16<float>(const uint4 &u, float *f) {
   f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
   f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
-}
-
-// dst[pair j] = R(pos) q~ scaled by `scale`, for the head whose pre-RoPE
-// query starts at element `src` of `q` and whose output starts at `dst`.
-// Explicitly rounded operations keep the result bitwise identical wherever
-// it is computed, so a decode miss and a full-attention call see the same
-// query.  Returns false for a non-finite input.
-template <typename T>
-__device__ __forceinline__ bool rope_rotate_pair(const void *q, int64_t src, float *dst, int j,
-                                                 int64_t pos, int mode, double w, float scale) {
-  const int half = kHeadDim / 2;
-  const int ia = (mode == MAC_ROPE_INTERLEAVED) ? 2 * j : j;
-  const int ib = (mode == MAC_ROPE_INTERLEAVED) ? 2 * j + 1 : j + half;
-  const float a = elem_f32<T>(q, src + ia), b = elem_f32<T>(q, src + ib);
-  float ra = a, rb = b;
-  if (mode != MAC_ROPE_NONE) {
-    float c, s;
-    rope_angle(pos, w, &c, &s);
-    ra = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
-    rb = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s));
-  }
-  dst[ia] = __fmul_rn(ra, scale);
-  dst[ib] = __fmul_rn(rb, scale);
-  return isfinite(a) && isfinite(b);
 }
 
 #endif  // __CUDACC__

@@ -31,6 +31,7 @@ int validate(const mac_config *c) {
   if (c->thr_mode != MAC_THR_ONE_MINUS_TAU && c->thr_mode != MAC_THR_TAU) return MAC_ERR_INVALID_ARG;
   if (c->rope_mode < MAC_ROPE_HALF || c->rope_mode > MAC_ROPE_NONE) return MAC_ERR_INVALID_ARG;
   if ((int64_t)c->batch * c->n_kv_heads > kMaxUnits) return MAC_ERR_UNSUPPORTED;
+  if ((int64_t)c->batch * c->n_q_heads > kMaxHeads) return MAC_ERR_UNSUPPORTED;
   if (c->max_context > 0x7fffffffLL - 1) return MAC_ERR_UNSUPPORTED;
   return MAC_OK;
 }
@@ -51,20 +52,18 @@ mac_ring_layout ring_layout(const mac_config *c) {
   return L;
 }
 
+// Everything before part_a must start at zero (the status word, the grid
+// barrier counter and the per-head minima); the partials need no clearing.
 ScratchLayout scratch_layout(const mac_config *c) {
   const size_t B = c->batch, H = c->n_q_heads, U = (size_t)c->batch * c->n_kv_heads;
   const size_t G = c->n_q_heads / c->n_kv_heads;
+  const size_t slots = U + kMaxGrid;
   ScratchLayout S;
-  S.max_items = (int64_t)U * max_band_items_per_unit(c->max_context);
-  const size_t n_tail = (size_t)n_tail_chunks(c->band_r);
   size_t off = 0;
-  S.ctl = off;        off = align_up(off + 64 * 4, 256);
-  S.best = off;       off = align_up(off + B * H * 8, 256);
-  S.match_cnt = off;  off = align_up(off + U * 4, 256);
-  S.head_info = off;  off = align_up(off + B * H * 8, 256);
-  S.unit_s = off;     off = align_up(off + U * 4, 256);
-  S.tail_part = off;  off = align_up(off + U * n_tail * G * kPartStride * 4, 256);
-  S.partials = off;   off = align_up(off + (size_t)S.max_items * G * kPartStride * 4, 256);
+  S.ctl = off;     off = align_up(off + 64 * 4, 256);
+  S.best = off;    off = align_up(off + B * H * 8, 256);
+  S.part_a = off;  off = align_up(off + slots * G * kPartStride * 4, 256);
+  S.part_b = off;  off = align_up(off + slots * G * kPartStride * 4, 256);
   S.total = off;
   return S;
 }
@@ -114,15 +113,17 @@ int num_sms() {
   return n;
 }
 
-// Persistent grid: as many CTAs as can be resident at once (one per SM).
+// Persistent grid: as many CTAs as can be resident at once (one per SM), at
+// most kMaxGrid (the partial slots are sized for that many).
 int step_grid(const mac_config *c) {
   const int G = c->n_q_heads / c->n_kv_heads;
-  const int units = c->batch * c->n_kv_heads;
+  const int heads = c->batch * c->n_q_heads, units = c->batch * c->n_kv_heads;
   const bool paged = c->page_size != 0;
-  int per_sm = c->dtype == MAC_F32 ? step_occupancy_f32(G, paged, units)
-                                   : step_occupancy_bf16(G, paged, units);
+  int per_sm = c->dtype == MAC_F32 ? step_occupancy_f32(G, paged, heads, units, c->ring_k)
+                                   : step_occupancy_bf16(G, paged, heads, units, c->ring_k);
   if (per_sm < 1) return 0;
-  return num_sms() * per_sm;
+  const int grid = num_sms() * per_sm;
+  return grid < kMaxGrid ? grid : kMaxGrid;
 }
 
 cudaError_t launch_step(StepParams p, const mac_config *c, cudaStream_t s);
@@ -140,7 +141,6 @@ StepParams step_params(const mac_config *c, const ScratchLayout &S, uint8_t *scr
   a.G = c->n_q_heads / c->n_kv_heads;
   a.K = c->ring_k;
   a.r = c->band_r;
-  a.n_tail = n_tail_chunks(c->band_r);
   a.min_context = c->min_context;
   a.thr2 = threshold_sq(c);
   a.q_scale = q_scale(c);
@@ -152,11 +152,8 @@ StepParams step_params(const mac_config *c, const ScratchLayout &S, uint8_t *scr
     a.rope_w[j] = pow(c->rope_base, -2.0 * (double)j / (double)c->head_dim);
   a.ctl = (uint32_t *)(scratch + S.ctl);
   a.best = (unsigned long long *)(scratch + S.best);
-  a.match_cnt = (int32_t *)(scratch + S.match_cnt);
-  a.head_info = (int2 *)(scratch + S.head_info);
-  a.unit_s = (int32_t *)(scratch + S.unit_s);
-  a.tail_part = (float *)(scratch + S.tail_part);
-  a.partials = (float *)(scratch + S.partials);
+  a.part_a = (float *)(scratch + S.part_a);
+  a.part_b = (float *)(scratch + S.part_b);
   return a;
 }
 
@@ -297,7 +294,7 @@ int mac_init_rings(const mac_config *cfg, void *ring_ws, void *scratch_ws, const
   const ScratchLayout S = scratch_layout(cfg);
   uint8_t *ring = (uint8_t *)ring_ws, *scr = (uint8_t *)scratch_ws;
   if (cudaMemsetAsync(ring + R.pos, 0, (size_t)cfg->batch * cfg->ring_k * 4, s) != cudaSuccess ||
-      cudaMemsetAsync(scr, 0, S.partials, s) != cudaSuccess)
+      cudaMemsetAsync(scr, 0, S.part_a, s) != cudaSuccess)
     return MAC_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -428,7 +425,7 @@ int mac_full_attention_noalloc(const mac_config *cfg, const void *q_pre, const i
   if (!scratch) return MAC_ERR_CUDA;
   // the previous call left its counters and status in the array: clear the
   // control part (everything before the partials) on this call's stream
-  if (cudaMemsetAsync(scratch, 0, scratch_layout(cfg).partials, (cudaStream_t)stream) != cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, scratch_layout(cfg).part_a, (cudaStream_t)stream) != cudaSuccess)
     return MAC_ERR_CUDA;
   return mac_full_attention(cfg, scratch, q_pre, seq_len, kv, out, lse, stream);
 }

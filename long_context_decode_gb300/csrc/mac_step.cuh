@@ -5,40 +5,48 @@
 //   rings of all (request, head) pairs form one contiguous array of B*Hq*K
 //   rows; CTA c streams rows [c*N/P, (c+1)*N/P) through shared memory and
 //   computes each candidate's squared distance to its head's current query.
-//   Each lane sums (a-b)^2 of its elements in a pairwise tree (a-b of two
-//   bf16 values is exact in fp32) and the lanes of a row finish the tree with
-//   shuffles, so the distance carries at most ~8 roundings; the pages'
-//   expansion |a|^2+|b|^2-2a.b cancels badly for close pairs and is not
-//   used.  A head's best (distance, position) is combined across CTAs with a
-//   64-bit atomic max of a packed key, a total order (smaller distance, then
-//   more recent position), so the result does not depend on scheduling.  The
-//   last CTA to finish a (request, kv-head) unit turns the minima into
-//   decisions and the unit's fresh-range start.
+//   Eight lanes share a row; each sums (a-b)^2 of its 16 elements in a
+//   pairwise tree (a-b of two bf16 values is exact in fp32) and the eight
+//   finish the tree with shuffles, so a distance carries at most 8 roundings
+//   of non-negative terms.  The pages' expansion |a|^2+|b|^2-2a.b cancels
+//   badly for close pairs and is not used.  A head's best (distance,
+//   position) is combined across CTAs with a 64-bit atomic max of a packed
+//   key, a total order (smaller distance, then more recent position), so the
+//   result does not depend on scheduling.
 //
-//   Tail chunks (Complete, K2, part 1): the last r tokens of every unit are
-//   attended by every head whatever the match says (each head's band starts
-//   at or before m-r+1), so they are streamed right after the match slice,
-//   before the grid barrier.
+//   Phase A (Complete, K2, part 1): the last r tokens of every unit (request,
+//   kv head) are attended by every head whatever the match says (each head's
+//   band starts at or before m-r+1), so they are streamed right after the
+//   match slice, before the grid barrier.
 //
-//   Grid barrier; band chunks (K2, part 2): the band [s, m-r] of every unit,
-//   which depends on the decisions, cut into chunks (plan_band) dealt
-//   round-robin to the CTAs.  A GQA group loads each K/V tile once for its G
-//   query heads ([MAC] "GQA intra-group skew"); heads that reuse from a later
-//   position mask the tokens before their own band start.  Every chunk leaves
-//   a partial summary (running max, sum, weighted values; base-2 log domain,
-//   [MAC] "Complete").
+//   Grid barrier; every CTA turns the minima into decisions ([MAC] K1: hit
+//   iff the smallest squared distance is strictly below thr^2) and lays out
+//   the band [s, m-r] of every unit (s = first token any head of the unit
+//   needs: p-r+1 for a hit at p, 1 for a miss).  Phase B (K2, part 2)
+//   attends the bands; a head whose band starts later than s masks the
+//   tokens before its own start ([MAC] "GQA intra-group skew").
 //
-//   Grid barrier; phase R: per (request, head), the chunk partials are merged
-//   in a fixed order after the cached rectified summary of a hit head: the
-//   band chunks give AS_{1:m-r}, the tail chunks then give the output.
+//   Grid barrier; phase R: per (request, head), the piece partials are merged
+//   in token order after the cached rectified summary of a hit head: the band
+//   pieces give AS_{1:m-r}, the tail pieces then give the output.
 //
-// Full attention (and ring seeding) run the same attention code with s = 1,
-// which is what makes a miss bitwise equal to it.  All phases stream through
-// one ring of kStages shared-memory stages filled with 1-D TMA bulk copies
-// (issued by thread 0, which polls the empty barriers without blocking and
-// refills every stage it finds released) and drained by the CTA's 8 warps
-// (full/empty mbarriers);
-// every wait is bounded and reports MAC_DEV_WAIT_TIMEOUT instead of hanging.
+// Work balance ("span-balanced" flash decode): in phases A and B the tokens
+// of all units are laid end to end and cut into one contiguous span per CTA,
+// so every CTA streams the same number of tokens however the band lengths
+// are spread.  A span meets a few units; each meeting (a piece) leaves one
+// partial summary (running max, sum, weighted values; base-2 log domain,
+// [MAC] "Complete").  A GQA group loads each K/V tile once for its G query
+// heads.  Full attention (and ring seeding) run phases A and B with s = 1 and
+// no match; the pieces are then the same as those of a decode step whose
+// heads all miss, which makes such a step bitwise equal to full attention.
+//
+// Streaming: one ring of kStages shared-memory stages filled with 1-D TMA
+// bulk copies and drained by the CTA's 8 warps.  Every warp releases a stage
+// with an acquire-release add on the stage's counter; the warp whose release
+// completes the count refills the stage with the next use of the CTA's
+// sequence (issue cursor in shared memory, taken in order).  No thread waits
+// for another warp to refill, and every wait is bounded and reports
+// MAC_DEV_WAIT_TIMEOUT instead of hanging.
 #pragma once
 
 #include "mac_common.cuh"
@@ -80,60 +88,97 @@ __device__ __forceinline__ void unpack16x2<float>(const uint4 &u, float2 *f) {
   f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
 }
 
+constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x >> 1); }
+
+// Running maxima start here (finite, so that empty states never produce
+// inf - inf) and are raised only when a score exceeds them by kLazy (base-2
+// log units): the accumulators then stay within 2^kLazy of the true scale.
+constexpr float kMInit = -1e30f;
+constexpr float kLazy = 8.f;
+constexpr unsigned kFull = 0xffffffffu;
+
 template <typename T, int G, bool PAGED>
 struct Step {
   static constexpr int kRowBytes = kHeadDim * (int)sizeof(T);
   static constexpr int kTileTok = kStageBytes / (2 * kRowBytes);  // 64 (bf16) / 32 (fp32)
-  static constexpr int kTokPerGroup = kTileTok / 32;              // tokens per lane group per tile
+  static constexpr int kTPG = kTileTok / 32;                      // tokens per lane group per tile
   static constexpr int kMatchRows = kStageBytes / kRowBytes;      // ring rows per stage
   static constexpr int kPer = 16 / (int)sizeof(T);                // elements per 16-byte piece
   static constexpr int kNP = 16 / kPer;                           // pieces per lane (16 dims)
   static constexpr int kPairs = 8;                                // float2 pairs per lane (16 dims)
-  static constexpr int kLPS = kHeadDim / kPer;                    // lanes per ring row
-  static constexpr int kRowGroups = kThreads / kLPS;              // ring rows in flight per pass
+  static constexpr int kV = kTPG * G;                             // scores of a lane group per tile
+  static constexpr int kScat = ilog2c(kV);                        // reduce-scatter levels
+  static constexpr int kPlain = 3 - kScat;                        // plain butterfly levels after them
   static constexpr int kQBytes = G * kRowBytes;
+  static constexpr int kRedGroups = 2;                            // lane groups per warp per epilogue round
+  static constexpr int kOutPer = (G * kHeadDim + kThreads - 1) / kThreads;
+  static_assert(kV <= 8, "one score per lane of a group at most");
 
   // dynamic shared memory layout
   static constexpr size_t kOffQ = (size_t)kStages * kStageBytes;
   static constexpr size_t kOffBar = kOffQ + (size_t)kStages * kQBytes;
-  static constexpr size_t kOffQrot = kOffBar + 128;
-  static constexpr size_t kOffRed = kOffQrot + (size_t)G * kHeadDim * 4;
-  static constexpr size_t kOffPos = kOffRed + (size_t)kWarps * G * kPartStride * 4;
-  // phase M: ring positions of the requests a match slice touches; band
-  // chunks and phase R: the first fresh token of every head
-  static constexpr int kPosInts = kMaxHeads;
-  static constexpr size_t kOffUnits = kOffPos + 4 * (size_t)kPosInts;
-  // per unit: first band chunk (prefix, n_units + 1), query position, fresh-range start
-  static size_t smem_bytes(int n_units) { return kOffUnits + 4 * (size_t)(3 * n_units + 1); }
+  static constexpr size_t kOffAng = kOffBar + 64;
+  static constexpr size_t kOffQrot = kOffAng + 8 * (kHeadDim / 2);
+  static constexpr size_t kOffRedO = kOffQrot + 4 * (size_t)G * kHeadDim;
+  static constexpr size_t kOffRedL = kOffRedO + 4 * (size_t)kWarps * kRedGroups * G * kHeadDim;
+  static constexpr size_t kOffRedM = kOffRedL + 4 * (size_t)kWarps * 4 * G;
+  static constexpr size_t kOffX = kOffRedM + 4 * (size_t)kWarps * G;
+  static_assert(kOffBar % 8 == 0 && kOffX % 8 == 0, "alignment");
+
+  // phase M: ring positions of the requests a match slice touches; after the
+  // decisions: the matched position of every head (-1: miss)
+  __host__ __device__ static int x_ints(int n_heads, int K) {
+    const int stage = 2 * K < kPosStage ? 2 * K : kPosStage;
+    return n_heads > stage ? n_heads : stage;
+  }
+  __host__ __device__ static size_t off_units(int n_heads, int K) {
+    return (kOffX + 4 * (size_t)x_ints(n_heads, K) + 7) / 8 * 8;
+  }
+  // + offsets of the tail and band segments (int64, n_units + 1 each), query
+  // position and band start of every unit (int32)
+  __host__ __device__ static size_t smem_bytes(int n_heads, int n_units, int K) {
+    return off_units(n_heads, K) + 16 * ((size_t)n_units + 1) + 8 * (size_t)n_units;
+  }
+
+  // Issue cursor: the next use of the CTA's stage sequence (match chunks,
+  // then the tiles of the CTA's pieces).  Only the thread issuing use n
+  // touches it, after the issue of use n - 1 has published n.
+  enum { C_MATCH = 0, C_TILES = 1, C_END = 2 };
+  struct Cursor {
+    uint32_t n;          // next use to issue
+    uint32_t n_copied;   // uses issued with their copies (all of them unless aborted)
+    int kind;
+    int ph;              // phase of the tile sequence: 0 tails, 1 bands
+    int cont;            // go on from phase 0 into phase 1 (full attention)
+    int u, lo, hi, first;
+    int64_t r, s1;       // match: next ring row, end of the slice
+    int64_t tile, tile_last;
+    int64_t g0, g1;      // span of this CTA in phase ph
+  };
 
   struct Smem {
     uint8_t *stage;     // [kStages][kStageBytes]
-    uint8_t *qbuf;      // [kStages][kQBytes]
+    uint8_t *qbuf;      // [kStages][G][d]: pre-RoPE query rows of a piece's unit
     uint64_t *full;     // [kStages]
-    uint64_t *empty;    // [kStages]
+    float2 *ang;        // [d/2]: cos, sin of the RoPE angles of the current piece
     float *qrot;        // [G][d]
-    float *red;         // [kWarps][G][kPartStride]
-    int32_t *pos;       // [kPosInts]
-    int32_t *prefix;    // [n_units + 1]
+    float *red_o;       // [kWarps][kRedGroups][G][d]
+    float *red_l;       // [kWarps * 4][G]
+    float *red_m;       // [kWarps][G]
+    int32_t *X;
+    int nx;
+    int64_t *offA;      // [n_units + 1]: first global index of each unit's tail segment
+    int64_t *offB;      // [n_units + 1]: same for the band segments
     int32_t *u_pos;     // [n_units]: position of the unit's query (RoPE angle pos - 1)
-    int32_t *u_s;       // [n_units]: first token any head of the unit reads
+    int32_t *u_s;       // [n_units]: first band token of the unit
+    uint32_t *cnt;      // [kStages]: releases of the stage's current use
     int *mask;          // [kStages]: valid 16-token pages of the tile in the stage
     volatile int *abort;
+    Cursor *cur;
   };
 
-  // Producer cursor, kept by thread 0: the next stage use to fill in the
-  // CTA's sequence (match chunks, tail tiles, band tiles).  n counts the uses
-  // issued so far; the consumers count the same sequence, so use n goes to
-  // stage n % kStages.  Thread 0 never blocks on a release: it polls (pump)
-  // after each of its own releases and while it waits for data.
-  enum { P_MATCH = 0, P_TAIL = 1, P_IDLE = 2, P_BAND = 3, P_DONE = 4 };
-  struct Producer {
-    uint32_t n;
-    int phase;
-    int64_t r, s1;   // match: next ring row, end of the slice
-    int item, total; // tail/band: current item index, number of items
-    int k, ntiles, b, g, lo, hi;
-    int64_t tile0;
+  struct Piece {
+    int u, lo, hi;
   };
 
   // Lane `sub` (0..7) of a token's 8-lane group owns 16 dimensions: piece c
@@ -141,51 +186,106 @@ struct Step {
   // contiguous bytes of a row per piece (no shared-memory bank conflicts).
   __device__ static int piece_dim(int c, int sub) { return c * 8 * kPer + sub * kPer; }
 
-  // the scratch holds the chunk partials of lengths up to max_len only
+  // the lengths the scratch and the cache hold
   __device__ static bool len_ok(const StepParams &p, int64_t m) { return m >= 1 && m <= p.max_len; }
   __device__ static int64_t unit_len(const StepParams &p, const Smem &S, int u) {
     return (int64_t)S.u_pos[u] - p.len_sub;
   }
 
-  __device__ static BandPlan plan(const StepParams &p, const Smem &S, int u) {
+  // ---------------------------------------------------------------------
+  // segments, spans and pieces
+  // ---------------------------------------------------------------------
+
+  // First token of unit u's segment: tails [max(1, m-r+1), m], bands [s, m-r].
+  __device__ static int64_t seg_first(const StepParams &p, const Smem &S, int ph, int u) {
+    if (ph == 1) return S.u_s[u];
+    const int64_t a = unit_len(p, S, u) - p.r + 1;
+    return a > 1 ? a : 1;
+  }
+  __device__ static int64_t seg_len(const StepParams &p, const Smem &S, int ph, int u) {
     const int64_t m = unit_len(p, S, u);
-    if (!len_ok(p, m)) return plan_band(0, 1, p.r);
-    return plan_band(m, S.u_s[u], p.r);
+    if (!len_ok(p, m)) return 0;
+    if (ph == 0) return m < p.r ? m : p.r;
+    const int64_t n = (m - p.r) - (int64_t)S.u_s[u] + 1;
+    return n > 0 ? n : 0;
   }
 
-  // tail chunk ti (unit ti / n_tail, chunk ti % n_tail)
-  __device__ static void tail_item(const StepParams &p, const Smem &S, int ti, int *u, int *lo,
-                                   int *hi) {
-    *u = ti / p.n_tail;
-    const int64_t m = unit_len(p, S, *u);
-    int64_t a = 1, z = 0;
-    if (len_ok(p, m)) tail_range(m, p.r, ti % p.n_tail, &a, &z);
-    *lo = (int)a;
-    *hi = (int)z;
-  }
+  __device__ static const int64_t *offs(const Smem &S, int ph) { return ph ? S.offB : S.offA; }
 
-  __device__ static int unit_of_item(const int32_t *prefix, int n_units, int item) {
-    int lo = 0, hi = n_units - 1;
+  // span [g0, g1) of CTA c: global indices c*T/P .. (c+1)*T/P
+  __device__ static int64_t span_beg(const int64_t *off, int U, int c, int P) {
+    return (int64_t)c * off[U] / P;
+  }
+  // the CTA whose (non-empty) span holds global index x (x < total)
+  __device__ static int cta_of(int64_t x, int64_t total, int P) {
+    return (int)(((x + 1) * (int64_t)P + total - 1) / total) - 1;
+  }
+  // unit whose segment holds global index g (g < T)
+  __device__ static int unit_of(const int64_t *off, int U, int64_t g) {
+    int lo = 0, hi = U - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+      if (off[mid] <= g) lo = mid; else hi = mid - 1;
     }
     return lo;
   }
 
-  // band chunk `item` (global index over all units' band chunks)
-  __device__ static void band_item(const StepParams &p, const Smem &S, int item, int *u, int *lo,
-                                   int *hi) {
-    *u = unit_of_item(S.prefix, p.B * p.Hkv, item);
-    int64_t a, z;
-    band_range(plan(p, S, *u), p.r, item - S.prefix[*u], &a, &z);
-    *lo = (int)a;
-    *hi = (int)z;
+  // The first piece of span [g0, g1) at unit >= u; false when none is left.
+  __device__ static bool find_piece(const StepParams &p, const Smem &S, int ph, int u, int64_t g0,
+                                    int64_t g1, Piece *pc) {
+    const int64_t *off = offs(S, ph);
+    const int U = p.B * p.Hkv;
+    for (; u < U; ++u) {
+      const int64_t a0 = off[u], z0 = off[u + 1];
+      if (a0 >= g1) return false;
+      const int64_t a = a0 > g0 ? a0 : g0, z = z0 < g1 ? z0 : g1;
+      if (a < z) {
+        const int64_t t0 = seg_first(p, S, ph, u);
+        pc->u = u;
+        pc->lo = (int)(t0 + (a - a0));
+        pc->hi = (int)(t0 + (z - a0) - 1);
+        return true;
+      }
+    }
+    return false;
   }
 
-  // first CTA whose match slice contains ring row x
-  __device__ static int cta_of_row(int64_t x, int64_t N, int P) {
-    return (int)(((x + 1) * (int64_t)P - 1) / N);
+  // Exclusive prefix of the segment lengths of phase ph over all units
+  // (block-wide scan; ends with a __syncthreads).
+  __device__ static void layout_phase(const StepParams &p, const Smem &S, int ph) {
+    __shared__ long long wsum[kWarps];
+    int64_t *off = ph ? S.offB : S.offA;
+    const int U = p.B * p.Hkv;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (U + kThreads - 1) / kThreads;
+    const int beg = min(tid * per, U), end = min(beg + per, U);
+    long long run = 0;
+    for (int u = beg; u < end; ++u) {
+      run += seg_len(p, S, ph, u);
+      off[u + 1] = run;
+    }
+    long long x = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      long long w = lane < kWarps ? wsum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(kFull, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < kWarps) wsum[lane] = w;
+    }
+    __syncthreads();
+    const long long excl = x - run + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int u = beg; u < end; ++u) off[u + 1] += excl;
+    if (tid == 0) off[0] = 0;
+    __syncthreads();
   }
 
   // ---------------------------------------------------------------------
@@ -194,9 +294,10 @@ struct Step {
 
   // Rows of K/V tile `tile` (tokens tile*kTileTok+1 .. +kTileTok) that fall in
   // [lo, hi], each copied to its own row of the stage, so no byte outside the
-  // chunk is read; with_q also brings the unit's G pre-RoPE query rows.
-  __device__ static void issue_tile(const StepParams &p, const Smem &S, int st, int b, int g, int lo,
+  // piece is read; with_q also brings the unit's G pre-RoPE query rows.
+  __device__ static void issue_tile(const StepParams &p, const Smem &S, int st, int u, int lo,
                                     int hi, int64_t tile, bool with_q) {
+    const int b = u / p.Hkv, g = u % p.Hkv;
     uint8_t *kbuf = S.stage + (size_t)st * kStageBytes;
     uint8_t *vbuf = kbuf + kStageBytes / 2;
     const uint32_t bar = smem_addr(&S.full[st]);
@@ -270,104 +371,164 @@ struct Step {
     return e;
   }
 
-  // Position the cursor on the next stage use of the CTA's sequence; false
-  // when the current phase has nothing more (tail -> idle until the band
-  // chunks are known, band -> done).
-  __device__ static bool next_use(const StepParams &p, const Smem &S, Producer &pr) {
-    for (;;) {
-      if (pr.phase == P_MATCH) {
-        if (pr.r < pr.s1) return true;
-        pr.phase = P_TAIL;
-        pr.item = -1;
-        pr.total = p.B * p.Hkv * p.n_tail;
-        pr.k = pr.ntiles = 0;
+  __device__ static void cursor_piece(Cursor &c, const Piece &pc) {
+    c.kind = C_TILES;
+    c.u = pc.u;
+    c.lo = pc.lo;
+    c.hi = pc.hi;
+    c.tile = (pc.lo - 1) / kTileTok;
+    c.tile_last = (pc.hi - 1) / kTileTok;
+    c.first = 1;
+  }
+
+  // Put the cursor on the first tile of this CTA's pieces in phase ph (then
+  // phase 1 when c.cont), or end it.
+  __device__ static void cursor_phase(const StepParams &p, const Smem &S, Cursor &c, int ph) {
+    const int U = p.B * p.Hkv, P = gridDim.x;
+    for (;; ++ph) {
+      const int64_t *off = offs(S, ph);
+      c.ph = ph;
+      c.g0 = span_beg(off, U, blockIdx.x, P);
+      c.g1 = span_beg(off, U, blockIdx.x + 1, P);
+      Piece pc;
+      if (c.g0 < c.g1 && find_piece(p, S, ph, unit_of(off, U, c.g0), c.g0, c.g1, &pc)) {
+        cursor_piece(c, pc);
+        return;
       }
-      if (pr.phase != P_TAIL && pr.phase != P_BAND) return false;
-      if (pr.k < pr.ntiles) return true;
-      pr.item = pr.item < 0 ? (int)blockIdx.x : pr.item + (int)gridDim.x;
-      if (pr.item >= pr.total) {
-        pr.phase = pr.phase == P_TAIL ? P_IDLE : P_DONE;
-        return false;
-      }
-      int u;
-      if (pr.phase == P_TAIL)
-        tail_item(p, S, pr.item, &u, &pr.lo, &pr.hi);
-      else
-        band_item(p, S, pr.item, &u, &pr.lo, &pr.hi);
-      pr.b = u / p.Hkv;
-      pr.g = u % p.Hkv;
-      pr.k = 0;
-      pr.ntiles = 0;
-      if (pr.lo <= pr.hi) {
-        pr.tile0 = (pr.lo - 1) / kTileTok;
-        pr.ntiles = (int)((pr.hi - 1) / kTileTok - pr.tile0 + 1);
+      if (ph != 0 || !c.cont) {
+        c.kind = C_END;
+        return;
       }
     }
   }
 
-  // Issue the use the cursor is on into stage pr.n % kStages (free) and advance.
-  __device__ static void issue_current(const StepParams &p, const Smem &S, Producer &pr) {
-    const int st = pr.n % kStages;
-    if (pr.phase == P_MATCH) {
-      const int64_t e = chunk_end(pr.r, pr.s1, p.K);
-      if (!*S.abort) {
-        const uint32_t bytes = (uint32_t)(e - pr.r) * kRowBytes;
+  __device__ static void cursor_next(const StepParams &p, const Smem &S, Cursor &c) {
+    if (c.kind == C_MATCH) {
+      c.r = chunk_end(c.r, c.s1, p.K);
+      if (c.r >= c.s1) cursor_phase(p, S, c, 0);
+      return;
+    }
+    c.first = 0;
+    if (++c.tile <= c.tile_last) return;
+    Piece pc;
+    if (find_piece(p, S, c.ph, c.u + 1, c.g0, c.g1, &pc)) {
+      cursor_piece(c, pc);
+      return;
+    }
+    if (c.ph == 0 && c.cont) {
+      cursor_phase(p, S, c, 1);
+      return;
+    }
+    c.kind = C_END;
+  }
+
+  // Issue the cursor's use into its stage (free by construction), advance
+  // and publish the next use index.
+  __device__ static void issue_current(const StepParams &p, const Smem &S) {
+    Cursor &c = *S.cur;
+    const int st = c.n % kStages;
+    const bool go = !*S.abort;
+    if (c.kind == C_MATCH) {
+      if (go) {
+        const int64_t e = chunk_end(c.r, c.s1, p.K);
+        const uint32_t bytes = (uint32_t)(e - c.r) * kRowBytes;
         const uint32_t bar = smem_addr(&S.full[st]);
         fence_proxy_async();
         mbar_expect_tx(bar, bytes);
         bulk_g2s(smem_addr(S.stage + (size_t)st * kStageBytes),
-                 (const uint8_t *)p.ring_q + (size_t)pr.r * kRowBytes, bytes, bar);
+                 (const uint8_t *)p.ring_q + (size_t)c.r * kRowBytes, bytes, bar);
       }
-      pr.r = e;
-    } else {
-      if (!*S.abort) issue_tile(p, S, st, pr.b, pr.g, pr.lo, pr.hi, pr.tile0 + pr.k, pr.k == 0);
-      ++pr.k;
+    } else if (go) {
+      issue_tile(p, S, st, c.u, c.lo, c.hi, c.tile, c.first != 0);
     }
-    ++pr.n;
+    if (go) c.n_copied = c.n + 1;
+    cursor_next(p, S, c);
+    __threadfence_block();
+    *(volatile uint32_t *)&c.n = c.n + 1;
   }
 
-  // Issue every next use whose stage is already free, without blocking
-  // (thread 0 only).  Thread 0 also consumes tiles, so it must never wait
-  // for the other warps here: it refills as soon as it finds a stage free,
-  // here after each of its own releases and inside its own waits.
-  __device__ static void pump(const StepParams &p, const Smem &S, Producer &pr) {
-    while (next_use(p, S, pr)) {
-      const int st = pr.n % kStages;
-      if (!*S.abort &&
-          !mbar_test_wait(smem_addr(&S.empty[st]), ((pr.n / kStages) & 1u) ^ 1u))
-        return;
-      issue_current(p, S, pr);
-    }
-  }
-
-  // Consumer wait for stage use n; thread 0 keeps the copies flowing while
-  // it waits.  Bounded like every wait (about a second, or at once after an
-  // abort).
-  __device__ static bool wait_full_pump(const StepParams &p, const Smem &S, Producer &pr, int st,
-                                        uint32_t n) {
-    const uint32_t bar = smem_addr(&S.full[st]);
-    const uint32_t parity = n & 1u;
-    if (threadIdx.x != 0) return mbar_wait_bounded(bar, parity, S.abort);
+  // Issue use `target` (by the warp whose release freed its stage): waits,
+  // bounded, until the issue of use target - 1 has been published.
+  __device__ static void issue_use(const StepParams &p, const Smem &S, uint32_t target) {
+    volatile Cursor *vc = S.cur;
     const long long t0 = clock64();
     for (;;) {
-      if (mbar_test_wait(bar, parity)) return true;
-      pump(p, S, pr);
-      if (*S.abort || clock64() - t0 > (1LL << 31)) return false;
+      if (vc->kind == C_END) return;
+      if (vc->n == target) break;
+      if (*S.abort) return;
+      if (clock64() - t0 > (1LL << 31)) {
+        set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
+        *S.abort = 1;
+        return;
+      }
     }
+    __threadfence_block();
+    if (S.cur->kind == C_END) return;
+    issue_current(p, S);
+  }
+
+  // Release stage use n (every warp, once); the last warp to release it
+  // refills the stage with use n + kStages.
+  __device__ static void release(const StepParams &p, const Smem &S, uint32_t n) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+      const int st = n % kStages;
+      if (atom_add_acqrel_shared(smem_addr(&S.cnt[st]), 1u) == kWarps - 1) {
+        S.cnt[st] = 0;
+        issue_use(p, S, n + kStages);
+      }
+    }
+    __syncwarp();
+  }
+
+  __device__ static bool wait_use(const Smem &S, uint32_t n) {
+    const bool ok = mbar_wait_bounded(smem_addr(&S.full[n % kStages]), (n / kStages) & 1u, S.abort);
+    if (!ok) *S.abort = 1;
+    return ok;
   }
 
   // ---------------------------------------------------------------------
   // phase M
   // ---------------------------------------------------------------------
 
-  // Combine the CTA's running best of head bh and publish it.
-  __device__ static void flush_best(const StepParams &p, int64_t bh, float bd, int bp, float *s_bd,
-                                    int *s_bp) {
+  // Squared L2 distance between the lane's 16 query elements and the row's:
+  // exact differences (bf16), squares and a pairwise tree in the lane, then
+  // the 8 lanes of the group (xor 1, 2, 4); every lane gets the sum.
+  __device__ static float row_dist(const uint8_t *row, int sub, const float2 *qv) {
+    float2 df[kPairs];
+#pragma unroll
+    for (int c = 0; c < kNP; ++c) {
+      float2 e2[kPer / 2];
+      unpack16x2<T>(*reinterpret_cast<const uint4 *>(row + c * 128 + sub * 16), e2);
+#pragma unroll
+      for (int k = 0; k < kPer / 2; ++k) {
+        const float2 q = qv[c * (kPer / 2) + k];
+        df[c * (kPer / 2) + k] = __fadd2_rn(q, make_float2(-e2[k].x, -e2[k].y));
+      }
+    }
+    float2 t[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) t[k] = __ffma2_rn(df[k + 4], df[k + 4], __fmul2_rn(df[k], df[k]));
+    t[0] = __fadd2_rn(t[0], t[2]);
+    t[1] = __fadd2_rn(t[1], t[3]);
+    t[0] = __fadd2_rn(t[0], t[1]);
+    float D = __fadd_rn(t[0].x, t[0].y);
+    D = __fadd_rn(D, __shfl_xor_sync(kFull, D, 1));
+    D = __fadd_rn(D, __shfl_xor_sync(kFull, D, 2));
+    D = __fadd_rn(D, __shfl_xor_sync(kFull, D, 4));
+    return D;
+  }
+
+  // The best candidate of head bh over this CTA (all groups hold theirs)
+  // joins the global minimum.
+  __device__ static void flush_best(const StepParams &p, const Smem &S, int64_t bh, float bd, int bp) {
+    __shared__ float s_bd[kWarps];
+    __shared__ int s_bp[kWarps];
     const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31;
 #pragma unroll
-    for (int off = 16; off >= kLPS; off >>= 1) {
-      const float d2 = __shfl_xor_sync(0xffffffffu, bd, off);
-      const int p2 = __shfl_xor_sync(0xffffffffu, bp, off);
+    for (int off = 8; off <= 16; off <<= 1) {
+      const float d2 = __shfl_xor_sync(kFull, bd, off);
+      const int p2 = __shfl_xor_sync(kFull, bp, off);
       if (better(d2, p2, bd, bp)) {
         bd = d2;
         bp = p2;
@@ -389,74 +550,45 @@ struct Step {
     consumer_sync();
   }
 
-  // Decisions of unit u from the combined minima ([MAC] K1: hit iff the
-  // smallest squared distance is strictly below thr^2).
-  __device__ static void finalize_unit(const StepParams &p, int u) {
-    const int b = u / p.Hkv, g = u % p.Hkv;
-    const int64_t m = (int64_t)p.pos_base[b] + p.pos_add - p.len_sub;
-    const bool m_ok = len_ok(p, m);
-    if (!m_ok && p.check_len) set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
-    int s = 0x7fffffff;
-    for (int hh = 0; hh < G; ++hh) {
-      const int64_t bh = (int64_t)b * p.Hq + g * G + hh;
-      const unsigned long long inv = atomicExch(&p.best[bh], 0ull);
-      bool hit = false;
-      int pos = -1;
-      if (inv != 0ull) {
-        const unsigned long long key = ~inv;
-        const float d = __uint_as_float((uint32_t)(key >> 32));
-        pos = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-        hit = m_ok && d < p.thr2 && m >= p.min_context;
-      }
-      const int lo = hit ? (pos - p.r + 1 > 1 ? pos - p.r + 1 : 1) : 1;
-      p.head_info[bh] = make_int2(hit ? pos : -1, lo);
-      if (p.match_pos_out) p.match_pos_out[bh] = hit ? pos : -1;
-      s = lo < s ? lo : s;
-    }
-    p.unit_s[u] = s;
-    p.match_cnt[u] = 0;
-  }
-
-  __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &tc, Producer &pr) {
-    __shared__ float s_bd[kWarps];
-    __shared__ int s_bp[kWarps];
+  __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n) {
     const int64_t N = (int64_t)p.B * p.Hq * p.K;
     const int P = gridDim.x, c = blockIdx.x;
     const int64_t s0 = (int64_t)c * N / P, s1 = (int64_t)(c + 1) * N / P;
-    const int ct = threadIdx.x, lane = ct & 31;
-    const int sub = lane % kLPS;  // lane within its row
-    const int rg = ct / kLPS;     // row group (rows rg, rg + kRowGroups, ...)
-    const unsigned gmask = kLPS == 32 ? 0xffffffffu : (0xffffu << (lane & 16));
+    const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31, sub = lane & 7;
+    const int grp = warp * 4 + (lane >> 3);  // row group: rows grp, grp + 32, ... of a chunk
 
-    // slot positions of the requests the slice touches, staged in shared
-    // memory once (they are shared by all heads of a request)
+    // slot positions of the requests the slice touches, staged once (they
+    // are shared by all heads of a request)
     const int64_t rows_per_req = (int64_t)p.Hq * p.K;
     const int b_lo = (int)(s0 / rows_per_req);
     const int b_hi = s1 > s0 ? (int)((s1 - 1) / rows_per_req) : b_lo - 1;
-    const bool staged = (int64_t)(b_hi - b_lo + 1) * p.K <= kPosInts;
+    const bool staged = (int64_t)(b_hi - b_lo + 1) * p.K <= S.nx;
     if (staged) {
-      const int n = (b_hi - b_lo + 1) * p.K;
+      const int cnt = (b_hi - b_lo + 1) * p.K;
       const int32_t *src = p.ring_pos + (int64_t)b_lo * p.K;
-      for (int i = ct; i < n; i += kThreads) S.pos[i] = src[i];
+      for (int i = ct; i < cnt; i += kThreads) S.X[i] = src[i];
     }
     __syncthreads();
 
     int64_t cur = -1;
     float bd = INFINITY;
     int bp = -1;
-    float2 qv[kPer / 2];
+    float2 qv[kPairs];
     int pos_lo = 1, pos_hi = 0;
     const int32_t *rpos = p.ring_pos;
-    for (int64_t r = s0; r < s1;) {
+    for (int64_t r = s0; r < s1; ++n) {
       const int64_t e = chunk_end(r, s1, p.K);
       const int64_t bh = r / p.K;
       const int b = (int)(bh / p.Hq);
       if (bh != cur) {
-        if (cur >= 0) flush_best(p, cur, bd, bp, s_bd, s_bp);
+        if (cur >= 0) flush_best(p, S, cur, bd, bp);
         cur = bh;
         bd = INFINITY;
         bp = -1;
-        unpack16x2<T>(reinterpret_cast<const uint4 *>(p.q)[(bh * p.q_stride + p.q_offset) / kPer + sub], qv);
+        const uint8_t *qrow = (const uint8_t *)p.q + (size_t)(bh * p.q_stride + p.q_offset) * sizeof(T);
+#pragma unroll
+        for (int cc = 0; cc < kNP; ++cc)
+          unpack16x2<T>(*reinterpret_cast<const uint4 *>(qrow + cc * 128 + sub * 16), qv + cc * (kPer / 2));
         const int64_t m = (int64_t)S.u_pos[b * p.Hkv] - p.len_sub;
         if (len_ok(p, m)) {
           pos_lo = m - p.K > 1 ? (int)(m - p.K) : 1;
@@ -465,68 +597,33 @@ struct Step {
           pos_lo = 1;
           pos_hi = 0;
         }
-        rpos = staged ? S.pos + (int64_t)(b - b_lo) * p.K : p.ring_pos + (int64_t)b * p.K;
+        rpos = staged ? S.X + (int64_t)(b - b_lo) * p.K : p.ring_pos + (int64_t)b * p.K;
       }
-      const int st = tc % kStages;
-      const bool ok = wait_full_pump(p, S, pr, st, tc / kStages);
-      if (!ok) *S.abort = 1;
-      const int n = (int)(e - r);
+      const bool ok = wait_use(S, n);
+      const int cnt = (int)(e - r);
       const int slot0 = (int)(r % p.K);
-      const uint8_t *rows = S.stage + (size_t)st * kStageBytes;
-      for (int i = rg; i < n; i += kRowGroups) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(rows + (size_t)i * kRowBytes + sub * 16);
-        const int ps = rpos[slot0 + i];
-        float2 e2[kPer / 2];
-        unpack16x2<T>(v, e2);
-        // squared differences, then a pairwise tree: element k of the lane's
-        // piece is added to element k + kPer/2, k + kPer/4, ... (the packed
-        // pairs hold elements (2i, 2i+1), so each level adds pair i to pair
-        // i + w2/2 and the last level adds the two halves of a pair)
-#pragma unroll
-        for (int k = 0; k < kPer / 2; ++k) {
-          const float2 df = __fadd2_rn(qv[k], make_float2(-e2[k].x, -e2[k].y));  // exact for bf16
-          e2[k] = __fmul2_rn(df, df);
+      const uint8_t *rows = S.stage + (size_t)(n % kStages) * kStageBytes;
+      // two rows per group and pass (independent chains); rows past the
+      // chunk read stale stage bytes and are not considered
+      for (int i0 = 0; i0 < cnt; i0 += 64) {
+        const int ia = i0 + grp, ib = ia + 32;
+        const int ra = ia < cnt ? ia : cnt - 1, rb = ib < cnt ? ib : cnt - 1;
+        const float Da = row_dist(rows + (size_t)ra * kRowBytes, sub, qv);
+        const float Db = row_dist(rows + (size_t)rb * kRowBytes, sub, qv);
+        const int pa = rpos[slot0 + ra], pb = rpos[slot0 + rb];
+        if (ok && ia < cnt && pa >= pos_lo && pa <= pos_hi && better(Da, pa, bd, bp)) {
+          bd = Da;
+          bp = pa;
         }
-#pragma unroll
-        for (int w2 = kPer / 4; w2 >= 1; w2 >>= 1)
-#pragma unroll
-          for (int k = 0; k < w2; ++k) e2[k] = __fadd2_rn(e2[k], e2[k + w2]);
-        float D = __fadd_rn(e2[0].x, e2[0].y);
-#pragma unroll
-        for (int off = kLPS / 2; off >= 1; off >>= 1)
-          D = __fadd_rn(D, __shfl_xor_sync(gmask, D, off));
-        if (ok && ps >= pos_lo && ps <= pos_hi && better(D, ps, bd, bp)) {
-          bd = D;
-          bp = ps;
+        if (ok && ib < cnt && pb >= pos_lo && pb <= pos_hi && better(Db, pb, bd, bp)) {
+          bd = Db;
+          bp = pb;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&S.empty[st]));
-      if (ct == 0) pump(p, S, pr);
-      ++tc;
+      release(p, S, n);
       r = e;
     }
-    if (cur >= 0) flush_best(p, cur, bd, bp, s_bd, s_bp);
-
-    // count this CTA off every unit its slice touched; the last one decides
-    if (ct == 0 && s0 < s1) {
-      const int64_t rows_per_unit = (int64_t)G * p.K;
-      const int u0 = (int)(s0 / rows_per_unit), u1 = (int)((s1 - 1) / rows_per_unit);
-      __threadfence();
-      for (int u = u0; u <= u1; ++u) {
-        // CTAs whose (non-empty) slice meets the unit: with N >= P every
-        // slice holds >= 1 row, so all CTAs from the one holding the unit's
-        // first row to the one holding its last; with N < P every non-empty
-        // slice holds exactly one row, one CTA per row of the unit
-        const int first = cta_of_row((int64_t)u * rows_per_unit, N, P);
-        const int last = cta_of_row((int64_t)(u + 1) * rows_per_unit - 1, N, P);
-        const int64_t target = N >= P ? (int64_t)(last - first + 1) : rows_per_unit;
-        if (atomicAdd(&p.match_cnt[u], 1) == target - 1) {
-          __threadfence();
-          finalize_unit(p, u);
-        }
-      }
-    }
+    if (cur >= 0) flush_best(p, S, cur, bd, bp);
   }
 
   // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.
@@ -550,246 +647,311 @@ struct Step {
     __syncthreads();
   }
 
-  // ---------------------------------------------------------------------
-  // attention over one chunk
-  // ---------------------------------------------------------------------
-
-  // Attend the unit's G heads to tokens [lo, hi] (heads with lo_h > t skip
-  // token t) and store the chunk's partial summaries at dst.
-  __device__ static void process_chunk(const StepParams &p, const Smem &S, uint32_t &tc,
-                                       Producer &pr, int u, int lo, int hi, const int *lo_h,
-                                       float *dst) {
-    const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31;
-    const int lg = lane >> 3, sub = lane & 7;
-    float2 q[G][kPairs], o[G][kPairs];
-    float mrun[G], lrun[G];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      mrun[hh] = -INFINITY;
-      lrun[hh] = 0.f;
-#pragma unroll
-      for (int i = 0; i < kPairs; ++i) o[hh][i] = make_float2(0.f, 0.f);
-    }
-
-    if (lo <= hi) {
-      const int64_t tile0 = (lo - 1) / kTileTok;
-      const int ntiles = (int)((hi - 1) / kTileTok - tile0 + 1);
-      for (int k = 0; k < ntiles; ++k) {
-        const int st = tc % kStages;
-        const bool ok = wait_full_pump(p, S, pr, st, tc / kStages);
-        if (!ok) *S.abort = 1;
-        if (k == 0) {
-          // R(pos) q~ * log2(e)/sqrt(d) for the unit's heads, from the query
-          // rows that came with the first tile
-          const int64_t pos = S.u_pos[u];
-          for (int idx = ct; idx < G * (kHeadDim / 2); idx += kThreads) {
-            const int hh = idx / (kHeadDim / 2), j = idx % (kHeadDim / 2);
-            if (!rope_rotate_pair<T>(S.qbuf + (size_t)st * kQBytes, (int64_t)hh * kHeadDim,
-                                     S.qrot + hh * kHeadDim, j, pos, p.rope_mode, p.rope_w[j],
-                                     p.q_scale))
-              set_status(p.ctl, MAC_DEV_NONFINITE_Q);
-          }
-          consumer_sync();
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-            for (int c = 0; c < kNP; ++c)
-#pragma unroll
-              for (int e4 = 0; e4 < kPer; e4 += 4) {
-                const float4 v =
-                    *reinterpret_cast<const float4 *>(S.qrot + hh * kHeadDim + piece_dim(c, sub) + e4);
-                q[hh][(c * kPer + e4) / 2] = make_float2(v.x, v.y);
-                q[hh][(c * kPer + e4) / 2 + 1] = make_float2(v.z, v.w);
-              }
-        }
-        const uint8_t *kb = S.stage + (size_t)st * kStageBytes;
-        const uint8_t *vb = kb + kStageBytes / 2;
-        const int t0 = (int)((tile0 + k) * kTileTok);
-        const int msk = S.mask[st];
-        float sc[kTokPerGroup][G];
-        bool tv[kTokPerGroup];
-#pragma unroll
-        for (int j = 0; j < kTokPerGroup; ++j) {
-          const int row = j * 32 + warp * 4 + lg;
-          const int t = t0 + row + 1;
-          tv[j] = ok && t >= lo && t <= hi && ((msk >> (row >> 4)) & 1);
-          float2 kf[kPairs];
-#pragma unroll
-          for (int c = 0; c < kNP; ++c)
-            unpack16x2<T>(*reinterpret_cast<const uint4 *>(kb + row * kRowBytes + c * 128 + sub * 16),
-                          kf + c * (kPer / 2));
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < kPairs; ++i) acc = __ffma2_rn(q[hh][i], kf[i], acc);
-            float a = acc.x + acc.y;
-            a += __shfl_xor_sync(0xffffffffu, a, 1);
-            a += __shfl_xor_sync(0xffffffffu, a, 2);
-            a += __shfl_xor_sync(0xffffffffu, a, 4);
-            sc[j][hh] = a;
-          }
-        }
-        // one rescale per head per tile, then accumulate the tile's tokens
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          float mx = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < kTokPerGroup; ++j) {
-            const int t = t0 + j * 32 + warp * 4 + lg + 1;
-            if (tv[j] && t >= lo_h[hh]) mx = fmaxf(mx, sc[j][hh]);
-          }
-          if (mx > mrun[hh]) {
-            const float f = ex2(mrun[hh] - mx);
-            const float2 f2 = make_float2(f, f);
-            lrun[hh] *= f;
-#pragma unroll
-            for (int i = 0; i < kPairs; ++i) o[hh][i] = __fmul2_rn(o[hh][i], f2);
-            mrun[hh] = mx;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kTokPerGroup; ++j) {
-          const int row = j * 32 + warp * 4 + lg;
-          const int t = t0 + row + 1;
-          float2 vf[kPairs];
-#pragma unroll
-          for (int c = 0; c < kNP; ++c)
-            unpack16x2<T>(*reinterpret_cast<const uint4 *>(vb + row * kRowBytes + c * 128 + sub * 16),
-                          vf + c * (kPer / 2));
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            if (tv[j] && t >= lo_h[hh]) {
-              const float w = ex2(sc[j][hh] - mrun[hh]);
-              const float2 w2 = make_float2(w, w);
-              lrun[hh] += w;
-#pragma unroll
-              for (int i = 0; i < kPairs; ++i) o[hh][i] = __ffma2_rn(w2, vf[i], o[hh][i]);
-            }
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&S.empty[st]));
-        if (ct == 0) pump(p, S, pr);
-        ++tc;
+  // Decisions of every head from the combined minima, then every unit's band
+  // start and the band layout (every CTA computes the same).
+  __device__ static void decide(const StepParams &p, const Smem &S) {
+    const int tid = threadIdx.x, n_bh = p.B * p.Hq, U = p.B * p.Hkv;
+    for (int bh = tid; bh < n_bh; bh += kThreads) {
+      const int b = bh / p.Hq, u = b * p.Hkv + (bh % p.Hq) / G;
+      const int64_t m = unit_len(p, S, u);
+      const unsigned long long inv = __ldcg(&p.best[bh]);
+      int pos = -1;
+      if (inv != 0ull && len_ok(p, m) && m >= p.min_context) {
+        const unsigned long long key = ~inv;
+        const float d = __uint_as_float((uint32_t)(key >> 32));
+        if (d < p.thr2) pos = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
       }
+      S.X[bh] = pos;
+      if (blockIdx.x == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
     }
-
-    // combine the 4 token groups of the warp (lanes differing in bits 3, 4)
-#pragma unroll
-    for (int off = 8; off <= 16; off <<= 1) {
-#pragma unroll
+    __syncthreads();
+    for (int u = tid; u < U; u += kThreads) {
+      const int b = u / p.Hkv, g = u % p.Hkv;
+      int s = 0x7fffffff;
       for (int hh = 0; hh < G; ++hh) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, mrun[hh], off);
-        const float l2 = __shfl_xor_sync(0xffffffffu, lrun[hh], off);
-        const float mn = fmaxf(mrun[hh], m2);
-        const float a = lrun[hh] > 0.f ? ex2(mrun[hh] - mn) : 0.f;
-        const float c2 = l2 > 0.f ? ex2(m2 - mn) : 0.f;
-        lrun[hh] = lrun[hh] * a + l2 * c2;
-        const float2 a2 = make_float2(a, a), cc = make_float2(c2, c2);
-#pragma unroll
-        for (int i = 0; i < kPairs; ++i) {
-          const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, o[hh][i].x, off),
-                                           __shfl_xor_sync(0xffffffffu, o[hh][i].y, off));
-          o[hh][i] = __ffma2_rn(other, cc, __fmul2_rn(o[hh][i], a2));
-        }
-        mrun[hh] = lrun[hh] > 0.f ? mn : -INFINITY;
+        const int pp = S.X[b * p.Hq + g * G + hh];
+        const int lo = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
+        s = lo < s ? lo : s;
       }
+      S.u_s[u] = s;
     }
-    if (lg == 0) {
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float *rw = S.red + ((size_t)warp * G + hh) * kPartStride;
-#pragma unroll
-        for (int c = 0; c < kNP; ++c)
-#pragma unroll
-          for (int e = 0; e < kPer; e += 2) {
-            const float2 v = o[hh][(c * kPer + e) / 2];
-            rw[piece_dim(c, sub) + e] = v.x;
-            rw[piece_dim(c, sub) + e + 1] = v.y;
-          }
-        if (sub == 0) {
-          rw[kHeadDim] = mrun[hh];
-          rw[kHeadDim + 1] = lrun[hh];
-        }
-      }
-    }
-    consumer_sync();
-    // the warps in a fixed order -> the chunk's partial
-    for (int idx = ct; idx < G * kHeadDim; idx += kThreads) {
-      const int hh = idx / kHeadDim, dim = idx % kHeadDim;
-      float M = -INFINITY, L = 0.f, O = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float *rw = S.red + ((size_t)w * G + hh) * kPartStride;
-        const float m2 = rw[kHeadDim], l2 = rw[kHeadDim + 1], o2 = rw[dim];
-        if (l2 == 0.f) continue;
-        if (L == 0.f) {
-          M = m2;
-          L = l2;
-          O = o2;
-          continue;
-        }
-        const float mn = fmaxf(M, m2);
-        const float a = ex2(M - mn), c2 = ex2(m2 - mn);
-        L = L * a + l2 * c2;
-        O = O * a + o2 * c2;
-        M = mn;
-      }
-      float *out = dst + (size_t)hh * kPartStride;
-      out[dim] = O;
-      if (dim == 0) {
-        out[kHeadDim] = M;
-        out[kHeadDim + 1] = L;
-      }
-    }
-    consumer_sync();  // S.red is rewritten by the next chunk
+    __syncthreads();
+    layout_phase(p, S, 1);
   }
 
   // ---------------------------------------------------------------------
-  // layout of the band chunks (after the match)
+  // phases A and B: attention over the CTA's pieces
   // ---------------------------------------------------------------------
 
-  // Cache every unit's fresh-range start and every head's first fresh token
-  // in shared memory, then lay the band chunks out: prefix[u] = first band
-  // chunk of unit u, prefix[n_units] = total.
-  __device__ static void build_prefix(const StepParams &p, const Smem &S, int n_units) {
-    __shared__ int wsum[kWarps];
-    int32_t *prefix = S.prefix;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int bh = tid; bh < p.B * p.Hq; bh += kThreads)
-      S.pos[bh] = p.mode == MODE_DECODE ? __ldcg(&p.head_info[bh]).y : 1;
-    const int seg = (n_units + kThreads - 1) / kThreads;
-    const int beg = tid * seg;
-    const int end = min(beg + seg, n_units);
-    for (int u = beg; u < end; ++u) S.u_s[u] = p.mode == MODE_DECODE ? __ldcg(&p.unit_s[u]) : 1;
-    int run = 0;
-    for (int u = beg; u < end; ++u) {
-      run += plan(p, S, u).nb;
-      prefix[u + 1] = run;
+  // R(pos) q~ * log2(e)/sqrt(d) for the piece's heads, from the query rows
+  // that came with its first tile; every lane then loads its 16 dims.
+  __device__ static void rotate_query(const StepParams &p, const Smem &S, int st, int64_t pos,
+                                      float2 (&q)[G][kPairs]) {
+    const int tid = threadIdx.x, sub = tid & 7;
+    const int half = kHeadDim / 2;
+    if (tid < half) {
+      float c = 1.f, s = 0.f;
+      if (p.rope_mode != MAC_ROPE_NONE) rope_angle(pos, p.rope_w[tid], &c, &s);
+      S.ang[tid] = make_float2(c, s);
     }
-    int x = run;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
-    }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-      int w = lane < kWarps ? wsum[lane] : 0;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, w, off);
-        if (lane >= off) w += y;
+    consumer_sync();
+    const bool inter = p.rope_mode == MAC_ROPE_INTERLEAVED;
+    for (int i = tid; i < G * half; i += kThreads) {
+      const int hh = i / half, j = i % half;
+      const int ia = inter ? 2 * j : j, ib = inter ? 2 * j + 1 : j + half;
+      const void *row = S.qbuf + (size_t)st * kQBytes + hh * kRowBytes;
+      const float a = elem_f32<T>(row, ia), b = elem_f32<T>(row, ib);
+      float ra = a, rb = b;
+      if (p.rope_mode != MAC_ROPE_NONE) {
+        const float2 cs = S.ang[j];
+        ra = __fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y));
+        rb = __fadd_rn(__fmul_rn(b, cs.x), __fmul_rn(a, cs.y));
       }
-      if (lane < kWarps) wsum[lane] = w;
+      S.qrot[hh * kHeadDim + ia] = __fmul_rn(ra, p.q_scale);
+      S.qrot[hh * kHeadDim + ib] = __fmul_rn(rb, p.q_scale);
+      if (!(isfinite(a) && isfinite(b))) set_status(p.ctl, MAC_DEV_NONFINITE_Q);
     }
-    __syncthreads();
-    const int excl = x - run + (warp > 0 ? wsum[warp - 1] : 0);
-    for (int u = beg; u < end; ++u) prefix[u + 1] += excl;
-    if (tid == 0) prefix[0] = 0;
-    __syncthreads();
+    consumer_sync();
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+      for (int c = 0; c < kNP; ++c)
+#pragma unroll
+        for (int e4 = 0; e4 < kPer; e4 += 4) {
+          const float4 v = *reinterpret_cast<const float4 *>(S.qrot + hh * kHeadDim + piece_dim(c, sub) + e4);
+          q[hh][(c * kPer + e4) / 2] = make_float2(v.x, v.y);
+          q[hh][(c * kPer + e4) / 2 + 1] = make_float2(v.z, v.w);
+        }
+  }
+
+  // v[i] (i = token slot * G + head, partial dot products of the lane's 16
+  // dims) -> the full dot product of slot sub >> kPlain: reduce-scatter over
+  // the group's lanes (xor 4, 2, 1), then plain butterflies for the rest.
+  __device__ static float reduce_scores(float (&v)[kV], int lane) {
+#pragma unroll
+    for (int lev = 0; lev < kScat; ++lev) {
+      const int off = 4 >> lev;
+      const bool up = (lane & off) != 0;
+      constexpr int kMax = kV;
+      const int half = kMax >> (lev + 1);
+#pragma unroll
+      for (int i = 0; i < kMax / 2; ++i) {
+        if (i < half) {
+          const float send = up ? v[i] : v[i + half];
+          const float keep = up ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(kFull, send, off);
+        }
+      }
+    }
+    float s = v[0];
+#pragma unroll
+    for (int lev = kScat; lev < 3; ++lev) s += __shfl_xor_sync(kFull, s, 4 >> lev);
+    return s;
+  }
+
+  // One piece: tokens [pc.lo, pc.hi] of unit pc.u for its G heads; the
+  // piece's partial summary goes to dst ([G][kPartStride]).
+  __device__ static void attend_piece(const StepParams &p, const Smem &S, uint32_t &n, int ph,
+                                      const Piece &pc, float *dst) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = lane >> 3, sub = lane & 7;
+    const int b = pc.u / p.Hkv, g = pc.u % p.Hkv;
+    const int idx = sub >> kPlain;         // this lane's score slot
+    const int ti = idx / G, hm = idx % G;  // its token (within the group's tile share) and head
+    int lo_mine = pc.lo;                   // first token of the lane's head in this piece
+    if (ph == 1 && p.mode == MODE_DECODE) {
+      const int pp = S.X[b * p.Hq + g * G + hm];
+      const int lh = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
+      lo_mine = lh > lo_mine ? lh : lo_mine;
+    }
+    float2 q[G][kPairs], o[G][kPairs];
+    float mrun[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      mrun[hh] = kMInit;
+#pragma unroll
+      for (int i = 0; i < kPairs; ++i) o[hh][i] = make_float2(0.f, 0.f);
+    }
+    float m_mine = kMInit, l_mine = 0.f;
+
+    const int64_t tile0 = (pc.lo - 1) / kTileTok;
+    const int ntiles = (int)((pc.hi - 1) / kTileTok - tile0 + 1);
+    for (int k = 0; k < ntiles; ++k, ++n) {
+      const int st = n % kStages;
+      const bool ok = wait_use(S, n);
+      if (k == 0) rotate_query(p, S, st, S.u_pos[pc.u], q);
+      const uint8_t *kb = S.stage + (size_t)st * kStageBytes;
+      const uint8_t *vb = kb + kStageBytes / 2;
+      const int t0 = (int)((tile0 + k) * kTileTok);
+      // partial scores of the group's kTPG tokens for the G heads
+      float v[kV];
+#pragma unroll
+      for (int tt = 0; tt < kTPG; ++tt) {
+        const int row = tt * 32 + warp * 4 + lg;
+        float2 kf[kPairs];
+#pragma unroll
+        for (int c = 0; c < kNP; ++c)
+          unpack16x2<T>(*reinterpret_cast<const uint4 *>(kb + row * kRowBytes + c * 128 + sub * 16),
+                        kf + c * (kPer / 2));
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          float2 acc = __fmul2_rn(q[hh][0], kf[0]);
+#pragma unroll
+          for (int i = 1; i < kPairs; ++i) acc = __ffma2_rn(q[hh][i], kf[i], acc);
+          v[tt * G + hh] = acc.x + acc.y;
+        }
+      }
+      float s = reduce_scores(v, lane);
+      const int row_m = ti * 32 + warp * 4 + lg;
+      const int t_m = t0 + row_m + 1;
+      const bool valid = ok && t_m >= lo_mine && t_m <= pc.hi && ((S.mask[st] >> (row_m >> 4)) & 1);
+      s = valid ? s : -INFINITY;
+      // lazy running max (per group and head): raised only when a score
+      // exceeds it by kLazy
+      float mt = s;
+      if (kTPG == 2) mt = fmaxf(mt, __shfl_xor_sync(kFull, s, 4));
+      if (__any_sync(kFull, mt > m_mine + kLazy)) {
+        const float mn_mine = fmaxf(m_mine, mt);
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float mn = __shfl_sync(kFull, mn_mine, (lane & 24) | (hh << kPlain));
+          const float f = ex2(mrun[hh] - mn);
+          const float2 f2 = make_float2(f, f);
+#pragma unroll
+          for (int i = 0; i < kPairs; ++i) o[hh][i] = __fmul2_rn(o[hh][i], f2);
+          mrun[hh] = mn;
+        }
+        l_mine *= ex2(m_mine - mn_mine);
+        m_mine = mn_mine;
+      }
+      const float w = ex2(s - m_mine);
+      l_mine += w;
+      float wa[kV];
+#pragma unroll
+      for (int i = 0; i < kV; ++i) wa[i] = __shfl_sync(kFull, w, (lane & 24) | (i << kPlain));
+      // rows the piece did not copy hold stale bytes, possibly NaN patterns,
+      // and 0 * NaN is NaN: in a partly covered tile they are zeroed
+      const int msk = S.mask[st];
+      const bool whole = t0 + 1 >= pc.lo && t0 + kTileTok <= pc.hi && msk == (1 << (kTileTok / 16)) - 1;
+#pragma unroll
+      for (int tt = 0; tt < kTPG; ++tt) {
+        const int row = tt * 32 + warp * 4 + lg;
+        uint4 raw[kNP];
+#pragma unroll
+        for (int c = 0; c < kNP; ++c) raw[c] = *reinterpret_cast<const uint4 *>(vb + row * kRowBytes + c * 128 + sub * 16);
+        if (!whole) {
+          const int t = t0 + row + 1;
+          const uint32_t vm = (t >= pc.lo && t <= pc.hi && ((msk >> (row >> 4)) & 1)) ? ~0u : 0u;
+#pragma unroll
+          for (int c = 0; c < kNP; ++c) raw[c] = make_uint4(raw[c].x & vm, raw[c].y & vm, raw[c].z & vm, raw[c].w & vm);
+        }
+        float2 vf[kPairs];
+#pragma unroll
+        for (int c = 0; c < kNP; ++c) unpack16x2<T>(raw[c], vf + c * (kPer / 2));
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float2 w2 = make_float2(wa[tt * G + hh], wa[tt * G + hh]);
+#pragma unroll
+          for (int i = 0; i < kPairs; ++i) o[hh][i] = __ffma2_rn(w2, vf[i], o[hh][i]);
+        }
+      }
+      release(p, S, n);
+    }
+    epilogue(p, S, o, mrun, m_mine, l_mine, dst);
+  }
+
+  // The CTA's 32 lane-group states -> one partial summary per head: common
+  // maximum, every group rescaled to it, then summed in a fixed order
+  // through shared memory.
+  __device__ static void epilogue(const StepParams &p, const Smem &S, float2 (&o)[G][kPairs],
+                                  const float (&mrun)[G], float m_mine, float l_mine, float *dst) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = lane >> 3, sub = lane & 7;
+    const int idx = sub >> kPlain, ti = idx / G, hm = idx % G;
+    float l_grp = l_mine;  // the group's sum for head hm (both token slots)
+    if (kTPG == 2) l_grp += __shfl_xor_sync(kFull, l_mine, 4);
+    float mw[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      mw[hh] = fmaxf(mrun[hh], __shfl_xor_sync(kFull, mrun[hh], 8));
+      mw[hh] = fmaxf(mw[hh], __shfl_xor_sync(kFull, mw[hh], 16));
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) S.red_m[warp * G + hh] = mw[hh];
+    consumer_sync();
+    float mc[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      mc[hh] = S.red_m[hh];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) mc[hh] = fmaxf(mc[hh], S.red_m[w * G + hh]);
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      const float f = ex2(mrun[hh] - mc[hh]);
+      const float2 f2 = make_float2(f, f);
+#pragma unroll
+      for (int i = 0; i < kPairs; ++i) o[hh][i] = __fmul2_rn(o[hh][i], f2);
+    }
+    if (ti == 0 && (sub & ((1 << kPlain) - 1)) == 0) {
+      float mcm = mc[0];
+#pragma unroll
+      for (int hh = 1; hh < G; ++hh) mcm = hm == hh ? mc[hh] : mcm;
+      S.red_l[(warp * 4 + lg) * G + hm] = l_grp * ex2(m_mine - mcm);
+    }
+    float acc[kOutPer];
+#pragma unroll
+    for (int j = 0; j < kOutPer; ++j) acc[j] = 0.f;
+#pragma unroll
+    for (int rd = 0; rd < 4 / kRedGroups; ++rd) {
+      if (lg / kRedGroups == rd) {
+        float *wr = S.red_o + (size_t)(warp * kRedGroups + lg % kRedGroups) * G * kHeadDim;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+          for (int c = 0; c < kNP; ++c)
+#pragma unroll
+            for (int e4 = 0; e4 < kPer; e4 += 4) {
+              const float2 a = o[hh][(c * kPer + e4) / 2], bb = o[hh][(c * kPer + e4) / 2 + 1];
+              *reinterpret_cast<float4 *>(wr + hh * kHeadDim + piece_dim(c, sub) + e4) =
+                  make_float4(a.x, a.y, bb.x, bb.y);
+            }
+      }
+      consumer_sync();
+#pragma unroll
+      for (int j = 0; j < kOutPer; ++j) {
+        const int e = tid + j * kThreads;
+        if (e < G * kHeadDim) {
+#pragma unroll 4
+          for (int w2 = 0; w2 < kWarps * kRedGroups; ++w2) acc[j] += S.red_o[(size_t)w2 * G * kHeadDim + e];
+        }
+      }
+      consumer_sync();
+    }
+#pragma unroll
+    for (int j = 0; j < kOutPer; ++j) {
+      const int e = tid + j * kThreads;
+      if (e < G * kHeadDim) dst[(e / kHeadDim) * kPartStride + e % kHeadDim] = acc[j];
+    }
+    if (tid < G) {
+      float L = 0.f;
+      for (int gi = 0; gi < kWarps * 4; ++gi) L += S.red_l[gi * G + tid];
+      dst[tid * kPartStride + kHeadDim] = mc[tid];
+      dst[tid * kPartStride + kHeadDim + 1] = L;
+    }
+  }
+
+  __device__ static void attend_phase(const StepParams &p, const Smem &S, uint32_t &n, int ph) {
+    const int U = p.B * p.Hkv, P = gridDim.x;
+    const int64_t *off = offs(S, ph);
+    const int64_t g0 = span_beg(off, U, blockIdx.x, P), g1 = span_beg(off, U, blockIdx.x + 1, P);
+    if (g0 >= g1) return;
+    float *part = ph ? p.part_b : p.part_a;
+    Piece pc;
+    int u = unit_of(off, U, g0);
+    while (find_piece(p, S, ph, u, g0, g1, &pc)) {
+      attend_piece(p, S, n, ph, pc, part + (size_t)(pc.u + blockIdx.x) * G * kPartStride);
+      u = pc.u + 1;
+    }
   }
 
   // ---------------------------------------------------------------------
@@ -815,23 +977,38 @@ struct Step {
     M = mn;
   }
 
+  // CTAs whose spans meet unit u's segment in phase ph: [*c0, *c1] (empty
+  // when *c1 < *c0).
+  __device__ static void seg_ctas(const Smem &S, int ph, int U, int u, int *c0, int *c1) {
+    const int64_t *off = offs(S, ph);
+    const int P = gridDim.x;
+    if (off[u + 1] <= off[u]) {
+      *c0 = 0;
+      *c1 = -1;
+      return;
+    }
+    *c0 = cta_of(off[u], off[U], P);
+    *c1 = cta_of(off[u + 1] - 1, off[U], P);
+  }
+
   // For each (request, head) -- one per CTA at a time -- merge the unit's
-  // chunk partials in order: band chunks, then tail chunks.  The 8 warps
-  // each take a contiguous segment of that list (lane l owns dims 4l..4l+3)
-  // and keep two running states, band and tail.  Warp 0 then merges, in
-  // order: the cached summary of a hit head, the band states of warps 0..7
-  // (giving AS_{1:m-r}), and the tail states (giving the output).
+  // pieces in order: band pieces, then tail pieces.  The 8 warps each take a
+  // contiguous segment of that list (lane l owns dims 4l..4l+3) and keep two
+  // running states, band and tail.  Warp 0 then merges, in order: the cached
+  // summary of a hit head, the band states of warps 0..7 (giving
+  // AS_{1:m-r}), and the tail states (giving the output).
   __device__ static void reduce_phase(const StepParams &p, const Smem &S) {
     constexpr int kSeg = kHeadDim + 4;                // m, l, -, -, o[d]
     float *seg = reinterpret_cast<float *>(S.stage);  // [kWarps][2][kSeg]; the stages are idle now
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n_bh = p.B * p.Hq;
+    const int n_bh = p.B * p.Hq, U = p.B * p.Hkv, P = gridDim.x;
     for (int bh = blockIdx.x; bh < n_bh; bh += gridDim.x) {
       const int b = bh / p.Hq, h = bh % p.Hq, g = h / G, hh = h % G;
       const int u = b * p.Hkv + g;
-      const int first = S.prefix[u];
-      const int nb = S.prefix[u + 1] - first;
-      const int n = nb + p.n_tail;
+      int cb0, cb1, ca0, ca1;
+      seg_ctas(S, 1, U, u, &cb0, &cb1);
+      seg_ctas(S, 0, U, u, &ca0, &ca1);
+      const int nb = cb1 - cb0 + 1, n = nb + (ca1 - ca0 + 1);
       if (p.mode == MODE_DECODE && warp == kWarps - 1 && lane < kHeadDim / kPer) {
         // the append (on the aux stream) reads the step's query from the ring
         // workspace, so the caller may reuse its query buffer right away
@@ -846,17 +1023,22 @@ struct Step {
         float pm[4], pl[4], po[4][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (i + j < i1) {
-            const int it = i + j;
-            const float *pp = it < nb ? p.partials + ((int64_t)(first + it) * G + hh) * kPartStride
-                                      : p.tail_part + (((int64_t)u * p.n_tail + (it - nb)) * G + hh) * kPartStride;
-            pm[j] = __ldcg(pp + kHeadDim);
-            pl[j] = __ldcg(pp + kHeadDim + 1);
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp) + lane);
-            po[j][0] = v.x;
-            po[j][1] = v.y;
-            po[j][2] = v.z;
-            po[j][3] = v.w;
+          pl[j] = 0.f;
+          const int it = i + j;
+          if (it < i1) {
+            const int ph = it < nb ? 1 : 0;
+            const int c = it < nb ? cb0 + it : ca0 + (it - nb);
+            const int64_t *off = offs(S, ph);
+            if (span_beg(off, U, c, P) < span_beg(off, U, c + 1, P)) {
+              const float *pp = (ph ? p.part_b : p.part_a) + ((int64_t)(u + c) * G + hh) * kPartStride;
+              pm[j] = __ldcg(pp + kHeadDim);
+              pl[j] = __ldcg(pp + kHeadDim + 1);
+              const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp) + lane);
+              po[j][0] = v.x;
+              po[j][1] = v.y;
+              po[j][2] = v.z;
+              po[j][3] = v.w;
+            }
           }
         }
 #pragma unroll
@@ -881,9 +1063,9 @@ struct Step {
       if (warp == 0) {
         float M = -INFINITY, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
         if (p.mode == MODE_DECODE) {
-          const int2 hi = __ldcg(&p.head_info[bh]);
-          if (hi.x >= 1) {
-            const int64_t slot = (int64_t)bh * p.K + hi.x % p.K;
+          const int pos = S.X[bh];
+          if (pos >= 1) {
+            const int64_t slot = (int64_t)bh * p.K + pos % p.K;
             const float lse = p.ring_lse[slot];
             if (lse > -INFINITY) {
               const float4 v = reinterpret_cast<const float4 *>(p.ring_o + slot * kHeadDim)[lane];
@@ -891,6 +1073,7 @@ struct Step {
               merge4(M, L, O, lse * kLog2e, 1.f, a);
             }
           }
+          if (lane == 0) p.best[bh] = 0ull;  // every CTA read it before the barrier
         }
         for (int w = 0; w < kWarps; ++w) {
           const float *s = seg + (size_t)w * 2 * kSeg;
@@ -920,21 +1103,30 @@ struct Step {
   __device__ static void run(const StepParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_mask[kStages];
+    __shared__ uint32_t s_cnt[kStages];
     __shared__ int s_abort;
-    const int n_units = p.B * p.Hkv;
+    __shared__ Cursor s_cur;
+    const int n_units = p.B * p.Hkv, n_heads = p.B * p.Hq;
     Smem S;
     S.stage = smem;
     S.qbuf = smem + kOffQ;
     S.full = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    S.empty = S.full + kStages;
+    S.ang = reinterpret_cast<float2 *>(smem + kOffAng);
     S.qrot = reinterpret_cast<float *>(smem + kOffQrot);
-    S.red = reinterpret_cast<float *>(smem + kOffRed);
-    S.pos = reinterpret_cast<int32_t *>(smem + kOffPos);
-    S.prefix = reinterpret_cast<int32_t *>(smem + kOffUnits);
-    S.u_pos = S.prefix + (n_units + 1);
+    S.red_o = reinterpret_cast<float *>(smem + kOffRedO);
+    S.red_l = reinterpret_cast<float *>(smem + kOffRedL);
+    S.red_m = reinterpret_cast<float *>(smem + kOffRedM);
+    S.X = reinterpret_cast<int32_t *>(smem + kOffX);
+    S.nx = x_ints(n_heads, p.K);
+    S.offA = reinterpret_cast<int64_t *>(smem + off_units(n_heads, p.K));
+    S.offB = S.offA + (n_units + 1);
+    S.u_pos = reinterpret_cast<int32_t *>(S.offB + (n_units + 1));
     S.u_s = S.u_pos + n_units;
+    S.cnt = s_cnt;
     S.mask = s_mask;
     S.abort = &s_abort;
+    S.cur = &s_cur;
+    const bool decode = p.mode == MODE_DECODE;
 
     const int tid = threadIdx.x;
     unsigned long long *trace = p.trace ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
@@ -942,65 +1134,72 @@ struct Step {
     if (tid == 0) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(smem_addr(&S.full[i]), 1);
-        mbar_init(smem_addr(&S.empty[i]), kWarps);
+        s_cnt[i] = 0;
       }
       s_abort = 0;
       mbar_fence_init();
     }
-    for (int u = tid; u < n_units; u += kThreads)
+    for (int u = tid; u < n_units; u += kThreads) {
       S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
+      S.u_s[u] = 1;
+      if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
+        set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
+    }
     __syncthreads();
+    layout_phase(p, S, 0);
+    if (!decode) layout_phase(p, S, 1);
 
-    uint32_t tc = 0;  // stage uses consumed so far (every thread counts the same sequence)
-    Producer pr;      // meaningful in thread 0 only
     if (tid == 0) {
-      const int64_t N = (int64_t)p.B * p.Hq * p.K;
-      pr.n = 0;
-      pr.phase = p.mode == MODE_DECODE ? P_MATCH : P_TAIL;
-      pr.r = (int64_t)blockIdx.x * N / gridDim.x;
-      pr.s1 = p.mode == MODE_DECODE ? (int64_t)(blockIdx.x + 1) * N / gridDim.x : pr.r;
-      pr.item = -1;
-      pr.total = n_units * p.n_tail;
-      pr.k = pr.ntiles = 0;
-      pump(p, S, pr);
+      Cursor &c = s_cur;
+      c.n = 0;
+      c.n_copied = 0;
+      c.cont = !decode;
+      if (decode) {
+        const int64_t N = (int64_t)p.B * p.Hq * p.K;
+        c.kind = C_MATCH;
+        c.r = (int64_t)blockIdx.x * N / gridDim.x;
+        c.s1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
+        if (c.r >= c.s1) cursor_phase(p, S, c, 0);
+      } else {
+        cursor_phase(p, S, c, 0);
+      }
+      for (int i = 0; i < kStages && c.kind != C_END; ++i) issue_current(p, S);
     }
 
-    if (p.mode == MODE_DECODE) match_phase(p, S, tc, pr);
+    uint32_t n = 0;  // stage uses consumed so far (every thread counts the same sequence)
+    if (decode) match_phase(p, S, n);
     if (trace && tid == 0) trace[1] = globaltimer();
-    // tail chunks: independent of the match
-    const int all1[4] = {1, 1, 1, 1};
-    for (int ti = blockIdx.x; ti < n_units * p.n_tail; ti += gridDim.x) {
-      int u, lo, hi;
-      tail_item(p, S, ti, &u, &lo, &hi);
-      process_chunk(p, S, tc, pr, u, lo, hi, all1,
-                    p.tail_part + (size_t)ti * G * kPartStride);
-    }
+    attend_phase(p, S, n, 0);
     __syncthreads();
     if (trace && tid == 0) trace[2] = globaltimer();
-    if (p.mode == MODE_DECODE) grid_barrier(p, S);  // decisions and unit starts are visible
+    if (decode) {
+      grid_barrier(p, S);  // the minima of every head are final
+      decide(p, S);
+      if (tid == 0) {
+        Cursor &c = s_cur;
+        c.n = n;
+        c.cont = 0;
+        cursor_phase(p, S, c, 1);
+        for (int i = 0; i < kStages && c.kind != C_END; ++i) issue_current(p, S);
+      }
+    }
     if (trace && tid == 0) trace[3] = globaltimer();
-
-    build_prefix(p, S, n_units);
-    const int total = S.prefix[n_units];
-    if (tid == 0) {
-      pr.phase = P_BAND;
-      pr.item = -1;
-      pr.total = total;
-      pr.k = pr.ntiles = 0;
-      pump(p, S, pr);
-    }
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-      int u, lo, hi;
-      band_item(p, S, item, &u, &lo, &hi);
-      const int b = u / p.Hkv, g = u % p.Hkv;
-      int lo_h[G];
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) lo_h[hh] = S.pos[b * p.Hq + g * G + hh];
-      process_chunk(p, S, tc, pr, u, lo, hi, lo_h, p.partials + (size_t)item * G * kPartStride);
-    }
+    attend_phase(p, S, n, 1);
     __syncthreads();
     if (trace && tid == 0) trace[4] = globaltimer();
-    grid_barrier(p, S);  // every chunk partial is written
+    if (*S.abort && tid == 0) {
+      // Copies still in flight into the stages: let them land (bounded).  A
+      // use was refilled with a copy only after every warp had waited for it
+      // successfully, so only the last kStages copied uses can be pending.
+      const uint32_t nc = s_cur.n_copied;
+      for (uint32_t j = nc > (uint32_t)kStages ? nc - kStages : 0u; j < nc; ++j) {
+        const uint32_t bar = smem_addr(&S.full[j % kStages]);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, (j / kStages) & 1u) && clock64() - t0 < (1LL << 30)) {
+        }
+      }
+    }
+    grid_barrier(p, S);  // every piece partial is written
     if (trace && tid == 0) trace[5] = globaltimer();
     reduce_phase(p, S);
     if (trace && tid == 0) trace[6] = globaltimer();

@@ -8,26 +8,36 @@
 namespace mac {
 
 template <typename T, int G, bool PAGED>
-static cudaError_t prepare_step(int n_units, size_t *smem) {
+static cudaError_t prepare_step(int n_heads, int n_units, int K, size_t *smem) {
   using S = Step<T, G, PAGED>;
-  *smem = S::smem_bytes(n_units);
-  static size_t configured[64] = {0};  // per device: dynamic shared memory limit already set
+  *smem = S::smem_bytes(n_heads, n_units, K);
+  static size_t limit[64] = {0};  // per device: dynamic shared memory limit set on the kernel
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && configured[dev] >= *smem) return cudaSuccess;
-  e = cudaFuncSetAttribute(step_kernel<T, G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)S::smem_bytes(kMaxUnits));
-  if (e == cudaSuccess && dev < 64) configured[dev] = S::smem_bytes(kMaxUnits);
-  return e;
+  if (dev < 64 && limit[dev] == 0) {
+    // the opt-in maximum per block, less the kernel's static shared memory
+    int optin = 0;
+    cudaFuncAttributes fa;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
+        (e = cudaFuncGetAttributes(&fa, step_kernel<T, G, PAGED>)) != cudaSuccess)
+      return e;
+    size_t dyn = (size_t)optin - fa.sharedSizeBytes;
+    if (dyn > kMaxSmem) dyn = kMaxSmem;
+    e = cudaFuncSetAttribute(step_kernel<T, G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e != cudaSuccess) return e;
+    limit[dev] = dyn;
+  }
+  if (dev < 64 && *smem > limit[dev]) return cudaErrorInvalidValue;
+  return cudaSuccess;
 }
 
 // Cooperative launch: the grid (one CTA per SM) is guaranteed co-resident,
-// which the grid barrier between the match and the attention relies on.
+// which the grid barriers of the step rely on.
 template <typename T, int G, bool PAGED>
 static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) {
   size_t smem = 0;
-  cudaError_t e = prepare_step<T, G, PAGED>(p.B * p.Hkv, &smem);
+  cudaError_t e = prepare_step<T, G, PAGED>(p.B * p.Hq, p.B * p.Hkv, p.K, &smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -43,9 +53,9 @@ static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) 
 }
 
 template <typename T, int G, bool PAGED>
-static int occupancy_g(int n_units) {
+static int occupancy_g(int n_heads, int n_units, int K) {
   size_t smem = 0;
-  if (prepare_step<T, G, PAGED>(n_units, &smem) != cudaSuccess) return 0;
+  if (prepare_step<T, G, PAGED>(n_heads, n_units, K, &smem) != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<T, G, PAGED>, kThreads, smem) !=
       cudaSuccess)
@@ -65,11 +75,11 @@ static cudaError_t launch_step_t(const StepParams &p, int grid, cudaStream_t s) 
 }
 
 template <typename T>
-static int occupancy_t(int G, bool paged, int n_units) {
+static int occupancy_t(int G, bool paged, int n_heads, int n_units, int K) {
   switch (G) {
-    case 1: return paged ? occupancy_g<T, 1, true>(n_units) : occupancy_g<T, 1, false>(n_units);
-    case 2: return paged ? occupancy_g<T, 2, true>(n_units) : occupancy_g<T, 2, false>(n_units);
-    case 4: return paged ? occupancy_g<T, 4, true>(n_units) : occupancy_g<T, 4, false>(n_units);
+    case 1: return paged ? occupancy_g<T, 1, true>(n_heads, n_units, K) : occupancy_g<T, 1, false>(n_heads, n_units, K);
+    case 2: return paged ? occupancy_g<T, 2, true>(n_heads, n_units, K) : occupancy_g<T, 2, false>(n_heads, n_units, K);
+    case 4: return paged ? occupancy_g<T, 4, true>(n_heads, n_units, K) : occupancy_g<T, 4, false>(n_heads, n_units, K);
     default: return 0;
   }
 }
