@@ -48,6 +48,7 @@ extern "C" {
 #define MAC_DEV_BAD_PAGE 0x2       /* page id outside [0, n_pages): its tokens skipped */
 #define MAC_DEV_WAIT_TIMEOUT 0x4   /* a bounded wait on a copy gave up: item skipped */
 #define MAC_DEV_NONFINITE_Q 0x8    /* non-finite query: treated as a miss */
+#define MAC_DEV_BAD_COPY 0x10      /* a copy outside its tile was refused (internal check) */
 
 /* ---- configuration ------------------------------------------------------ */
 enum { MAC_BF16 = 0, MAC_F32 = 1 };

@@ -99,7 +99,9 @@ struct StepParams {
   float *part_a;             // tail pieces
   float *part_b;             // band pieces
   unsigned long long *trace;  // optional: [grid][kTracePoints] %globaltimer stamps
-  double rope_w[kHeadDim / 2];
+  // RoPE frequency j as a 64-bit fixed-point fraction of a turn per
+  // position: round(w_j / (2 pi) * 2^64), w_j = base^(-2j/d)
+  unsigned long long rope_f[kHeadDim / 2];
 };
 
 struct AppendParams {
@@ -213,9 +215,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
-// Barrier of the CTA's consumer threads (all of them).
+// Barrier of the CTA's consumer threads (all of them).  bar.sync counts
+// whole warps, so each warp first reconverges: a lane still inside a
+// single-lane region must not be counted as arrived.
 __device__ __forceinline__ void consumer_sync() {
+  __syncwarp();
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+// __syncthreads() after reconverging the warp (same reason).
+__device__ __forceinline__ void block_sync() {
+  __syncwarp();
+  __syncthreads();
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -236,18 +247,16 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
-// Query rotation for one 2x2 block: angle (pos-1) w computed in fp64 and
-// reduced modulo 2 pi with a two-part constant (Cody-Waite additive
-// reduction), so positions up to 2^31 keep ~1e-7 rad accuracy; the sine and
-// cosine of the reduced angle are taken in fp32.
-__device__ __forceinline__ void rope_angle(int64_t pos, double w, float *c, float *s) {
-  const double kTwoPiHi = 6.283185307179586;      // nearest double to 2 pi
-  const double kTwoPiLo = 2.4492935982947064e-16; // 2 pi - kTwoPiHi
-  double th = (double)(pos - 1) * w;
-  double k = rint(th * (1.0 / 6.283185307179586));
-  double rr = fma(-k, kTwoPiHi, th);
-  rr = fma(-k, kTwoPiLo, rr);
-  sincosf((float)rr, s, c);
+// Query rotation angle of one 2x2 block, (pos-1) w_j modulo 2 pi, from the
+// frequency as a 64-bit fixed-point fraction of a turn (f = w_j / 2pi * 2^64):
+// the product (pos-1) f taken modulo 2^64 is the angle's fraction of a turn,
+// exact up to the rounding of f (relative 2^-53), read as a signed value so
+// the angle lands in [-pi, pi); its sine and cosine are taken in fp32.  All
+// integer and fp32 arithmetic (GB300's fp64 rate is a small fraction of it).
+__device__ __forceinline__ void rope_angle(int64_t pos, unsigned long long f, float *c, float *s) {
+  const unsigned long long turn = (unsigned long long)(pos - 1) * f;
+  const float a = (float)(long long)turn * 3.4061215800865545e-19f;  // 2 pi / 2^64
+  sincosf(a, s, c);
 }
 
 template <typename T>

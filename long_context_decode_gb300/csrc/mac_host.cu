@@ -149,7 +149,8 @@ StepParams step_params(const mac_config *c, const ScratchLayout &S, uint8_t *scr
   a.max_len = max_len(c, a.kv);
   a.q_stride = c->head_dim;
   for (int j = 0; j < kHeadDim / 2; ++j)
-    a.rope_w[j] = pow(c->rope_base, -2.0 * (double)j / (double)c->head_dim);
+    a.rope_f[j] = (unsigned long long)ldexp(
+        pow(c->rope_base, -2.0 * (double)j / (double)c->head_dim) / 6.283185307179586, 64);
   a.ctl = (uint32_t *)(scratch + S.ctl);
   a.best = (unsigned long long *)(scratch + S.best);
   a.part_a = (float *)(scratch + S.part_a);

@@ -90,6 +90,12 @@ __device__ __forceinline__ void unpack16x2<float>(const uint4 &u, float2 *f) {
 
 constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x >> 1); }
 
+// A position in the ring rows of a match slice: head bh (global row
+// bh * K + slot); the slice ends before slot_end of head bh_last.
+struct MatchPos {
+  int bh, slot, bh_last, slot_end;
+};
+
 // Running maxima start here (finite, so that empty states never produce
 // inf - inf) and are raised only when a score exceeds them by kLazy (base-2
 // log units): the accumulators then stay within 2^kLazy of the true scale.
@@ -117,8 +123,7 @@ struct Step {
   // dynamic shared memory layout
   static constexpr size_t kOffQ = (size_t)kStages * kStageBytes;
   static constexpr size_t kOffBar = kOffQ + (size_t)kStages * kQBytes;
-  static constexpr size_t kOffAng = kOffBar + 64;
-  static constexpr size_t kOffQrot = kOffAng + 8 * (kHeadDim / 2);
+  static constexpr size_t kOffQrot = kOffBar + 64;
   static constexpr size_t kOffRedO = kOffQrot + 4 * (size_t)G * kHeadDim;
   static constexpr size_t kOffRedL = kOffRedO + 4 * (size_t)kWarps * kRedGroups * G * kHeadDim;
   static constexpr size_t kOffRedM = kOffRedL + 4 * (size_t)kWarps * 4 * G;
@@ -143,7 +148,9 @@ struct Step {
   // Issue cursor: the next use of the CTA's stage sequence (match chunks,
   // then the tiles of the CTA's pieces).  Only the thread issuing use n
   // touches it, after the issue of use n - 1 has published n.
-  enum { C_MATCH = 0, C_TILES = 1, C_END = 2 };
+  // C_PEND: the tile sequence of phase 0 comes next but its layout may not
+  // be ready yet (resolved by the first issue after the layout).
+  enum { C_MATCH = 0, C_TILES = 1, C_END = 2, C_PEND = 3 };
   struct Cursor {
     uint32_t n;          // next use to issue
     uint32_t n_copied;   // uses issued with their copies (all of them unless aborted)
@@ -151,7 +158,7 @@ struct Step {
     int ph;              // phase of the tile sequence: 0 tails, 1 bands
     int cont;            // go on from phase 0 into phase 1 (full attention)
     int u, lo, hi, first;
-    int64_t r, s1;       // match: next ring row, end of the slice
+    MatchPos mp;         // match: next chunk
     int64_t tile, tile_last;
     int64_t g0, g1;      // span of this CTA in phase ph
   };
@@ -160,7 +167,6 @@ struct Step {
     uint8_t *stage;     // [kStages][kStageBytes]
     uint8_t *qbuf;      // [kStages][G][d]: pre-RoPE query rows of a piece's unit
     uint64_t *full;     // [kStages]
-    float2 *ang;        // [d/2]: cos, sin of the RoPE angles of the current piece
     float *qrot;        // [G][d]
     float *red_o;       // [kWarps][kRedGroups][G][d]
     float *red_l;       // [kWarps * 4][G]
@@ -169,6 +175,8 @@ struct Step {
     int nx;
     int64_t *offA;      // [n_units + 1]: first global index of each unit's tail segment
     int64_t *offB;      // [n_units + 1]: same for the band segments
+    int64_t *spanA;     // [grid + 1]: CTA c's tail span is [spanA[c], spanA[c+1])
+    int64_t *spanB;     // [grid + 1]: same for the bands
     int32_t *u_pos;     // [n_units]: position of the unit's query (RoPE angle pos - 1)
     int32_t *u_s;       // [n_units]: first band token of the unit
     uint32_t *cnt;      // [kStages]: releases of the stage's current use
@@ -211,14 +219,17 @@ struct Step {
   }
 
   __device__ static const int64_t *offs(const Smem &S, int ph) { return ph ? S.offB : S.offA; }
+  __device__ static const int64_t *spans(const Smem &S, int ph) { return ph ? S.spanB : S.spanA; }
 
-  // span [g0, g1) of CTA c: global indices c*T/P .. (c+1)*T/P
-  __device__ static int64_t span_beg(const int64_t *off, int U, int c, int P) {
-    return (int64_t)c * off[U] / P;
-  }
-  // the CTA whose (non-empty) span holds global index x (x < total)
-  __device__ static int cta_of(int64_t x, int64_t total, int P) {
-    return (int)(((x + 1) * (int64_t)P + total - 1) / total) - 1;
+  // the CTA whose (non-empty) span holds global index x (x < total): the
+  // last c with span[c] <= x
+  __device__ static int cta_of(const int64_t *span, int P, int64_t x) {
+    int lo = 0, hi = P - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (span[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
   }
   // unit whose segment holds global index g (g < T)
   __device__ static int unit_of(const int64_t *off, int U, int64_t g) {
@@ -271,7 +282,7 @@ struct Step {
       if (lane >= o) x += y;
     }
     if (lane == 31) wsum[warp] = x;
-    __syncthreads();
+    block_sync();
     if (warp == 0) {
       long long w = lane < kWarps ? wsum[lane] : 0;
 #pragma unroll
@@ -281,11 +292,16 @@ struct Step {
       }
       if (lane < kWarps) wsum[lane] = w;
     }
-    __syncthreads();
+    block_sync();
     const long long excl = x - run + (warp > 0 ? wsum[warp - 1] : 0);
     for (int u = beg; u < end; ++u) off[u + 1] += excl;
     if (tid == 0) off[0] = 0;
-    __syncthreads();
+    block_sync();
+    // span c = global indices [c*total/P, (c+1)*total/P)
+    int64_t *span = ph ? S.spanB : S.spanA;
+    const int64_t total = off[U];
+    for (int c = tid; c <= (int)gridDim.x; c += kThreads) span[c] = (int64_t)c * total / gridDim.x;
+    block_sync();
   }
 
   // ---------------------------------------------------------------------
@@ -297,6 +313,12 @@ struct Step {
   // piece is read; with_q also brings the unit's G pre-RoPE query rows.
   __device__ static void issue_tile(const StepParams &p, const Smem &S, int st, int u, int lo,
                                     int hi, int64_t tile, bool with_q) {
+    if (u < 0 || u >= p.B * p.Hkv) {
+      set_status(p.ctl, MAC_DEV_BAD_COPY);
+      S.mask[st] = 0;
+      mbar_arrive(smem_addr(&S.full[st]));
+      return;
+    }
     const int b = u / p.Hkv, g = u % p.Hkv;
     uint8_t *kbuf = S.stage + (size_t)st * kStageBytes;
     uint8_t *vbuf = kbuf + kStageBytes / 2;
@@ -310,7 +332,16 @@ struct Step {
       msk = (1 << (kTileTok / 16)) - 1;
       ra[0] = t0 + 1 > lo ? t0 + 1 : lo;
       rz[0] = t0 + kTileTok < hi ? t0 + kTileTok : hi;
-      bytes += 2u * (uint32_t)(rz[0] - ra[0] + 1) * kRowBytes;
+      // the schedule only issues tiles that meet [lo, hi] inside the cache;
+      // anything else is refused rather than copied
+      if (ra[0] > rz[0] || ra[0] < 1 || rz[0] > p.kv.capacity || u < 0 || u >= p.B * p.Hkv) {
+        set_status(p.ctl, MAC_DEV_BAD_COPY);
+        msk = 0;
+        with_q = false;
+        bytes = 0;
+      } else {
+        bytes += 2u * (uint32_t)(rz[0] - ra[0] + 1) * kRowBytes;
+      }
     } else {
       for (int pg = 0; pg < kTileTok / 16; ++pg) {
         const int64_t slot = tile * (kTileTok / 16) + pg;
@@ -345,6 +376,7 @@ struct Step {
       }
     }
     if (!PAGED) {
+      if (msk == 0) return;
       const size_t off = (((size_t)b * p.Hkv + g) * (size_t)p.kv.capacity + (size_t)(ra[0] - 1)) * kRowBytes;
       const uint32_t n = (uint32_t)(rz[0] - ra[0] + 1) * kRowBytes;
       const uint32_t dst = (uint32_t)(ra[0] - t0 - 1) * kRowBytes;
@@ -362,13 +394,32 @@ struct Step {
     }
   }
 
-  // next chunk of the match slice: rows [r, e) within one head, <= kMatchRows
-  __device__ static int64_t chunk_end(int64_t r, int64_t s1, int K) {
-    int64_t e = r + kMatchRows;
-    const int64_t head_end = (r / K + 1) * K;
-    if (e > head_end) e = head_end;
-    if (e > s1) e = s1;
-    return e;
+  // Rows of the next match chunk at mp: within one head, at most kMatchRows.
+  __device__ static int match_rows(const MatchPos &mp, int K) {
+    int e = mp.slot + kMatchRows;
+    if (e > K) e = K;
+    if (mp.bh == mp.bh_last && e > mp.slot_end) e = mp.slot_end;
+    return e - mp.slot;
+  }
+  // advance past a chunk of n rows; false when the slice is done
+  __device__ static bool match_next(MatchPos &mp, int n, int K) {
+    mp.slot += n;
+    if (mp.slot >= K) {
+      ++mp.bh;
+      mp.slot = 0;
+    }
+    return mp.bh < mp.bh_last || (mp.bh == mp.bh_last && mp.slot < mp.slot_end);
+  }
+  // CTA c's slice of the B*Hq*K ring rows: [c*N/P, (c+1)*N/P); false if empty
+  __device__ static bool match_slice(const StepParams &p, MatchPos *mp) {
+    const int64_t N = (int64_t)p.B * p.Hq * p.K;
+    const int64_t s0 = (int64_t)blockIdx.x * N / gridDim.x, s1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
+    if (s0 >= s1) return false;
+    mp->bh = (int)(s0 / p.K);
+    mp->slot = (int)(s0 % p.K);
+    mp->bh_last = (int)((s1 - 1) / p.K);
+    mp->slot_end = (int)((s1 - 1) % p.K) + 1;
+    return true;
   }
 
   __device__ static void cursor_piece(Cursor &c, const Piece &pc) {
@@ -384,12 +435,12 @@ struct Step {
   // Put the cursor on the first tile of this CTA's pieces in phase ph (then
   // phase 1 when c.cont), or end it.
   __device__ static void cursor_phase(const StepParams &p, const Smem &S, Cursor &c, int ph) {
-    const int U = p.B * p.Hkv, P = gridDim.x;
+    const int U = p.B * p.Hkv;
     for (;; ++ph) {
       const int64_t *off = offs(S, ph);
       c.ph = ph;
-      c.g0 = span_beg(off, U, blockIdx.x, P);
-      c.g1 = span_beg(off, U, blockIdx.x + 1, P);
+      c.g0 = spans(S, ph)[blockIdx.x];
+      c.g1 = spans(S, ph)[blockIdx.x + 1];
       Piece pc;
       if (c.g0 < c.g1 && find_piece(p, S, ph, unit_of(off, U, c.g0), c.g0, c.g1, &pc)) {
         cursor_piece(c, pc);
@@ -404,8 +455,7 @@ struct Step {
 
   __device__ static void cursor_next(const StepParams &p, const Smem &S, Cursor &c) {
     if (c.kind == C_MATCH) {
-      c.r = chunk_end(c.r, c.s1, p.K);
-      if (c.r >= c.s1) cursor_phase(p, S, c, 0);
+      if (!match_next(c.mp, match_rows(c.mp, p.K), p.K)) c.kind = C_PEND;
       return;
     }
     c.first = 0;
@@ -426,17 +476,24 @@ struct Step {
   // and publish the next use index.
   __device__ static void issue_current(const StepParams &p, const Smem &S) {
     Cursor &c = *S.cur;
+    if (c.kind == C_PEND) {
+      cursor_phase(p, S, c, 0);
+      if (c.kind == C_END) return;
+    }
     const int st = c.n % kStages;
     const bool go = !*S.abort;
     if (c.kind == C_MATCH) {
-      if (go) {
-        const int64_t e = chunk_end(c.r, c.s1, p.K);
-        const uint32_t bytes = (uint32_t)(e - c.r) * kRowBytes;
+      const int rows = match_rows(c.mp, p.K);
+      if (rows < 1 || c.mp.bh >= p.B * p.Hq) {
+        set_status(p.ctl, MAC_DEV_BAD_COPY);
+        mbar_arrive(smem_addr(&S.full[st]));
+      } else if (go) {
+        const uint32_t bytes = (uint32_t)rows * kRowBytes;
         const uint32_t bar = smem_addr(&S.full[st]);
         fence_proxy_async();
         mbar_expect_tx(bar, bytes);
         bulk_g2s(smem_addr(S.stage + (size_t)st * kStageBytes),
-                 (const uint8_t *)p.ring_q + (size_t)c.r * kRowBytes, bytes, bar);
+                 (const uint8_t *)p.ring_q + ((size_t)c.mp.bh * p.K + c.mp.slot) * kRowBytes, bytes, bar);
       }
     } else if (go) {
       issue_tile(p, S, st, c.u, c.lo, c.hi, c.tile, c.first != 0);
@@ -481,9 +538,12 @@ struct Step {
     __syncwarp();
   }
 
-  __device__ static bool wait_use(const Smem &S, uint32_t n) {
+  __device__ static bool wait_use(const StepParams &p, const Smem &S, uint32_t n) {
     const bool ok = mbar_wait_bounded(smem_addr(&S.full[n % kStages]), (n / kStages) & 1u, S.abort);
-    if (!ok) *S.abort = 1;
+    if (!ok && !*S.abort) {
+      set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
+      *S.abort = 1;
+    }
     return ok;
   }
 
@@ -551,41 +611,37 @@ struct Step {
   }
 
   __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n) {
-    const int64_t N = (int64_t)p.B * p.Hq * p.K;
-    const int P = gridDim.x, c = blockIdx.x;
-    const int64_t s0 = (int64_t)c * N / P, s1 = (int64_t)(c + 1) * N / P;
+    MatchPos mp;
+    if (!match_slice(p, &mp)) return;
     const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31, sub = lane & 7;
     const int grp = warp * 4 + (lane >> 3);  // row group: rows grp, grp + 32, ... of a chunk
 
     // slot positions of the requests the slice touches, staged once (they
     // are shared by all heads of a request)
-    const int64_t rows_per_req = (int64_t)p.Hq * p.K;
-    const int b_lo = (int)(s0 / rows_per_req);
-    const int b_hi = s1 > s0 ? (int)((s1 - 1) / rows_per_req) : b_lo - 1;
-    const bool staged = (int64_t)(b_hi - b_lo + 1) * p.K <= S.nx;
+    const int b_lo = mp.bh / p.Hq, b_hi = mp.bh_last / p.Hq;
+    const bool staged = (b_hi - b_lo + 1) * p.K <= S.nx;
     if (staged) {
       const int cnt = (b_hi - b_lo + 1) * p.K;
       const int32_t *src = p.ring_pos + (int64_t)b_lo * p.K;
       for (int i = ct; i < cnt; i += kThreads) S.X[i] = src[i];
     }
-    __syncthreads();
+    block_sync();
 
-    int64_t cur = -1;
+    int cur = -1;
     float bd = INFINITY;
     int bp = -1;
     float2 qv[kPairs];
     int pos_lo = 1, pos_hi = 0;
     const int32_t *rpos = p.ring_pos;
-    for (int64_t r = s0; r < s1; ++n) {
-      const int64_t e = chunk_end(r, s1, p.K);
-      const int64_t bh = r / p.K;
-      const int b = (int)(bh / p.Hq);
-      if (bh != cur) {
+    for (bool more = true; more; ++n) {
+      const int cnt = match_rows(mp, p.K);
+      if (mp.bh != cur) {
         if (cur >= 0) flush_best(p, S, cur, bd, bp);
-        cur = bh;
+        cur = mp.bh;
         bd = INFINITY;
         bp = -1;
-        const uint8_t *qrow = (const uint8_t *)p.q + (size_t)(bh * p.q_stride + p.q_offset) * sizeof(T);
+        const int b = cur / p.Hq;
+        const uint8_t *qrow = (const uint8_t *)p.q + (size_t)((int64_t)cur * p.q_stride + p.q_offset) * sizeof(T);
 #pragma unroll
         for (int cc = 0; cc < kNP; ++cc)
           unpack16x2<T>(*reinterpret_cast<const uint4 *>(qrow + cc * 128 + sub * 16), qv + cc * (kPer / 2));
@@ -597,11 +653,10 @@ struct Step {
           pos_lo = 1;
           pos_hi = 0;
         }
-        rpos = staged ? S.X + (int64_t)(b - b_lo) * p.K : p.ring_pos + (int64_t)b * p.K;
+        rpos = staged ? S.X + (b - b_lo) * p.K : p.ring_pos + (int64_t)b * p.K;
       }
-      const bool ok = wait_use(S, n);
-      const int cnt = (int)(e - r);
-      const int slot0 = (int)(r % p.K);
+      const bool ok = wait_use(p, S, n);
+      const int32_t *rp = rpos + mp.slot;
       const uint8_t *rows = S.stage + (size_t)(n % kStages) * kStageBytes;
       // two rows per group and pass (independent chains); rows past the
       // chunk read stale stage bytes and are not considered
@@ -610,7 +665,7 @@ struct Step {
         const int ra = ia < cnt ? ia : cnt - 1, rb = ib < cnt ? ib : cnt - 1;
         const float Da = row_dist(rows + (size_t)ra * kRowBytes, sub, qv);
         const float Db = row_dist(rows + (size_t)rb * kRowBytes, sub, qv);
-        const int pa = rpos[slot0 + ra], pb = rpos[slot0 + rb];
+        const int pa = rp[ra], pb = rp[rb];
         if (ok && ia < cnt && pa >= pos_lo && pa <= pos_hi && better(Da, pa, bd, bp)) {
           bd = Da;
           bp = pa;
@@ -621,9 +676,9 @@ struct Step {
         }
       }
       release(p, S, n);
-      r = e;
+      more = match_next(mp, cnt, p.K);
     }
-    if (cur >= 0) flush_best(p, S, cur, bd, bp);
+    flush_best(p, S, cur, bd, bp);
   }
 
   // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.
@@ -644,7 +699,7 @@ struct Step {
       }
       __threadfence();
     }
-    __syncthreads();
+    block_sync();
   }
 
   // Decisions of every head from the combined minima, then every unit's band
@@ -664,7 +719,7 @@ struct Step {
       S.X[bh] = pos;
       if (blockIdx.x == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
     }
-    __syncthreads();
+    block_sync();
     for (int u = tid; u < U; u += kThreads) {
       const int b = u / p.Hkv, g = u % p.Hkv;
       int s = 0x7fffffff;
@@ -675,7 +730,7 @@ struct Step {
       }
       S.u_s[u] = s;
     }
-    __syncthreads();
+    block_sync();
     layout_phase(p, S, 1);
   }
 
@@ -689,12 +744,6 @@ struct Step {
                                       float2 (&q)[G][kPairs]) {
     const int tid = threadIdx.x, sub = tid & 7;
     const int half = kHeadDim / 2;
-    if (tid < half) {
-      float c = 1.f, s = 0.f;
-      if (p.rope_mode != MAC_ROPE_NONE) rope_angle(pos, p.rope_w[tid], &c, &s);
-      S.ang[tid] = make_float2(c, s);
-    }
-    consumer_sync();
     const bool inter = p.rope_mode == MAC_ROPE_INTERLEAVED;
     for (int i = tid; i < G * half; i += kThreads) {
       const int hh = i / half, j = i % half;
@@ -703,9 +752,10 @@ struct Step {
       const float a = elem_f32<T>(row, ia), b = elem_f32<T>(row, ib);
       float ra = a, rb = b;
       if (p.rope_mode != MAC_ROPE_NONE) {
-        const float2 cs = S.ang[j];
-        ra = __fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y));
-        rb = __fadd_rn(__fmul_rn(b, cs.x), __fmul_rn(a, cs.y));
+        float c, sn;
+        rope_angle(pos, p.rope_f[j], &c, &sn);
+        ra = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
+        rb = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
       }
       S.qrot[hh * kHeadDim + ia] = __fmul_rn(ra, p.q_scale);
       S.qrot[hh * kHeadDim + ib] = __fmul_rn(rb, p.q_scale);
@@ -777,7 +827,7 @@ struct Step {
     const int ntiles = (int)((pc.hi - 1) / kTileTok - tile0 + 1);
     for (int k = 0; k < ntiles; ++k, ++n) {
       const int st = n % kStages;
-      const bool ok = wait_use(S, n);
+      const bool ok = wait_use(p, S, n);
       if (k == 0) rotate_query(p, S, st, S.u_pos[pc.u], q);
       const uint8_t *kb = S.stage + (size_t)st * kStageBytes;
       const uint8_t *vb = kb + kStageBytes / 2;
@@ -932,18 +982,25 @@ struct Step {
       const int e = tid + j * kThreads;
       if (e < G * kHeadDim) dst[(e / kHeadDim) * kPartStride + e % kHeadDim] = acc[j];
     }
-    if (tid < G) {
-      float L = 0.f;
-      for (int gi = 0; gi < kWarps * 4; ++gi) L += S.red_l[gi * G + tid];
-      dst[tid * kPartStride + kHeadDim] = mc[tid];
-      dst[tid * kPartStride + kHeadDim + 1] = L;
+    if (warp == 0) {
+      // lane i holds group i's sums; butterfly over the 32 groups
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        float L = S.red_l[lane * G + hh];
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
+        if (lane == hh) {
+          dst[hh * kPartStride + kHeadDim] = mc[hh];
+          dst[hh * kPartStride + kHeadDim + 1] = L;
+        }
+      }
     }
   }
 
   __device__ static void attend_phase(const StepParams &p, const Smem &S, uint32_t &n, int ph) {
-    const int U = p.B * p.Hkv, P = gridDim.x;
+    const int U = p.B * p.Hkv;
     const int64_t *off = offs(S, ph);
-    const int64_t g0 = span_beg(off, U, blockIdx.x, P), g1 = span_beg(off, U, blockIdx.x + 1, P);
+    const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
     if (g0 >= g1) return;
     float *part = ph ? p.part_b : p.part_a;
     Piece pc;
@@ -979,16 +1036,15 @@ struct Step {
 
   // CTAs whose spans meet unit u's segment in phase ph: [*c0, *c1] (empty
   // when *c1 < *c0).
-  __device__ static void seg_ctas(const Smem &S, int ph, int U, int u, int *c0, int *c1) {
-    const int64_t *off = offs(S, ph);
-    const int P = gridDim.x;
+  __device__ static void seg_ctas(const Smem &S, int ph, int u, int *c0, int *c1) {
+    const int64_t *off = offs(S, ph), *span = spans(S, ph);
     if (off[u + 1] <= off[u]) {
       *c0 = 0;
       *c1 = -1;
       return;
     }
-    *c0 = cta_of(off[u], off[U], P);
-    *c1 = cta_of(off[u + 1] - 1, off[U], P);
+    *c0 = cta_of(span, gridDim.x, off[u]);
+    *c1 = cta_of(span, gridDim.x, off[u + 1] - 1);
   }
 
   // For each (request, head) -- one per CTA at a time -- merge the unit's
@@ -999,16 +1055,28 @@ struct Step {
   // AS_{1:m-r}), and the tail states (giving the output).
   __device__ static void reduce_phase(const StepParams &p, const Smem &S) {
     constexpr int kSeg = kHeadDim + 4;                // m, l, -, -, o[d]
+    constexpr int kBatch = 8;                         // pieces loaded at once per warp
     float *seg = reinterpret_cast<float *>(S.stage);  // [kWarps][2][kSeg]; the stages are idle now
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n_bh = p.B * p.Hq, U = p.B * p.Hkv, P = gridDim.x;
+    const int n_bh = p.B * p.Hq;
     for (int bh = blockIdx.x; bh < n_bh; bh += gridDim.x) {
       const int b = bh / p.Hq, h = bh % p.Hq, g = h / G, hh = h % G;
       const int u = b * p.Hkv + g;
       int cb0, cb1, ca0, ca1;
-      seg_ctas(S, 1, U, u, &cb0, &cb1);
-      seg_ctas(S, 0, U, u, &ca0, &ca1);
+      seg_ctas(S, 1, u, &cb0, &cb1);
+      seg_ctas(S, 0, u, &ca0, &ca1);
       const int nb = cb1 - cb0 + 1, n = nb + (ca1 - ca0 + 1);
+      // cached rectified summary of a hit head, fetched ahead of its use
+      float c_lse = -INFINITY;
+      float4 c_o = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p.mode == MODE_DECODE && warp == 0) {
+        const int pos = S.X[bh];
+        if (pos >= 1) {
+          const int64_t slot = (int64_t)bh * p.K + pos % p.K;
+          c_lse = p.ring_lse[slot];
+          c_o = reinterpret_cast<const float4 *>(p.ring_o + slot * kHeadDim)[lane];
+        }
+      }
       if (p.mode == MODE_DECODE && warp == kWarps - 1 && lane < kHeadDim / kPer) {
         // the append (on the aux stream) reads the step's query from the ring
         // workspace, so the caller may reuse its query buffer right away
@@ -1019,35 +1087,35 @@ struct Step {
       const int i0 = warp * per, i1 = min(n, i0 + per);
       float bm = -INFINITY, bl = 0.f, bo[4] = {0.f, 0.f, 0.f, 0.f};
       float tm = -INFINITY, tl = 0.f, to[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int i = i0; i < i1; i += 4) {
-        float pm[4], pl[4], po[4][4];
+      for (int i = i0; i < i1; i += kBatch) {
+        float pm[kBatch], pl[kBatch];
+        float4 po[kBatch];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kBatch; ++j) {
           pl[j] = 0.f;
+          pm[j] = 0.f;
+          po[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           const int it = i + j;
           if (it < i1) {
             const int ph = it < nb ? 1 : 0;
             const int c = it < nb ? cb0 + it : ca0 + (it - nb);
-            const int64_t *off = offs(S, ph);
-            if (span_beg(off, U, c, P) < span_beg(off, U, c + 1, P)) {
+            const int64_t *span = spans(S, ph);
+            if (span[c] < span[c + 1]) {  // CTAs with an empty span have no piece
               const float *pp = (ph ? p.part_b : p.part_a) + ((int64_t)(u + c) * G + hh) * kPartStride;
               pm[j] = __ldcg(pp + kHeadDim);
               pl[j] = __ldcg(pp + kHeadDim + 1);
-              const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp) + lane);
-              po[j][0] = v.x;
-              po[j][1] = v.y;
-              po[j][2] = v.z;
-              po[j][3] = v.w;
+              po[j] = __ldcg(reinterpret_cast<const float4 *>(pp) + lane);
             }
           }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kBatch; ++j) {
           if (i + j >= i1) break;
+          const float o2[4] = {po[j].x, po[j].y, po[j].z, po[j].w};
           if (i + j < nb)
-            merge4(bm, bl, bo, pm[j], pl[j], po[j]);
+            merge4(bm, bl, bo, pm[j], pl[j], o2);
           else
-            merge4(tm, tl, to, pm[j], pl[j], po[j]);
+            merge4(tm, tl, to, pm[j], pl[j], o2);
         }
       }
       float *sw = seg + (size_t)warp * 2 * kSeg;
@@ -1059,22 +1127,14 @@ struct Step {
       }
       *reinterpret_cast<float4 *>(sw + 4 + lane * 4) = make_float4(bo[0], bo[1], bo[2], bo[3]);
       *reinterpret_cast<float4 *>(sw + kSeg + 4 + lane * 4) = make_float4(to[0], to[1], to[2], to[3]);
-      __syncthreads();
+      block_sync();
       if (warp == 0) {
         float M = -INFINITY, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-        if (p.mode == MODE_DECODE) {
-          const int pos = S.X[bh];
-          if (pos >= 1) {
-            const int64_t slot = (int64_t)bh * p.K + pos % p.K;
-            const float lse = p.ring_lse[slot];
-            if (lse > -INFINITY) {
-              const float4 v = reinterpret_cast<const float4 *>(p.ring_o + slot * kHeadDim)[lane];
-              const float a[4] = {v.x, v.y, v.z, v.w};
-              merge4(M, L, O, lse * kLog2e, 1.f, a);
-            }
-          }
-          if (lane == 0) p.best[bh] = 0ull;  // every CTA read it before the barrier
+        if (c_lse > -INFINITY) {
+          const float a[4] = {c_o.x, c_o.y, c_o.z, c_o.w};
+          merge4(M, L, O, c_lse * kLog2e, 1.f, a);
         }
+        if (p.mode == MODE_DECODE && lane == 0) p.best[bh] = 0ull;  // every CTA read it before the barrier
         for (int w = 0; w < kWarps; ++w) {
           const float *s = seg + (size_t)w * 2 * kSeg;
           merge4(M, L, O, s[0], s[1], s + 4 + lane * 4);
@@ -1094,11 +1154,19 @@ struct Step {
             make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
         if (p.out_lse && lane == 0) p.out_lse[bh] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
       }
-      __syncthreads();
+      block_sync();
     }
   }
 
   // ---------------------------------------------------------------------
+
+  // Phase trace point: thread 0 records %globaltimer.  Like every region run
+  // by one thread, it ends with the warp reconverged before the barriers and
+  // shuffles that follow.
+  __device__ static void stamp(unsigned long long *trace, int k) {
+    if (trace && threadIdx.x == 0) trace[k] = globaltimer();
+    __syncwarp();
+  }
 
   __device__ static void run(const StepParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1106,12 +1174,12 @@ struct Step {
     __shared__ uint32_t s_cnt[kStages];
     __shared__ int s_abort;
     __shared__ Cursor s_cur;
+    __shared__ int64_t s_span[2][kMaxGrid + 1];
     const int n_units = p.B * p.Hkv, n_heads = p.B * p.Hq;
     Smem S;
     S.stage = smem;
     S.qbuf = smem + kOffQ;
     S.full = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    S.ang = reinterpret_cast<float2 *>(smem + kOffAng);
     S.qrot = reinterpret_cast<float *>(smem + kOffQrot);
     S.red_o = reinterpret_cast<float *>(smem + kOffRedO);
     S.red_l = reinterpret_cast<float *>(smem + kOffRedL);
@@ -1120,6 +1188,8 @@ struct Step {
     S.nx = x_ints(n_heads, p.K);
     S.offA = reinterpret_cast<int64_t *>(smem + off_units(n_heads, p.K));
     S.offB = S.offA + (n_units + 1);
+    S.spanA = s_span[0];
+    S.spanB = s_span[1];
     S.u_pos = reinterpret_cast<int32_t *>(S.offB + (n_units + 1));
     S.u_s = S.u_pos + n_units;
     S.cnt = s_cnt;
@@ -1130,7 +1200,7 @@ struct Step {
 
     const int tid = threadIdx.x;
     unsigned long long *trace = p.trace ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
-    if (trace && tid == 0) trace[0] = globaltimer();
+    stamp(trace, 0);
     if (tid == 0) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(smem_addr(&S.full[i]), 1);
@@ -1138,40 +1208,38 @@ struct Step {
       }
       s_abort = 0;
       mbar_fence_init();
+      // the match chunks need no layout: start streaming them right away
+      Cursor &c = s_cur;
+      c.n = 0;
+      c.n_copied = 0;
+      c.cont = !decode;
+      c.kind = decode && match_slice(p, &c.mp) ? C_MATCH : C_PEND;
+      for (int i = 0; i < kStages && c.kind == C_MATCH; ++i) issue_current(p, S);
     }
+    __syncwarp();
     for (int u = tid; u < n_units; u += kThreads) {
       S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
       S.u_s[u] = 1;
       if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
         set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
     }
-    __syncthreads();
+    block_sync();
     layout_phase(p, S, 0);
     if (!decode) layout_phase(p, S, 1);
-
     if (tid == 0) {
+      // the rest of the first kStages uses (tail tiles, or all of them in
+      // full attention); no release can happen before the consumers start
       Cursor &c = s_cur;
-      c.n = 0;
-      c.n_copied = 0;
-      c.cont = !decode;
-      if (decode) {
-        const int64_t N = (int64_t)p.B * p.Hq * p.K;
-        c.kind = C_MATCH;
-        c.r = (int64_t)blockIdx.x * N / gridDim.x;
-        c.s1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
-        if (c.r >= c.s1) cursor_phase(p, S, c, 0);
-      } else {
-        cursor_phase(p, S, c, 0);
-      }
-      for (int i = 0; i < kStages && c.kind != C_END; ++i) issue_current(p, S);
+      while (c.n < (uint32_t)kStages && c.kind != C_END && c.kind != C_MATCH) issue_current(p, S);
     }
+    __syncwarp();
 
     uint32_t n = 0;  // stage uses consumed so far (every thread counts the same sequence)
     if (decode) match_phase(p, S, n);
-    if (trace && tid == 0) trace[1] = globaltimer();
+    stamp(trace, 1);
     attend_phase(p, S, n, 0);
-    __syncthreads();
-    if (trace && tid == 0) trace[2] = globaltimer();
+    block_sync();
+    stamp(trace, 2);
     if (decode) {
       grid_barrier(p, S);  // the minima of every head are final
       decide(p, S);
@@ -1182,11 +1250,12 @@ struct Step {
         cursor_phase(p, S, c, 1);
         for (int i = 0; i < kStages && c.kind != C_END; ++i) issue_current(p, S);
       }
+      __syncwarp();
     }
-    if (trace && tid == 0) trace[3] = globaltimer();
+    stamp(trace, 3);
     attend_phase(p, S, n, 1);
-    __syncthreads();
-    if (trace && tid == 0) trace[4] = globaltimer();
+    block_sync();
+    stamp(trace, 4);
     if (*S.abort && tid == 0) {
       // Copies still in flight into the stages: let them land (bounded).  A
       // use was refilled with a copy only after every warp had waited for it
@@ -1200,9 +1269,9 @@ struct Step {
       }
     }
     grid_barrier(p, S);  // every piece partial is written
-    if (trace && tid == 0) trace[5] = globaltimer();
+    stamp(trace, 5);
     reduce_phase(p, S);
-    if (trace && tid == 0) trace[6] = globaltimer();
+    stamp(trace, 6);
   }
 };
 
