@@ -30,7 +30,8 @@ constexpr int kMaxUnits = 1024;         // B * Hkv
 constexpr int kMaxHeads = 4096;         // B * Hq
 constexpr int kMaxGrid = 256;           // CTAs of the step grid (one per SM)
 constexpr int kPosStage = 4096;         // ring positions staged in shared memory for the match
-constexpr int kTracePoints = 8;         // timestamps per CTA in a phase trace
+constexpr int kRopeTab = 16;            // requests whose RoPE angles are tabulated per CTA
+constexpr int kTracePoints = MAC_TRACE_POINTS;  // timestamps per CTA in a phase trace
 constexpr size_t kMaxSmem = 232448;     // dynamic shared memory per CTA (227 KiB)
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -124,8 +125,8 @@ struct AppendParams {
 // ---------------------------------------------------------------------------
 cudaError_t launch_step_bf16(const StepParams &p, int grid, cudaStream_t s);
 cudaError_t launch_step_f32(const StepParams &p, int grid, cudaStream_t s);
-int step_occupancy_bf16(int G, bool paged, int n_heads, int n_units, int K);
-int step_occupancy_f32(int G, bool paged, int n_heads, int n_units, int K);
+int step_occupancy_bf16(int G, bool paged, int B, int Hq, int Hkv, int K);
+int step_occupancy_f32(int G, bool paged, int B, int Hq, int Hkv, int K);
 cudaError_t launch_append(const AppendParams &p, int dtype, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
@@ -251,12 +252,13 @@ __device__ __forceinline__ unsigned long long globaltimer() {
 // frequency as a 64-bit fixed-point fraction of a turn (f = w_j / 2pi * 2^64):
 // the product (pos-1) f taken modulo 2^64 is the angle's fraction of a turn,
 // exact up to the rounding of f (relative 2^-53), read as a signed value so
-// the angle lands in [-pi, pi); its sine and cosine are taken in fp32.  All
-// integer and fp32 arithmetic (GB300's fp64 rate is a small fraction of it).
+// the angle lands in [-pi, pi).  Its sine and cosine come from the hardware
+// approximations (absolute error about 4e-7 on [-pi, pi]).  All integer and
+// fp32 arithmetic: GB300's fp64 rate is a small fraction of its fp32 rate.
 __device__ __forceinline__ void rope_angle(int64_t pos, unsigned long long f, float *c, float *s) {
   const unsigned long long turn = (unsigned long long)(pos - 1) * f;
   const float a = (float)(long long)turn * 3.4061215800865545e-19f;  // 2 pi / 2^64
-  sincosf(a, s, c);
+  __sincosf(a, s, c);
 }
 
 template <typename T>

@@ -117,10 +117,9 @@ int num_sms() {
 // most kMaxGrid (the partial slots are sized for that many).
 int step_grid(const mac_config *c) {
   const int G = c->n_q_heads / c->n_kv_heads;
-  const int heads = c->batch * c->n_q_heads, units = c->batch * c->n_kv_heads;
   const bool paged = c->page_size != 0;
-  int per_sm = c->dtype == MAC_F32 ? step_occupancy_f32(G, paged, heads, units, c->ring_k)
-                                   : step_occupancy_bf16(G, paged, heads, units, c->ring_k);
+  int per_sm = c->dtype == MAC_F32 ? step_occupancy_f32(G, paged, c->batch, c->n_q_heads, c->n_kv_heads, c->ring_k)
+                                   : step_occupancy_bf16(G, paged, c->batch, c->n_q_heads, c->n_kv_heads, c->ring_k);
   if (per_sm < 1) return 0;
   const int grid = num_sms() * per_sm;
   return grid < kMaxGrid ? grid : kMaxGrid;

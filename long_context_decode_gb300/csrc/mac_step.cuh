@@ -66,6 +66,12 @@ __device__ __forceinline__ bool better(float d_a, int p_a, float d_b, int p_b) {
   return d_a < d_b || (d_a == d_b && p_a > p_b);
 }
 
+__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long *p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -109,6 +115,7 @@ struct Step {
   static constexpr int kTileTok = kStageBytes / (2 * kRowBytes);  // 64 (bf16) / 32 (fp32)
   static constexpr int kTPG = kTileTok / 32;                      // tokens per lane group per tile
   static constexpr int kMatchRows = kStageBytes / kRowBytes;      // ring rows per stage
+  static constexpr int kRPG = kMatchRows / 32;                     // rows per lane group per match chunk
   static constexpr int kPer = 16 / (int)sizeof(T);                // elements per 16-byte piece
   static constexpr int kNP = 16 / kPer;                           // pieces per lane (16 dims)
   static constexpr int kPairs = 8;                                // float2 pairs per lane (16 dims)
@@ -116,16 +123,14 @@ struct Step {
   static constexpr int kScat = ilog2c(kV);                        // reduce-scatter levels
   static constexpr int kPlain = 3 - kScat;                        // plain butterfly levels after them
   static constexpr int kQBytes = G * kRowBytes;
-  static constexpr int kRedGroups = 2;                            // lane groups per warp per epilogue round
   static constexpr int kOutPer = (G * kHeadDim + kThreads - 1) / kThreads;
   static_assert(kV <= 8, "one score per lane of a group at most");
 
   // dynamic shared memory layout
   static constexpr size_t kOffQ = (size_t)kStages * kStageBytes;
   static constexpr size_t kOffBar = kOffQ + (size_t)kStages * kQBytes;
-  static constexpr size_t kOffQrot = kOffBar + 64;
-  static constexpr size_t kOffRedO = kOffQrot + 4 * (size_t)G * kHeadDim;
-  static constexpr size_t kOffRedL = kOffRedO + 4 * (size_t)kWarps * kRedGroups * G * kHeadDim;
+  static constexpr size_t kOffRedO = kOffBar + 64;
+  static constexpr size_t kOffRedL = kOffRedO + 4 * (size_t)kWarps * 4 * G * kHeadDim;
   static constexpr size_t kOffRedM = kOffRedL + 4 * (size_t)kWarps * 4 * G;
   static constexpr size_t kOffX = kOffRedM + 4 * (size_t)kWarps * G;
   static_assert(kOffBar % 8 == 0 && kOffX % 8 == 0, "alignment");
@@ -140,9 +145,14 @@ struct Step {
     return (kOffX + 4 * (size_t)x_ints(n_heads, K) + 7) / 8 * 8;
   }
   // + offsets of the tail and band segments (int64, n_units + 1 each), query
-  // position and band start of every unit (int32)
-  __host__ __device__ static size_t smem_bytes(int n_heads, int n_units, int K) {
-    return off_units(n_heads, K) + 16 * ((size_t)n_units + 1) + 8 * (size_t)n_units;
+  // position and band start of every unit (int32), then the RoPE cos/sin
+  // table of every request when there are at most kRopeTab of them
+  __host__ __device__ static size_t off_rope(int n_heads, int n_units, int K) {
+    return (off_units(n_heads, K) + 16 * ((size_t)n_units + 1) + 8 * (size_t)n_units + 7) / 8 * 8;
+  }
+  __host__ __device__ static size_t smem_bytes(int B, int Hq, int Hkv, int K) {
+    const size_t tab = B <= kRopeTab ? 8 * (size_t)B * (kHeadDim / 2) : 0;
+    return off_rope(B * Hq, B * Hkv, K) + tab;
   }
 
   // Issue cursor: the next use of the CTA's stage sequence (match chunks,
@@ -167,8 +177,7 @@ struct Step {
     uint8_t *stage;     // [kStages][kStageBytes]
     uint8_t *qbuf;      // [kStages][G][d]: pre-RoPE query rows of a piece's unit
     uint64_t *full;     // [kStages]
-    float *qrot;        // [G][d]
-    float *red_o;       // [kWarps][kRedGroups][G][d]
+    float *red_o;       // [kWarps][4][G][d]
     float *red_l;       // [kWarps * 4][G]
     float *red_m;       // [kWarps][G]
     int32_t *X;
@@ -179,6 +188,7 @@ struct Step {
     int64_t *spanB;     // [grid + 1]: same for the bands
     int32_t *u_pos;     // [n_units]: position of the unit's query (RoPE angle pos - 1)
     int32_t *u_s;       // [n_units]: first band token of the unit
+    float2 *rope;       // [B][d/2]: cos, sin of the query's rotation angles (B <= kRopeTab), or null
     uint32_t *cnt;      // [kStages]: releases of the stage's current use
     int *mask;          // [kStages]: valid 16-token pages of the tile in the stage
     volatile int *abort;
@@ -188,6 +198,17 @@ struct Step {
   struct Piece {
     int u, lo, hi;
   };
+
+  // Phase trace point (see mac_set_trace): thread 0 records %globaltimer.
+  // Like every region run by one thread, it ends with the warp reconverged
+  // before the barriers and shuffles that follow.
+  __device__ static void stamp(unsigned long long *trace, int k) {
+    if (trace && threadIdx.x == 0) trace[k] = globaltimer();
+    __syncwarp();
+  }
+  __device__ static unsigned long long *cta_trace(const StepParams &p) {
+    return p.trace ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
+  }
 
   // Lane `sub` (0..7) of a token's 8-lane group owns 16 dimensions: piece c
   // covers dims [c*8*kPer + sub*kPer, +kPer), so each group reads 128
@@ -219,6 +240,13 @@ struct Step {
   }
 
   __device__ static const int64_t *offs(const Smem &S, int ph) { return ph ? S.offB : S.offA; }
+
+  // c * total / P, in 32-bit arithmetic whenever the product fits (the
+  // common case: 64-bit division is a long serial routine)
+  __device__ static int64_t part_of(int c, int64_t total, int P) {
+    if (total < (1LL << 23)) return (int64_t)((uint32_t)c * (uint32_t)total / (uint32_t)P);
+    return (int64_t)c * total / P;
+  }
   __device__ static const int64_t *spans(const Smem &S, int ph) { return ph ? S.spanB : S.spanA; }
 
   // the CTA whose (non-empty) span holds global index x (x < total): the
@@ -300,7 +328,7 @@ struct Step {
     // span c = global indices [c*total/P, (c+1)*total/P)
     int64_t *span = ph ? S.spanB : S.spanA;
     const int64_t total = off[U];
-    for (int c = tid; c <= (int)gridDim.x; c += kThreads) span[c] = (int64_t)c * total / gridDim.x;
+    for (int c = tid; c <= (int)gridDim.x; c += kThreads) span[c] = part_of(c, total, gridDim.x);
     block_sync();
   }
 
@@ -365,7 +393,6 @@ struct Step {
       mbar_arrive(bar);
       return;
     }
-    fence_proxy_async();
     mbar_expect_tx(bar, bytes);
     if (with_q) {
       const uint8_t *q = (const uint8_t *)p.q;
@@ -413,12 +440,20 @@ struct Step {
   // CTA c's slice of the B*Hq*K ring rows: [c*N/P, (c+1)*N/P); false if empty
   __device__ static bool match_slice(const StepParams &p, MatchPos *mp) {
     const int64_t N = (int64_t)p.B * p.Hq * p.K;
-    const int64_t s0 = (int64_t)blockIdx.x * N / gridDim.x, s1 = (int64_t)(blockIdx.x + 1) * N / gridDim.x;
+    const int64_t s0 = part_of(blockIdx.x, N, gridDim.x), s1 = part_of(blockIdx.x + 1, N, gridDim.x);
     if (s0 >= s1) return false;
-    mp->bh = (int)(s0 / p.K);
-    mp->slot = (int)(s0 % p.K);
-    mp->bh_last = (int)((s1 - 1) / p.K);
-    mp->slot_end = (int)((s1 - 1) % p.K) + 1;
+    if (s1 < (1LL << 31)) {
+      const uint32_t a = (uint32_t)s0, z = (uint32_t)(s1 - 1), K = (uint32_t)p.K;
+      mp->bh = (int)(a / K);
+      mp->slot = (int)(a % K);
+      mp->bh_last = (int)(z / K);
+      mp->slot_end = (int)(z % K) + 1;
+    } else {
+      mp->bh = (int)(s0 / p.K);
+      mp->slot = (int)(s0 % p.K);
+      mp->bh_last = (int)((s1 - 1) / p.K);
+      mp->slot_end = (int)((s1 - 1) % p.K) + 1;
+    }
     return true;
   }
 
@@ -490,7 +525,6 @@ struct Step {
       } else if (go) {
         const uint32_t bytes = (uint32_t)rows * kRowBytes;
         const uint32_t bar = smem_addr(&S.full[st]);
-        fence_proxy_async();
         mbar_expect_tx(bar, bytes);
         bulk_g2s(smem_addr(S.stage + (size_t)st * kStageBytes),
                  (const uint8_t *)p.ring_q + ((size_t)c.mp.bh * p.K + c.mp.slot) * kRowBytes, bytes, bar);
@@ -656,28 +690,42 @@ struct Step {
         rpos = staged ? S.X + (b - b_lo) * p.K : p.ring_pos + (int64_t)b * p.K;
       }
       const bool ok = wait_use(p, S, n);
+      if (n == 0) stamp(cta_trace(p), 8);
       const int32_t *rp = rpos + mp.slot;
       const uint8_t *rows = S.stage + (size_t)(n % kStages) * kStageBytes;
-      // two rows per group and pass (independent chains); rows past the
-      // chunk read stale stage bytes and are not considered
-      for (int i0 = 0; i0 < cnt; i0 += 64) {
-        const int ia = i0 + grp, ib = ia + 32;
-        const int ra = ia < cnt ? ia : cnt - 1, rb = ib < cnt ? ib : cnt - 1;
-        const float Da = row_dist(rows + (size_t)ra * kRowBytes, sub, qv);
-        const float Db = row_dist(rows + (size_t)rb * kRowBytes, sub, qv);
-        const int pa = rp[ra], pb = rp[rb];
-        if (ok && ia < cnt && pa >= pos_lo && pa <= pos_hi && better(Da, pa, bd, bp)) {
-          bd = Da;
-          bp = pa;
+      // all of the group's rows of the chunk at once (independent chains),
+      // then a tree over them; rows past the chunk read stale stage bytes and
+      // are not considered
+      {
+        float D[kRPG];
+        int ps[kRPG];
+#pragma unroll
+        for (int k = 0; k < kRPG; ++k) {
+          const int i = grp + 32 * k;
+          const int ri = i < cnt ? i : cnt - 1;
+          D[k] = row_dist(rows + (size_t)ri * kRowBytes, sub, qv);
+          const int pk = rp[ri];
+          const bool valid = ok && i < cnt && pk >= pos_lo && pk <= pos_hi;
+          ps[k] = valid ? pk : -1;
+          D[k] = valid ? D[k] : INFINITY;
         }
-        if (ok && ib < cnt && pb >= pos_lo && pb <= pos_hi && better(Db, pb, bd, bp)) {
-          bd = Db;
-          bp = pb;
+#pragma unroll
+        for (int w = 1; w < kRPG; w <<= 1)
+#pragma unroll
+          for (int k = 0; k + w < kRPG; k += 2 * w)
+            if (better(D[k + w], ps[k + w], D[k], ps[k])) {
+              D[k] = D[k + w];
+              ps[k] = ps[k + w];
+            }
+        if (ps[0] >= 1 && better(D[0], ps[0], bd, bp)) {
+          bd = D[0];
+          bp = ps[0];
         }
       }
       release(p, S, n);
       more = match_next(mp, cnt, p.K);
     }
+    stamp(cta_trace(p), 9);
     flush_best(p, S, cur, bd, bp);
   }
 
@@ -685,8 +733,7 @@ struct Step {
   __device__ static void grid_barrier(const StepParams &p, const Smem &S) {
     if (threadIdx.x == 0) {
       unsigned long long *ctr = reinterpret_cast<unsigned long long *>(p.ctl + 2);
-      __threadfence();
-      const unsigned long long old = atomicAdd(ctr, 1ull);
+      const unsigned long long old = atom_add_release_u64(ctr, 1ull);
       const unsigned long long target = old - old % gridDim.x + gridDim.x;
       const long long t0 = clock64();
       while (ld_acquire_u64(ctr) < target) {
@@ -697,7 +744,6 @@ struct Step {
         }
         __nanosleep(32);
       }
-      __threadfence();
     }
     block_sync();
   }
@@ -730,6 +776,17 @@ struct Step {
       }
       S.u_s[u] = s;
     }
+    // the cached summaries phase R will merge: start bringing them into L2
+    // now, behind the band attention
+    for (int bh = blockIdx.x + (tid >> 5) * gridDim.x; bh < n_bh; bh += kWarps * gridDim.x) {
+      const int pos = S.X[bh];
+      if (pos >= 1 && (tid & 31) < kHeadDim * 4 / 128 + 1) {
+        const int64_t slot = (int64_t)bh * p.K + pos % p.K;
+        const void *a = (tid & 31) < kHeadDim * 4 / 128 ? (const void *)(p.ring_o + slot * kHeadDim + (tid & 31) * 32)
+                                                         : (const void *)(p.ring_lse + slot);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+      }
+    }
     block_sync();
     layout_phase(p, S, 1);
   }
@@ -738,40 +795,73 @@ struct Step {
   // phases A and B: attention over the CTA's pieces
   // ---------------------------------------------------------------------
 
-  // R(pos) q~ * log2(e)/sqrt(d) for the piece's heads, from the query rows
-  // that came with its first tile; every lane then loads its 16 dims.
-  __device__ static void rotate_query(const StepParams &p, const Smem &S, int st, int64_t pos,
-                                      float2 (&q)[G][kPairs]) {
-    const int tid = threadIdx.x, sub = tid & 7;
-    const int half = kHeadDim / 2;
-    const bool inter = p.rope_mode == MAC_ROPE_INTERLEAVED;
-    for (int i = tid; i < G * half; i += kThreads) {
-      const int hh = i / half, j = i % half;
-      const int ia = inter ? 2 * j : j, ib = inter ? 2 * j + 1 : j + half;
-      const void *row = S.qbuf + (size_t)st * kQBytes + hh * kRowBytes;
-      const float a = elem_f32<T>(row, ia), b = elem_f32<T>(row, ib);
-      float ra = a, rb = b;
-      if (p.rope_mode != MAC_ROPE_NONE) {
-        float c, sn;
-        rope_angle(pos, p.rope_f[j], &c, &sn);
-        ra = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
-        rb = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
-      }
-      S.qrot[hh * kHeadDim + ia] = __fmul_rn(ra, p.q_scale);
-      S.qrot[hh * kHeadDim + ib] = __fmul_rn(rb, p.q_scale);
-      if (!(isfinite(a) && isfinite(b))) set_status(p.ctl, MAC_DEV_NONFINITE_Q);
+  // Lane element k (0..15) of a 16-dim share: piece k / kPer, offset k % kPer.
+  __device__ static int lane_dim(int k, int sub) { return piece_dim(k / kPer, sub) + k % kPer; }
+
+  // cos, sin of rotation angle j of request b at position pos: from the
+  // CTA's table when there is one, else computed here.
+  __device__ static float2 rope_cs(const StepParams &p, const Smem &S, int b, int64_t pos, int j) {
+    if (S.rope) return S.rope[b * (kHeadDim / 2) + j];
+    float c, sn;
+    rope_angle(pos, p.rope_f[j], &c, &sn);
+    return make_float2(c, sn);
+  }
+
+  __device__ static void rotate_pair(float a, float b, float2 cs, float scale, float *ra, float *rb) {
+    *ra = __fmul_rn(__fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y)), scale);
+    *rb = __fmul_rn(__fadd_rn(__fmul_rn(b, cs.x), __fmul_rn(a, cs.y)), scale);
+  }
+
+  // R(pos) q~ * log2(e)/sqrt(d) for this lane's 16 dims of the piece's G
+  // heads, from the pre-RoPE rows that came with the piece's first tile.
+  // Both members of every rotation pair lie in the same lane (half split:
+  // dims j and j + d/2 are lane elements k and k + 8; interleaved: 2j and
+  // 2j + 1 are adjacent elements), so no lane waits for another.  Explicit
+  // roundings keep the result identical wherever it is computed.
+  __device__ static void load_query(const StepParams &p, const Smem &S, int st, int b, int64_t pos,
+                                    float2 (&q)[G][kPairs]) {
+    const int sub = threadIdx.x & 7;
+    const int mode = p.rope_mode;
+    float2 cs[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      cs[i] = make_float2(1.f, 0.f);
+      if (mode == MAC_ROPE_HALF) cs[i] = rope_cs(p, S, b, pos, lane_dim(i, sub));
+      else if (mode == MAC_ROPE_INTERLEAVED) cs[i] = rope_cs(p, S, b, pos, lane_dim(2 * i, sub) / 2);
     }
-    consumer_sync();
+    const float scale = p.q_scale;
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh)
+    for (int hh = 0; hh < G; ++hh) {
+      const uint8_t *row = S.qbuf + (size_t)st * kQBytes + hh * kRowBytes;
+      float x[16];
 #pragma unroll
-      for (int c = 0; c < kNP; ++c)
+      for (int c = 0; c < kNP; ++c) {
+        float2 e2[kPer / 2];
+        unpack16x2<T>(*reinterpret_cast<const uint4 *>(row + c * 128 + sub * 16), e2);
 #pragma unroll
-        for (int e4 = 0; e4 < kPer; e4 += 4) {
-          const float4 v = *reinterpret_cast<const float4 *>(S.qrot + hh * kHeadDim + piece_dim(c, sub) + e4);
-          q[hh][(c * kPer + e4) / 2] = make_float2(v.x, v.y);
-          q[hh][(c * kPer + e4) / 2 + 1] = make_float2(v.z, v.w);
+        for (int e = 0; e < kPer / 2; ++e) {
+          x[c * kPer + 2 * e] = e2[e].x;
+          x[c * kPer + 2 * e + 1] = e2[e].y;
         }
+      }
+      bool finite = true;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) finite = finite && isfinite(x[k]);
+      if (!finite) set_status(p.ctl, MAC_DEV_NONFINITE_Q);
+      float y[16];
+      if (mode == MAC_ROPE_INTERLEAVED) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rotate_pair(x[2 * i], x[2 * i + 1], cs[i], scale, &y[2 * i], &y[2 * i + 1]);
+      } else if (mode == MAC_ROPE_HALF) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rotate_pair(x[i], x[i + 8], cs[i], scale, &y[i], &y[i + 8]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) y[k] = __fmul_rn(x[k], scale);
+      }
+#pragma unroll
+      for (int i = 0; i < kPairs; ++i) q[hh][i] = make_float2(y[2 * i], y[2 * i + 1]);
+    }
   }
 
   // v[i] (i = token slot * G + head, partial dot products of the lane's 16
@@ -802,7 +892,8 @@ struct Step {
   // One piece: tokens [pc.lo, pc.hi] of unit pc.u for its G heads; the
   // piece's partial summary goes to dst ([G][kPartStride]).
   __device__ static void attend_piece(const StepParams &p, const Smem &S, uint32_t &n, int ph,
-                                      const Piece &pc, float *dst) {
+                                      const Piece &pc, float *dst, bool first_piece) {
+    unsigned long long *trace = first_piece ? cta_trace(p) : nullptr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = lane >> 3, sub = lane & 7;
     const int b = pc.u / p.Hkv, g = pc.u % p.Hkv;
     const int idx = sub >> kPlain;         // this lane's score slot
@@ -828,7 +919,10 @@ struct Step {
     for (int k = 0; k < ntiles; ++k, ++n) {
       const int st = n % kStages;
       const bool ok = wait_use(p, S, n);
-      if (k == 0) rotate_query(p, S, st, S.u_pos[pc.u], q);
+      if (k == 0) {
+        stamp(trace, ph ? 13 : 11);
+        load_query(p, S, st, b, S.u_pos[pc.u], q);
+      }
       const uint8_t *kb = S.stage + (size_t)st * kStageBytes;
       const uint8_t *vb = kb + kStageBytes / 2;
       const int t0 = (int)((tile0 + k) * kTileTok);
@@ -906,7 +1000,9 @@ struct Step {
       }
       release(p, S, n);
     }
+    stamp(trace, ph ? 14 : 12);
     epilogue(p, S, o, mrun, m_mine, l_mine, dst);
+    if (ph == 1) stamp(trace, 15);
   }
 
   // The CTA's 32 lane-group states -> one partial summary per head: common
@@ -948,34 +1044,34 @@ struct Step {
       for (int hh = 1; hh < G; ++hh) mcm = hm == hh ? mc[hh] : mcm;
       S.red_l[(warp * 4 + lg) * G + hm] = l_grp * ex2(m_mine - mcm);
     }
+    {
+      float *wr = S.red_o + (size_t)(warp * 4 + lg) * G * kHeadDim;
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int c = 0; c < kNP; ++c)
+#pragma unroll
+          for (int e4 = 0; e4 < kPer; e4 += 4) {
+            const float2 a = o[hh][(c * kPer + e4) / 2], bb = o[hh][(c * kPer + e4) / 2 + 1];
+            *reinterpret_cast<float4 *>(wr + hh * kHeadDim + piece_dim(c, sub) + e4) =
+                make_float4(a.x, a.y, bb.x, bb.y);
+          }
+    }
+    consumer_sync();
+    // each output element: the 32 group states in a fixed order (the next
+    // piece's epilogue writes these buffers only after its first barrier,
+    // which every thread reaches after these reads)
     float acc[kOutPer];
 #pragma unroll
-    for (int j = 0; j < kOutPer; ++j) acc[j] = 0.f;
+    for (int j = 0; j < kOutPer; ++j) {
+      acc[j] = 0.f;
+      const int e = tid + j * kThreads;
+      if (e < G * kHeadDim) {
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int rd = 0; rd < 4 / kRedGroups; ++rd) {
-      if (lg / kRedGroups == rd) {
-        float *wr = S.red_o + (size_t)(warp * kRedGroups + lg % kRedGroups) * G * kHeadDim;
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-          for (int c = 0; c < kNP; ++c)
-#pragma unroll
-            for (int e4 = 0; e4 < kPer; e4 += 4) {
-              const float2 a = o[hh][(c * kPer + e4) / 2], bb = o[hh][(c * kPer + e4) / 2 + 1];
-              *reinterpret_cast<float4 *>(wr + hh * kHeadDim + piece_dim(c, sub) + e4) =
-                  make_float4(a.x, a.y, bb.x, bb.y);
-            }
+        for (int w2 = 0; w2 < kWarps * 4; ++w2) part[w2 & 3] += S.red_o[(size_t)w2 * G * kHeadDim + e];
+        acc[j] = (part[0] + part[1]) + (part[2] + part[3]);
       }
-      consumer_sync();
-#pragma unroll
-      for (int j = 0; j < kOutPer; ++j) {
-        const int e = tid + j * kThreads;
-        if (e < G * kHeadDim) {
-#pragma unroll 4
-          for (int w2 = 0; w2 < kWarps * kRedGroups; ++w2) acc[j] += S.red_o[(size_t)w2 * G * kHeadDim + e];
-        }
-      }
-      consumer_sync();
     }
 #pragma unroll
     for (int j = 0; j < kOutPer; ++j) {
@@ -1005,9 +1101,11 @@ struct Step {
     float *part = ph ? p.part_b : p.part_a;
     Piece pc;
     int u = unit_of(off, U, g0);
+    bool first = true;
     while (find_piece(p, S, ph, u, g0, g1, &pc)) {
-      attend_piece(p, S, n, ph, pc, part + (size_t)(pc.u + blockIdx.x) * G * kPartStride);
+      attend_piece(p, S, n, ph, pc, part + (size_t)(pc.u + blockIdx.x) * G * kPartStride, first);
       u = pc.u + 1;
+      first = false;
     }
   }
 
@@ -1160,14 +1258,6 @@ struct Step {
 
   // ---------------------------------------------------------------------
 
-  // Phase trace point: thread 0 records %globaltimer.  Like every region run
-  // by one thread, it ends with the warp reconverged before the barriers and
-  // shuffles that follow.
-  __device__ static void stamp(unsigned long long *trace, int k) {
-    if (trace && threadIdx.x == 0) trace[k] = globaltimer();
-    __syncwarp();
-  }
-
   __device__ static void run(const StepParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_mask[kStages];
@@ -1180,7 +1270,6 @@ struct Step {
     S.stage = smem;
     S.qbuf = smem + kOffQ;
     S.full = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    S.qrot = reinterpret_cast<float *>(smem + kOffQrot);
     S.red_o = reinterpret_cast<float *>(smem + kOffRedO);
     S.red_l = reinterpret_cast<float *>(smem + kOffRedL);
     S.red_m = reinterpret_cast<float *>(smem + kOffRedM);
@@ -1192,6 +1281,7 @@ struct Step {
     S.spanB = s_span[1];
     S.u_pos = reinterpret_cast<int32_t *>(S.offB + (n_units + 1));
     S.u_s = S.u_pos + n_units;
+    S.rope = p.B <= kRopeTab ? reinterpret_cast<float2 *>(smem + off_rope(n_heads, n_units, p.K)) : nullptr;
     S.cnt = s_cnt;
     S.mask = s_mask;
     S.abort = &s_abort;
@@ -1199,7 +1289,8 @@ struct Step {
     const bool decode = p.mode == MODE_DECODE;
 
     const int tid = threadIdx.x;
-    unsigned long long *trace = p.trace ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
+    unsigned long long *trace = cta_trace(p);
+    if (trace && tid == 0) trace[16] = (unsigned long long)clock64();
     stamp(trace, 0);
     if (tid == 0) {
       for (int i = 0; i < kStages; ++i) {
@@ -1223,9 +1314,19 @@ struct Step {
       if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
         set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
     }
+    if (S.rope && p.rope_mode != MAC_ROPE_NONE) {
+      // the rotation angles of every request's query (shared by its heads)
+      for (int i = tid; i < p.B * (kHeadDim / 2); i += kThreads) {
+        const int b = i / (kHeadDim / 2), j = i % (kHeadDim / 2);
+        float c, sn;
+        rope_angle((int64_t)p.pos_base[b] + p.pos_add, p.rope_f[j], &c, &sn);
+        S.rope[i] = make_float2(c, sn);
+      }
+    }
     block_sync();
     layout_phase(p, S, 0);
     if (!decode) layout_phase(p, S, 1);
+    stamp(trace, 7);
     if (tid == 0) {
       // the rest of the first kStages uses (tail tiles, or all of them in
       // full attention); no release can happen before the consumers start
@@ -1242,6 +1343,7 @@ struct Step {
     stamp(trace, 2);
     if (decode) {
       grid_barrier(p, S);  // the minima of every head are final
+      stamp(trace, 10);
       decide(p, S);
       if (tid == 0) {
         Cursor &c = s_cur;
@@ -1256,12 +1358,15 @@ struct Step {
     attend_phase(p, S, n, 1);
     block_sync();
     stamp(trace, 4);
-    if (*S.abort && tid == 0) {
-      // Copies still in flight into the stages: let them land (bounded).  A
-      // use was refilled with a copy only after every warp had waited for it
-      // successfully, so only the last kStages copied uses can be pending.
+    if (tid == 0) {
+      // No copy may still be in flight into the stages once they are reused
+      // below (or the CTA exits): wait, bounded, for every copied use the
+      // consumers did not see complete.  Normally none (every issued use is
+      // consumed); after an abort at most the last kStages.
       const uint32_t nc = s_cur.n_copied;
-      for (uint32_t j = nc > (uint32_t)kStages ? nc - kStages : 0u; j < nc; ++j) {
+      uint32_t j = nc > (uint32_t)kStages ? nc - kStages : 0u;
+      if (!*S.abort && j < n) j = n;
+      for (; j < nc; ++j) {
         const uint32_t bar = smem_addr(&S.full[j % kStages]);
         const long long t0 = clock64();
         while (!mbar_try_wait(bar, (j / kStages) & 1u) && clock64() - t0 < (1LL << 30)) {
@@ -1272,6 +1377,8 @@ struct Step {
     stamp(trace, 5);
     reduce_phase(p, S);
     stamp(trace, 6);
+    if (trace && tid == 0) trace[17] = (unsigned long long)clock64();
+    __syncwarp();
   }
 };
 

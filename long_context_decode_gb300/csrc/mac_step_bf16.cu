@@ -5,7 +5,7 @@ namespace mac {
 cudaError_t launch_step_bf16(const StepParams &p, int grid, cudaStream_t s) {
   return launch_step_t<uint16_t>(p, grid, s);
 }
-int step_occupancy_bf16(int G, bool paged, int n_heads, int n_units, int K) {
-  return occupancy_t<uint16_t>(G, paged, n_heads, n_units, K);
+int step_occupancy_bf16(int G, bool paged, int B, int Hq, int Hkv, int K) {
+  return occupancy_t<uint16_t>(G, paged, B, Hq, Hkv, K);
 }
 }  // namespace mac

@@ -8,9 +8,9 @@
 namespace mac {
 
 template <typename T, int G, bool PAGED>
-static cudaError_t prepare_step(int n_heads, int n_units, int K, size_t *smem) {
+static cudaError_t prepare_step(int B, int Hq, int Hkv, int K, size_t *smem) {
   using S = Step<T, G, PAGED>;
-  *smem = S::smem_bytes(n_heads, n_units, K);
+  *smem = S::smem_bytes(B, Hq, Hkv, K);
   static size_t limit[64] = {0};  // per device: dynamic shared memory limit set on the kernel
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -37,7 +37,7 @@ static cudaError_t prepare_step(int n_heads, int n_units, int K, size_t *smem) {
 template <typename T, int G, bool PAGED>
 static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) {
   size_t smem = 0;
-  cudaError_t e = prepare_step<T, G, PAGED>(p.B * p.Hq, p.B * p.Hkv, p.K, &smem);
+  cudaError_t e = prepare_step<T, G, PAGED>(p.B, p.Hq, p.Hkv, p.K, &smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -53,9 +53,9 @@ static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) 
 }
 
 template <typename T, int G, bool PAGED>
-static int occupancy_g(int n_heads, int n_units, int K) {
+static int occupancy_g(int B, int Hq, int Hkv, int K) {
   size_t smem = 0;
-  if (prepare_step<T, G, PAGED>(n_heads, n_units, K, &smem) != cudaSuccess) return 0;
+  if (prepare_step<T, G, PAGED>(B, Hq, Hkv, K, &smem) != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<T, G, PAGED>, kThreads, smem) !=
       cudaSuccess)
@@ -75,11 +75,11 @@ static cudaError_t launch_step_t(const StepParams &p, int grid, cudaStream_t s) 
 }
 
 template <typename T>
-static int occupancy_t(int G, bool paged, int n_heads, int n_units, int K) {
+static int occupancy_t(int G, bool paged, int B, int Hq, int Hkv, int K) {
   switch (G) {
-    case 1: return paged ? occupancy_g<T, 1, true>(n_heads, n_units, K) : occupancy_g<T, 1, false>(n_heads, n_units, K);
-    case 2: return paged ? occupancy_g<T, 2, true>(n_heads, n_units, K) : occupancy_g<T, 2, false>(n_heads, n_units, K);
-    case 4: return paged ? occupancy_g<T, 4, true>(n_heads, n_units, K) : occupancy_g<T, 4, false>(n_heads, n_units, K);
+    case 1: return paged ? occupancy_g<T, 1, true>(B, Hq, Hkv, K) : occupancy_g<T, 1, false>(B, Hq, Hkv, K);
+    case 2: return paged ? occupancy_g<T, 2, true>(B, Hq, Hkv, K) : occupancy_g<T, 2, false>(B, Hq, Hkv, K);
+    case 4: return paged ? occupancy_g<T, 4, true>(B, Hq, Hkv, K) : occupancy_g<T, 4, false>(B, Hq, Hkv, K);
     default: return 0;
   }
 }
