@@ -20,9 +20,9 @@ namespace mac {
 // work decomposition constants
 // ---------------------------------------------------------------------------
 constexpr int kHeadDim = 128;           // supported head dimension
-constexpr int kThreads = 256;           // threads per CTA (8 warps)
-constexpr int kConsumers = kThreads;
-constexpr int kWarps = kThreads / 32;
+constexpr int kConsumers = 256;         // consumer threads per CTA (8 warps) ...
+constexpr int kThreads = kConsumers + 32;  // ... plus one producer warp
+constexpr int kWarps = kConsumers / 32;  // consumer warps
 constexpr int kStages = 4;              // stage buffers in the TMA ring
 constexpr int kStageBytes = 32768;      // bytes per stage (K+V tile, or ring rows)
 constexpr int kPartStride = kHeadDim + 4;  // floats per (piece, head) partial: o[d], m, l, 0, 0
@@ -216,6 +216,23 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       : "memory");
 }
 
+// Same, with an L2 eviction policy (streams read once per step: K/V rows,
+// ring rows) so they do not push out what is reused.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar, unsigned long long policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ unsigned long long l2_evict_first_policy() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // Barrier of the CTA's consumer threads (all of them).  bar.sync counts
 // whole warps, so each warp first reconverges: a lane still inside a
 // single-lane region must not be counted as arrived.
@@ -241,6 +258,10 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 __device__ __forceinline__ void set_status(uint32_t *ctl, uint32_t bits) { atomicOr(ctl, bits); }
+
+// 64-bit division, kept out of line: the inlined routine is long and only
+// the rare large-size paths need it.
+__device__ __noinline__ static long long div_s64(long long a, long long b) { return a / b; }
 
 __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;

@@ -1,52 +1,46 @@
 // mac_step.cuh -- one persistent kernel per decode step (cooperative launch,
-// one CTA per SM).
+// one CTA per SM): eight consumer warps and one producer warp.
 //
 //   Phase M (Match, [MAC] "Match (2)"/"Match (3)", K1): the pre-RoPE query
-//   rings of all (request, head) pairs form one contiguous array of B*Hq*K
-//   rows; CTA c streams rows [c*N/P, (c+1)*N/P) through shared memory and
-//   computes each candidate's squared distance to its head's current query.
-//   Eight lanes share a row; each sums (a-b)^2 of its 16 elements in a
-//   pairwise tree (a-b of two bf16 values is exact in fp32) and the eight
-//   finish the tree with shuffles, so a distance carries at most 8 roundings
-//   of non-negative terms.  The pages' expansion |a|^2+|b|^2-2a.b cancels
-//   badly for close pairs and is not used.  A head's best (distance,
-//   position) is combined across CTAs with a 64-bit atomic max of a packed
-//   key, a total order (smaller distance, then more recent position), so the
-//   result does not depend on scheduling.
-//
-//   Phase A (Complete, K2, part 1): the last r tokens of every unit (request,
-//   kv head) are attended by every head whatever the match says (each head's
-//   band starts at or before m-r+1), so they are streamed right after the
-//   match slice, before the grid barrier.
+//   rings of all (request, head) pairs form B*Hq*K rows, cut into chunks of at
+//   most a stage (never across heads) dealt round-robin to the CTAs, so every
+//   CTA reads every part of the memory.  Eight lanes share a row; each sums
+//   (a-b)^2 of its 16 elements in a pairwise tree (a-b of two bf16 values is
+//   exact in fp32) and the eight finish the tree with shuffles, so a distance
+//   carries at most 8 roundings of non-negative terms.  The pages' expansion
+//   |a|^2+|b|^2-2a.b cancels badly for close pairs and is not used.  Each warp
+//   combines its rows' best (distance, position) into the head's minimum with
+//   a 64-bit atomic max of a packed key, a total order (smaller distance, then
+//   more recent position), so the result does not depend on scheduling.
 //
 //   Grid barrier; every CTA turns the minima into decisions ([MAC] K1: hit
 //   iff the smallest squared distance is strictly below thr^2) and lays out
-//   the band [s, m-r] of every unit (s = first token any head of the unit
-//   needs: p-r+1 for a hit at p, 1 for a miss).  Phase B (K2, part 2)
-//   attends the bands; a head whose band starts later than s masks the
-//   tokens before its own start ([MAC] "GQA intra-group skew").
+//   the band [s, m-r] of every unit (request, kv head), s = the first token
+//   any head of the unit needs (p-r+1 for a hit at p, 1 for a miss).
+//
+//   Complete (K2): tail pieces first -- the last r tokens of every unit, which
+//   every head attends whatever the match says, so the producer streams them
+//   into the stages during the match -- then band pieces; a head whose band
+//   starts after s masks the tokens before its own start ([MAC] "GQA
+//   intra-group skew").
 //
 //   Grid barrier; phase R: per (request, head), the piece partials are merged
 //   in token order after the cached rectified summary of a hit head: the band
 //   pieces give AS_{1:m-r}, the tail pieces then give the output.
 //
-// Work balance ("span-balanced" flash decode): in phases A and B the tokens
-// of all units are laid end to end and cut into one contiguous span per CTA,
-// so every CTA streams the same number of tokens however the band lengths
-// are spread.  A span meets a few units; each meeting (a piece) leaves one
-// partial summary (running max, sum, weighted values; base-2 log domain,
-// [MAC] "Complete").  A GQA group loads each K/V tile once for its G query
-// heads.  Full attention (and ring seeding) run phases A and B with s = 1 and
-// no match; the pieces are then the same as those of a decode step whose
-// heads all miss, which makes such a step bitwise equal to full attention.
+// Work balance ("span-balanced" flash decode): the tail tokens of all units
+// are laid end to end and cut into one contiguous span per CTA, and so are
+// the band tokens; a span meets a few units, and each meeting (a piece)
+// leaves one partial summary (running max, sum, weighted values; base-2 log
+// domain, [MAC] "Complete").  A GQA group loads each K/V tile once for its G
+// query heads.  Full attention (and ring seeding) run the same pieces with
+// s = 1 and no match, so a decode step whose heads all miss is bitwise equal
+// to full attention.
 //
 // Streaming: one ring of kStages shared-memory stages filled with 1-D TMA
-// bulk copies and drained by the CTA's 8 warps.  Every warp releases a stage
-// with an acquire-release add on the stage's counter; the warp whose release
-// completes the count refills the stage with the next use of the CTA's
-// sequence (issue cursor in shared memory, taken in order).  No thread waits
-// for another warp to refill, and every wait is bounded and reports
-// MAC_DEV_WAIT_TIMEOUT instead of hanging.
+// bulk copies by the producer warp (full/empty mbarriers) and drained by the
+// consumer warps.  Every wait is bounded and reports MAC_DEV_WAIT_TIMEOUT
+// instead of hanging.
 #pragma once
 
 #include "mac_common.cuh"
@@ -94,13 +88,8 @@ __device__ __forceinline__ void unpack16x2<float>(const uint4 &u, float2 *f) {
   f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
 }
 
-constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x >> 1); }
 
-// A position in the ring rows of a match slice: head bh (global row
-// bh * K + slot); the slice ends before slot_end of head bh_last.
-struct MatchPos {
-  int bh, slot, bh_last, slot_end;
-};
+constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x >> 1); }
 
 // Running maxima start here (finite, so that empty states never produce
 // inf - inf) and are raised only when a score exceeds them by kLazy (base-2
@@ -115,7 +104,7 @@ struct Step {
   static constexpr int kTileTok = kStageBytes / (2 * kRowBytes);  // 64 (bf16) / 32 (fp32)
   static constexpr int kTPG = kTileTok / 32;                      // tokens per lane group per tile
   static constexpr int kMatchRows = kStageBytes / kRowBytes;      // ring rows per stage
-  static constexpr int kRPG = kMatchRows / 32;                     // rows per lane group per match chunk
+  static constexpr int kRPG = kMatchRows / 32;                    // rows per lane group per match chunk
   static constexpr int kPer = 16 / (int)sizeof(T);                // elements per 16-byte piece
   static constexpr int kNP = 16 / kPer;                           // pieces per lane (16 dims)
   static constexpr int kPairs = 8;                                // float2 pairs per lane (16 dims)
@@ -123,65 +112,52 @@ struct Step {
   static constexpr int kScat = ilog2c(kV);                        // reduce-scatter levels
   static constexpr int kPlain = 3 - kScat;                        // plain butterfly levels after them
   static constexpr int kQBytes = G * kRowBytes;
-  static constexpr int kOutPer = (G * kHeadDim + kThreads - 1) / kThreads;
+  static constexpr int kOutPer = (G * kHeadDim + kConsumers - 1) / kConsumers;
   static_assert(kV <= 8, "one score per lane of a group at most");
 
   // dynamic shared memory layout
   static constexpr size_t kOffQ = (size_t)kStages * kStageBytes;
-  static constexpr size_t kOffBar = kOffQ + (size_t)kStages * kQBytes;
-  static constexpr size_t kOffRedO = kOffBar + 64;
+  static constexpr size_t kOffBar = kOffQ + (size_t)kStages * kQBytes;     // full[kStages], empty[kStages]
+  static constexpr size_t kOffQrot = kOffBar + 128;                        // [G][d] f32
+  static constexpr size_t kOffRedO = kOffQrot + 4 * (size_t)G * kHeadDim;  // [kWarps][4][G][d]
   static constexpr size_t kOffRedL = kOffRedO + 4 * (size_t)kWarps * 4 * G * kHeadDim;
   static constexpr size_t kOffRedM = kOffRedL + 4 * (size_t)kWarps * 4 * G;
   static constexpr size_t kOffX = kOffRedM + 4 * (size_t)kWarps * G;
   static_assert(kOffBar % 8 == 0 && kOffX % 8 == 0, "alignment");
 
-  // phase M: ring positions of the requests a match slice touches; after the
-  // decisions: the matched position of every head (-1: miss)
-  __host__ __device__ static int x_ints(int n_heads, int K) {
-    const int stage = 2 * K < kPosStage ? 2 * K : kPosStage;
-    return n_heads > stage ? n_heads : stage;
+  // X: during the match the ring positions of all requests ([B][K], when
+  // they fit), afterwards the matched position of every head (-1: miss)
+  __host__ __device__ static int x_ints(int B, int Hq, int K) {
+    const long long pos = (long long)B * K;
+    const int stage = pos <= kPosStage ? (int)pos : 0;
+    return B * Hq > stage ? B * Hq : stage;
   }
-  __host__ __device__ static size_t off_units(int n_heads, int K) {
-    return (kOffX + 4 * (size_t)x_ints(n_heads, K) + 7) / 8 * 8;
+  __host__ __device__ static size_t off_units(int B, int Hq, int K) {
+    return (kOffX + 4 * (size_t)x_ints(B, Hq, K) + 7) / 8 * 8;
   }
   // + offsets of the tail and band segments (int64, n_units + 1 each), query
   // position and band start of every unit (int32), then the RoPE cos/sin
   // table of every request when there are at most kRopeTab of them
-  __host__ __device__ static size_t off_rope(int n_heads, int n_units, int K) {
-    return (off_units(n_heads, K) + 16 * ((size_t)n_units + 1) + 8 * (size_t)n_units + 7) / 8 * 8;
+  __host__ __device__ static size_t off_rope(int B, int Hq, int Hkv, int K) {
+    const size_t U = (size_t)B * Hkv;
+    return (off_units(B, Hq, K) + 16 * (U + 1) + 8 * U + 7) / 8 * 8;
   }
   __host__ __device__ static size_t smem_bytes(int B, int Hq, int Hkv, int K) {
     const size_t tab = B <= kRopeTab ? 8 * (size_t)B * (kHeadDim / 2) : 0;
-    return off_rope(B * Hq, B * Hkv, K) + tab;
+    return off_rope(B, Hq, Hkv, K) + tab;
   }
-
-  // Issue cursor: the next use of the CTA's stage sequence (match chunks,
-  // then the tiles of the CTA's pieces).  Only the thread issuing use n
-  // touches it, after the issue of use n - 1 has published n.
-  // C_PEND: the tile sequence of phase 0 comes next but its layout may not
-  // be ready yet (resolved by the first issue after the layout).
-  enum { C_MATCH = 0, C_TILES = 1, C_END = 2, C_PEND = 3 };
-  struct Cursor {
-    uint32_t n;          // next use to issue
-    uint32_t n_copied;   // uses issued with their copies (all of them unless aborted)
-    int kind;
-    int ph;              // phase of the tile sequence: 0 tails, 1 bands
-    int cont;            // go on from phase 0 into phase 1 (full attention)
-    int u, lo, hi, first;
-    MatchPos mp;         // match: next chunk
-    int64_t tile, tile_last;
-    int64_t g0, g1;      // span of this CTA in phase ph
-  };
 
   struct Smem {
     uint8_t *stage;     // [kStages][kStageBytes]
     uint8_t *qbuf;      // [kStages][G][d]: pre-RoPE query rows of a piece's unit
-    uint64_t *full;     // [kStages]
+    uint64_t *full;     // [kStages]: the stage's copy has landed
+    uint64_t *empty;    // [kStages]: every consumer warp is done with the stage
+    float *qrot;        // [G][d]: rotated, scaled query of the current piece
     float *red_o;       // [kWarps][4][G][d]
     float *red_l;       // [kWarps * 4][G]
     float *red_m;       // [kWarps][G]
     int32_t *X;
-    int nx;
+    bool pos_staged;    // X holds the ring positions during the match
     int64_t *offA;      // [n_units + 1]: first global index of each unit's tail segment
     int64_t *offB;      // [n_units + 1]: same for the band segments
     int64_t *spanA;     // [grid + 1]: CTA c's tail span is [spanA[c], spanA[c+1])
@@ -189,10 +165,10 @@ struct Step {
     int32_t *u_pos;     // [n_units]: position of the unit's query (RoPE angle pos - 1)
     int32_t *u_s;       // [n_units]: first band token of the unit
     float2 *rope;       // [B][d/2]: cos, sin of the query's rotation angles (B <= kRopeTab), or null
-    uint32_t *cnt;      // [kStages]: releases of the stage's current use
     int *mask;          // [kStages]: valid 16-token pages of the tile in the stage
     volatile int *abort;
-    Cursor *cur;
+    volatile int *ready;  // layouts known to the producer: 1 tails (and bands in full mode), 2 bands
+    volatile uint32_t *issued;  // uses the producer copied (published at its end)
   };
 
   struct Piece {
@@ -245,7 +221,7 @@ struct Step {
   // common case: 64-bit division is a long serial routine)
   __device__ static int64_t part_of(int c, int64_t total, int P) {
     if (total < (1LL << 23)) return (int64_t)((uint32_t)c * (uint32_t)total / (uint32_t)P);
-    return (int64_t)c * total / P;
+    return div_s64((int64_t)c * total, P);
   }
   __device__ static const int64_t *spans(const Smem &S, int ph) { return ph ? S.spanB : S.spanA; }
 
@@ -289,47 +265,29 @@ struct Step {
     return false;
   }
 
-  // Exclusive prefix of the segment lengths of phase ph over all units
-  // (block-wide scan; ends with a __syncthreads).
-  __device__ static void layout_phase(const StepParams &p, const Smem &S, int ph) {
-    __shared__ long long wsum[kWarps];
+  // Exclusive prefix of the segment lengths of phase ph over all units and
+  // the CTA span boundaries, by one warp (warp-level scans, no CTA barrier;
+  // the caller makes the result visible to the other warps).
+  __device__ static void layout_warp(const StepParams &p, const Smem &S, int ph) {
     int64_t *off = ph ? S.offB : S.offA;
-    const int U = p.B * p.Hkv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int per = (U + kThreads - 1) / kThreads;
-    const int beg = min(tid * per, U), end = min(beg + per, U);
-    long long run = 0;
-    for (int u = beg; u < end; ++u) {
-      run += seg_len(p, S, ph, u);
-      off[u + 1] = run;
-    }
-    long long x = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(kFull, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) wsum[warp] = x;
-    block_sync();
-    if (warp == 0) {
-      long long w = lane < kWarps ? wsum[lane] : 0;
+    const int U = p.B * p.Hkv, lane = threadIdx.x & 31;
+    long long carry = 0;
+    for (int base = 0; base < U; base += 32) {
+      const int u = base + lane;
+      long long x = u < U ? (long long)seg_len(p, S, ph, u) : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(kFull, w, o);
-        if (lane >= o) w += y;
+        const long long y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
       }
-      if (lane < kWarps) wsum[lane] = w;
+      if (u < U) off[u + 1] = carry + x;
+      carry += __shfl_sync(kFull, x, 31);
     }
-    block_sync();
-    const long long excl = x - run + (warp > 0 ? wsum[warp - 1] : 0);
-    for (int u = beg; u < end; ++u) off[u + 1] += excl;
-    if (tid == 0) off[0] = 0;
-    block_sync();
+    if (lane == 0) off[0] = 0;
     // span c = global indices [c*total/P, (c+1)*total/P)
     int64_t *span = ph ? S.spanB : S.spanA;
-    const int64_t total = off[U];
-    for (int c = tid; c <= (int)gridDim.x; c += kThreads) span[c] = part_of(c, total, gridDim.x);
-    block_sync();
+    for (int c = lane; c <= (int)gridDim.x; c += 32) span[c] = part_of(c, carry, gridDim.x);
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------------
@@ -396,182 +354,107 @@ struct Step {
     mbar_expect_tx(bar, bytes);
     if (with_q) {
       const uint8_t *q = (const uint8_t *)p.q;
-      for (int hh = 0; hh < G; ++hh) {
-        const int64_t bh = (int64_t)b * p.Hq + g * G + hh;
-        bulk_g2s(smem_addr(S.qbuf + (size_t)st * kQBytes + hh * kRowBytes),
-                 q + (size_t)(bh * p.q_stride + p.q_offset) * sizeof(T), kRowBytes, bar);
+      const int64_t bh0 = (int64_t)b * p.Hq + g * G;
+      if (p.q_stride == kHeadDim && p.q_offset == 0) {  // the group's G rows are contiguous
+        bulk_g2s(smem_addr(S.qbuf + (size_t)st * kQBytes), q + (size_t)bh0 * kRowBytes, kQBytes, bar);
+      } else {
+        for (int hh = 0; hh < G; ++hh)
+          bulk_g2s(smem_addr(S.qbuf + (size_t)st * kQBytes + hh * kRowBytes),
+                   q + (size_t)((bh0 + hh) * p.q_stride + p.q_offset) * sizeof(T), kRowBytes, bar);
       }
     }
+    const unsigned long long pol = l2_evict_first_policy();
     if (!PAGED) {
       if (msk == 0) return;
       const size_t off = (((size_t)b * p.Hkv + g) * (size_t)p.kv.capacity + (size_t)(ra[0] - 1)) * kRowBytes;
       const uint32_t n = (uint32_t)(rz[0] - ra[0] + 1) * kRowBytes;
       const uint32_t dst = (uint32_t)(ra[0] - t0 - 1) * kRowBytes;
-      bulk_g2s(smem_addr(kbuf + dst), (const uint8_t *)p.kv.k + off, n, bar);
-      bulk_g2s(smem_addr(vbuf + dst), (const uint8_t *)p.kv.v + off, n, bar);
+      bulk_g2s_hint(smem_addr(kbuf + dst), (const uint8_t *)p.kv.k + off, n, bar, pol);
+      bulk_g2s_hint(smem_addr(vbuf + dst), (const uint8_t *)p.kv.v + off, n, bar, pol);
     } else {
       for (int pg = 0; pg < kTileTok / 16; ++pg) {
         if (pid[pg] < 0) continue;
         const size_t off = (((size_t)pid[pg] * p.Hkv + g) * 16 + (size_t)((ra[pg] - 1) % 16)) * kRowBytes;
         const uint32_t n = (uint32_t)(rz[pg] - ra[pg] + 1) * kRowBytes;
         const uint32_t dst = (uint32_t)(ra[pg] - t0 - 1) * kRowBytes;
-        bulk_g2s(smem_addr(kbuf + dst), (const uint8_t *)p.kv.k + off, n, bar);
-        bulk_g2s(smem_addr(vbuf + dst), (const uint8_t *)p.kv.v + off, n, bar);
+        bulk_g2s_hint(smem_addr(kbuf + dst), (const uint8_t *)p.kv.k + off, n, bar, pol);
+        bulk_g2s_hint(smem_addr(vbuf + dst), (const uint8_t *)p.kv.v + off, n, bar, pol);
       }
     }
   }
 
-  // Rows of the next match chunk at mp: within one head, at most kMatchRows.
-  __device__ static int match_rows(const MatchPos &mp, int K) {
-    int e = mp.slot + kMatchRows;
-    if (e > K) e = K;
-    if (mp.bh == mp.bh_last && e > mp.slot_end) e = mp.slot_end;
-    return e - mp.slot;
-  }
-  // advance past a chunk of n rows; false when the slice is done
-  __device__ static bool match_next(MatchPos &mp, int n, int K) {
-    mp.slot += n;
-    if (mp.slot >= K) {
-      ++mp.bh;
-      mp.slot = 0;
+  // Match chunk j: head j / cph, rows [(j % cph) * kMatchRows, +rows) of its
+  // ring, cph = chunks per head (chunks never cross heads).
+  __device__ static int chunks_per_head(int K) { return (K + kMatchRows - 1) / kMatchRows; }
+
+  // Bounded spin of the producer lane on a shared flag set by a consumer.
+  __device__ static bool wait_ready(const StepParams &p, const Smem &S, int level) {
+    const long long t0 = clock64();
+    while (*S.ready < level) {
+      if (*S.abort) return false;
+      if (clock64() - t0 > (1LL << 31)) {
+        set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
+        *S.abort = 1;
+        return false;
+      }
     }
-    return mp.bh < mp.bh_last || (mp.bh == mp.bh_last && mp.slot < mp.slot_end);
+    __threadfence_block();
+    return true;
   }
-  // CTA c's slice of the B*Hq*K ring rows: [c*N/P, (c+1)*N/P); false if empty
-  __device__ static bool match_slice(const StepParams &p, MatchPos *mp) {
-    const int64_t N = (int64_t)p.B * p.Hq * p.K;
-    const int64_t s0 = part_of(blockIdx.x, N, gridDim.x), s1 = part_of(blockIdx.x + 1, N, gridDim.x);
-    if (s0 >= s1) return false;
-    if (s1 < (1LL << 31)) {
-      const uint32_t a = (uint32_t)s0, z = (uint32_t)(s1 - 1), K = (uint32_t)p.K;
-      mp->bh = (int)(a / K);
-      mp->slot = (int)(a % K);
-      mp->bh_last = (int)(z / K);
-      mp->slot_end = (int)(z % K) + 1;
-    } else {
-      mp->bh = (int)(s0 / p.K);
-      mp->slot = (int)(s0 % p.K);
-      mp->bh_last = (int)((s1 - 1) / p.K);
-      mp->slot_end = (int)((s1 - 1) % p.K) + 1;
+
+  // Producer lane: wait for stage use n to be free, then arm its full barrier.
+  __device__ static bool acquire_stage(const StepParams &p, const Smem &S, uint32_t n) {
+    if (!mbar_wait_bounded(smem_addr(&S.empty[n % kStages]), ((n / kStages) & 1u) ^ 1u, S.abort)) {
+      if (!*S.abort) set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
+      *S.abort = 1;
+      return false;
     }
     return true;
   }
 
-  __device__ static void cursor_piece(Cursor &c, const Piece &pc) {
-    c.kind = C_TILES;
-    c.u = pc.u;
-    c.lo = pc.lo;
-    c.hi = pc.hi;
-    c.tile = (pc.lo - 1) / kTileTok;
-    c.tile_last = (pc.hi - 1) / kTileTok;
-    c.first = 1;
-  }
-
-  // Put the cursor on the first tile of this CTA's pieces in phase ph (then
-  // phase 1 when c.cont), or end it.
-  __device__ static void cursor_phase(const StepParams &p, const Smem &S, Cursor &c, int ph) {
-    const int U = p.B * p.Hkv;
-    for (;; ++ph) {
-      const int64_t *off = offs(S, ph);
-      c.ph = ph;
-      c.g0 = spans(S, ph)[blockIdx.x];
-      c.g1 = spans(S, ph)[blockIdx.x + 1];
-      Piece pc;
-      if (c.g0 < c.g1 && find_piece(p, S, ph, unit_of(off, U, c.g0), c.g0, c.g1, &pc)) {
-        cursor_piece(c, pc);
-        return;
-      }
-      if (ph != 0 || !c.cont) {
-        c.kind = C_END;
-        return;
-      }
-    }
-  }
-
-  __device__ static void cursor_next(const StepParams &p, const Smem &S, Cursor &c) {
-    if (c.kind == C_MATCH) {
-      if (!match_next(c.mp, match_rows(c.mp, p.K), p.K)) c.kind = C_PEND;
-      return;
-    }
-    c.first = 0;
-    if (++c.tile <= c.tile_last) return;
-    Piece pc;
-    if (find_piece(p, S, c.ph, c.u + 1, c.g0, c.g1, &pc)) {
-      cursor_piece(c, pc);
-      return;
-    }
-    if (c.ph == 0 && c.cont) {
-      cursor_phase(p, S, c, 1);
-      return;
-    }
-    c.kind = C_END;
-  }
-
-  // Issue the cursor's use into its stage (free by construction), advance
-  // and publish the next use index.
-  __device__ static void issue_current(const StepParams &p, const Smem &S) {
-    Cursor &c = *S.cur;
-    if (c.kind == C_PEND) {
-      cursor_phase(p, S, c, 0);
-      if (c.kind == C_END) return;
-    }
-    const int st = c.n % kStages;
-    const bool go = !*S.abort;
-    if (c.kind == C_MATCH) {
-      const int rows = match_rows(c.mp, p.K);
-      if (rows < 1 || c.mp.bh >= p.B * p.Hq) {
-        set_status(p.ctl, MAC_DEV_BAD_COPY);
-        mbar_arrive(smem_addr(&S.full[st]));
-      } else if (go) {
-        const uint32_t bytes = (uint32_t)rows * kRowBytes;
+  // The whole copy sequence of this CTA, in the order the consumers use it:
+  // match chunks (decode), tail tiles, band tiles.  Run by one lane.
+  __device__ static void producer(const StepParams &p, const Smem &S) {
+    const int P = gridDim.x, U = p.B * p.Hkv;
+    const bool decode = p.mode == MODE_DECODE;
+    const unsigned long long pol = l2_evict_first_policy();
+    uint32_t n = 0;
+    if (decode) {
+      const int cph = chunks_per_head(p.K);
+      const int nc = p.B * p.Hq * cph;
+      for (int j = blockIdx.x; j < nc; j += P, ++n) {
+        if (!acquire_stage(p, S, n)) break;
+        const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
+        const int rows = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
+        const int st = n % kStages;
         const uint32_t bar = smem_addr(&S.full[st]);
-        mbar_expect_tx(bar, bytes);
-        bulk_g2s(smem_addr(S.stage + (size_t)st * kStageBytes),
-                 (const uint8_t *)p.ring_q + ((size_t)c.mp.bh * p.K + c.mp.slot) * kRowBytes, bytes, bar);
+        mbar_expect_tx(bar, (uint32_t)rows * kRowBytes);
+        bulk_g2s_hint(smem_addr(S.stage + (size_t)st * kStageBytes),
+                      (const uint8_t *)p.ring_q + ((size_t)bh * p.K + slot0) * kRowBytes,
+                      (uint32_t)rows * kRowBytes, bar, pol);
       }
-    } else if (go) {
-      issue_tile(p, S, st, c.u, c.lo, c.hi, c.tile, c.first != 0);
     }
-    if (go) c.n_copied = c.n + 1;
-    cursor_next(p, S, c);
-    __threadfence_block();
-    *(volatile uint32_t *)&c.n = c.n + 1;
-  }
-
-  // Issue use `target` (by the warp whose release freed its stage): waits,
-  // bounded, until the issue of use target - 1 has been published.
-  __device__ static void issue_use(const StepParams &p, const Smem &S, uint32_t target) {
-    volatile Cursor *vc = S.cur;
-    const long long t0 = clock64();
-    for (;;) {
-      if (vc->kind == C_END) return;
-      if (vc->n == target) break;
-      if (*S.abort) return;
-      if (clock64() - t0 > (1LL << 31)) {
-        set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
-        *S.abort = 1;
-        return;
+    for (int ph = 0; ph < 2 && !*S.abort; ++ph) {
+      if (!wait_ready(p, S, ph == 1 && decode ? 2 : 1)) break;
+      const int64_t *off = offs(S, ph);
+      const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
+      if (g0 >= g1) continue;
+      Piece pc;
+      int u = unit_of(off, U, g0);
+      while (!*S.abort && find_piece(p, S, ph, u, g0, g1, &pc)) {
+        const int64_t t0 = (pc.lo - 1) / kTileTok, t1 = (pc.hi - 1) / kTileTok;
+        for (int64_t t = t0; t <= t1; ++t, ++n) {
+          if (!acquire_stage(p, S, n)) break;
+          issue_tile(p, S, n % kStages, pc.u, pc.lo, pc.hi, t, t == t0);
+        }
+        u = pc.u + 1;
       }
     }
     __threadfence_block();
-    if (S.cur->kind == C_END) return;
-    issue_current(p, S);
+    *S.issued = n;
   }
 
-  // Release stage use n (every warp, once); the last warp to release it
-  // refills the stage with use n + kStages.
-  __device__ static void release(const StepParams &p, const Smem &S, uint32_t n) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) {
-      const int st = n % kStages;
-      if (atom_add_acqrel_shared(smem_addr(&S.cnt[st]), 1u) == kWarps - 1) {
-        S.cnt[st] = 0;
-        issue_use(p, S, n + kStages);
-      }
-    }
-    __syncwarp();
-  }
-
+  // Consumer side of stage use n.
   __device__ static bool wait_use(const StepParams &p, const Smem &S, uint32_t n) {
     const bool ok = mbar_wait_bounded(smem_addr(&S.full[n % kStages]), (n / kStages) & 1u, S.abort);
     if (!ok && !*S.abort) {
@@ -579,6 +462,10 @@ struct Step {
       *S.abort = 1;
     }
     return ok;
+  }
+  __device__ static void release(const Smem &S, uint32_t n) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&S.empty[n % kStages]));
   }
 
   // ---------------------------------------------------------------------
@@ -613,12 +500,8 @@ struct Step {
     return D;
   }
 
-  // The best candidate of head bh over this CTA (all groups hold theirs)
-  // joins the global minimum.
-  __device__ static void flush_best(const StepParams &p, const Smem &S, int64_t bh, float bd, int bp) {
-    __shared__ float s_bd[kWarps];
-    __shared__ int s_bp[kWarps];
-    const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31;
+  // The warp's best (distance, position) joins head bh's global minimum.
+  __device__ static void flush_best(const StepParams &p, int bh, float bd, int bp) {
 #pragma unroll
     for (int off = 8; off <= 16; off <<= 1) {
       const float d2 = __shfl_xor_sync(kFull, bd, off);
@@ -628,105 +511,61 @@ struct Step {
         bp = p2;
       }
     }
-    if (lane == 0) {
-      s_bd[warp] = bd;
-      s_bp[warp] = bp;
-    }
-    consumer_sync();
-    if (ct == 0) {
-      for (int w = 1; w < kWarps; ++w)
-        if (better(s_bd[w], s_bp[w], bd, bp)) {
-          bd = s_bd[w];
-          bp = s_bp[w];
-        }
-      if (bp >= 1) atomicMax(&p.best[bh], pack_best(bd, bp));
-    }
-    consumer_sync();
+    if ((threadIdx.x & 31) == 0 && bp >= 1) atomicMax(&p.best[bh], pack_best(bd, bp));
   }
 
   __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n) {
-    MatchPos mp;
-    if (!match_slice(p, &mp)) return;
+    const int P = gridDim.x;
+    const int cph = chunks_per_head(p.K);
+    const int nc = p.B * p.Hq * cph;
     const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31, sub = lane & 7;
     const int grp = warp * 4 + (lane >> 3);  // row group: rows grp, grp + 32, ... of a chunk
-
-    // slot positions of the requests the slice touches, staged once (they
-    // are shared by all heads of a request)
-    const int b_lo = mp.bh / p.Hq, b_hi = mp.bh_last / p.Hq;
-    const bool staged = (b_hi - b_lo + 1) * p.K <= S.nx;
-    if (staged) {
-      const int cnt = (b_hi - b_lo + 1) * p.K;
-      const int32_t *src = p.ring_pos + (int64_t)b_lo * p.K;
-      for (int i = ct; i < cnt; i += kThreads) S.X[i] = src[i];
-    }
-    block_sync();
-
-    int cur = -1;
-    float bd = INFINITY;
-    int bp = -1;
-    float2 qv[kPairs];
-    int pos_lo = 1, pos_hi = 0;
-    const int32_t *rpos = p.ring_pos;
-    for (bool more = true; more; ++n) {
-      const int cnt = match_rows(mp, p.K);
-      if (mp.bh != cur) {
-        if (cur >= 0) flush_best(p, S, cur, bd, bp);
-        cur = mp.bh;
-        bd = INFINITY;
-        bp = -1;
-        const int b = cur / p.Hq;
-        const uint8_t *qrow = (const uint8_t *)p.q + (size_t)((int64_t)cur * p.q_stride + p.q_offset) * sizeof(T);
+    for (int j = blockIdx.x; j < nc; j += P, ++n) {
+      const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
+      const int cnt = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
+      const int b = bh / p.Hq;
+      // the head's query (its 16 elements per lane), loaded before the wait
+      float2 qv[kPairs];
+      const uint8_t *qrow = (const uint8_t *)p.q + (size_t)((int64_t)bh * p.q_stride + p.q_offset) * sizeof(T);
 #pragma unroll
-        for (int cc = 0; cc < kNP; ++cc)
-          unpack16x2<T>(*reinterpret_cast<const uint4 *>(qrow + cc * 128 + sub * 16), qv + cc * (kPer / 2));
-        const int64_t m = (int64_t)S.u_pos[b * p.Hkv] - p.len_sub;
-        if (len_ok(p, m)) {
-          pos_lo = m - p.K > 1 ? (int)(m - p.K) : 1;
-          pos_hi = (int)(m - 1);
-        } else {
-          pos_lo = 1;
-          pos_hi = 0;
-        }
-        rpos = staged ? S.X + (b - b_lo) * p.K : p.ring_pos + (int64_t)b * p.K;
+      for (int cc = 0; cc < kNP; ++cc)
+        unpack16x2<T>(__ldg(reinterpret_cast<const uint4 *>(qrow + cc * 128 + sub * 16)), qv + cc * (kPer / 2));
+      const int64_t m = (int64_t)S.u_pos[b * p.Hkv] - p.len_sub;
+      int pos_lo = 1, pos_hi = 0;
+      if (len_ok(p, m)) {
+        pos_lo = m - p.K > 1 ? (int)(m - p.K) : 1;
+        pos_hi = (int)(m - 1);
       }
+      const int32_t *rp = (S.pos_staged ? S.X : p.ring_pos) + (int64_t)b * p.K + slot0;
       const bool ok = wait_use(p, S, n);
       if (n == 0) stamp(cta_trace(p), 8);
-      const int32_t *rp = rpos + mp.slot;
       const uint8_t *rows = S.stage + (size_t)(n % kStages) * kStageBytes;
-      // all of the group's rows of the chunk at once (independent chains),
-      // then a tree over them; rows past the chunk read stale stage bytes and
-      // are not considered
-      {
-        float D[kRPG];
-        int ps[kRPG];
+      // all of the group's rows at once (independent chains), then a tree;
+      // rows past the chunk read stale stage bytes and are not considered
+      float D[kRPG];
+      int ps[kRPG];
 #pragma unroll
-        for (int k = 0; k < kRPG; ++k) {
-          const int i = grp + 32 * k;
-          const int ri = i < cnt ? i : cnt - 1;
-          D[k] = row_dist(rows + (size_t)ri * kRowBytes, sub, qv);
-          const int pk = rp[ri];
-          const bool valid = ok && i < cnt && pk >= pos_lo && pk <= pos_hi;
-          ps[k] = valid ? pk : -1;
-          D[k] = valid ? D[k] : INFINITY;
-        }
-#pragma unroll
-        for (int w = 1; w < kRPG; w <<= 1)
-#pragma unroll
-          for (int k = 0; k + w < kRPG; k += 2 * w)
-            if (better(D[k + w], ps[k + w], D[k], ps[k])) {
-              D[k] = D[k + w];
-              ps[k] = ps[k + w];
-            }
-        if (ps[0] >= 1 && better(D[0], ps[0], bd, bp)) {
-          bd = D[0];
-          bp = ps[0];
-        }
+      for (int k = 0; k < kRPG; ++k) {
+        const int i = grp + 32 * k;
+        const int ri = i < cnt ? i : cnt - 1;
+        D[k] = row_dist(rows + (size_t)ri * kRowBytes, sub, qv);
+        const int pk = rp[ri];
+        const bool valid = ok && i < cnt && pk >= pos_lo && pk <= pos_hi;
+        ps[k] = valid ? pk : -1;
+        D[k] = valid ? D[k] : INFINITY;
       }
-      release(p, S, n);
-      more = match_next(mp, cnt, p.K);
+#pragma unroll
+      for (int w = 1; w < kRPG; w <<= 1)
+#pragma unroll
+        for (int k = 0; k + w < kRPG; k += 2 * w)
+          if (better(D[k + w], ps[k + w], D[k], ps[k])) {
+            D[k] = D[k + w];
+            ps[k] = ps[k + w];
+          }
+      release(S, n);
+      flush_best(p, bh, D[0], ps[0]);
     }
     stamp(cta_trace(p), 9);
-    flush_best(p, S, cur, bd, bp);
   }
 
   // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.
@@ -745,39 +584,50 @@ struct Step {
         __nanosleep(32);
       }
     }
-    block_sync();
+    consumer_sync();
   }
 
   // Decisions of every head from the combined minima, then every unit's band
-  // start and the band layout (every CTA computes the same).
+  // start and the band layout (every CTA computes the same), by warp 0,
+  // which then tells the producer the band layout is ready; the other warps
+  // meanwhile start bringing the cached summaries phase R will merge into L2.
+  // Ends with a consumer barrier.
   __device__ static void decide(const StepParams &p, const Smem &S) {
-    const int tid = threadIdx.x, n_bh = p.B * p.Hq, U = p.B * p.Hkv;
-    for (int bh = tid; bh < n_bh; bh += kThreads) {
-      const int b = bh / p.Hq, u = b * p.Hkv + (bh % p.Hq) / G;
-      const int64_t m = unit_len(p, S, u);
-      const unsigned long long inv = __ldcg(&p.best[bh]);
-      int pos = -1;
-      if (inv != 0ull && len_ok(p, m) && m >= p.min_context) {
-        const unsigned long long key = ~inv;
-        const float d = __uint_as_float((uint32_t)(key >> 32));
-        if (d < p.thr2) pos = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+    const int tid = threadIdx.x, lane = tid & 31, n_bh = p.B * p.Hq, U = p.B * p.Hkv;
+    if (tid < 32) {
+      for (int bh = lane; bh < n_bh; bh += 32) {
+        const int b = bh / p.Hq, u = b * p.Hkv + (bh % p.Hq) / G;
+        const int64_t m = unit_len(p, S, u);
+        const unsigned long long inv = __ldcg(&p.best[bh]);
+        int pos = -1;
+        if (inv != 0ull && len_ok(p, m) && m >= p.min_context) {
+          const unsigned long long key = ~inv;
+          const float d = __uint_as_float((uint32_t)(key >> 32));
+          if (d < p.thr2) pos = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+        }
+        S.X[bh] = pos;
+        if (blockIdx.x == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
       }
-      S.X[bh] = pos;
-      if (blockIdx.x == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
-    }
-    block_sync();
-    for (int u = tid; u < U; u += kThreads) {
-      const int b = u / p.Hkv, g = u % p.Hkv;
-      int s = 0x7fffffff;
-      for (int hh = 0; hh < G; ++hh) {
-        const int pp = S.X[b * p.Hq + g * G + hh];
-        const int lo = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
-        s = lo < s ? lo : s;
+      __syncwarp();
+      for (int u = lane; u < U; u += 32) {
+        const int b = u / p.Hkv, g = u % p.Hkv;
+        int s = 0x7fffffff;
+        for (int hh = 0; hh < G; ++hh) {
+          const int pp = S.X[b * p.Hq + g * G + hh];
+          const int lo = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
+          s = lo < s ? lo : s;
+        }
+        S.u_s[u] = s;
       }
-      S.u_s[u] = s;
+      __syncwarp();
+      layout_warp(p, S, 1);
+      __threadfence_block();
+      if (lane == 0) *S.ready = 2;
+      __syncwarp();
     }
-    // the cached summaries phase R will merge: start bringing them into L2
-    // now, behind the band attention
+    consumer_sync();
+    // the cached summaries of this CTA's phase-R heads: into L2 now, behind
+    // the band attention
     for (int bh = blockIdx.x + (tid >> 5) * gridDim.x; bh < n_bh; bh += kWarps * gridDim.x) {
       const int pos = S.X[bh];
       if (pos >= 1 && (tid & 31) < kHeadDim * 4 / 128 + 1) {
@@ -787,12 +637,11 @@ struct Step {
         asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
       }
     }
-    block_sync();
-    layout_phase(p, S, 1);
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------------
-  // phases A and B: attention over the CTA's pieces
+  // attention over the CTA's pieces
   // ---------------------------------------------------------------------
 
   // Lane element k (0..15) of a 16-dim share: piece k / kPer, offset k % kPer.
@@ -812,56 +661,38 @@ struct Step {
     *rb = __fmul_rn(__fadd_rn(__fmul_rn(b, cs.x), __fmul_rn(a, cs.y)), scale);
   }
 
-  // R(pos) q~ * log2(e)/sqrt(d) for this lane's 16 dims of the piece's G
-  // heads, from the pre-RoPE rows that came with the piece's first tile.
-  // Both members of every rotation pair lie in the same lane (half split:
-  // dims j and j + d/2 are lane elements k and k + 8; interleaved: 2j and
-  // 2j + 1 are adjacent elements), so no lane waits for another.  Explicit
-  // roundings keep the result identical wherever it is computed.
-  __device__ static void load_query(const StepParams &p, const Smem &S, int st, int b, int64_t pos,
-                                    float2 (&q)[G][kPairs]) {
-    const int sub = threadIdx.x & 7;
-    const int mode = p.rope_mode;
-    float2 cs[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      cs[i] = make_float2(1.f, 0.f);
-      if (mode == MAC_ROPE_HALF) cs[i] = rope_cs(p, S, b, pos, lane_dim(i, sub));
-      else if (mode == MAC_ROPE_INTERLEAVED) cs[i] = rope_cs(p, S, b, pos, lane_dim(2 * i, sub) / 2);
+  // R(pos) q~ * log2(e)/sqrt(d) of the piece's G heads into shared memory,
+  // from the pre-RoPE rows that came with its first tile: one rotation pair
+  // per consumer thread (explicit roundings keep the result identical
+  // wherever it is computed).  Ends with a consumer barrier.
+  __device__ static void rotate_query(const StepParams &p, const Smem &S, int st, int b, int64_t pos) {
+    const int half = kHeadDim / 2;
+    const bool inter = p.rope_mode == MAC_ROPE_INTERLEAVED;
+    for (int i = threadIdx.x; i < G * half; i += kConsumers) {
+      const int hh = i / half, j = i % half;
+      const int ia = inter ? 2 * j : j, ib = inter ? 2 * j + 1 : j + half;
+      const void *row = S.qbuf + (size_t)st * kQBytes + hh * kRowBytes;
+      const float a = elem_f32<T>(row, ia), bb = elem_f32<T>(row, ib);
+      const float2 cs = p.rope_mode == MAC_ROPE_NONE ? make_float2(1.f, 0.f) : rope_cs(p, S, b, pos, j);
+      float ra, rb;
+      rotate_pair(a, bb, cs, p.q_scale, &ra, &rb);
+      S.qrot[hh * kHeadDim + ia] = ra;
+      S.qrot[hh * kHeadDim + ib] = rb;
+      if (!(isfinite(a) && isfinite(bb))) set_status(p.ctl, MAC_DEV_NONFINITE_Q);
     }
-    const float scale = p.q_scale;
+    consumer_sync();
+  }
+
+  // the lane's 16 dims of head hh's rotated query
+  __device__ static void query_pairs(const Smem &S, int hh, int sub, float2 (&q)[kPairs]) {
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      const uint8_t *row = S.qbuf + (size_t)st * kQBytes + hh * kRowBytes;
-      float x[16];
+    for (int c = 0; c < kNP; ++c)
 #pragma unroll
-      for (int c = 0; c < kNP; ++c) {
-        float2 e2[kPer / 2];
-        unpack16x2<T>(*reinterpret_cast<const uint4 *>(row + c * 128 + sub * 16), e2);
-#pragma unroll
-        for (int e = 0; e < kPer / 2; ++e) {
-          x[c * kPer + 2 * e] = e2[e].x;
-          x[c * kPer + 2 * e + 1] = e2[e].y;
-        }
+      for (int e4 = 0; e4 < kPer; e4 += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(S.qrot + hh * kHeadDim + piece_dim(c, sub) + e4);
+        q[(c * kPer + e4) / 2] = make_float2(v.x, v.y);
+        q[(c * kPer + e4) / 2 + 1] = make_float2(v.z, v.w);
       }
-      bool finite = true;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) finite = finite && isfinite(x[k]);
-      if (!finite) set_status(p.ctl, MAC_DEV_NONFINITE_Q);
-      float y[16];
-      if (mode == MAC_ROPE_INTERLEAVED) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rotate_pair(x[2 * i], x[2 * i + 1], cs[i], scale, &y[2 * i], &y[2 * i + 1]);
-      } else if (mode == MAC_ROPE_HALF) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) rotate_pair(x[i], x[i + 8], cs[i], scale, &y[i], &y[i + 8]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) y[k] = __fmul_rn(x[k], scale);
-      }
-#pragma unroll
-      for (int i = 0; i < kPairs; ++i) q[hh][i] = make_float2(y[2 * i], y[2 * i + 1]);
-    }
   }
 
   // v[i] (i = token slot * G + head, partial dot products of the lane's 16
@@ -904,7 +735,7 @@ struct Step {
       const int lh = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
       lo_mine = lh > lo_mine ? lh : lo_mine;
     }
-    float2 q[G][kPairs], o[G][kPairs];
+    float2 o[G][kPairs];
     float mrun[G];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
@@ -921,26 +752,31 @@ struct Step {
       const bool ok = wait_use(p, S, n);
       if (k == 0) {
         stamp(trace, ph ? 13 : 11);
-        load_query(p, S, st, b, S.u_pos[pc.u], q);
+        rotate_query(p, S, st, b, S.u_pos[pc.u]);
       }
       const uint8_t *kb = S.stage + (size_t)st * kStageBytes;
       const uint8_t *vb = kb + kStageBytes / 2;
       const int t0 = (int)((tile0 + k) * kTileTok);
       // partial scores of the group's kTPG tokens for the G heads
-      float v[kV];
+      float2 kf[kTPG][kPairs];
 #pragma unroll
       for (int tt = 0; tt < kTPG; ++tt) {
         const int row = tt * 32 + warp * 4 + lg;
-        float2 kf[kPairs];
 #pragma unroll
         for (int c = 0; c < kNP; ++c)
           unpack16x2<T>(*reinterpret_cast<const uint4 *>(kb + row * kRowBytes + c * 128 + sub * 16),
-                        kf + c * (kPer / 2));
+                        kf[tt] + c * (kPer / 2));
+      }
+      float v[kV];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          float2 acc = __fmul2_rn(q[hh][0], kf[0]);
+      for (int hh = 0; hh < G; ++hh) {
+        float2 q[kPairs];
+        query_pairs(S, hh, sub, q);
 #pragma unroll
-          for (int i = 1; i < kPairs; ++i) acc = __ffma2_rn(q[hh][i], kf[i], acc);
+        for (int tt = 0; tt < kTPG; ++tt) {
+          float2 acc = __fmul2_rn(q[0], kf[tt][0]);
+#pragma unroll
+          for (int i = 1; i < kPairs; ++i) acc = __ffma2_rn(q[i], kf[tt][i], acc);
           v[tt * G + hh] = acc.x + acc.y;
         }
       }
@@ -998,7 +834,7 @@ struct Step {
           for (int i = 0; i < kPairs; ++i) o[hh][i] = __ffma2_rn(w2, vf[i], o[hh][i]);
         }
       }
-      release(p, S, n);
+      release(S, n);
     }
     stamp(trace, ph ? 14 : 12);
     epilogue(p, S, o, mrun, m_mine, l_mine, dst);
@@ -1065,7 +901,7 @@ struct Step {
 #pragma unroll
     for (int j = 0; j < kOutPer; ++j) {
       acc[j] = 0.f;
-      const int e = tid + j * kThreads;
+      const int e = tid + j * kConsumers;
       if (e < G * kHeadDim) {
         float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1075,7 +911,7 @@ struct Step {
     }
 #pragma unroll
     for (int j = 0; j < kOutPer; ++j) {
-      const int e = tid + j * kThreads;
+      const int e = tid + j * kConsumers;
       if (e < G * kHeadDim) dst[(e / kHeadDim) * kPartStride + e % kHeadDim] = acc[j];
     }
     if (warp == 0) {
@@ -1225,7 +1061,7 @@ struct Step {
       }
       *reinterpret_cast<float4 *>(sw + 4 + lane * 4) = make_float4(bo[0], bo[1], bo[2], bo[3]);
       *reinterpret_cast<float4 *>(sw + kSeg + 4 + lane * 4) = make_float4(to[0], to[1], to[2], to[3]);
-      block_sync();
+      consumer_sync();
       if (warp == 0) {
         float M = -INFINITY, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
         if (c_lse > -INFINITY) {
@@ -1252,7 +1088,7 @@ struct Step {
             make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
         if (p.out_lse && lane == 0) p.out_lse[bh] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
       }
-      block_sync();
+      consumer_sync();
     }
   }
 
@@ -1261,54 +1097,57 @@ struct Step {
   __device__ static void run(const StepParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_mask[kStages];
-    __shared__ uint32_t s_cnt[kStages];
-    __shared__ int s_abort;
-    __shared__ Cursor s_cur;
+    __shared__ int s_abort, s_ready;
+    __shared__ uint32_t s_issued;
     __shared__ int64_t s_span[2][kMaxGrid + 1];
     const int n_units = p.B * p.Hkv, n_heads = p.B * p.Hq;
     Smem S;
     S.stage = smem;
     S.qbuf = smem + kOffQ;
     S.full = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    S.empty = S.full + kStages;
+    S.qrot = reinterpret_cast<float *>(smem + kOffQrot);
     S.red_o = reinterpret_cast<float *>(smem + kOffRedO);
     S.red_l = reinterpret_cast<float *>(smem + kOffRedL);
     S.red_m = reinterpret_cast<float *>(smem + kOffRedM);
     S.X = reinterpret_cast<int32_t *>(smem + kOffX);
-    S.nx = x_ints(n_heads, p.K);
-    S.offA = reinterpret_cast<int64_t *>(smem + off_units(n_heads, p.K));
+    S.pos_staged = p.mode == MODE_DECODE && (int64_t)p.B * p.K <= kPosStage;
+    S.offA = reinterpret_cast<int64_t *>(smem + off_units(p.B, p.Hq, p.K));
     S.offB = S.offA + (n_units + 1);
     S.spanA = s_span[0];
     S.spanB = s_span[1];
     S.u_pos = reinterpret_cast<int32_t *>(S.offB + (n_units + 1));
     S.u_s = S.u_pos + n_units;
-    S.rope = p.B <= kRopeTab ? reinterpret_cast<float2 *>(smem + off_rope(n_heads, n_units, p.K)) : nullptr;
-    S.cnt = s_cnt;
+    S.rope = p.B <= kRopeTab ? reinterpret_cast<float2 *>(smem + off_rope(p.B, p.Hq, p.Hkv, p.K)) : nullptr;
     S.mask = s_mask;
     S.abort = &s_abort;
-    S.cur = &s_cur;
+    S.ready = &s_ready;
+    S.issued = &s_issued;
     const bool decode = p.mode == MODE_DECODE;
-
     const int tid = threadIdx.x;
-    unsigned long long *trace = cta_trace(p);
+    unsigned long long *trace = tid < kConsumers ? cta_trace(p) : nullptr;
     if (trace && tid == 0) trace[16] = (unsigned long long)clock64();
     stamp(trace, 0);
     if (tid == 0) {
       for (int i = 0; i < kStages; ++i) {
         mbar_init(smem_addr(&S.full[i]), 1);
-        s_cnt[i] = 0;
+        mbar_init(smem_addr(&S.empty[i]), kWarps);
       }
       s_abort = 0;
+      s_ready = 0;
+      s_issued = 0;
       mbar_fence_init();
-      // the match chunks need no layout: start streaming them right away
-      Cursor &c = s_cur;
-      c.n = 0;
-      c.n_copied = 0;
-      c.cont = !decode;
-      c.kind = decode && match_slice(p, &c.mp) ? C_MATCH : C_PEND;
-      for (int i = 0; i < kStages && c.kind == C_MATCH; ++i) issue_current(p, S);
     }
-    __syncwarp();
-    for (int u = tid; u < n_units; u += kThreads) {
+    __syncthreads();  // the last barrier of all kThreads threads
+
+    if (tid >= kConsumers) {
+      // the producer warp: its first lane runs the copy sequence (the match
+      // chunks right away, the tiles once the consumers publish the layouts)
+      if (tid == kConsumers) producer(p, S);
+      return;
+    }
+
+    for (int u = tid; u < n_units; u += kConsumers) {
       S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
       S.u_s[u] = 1;
       if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
@@ -1316,60 +1155,54 @@ struct Step {
     }
     if (S.rope && p.rope_mode != MAC_ROPE_NONE) {
       // the rotation angles of every request's query (shared by its heads)
-      for (int i = tid; i < p.B * (kHeadDim / 2); i += kThreads) {
+      for (int i = tid; i < p.B * (kHeadDim / 2); i += kConsumers) {
         const int b = i / (kHeadDim / 2), j = i % (kHeadDim / 2);
         float c, sn;
         rope_angle((int64_t)p.pos_base[b] + p.pos_add, p.rope_f[j], &c, &sn);
         S.rope[i] = make_float2(c, sn);
       }
     }
-    block_sync();
-    layout_phase(p, S, 0);
-    if (!decode) layout_phase(p, S, 1);
-    stamp(trace, 7);
-    if (tid == 0) {
-      // the rest of the first kStages uses (tail tiles, or all of them in
-      // full attention); no release can happen before the consumers start
-      Cursor &c = s_cur;
-      while (c.n < (uint32_t)kStages && c.kind != C_END && c.kind != C_MATCH) issue_current(p, S);
+    if (S.pos_staged)
+      for (int i = tid; i < p.B * p.K; i += kConsumers) S.X[i] = p.ring_pos[i];
+    consumer_sync();
+    if (tid < 32) {
+      layout_warp(p, S, 0);
+      if (!decode) layout_warp(p, S, 1);
+      __threadfence_block();
+      if (tid == 0) s_ready = 1;
+      __syncwarp();
     }
-    __syncwarp();
+    consumer_sync();
+    stamp(trace, 7);
 
-    uint32_t n = 0;  // stage uses consumed so far (every thread counts the same sequence)
-    if (decode) match_phase(p, S, n);
-    stamp(trace, 1);
-    attend_phase(p, S, n, 0);
-    block_sync();
-    stamp(trace, 2);
+    uint32_t n = 0;  // stage uses consumed so far (every consumer counts the same sequence)
     if (decode) {
+      match_phase(p, S, n);
+      stamp(trace, 1);
       grid_barrier(p, S);  // the minima of every head are final
       stamp(trace, 10);
       decide(p, S);
-      if (tid == 0) {
-        Cursor &c = s_cur;
-        c.n = n;
-        c.cont = 0;
-        cursor_phase(p, S, c, 1);
-        for (int i = 0; i < kStages && c.kind != C_END; ++i) issue_current(p, S);
-      }
-      __syncwarp();
     }
     stamp(trace, 3);
-    attend_phase(p, S, n, 1);
-    block_sync();
+    // tail pieces (their tiles mostly in the stages already), then bands
+#pragma unroll 1
+    for (int ph = 0; ph < 2; ++ph) {
+      attend_phase(p, S, n, ph);
+      if (ph == 0) stamp(trace, 2);
+    }
+    consumer_sync();
     stamp(trace, 4);
-    if (tid == 0) {
-      // No copy may still be in flight into the stages once they are reused
-      // below (or the CTA exits): wait, bounded, for every copied use the
-      // consumers did not see complete.  Normally none (every issued use is
-      // consumed); after an abort at most the last kStages.
-      const uint32_t nc = s_cur.n_copied;
-      uint32_t j = nc > (uint32_t)kStages ? nc - kStages : 0u;
-      if (!*S.abort && j < n) j = n;
-      for (; j < nc; ++j) {
+    if (tid == 0 && *S.abort) {
+      // after an abort the producer may have copies in flight into the
+      // stages phase R reuses: wait for them, bounded
+      const long long t0 = clock64();
+      while (*S.issued == 0 && clock64() - t0 < (1LL << 30)) {
+      }
+      const uint32_t nc = *S.issued;
+      for (uint32_t j = nc > (uint32_t)kStages ? nc - kStages : 0u; j < nc; ++j) {
         const uint32_t bar = smem_addr(&S.full[j % kStages]);
-        const long long t0 = clock64();
-        while (!mbar_try_wait(bar, (j / kStages) & 1u) && clock64() - t0 < (1LL << 30)) {
+        const long long t1 = clock64();
+        while (!mbar_try_wait(bar, (j / kStages) & 1u) && clock64() - t1 < (1LL << 30)) {
         }
       }
     }
