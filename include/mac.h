@@ -216,18 +216,23 @@ int mac_set_phase_events(void *before_step, void *after_step, void *after_append
  * CTA, MAC_TRACE_POINTS uint64 %globaltimer stamps (ns) into device_buffer
  * [grid][MAC_TRACE_POINTS]:
  *    0 start            1 end of the match       2 end of the tail pieces
- *    3 bands laid out   4 end of the band pieces 5 after the last grid barrier
- *    6 end              7 tail layout done       8 first match chunk arrived
- *    9 match chunks done  10 after the first grid barrier
+ *    3 bands laid out   4 end of the band pieces and merges
+ *    5 decisions read   6 end              7 ready to match
+ *    8 first match chunk arrived   9 match chunks done
+ *   10 after the grid barrier
  *   11/12 first tail piece: first tile arrived / tiles done
  *   13/14 first band piece: first tile arrived / tiles done
  *   15 first band piece's partial written
  *   16/17 the SM's clock64() at start / end (cycles; with 0 and 6 they give
  *         the SM clock during the launch)
+ *   18/19 time spent merging units (ns) / units merged
+ *   20/21 the longest merge (ns) / its pieces
+ *   22/23 band tokens / band pieces the CTA attended
+ *   24 last band piece's tiles done   25 time spent waiting for band tiles (ns)
  * Stamps of phases a launch does not run are left as they were.  The buffer
  * must hold MAC_TRACE_POINTS * (number of SMs) uint64.  The hook clears
  * itself. */
-#define MAC_TRACE_POINTS 18
+#define MAC_TRACE_POINTS 26
 int mac_set_trace(void *device_buffer);
 
 /* Static string for a MAC_OK / MAC_ERR_* code. */

@@ -29,7 +29,8 @@ constexpr int kPartStride = kHeadDim + 4;  // floats per (piece, head) partial: 
 constexpr int kMaxUnits = 1024;         // B * Hkv
 constexpr int kMaxHeads = 4096;         // B * Hq
 constexpr int kMaxGrid = 256;           // CTAs of the step grid (one per SM)
-constexpr int kPosStage = 4096;         // ring positions staged in shared memory for the match
+constexpr int kGroupCtas = 16;          // CTAs per merge group of a long band
+constexpr int kGroups = kMaxGrid / kGroupCtas;
 constexpr int kRopeTab = 16;            // requests whose RoPE angles are tabulated per CTA
 constexpr int kTracePoints = MAC_TRACE_POINTS;  // timestamps per CTA in a phase trace
 constexpr size_t kMaxSmem = 232448;     // dynamic shared memory per CTA (227 KiB)
@@ -41,16 +42,29 @@ constexpr float kLn2 = 0.6931471805599453f;
 // scratch workspace (shared by the kernels of one stream)
 // ---------------------------------------------------------------------------
 // The tail tokens of all units, laid end to end in unit order, are split
-// into one contiguous span per CTA, and so are the band tokens; a CTA's span
+// into one contiguous span per CTA, and so are the long bands; a CTA's span
 // meets a few units, each meeting is a piece with its own partial summary.
 // Piece (unit u, CTA c) goes to slot u + c: the CTAs meeting a unit form a
 // run that starts at or after the last CTA of the previous unit, so the
 // slots of different pieces never coincide and B*Hkv + grid - 1 suffice.
+// A short band is one piece, in band slot u; long-band pieces follow at
+// B*Hkv + u + c.  A long band run over more than kGroupCtas CTAs is merged
+// in two levels: CTA group k = c / kGroupCtas first, into group slot u + k
+// (unique for the same reason), then the groups.
+// The per-head minima are double-buffered: decode launch k combines into
+// buffer k & 1 and clears the other for launch k + 1, so no launch has to
+// wait for every CTA to finish reading before clearing.
 struct ScratchLayout {
-  size_t ctl;        // uint32[64]: [0] status word, [2..3] grid-barrier counter (u64)
-  size_t best;       // uint64 [B][Hq]: ~(dist bits << 32 | ~pos) of the best candidate, 0 = none
+  size_t ctl;        // uint32[64]: [0] status word, [2..3] grid-barrier counter (u64),
+                     // [4] CTAs of the running launch finished (the last resets
+                     // it), [6] decode launch count
+  size_t best;       // uint64 [2][B][Hq]: ~(dist bits << 32 | ~pos) of the best candidate, 0 = none
+  size_t unit_done;  // uint32 [B*Hkv]: pieces (or groups) of the unit finished in this launch
+  size_t group_done; // uint32 [B*Hkv + kGroups]: long-band pieces finished per (unit, CTA group)
   size_t part_a;     // f32 [B*Hkv + kMaxGrid][G][kPartStride]: tail pieces
-  size_t part_b;     // f32 [B*Hkv + kMaxGrid][G][kPartStride]: band pieces
+  size_t part_b;     // f32 [2*B*Hkv + kMaxGrid][G][kPartStride]: band pieces (short
+                     // bands at u, long-band pieces at B*Hkv + u + c)
+  size_t part_g;     // f32 [B*Hkv + kGroups][G][kPartStride]: merged CTA groups of a long band
   size_t total;
 };
 
@@ -96,9 +110,12 @@ struct StepParams {
   float *out_lse;            // [B][Hq] or null
   // scratch
   uint32_t *ctl;
-  unsigned long long *best;
+  unsigned long long *best;  // [2][B*Hq]
+  uint32_t *unit_done;       // [B*Hkv]
   float *part_a;             // tail pieces
   float *part_b;             // band pieces
+  uint32_t *group_done;      // [B*Hkv + kGroups]
+  float *part_g;             // merged CTA groups
   unsigned long long *trace;  // optional: [grid][kTracePoints] %globaltimer stamps
   // RoPE frequency j as a 64-bit fixed-point fraction of a turn per
   // position: round(w_j / (2 pi) * 2^64), w_j = base^(-2j/d)
@@ -225,6 +242,21 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uin
       "%2, [%3], %4;" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through L2 (both addresses
+// 16-byte aligned); cp_async_wait_all waits for this thread's copies.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Bulk prefetch of global memory into L2 (16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long l2_evict_first_policy() {

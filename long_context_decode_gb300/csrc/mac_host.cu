@@ -52,8 +52,9 @@ mac_ring_layout ring_layout(const mac_config *c) {
   return L;
 }
 
-// Everything before part_a must start at zero (the status word, the grid
-// barrier counter and the per-head minima); the partials need no clearing.
+// Everything before part_a must start at zero (the status word, the
+// counters, the per-head minima and the per-unit piece counts); the
+// partials need no clearing.  A clean launch leaves it so for the next one.
 ScratchLayout scratch_layout(const mac_config *c) {
   const size_t B = c->batch, H = c->n_q_heads, U = (size_t)c->batch * c->n_kv_heads;
   const size_t G = c->n_q_heads / c->n_kv_heads;
@@ -61,9 +62,12 @@ ScratchLayout scratch_layout(const mac_config *c) {
   ScratchLayout S;
   size_t off = 0;
   S.ctl = off;     off = align_up(off + 64 * 4, 256);
-  S.best = off;    off = align_up(off + B * H * 8, 256);
+  S.best = off;    off = align_up(off + 2 * B * H * 8, 256);
+  S.unit_done = off;  off = align_up(off + U * 4, 256);
+  S.group_done = off;  off = align_up(off + (U + kGroups) * 4, 256);
   S.part_a = off;  off = align_up(off + slots * G * kPartStride * 4, 256);
-  S.part_b = off;  off = align_up(off + slots * G * kPartStride * 4, 256);
+  S.part_b = off;  off = align_up(off + (U + slots) * G * kPartStride * 4, 256);
+  S.part_g = off;  off = align_up(off + (U + kGroups) * G * kPartStride * 4, 256);
   S.total = off;
   return S;
 }
@@ -152,8 +156,11 @@ StepParams step_params(const mac_config *c, const ScratchLayout &S, uint8_t *scr
         pow(c->rope_base, -2.0 * (double)j / (double)c->head_dim) / 6.283185307179586, 64);
   a.ctl = (uint32_t *)(scratch + S.ctl);
   a.best = (unsigned long long *)(scratch + S.best);
+  a.unit_done = (uint32_t *)(scratch + S.unit_done);
   a.part_a = (float *)(scratch + S.part_a);
   a.part_b = (float *)(scratch + S.part_b);
+  a.group_done = (uint32_t *)(scratch + S.group_done);
+  a.part_g = (float *)(scratch + S.part_g);
   return a;
 }
 

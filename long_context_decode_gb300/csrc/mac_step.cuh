@@ -13,20 +13,22 @@
 //   a 64-bit atomic max of a packed key, a total order (smaller distance, then
 //   more recent position), so the result does not depend on scheduling.
 //
+//   Complete (K2), tail pieces: the last r tokens of every unit, which every
+//   head attends whatever the match decides, so they run before the
+//   decisions exist (their tiles are copied during the match).
+//
 //   Grid barrier; every CTA turns the minima into decisions ([MAC] K1: hit
 //   iff the smallest squared distance is strictly below thr^2) and lays out
 //   the band [s, m-r] of every unit (request, kv head), s = the first token
-//   any head of the unit needs (p-r+1 for a hit at p, 1 for a miss).
+//   any head of the unit needs (p-r+1 for a hit at p, 1 for a miss).  Band
+//   pieces follow; a head whose band starts after s masks the tokens before
+//   its own start ([MAC] "GQA intra-group skew").
 //
-//   Complete (K2): tail pieces first -- the last r tokens of every unit, which
-//   every head attends whatever the match says, so the producer streams them
-//   into the stages during the match -- then band pieces; a head whose band
-//   starts after s masks the tokens before its own start ([MAC] "GQA
-//   intra-group skew").
-//
-//   Grid barrier; phase R: per (request, head), the piece partials are merged
-//   in token order after the cached rectified summary of a hit head: the band
-//   pieces give AS_{1:m-r}, the tail pieces then give the output.
+//   Merge: the CTA that finishes a unit's last piece (a count per unit)
+//   merges, per head, the cached rectified summary of a hit, the band
+//   pieces in token order (giving AS_{1:m-r}) and then the tail pieces
+//   (giving the output); a unit without band pieces is merged after the
+//   decisions by one CTA chosen by its index.
 //
 // Work balance ("span-balanced" flash decode): the tail tokens of all units
 // are laid end to end and cut into one contiguous span per CTA, and so are
@@ -125,22 +127,19 @@ struct Step {
   static constexpr size_t kOffX = kOffRedM + 4 * (size_t)kWarps * G;
   static_assert(kOffBar % 8 == 0 && kOffX % 8 == 0, "alignment");
 
-  // X: during the match the ring positions of all requests ([B][K], when
-  // they fit), afterwards the matched position of every head (-1: miss)
-  __host__ __device__ static int x_ints(int B, int Hq, int K) {
-    const long long pos = (long long)B * K;
-    const int stage = pos <= kPosStage ? (int)pos : 0;
-    return B * Hq > stage ? B * Hq : stage;
-  }
+  // X: the matched position of every head (-1: miss)
+  __host__ __device__ static int x_ints(int B, int Hq, int K) { (void)K; return B * Hq; }
   __host__ __device__ static size_t off_units(int B, int Hq, int K) {
     return (kOffX + 4 * (size_t)x_ints(B, Hq, K) + 7) / 8 * 8;
   }
-  // + offsets of the tail and band segments (int64, n_units + 1 each), query
-  // position and band start of every unit (int32), then the RoPE cos/sin
-  // table of every request when there are at most kRopeTab of them
+  // + offsets of the tail and long-band segments and the short-band cost
+  // prefix (int64, n_units + 1 each), query position, band start and the
+  // short-band list (int32) and the tail and band CTA runs (short2) of every
+  // unit, then the RoPE cos/sin table of every request when there are at
+  // most kRopeTab of them
   __host__ __device__ static size_t off_rope(int B, int Hq, int Hkv, int K) {
     const size_t U = (size_t)B * Hkv;
-    return (off_units(B, Hq, K) + 16 * (U + 1) + 8 * U + 7) / 8 * 8;
+    return (off_units(B, Hq, K) + 24 * (U + 1) + 20 * U + 7) / 8 * 8;
   }
   __host__ __device__ static size_t smem_bytes(int B, int Hq, int Hkv, int K) {
     const size_t tab = B <= kRopeTab ? 8 * (size_t)B * (kHeadDim / 2) : 0;
@@ -157,18 +156,29 @@ struct Step {
     float *red_l;       // [kWarps * 4][G]
     float *red_m;       // [kWarps][G]
     int32_t *X;
-    bool pos_staged;    // X holds the ring positions during the match
     int64_t *offA;      // [n_units + 1]: first global index of each unit's tail segment
-    int64_t *offB;      // [n_units + 1]: same for the band segments
+    int64_t *offB;      // [n_units + 1]: same for the long bands (short ones count 0)
     int64_t *spanA;     // [grid + 1]: CTA c's tail span is [spanA[c], spanA[c+1])
-    int64_t *spanB;     // [grid + 1]: same for the bands
+    int64_t *spanB;     // [grid + 1]: same for the long bands
+    int *neA, *neB;     // [grid + 1]: non-empty spans among CTAs 0..c-1
     int32_t *u_pos;     // [n_units]: position of the unit's query (RoPE angle pos - 1)
     int32_t *u_s;       // [n_units]: first band token of the unit
+    int32_t *shortU;    // [n_units]: the units with a short band, in unit order
+    int64_t *scp;       // [n_units + 1]: prefix of their costs (tokens + kPieceCost)
+    short2 *runA;       // [n_units]: first and last CTA meeting the unit's tail (x > y: none)
+    short2 *runB;       // [n_units]: same for its long band
+    const float **mptr; // [32]: partials a merge round stages
+    long long *scan;    // [kWarps]: block_scan's warp totals
+    int *n_short;       // their number; CTA c has entries [c*n/P, (c+1)*n/P)
+    long long *short_max;  // longest band that is one piece
     float2 *rope;       // [B][d/2]: cos, sin of the query's rotation angles (B <= kRopeTab), or null
     int *mask;          // [kStages]: valid 16-token pages of the tile in the stage
     volatile int *abort;
     volatile int *ready;  // layouts known to the producer: 1 tails (and bands in full mode), 2 bands
     volatile uint32_t *issued;  // uses the producer copied (published at its end)
+    unsigned long long *best;   // this launch's per-head minima (decode)
+    unsigned long long *best_next;  // cleared here for the next decode launch
+    volatile int *last;         // this CTA finished the last piece of a unit
   };
 
   struct Piece {
@@ -265,16 +275,39 @@ struct Step {
     return false;
   }
 
-  // Exclusive prefix of the segment lengths of phase ph over all units and
-  // the CTA span boundaries, by one warp (warp-level scans, no CTA barrier;
-  // the caller makes the result visible to the other warps).
-  __device__ static void layout_warp(const StepParams &p, const Smem &S, int ph) {
-    int64_t *off = ph ? S.offB : S.offA;
-    const int U = p.B * p.Hkv, lane = threadIdx.x & 31;
+  // Prefix counts of the non-empty spans of phase ph, by one warp.
+  __device__ static void count_spans_warp(const Smem &S, int ph) {
+    const int64_t *span = spans(S, ph);
+    int *ne = ph ? S.neB : S.neA;
+    const int lane = threadIdx.x & 31, P = gridDim.x;
+    int pre = 0;
+    for (int base = 0; base <= P; base += 32) {
+      const int c = base + lane;
+      const int f = c < P && span[c] < span[c + 1] ? 1 : 0;
+      int x = f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+      }
+      if (c <= P) ne[c] = pre + x - f;
+      pre += __shfl_sync(kFull, x, 31);
+    }
+    __syncwarp();
+  }
+
+  // Tail layout, by one warp: the exclusive prefix of the tail lengths, and
+  // the CTA spans.  With at most as many units as CTAs, unit u owns the CTAs
+  // [u*P/U, (u+1)*P/U) and its tail is cut evenly among them, so no CTA
+  // meets two units (a second piece would double its fixed costs); with
+  // more units the tails, laid end to end, are cut into equal spans.
+  __device__ static void layout_tail_warp(const StepParams &p, const Smem &S) {
+    int64_t *off = S.offA;
+    const int U = p.B * p.Hkv, lane = threadIdx.x & 31, P = gridDim.x;
     long long carry = 0;
     for (int base = 0; base < U; base += 32) {
       const int u = base + lane;
-      long long x = u < U ? (long long)seg_len(p, S, ph, u) : 0;
+      long long x = u < U ? (long long)seg_len(p, S, 0, u) : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const long long y = __shfl_up_sync(kFull, x, o);
@@ -284,10 +317,164 @@ struct Step {
       carry += __shfl_sync(kFull, x, 31);
     }
     if (lane == 0) off[0] = 0;
-    // span c = global indices [c*total/P, (c+1)*total/P)
-    int64_t *span = ph ? S.spanB : S.spanA;
-    for (int c = lane; c <= (int)gridDim.x; c += 32) span[c] = part_of(c, carry, gridDim.x);
     __syncwarp();
+    for (int c = lane; c <= P; c += 32) {
+      int64_t st = carry;
+      if (c < P) {
+        if (U <= P) {
+          const int u = (int)(((long long)(c + 1) * U - 1) / P);
+          const int a = (int)((long long)u * P / U), k = (int)((long long)(u + 1) * P / U) - a;
+          st = off[u] + (off[u + 1] - off[u]) * (c - a) / k;
+        } else {
+          st = part_of(c, carry, P);
+        }
+      }
+      S.spanA[c] = st;
+    }
+    __syncwarp();
+    count_spans_warp(S, 0);
+    for (int u = lane; u < U; u += 32) S.runA[u] = find_run(S, 0, u);
+    __syncwarp();
+  }
+
+  // Exclusive scan of one value per consumer thread, in thread order, and
+  // the total (both returned to every thread).  All consumer threads call
+  // it; it holds two consumer barriers.
+  __device__ static long long block_scan(const Smem &S, long long x, long long *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(kFull, xi, o);
+      if (lane >= o) xi += y;
+    }
+    if (lane == 31) S.scan[warp] = xi;
+    consumer_sync();
+    long long base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const long long v = S.scan[w];
+      base += w < warp ? v : 0;
+      tot += v;
+    }
+    consumer_sync();
+    *total = tot;
+    return base + xi - x;
+  }
+
+  // Band layout, by all consumer threads (ends with a consumer barrier).  A
+  // band of at most max(kShortBand, all band tokens / P) tokens (a hit
+  // whose match is recent: the common case) is one piece on its own, since
+  // splitting it would cost more merges than it saves; these short bands are
+  // dealt out in unit order, CTA c taking list entries [c*n/P, (c+1)*n/P).  The long
+  // bands (misses, old matches) are laid end to end and cut into CTA spans:
+  // the token count of all bands plus kPieceCost per short piece is split
+  // evenly over the CTAs, and each CTA's span is its share less its short
+  // pieces' cost.  So neither a run of short bands nor a long band piles up
+  // on a CTA.  In a decode step the band start of every unit comes first,
+  // from the decisions.
+  static constexpr int kShortBand = 128;
+  static constexpr int kPieceCost = 128;  // fixed cost of a piece (and its merge), in tokens
+  __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
+    const int64_t n = seg_len(p, S, 1, u);
+    return n > 0 && n <= *S.short_max;
+  }
+  __device__ static void short_range(const Smem &S, int *j0, int *j1) {
+    const int ns = *S.n_short, c = blockIdx.x, P = gridDim.x;
+    *j0 = c * ns / P;
+    *j1 = (c + 1) * ns / P;
+  }
+  __device__ static Piece short_piece(const StepParams &p, const Smem &S, int j) {
+    Piece pc;
+    pc.u = S.shortU[j];
+    pc.lo = S.u_s[pc.u];
+    pc.hi = (int)(unit_len(p, S, pc.u) - p.r);
+    return pc;
+  }
+  __device__ static void layout_band_block(const StepParams &p, const Smem &S) {
+    const int U = p.B * p.Hkv, tid = threadIdx.x, P = gridDim.x;
+    const bool decode = p.mode == MODE_DECODE;
+    // units: band starts and the token total, then long-band offsets, the
+    // short list and its costs
+    long long all = 0;
+    for (int base = 0; base < U; base += kConsumers) {
+      const int u = base + tid;
+      long long len = 0;
+      if (u < U) {
+        if (decode) {
+          const int b = u / p.Hkv, g = u % p.Hkv;
+          int st = 0x7fffffff;
+          for (int hh = 0; hh < G; ++hh) {
+            const int pp = S.X[b * p.Hq + g * G + hh];
+            const int lo = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
+            st = lo < st ? lo : st;
+          }
+          S.u_s[u] = st;
+        }
+        len = seg_len(p, S, 1, u);
+      }
+      long long t;
+      block_scan(S, len, &t);
+      all += t;
+    }
+    // (only while few units qualify: many whole units dealt by count would
+    // load some CTAs with two where spans give each its exact share)
+    long long smax = all / P > kShortBand ? all / P : kShortBand;
+    if (smax > kShortBand) {
+      long long cnt = 0;
+      for (int base = 0; base < U; base += kConsumers) {
+        const int u = base + tid;
+        const long long len = u < U ? (long long)seg_len(p, S, 1, u) : 0;
+        long long t;
+        block_scan(S, len > 0 && len <= smax ? 1 : 0, &t);
+        cnt += t;
+      }
+      if (cnt > P / 2) smax = kShortBand;
+    }
+    if (tid == 0) *S.short_max = smax;
+    long long cb = 0, cs = 0;  // carries: long tokens; short cost << 11 | short count
+    for (int base = 0; base < U; base += kConsumers) {
+      const int u = base + tid;
+      const long long len = u < U ? (long long)seg_len(p, S, 1, u) : 0;
+      const bool sh = len > 0 && len <= smax;
+      const long long big = sh ? 0 : len, pk = sh ? ((len + kPieceCost) << 11) | 1 : 0;
+      long long tb, ts;
+      const long long eb = block_scan(S, big, &tb);
+      const long long es = block_scan(S, pk, &ts);
+      if (u < U) S.offB[u + 1] = cb + eb + big;
+      if (sh) {
+        const int j = (int)((cs + es) & 2047);
+        S.shortU[j] = u;
+        S.scp[j + 1] = ((cs + es) >> 11) + len + kPieceCost;
+      }
+      cb += tb;
+      cs += ts;
+    }
+    const long long tb = cb, tv = tb + (cs >> 11);
+    const int ns = (int)(cs & 2047);
+    if (tid == 0) {
+      S.offB[0] = 0;
+      S.scp[0] = 0;
+      *S.n_short = ns;
+    }
+    consumer_sync();
+    // CTA spans of the long bands
+    long long cap = 0;
+    const int c = tid;
+    if (c < P) {
+      const int j0 = c * ns / P, j1 = (c + 1) * ns / P;
+      cap = part_of(c + 1, tv, P) - part_of(c, tv, P) - (S.scp[j1] - S.scp[j0]);
+      cap = cap > 0 ? cap : 0;
+    }
+    long long tot;
+    const long long st = block_scan(S, cap, &tot);
+    if (c <= P) S.spanB[c] = st < tb ? st : tb;
+    consumer_sync();
+    const int f = c < P && S.spanB[c] < S.spanB[c + 1] ? 1 : 0;
+    const long long ef = block_scan(S, f, &tot);
+    if (c <= P) S.neB[c] = (int)ef;
+    for (int u = tid; u < U; u += kConsumers) S.runB[u] = find_run(S, 1, u);
+    consumer_sync();
   }
 
   // ---------------------------------------------------------------------
@@ -412,41 +599,95 @@ struct Step {
     return true;
   }
 
-  // The whole copy sequence of this CTA, in the order the consumers use it:
-  // match chunks (decode), tail tiles, band tiles.  Run by one lane.
-  __device__ static void producer(const StepParams &p, const Smem &S) {
-    const int P = gridDim.x, U = p.B * p.Hkv;
-    const bool decode = p.mode == MODE_DECODE;
+  // The tiles of one piece, from stage use n on; returns the next use.
+  __device__ static uint32_t copy_piece(const StepParams &p, const Smem &S, const Piece &pc, uint32_t n) {
+    const int64_t t0 = (pc.lo - 1) / kTileTok, t1 = (pc.hi - 1) / kTileTok;
+    for (int64_t t = t0; t <= t1; ++t, ++n) {
+      if (!acquire_stage(p, S, n)) break;
+      issue_tile(p, S, n % kStages, pc.u, pc.lo, pc.hi, t, t == t0);
+    }
+    return n;
+  }
+
+  // Match chunks of this CTA (stage uses n, n+1, ... while below `until`),
+  // in the order the consumers use them; returns the next use.
+  __device__ static uint32_t copy_match(const StepParams &p, const Smem &S, uint32_t n, uint32_t until) {
+    const int P = gridDim.x;
+    const int cph = chunks_per_head(p.K);
+    const int nc = p.B * p.Hq * cph;
     const unsigned long long pol = l2_evict_first_policy();
+    for (int j = blockIdx.x + (int)n * P; j < nc && n < until; j += P, ++n) {
+      if (!acquire_stage(p, S, n)) break;
+      const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
+      const int rows = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
+      const int st = n % kStages;
+      const uint32_t bar = smem_addr(&S.full[st]);
+      mbar_expect_tx(bar, (uint32_t)rows * kRowBytes);
+      bulk_g2s_hint(smem_addr(S.stage + (size_t)st * kStageBytes),
+                    (const uint8_t *)p.ring_q + ((size_t)bh * p.K + slot0) * kRowBytes,
+                    (uint32_t)rows * kRowBytes, bar, pol);
+    }
+    return n;
+  }
+
+  // The producer warp.  Its first lane starts the match copies (they need
+  // nothing but the parameters); the warp then lays out every unit's
+  // position and the tail segments (and, for full attention, the bands)
+  // and publishes them, and the first lane runs the rest of the copy
+  // sequence: match chunks (decode), tail tiles, band tiles.
+  __device__ static void producer_warp(const StepParams &p, const Smem &S) {
+    const int lane = threadIdx.x & 31, U = p.B * p.Hkv;
+    const bool decode = p.mode == MODE_DECODE;
     uint32_t n = 0;
-    if (decode) {
-      const int cph = chunks_per_head(p.K);
-      const int nc = p.B * p.Hq * cph;
-      for (int j = blockIdx.x; j < nc; j += P, ++n) {
-        if (!acquire_stage(p, S, n)) break;
-        const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
-        const int rows = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
-        const int st = n % kStages;
-        const uint32_t bar = smem_addr(&S.full[st]);
-        mbar_expect_tx(bar, (uint32_t)rows * kRowBytes);
-        bulk_g2s_hint(smem_addr(S.stage + (size_t)st * kStageBytes),
-                      (const uint8_t *)p.ring_q + ((size_t)bh * p.K + slot0) * kRowBytes,
-                      (uint32_t)rows * kRowBytes, bar, pol);
+    if (decode && lane == 0) n = copy_match(p, S, 0, kStages);
+    __syncwarp();
+    for (int u = lane; u < U; u += 32) {
+      S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
+      S.u_s[u] = 1;
+      if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
+        set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
+    }
+    __syncwarp();
+    layout_tail_warp(p, S);
+    __threadfence_block();
+    if (lane == 0) *S.ready = 1;
+    __syncwarp();
+    if (decode && !PAGED) {
+      // the tile a recent match's band needs (a hit at m-1 starts it at
+      // m-r) into L2 while the match runs, for the units u = c mod P
+      for (int u = blockIdx.x + lane * (int)gridDim.x; u < U; u += 32 * (int)gridDim.x) {
+        const int64_t m = unit_len(p, S, u), hi = m - p.r;
+        if (!len_ok(p, m) || hi < 1 || hi > p.kv.capacity) continue;
+        const int64_t lo = hi - kTileTok + 1 > 1 ? hi - kTileTok + 1 : 1;
+        const size_t off = ((size_t)u * (size_t)p.kv.capacity + (size_t)(lo - 1)) * kRowBytes;
+        const uint32_t bytes = (uint32_t)(hi - lo + 1) * kRowBytes;
+        bulk_prefetch_l2((const uint8_t *)p.kv.k + off, bytes);
+        bulk_prefetch_l2((const uint8_t *)p.kv.v + off, bytes);
       }
     }
+    if (lane == 0) producer(p, S, n);
+    __syncwarp();
+  }
+
+  // The rest of the copy sequence from stage use n on.  Run by one lane.
+  __device__ static void producer(const StepParams &p, const Smem &S, uint32_t n) {
+    const int U = p.B * p.Hkv;
+    const bool decode = p.mode == MODE_DECODE;
+    if (decode) n = copy_match(p, S, n, 0xFFFFFFFFu);
     for (int ph = 0; ph < 2 && !*S.abort; ++ph) {
-      if (!wait_ready(p, S, ph == 1 && decode ? 2 : 1)) break;
+      if (!wait_ready(p, S, ph + 1)) break;
+      if (ph == 1) {
+        int j0, j1;
+        short_range(S, &j0, &j1);
+        for (int j = j0; j < j1 && !*S.abort; ++j) n = copy_piece(p, S, short_piece(p, S, j), n);
+      }
       const int64_t *off = offs(S, ph);
       const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
       if (g0 >= g1) continue;
       Piece pc;
       int u = unit_of(off, U, g0);
       while (!*S.abort && find_piece(p, S, ph, u, g0, g1, &pc)) {
-        const int64_t t0 = (pc.lo - 1) / kTileTok, t1 = (pc.hi - 1) / kTileTok;
-        for (int64_t t = t0; t <= t1; ++t, ++n) {
-          if (!acquire_stage(p, S, n)) break;
-          issue_tile(p, S, n % kStages, pc.u, pc.lo, pc.hi, t, t == t0);
-        }
+        n = copy_piece(p, S, pc, n);
         u = pc.u + 1;
       }
     }
@@ -501,7 +742,7 @@ struct Step {
   }
 
   // The warp's best (distance, position) joins head bh's global minimum.
-  __device__ static void flush_best(const StepParams &p, int bh, float bd, int bp) {
+  __device__ static void flush_best(const Smem &S, int bh, float bd, int bp) {
 #pragma unroll
     for (int off = 8; off <= 16; off <<= 1) {
       const float d2 = __shfl_xor_sync(kFull, bd, off);
@@ -511,7 +752,7 @@ struct Step {
         bp = p2;
       }
     }
-    if ((threadIdx.x & 31) == 0 && bp >= 1) atomicMax(&p.best[bh], pack_best(bd, bp));
+    if ((threadIdx.x & 31) == 0 && bp >= 1) atomicMax(&S.best[bh], pack_best(bd, bp));
   }
 
   __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n) {
@@ -530,13 +771,20 @@ struct Step {
 #pragma unroll
       for (int cc = 0; cc < kNP; ++cc)
         unpack16x2<T>(__ldg(reinterpret_cast<const uint4 *>(qrow + cc * 128 + sub * 16)), qv + cc * (kPer / 2));
-      const int64_t m = (int64_t)S.u_pos[b * p.Hkv] - p.len_sub;
+      const int64_t m = (int64_t)__ldg(p.pos_base + b) + p.pos_add - p.len_sub;
       int pos_lo = 1, pos_hi = 0;
       if (len_ok(p, m)) {
         pos_lo = m - p.K > 1 ? (int)(m - p.K) : 1;
         pos_hi = (int)(m - 1);
       }
-      const int32_t *rp = (S.pos_staged ? S.X : p.ring_pos) + (int64_t)b * p.K + slot0;
+      // the positions of the group's rows, also before the wait
+      const int32_t *rp = p.ring_pos + (int64_t)b * p.K + slot0;
+      int pk[kRPG];
+#pragma unroll
+      for (int k = 0; k < kRPG; ++k) {
+        const int i = grp + 32 * k;
+        pk[k] = __ldg(rp + (i < cnt ? i : cnt - 1));
+      }
       const bool ok = wait_use(p, S, n);
       if (n == 0) stamp(cta_trace(p), 8);
       const uint8_t *rows = S.stage + (size_t)(n % kStages) * kStageBytes;
@@ -549,9 +797,8 @@ struct Step {
         const int i = grp + 32 * k;
         const int ri = i < cnt ? i : cnt - 1;
         D[k] = row_dist(rows + (size_t)ri * kRowBytes, sub, qv);
-        const int pk = rp[ri];
-        const bool valid = ok && i < cnt && pk >= pos_lo && pk <= pos_hi;
-        ps[k] = valid ? pk : -1;
+        const bool valid = ok && i < cnt && pk[k] >= pos_lo && pk[k] <= pos_hi;
+        ps[k] = valid ? pk[k] : -1;
         D[k] = valid ? D[k] : INFINITY;
       }
 #pragma unroll
@@ -563,7 +810,7 @@ struct Step {
             ps[k] = ps[k + w];
           }
       release(S, n);
-      flush_best(p, bh, D[0], ps[0]);
+      flush_best(S, bh, D[0], ps[0]);
     }
     stamp(cta_trace(p), 9);
   }
@@ -587,57 +834,39 @@ struct Step {
     consumer_sync();
   }
 
-  // Decisions of every head from the combined minima, then every unit's band
-  // start and the band layout (every CTA computes the same), by warp 0,
-  // which then tells the producer the band layout is ready; the other warps
-  // meanwhile start bringing the cached summaries phase R will merge into L2.
-  // Ends with a consumer barrier.
-  __device__ static void decide(const StepParams &p, const Smem &S) {
-    const int tid = threadIdx.x, lane = tid & 31, n_bh = p.B * p.Hq, U = p.B * p.Hkv;
-    if (tid < 32) {
-      for (int bh = lane; bh < n_bh; bh += 32) {
-        const int b = bh / p.Hq, u = b * p.Hkv + (bh % p.Hq) / G;
-        const int64_t m = unit_len(p, S, u);
-        const unsigned long long inv = __ldcg(&p.best[bh]);
-        int pos = -1;
-        if (inv != 0ull && len_ok(p, m) && m >= p.min_context) {
-          const unsigned long long key = ~inv;
-          const float d = __uint_as_float((uint32_t)(key >> 32));
-          if (d < p.thr2) pos = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-        }
-        S.X[bh] = pos;
-        if (blockIdx.x == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
+  // Decisions of every head from the combined minima (one head per consumer
+  // thread); the cached summaries of the hits are asked into L2 for the
+  // merges; then every unit's band start and the band layout (every CTA
+  // computes the same), after which the producer may copy band tiles.  Ends
+  // with a consumer barrier.
+  __device__ static void decide(const StepParams &p, const Smem &S, unsigned long long *trace) {
+    const int tid = threadIdx.x, n_bh = p.B * p.Hq;
+    for (int bh = tid; bh < n_bh; bh += kConsumers) {
+      const int b = bh / p.Hq, u = b * p.Hkv + (bh % p.Hq) / G;
+      const int64_t m = unit_len(p, S, u);
+      const unsigned long long inv = __ldcg(&S.best[bh]);
+      int pos = -1;
+      if (inv != 0ull && len_ok(p, m) && m >= p.min_context) {
+        const unsigned long long key = ~inv;
+        const float d = __uint_as_float((uint32_t)(key >> 32));
+        if (d < p.thr2) pos = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
       }
-      __syncwarp();
-      for (int u = lane; u < U; u += 32) {
-        const int b = u / p.Hkv, g = u % p.Hkv;
-        int s = 0x7fffffff;
-        for (int hh = 0; hh < G; ++hh) {
-          const int pp = S.X[b * p.Hq + g * G + hh];
-          const int lo = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
-          s = lo < s ? lo : s;
-        }
-        S.u_s[u] = s;
+      S.X[bh] = pos;
+      if (blockIdx.x == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
+      if (pos >= 1 && bh % gridDim.x == blockIdx.x) {
+        const int64_t slot = (int64_t)bh * p.K + pos % p.K;
+        for (int k = 0; k < kHeadDim * 4; k += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(p.ring_o + slot * kHeadDim + k / 4));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.ring_lse + slot));
       }
-      __syncwarp();
-      layout_warp(p, S, 1);
-      __threadfence_block();
-      if (lane == 0) *S.ready = 2;
-      __syncwarp();
     }
     consumer_sync();
-    // the cached summaries of this CTA's phase-R heads: into L2 now, behind
-    // the band attention
-    for (int bh = blockIdx.x + (tid >> 5) * gridDim.x; bh < n_bh; bh += kWarps * gridDim.x) {
-      const int pos = S.X[bh];
-      if (pos >= 1 && (tid & 31) < kHeadDim * 4 / 128 + 1) {
-        const int64_t slot = (int64_t)bh * p.K + pos % p.K;
-        const void *a = (tid & 31) < kHeadDim * 4 / 128 ? (const void *)(p.ring_o + slot * kHeadDim + (tid & 31) * 32)
-                                                         : (const void *)(p.ring_lse + slot);
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-      }
+    stamp(trace, 5);
+    layout_band_block(p, S);
+    if (threadIdx.x == 0) {
+      __threadfence_block();
+      *S.ready = 2;
     }
-    __syncwarp();
   }
 
   // ---------------------------------------------------------------------
@@ -725,6 +954,11 @@ struct Step {
   __device__ static void attend_piece(const StepParams &p, const Smem &S, uint32_t &n, int ph,
                                       const Piece &pc, float *dst, bool first_piece) {
     unsigned long long *trace = first_piece ? cta_trace(p) : nullptr;
+    unsigned long long *tr_all = ph == 1 && threadIdx.x == 0 ? cta_trace(p) : nullptr;
+    if (tr_all) {
+      tr_all[22] += (unsigned long long)(pc.hi - pc.lo + 1);
+      tr_all[23] += 1;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = lane >> 3, sub = lane & 7;
     const int b = pc.u / p.Hkv, g = pc.u % p.Hkv;
     const int idx = sub >> kPlain;         // this lane's score slot
@@ -749,7 +983,9 @@ struct Step {
     const int ntiles = (int)((pc.hi - 1) / kTileTok - tile0 + 1);
     for (int k = 0; k < ntiles; ++k, ++n) {
       const int st = n % kStages;
+      const unsigned long long tw = tr_all ? globaltimer() : 0ull;
       const bool ok = wait_use(p, S, n);
+      if (tr_all) tr_all[25] += globaltimer() - tw;
       if (k == 0) {
         stamp(trace, ph ? 13 : 11);
         rotate_query(p, S, st, b, S.u_pos[pc.u]);
@@ -837,6 +1073,7 @@ struct Step {
       release(S, n);
     }
     stamp(trace, ph ? 14 : 12);
+    if (tr_all) tr_all[24] = globaltimer();
     epilogue(p, S, o, mrun, m_mine, l_mine, dst);
     if (ph == 1) stamp(trace, 15);
   }
@@ -929,24 +1166,40 @@ struct Step {
     }
   }
 
+  // The CTA's pieces of phase ph.  Partial slots: tail piece (u, CTA c) at
+  // u + c of part_a; short band of u at u of part_b, long-band piece (u, c)
+  // at n_units + u + c (the CTAs meeting a unit in a span layout form a run
+  // that starts at or after the last CTA of the previous unit, so u + c
+  // never repeats).
   __device__ static void attend_phase(const StepParams &p, const Smem &S, uint32_t &n, int ph) {
     const int U = p.B * p.Hkv;
+    bool first = true;
+    if (ph == 1) {
+      int j0, j1;
+      short_range(S, &j0, &j1);
+      for (int j = j0; j < j1; ++j) {
+        const Piece pc = short_piece(p, S, j);
+        attend_piece(p, S, n, 1, pc, p.part_b + (size_t)pc.u * G * kPartStride, first);
+        piece_done(p, S, pc.u, 1, true);
+        first = false;
+      }
+    }
     const int64_t *off = offs(S, ph);
     const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
     if (g0 >= g1) return;
-    float *part = ph ? p.part_b : p.part_a;
+    float *part = ph ? p.part_b + (size_t)U * G * kPartStride : p.part_a;
     Piece pc;
     int u = unit_of(off, U, g0);
-    bool first = true;
     while (find_piece(p, S, ph, u, g0, g1, &pc)) {
       attend_piece(p, S, n, ph, pc, part + (size_t)(pc.u + blockIdx.x) * G * kPartStride, first);
+      piece_done(p, S, pc.u, ph, false);
       u = pc.u + 1;
       first = false;
     }
   }
 
   // ---------------------------------------------------------------------
-  // phase R
+  // merges
   // ---------------------------------------------------------------------
 
   // (M, L, O[4]) <- (M, L, O) (+) (m2, l2, o2[4]) in base-2 log domain; an
@@ -971,124 +1224,294 @@ struct Step {
   // CTAs whose spans meet unit u's segment in phase ph: [*c0, *c1] (empty
   // when *c1 < *c0).
   __device__ static void seg_ctas(const Smem &S, int ph, int u, int *c0, int *c1) {
+    const short2 r = (ph ? S.runB : S.runA)[u];
+    *c0 = r.x;
+    *c1 = r.y;
+  }
+  // the run of unit u in phase ph, from the offsets and spans
+  __device__ static short2 find_run(const Smem &S, int ph, int u) {
     const int64_t *off = offs(S, ph), *span = spans(S, ph);
-    if (off[u + 1] <= off[u]) {
-      *c0 = 0;
-      *c1 = -1;
-      return;
-    }
-    *c0 = cta_of(span, gridDim.x, off[u]);
-    *c1 = cta_of(span, gridDim.x, off[u + 1] - 1);
+    if (off[u + 1] <= off[u]) return make_short2(0, -1);
+    return make_short2((short)cta_of(span, gridDim.x, off[u]), (short)cta_of(span, gridDim.x, off[u + 1] - 1));
   }
 
-  // For each (request, head) -- one per CTA at a time -- merge the unit's
-  // pieces in order: band pieces, then tail pieces.  The 8 warps each take a
-  // contiguous segment of that list (lane l owns dims 4l..4l+3) and keep two
-  // running states, band and tail.  Warp 0 then merges, in order: the cached
-  // summary of a hit head, the band states of warps 0..7 (giving
-  // AS_{1:m-r}), and the tail states (giving the output).
-  __device__ static void reduce_phase(const StepParams &p, const Smem &S) {
-    constexpr int kSeg = kHeadDim + 4;                // m, l, -, -, o[d]
-    constexpr int kBatch = 8;                         // pieces loaded at once per warp
-    float *seg = reinterpret_cast<float *>(S.stage);  // [kWarps][2][kSeg]; the stages are idle now
+  // Non-empty spans of phase ph among CTAs [c0, c1].
+  __device__ static int nonempty(const Smem &S, int ph, int c0, int c1) {
+    if (c1 < c0) return 0;
+    const int *ne = ph ? S.neB : S.neA;
+    return ne[c1 + 1] - ne[c0];
+  }
+
+  // The partials a merge reads, in order: nb band entries, then (for a unit)
+  // one per CTA of its tail run.  Band entries: the short piece, one per CTA
+  // of the long-band run, or, for a run over more than kGroupCtas CTAs, one
+  // per CTA group (merged first, each by the CTA that finishes the group's
+  // last piece).  A group merge lists the run's CTAs in group k.
+  enum { kShort = 0, kCtas = 1, kGroupList = 2 };
+  struct PieceList {
+    int kind, nb, n;
+    int b0, b1;  // the band entries' CTA range (kCtas) / the whole run (kGroupList)
+    int ca0;     // first CTA of the tail run
+    int u;
+  };
+  __device__ static PieceList unit_list(const StepParams &p, const Smem &S, int u) {
+    PieceList L;
+    int ca1;
+    L.u = u;
+    seg_ctas(S, 1, u, &L.b0, &L.b1);
+    seg_ctas(S, 0, u, &L.ca0, &ca1);
+    if (short_band(p, S, u)) {
+      L.kind = kShort;
+      L.nb = 1;
+    } else if (L.b1 - L.b0 + 1 > kGroupCtas) {
+      L.kind = kGroupList;
+      L.nb = L.b1 / kGroupCtas - L.b0 / kGroupCtas + 1;
+    } else {
+      L.kind = kCtas;
+      L.nb = L.b1 - L.b0 + 1;
+    }
+    L.n = L.nb + (ca1 - L.ca0 + 1);
+    return L;
+  }
+  __device__ static void group_ctas(const PieceList &L, int k, int *lo, int *hi) {
+    *lo = max(L.b0, k * kGroupCtas);
+    *hi = min(L.b1, k * kGroupCtas + kGroupCtas - 1);
+  }
+  __device__ static PieceList group_list(const PieceList &U_, int k) {
+    PieceList L = U_;
+    L.kind = kCtas;
+    group_ctas(U_, k, &L.b0, &L.b1);
+    L.nb = L.n = L.b1 - L.b0 + 1;
+    return L;
+  }
+  // band pieces of the unit (merge inputs made by attention)
+  __device__ static int band_pieces(const Smem &S, const PieceList &L) {
+    return L.kind == kShort ? 1 : nonempty(S, 1, L.b0, L.b1);
+  }
+  // what the unit's count must reach: its band entries that exist (pieces,
+  // or groups with a piece) and, without a grid barrier before the bands,
+  // its tail pieces
+  __device__ static int unit_target(const StepParams &p, const Smem &S, const PieceList &L) {
+    int n = 0;
+    if (L.kind == kGroupList) {
+      for (int k = L.b0 / kGroupCtas; k <= L.b1 / kGroupCtas; ++k) {
+        int lo, hi;
+        group_ctas(L, k, &lo, &hi);
+        n += nonempty(S, 1, lo, hi) > 0;
+      }
+    } else {
+      n = band_pieces(S, L);
+    }
+    if (p.mode != MODE_DECODE) n += nonempty(S, 0, L.ca0, L.ca0 + (L.n - L.nb) - 1);
+    return n;
+  }
+  __device__ static const float *piece_at(const StepParams &p, const Smem &S, const PieceList &L, int hh, int i) {
+    const int U = p.B * p.Hkv, u = L.u;
+    if (i < L.nb) {
+      if (L.kind == kShort) return p.part_b + ((size_t)u * G + hh) * kPartStride;
+      if (L.kind == kCtas) {
+        const int c = L.b0 + i;
+        if (S.spanB[c] >= S.spanB[c + 1]) return nullptr;
+        return p.part_b + ((size_t)(U + u + c) * G + hh) * kPartStride;
+      }
+      const int k = L.b0 / kGroupCtas + i;
+      int lo, hi;
+      group_ctas(L, k, &lo, &hi);
+      if (nonempty(S, 1, lo, hi) == 0) return nullptr;
+      return p.part_g + ((size_t)(u + k) * G + hh) * kPartStride;
+    }
+    const int c = L.ca0 + (i - L.nb);
+    if (S.spanA[c] >= S.spanA[c + 1]) return nullptr;
+    return p.part_a + ((size_t)(u + c) * G + hh) * kPartStride;
+  }
+
+  // Merge of a unit (group < 0) or of CTA group `group` of its long band.
+  // The G heads are merged concurrently: kWarps / G warps per head, each
+  // taking a contiguous segment of the list (lane l owns dims 4l..4l+3; the
+  // (m, l) pairs of up to 32 entries are loaded one per lane) and keeping
+  // two running states, band and tail.  The head's first warp then merges
+  // them in order.  A unit: the cached summary of a hit head, the band
+  // states (giving AS_{1:m-r}), the tail states (giving the output).  A
+  // group: the band states, written as a partial like a piece's.  The count
+  // the merge answered is cleared for the next launch.
+  __device__ static void merge_unit(const StepParams &p, const Smem &S, const PieceList &L, int group) {
+    unsigned long long *trace = cta_trace(p);
+    const unsigned long long t_in = trace && threadIdx.x == 0 ? globaltimer() : 0ull;
+    merge_heads(p, S, L, group);
+    if (trace && threadIdx.x == 0) {
+      // merge statistics: total time, count, longest merge and its entries
+      const unsigned long long dt = globaltimer() - t_in;
+      trace[18] += dt;
+      trace[19] += 1;
+      if (dt > trace[20]) {
+        trace[20] = dt;
+        trace[21] = (unsigned long long)L.n;
+      }
+    }
+    __syncwarp();
+  }
+
+  __device__ static void merge_heads(const StepParams &p, const Smem &S, const PieceList &L, int group) {
+    constexpr int kSeg = kHeadDim + 4;  // m, l, -, -, o[d]
+    constexpr int kWPH = kWarps / G;    // warps per head
+    constexpr int kEntry = G * kPartStride;  // floats of one list entry (all heads)
+    constexpr int kChunks = kEntry / 4;      // its 16-byte pieces
+    constexpr int kRound = (kWarps * 4 * G * kHeadDim - G * kWPH * 2 * kSeg) / kEntry;  // entries staged at once
+    static_assert(kRound >= 8 && kRound <= 32, "merge staging");
+    float *buf = S.red_o;                        // [kRound][kEntry]
+    float *seg = S.red_o + (size_t)kRound * kEntry;  // [G][kWPH][2][kSeg]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n_bh = p.B * p.Hq;
-    for (int bh = blockIdx.x; bh < n_bh; bh += gridDim.x) {
-      const int b = bh / p.Hq, h = bh % p.Hq, g = h / G, hh = h % G;
-      const int u = b * p.Hkv + g;
-      int cb0, cb1, ca0, ca1;
-      seg_ctas(S, 1, u, &cb0, &cb1);
-      seg_ctas(S, 0, u, &ca0, &ca1);
-      const int nb = cb1 - cb0 + 1, n = nb + (ca1 - ca0 + 1);
-      // cached rectified summary of a hit head, fetched ahead of its use
-      float c_lse = -INFINITY;
-      float4 c_o = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (p.mode == MODE_DECODE && warp == 0) {
-        const int pos = S.X[bh];
-        if (pos >= 1) {
-          const int64_t slot = (int64_t)bh * p.K + pos % p.K;
-          c_lse = p.ring_lse[slot];
-          c_o = reinterpret_cast<const float4 *>(p.ring_o + slot * kHeadDim)[lane];
-        }
+    const int hh = warp / kWPH, wi = warp % kWPH;
+    const int u = L.u, b = u / p.Hkv, g = u % p.Hkv;
+    const int bh = b * p.Hq + g * G + hh;
+    const int n = L.n, nb = L.nb;
+    const bool fin = group < 0;
+    // cached rectified summary of a hit head, fetched ahead of its use
+    float c_lse = -INFINITY;
+    float4 c_o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (fin && p.mode == MODE_DECODE && wi == 0) {
+      const int pos = S.X[bh];
+      if (pos >= 1) {
+        const int64_t slot = (int64_t)bh * p.K + pos % p.K;
+        c_lse = p.ring_lse[slot];
+        c_o = reinterpret_cast<const float4 *>(p.ring_o + slot * kHeadDim)[lane];
       }
-      if (p.mode == MODE_DECODE && warp == kWarps - 1 && lane < kHeadDim / kPer) {
-        // the append (on the aux stream) reads the step's query from the ring
-        // workspace, so the caller may reuse its query buffer right away
-        reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * (kHeadDim / kPer) + lane] =
-            reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
-      }
-      const int per = (n + kWarps - 1) / kWarps;
-      const int i0 = warp * per, i1 = min(n, i0 + per);
-      float bm = -INFINITY, bl = 0.f, bo[4] = {0.f, 0.f, 0.f, 0.f};
-      float tm = -INFINITY, tl = 0.f, to[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int i = i0; i < i1; i += kBatch) {
-        float pm[kBatch], pl[kBatch];
-        float4 po[kBatch];
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-          pl[j] = 0.f;
-          pm[j] = 0.f;
-          po[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-          const int it = i + j;
-          if (it < i1) {
-            const int ph = it < nb ? 1 : 0;
-            const int c = it < nb ? cb0 + it : ca0 + (it - nb);
-            const int64_t *span = spans(S, ph);
-            if (span[c] < span[c + 1]) {  // CTAs with an empty span have no piece
-              const float *pp = (ph ? p.part_b : p.part_a) + ((int64_t)(u + c) * G + hh) * kPartStride;
-              pm[j] = __ldcg(pp + kHeadDim);
-              pl[j] = __ldcg(pp + kHeadDim + 1);
-              po[j] = __ldcg(reinterpret_cast<const float4 *>(pp) + lane);
-            }
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < kBatch; ++j) {
-          if (i + j >= i1) break;
-          const float o2[4] = {po[j].x, po[j].y, po[j].z, po[j].w};
-          if (i + j < nb)
-            merge4(bm, bl, bo, pm[j], pl[j], o2);
-          else
-            merge4(tm, tl, to, pm[j], pl[j], o2);
-        }
-      }
-      float *sw = seg + (size_t)warp * 2 * kSeg;
-      if (lane == 0) {
-        sw[0] = bm;
-        sw[1] = bl;
-        sw[kSeg] = tm;
-        sw[kSeg + 1] = tl;
-      }
-      *reinterpret_cast<float4 *>(sw + 4 + lane * 4) = make_float4(bo[0], bo[1], bo[2], bo[3]);
-      *reinterpret_cast<float4 *>(sw + kSeg + 4 + lane * 4) = make_float4(to[0], to[1], to[2], to[3]);
+    }
+    if (fin && p.mode == MODE_DECODE && wi == kWPH - 1 && lane < kHeadDim / kPer) {
+      // the append (on the aux stream) reads the step's query from the ring
+      // workspace, so the caller may reuse its query buffer right away
+      reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * (kHeadDim / kPer) + lane] =
+          reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
+    }
+    float bm = -INFINITY, bl = 0.f, bo[4] = {0.f, 0.f, 0.f, 0.f};
+    float tm = -INFINITY, tl = 0.f, to[4] = {0.f, 0.f, 0.f, 0.f};
+    // rounds of up to kRound entries: every consumer thread copies 16-byte
+    // pieces of them into shared memory (one L2 round trip per round), then
+    // the warps of each head merge their share of the round in list order
+    for (int base = 0; base < n; base += kRound) {
+      const int cnt = min(kRound, n - base);
+      if (tid < cnt) S.mptr[tid] = piece_at(p, S, L, 0, base + tid);
       consumer_sync();
-      if (warp == 0) {
-        float M = -INFINITY, L = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-        if (c_lse > -INFINITY) {
-          const float a[4] = {c_o.x, c_o.y, c_o.z, c_o.w};
-          merge4(M, L, O, c_lse * kLog2e, 1.f, a);
+      for (int x = tid; x < cnt * kChunks; x += kConsumers) {
+        const int e = x / kChunks, q = x - e * kChunks;
+        const float *src = S.mptr[e];
+        if (src) cp_async16(smem_addr(buf + (size_t)e * kEntry + q * 4), src + q * 4);
+      }
+      cp_async_wait_all();
+      consumer_sync();
+      const int per = (cnt + kWPH - 1) / kWPH;
+      const int e0 = wi * per, e1 = min(cnt, e0 + per);
+      for (int e = e0; e < e1; ++e) {
+        if (!S.mptr[e]) continue;
+        const float *src = buf + (size_t)e * kEntry + hh * kPartStride;
+        const float4 o4 = *reinterpret_cast<const float4 *>(src + lane * 4);
+        const float o2[4] = {o4.x, o4.y, o4.z, o4.w};
+        if (base + e < nb)
+          merge4(bm, bl, bo, src[kHeadDim], src[kHeadDim + 1], o2);
+        else
+          merge4(tm, tl, to, src[kHeadDim], src[kHeadDim + 1], o2);
+      }
+      consumer_sync();  // the staging buffer and pointers are reused
+    }
+    float *sw = seg + ((size_t)hh * kWPH + wi) * 2 * kSeg;
+    if (lane == 0) {
+      sw[0] = bm;
+      sw[1] = bl;
+      sw[kSeg] = tm;
+      sw[kSeg + 1] = tl;
+    }
+    *reinterpret_cast<float4 *>(sw + 4 + lane * 4) = make_float4(bo[0], bo[1], bo[2], bo[3]);
+    *reinterpret_cast<float4 *>(sw + kSeg + 4 + lane * 4) = make_float4(to[0], to[1], to[2], to[3]);
+    consumer_sync();
+    if (wi == 0) {
+      const float *sh = seg + (size_t)hh * kWPH * 2 * kSeg;
+      float M = -INFINITY, Lsum = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
+      if (c_lse > -INFINITY) {
+        const float a[4] = {c_o.x, c_o.y, c_o.z, c_o.w};
+        merge4(M, Lsum, O, c_lse * kLog2e, 1.f, a);
+      }
+      for (int w = 0; w < kWPH; ++w) {
+        const float *s = sh + (size_t)w * 2 * kSeg;
+        merge4(M, Lsum, O, s[0], s[1], s + 4 + lane * 4);
+      }
+      if (!fin) {
+        // the group's partial: the raw state, in a piece partial's layout
+        float *dst = p.part_g + ((size_t)(u + group) * G + hh) * kPartStride;
+        *reinterpret_cast<float4 *>(dst + lane * 4) = make_float4(O[0], O[1], O[2], O[3]);
+        if (lane == 0) {
+          dst[kHeadDim] = M;
+          dst[kHeadDim + 1] = Lsum;
         }
-        if (p.mode == MODE_DECODE && lane == 0) p.best[bh] = 0ull;  // every CTA read it before the barrier
-        for (int w = 0; w < kWarps; ++w) {
-          const float *s = seg + (size_t)w * 2 * kSeg;
-          merge4(M, L, O, s[0], s[1], s + 4 + lane * 4);
-        }
+      } else {
         if (p.as_o) {
-          const float inv = L > 0.f ? 1.f / L : 0.f;
+          const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
           *reinterpret_cast<float4 *>(p.as_o + (int64_t)bh * kHeadDim + lane * 4) =
               make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-          if (lane == 0) p.as_lse[bh] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+          if (lane == 0) p.as_lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
         }
-        for (int w = 0; w < kWarps; ++w) {
-          const float *s = seg + (size_t)w * 2 * kSeg + kSeg;
-          merge4(M, L, O, s[0], s[1], s + 4 + lane * 4);
+        for (int w = 0; w < kWPH; ++w) {
+          const float *s = sh + (size_t)w * 2 * kSeg + kSeg;
+          merge4(M, Lsum, O, s[0], s[1], s + 4 + lane * 4);
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         *reinterpret_cast<float4 *>(p.out + (int64_t)bh * kHeadDim + lane * 4) =
             make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-        if (p.out_lse && lane == 0) p.out_lse[bh] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+        if (p.out_lse && lane == 0) p.out_lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+      }
+    }
+    if (tid == 0) {
+      if (fin)
+        p.unit_done[u] = 0;
+      else
+        p.group_done[u + group] = 0;
+    }
+    consumer_sync();
+  }
+
+  // After a piece's partial is written: count it, and merge what it
+  // completes here (every CTA knows how many pieces each unit and group
+  // has, so no grid barrier is needed before the merges).  A long-band piece
+  // of a two-level unit counts in its CTA group; the group's last piece
+  // merges the group and counts the group in the unit.  A decode step's
+  // tail pieces are not counted: they all finish before the grid barrier,
+  // which orders them before every merge.
+  __device__ static void piece_done(const StepParams &p, const Smem &S, int u, int ph, bool is_short) {
+    const bool decode = p.mode == MODE_DECODE;
+    if (decode && ph == 0) return;
+    const int k = blockIdx.x / kGroupCtas;
+    __threadfence();  // this thread's part of the partial, before the count
+    consumer_sync();
+    if (threadIdx.x == 0) {
+      const PieceList L = unit_list(p, S, u);
+      int act = 0;
+      if (ph == 1 && !is_short && L.kind == kGroupList) {
+        int lo, hi;
+        group_ctas(L, k, &lo, &hi);
+        const uint32_t old = atomicAdd(&p.group_done[u + k], 1u);
+        act = (int)(old + 1) == nonempty(S, 1, lo, hi) ? 1 : 0;
+      } else {
+        const uint32_t old = atomicAdd(&p.unit_done[u], 1u);
+        act = (int)(old + 1) == unit_target(p, S, L) ? 2 : 0;
+      }
+      *S.last = act;
+    }
+    consumer_sync();
+    if (*S.last == 0) return;
+    const PieceList L = unit_list(p, S, u);
+    if (*S.last == 1) {
+      __threadfence();  // the group's other partials, after their counts
+      merge_unit(p, S, group_list(L, k), k);
+      __threadfence();  // the group partial, before the unit count
+      consumer_sync();
+      if (threadIdx.x == 0) {
+        const uint32_t old = atomicAdd(&p.unit_done[u], 1u);
+        *S.last = (int)(old + 1) == unit_target(p, S, L) ? 2 : 0;
       }
       consumer_sync();
+    }
+    if (*S.last == 2) {
+      __threadfence();  // the other CTAs' partials, after their counts
+      merge_unit(p, S, L, -1);
     }
   }
 
@@ -1097,9 +1520,13 @@ struct Step {
   __device__ static void run(const StepParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_mask[kStages];
-    __shared__ int s_abort, s_ready;
+    __shared__ int s_abort, s_ready, s_last, s_par, s_nshort;
     __shared__ uint32_t s_issued;
     __shared__ int64_t s_span[2][kMaxGrid + 1];
+    __shared__ int s_ne[2][kMaxGrid + 1];
+    __shared__ long long s_scan[kWarps];
+    __shared__ long long s_short_max;
+    __shared__ const float *s_mptr[32];
     const int n_units = p.B * p.Hkv, n_heads = p.B * p.Hq;
     Smem S;
     S.stage = smem;
@@ -1111,22 +1538,35 @@ struct Step {
     S.red_l = reinterpret_cast<float *>(smem + kOffRedL);
     S.red_m = reinterpret_cast<float *>(smem + kOffRedM);
     S.X = reinterpret_cast<int32_t *>(smem + kOffX);
-    S.pos_staged = p.mode == MODE_DECODE && (int64_t)p.B * p.K <= kPosStage;
     S.offA = reinterpret_cast<int64_t *>(smem + off_units(p.B, p.Hq, p.K));
     S.offB = S.offA + (n_units + 1);
     S.spanA = s_span[0];
     S.spanB = s_span[1];
-    S.u_pos = reinterpret_cast<int32_t *>(S.offB + (n_units + 1));
+    S.neA = s_ne[0];
+    S.neB = s_ne[1];
+    S.scp = S.offB + (n_units + 1);
+    S.u_pos = reinterpret_cast<int32_t *>(S.scp + (n_units + 1));
     S.u_s = S.u_pos + n_units;
+    S.shortU = S.u_s + n_units;
+    S.runA = reinterpret_cast<short2 *>(S.shortU + n_units);
+    S.runB = S.runA + n_units;
+    S.mptr = s_mptr;
+    S.scan = s_scan;
+    S.n_short = &s_nshort;
+    S.short_max = &s_short_max;
     S.rope = p.B <= kRopeTab ? reinterpret_cast<float2 *>(smem + off_rope(p.B, p.Hq, p.Hkv, p.K)) : nullptr;
     S.mask = s_mask;
     S.abort = &s_abort;
     S.ready = &s_ready;
     S.issued = &s_issued;
+    S.last = &s_last;
     const bool decode = p.mode == MODE_DECODE;
     const int tid = threadIdx.x;
     unsigned long long *trace = tid < kConsumers ? cta_trace(p) : nullptr;
-    if (trace && tid == 0) trace[16] = (unsigned long long)clock64();
+    if (trace && tid == 0) {
+      trace[16] = (unsigned long long)clock64();
+      for (int k = 18; k < kTracePoints; ++k) trace[k] = 0;
+    }
     stamp(trace, 0);
     if (tid == 0) {
       for (int i = 0; i < kStages; ++i) {
@@ -1136,23 +1576,22 @@ struct Step {
       s_abort = 0;
       s_ready = 0;
       s_issued = 0;
+      // decode launches alternate between the two buffers of minima; every
+      // CTA reads the count before the first grid barrier, and it only
+      // changes after every CTA has finished
+      s_par = decode ? (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u) : 0;
       mbar_fence_init();
     }
     __syncthreads();  // the last barrier of all kThreads threads
+    const int n_bh = n_heads;
+    S.best = p.best + (size_t)s_par * n_bh;
+    S.best_next = p.best + (size_t)(s_par ^ 1) * n_bh;
 
     if (tid >= kConsumers) {
-      // the producer warp: its first lane runs the copy sequence (the match
-      // chunks right away, the tiles once the consumers publish the layouts)
-      if (tid == kConsumers) producer(p, S);
+      producer_warp(p, S);
       return;
     }
 
-    for (int u = tid; u < n_units; u += kConsumers) {
-      S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
-      S.u_s[u] = 1;
-      if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
-        set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
-    }
     if (S.rope && p.rope_mode != MAC_ROPE_NONE) {
       // the rotation angles of every request's query (shared by its heads)
       for (int i = tid; i < p.B * (kHeadDim / 2); i += kConsumers) {
@@ -1162,16 +1601,6 @@ struct Step {
         S.rope[i] = make_float2(c, sn);
       }
     }
-    if (S.pos_staged)
-      for (int i = tid; i < p.B * p.K; i += kConsumers) S.X[i] = p.ring_pos[i];
-    consumer_sync();
-    if (tid < 32) {
-      layout_warp(p, S, 0);
-      if (!decode) layout_warp(p, S, 1);
-      __threadfence_block();
-      if (tid == 0) s_ready = 1;
-      __syncwarp();
-    }
     consumer_sync();
     stamp(trace, 7);
 
@@ -1179,22 +1608,42 @@ struct Step {
     if (decode) {
       match_phase(p, S, n);
       stamp(trace, 1);
-      grid_barrier(p, S);  // the minima of every head are final
+    }
+    // tail pieces (their tiles in the stages already, copied during the
+    // match): every head attends them whatever the match decides
+    if (tid == 0) wait_ready(p, S, 1);
+    consumer_sync();
+    if (!decode) {
+      // full attention: every band starts at 1, so its layout is known now
+      layout_band_block(p, S);
+      if (tid == 0) {
+        __threadfence_block();
+        *S.ready = 2;
+      }
+    }
+    attend_phase(p, S, n, 0);
+    stamp(trace, 2);
+    if (decode) {
+      grid_barrier(p, S);  // the minima of every head are final, the tail partials written
       stamp(trace, 10);
-      decide(p, S);
+      decide(p, S, trace);
+      // nobody reads the other buffer in this launch: clear it for the next
+      for (int i = blockIdx.x * kConsumers + tid; i < n_bh; i += gridDim.x * kConsumers) S.best_next[i] = 0ull;
     }
     stamp(trace, 3);
-    // tail pieces (their tiles mostly in the stages already), then bands
-#pragma unroll 1
-    for (int ph = 0; ph < 2; ++ph) {
-      attend_phase(p, S, n, ph);
-      if (ph == 0) stamp(trace, 2);
+    attend_phase(p, S, n, 1);
+    // units whose last piece no band piece could see finish (no band: it
+    // was a tail piece before the decisions; no piece at all: no valid
+    // length) are merged by one CTA each
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const PieceList L = unit_list(p, S, u);
+      if (band_pieces(S, L) == 0 && (decode || nonempty(S, 0, L.ca0, L.ca0 + (L.n - L.nb) - 1) == 0))
+        merge_unit(p, S, L, -1);
     }
-    consumer_sync();
     stamp(trace, 4);
     if (tid == 0 && *S.abort) {
       // after an abort the producer may have copies in flight into the
-      // stages phase R reuses: wait for them, bounded
+      // stages: wait for them, bounded, before the CTA exits
       const long long t0 = clock64();
       while (*S.issued == 0 && clock64() - t0 < (1LL << 30)) {
       }
@@ -1206,9 +1655,20 @@ struct Step {
         }
       }
     }
-    grid_barrier(p, S);  // every piece partial is written
-    stamp(trace, 5);
-    reduce_phase(p, S);
+    if (tid == 0) {
+      // the last CTA to finish advances the decode launch count; after a
+      // failed launch it also clears the piece counts the merges of that
+      // launch may have left
+      __threadfence();
+      const uint32_t old = atomicAdd(p.ctl + 4, 1u);
+      if (old == gridDim.x - 1) {  // every CTA of the launch has finished
+        p.ctl[4] = 0;
+        if (decode) atomicAdd(p.ctl + 6, 1u);
+        if (*(volatile uint32_t *)p.ctl != 0)
+          for (int u = 0; u < n_units; ++u) p.unit_done[u] = 0;
+      }
+    }
+    __syncwarp();
     stamp(trace, 6);
     if (trace && tid == 0) trace[17] = (unsigned long long)clock64();
     __syncwarp();
