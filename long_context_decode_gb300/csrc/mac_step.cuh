@@ -168,9 +168,10 @@ struct Step {
     short2 *runA;       // [n_units]: first and last CTA meeting the unit's tail (x > y: none)
     short2 *runB;       // [n_units]: same for its long band
     const float **mptr; // [32]: partials a merge round stages
-    long long *scan;    // [kWarps]: block_scan's warp totals
     int *n_short;       // their number; CTA c has entries [c*n/P, (c+1)*n/P)
+    long long *scan;    // [kWarps]: block_scan's warp totals
     long long *short_max;  // longest band that is one piece
+    long long *band_tot;   // [2]: long-band tokens, their cost plus the short pieces'
     float2 *rope;       // [B][d/2]: cos, sin of the query's rotation angles (B <= kRopeTab), or null
     int *mask;          // [kStages]: valid 16-token pages of the tile in the stage
     volatile int *abort;
@@ -337,6 +338,112 @@ struct Step {
     __syncwarp();
   }
 
+  // Band layout.  A band of at most max(kShortBand, all band tokens / P)
+  // tokens (a hit whose match is recent: the common case) is one piece on
+  // its own, since splitting it would cost more merges than it saves -- as
+  // long as at most P/2 units qualify, else the bound is kShortBand (many
+  // whole units dealt by count would give some CTAs two where spans give
+  // each its exact share).  These short bands are dealt out in unit order,
+  // CTA c taking list entries [c*n/P, (c+1)*n/P).  The long bands (misses,
+  // old matches) are laid end to end and cut into CTA spans: the token
+  // count of all bands plus kPieceCost per short piece is split evenly over
+  // the CTAs, and each CTA's span is its share less its short pieces' cost.
+  // So neither a run of short bands nor a long band piles up on a CTA.
+  //
+  // Two parts, each by one warp: band_units_warp (band starts, the short
+  // list, long-band offsets) right after the decisions, so that the short
+  // pieces can start; band_spans_block (the long-band spans, their
+  // non-empty counts and every long unit's CTA run) by all consumer threads
+  // while the producer copies the short pieces.
+  static constexpr int kShortBand = 128;
+  static constexpr int kPieceCost = 128;  // fixed cost of a piece (and its merge), in tokens
+  __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
+    const int64_t n = seg_len(p, S, 1, u);
+    return n > 0 && n <= *S.short_max;
+  }
+  __device__ static void short_range(const Smem &S, int *j0, int *j1) {
+    const int ns = *S.n_short, c = blockIdx.x, P = gridDim.x;
+    *j0 = c * ns / P;
+    *j1 = (c + 1) * ns / P;
+  }
+  __device__ static Piece short_piece(const StepParams &p, const Smem &S, int j) {
+    Piece pc;
+    pc.u = S.shortU[j];
+    pc.lo = S.u_s[pc.u];
+    pc.hi = (int)(unit_len(p, S, pc.u) - p.r);
+    return pc;
+  }
+  __device__ static void band_units_warp(const StepParams &p, const Smem &S) {
+    const int U = p.B * p.Hkv, lane = threadIdx.x & 31, P = gridDim.x;
+    const bool decode = p.mode == MODE_DECODE;
+    long long all = 0;
+    for (int base = 0; base < U; base += 32) {
+      const int u = base + lane;
+      long long len = 0;
+      if (u < U) {
+        if (decode) {
+          int st = 0x7fffffff;
+          for (int hh = 0; hh < G; ++hh) {
+            const int pp = S.X[u * G + hh];  // head b*Hq + g*G + hh of unit u = b*Hkv + g
+            const int lo = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
+            st = lo < st ? lo : st;
+          }
+          S.u_s[u] = st;
+        }
+        len = seg_len(p, S, 1, u);
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) len += __shfl_xor_sync(kFull, len, o);
+      all += len;
+    }
+    long long smax = all / P > kShortBand ? all / P : kShortBand;
+    if (smax > kShortBand) {
+      int cnt = 0;
+      for (int base = 0; base < U; base += 32) {
+        const int u = base + lane;
+        const long long len = u < U ? (long long)seg_len(p, S, 1, u) : 0;
+        cnt += __popc(__ballot_sync(kFull, len > 0 && len <= smax));
+      }
+      if (cnt > P / 2) smax = kShortBand;
+    }
+    long long cb = 0, cc = 0;  // carries: long tokens, short costs
+    int ns = 0;
+    for (int base = 0; base < U; base += 32) {
+      const int u = base + lane;
+      const long long len = u < U ? (long long)seg_len(p, S, 1, u) : 0;
+      const bool sh = len > 0 && len <= smax;
+      long long x = sh ? 0 : len, y = sh ? len + kPieceCost : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long x2 = __shfl_up_sync(kFull, x, o), y2 = __shfl_up_sync(kFull, y, o);
+        if (lane >= o) {
+          x += x2;
+          y += y2;
+        }
+      }
+      const unsigned bal = __ballot_sync(kFull, sh);
+      if (u < U) S.offB[u + 1] = cb + x;
+      if (sh) {
+        const int j = ns + __popc(bal & ((1u << lane) - 1u));
+        S.shortU[j] = u;
+        S.scp[j + 1] = cc + y;
+        S.runB[u] = make_short2(0, -1);
+      }
+      cb += __shfl_sync(kFull, x, 31);
+      cc += __shfl_sync(kFull, y, 31);
+      ns += __popc(bal);
+    }
+    if (lane == 0) {
+      S.offB[0] = 0;
+      S.scp[0] = 0;
+      *S.n_short = ns;
+      *S.short_max = smax;
+      S.band_tot[0] = cb;       // long-band tokens
+      S.band_tot[1] = cb + cc;  // all cost
+    }
+    __syncwarp();
+  }
+
   // Exclusive scan of one value per consumer thread, in thread order, and
   // the total (both returned to every thread).  All consumer threads call
   // it; it holds two consumer barriers.
@@ -362,118 +469,29 @@ struct Step {
     return base + xi - x;
   }
 
-  // Band layout, by all consumer threads (ends with a consumer barrier).  A
-  // band of at most max(kShortBand, all band tokens / P) tokens (a hit
-  // whose match is recent: the common case) is one piece on its own, since
-  // splitting it would cost more merges than it saves; these short bands are
-  // dealt out in unit order, CTA c taking list entries [c*n/P, (c+1)*n/P).  The long
-  // bands (misses, old matches) are laid end to end and cut into CTA spans:
-  // the token count of all bands plus kPieceCost per short piece is split
-  // evenly over the CTAs, and each CTA's span is its share less its short
-  // pieces' cost.  So neither a run of short bands nor a long band piles up
-  // on a CTA.  In a decode step the band start of every unit comes first,
-  // from the decisions.
-  static constexpr int kShortBand = 128;
-  static constexpr int kPieceCost = 128;  // fixed cost of a piece (and its merge), in tokens
-  __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
-    const int64_t n = seg_len(p, S, 1, u);
-    return n > 0 && n <= *S.short_max;
-  }
-  __device__ static void short_range(const Smem &S, int *j0, int *j1) {
-    const int ns = *S.n_short, c = blockIdx.x, P = gridDim.x;
-    *j0 = c * ns / P;
-    *j1 = (c + 1) * ns / P;
-  }
-  __device__ static Piece short_piece(const StepParams &p, const Smem &S, int j) {
-    Piece pc;
-    pc.u = S.shortU[j];
-    pc.lo = S.u_s[pc.u];
-    pc.hi = (int)(unit_len(p, S, pc.u) - p.r);
-    return pc;
-  }
-  __device__ static void layout_band_block(const StepParams &p, const Smem &S) {
-    const int U = p.B * p.Hkv, tid = threadIdx.x, P = gridDim.x;
-    const bool decode = p.mode == MODE_DECODE;
-    // units: band starts and the token total, then long-band offsets, the
-    // short list and its costs
-    long long all = 0;
-    for (int base = 0; base < U; base += kConsumers) {
-      const int u = base + tid;
-      long long len = 0;
-      if (u < U) {
-        if (decode) {
-          const int b = u / p.Hkv, g = u % p.Hkv;
-          int st = 0x7fffffff;
-          for (int hh = 0; hh < G; ++hh) {
-            const int pp = S.X[b * p.Hq + g * G + hh];
-            const int lo = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
-            st = lo < st ? lo : st;
-          }
-          S.u_s[u] = st;
-        }
-        len = seg_len(p, S, 1, u);
-      }
-      long long t;
-      block_scan(S, len, &t);
-      all += t;
-    }
-    // (only while few units qualify: many whole units dealt by count would
-    // load some CTAs with two where spans give each its exact share)
-    long long smax = all / P > kShortBand ? all / P : kShortBand;
-    if (smax > kShortBand) {
-      long long cnt = 0;
-      for (int base = 0; base < U; base += kConsumers) {
-        const int u = base + tid;
-        const long long len = u < U ? (long long)seg_len(p, S, 1, u) : 0;
-        long long t;
-        block_scan(S, len > 0 && len <= smax ? 1 : 0, &t);
-        cnt += t;
-      }
-      if (cnt > P / 2) smax = kShortBand;
-    }
-    if (tid == 0) *S.short_max = smax;
-    long long cb = 0, cs = 0;  // carries: long tokens; short cost << 11 | short count
-    for (int base = 0; base < U; base += kConsumers) {
-      const int u = base + tid;
-      const long long len = u < U ? (long long)seg_len(p, S, 1, u) : 0;
-      const bool sh = len > 0 && len <= smax;
-      const long long big = sh ? 0 : len, pk = sh ? ((len + kPieceCost) << 11) | 1 : 0;
-      long long tb, ts;
-      const long long eb = block_scan(S, big, &tb);
-      const long long es = block_scan(S, pk, &ts);
-      if (u < U) S.offB[u + 1] = cb + eb + big;
-      if (sh) {
-        const int j = (int)((cs + es) & 2047);
-        S.shortU[j] = u;
-        S.scp[j + 1] = ((cs + es) >> 11) + len + kPieceCost;
-      }
-      cb += tb;
-      cs += ts;
-    }
-    const long long tb = cb, tv = tb + (cs >> 11);
-    const int ns = (int)(cs & 2047);
-    if (tid == 0) {
-      S.offB[0] = 0;
-      S.scp[0] = 0;
-      *S.n_short = ns;
-    }
-    consumer_sync();
-    // CTA spans of the long bands
-    long long cap = 0;
-    const int c = tid;
+  // The long-band spans (CTA c = consumer thread c), their non-empty counts
+  // and every long unit's CTA run, by all consumer threads (ends with a
+  // consumer barrier).
+  __device__ static void band_spans_block(const StepParams &p, const Smem &S) {
+    const int U = p.B * p.Hkv, c = threadIdx.x, P = gridDim.x;
+    const int ns = *S.n_short;
+    const long long tb = S.band_tot[0], tv = S.band_tot[1];
+    long long cap = 0, tot;
     if (c < P) {
       const int j0 = c * ns / P, j1 = (c + 1) * ns / P;
       cap = part_of(c + 1, tv, P) - part_of(c, tv, P) - (S.scp[j1] - S.scp[j0]);
       cap = cap > 0 ? cap : 0;
     }
-    long long tot;
     const long long st = block_scan(S, cap, &tot);
-    if (c <= P) S.spanB[c] = st < tb ? st : tb;
+    if (c < P) S.spanB[c] = st < tb ? st : tb;
+    if (c == 0) S.spanB[P] = tb;
     consumer_sync();
     const int f = c < P && S.spanB[c] < S.spanB[c + 1] ? 1 : 0;
     const long long ef = block_scan(S, f, &tot);
-    if (c <= P) S.neB[c] = (int)ef;
-    for (int u = tid; u < U; u += kConsumers) S.runB[u] = find_run(S, 1, u);
+    if (c < P) S.neB[c] = (int)ef;
+    if (c == 0) S.neB[P] = (int)tot;
+    for (int u = c; u < U; u += kConsumers)
+      if (!short_band(p, S, u)) S.runB[u] = find_run(S, 1, u);
     consumer_sync();
   }
 
@@ -630,13 +648,33 @@ struct Step {
     return n;
   }
 
+  // The tiles of the pieces of CTA span g0..g1 of phase ph, from stage use n
+  // on; returns the next use.  Run by one lane.
+  __device__ static uint32_t copy_span(const StepParams &p, const Smem &S, int ph, uint32_t n) {
+    const int U = p.B * p.Hkv;
+    const int64_t *off = offs(S, ph);
+    const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
+    if (g0 >= g1) return n;
+    Piece pc;
+    int u = unit_of(off, U, g0);
+    while (!*S.abort && find_piece(p, S, ph, u, g0, g1, &pc)) {
+      n = copy_piece(p, S, pc, n);
+      u = pc.u + 1;
+    }
+    return n;
+  }
+
   // The producer warp.  Its first lane starts the match copies (they need
   // nothing but the parameters); the warp then lays out every unit's
-  // position and the tail segments (and, for full attention, the bands)
-  // and publishes them, and the first lane runs the rest of the copy
-  // sequence: match chunks (decode), tail tiles, band tiles.
+  // position and the tail spans (for full attention also the band starts
+  // and the short-band list) and publishes them, and the first lane copies
+  // the rest of the match chunks and the tail tiles, then the short pieces
+  // once the short-band list is published, then the long-band pieces once
+  // their spans are.  Every copy goes in the order the consumers use the
+  // stages: match chunks, tail pieces, short pieces, long-band pieces.
   __device__ static void producer_warp(const StepParams &p, const Smem &S) {
     const int lane = threadIdx.x & 31, U = p.B * p.Hkv;
+    unsigned long long *tr = lane == 0 ? cta_trace(p) : nullptr;
     const bool decode = p.mode == MODE_DECODE;
     uint32_t n = 0;
     if (decode && lane == 0) n = copy_match(p, S, 0, kStages);
@@ -649,8 +687,9 @@ struct Step {
     }
     __syncwarp();
     layout_tail_warp(p, S);
+    if (!decode) band_units_warp(p, S);  // every band starts at 1
     __threadfence_block();
-    if (lane == 0) *S.ready = 1;
+    if (lane == 0) *S.ready = decode ? 1 : 2;
     __syncwarp();
     if (decode && !PAGED) {
       // the tile a recent match's band needs (a hit at m-1 starts it at
@@ -665,34 +704,24 @@ struct Step {
         bulk_prefetch_l2((const uint8_t *)p.kv.v + off, bytes);
       }
     }
-    if (lane == 0) producer(p, S, n);
-    __syncwarp();
-  }
-
-  // The rest of the copy sequence from stage use n on.  Run by one lane.
-  __device__ static void producer(const StepParams &p, const Smem &S, uint32_t n) {
-    const int U = p.B * p.Hkv;
-    const bool decode = p.mode == MODE_DECODE;
-    if (decode) n = copy_match(p, S, n, 0xFFFFFFFFu);
-    for (int ph = 0; ph < 2 && !*S.abort; ++ph) {
-      if (!wait_ready(p, S, ph + 1)) break;
-      if (ph == 1) {
+    if (lane == 0) {
+      if (decode) n = copy_match(p, S, n, 0xFFFFFFFFu);
+      n = copy_span(p, S, 0, n);
+      if (!wait_ready(p, S, 2)) *S.abort = 1;
+      if (tr) tr[26] = globaltimer();
+      if (!*S.abort) {
         int j0, j1;
         short_range(S, &j0, &j1);
         for (int j = j0; j < j1 && !*S.abort; ++j) n = copy_piece(p, S, short_piece(p, S, j), n);
       }
-      const int64_t *off = offs(S, ph);
-      const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
-      if (g0 >= g1) continue;
-      Piece pc;
-      int u = unit_of(off, U, g0);
-      while (!*S.abort && find_piece(p, S, ph, u, g0, g1, &pc)) {
-        n = copy_piece(p, S, pc, n);
-        u = pc.u + 1;
-      }
+      if (tr) tr[9] = globaltimer();
+      if (!wait_ready(p, S, 3)) *S.abort = 1;
+      if (tr) tr[27] = globaltimer();
+      if (!*S.abort) n = copy_span(p, S, 1, n);
+      __threadfence_block();
+      *S.issued = n;
     }
-    __threadfence_block();
-    *S.issued = n;
+    __syncwarp();
   }
 
   // Consumer side of stage use n.
@@ -812,7 +841,6 @@ struct Step {
       release(S, n);
       flush_best(S, bh, D[0], ps[0]);
     }
-    stamp(cta_trace(p), 9);
   }
 
   // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.
@@ -836,9 +864,9 @@ struct Step {
 
   // Decisions of every head from the combined minima (one head per consumer
   // thread); the cached summaries of the hits are asked into L2 for the
-  // merges; then every unit's band start and the band layout (every CTA
-  // computes the same), after which the producer may copy band tiles.  Ends
-  // with a consumer barrier.
+  // merges; then, by warp 0, every unit's band start and the short-band list
+  // (every CTA computes the same), after which the producer may copy short
+  // pieces and lay out the long bands.  Ends with a consumer barrier.
   __device__ static void decide(const StepParams &p, const Smem &S, unsigned long long *trace) {
     const int tid = threadIdx.x, n_bh = p.B * p.Hq;
     for (int bh = tid; bh < n_bh; bh += kConsumers) {
@@ -862,10 +890,17 @@ struct Step {
     }
     consumer_sync();
     stamp(trace, 5);
-    layout_band_block(p, S);
-    if (threadIdx.x == 0) {
+    if (tid < 32) {
+      band_units_warp(p, S);
       __threadfence_block();
-      *S.ready = 2;
+      if (tid == 0) *S.ready = 2;  // the producer may copy the short pieces
+      __syncwarp();
+    }
+    consumer_sync();
+    band_spans_block(p, S);
+    if (tid == 0) {
+      __threadfence_block();
+      *S.ready = 3;
     }
   }
 
@@ -1166,34 +1201,36 @@ struct Step {
     }
   }
 
-  // The CTA's pieces of phase ph.  Partial slots: tail piece (u, CTA c) at
-  // u + c of part_a; short band of u at u of part_b, long-band piece (u, c)
-  // at n_units + u + c (the CTAs meeting a unit in a span layout form a run
-  // that starts at or after the last CTA of the previous unit, so u + c
-  // never repeats).
-  __device__ static void attend_phase(const StepParams &p, const Smem &S, uint32_t &n, int ph) {
-    const int U = p.B * p.Hkv;
-    bool first = true;
-    if (ph == 1) {
-      int j0, j1;
-      short_range(S, &j0, &j1);
-      for (int j = j0; j < j1; ++j) {
-        const Piece pc = short_piece(p, S, j);
-        attend_piece(p, S, n, 1, pc, p.part_b + (size_t)pc.u * G * kPartStride, first);
-        piece_done(p, S, pc.u, 1, true);
-        first = false;
+  // Partial slots: tail piece (u, CTA c) at u + c of part_a; short band of
+  // u at u of part_b, long-band piece (u, c) at n_units + u + c (the CTAs
+  // meeting a unit in a span layout form a run that starts at or after the
+  // last CTA of the previous unit, so u + c never repeats).
+
+  // The CTA's pieces of one kind: 0 its tail span, 1 its short bands, 2 its
+  // long-band span (one loop, so the attention code is inlined once; the
+  // loop state lives in shared memory and a counter, not in registers the
+  // attention needs).  The first band piece of the CTA is traced.
+  __device__ static void attend_kind(const StepParams &p, const Smem &S, uint32_t &n, int kind) {
+    const int U = p.B * p.Hkv, ph = kind ? 1 : 0;
+    int j0, j1;
+    short_range(S, &j0, &j1);
+    int it = kind == 1 ? j0 : (spans(S, ph)[blockIdx.x] < spans(S, ph)[blockIdx.x + 1]
+                                   ? unit_of(offs(S, ph), U, spans(S, ph)[blockIdx.x]) : U);
+    bool first = kind != 2 || j1 == j0;
+#pragma unroll 1
+    for (;;) {
+      Piece pc;
+      if (kind == 1) {
+        if (it >= j1) break;
+        pc = short_piece(p, S, it++);
+      } else {
+        if (!find_piece(p, S, ph, it, spans(S, ph)[blockIdx.x], spans(S, ph)[blockIdx.x + 1], &pc)) break;
+        it = pc.u + 1;
       }
-    }
-    const int64_t *off = offs(S, ph);
-    const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
-    if (g0 >= g1) return;
-    float *part = ph ? p.part_b + (size_t)U * G * kPartStride : p.part_a;
-    Piece pc;
-    int u = unit_of(off, U, g0);
-    while (find_piece(p, S, ph, u, g0, g1, &pc)) {
-      attend_piece(p, S, n, ph, pc, part + (size_t)(pc.u + blockIdx.x) * G * kPartStride, first);
-      piece_done(p, S, pc.u, ph, false);
-      u = pc.u + 1;
+      const size_t slot = kind == 0 ? (size_t)(pc.u + blockIdx.x)
+                                    : kind == 1 ? (size_t)pc.u : (size_t)(U + pc.u + blockIdx.x);
+      attend_piece(p, S, n, ph, pc, (ph ? p.part_b : p.part_a) + slot * G * kPartStride, first);
+      piece_done(p, S, pc.u, ph, kind == 1);
       first = false;
     }
   }
@@ -1524,8 +1561,7 @@ struct Step {
     __shared__ uint32_t s_issued;
     __shared__ int64_t s_span[2][kMaxGrid + 1];
     __shared__ int s_ne[2][kMaxGrid + 1];
-    __shared__ long long s_scan[kWarps];
-    __shared__ long long s_short_max;
+    __shared__ long long s_short_max, s_band_tot[2], s_scan[kWarps];
     __shared__ const float *s_mptr[32];
     const int n_units = p.B * p.Hkv, n_heads = p.B * p.Hq;
     Smem S;
@@ -1551,9 +1587,10 @@ struct Step {
     S.runA = reinterpret_cast<short2 *>(S.shortU + n_units);
     S.runB = S.runA + n_units;
     S.mptr = s_mptr;
-    S.scan = s_scan;
     S.n_short = &s_nshort;
     S.short_max = &s_short_max;
+    S.band_tot = s_band_tot;
+    S.scan = s_scan;
     S.rope = p.B <= kRopeTab ? reinterpret_cast<float2 *>(smem + off_rope(p.B, p.Hq, p.Hkv, p.K)) : nullptr;
     S.mask = s_mask;
     S.abort = &s_abort;
@@ -1611,27 +1648,36 @@ struct Step {
     }
     // tail pieces (their tiles in the stages already, copied during the
     // match): every head attends them whatever the match decides
-    if (tid == 0) wait_ready(p, S, 1);
+    // (full attention counts every piece at its unit, so it needs the whole
+    // layout first: the producer warp publishes it at once)
+    if (tid == 0) wait_ready(p, S, decode ? 1 : 2);
     consumer_sync();
     if (!decode) {
-      // full attention: every band starts at 1, so its layout is known now
-      layout_band_block(p, S);
+      band_spans_block(p, S);
       if (tid == 0) {
         __threadfence_block();
-        *S.ready = 2;
+        *S.ready = 3;
       }
     }
-    attend_phase(p, S, n, 0);
-    stamp(trace, 2);
-    if (decode) {
-      grid_barrier(p, S);  // the minima of every head are final, the tail partials written
-      stamp(trace, 10);
-      decide(p, S, trace);
-      // nobody reads the other buffer in this launch: clear it for the next
-      for (int i = blockIdx.x * kConsumers + tid; i < n_bh; i += gridDim.x * kConsumers) S.best_next[i] = 0ull;
+    // tail pieces, short bands, long-band pieces
+#pragma unroll 1
+    for (int kind = 0; kind < 3; ++kind) {
+      if (kind == 1) {
+        stamp(trace, 2);
+        if (decode) {
+          grid_barrier(p, S);  // the minima of every head are final, the tail partials written
+          stamp(trace, 10);
+          decide(p, S, trace);
+          // nobody reads the other buffer in this launch: clear it for the next
+          for (int i = blockIdx.x * kConsumers + tid; i < n_bh; i += gridDim.x * kConsumers) S.best_next[i] = 0ull;
+        }
+        stamp(trace, 3);
+      } else if (kind == 2) {
+        if (tid == 0) wait_ready(p, S, 3);  // the long-band spans
+        consumer_sync();
+      }
+      attend_kind(p, S, n, kind);
     }
-    stamp(trace, 3);
-    attend_phase(p, S, n, 1);
     // units whose last piece no band piece could see finish (no band: it
     // was a tail piece before the decisions; no piece at all: no valid
     // length) are merged by one CTA each
