@@ -230,10 +230,11 @@ int mac_set_phase_events(void *before_step, void *after_step, void *after_append
  *   22/23 band tokens / band pieces the CTA attended
  *   24 last band piece's tiles done   25 time spent waiting for band tiles (ns)
  *   26/27 producer: short-band list seen / long-band layout published
+ *   28/29 time spent waiting for match chunks (ns) / match chunks scanned
  * Stamps of phases a launch does not run are left as they were.  The buffer
  * must hold MAC_TRACE_POINTS * (number of SMs) uint64.  The hook clears
  * itself. */
-#define MAC_TRACE_POINTS 28
+#define MAC_TRACE_POINTS 30
 int mac_set_trace(void *device_buffer);
 
 /* Static string for a MAC_OK / MAC_ERR_* code. */

@@ -104,22 +104,32 @@ template <typename T, int G, bool PAGED>
 struct Step {
   static constexpr int kRowBytes = kHeadDim * (int)sizeof(T);
   static constexpr int kTileTok = kStageBytes / (2 * kRowBytes);  // 64 (bf16) / 32 (fp32)
-  static constexpr int kTPG = kTileTok / 32;                      // tokens per lane group per tile
   static constexpr int kMatchRows = kStageBytes / kRowBytes;      // ring rows per stage
   static constexpr int kRPG = kMatchRows / 32;                    // rows per lane group per match chunk
   static constexpr int kPer = 16 / (int)sizeof(T);                // elements per 16-byte piece
   static constexpr int kNP = 16 / kPer;                           // pieces per lane (16 dims)
   static constexpr int kPairs = 8;                                // float2 pairs per lane (16 dims)
-  static constexpr int kV = kTPG * G;                             // scores of a lane group per tile
-  static constexpr int kScat = ilog2c(kV);                        // reduce-scatter levels
-  static constexpr int kPlain = 3 - kScat;                        // plain butterfly levels after them
+  // attention: a half-warp (16 lanes, 8 dims each) per token; kAGroups
+  // half-warps per CTA, kATPG tokens each per tile
+  static constexpr int kAGroups = kWarps * 2;
+  static constexpr int kATPG = kTileTok / kAGroups;               // 4 (bf16) / 2 (fp32)
+  static constexpr int kAPairs = 4;                               // float2 pairs per lane (8 dims)
+  static constexpr int kALoads = 8 * (int)sizeof(T) / 16;         // 16-byte loads per lane and row
+  static constexpr int kAV = kATPG * G;                           // scores of a half-warp per tile
+  static constexpr int kAScat = ilog2c(kAV);                      // reduce-scatter levels
+  static constexpr int kAPlain = 4 - kAScat;                      // plain butterfly levels after them
+  static constexpr int kLogG = ilog2c(G);
+  static constexpr int kLogATPG = ilog2c(kATPG);
   static constexpr int kQBytes = G * kRowBytes;
+  // per-stage side buffer: a tile's G query rows, or a match chunk's query
+  // row and ring positions
+  static constexpr int kAux = (kQBytes > kRowBytes + 4 * kMatchRows ? kQBytes : kRowBytes + 4 * kMatchRows);
   static constexpr int kOutPer = (G * kHeadDim + kConsumers - 1) / kConsumers;
-  static_assert(kV <= 8, "one score per lane of a group at most");
+  static_assert(kAV <= 16 && kAV >= 2, "one score per lane of a half-warp at most");
 
   // dynamic shared memory layout
   static constexpr size_t kOffQ = (size_t)kStages * kStageBytes;
-  static constexpr size_t kOffBar = kOffQ + (size_t)kStages * kQBytes;     // full[kStages], empty[kStages]
+  static constexpr size_t kOffBar = kOffQ + (size_t)kStages * kAux;       // full[kStages], empty[kStages]
   static constexpr size_t kOffQrot = kOffBar + 128;                        // [G][d] f32
   static constexpr size_t kOffRedO = kOffQrot + 4 * (size_t)G * kHeadDim;  // [kWarps][4][G][d]
   static constexpr size_t kOffRedL = kOffRedO + 4 * (size_t)kWarps * 4 * G * kHeadDim;
@@ -148,7 +158,8 @@ struct Step {
 
   struct Smem {
     uint8_t *stage;     // [kStages][kStageBytes]
-    uint8_t *qbuf;      // [kStages][G][d]: pre-RoPE query rows of a piece's unit
+    uint8_t *qbuf;      // [kStages][kAux]: pre-RoPE query rows of a piece's unit, or a
+                        // match chunk's query row and ring positions
     uint64_t *full;     // [kStages]: the stage's copy has landed
     uint64_t *empty;    // [kStages]: every consumer warp is done with the stage
     float *qrot;        // [G][d]: rotated, scaled query of the current piece
@@ -323,9 +334,12 @@ struct Step {
       int64_t st = carry;
       if (c < P) {
         if (U <= P) {
-          const int u = (int)(((long long)(c + 1) * U - 1) / P);
-          const int a = (int)((long long)u * P / U), k = (int)((long long)(u + 1) * P / U) - a;
-          st = off[u] + (off[u + 1] - off[u]) * (c - a) / k;
+          // unit u owns CTAs [a, a + k); all 32-bit (c, U, P <= 1024)
+          const int u = ((c + 1) * U - 1) / P;
+          const int a = u * P / U, k = (u + 1) * P / U - a;
+          const int64_t len = off[u + 1] - off[u];
+          st = off[u] + (len < (1LL << 22) ? (int64_t)((uint32_t)len * (uint32_t)(c - a) / (uint32_t)k)
+                                           : div_s64(len * (c - a), k));
         } else {
           st = part_of(c, carry, P);
         }
@@ -561,10 +575,10 @@ struct Step {
       const uint8_t *q = (const uint8_t *)p.q;
       const int64_t bh0 = (int64_t)b * p.Hq + g * G;
       if (p.q_stride == kHeadDim && p.q_offset == 0) {  // the group's G rows are contiguous
-        bulk_g2s(smem_addr(S.qbuf + (size_t)st * kQBytes), q + (size_t)bh0 * kRowBytes, kQBytes, bar);
+        bulk_g2s(smem_addr(S.qbuf + (size_t)st * kAux), q + (size_t)bh0 * kRowBytes, kQBytes, bar);
       } else {
         for (int hh = 0; hh < G; ++hh)
-          bulk_g2s(smem_addr(S.qbuf + (size_t)st * kQBytes + hh * kRowBytes),
+          bulk_g2s(smem_addr(S.qbuf + (size_t)st * kAux + hh * kRowBytes),
                    q + (size_t)((bh0 + hh) * p.q_stride + p.q_offset) * sizeof(T), kRowBytes, bar);
       }
     }
@@ -602,6 +616,7 @@ struct Step {
         *S.abort = 1;
         return false;
       }
+      __nanosleep(64);  // leave the issue slots to the warp doing the work
     }
     __threadfence_block();
     return true;
@@ -627,57 +642,53 @@ struct Step {
     return n;
   }
 
-  // Match chunks of this CTA (stage uses n, n+1, ... while below `until`),
-  // in the order the consumers use them; returns the next use.
-  __device__ static uint32_t copy_match(const StepParams &p, const Smem &S, uint32_t n, uint32_t until) {
+  // Match chunks i0 .. i1-1 of this CTA (chunk i is j = c + i*P) into stage
+  // uses n, n+1, ...; returns the next use.
+  __device__ static uint32_t copy_match(const StepParams &p, const Smem &S, uint32_t n, int i0, int i1) {
     const int P = gridDim.x;
     const int cph = chunks_per_head(p.K);
-    const int nc = p.B * p.Hq * cph;
     const unsigned long long pol = l2_evict_first_policy();
-    for (int j = blockIdx.x + (int)n * P; j < nc && n < until; j += P, ++n) {
+    for (int i = i0; i < i1; ++i, ++n) {
       if (!acquire_stage(p, S, n)) break;
+      const int j = blockIdx.x + i * P;
       const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
       const int rows = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
       const int st = n % kStages;
       const uint32_t bar = smem_addr(&S.full[st]);
-      mbar_expect_tx(bar, (uint32_t)rows * kRowBytes);
+      const bool pos_copy = pos_by_copy(p);
+      mbar_expect_tx(bar, (uint32_t)rows * kRowBytes + kRowBytes + (pos_copy ? 4u * rows : 0u));
       bulk_g2s_hint(smem_addr(S.stage + (size_t)st * kStageBytes),
                     (const uint8_t *)p.ring_q + ((size_t)bh * p.K + slot0) * kRowBytes,
                     (uint32_t)rows * kRowBytes, bar, pol);
+      // the head's query row and the chunk's ring positions, into the side buffer
+      uint8_t *side = S.qbuf + (size_t)st * kAux;
+      bulk_g2s(smem_addr(side), (const uint8_t *)p.q + (size_t)((int64_t)bh * p.q_stride + p.q_offset) * sizeof(T),
+               kRowBytes, bar);
+      if (pos_copy)
+        bulk_g2s(smem_addr(side + kRowBytes), p.ring_pos + (size_t)(bh / p.Hq) * p.K + slot0, 4u * rows, bar);
     }
     return n;
   }
+  // Ring positions come with the chunk when their rows are 16-byte aligned.
+  __device__ static bool pos_by_copy(const StepParams &p) { return (p.K & 3) == 0; }
 
-  // The tiles of the pieces of CTA span g0..g1 of phase ph, from stage use n
-  // on; returns the next use.  Run by one lane.
-  __device__ static uint32_t copy_span(const StepParams &p, const Smem &S, int ph, uint32_t n) {
-    const int U = p.B * p.Hkv;
-    const int64_t *off = offs(S, ph);
-    const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
-    if (g0 >= g1) return n;
-    Piece pc;
-    int u = unit_of(off, U, g0);
-    while (!*S.abort && find_piece(p, S, ph, u, g0, g1, &pc)) {
-      n = copy_piece(p, S, pc, n);
-      u = pc.u + 1;
-    }
-    return n;
-  }
-
-  // The producer warp.  Its first lane starts the match copies (they need
-  // nothing but the parameters); the warp then lays out every unit's
+  // The producer warp.  Its first lane starts the first match copies (they
+  // need nothing but the parameters); the warp then lays out every unit's
   // position and the tail spans (for full attention also the band starts
   // and the short-band list) and publishes them, and the first lane copies
-  // the rest of the match chunks and the tail tiles, then the short pieces
+  // the tail tiles and the rest of the match chunks, then the short pieces
   // once the short-band list is published, then the long-band pieces once
   // their spans are.  Every copy goes in the order the consumers use the
-  // stages: match chunks, tail pieces, short pieces, long-band pieces.
+  // stages: kEarlyChunks match chunks, tail pieces, the other match chunks,
+  // short pieces, long-band pieces.
   __device__ static void producer_warp(const StepParams &p, const Smem &S) {
     const int lane = threadIdx.x & 31, U = p.B * p.Hkv;
     unsigned long long *tr = lane == 0 ? cta_trace(p) : nullptr;
     const bool decode = p.mode == MODE_DECODE;
     uint32_t n = 0;
-    if (decode && lane == 0) n = copy_match(p, S, 0, kStages);
+    const int nchunks = decode ? match_chunks(p) : 0;
+    const int early = nchunks < kEarlyChunks ? nchunks : kEarlyChunks;
+    if (lane == 0) n = copy_match(p, S, 0, 0, early);
     __syncwarp();
     for (int u = lane; u < U; u += 32) {
       S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
@@ -687,9 +698,8 @@ struct Step {
     }
     __syncwarp();
     layout_tail_warp(p, S);
-    if (!decode) band_units_warp(p, S);  // every band starts at 1
     __threadfence_block();
-    if (lane == 0) *S.ready = decode ? 1 : 2;
+    if (lane == 0) *S.ready = 1;
     __syncwarp();
     if (decode && !PAGED) {
       // the tile a recent match's band needs (a hit at m-1 starts it at
@@ -705,19 +715,23 @@ struct Step {
       }
     }
     if (lane == 0) {
-      if (decode) n = copy_match(p, S, n, 0xFFFFFFFFu);
-      n = copy_span(p, S, 0, n);
-      if (!wait_ready(p, S, 2)) *S.abort = 1;
-      if (tr) tr[26] = globaltimer();
-      if (!*S.abort) {
-        int j0, j1;
-        short_range(S, &j0, &j1);
-        for (int j = j0; j < j1 && !*S.abort; ++j) n = copy_piece(p, S, short_piece(p, S, j), n);
+      // tails (the unit layout is known), the rest of the match, then the
+      // short bands and the long bands as their layouts are published
+#pragma unroll 1
+      for (int kind = 0; kind < 3 && !*S.abort; ++kind) {
+        if (kind == 1) {
+          n = copy_match(p, S, n, early, nchunks);
+          if (!wait_ready(p, S, 2)) break;
+          if (tr) tr[26] = globaltimer();
+        } else if (kind == 2) {
+          if (tr) tr[9] = globaltimer();
+          if (!wait_ready(p, S, 3)) break;
+          if (tr) tr[27] = globaltimer();
+        }
+        PieceIter I = piece_iter(p, S, kind);
+        Piece pc;
+        while (!*S.abort && next_piece(p, S, I, pc)) n = copy_piece(p, S, pc, n);
       }
-      if (tr) tr[9] = globaltimer();
-      if (!wait_ready(p, S, 3)) *S.abort = 1;
-      if (tr) tr[27] = globaltimer();
-      if (!*S.abort) n = copy_span(p, S, 1, n);
       __threadfence_block();
       *S.issued = n;
     }
@@ -784,64 +798,97 @@ struct Step {
     if ((threadIdx.x & 31) == 0 && bp >= 1) atomicMax(&S.best[bh], pack_best(bd, bp));
   }
 
-  __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n) {
-    const int P = gridDim.x;
+  // Scan match chunk j (stage use n): its rows, the head's query row and
+  // (K a multiple of 4) the rows' positions all arrive in the stage.
+  __device__ static void match_chunk(const StepParams &p, const Smem &S, uint32_t n, int j, int grp, int sub,
+                                     unsigned long long &wait_ns) {
     const int cph = chunks_per_head(p.K);
-    const int nc = p.B * p.Hq * cph;
-    const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31, sub = lane & 7;
-    const int grp = warp * 4 + (lane >> 3);  // row group: rows grp, grp + 32, ... of a chunk
-    for (int j = blockIdx.x; j < nc; j += P, ++n) {
-      const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
-      const int cnt = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
-      const int b = bh / p.Hq;
-      // the head's query (its 16 elements per lane), loaded before the wait
-      float2 qv[kPairs];
-      const uint8_t *qrow = (const uint8_t *)p.q + (size_t)((int64_t)bh * p.q_stride + p.q_offset) * sizeof(T);
-#pragma unroll
-      for (int cc = 0; cc < kNP; ++cc)
-        unpack16x2<T>(__ldg(reinterpret_cast<const uint4 *>(qrow + cc * 128 + sub * 16)), qv + cc * (kPer / 2));
-      const int64_t m = (int64_t)__ldg(p.pos_base + b) + p.pos_add - p.len_sub;
-      int pos_lo = 1, pos_hi = 0;
-      if (len_ok(p, m)) {
-        pos_lo = m - p.K > 1 ? (int)(m - p.K) : 1;
-        pos_hi = (int)(m - 1);
-      }
-      // the positions of the group's rows, also before the wait
+    const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
+    const int cnt = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
+    const int b = bh / p.Hq;
+    const bool pos_copy = pos_by_copy(p);
+    int pk[kRPG];
+    if (!pos_copy) {
       const int32_t *rp = p.ring_pos + (int64_t)b * p.K + slot0;
-      int pk[kRPG];
 #pragma unroll
       for (int k = 0; k < kRPG; ++k) {
         const int i = grp + 32 * k;
         pk[k] = __ldg(rp + (i < cnt ? i : cnt - 1));
       }
-      const bool ok = wait_use(p, S, n);
-      if (n == 0) stamp(cta_trace(p), 8);
-      const uint8_t *rows = S.stage + (size_t)(n % kStages) * kStageBytes;
-      // all of the group's rows at once (independent chains), then a tree;
-      // rows past the chunk read stale stage bytes and are not considered
-      float D[kRPG];
-      int ps[kRPG];
+    }
+    const int64_t m = S.X[b];  // the request's length, tabled before the match
+    int pos_lo = 1, pos_hi = 0;
+    if (len_ok(p, m)) {
+      pos_lo = m - p.K > 1 ? (int)(m - p.K) : 1;
+      pos_hi = (int)(m - 1);
+    }
+    const bool timed = threadIdx.x == 0 && p.trace;
+    const unsigned long long tw = timed ? globaltimer() : 0ull;
+    const bool ok = wait_use(p, S, n);
+    if (timed) wait_ns += globaltimer() - tw;
+    if (n == 0) stamp(cta_trace(p), 8);
+    const int st = n % kStages;
+    const uint8_t *rows = S.stage + (size_t)st * kStageBytes;
+    const uint8_t *side = S.qbuf + (size_t)st * kAux;
+    float2 qv[kPairs];
+#pragma unroll
+    for (int cc = 0; cc < kNP; ++cc)
+      unpack16x2<T>(*reinterpret_cast<const uint4 *>(side + cc * 128 + sub * 16), qv + cc * (kPer / 2));
+    if (pos_copy) {
+      const int32_t *sp = reinterpret_cast<const int32_t *>(side + kRowBytes);
 #pragma unroll
       for (int k = 0; k < kRPG; ++k) {
         const int i = grp + 32 * k;
-        const int ri = i < cnt ? i : cnt - 1;
-        D[k] = row_dist(rows + (size_t)ri * kRowBytes, sub, qv);
-        const bool valid = ok && i < cnt && pk[k] >= pos_lo && pk[k] <= pos_hi;
-        ps[k] = valid ? pk[k] : -1;
-        D[k] = valid ? D[k] : INFINITY;
+        pk[k] = sp[i < cnt ? i : cnt - 1];
       }
+    }
+    // all of the group's rows at once (independent chains), then a tree;
+    // rows past the chunk read stale stage bytes and are not considered
+    float D[kRPG];
+    int ps[kRPG];
 #pragma unroll
-      for (int w = 1; w < kRPG; w <<= 1)
+    for (int k = 0; k < kRPG; ++k) {
+      const int i = grp + 32 * k;
+      const int ri = i < cnt ? i : cnt - 1;
+      D[k] = row_dist(rows + (size_t)ri * kRowBytes, sub, qv);
+      const bool valid = ok && i < cnt && pk[k] >= pos_lo && pk[k] <= pos_hi;
+      ps[k] = valid ? pk[k] : -1;
+      D[k] = valid ? D[k] : INFINITY;
+    }
 #pragma unroll
-        for (int k = 0; k + w < kRPG; k += 2 * w)
-          if (better(D[k + w], ps[k + w], D[k], ps[k])) {
-            D[k] = D[k + w];
-            ps[k] = ps[k + w];
-          }
-      release(S, n);
-      flush_best(S, bh, D[0], ps[0]);
+    for (int w = 1; w < kRPG; w <<= 1)
+#pragma unroll
+      for (int k = 0; k + w < kRPG; k += 2 * w)
+        if (better(D[k + w], ps[k + w], D[k], ps[k])) {
+          D[k] = D[k + w];
+          ps[k] = ps[k + w];
+        }
+    release(S, n);
+    flush_best(S, bh, D[0], ps[0]);
+  }
+
+  // Match chunks i0 .. i1-1 of this CTA (chunk i is j = c + i*P), from stage
+  // use n on.
+  __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n, int i0, int i1) {
+    const int P = gridDim.x;
+    const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31, sub = lane & 7;
+    const int grp = warp * 4 + (lane >> 3);  // row group: rows grp, grp + 32, ... of a chunk
+    unsigned long long wait_ns = 0;
+#pragma unroll 1
+    for (int i = i0; i < i1; ++i) match_chunk(p, S, n++, blockIdx.x + i * P, grp, sub, wait_ns);
+    unsigned long long *tr = threadIdx.x == 0 ? cta_trace(p) : nullptr;
+    if (tr) {
+      tr[28] += wait_ns;
+      tr[29] += (unsigned long long)(i1 > i0 ? i1 - i0 : 0);
     }
   }
+
+  // Match chunks of this CTA, and how many come before its tail pieces.
+  __device__ static int match_chunks(const StepParams &p) {
+    const int nc = p.B * p.Hq * chunks_per_head(p.K), P = gridDim.x, c = blockIdx.x;
+    return c < nc ? (nc - c + P - 1) / P : 0;
+  }
+  static constexpr int kEarlyChunks = 2;
 
   // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.
   __device__ static void grid_barrier(const StepParams &p, const Smem &S) {
@@ -890,26 +937,32 @@ struct Step {
     }
     consumer_sync();
     stamp(trace, 5);
-    if (tid < 32) {
+  }
+
+  // Every unit's band start and the short-band list (warp 0), after which
+  // the producer may copy short pieces, then the long-band spans (all
+  // consumer threads), after which it may copy long-band pieces.  Ends with
+  // a consumer barrier.
+  __device__ static void layout_bands(const StepParams &p, const Smem &S, unsigned long long *trace) {
+    if (threadIdx.x < 32) {
       band_units_warp(p, S);
       __threadfence_block();
-      if (tid == 0) *S.ready = 2;  // the producer may copy the short pieces
+      if (threadIdx.x == 0) *S.ready = 2;
       __syncwarp();
     }
     consumer_sync();
     band_spans_block(p, S);
-    if (tid == 0) {
+    if (threadIdx.x == 0) {
       __threadfence_block();
       *S.ready = 3;
     }
+    (void)trace;
   }
 
   // ---------------------------------------------------------------------
   // attention over the CTA's pieces
   // ---------------------------------------------------------------------
 
-  // Lane element k (0..15) of a 16-dim share: piece k / kPer, offset k % kPer.
-  __device__ static int lane_dim(int k, int sub) { return piece_dim(k / kPer, sub) + k % kPer; }
 
   // cos, sin of rotation angle j of request b at position pos: from the
   // CTA's table when there is one, else computed here.
@@ -935,7 +988,7 @@ struct Step {
     for (int i = threadIdx.x; i < G * half; i += kConsumers) {
       const int hh = i / half, j = i % half;
       const int ia = inter ? 2 * j : j, ib = inter ? 2 * j + 1 : j + half;
-      const void *row = S.qbuf + (size_t)st * kQBytes + hh * kRowBytes;
+      const void *row = S.qbuf + (size_t)st * kAux + hh * kRowBytes;
       const float a = elem_f32<T>(row, ia), bb = elem_f32<T>(row, ib);
       const float2 cs = p.rope_mode == MAC_ROPE_NONE ? make_float2(1.f, 0.f) : rope_cs(p, S, b, pos, j);
       float ra, rb;
@@ -947,30 +1000,17 @@ struct Step {
     consumer_sync();
   }
 
-  // the lane's 16 dims of head hh's rotated query
-  __device__ static void query_pairs(const Smem &S, int hh, int sub, float2 (&q)[kPairs]) {
+  // v[i] (i = token slot * G + head, partial dot products of the lane's 8
+  // dims) -> the full dot product of slot sub >> kAPlain: reduce-scatter
+  // over the half-warp (xor 8, 4, ...), then plain butterflies for the rest.
+  __device__ static float reduce_scores(float (&v)[kAV], int lane) {
 #pragma unroll
-    for (int c = 0; c < kNP; ++c)
-#pragma unroll
-      for (int e4 = 0; e4 < kPer; e4 += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(S.qrot + hh * kHeadDim + piece_dim(c, sub) + e4);
-        q[(c * kPer + e4) / 2] = make_float2(v.x, v.y);
-        q[(c * kPer + e4) / 2 + 1] = make_float2(v.z, v.w);
-      }
-  }
-
-  // v[i] (i = token slot * G + head, partial dot products of the lane's 16
-  // dims) -> the full dot product of slot sub >> kPlain: reduce-scatter over
-  // the group's lanes (xor 4, 2, 1), then plain butterflies for the rest.
-  __device__ static float reduce_scores(float (&v)[kV], int lane) {
-#pragma unroll
-    for (int lev = 0; lev < kScat; ++lev) {
-      const int off = 4 >> lev;
+    for (int lev = 0; lev < kAScat; ++lev) {
+      const int off = 8 >> lev;
       const bool up = (lane & off) != 0;
-      constexpr int kMax = kV;
-      const int half = kMax >> (lev + 1);
+      const int half = kAV >> (lev + 1);
 #pragma unroll
-      for (int i = 0; i < kMax / 2; ++i) {
+      for (int i = 0; i < kAV / 2; ++i) {
         if (i < half) {
           const float send = up ? v[i] : v[i + half];
           const float keep = up ? v[i + half] : v[i];
@@ -980,12 +1020,36 @@ struct Step {
     }
     float s = v[0];
 #pragma unroll
-    for (int lev = kScat; lev < 3; ++lev) s += __shfl_xor_sync(kFull, s, 4 >> lev);
+    for (int lev = kAScat; lev < 4; ++lev) s += __shfl_xor_sync(kFull, s, 8 >> lev);
     return s;
   }
 
+  // max / sum over the lanes of the half-warp whose score slots hold the
+  // same head (the token bits of the slot index)
+  __device__ static float head_max(float x) {
+#pragma unroll
+    for (int b = 0; b < kLogATPG; ++b) x = fmaxf(x, __shfl_xor_sync(kFull, x, 1 << (kAPlain + kLogG + b)));
+    return x;
+  }
+  __device__ static float head_sum(float x) {
+#pragma unroll
+    for (int b = 0; b < kLogATPG; ++b) x += __shfl_xor_sync(kFull, x, 1 << (kAPlain + kLogG + b));
+    return x;
+  }
+
+  // the lane's 8 dims (d = 8 sub .. 8 sub + 7) of row `row`
+  __device__ static void row_dims(const uint8_t *base, int row, int sub, float2 (&f)[kAPairs]) {
+#pragma unroll
+    for (int c = 0; c < kALoads; ++c)
+      unpack16x2<T>(*reinterpret_cast<const uint4 *>(base + row * kRowBytes + sub * 8 * (int)sizeof(T) + c * 16),
+                    f + c * (kAPairs / kALoads));
+  }
+
   // One piece: tokens [pc.lo, pc.hi] of unit pc.u for its G heads; the
-  // piece's partial summary goes to dst ([G][kPartStride]).
+  // piece's partial summary goes to dst ([G][kPartStride]).  A half-warp
+  // takes one token of a kATPG-token slot of every tile; lane `sub` owns
+  // dims 8 sub .. 8 sub + 7 of the rotated query (held in registers for the
+  // whole piece) and of the weighted values.
   __device__ static void attend_piece(const StepParams &p, const Smem &S, uint32_t &n, int ph,
                                       const Piece &pc, float *dst, bool first_piece) {
     unsigned long long *trace = first_piece ? cta_trace(p) : nullptr;
@@ -994,25 +1058,27 @@ struct Step {
       tr_all[22] += (unsigned long long)(pc.hi - pc.lo + 1);
       tr_all[23] += 1;
     }
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = lane >> 3, sub = lane & 7;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, sub = lane & 15;
+    const int grp = warp * 2 + (lane >> 4);  // this half-warp: rows grp, grp + 16, ... of a tile
+    const int idx = sub >> kAPlain;          // this lane's score slot
+    const int ti = idx / G, hm = idx % G;    // its token (of the group's kATPG) and head
     const int b = pc.u / p.Hkv, g = pc.u % p.Hkv;
-    const int idx = sub >> kPlain;         // this lane's score slot
-    const int ti = idx / G, hm = idx % G;  // its token (within the group's tile share) and head
-    int lo_mine = pc.lo;                   // first token of the lane's head in this piece
+    int lo_mine = pc.lo;                     // first token of the lane's head in this piece
     if (ph == 1 && p.mode == MODE_DECODE) {
       const int pp = S.X[b * p.Hq + g * G + hm];
       const int lh = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
       lo_mine = lh > lo_mine ? lh : lo_mine;
     }
-    float2 o[G][kPairs];
+    float2 o[G][kAPairs], q[G][kAPairs];
     float mrun[G];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
       mrun[hh] = kMInit;
 #pragma unroll
-      for (int i = 0; i < kPairs; ++i) o[hh][i] = make_float2(0.f, 0.f);
+      for (int i = 0; i < kAPairs; ++i) o[hh][i] = make_float2(0.f, 0.f);
     }
     float m_mine = kMInit, l_mine = 0.f;
+    unsigned long long wait_ns = 0;  // traced band waits (kept in a register)
 
     const int64_t tile0 = (pc.lo - 1) / kTileTok;
     const int ntiles = (int)((pc.hi - 1) / kTileTok - tile0 + 1);
@@ -1020,55 +1086,54 @@ struct Step {
       const int st = n % kStages;
       const unsigned long long tw = tr_all ? globaltimer() : 0ull;
       const bool ok = wait_use(p, S, n);
-      if (tr_all) tr_all[25] += globaltimer() - tw;
+      if (tr_all) wait_ns += globaltimer() - tw;
       if (k == 0) {
         stamp(trace, ph ? 13 : 11);
         rotate_query(p, S, st, b, S.u_pos[pc.u]);
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float4 x0 = *reinterpret_cast<const float4 *>(S.qrot + hh * kHeadDim + sub * 8);
+          const float4 x1 = *reinterpret_cast<const float4 *>(S.qrot + hh * kHeadDim + sub * 8 + 4);
+          q[hh][0] = make_float2(x0.x, x0.y);
+          q[hh][1] = make_float2(x0.z, x0.w);
+          q[hh][2] = make_float2(x1.x, x1.y);
+          q[hh][3] = make_float2(x1.z, x1.w);
+        }
       }
       const uint8_t *kb = S.stage + (size_t)st * kStageBytes;
       const uint8_t *vb = kb + kStageBytes / 2;
       const int t0 = (int)((tile0 + k) * kTileTok);
-      // partial scores of the group's kTPG tokens for the G heads
-      float2 kf[kTPG][kPairs];
+      // partial scores of the group's kATPG tokens for the G heads
+      float v[kAV];
 #pragma unroll
-      for (int tt = 0; tt < kTPG; ++tt) {
-        const int row = tt * 32 + warp * 4 + lg;
+      for (int tt = 0; tt < kATPG; ++tt) {
+        float2 kf[kAPairs];
+        row_dims(kb, tt * kAGroups + grp, sub, kf);
 #pragma unroll
-        for (int c = 0; c < kNP; ++c)
-          unpack16x2<T>(*reinterpret_cast<const uint4 *>(kb + row * kRowBytes + c * 128 + sub * 16),
-                        kf[tt] + c * (kPer / 2));
-      }
-      float v[kV];
+        for (int hh = 0; hh < G; ++hh) {
+          float2 acc = __fmul2_rn(q[hh][0], kf[0]);
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float2 q[kPairs];
-        query_pairs(S, hh, sub, q);
-#pragma unroll
-        for (int tt = 0; tt < kTPG; ++tt) {
-          float2 acc = __fmul2_rn(q[0], kf[tt][0]);
-#pragma unroll
-          for (int i = 1; i < kPairs; ++i) acc = __ffma2_rn(q[i], kf[tt][i], acc);
+          for (int i = 1; i < kAPairs; ++i) acc = __ffma2_rn(q[hh][i], kf[i], acc);
           v[tt * G + hh] = acc.x + acc.y;
         }
       }
       float s = reduce_scores(v, lane);
-      const int row_m = ti * 32 + warp * 4 + lg;
+      const int row_m = ti * kAGroups + grp;
       const int t_m = t0 + row_m + 1;
       const bool valid = ok && t_m >= lo_mine && t_m <= pc.hi && ((S.mask[st] >> (row_m >> 4)) & 1);
       s = valid ? s : -INFINITY;
       // lazy running max (per group and head): raised only when a score
       // exceeds it by kLazy
-      float mt = s;
-      if (kTPG == 2) mt = fmaxf(mt, __shfl_xor_sync(kFull, s, 4));
+      const float mt = head_max(s);
       if (__any_sync(kFull, mt > m_mine + kLazy)) {
         const float mn_mine = fmaxf(m_mine, mt);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
-          const float mn = __shfl_sync(kFull, mn_mine, (lane & 24) | (hh << kPlain));
+          const float mn = __shfl_sync(kFull, mn_mine, (lane & 16) | (hh << kAPlain));
           const float f = ex2(mrun[hh] - mn);
           const float2 f2 = make_float2(f, f);
 #pragma unroll
-          for (int i = 0; i < kPairs; ++i) o[hh][i] = __fmul2_rn(o[hh][i], f2);
+          for (int i = 0; i < kAPairs; ++i) o[hh][i] = __fmul2_rn(o[hh][i], f2);
           mrun[hh] = mn;
         }
         l_mine *= ex2(m_mine - mn_mine);
@@ -1076,58 +1141,57 @@ struct Step {
       }
       const float w = ex2(s - m_mine);
       l_mine += w;
-      float wa[kV];
-#pragma unroll
-      for (int i = 0; i < kV; ++i) wa[i] = __shfl_sync(kFull, w, (lane & 24) | (i << kPlain));
       // rows the piece did not copy hold stale bytes, possibly NaN patterns,
       // and 0 * NaN is NaN: in a partly covered tile they are zeroed
       const int msk = S.mask[st];
       const bool whole = t0 + 1 >= pc.lo && t0 + kTileTok <= pc.hi && msk == (1 << (kTileTok / 16)) - 1;
 #pragma unroll
-      for (int tt = 0; tt < kTPG; ++tt) {
-        const int row = tt * 32 + warp * 4 + lg;
-        uint4 raw[kNP];
+      for (int tt = 0; tt < kATPG; ++tt) {
+        const int row = tt * kAGroups + grp;
+        uint4 raw[kALoads];
 #pragma unroll
-        for (int c = 0; c < kNP; ++c) raw[c] = *reinterpret_cast<const uint4 *>(vb + row * kRowBytes + c * 128 + sub * 16);
+        for (int c = 0; c < kALoads; ++c)
+          raw[c] = *reinterpret_cast<const uint4 *>(vb + row * kRowBytes + sub * 8 * (int)sizeof(T) + c * 16);
         if (!whole) {
           const int t = t0 + row + 1;
           const uint32_t vm = (t >= pc.lo && t <= pc.hi && ((msk >> (row >> 4)) & 1)) ? ~0u : 0u;
 #pragma unroll
-          for (int c = 0; c < kNP; ++c) raw[c] = make_uint4(raw[c].x & vm, raw[c].y & vm, raw[c].z & vm, raw[c].w & vm);
+          for (int c = 0; c < kALoads; ++c) raw[c] = make_uint4(raw[c].x & vm, raw[c].y & vm, raw[c].z & vm, raw[c].w & vm);
         }
-        float2 vf[kPairs];
+        float2 vf[kAPairs];
 #pragma unroll
-        for (int c = 0; c < kNP; ++c) unpack16x2<T>(raw[c], vf + c * (kPer / 2));
+        for (int c = 0; c < kALoads; ++c) unpack16x2<T>(raw[c], vf + c * (kAPairs / kALoads));
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
-          const float2 w2 = make_float2(wa[tt * G + hh], wa[tt * G + hh]);
+          const float wv = __shfl_sync(kFull, w, (lane & 16) | ((tt * G + hh) << kAPlain));
+          const float2 w2 = make_float2(wv, wv);
 #pragma unroll
-          for (int i = 0; i < kPairs; ++i) o[hh][i] = __ffma2_rn(w2, vf[i], o[hh][i]);
+          for (int i = 0; i < kAPairs; ++i) o[hh][i] = __ffma2_rn(w2, vf[i], o[hh][i]);
         }
       }
       release(S, n);
     }
     stamp(trace, ph ? 14 : 12);
-    if (tr_all) tr_all[24] = globaltimer();
+    if (tr_all) {
+      tr_all[24] = globaltimer();
+      tr_all[25] += wait_ns;
+    }
     epilogue(p, S, o, mrun, m_mine, l_mine, dst);
     if (ph == 1) stamp(trace, 15);
   }
 
-  // The CTA's 32 lane-group states -> one partial summary per head: common
-  // maximum, every group rescaled to it, then summed in a fixed order
+  // The CTA's kAGroups half-warp states -> one partial summary per head:
+  // common maximum, every group rescaled to it, then summed in a fixed order
   // through shared memory.
-  __device__ static void epilogue(const StepParams &p, const Smem &S, float2 (&o)[G][kPairs],
+  __device__ static void epilogue(const StepParams &p, const Smem &S, float2 (&o)[G][kAPairs],
                                   const float (&mrun)[G], float m_mine, float l_mine, float *dst) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, lg = lane >> 3, sub = lane & 7;
-    const int idx = sub >> kPlain, ti = idx / G, hm = idx % G;
-    float l_grp = l_mine;  // the group's sum for head hm (both token slots)
-    if (kTPG == 2) l_grp += __shfl_xor_sync(kFull, l_mine, 4);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, sub = lane & 15;
+    const int grp = warp * 2 + (lane >> 4);
+    const int idx = sub >> kAPlain, ti = idx / G, hm = idx % G;
+    const float l_grp = head_sum(l_mine);  // the group's sum for head hm (all its token slots)
     float mw[G];
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      mw[hh] = fmaxf(mrun[hh], __shfl_xor_sync(kFull, mrun[hh], 8));
-      mw[hh] = fmaxf(mw[hh], __shfl_xor_sync(kFull, mw[hh], 16));
-    }
+    for (int hh = 0; hh < G; ++hh) mw[hh] = fmaxf(mrun[hh], __shfl_xor_sync(kFull, mrun[hh], 16));
     if (lane == 0)
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) S.red_m[warp * G + hh] = mw[hh];
@@ -1144,31 +1208,26 @@ struct Step {
       const float f = ex2(mrun[hh] - mc[hh]);
       const float2 f2 = make_float2(f, f);
 #pragma unroll
-      for (int i = 0; i < kPairs; ++i) o[hh][i] = __fmul2_rn(o[hh][i], f2);
+      for (int i = 0; i < kAPairs; ++i) o[hh][i] = __fmul2_rn(o[hh][i], f2);
     }
-    if (ti == 0 && (sub & ((1 << kPlain) - 1)) == 0) {
+    if (ti == 0 && (sub & ((1 << kAPlain) - 1)) == 0) {
       float mcm = mc[0];
 #pragma unroll
       for (int hh = 1; hh < G; ++hh) mcm = hm == hh ? mc[hh] : mcm;
-      S.red_l[(warp * 4 + lg) * G + hm] = l_grp * ex2(m_mine - mcm);
+      S.red_l[grp * G + hm] = l_grp * ex2(m_mine - mcm);
     }
     {
-      float *wr = S.red_o + (size_t)(warp * 4 + lg) * G * kHeadDim;
+      float *wr = S.red_o + (size_t)grp * G * kHeadDim + sub * 8;
 #pragma unroll
-      for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-        for (int c = 0; c < kNP; ++c)
-#pragma unroll
-          for (int e4 = 0; e4 < kPer; e4 += 4) {
-            const float2 a = o[hh][(c * kPer + e4) / 2], bb = o[hh][(c * kPer + e4) / 2 + 1];
-            *reinterpret_cast<float4 *>(wr + hh * kHeadDim + piece_dim(c, sub) + e4) =
-                make_float4(a.x, a.y, bb.x, bb.y);
-          }
+      for (int hh = 0; hh < G; ++hh) {
+        *reinterpret_cast<float4 *>(wr + hh * kHeadDim) = make_float4(o[hh][0].x, o[hh][0].y, o[hh][1].x, o[hh][1].y);
+        *reinterpret_cast<float4 *>(wr + hh * kHeadDim + 4) = make_float4(o[hh][2].x, o[hh][2].y, o[hh][3].x, o[hh][3].y);
+      }
     }
     consumer_sync();
-    // each output element: the 32 group states in a fixed order (the next
-    // piece's epilogue writes these buffers only after its first barrier,
-    // which every thread reaches after these reads)
+    // each output element: the kAGroups group states in a fixed order (the
+    // next piece's epilogue writes these buffers only after its first
+    // barrier, which every thread reaches after these reads)
     float acc[kOutPer];
 #pragma unroll
     for (int j = 0; j < kOutPer; ++j) {
@@ -1177,7 +1236,7 @@ struct Step {
       if (e < G * kHeadDim) {
         float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w2 = 0; w2 < kWarps * 4; ++w2) part[w2 & 3] += S.red_o[(size_t)w2 * G * kHeadDim + e];
+        for (int w2 = 0; w2 < kAGroups; ++w2) part[w2 & 3] += S.red_o[(size_t)w2 * G * kHeadDim + e];
         acc[j] = (part[0] + part[1]) + (part[2] + part[3]);
       }
     }
@@ -1187,12 +1246,12 @@ struct Step {
       if (e < G * kHeadDim) dst[(e / kHeadDim) * kPartStride + e % kHeadDim] = acc[j];
     }
     if (warp == 0) {
-      // lane i holds group i's sums; butterfly over the 32 groups
+      // lane i < kAGroups holds group i's sums; butterfly over the groups
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        float L = S.red_l[lane * G + hh];
+        float L = lane < kAGroups ? S.red_l[lane * G + hh] : 0.f;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
+        for (int o2 = kAGroups / 2; o2 >= 1; o2 >>= 1) L += __shfl_xor_sync(kFull, L, o2);
         if (lane == hh) {
           dst[hh * kPartStride + kHeadDim] = mc[hh];
           dst[hh * kPartStride + kHeadDim + 1] = L;
@@ -1201,37 +1260,76 @@ struct Step {
     }
   }
 
-  // Partial slots: tail piece (u, CTA c) at u + c of part_a; short band of
-  // u at u of part_b, long-band piece (u, c) at n_units + u + c (the CTAs
-  // meeting a unit in a span layout form a run that starts at or after the
-  // last CTA of the previous unit, so u + c never repeats).
+  // The CTA's pieces of one kind, in the order both the producer and the
+  // consumers walk them: 0 its tail span, 1 its short bands, 2 its
+  // long-band span; kind 3 lists (without attention) the units u = c mod P
+  // whose merge no band piece triggers: no band piece (the last piece was a
+  // tail piece, before the decisions) or no piece at all (no valid length).
+  struct PieceIter {
+    int kind, it, end;
+  };
+  __device__ static PieceIter piece_iter(const StepParams &p, const Smem &S, int kind) {
+    const int U = p.B * p.Hkv, ph = kind == 0 ? 0 : 1;
+    PieceIter I;
+    I.kind = kind;
+    if (kind == 1) {
+      short_range(S, &I.it, &I.end);
+    } else if (kind == 3) {
+      I.it = blockIdx.x;
+      I.end = U;
+    } else {
+      const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
+      I.it = g0 < g1 ? unit_of(offs(S, ph), U, g0) : U;
+      I.end = U;
+    }
+    return I;
+  }
+  __device__ static bool next_piece(const StepParams &p, const Smem &S, PieceIter &I, Piece &pc) {
+    if (I.kind == 1) {
+      if (I.it >= I.end) return false;
+      pc = short_piece(p, S, I.it++);
+      return true;
+    }
+    if (I.kind == 3) {
+      for (; I.it < I.end; I.it += gridDim.x) {
+        const PieceList L = unit_list(p, S, I.it);
+        if (band_pieces(S, L) == 0 &&
+            (p.mode == MODE_DECODE || nonempty(S, 0, L.ca0, L.ca0 + (L.n - L.nb) - 1) == 0)) {
+          pc.u = I.it;
+          pc.lo = 1;
+          pc.hi = 0;
+          I.it += gridDim.x;
+          return true;
+        }
+      }
+      return false;
+    }
+    const int ph = I.kind == 0 ? 0 : 1;
+    if (!find_piece(p, S, ph, I.it, spans(S, ph)[blockIdx.x], spans(S, ph)[blockIdx.x + 1], &pc)) return false;
+    I.it = pc.u + 1;
+    return true;
+  }
 
-  // The CTA's pieces of one kind: 0 its tail span, 1 its short bands, 2 its
-  // long-band span (one loop, so the attention code is inlined once; the
-  // loop state lives in shared memory and a counter, not in registers the
-  // attention needs).  The first band piece of the CTA is traced.
+  // The consumers' side: attention of each piece, its count, and the merges
+  // it completes (one call site each, so the code is inlined once).
   __device__ static void attend_kind(const StepParams &p, const Smem &S, uint32_t &n, int kind) {
-    const int U = p.B * p.Hkv, ph = kind ? 1 : 0;
+    const int U = p.B * p.Hkv, ph = kind == 0 ? 0 : 1;
+    PieceIter I = piece_iter(p, S, kind);
     int j0, j1;
     short_range(S, &j0, &j1);
-    int it = kind == 1 ? j0 : (spans(S, ph)[blockIdx.x] < spans(S, ph)[blockIdx.x + 1]
-                                   ? unit_of(offs(S, ph), U, spans(S, ph)[blockIdx.x]) : U);
-    bool first = kind != 2 || j1 == j0;
+    bool first = kind != 2 || j1 == j0;  // the CTA's first band piece is traced
+    Piece pc;
 #pragma unroll 1
-    for (;;) {
-      Piece pc;
-      if (kind == 1) {
-        if (it >= j1) break;
-        pc = short_piece(p, S, it++);
-      } else {
-        if (!find_piece(p, S, ph, it, spans(S, ph)[blockIdx.x], spans(S, ph)[blockIdx.x + 1], &pc)) break;
-        it = pc.u + 1;
+    while (next_piece(p, S, I, pc)) {
+      int act = 2, k = 0;
+      if (kind != 3) {
+        const size_t slot = kind == 0 ? (size_t)(pc.u + blockIdx.x)
+                                      : kind == 1 ? (size_t)pc.u : (size_t)(U + pc.u + blockIdx.x);
+        attend_piece(p, S, n, ph, pc, (ph ? p.part_b : p.part_a) + slot * G * kPartStride, first);
+        first = false;
+        act = piece_count(p, S, pc.u, ph, kind == 1, &k);
       }
-      const size_t slot = kind == 0 ? (size_t)(pc.u + blockIdx.x)
-                                    : kind == 1 ? (size_t)pc.u : (size_t)(U + pc.u + blockIdx.x);
-      attend_piece(p, S, n, ph, pc, (ph ? p.part_b : p.part_a) + slot * G * kPartStride, first);
-      piece_done(p, S, pc.u, ph, kind == 1);
-      first = false;
+      if (act) merge_chain(p, S, pc.u, act, k);
     }
   }
 
@@ -1505,17 +1603,17 @@ struct Step {
     consumer_sync();
   }
 
-  // After a piece's partial is written: count it, and merge what it
-  // completes here (every CTA knows how many pieces each unit and group
-  // has, so no grid barrier is needed before the merges).  A long-band piece
-  // of a two-level unit counts in its CTA group; the group's last piece
-  // merges the group and counts the group in the unit.  A decode step's
-  // tail pieces are not counted: they all finish before the grid barrier,
-  // which orders them before every merge.
-  __device__ static void piece_done(const StepParams &p, const Smem &S, int u, int ph, bool is_short) {
+  // After a piece's partial is written: count it.  Returns what the count
+  // completes: 0 nothing, 1 CTA group *k of the unit's long band (merge it
+  // first), 2 the unit (every CTA knows how many pieces each unit and group
+  // has, so no grid barrier is needed before the merges).  A long-band
+  // piece of a two-level unit counts in its CTA group.  A decode step's tail
+  // pieces are not counted: they all finish before the grid barrier, which
+  // orders them before every merge.
+  __device__ static int piece_count(const StepParams &p, const Smem &S, int u, int ph, bool is_short, int *k) {
     const bool decode = p.mode == MODE_DECODE;
-    if (decode && ph == 0) return;
-    const int k = blockIdx.x / kGroupCtas;
+    if (decode && ph == 0) return 0;
+    *k = blockIdx.x / kGroupCtas;
     __threadfence();  // this thread's part of the partial, before the count
     consumer_sync();
     if (threadIdx.x == 0) {
@@ -1523,8 +1621,8 @@ struct Step {
       int act = 0;
       if (ph == 1 && !is_short && L.kind == kGroupList) {
         int lo, hi;
-        group_ctas(L, k, &lo, &hi);
-        const uint32_t old = atomicAdd(&p.group_done[u + k], 1u);
+        group_ctas(L, *k, &lo, &hi);
+        const uint32_t old = atomicAdd(&p.group_done[u + *k], 1u);
         act = (int)(old + 1) == nonempty(S, 1, lo, hi) ? 1 : 0;
       } else {
         const uint32_t old = atomicAdd(&p.unit_done[u], 1u);
@@ -1533,22 +1631,26 @@ struct Step {
       *S.last = act;
     }
     consumer_sync();
-    if (*S.last == 0) return;
-    const PieceList L = unit_list(p, S, u);
-    if (*S.last == 1) {
-      __threadfence();  // the group's other partials, after their counts
-      merge_unit(p, S, group_list(L, k), k);
+    return *S.last;
+  }
+
+  // The merges a count completed: group k (act 1), which then counts in the
+  // unit and may complete it, and the unit (act 2).
+  __device__ static void merge_chain(const StepParams &p, const Smem &S, int u, int act, int k) {
+    const PieceList Lu = unit_list(p, S, u);
+#pragma unroll 1
+    while (act) {
+      __threadfence();  // the other CTAs' partials, after their counts
+      merge_unit(p, S, act == 1 ? group_list(Lu, k) : Lu, act == 1 ? k : -1);
+      if (act == 2) break;
       __threadfence();  // the group partial, before the unit count
       consumer_sync();
       if (threadIdx.x == 0) {
         const uint32_t old = atomicAdd(&p.unit_done[u], 1u);
-        *S.last = (int)(old + 1) == unit_target(p, S, L) ? 2 : 0;
+        *S.last = (int)(old + 1) == unit_target(p, S, Lu) ? 2 : 0;
       }
       consumer_sync();
-    }
-    if (*S.last == 2) {
-      __threadfence();  // the other CTAs' partials, after their counts
-      merge_unit(p, S, L, -1);
+      act = *S.last;
     }
   }
 
@@ -1629,6 +1731,14 @@ struct Step {
       return;
     }
 
+    if (decode) {
+      // every request's length, for the match (X holds the decisions only
+      // after the grid barrier)
+      for (int b = tid; b < p.B; b += kConsumers) {
+        const int64_t m = (int64_t)p.pos_base[b] + p.pos_add - p.len_sub;
+        S.X[b] = m >= 1 && m <= p.max_len ? (int32_t)m : 0;
+      }
+    }
     if (S.rope && p.rope_mode != MAC_ROPE_NONE) {
       // the rotation angles of every request's query (shared by its heads)
       for (int i = tid; i < p.B * (kHeadDim / 2); i += kConsumers) {
@@ -1642,49 +1752,35 @@ struct Step {
     stamp(trace, 7);
 
     uint32_t n = 0;  // stage uses consumed so far (every consumer counts the same sequence)
-    if (decode) {
-      match_phase(p, S, n);
-      stamp(trace, 1);
-    }
-    // tail pieces (their tiles in the stages already, copied during the
-    // match): every head attends them whatever the match decides
-    // (full attention counts every piece at its unit, so it needs the whole
-    // layout first: the producer warp publishes it at once)
-    if (tid == 0) wait_ready(p, S, decode ? 1 : 2);
+    const int nchunks = decode ? match_chunks(p) : 0;
+    const int early = nchunks < kEarlyChunks ? nchunks : kEarlyChunks;
+    // the first match chunks, then the tail pieces (every head attends them
+    // whatever the match decides), whose fixed costs so overlap the copies
+    // of the other match chunks; full attention counts every piece at its
+    // unit, so it lays out the bands before the first piece
+    match_phase(p, S, n, 0, early);
+    if (tid == 0) wait_ready(p, S, 1);  // unit positions and tail spans
     consumer_sync();
-    if (!decode) {
-      band_spans_block(p, S);
-      if (tid == 0) {
-        __threadfence_block();
-        *S.ready = 3;
-      }
-    }
-    // tail pieces, short bands, long-band pieces
+    // piece kinds: tails, short bands, long bands, then the merges no piece
+    // triggers; the band layout comes before the tails (full attention) or
+    // after the match and the decisions (decode): one call site
 #pragma unroll 1
-    for (int kind = 0; kind < 3; ++kind) {
-      if (kind == 1) {
-        stamp(trace, 2);
+    for (int kind = 0; kind < 4; ++kind) {
+      if (kind == (decode ? 1 : 0)) {
         if (decode) {
+          stamp(trace, 2);
+          match_phase(p, S, n, early, nchunks);
+          stamp(trace, 1);
           grid_barrier(p, S);  // the minima of every head are final, the tail partials written
           stamp(trace, 10);
           decide(p, S, trace);
           // nobody reads the other buffer in this launch: clear it for the next
           for (int i = blockIdx.x * kConsumers + tid; i < n_bh; i += gridDim.x * kConsumers) S.best_next[i] = 0ull;
         }
+        layout_bands(p, S, trace);
         stamp(trace, 3);
-      } else if (kind == 2) {
-        if (tid == 0) wait_ready(p, S, 3);  // the long-band spans
-        consumer_sync();
       }
       attend_kind(p, S, n, kind);
-    }
-    // units whose last piece no band piece could see finish (no band: it
-    // was a tail piece before the decisions; no piece at all: no valid
-    // length) are merged by one CTA each
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const PieceList L = unit_list(p, S, u);
-      if (band_pieces(S, L) == 0 && (decode || nonempty(S, 0, L.ca0, L.ca0 + (L.n - L.nb) - 1) == 0))
-        merge_unit(p, S, L, -1);
     }
     stamp(trace, 4);
     if (tid == 0 && *S.abort) {
