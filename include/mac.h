@@ -217,7 +217,7 @@ int mac_set_phase_events(void *before_step, void *after_step, void *after_append
  * [grid][MAC_TRACE_POINTS]:
  *    0 start            1 end of the match       2 end of the tail pieces
  *    3 bands laid out   4 end of the band pieces and merges
- *    5 decisions read   6 end              7 ready to match
+ *    5 decisions read   6 end              7 tail layout published
  *    8 first match chunk arrived   9 producer: short-band tiles issued
  *   10 after the grid barrier
  *   11/12 first tail piece: first tile arrived / tiles done
@@ -231,10 +231,11 @@ int mac_set_phase_events(void *before_step, void *after_step, void *after_append
  *   24 last band piece's tiles done   25 time spent waiting for band tiles (ns)
  *   26/27 producer: short-band list seen / long-band layout published
  *   28/29 time spent waiting for match chunks (ns) / match chunks scanned
+ *   30/31 producer: first match copies issued / tail layout seen
  * Stamps of phases a launch does not run are left as they were.  The buffer
  * must hold MAC_TRACE_POINTS * (number of SMs) uint64.  The hook clears
  * itself. */
-#define MAC_TRACE_POINTS 30
+#define MAC_TRACE_POINTS 32
 int mac_set_trace(void *device_buffer);
 
 /* Static string for a MAC_OK / MAC_ERR_* code. */

@@ -308,48 +308,78 @@ struct Step {
     __syncwarp();
   }
 
-  // Tail layout, by one warp: the exclusive prefix of the tail lengths, and
-  // the CTA spans.  With at most as many units as CTAs, unit u owns the CTAs
-  // [u*P/U, (u+1)*P/U) and its tail is cut evenly among them, so no CTA
-  // meets two units (a second piece would double its fixed costs); with
-  // more units the tails, laid end to end, are cut into equal spans.
-  __device__ static void layout_tail_warp(const StepParams &p, const Smem &S) {
+  // Tail layout, by all consumer threads (ends with a consumer barrier): the
+  // exclusive prefix of the tail lengths, the CTA spans, their non-empty
+  // counts and every unit's CTA run.  With at most as many units as CTAs,
+  // unit u owns the CTAs [u*P/U, (u+1)*P/U) and its tail is cut evenly among
+  // them, so no CTA meets two units (a second piece would double its fixed
+  // costs), and everything but the prefix has a closed form; with more
+  // units the tails, laid end to end, are cut into equal spans.
+  __device__ static void layout_tails(const StepParams &p, const Smem &S) {
     int64_t *off = S.offA;
-    const int U = p.B * p.Hkv, lane = threadIdx.x & 31, P = gridDim.x;
+    const int U = p.B * p.Hkv, tid = threadIdx.x, P = gridDim.x;
+    const bool aligned = U <= P;
+    // prefix of (length << 9 | non-empty spans of the unit's CTAs); a
+    // unit's k <= P <= 256 CTAs hold min(k, length) non-empty spans
     long long carry = 0;
-    for (int base = 0; base < U; base += 32) {
-      const int u = base + lane;
-      long long x = u < U ? (long long)seg_len(p, S, 0, u) : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += y;
+    for (int base = 0; base < U; base += kConsumers) {
+      const int u = base + tid;
+      long long x = 0;
+      if (u < U) {
+        const long long len = seg_len(p, S, 0, u);
+        const int k = aligned ? (u + 1) * P / U - u * P / U : 0;
+        x = (len << 9) | (long long)(len < k ? len : k);
       }
-      if (u < U) off[u + 1] = carry + x;
-      carry += __shfl_sync(kFull, x, 31);
+      long long tot;
+      const long long ex = block_scan(S, x, &tot);
+      if (u < U) {
+        off[u + 1] = (carry + ex + x) >> 9;
+        if (aligned) S.neA[u + 1] = (int)((carry + ex + x) & 511);  // per-unit prefix, per-CTA below
+      }
+      carry += tot;
     }
-    if (lane == 0) off[0] = 0;
-    __syncwarp();
-    for (int c = lane; c <= P; c += 32) {
-      int64_t st = carry;
+    const int64_t total = carry >> 9;
+    if (tid == 0) {
+      off[0] = 0;
+      if (aligned) S.neA[0] = 0;
+    }
+    consumer_sync();
+    const int c = tid;  // P <= kMaxGrid = kConsumers: one CTA per thread (CTA P by thread 0)
+    if (aligned) {
+      int ne = 0;
       if (c < P) {
-        if (U <= P) {
-          // unit u owns CTAs [a, a + k); all 32-bit (c, U, P <= 1024)
-          const int u = ((c + 1) * U - 1) / P;
-          const int a = u * P / U, k = (u + 1) * P / U - a;
-          const int64_t len = off[u + 1] - off[u];
-          st = off[u] + (len < (1LL << 22) ? (int64_t)((uint32_t)len * (uint32_t)(c - a) / (uint32_t)k)
-                                           : div_s64(len * (c - a), k));
-        } else {
-          st = part_of(c, carry, P);
-        }
+        const int u = ((c + 1) * U - 1) / P;
+        const int a = u * P / U, k = (u + 1) * P / U - a, j = c - a;
+        const int64_t len = off[u + 1] - off[u];
+        const int64_t share = len < (1LL << 22) ? (int64_t)((uint32_t)len * (uint32_t)j / (uint32_t)k)
+                                                : div_s64(len * j, k);
+        S.spanA[c] = off[u] + share;
+        // slices 0..j-1 of the unit: all non-empty when len >= k, else one
+        // token each for len*j/k of them
+        ne = S.neA[u] + (len >= k ? j : (int)share);
       }
-      S.spanA[c] = st;
+      const int neP = (int)(carry & 511);
+      consumer_sync();  // every per-unit prefix read before the per-CTA counts overwrite it
+      if (c < P) S.neA[c] = ne;
+      if (c == 0) {
+        S.spanA[P] = total;
+        S.neA[P] = neP;
+      }
+      for (int u = tid; u < U; u += kConsumers) {
+        const int a = u * P / U, k = (u + 1) * P / U - a;
+        S.runA[u] = off[u + 1] > off[u] ? make_short2((short)a, (short)(a + k - 1)) : make_short2(0, -1);
+      }
+    } else {
+      if (c <= P) S.spanA[c] = c < P ? part_of(c, total, P) : total;
+      consumer_sync();
+      long long tot;
+      const int f = c < P && S.spanA[c] < S.spanA[c + 1] ? 1 : 0;
+      const long long ef = block_scan(S, f, &tot);
+      if (c < P) S.neA[c] = (int)ef;
+      if (c == 0) S.neA[P] = (int)tot;
+      for (int u = tid; u < U; u += kConsumers) S.runA[u] = find_run(S, 0, u);
     }
-    __syncwarp();
-    count_spans_warp(S, 0);
-    for (int u = lane; u < U; u += 32) S.runA[u] = find_run(S, 0, u);
-    __syncwarp();
+    consumer_sync();
   }
 
   // Band layout.  A band of at most max(kShortBand, all band tokens / P)
@@ -672,13 +702,12 @@ struct Step {
   // Ring positions come with the chunk when their rows are 16-byte aligned.
   __device__ static bool pos_by_copy(const StepParams &p) { return (p.K & 3) == 0; }
 
-  // The producer warp.  Its first lane starts the first match copies (they
-  // need nothing but the parameters); the warp then lays out every unit's
-  // position and the tail spans (for full attention also the band starts
-  // and the short-band list) and publishes them, and the first lane copies
-  // the tail tiles and the rest of the match chunks, then the short pieces
-  // once the short-band list is published, then the long-band pieces once
-  // their spans are.  Every copy goes in the order the consumers use the
+  // The producer warp: a copy engine.  Its first lane starts the first match
+  // copies (they need nothing but the parameters), then copies the tail
+  // tiles and the rest of the match chunks once the consumers publish the
+  // unit positions and the tail layout, the short pieces once they publish
+  // the short-band list, and the long-band pieces once they publish the
+  // long-band spans.  Every copy goes in the order the consumers use the
   // stages: kEarlyChunks match chunks, tail pieces, the other match chunks,
   // short pieces, long-band pieces.
   __device__ static void producer_warp(const StepParams &p, const Smem &S) {
@@ -688,18 +717,12 @@ struct Step {
     uint32_t n = 0;
     const int nchunks = decode ? match_chunks(p) : 0;
     const int early = nchunks < kEarlyChunks ? nchunks : kEarlyChunks;
-    if (lane == 0) n = copy_match(p, S, 0, 0, early);
-    __syncwarp();
-    for (int u = lane; u < U; u += 32) {
-      S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
-      S.u_s[u] = 1;
-      if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
-        set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
+    if (lane == 0) {
+      n = copy_match(p, S, 0, 0, early);
+      if (tr) tr[30] = globaltimer();
+      if (!wait_ready(p, S, 1)) *S.abort = 1;  // unit positions and tail layout
+      if (tr) tr[31] = globaltimer();
     }
-    __syncwarp();
-    layout_tail_warp(p, S);
-    __threadfence_block();
-    if (lane == 0) *S.ready = 1;
     __syncwarp();
     if (decode && !PAGED) {
       // the tile a recent match's band needs (a hit at m-1 starts it at
@@ -1731,6 +1754,12 @@ struct Step {
       return;
     }
 
+    for (int u = tid; u < n_units; u += kConsumers) {
+      S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
+      S.u_s[u] = 1;
+      if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
+        set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
+    }
     if (decode) {
       // every request's length, for the match (X holds the decisions only
       // after the grid barrier)
@@ -1749,6 +1778,11 @@ struct Step {
       }
     }
     consumer_sync();
+    layout_tails(p, S);
+    if (tid == 0) {
+      __threadfence_block();
+      *S.ready = 1;  // the producer may copy tail tiles
+    }
     stamp(trace, 7);
 
     uint32_t n = 0;  // stage uses consumed so far (every consumer counts the same sequence)
@@ -1759,8 +1793,6 @@ struct Step {
     // of the other match chunks; full attention counts every piece at its
     // unit, so it lays out the bands before the first piece
     match_phase(p, S, n, 0, early);
-    if (tid == 0) wait_ready(p, S, 1);  // unit positions and tail spans
-    consumer_sync();
     // piece kinds: tails, short bands, long bands, then the merges no piece
     // triggers; the band layout comes before the tails (full attention) or
     // after the match and the decisions (decode): one call site

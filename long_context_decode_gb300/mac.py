@@ -14,7 +14,7 @@ from . import build as _build
 
 MAC_OK, MAC_ERR_INVALID_ARG, MAC_ERR_UNSUPPORTED, MAC_ERR_CUDA = 0, -1, -2, -3
 MAC_DEV_BAD_SEQ_LEN, MAC_DEV_BAD_PAGE, MAC_DEV_WAIT_TIMEOUT, MAC_DEV_NONFINITE_Q, MAC_DEV_BAD_COPY = 1, 2, 4, 8, 16
-MAC_TRACE_POINTS = 30
+MAC_TRACE_POINTS = 32
 MAC_BF16, MAC_F32 = 0, 1
 MAC_THR_ONE_MINUS_TAU, MAC_THR_TAU = 0, 1
 MAC_ROPE_HALF, MAC_ROPE_INTERLEAVED, MAC_ROPE_NONE = 0, 1, 2
