@@ -156,8 +156,10 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
  * fallback as a call of its own ([MAC] "Match (1)": a miss reproduces full
  * attention; [ACSP] MHA decode).  The query is rotated by R(m).  out: f32
  * [B][Hq][d]; lse: f32 [B][Hq] natural-log softmax denominator, or NULL.
- * Uses the same chunking and merge order as a miss in mac_decode_step, so a
- * missing head's output is bitwise equal to this call's. */
+ * Uses the same chunking and merge order as a decode step in which every
+ * head misses, so such a step's output is bitwise equal to this call's; a
+ * missing head in a step where others hit attends the same tokens with a
+ * chunking that depends on the other units' bands (equal to rounding). */
 int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pre,
                        const int32_t *seq_len, const mac_kv *kv, float *out, float *lse,
                        void *stream);
