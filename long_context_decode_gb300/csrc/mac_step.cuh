@@ -106,6 +106,7 @@ struct Step {
   static constexpr int kTileTok = kStageBytes / (2 * kRowBytes);  // 64 (bf16) / 32 (fp32)
   static constexpr int kMatchRows = kStageBytes / kRowBytes;      // ring rows per stage
   static constexpr int kRPG = kMatchRows / 32;                    // rows per lane group per match chunk
+  static constexpr int kLogRPG = ilog2c(kRPG);
   static constexpr int kPer = 16 / (int)sizeof(T);                // elements per 16-byte piece
   static constexpr int kNP = 16 / kPer;                           // pieces per lane (16 dims)
   static constexpr int kPairs = 8;                                // float2 pairs per lane (16 dims)
@@ -122,8 +123,9 @@ struct Step {
   static constexpr int kLogATPG = ilog2c(kATPG);
   static constexpr int kQBytes = G * kRowBytes;
   // per-stage side buffer: a tile's G query rows, or a match chunk's query
-  // row and ring positions
-  static constexpr int kAux = (kQBytes > kRowBytes + 4 * kMatchRows ? kQBytes : kRowBytes + 4 * kMatchRows);
+  // row, ring positions and chunk coordinates (int4 at kInfoOff)
+  static constexpr int kInfoOff = kRowBytes + 4 * kMatchRows;
+  static constexpr int kAux = (kQBytes > kInfoOff + 16 ? kQBytes : kInfoOff + 16);
   static constexpr int kOutPer = (G * kHeadDim + kConsumers - 1) / kConsumers;
   static_assert(kAV <= 16 && kAV >= 2, "one score per lane of a half-warp at most");
 
@@ -543,6 +545,20 @@ struct Step {
   // producer
   // ---------------------------------------------------------------------
 
+  // The G pre-RoPE query rows of unit u's heads into stage st's side buffer.
+  __device__ static void copy_q(const StepParams &p, const Smem &S, int st, int u, uint32_t bar) {
+    const uint8_t *q = (const uint8_t *)p.q;
+    const int b = u / p.Hkv, g = u % p.Hkv;
+    const int64_t bh0 = (int64_t)b * p.Hq + g * G;
+    if (p.q_stride == kHeadDim && p.q_offset == 0) {  // the group's G rows are contiguous
+      bulk_g2s(smem_addr(S.qbuf + (size_t)st * kAux), q + (size_t)bh0 * kRowBytes, kQBytes, bar);
+    } else {
+      for (int hh = 0; hh < G; ++hh)
+        bulk_g2s(smem_addr(S.qbuf + (size_t)st * kAux + hh * kRowBytes),
+                 q + (size_t)((bh0 + hh) * p.q_stride + p.q_offset) * sizeof(T), kRowBytes, bar);
+    }
+  }
+
   // Rows of K/V tile `tile` (tokens tile*kTileTok+1 .. +kTileTok) that fall in
   // [lo, hi], each copied to its own row of the stage, so no byte outside the
   // piece is read; with_q also brings the unit's G pre-RoPE query rows.
@@ -601,17 +617,7 @@ struct Step {
       return;
     }
     mbar_expect_tx(bar, bytes);
-    if (with_q) {
-      const uint8_t *q = (const uint8_t *)p.q;
-      const int64_t bh0 = (int64_t)b * p.Hq + g * G;
-      if (p.q_stride == kHeadDim && p.q_offset == 0) {  // the group's G rows are contiguous
-        bulk_g2s(smem_addr(S.qbuf + (size_t)st * kAux), q + (size_t)bh0 * kRowBytes, kQBytes, bar);
-      } else {
-        for (int hh = 0; hh < G; ++hh)
-          bulk_g2s(smem_addr(S.qbuf + (size_t)st * kAux + hh * kRowBytes),
-                   q + (size_t)((bh0 + hh) * p.q_stride + p.q_offset) * sizeof(T), kRowBytes, bar);
-      }
-    }
+    if (with_q) copy_q(p, S, st, u, bar);
     const unsigned long long pol = l2_evict_first_policy();
     if (!PAGED) {
       if (msk == 0) return;
@@ -664,10 +670,34 @@ struct Step {
 
   // The tiles of one piece, from stage use n on; returns the next use.
   __device__ static uint32_t copy_piece(const StepParams &p, const Smem &S, const Piece &pc, uint32_t n) {
-    const int64_t t0 = (pc.lo - 1) / kTileTok, t1 = (pc.hi - 1) / kTileTok;
-    for (int64_t t = t0; t <= t1; ++t, ++n) {
+    const int t0 = (pc.lo - 1) / kTileTok, t1 = (pc.hi - 1) / kTileTok;
+    if (PAGED || pc.u < 0 || pc.u >= p.B * p.Hkv || pc.lo < 1 || pc.hi < pc.lo || pc.hi > p.kv.capacity) {
+      // pages need a table lookup per 16 rows; a piece outside the cache is
+      // refused tile by tile
+      for (int t = t0; t <= t1; ++t, ++n) {
+        if (!acquire_stage(p, S, n)) break;
+        issue_tile(p, S, n % kStages, pc.u, pc.lo, pc.hi, t, t == t0);
+      }
+      return n;
+    }
+    // contiguous cache, a piece inside it: checked once, then each tile is
+    // two row ranges (the unit's K and V rows are contiguous)
+    const size_t unit_off = (size_t)pc.u * (size_t)p.kv.capacity * kRowBytes;
+    const uint8_t *kg = (const uint8_t *)p.kv.k + unit_off, *vg = (const uint8_t *)p.kv.v + unit_off;
+    const unsigned long long pol = l2_evict_first_policy();
+    for (int t = t0; t <= t1; ++t, ++n) {
       if (!acquire_stage(p, S, n)) break;
-      issue_tile(p, S, n % kStages, pc.u, pc.lo, pc.hi, t, t == t0);
+      const int st = n % kStages;
+      const int ra = t * kTileTok + 1 > pc.lo ? t * kTileTok + 1 : pc.lo;
+      const int rz = t * kTileTok + kTileTok < pc.hi ? t * kTileTok + kTileTok : pc.hi;
+      const uint32_t nb = (uint32_t)(rz - ra + 1) * kRowBytes;
+      const uint32_t bar = smem_addr(&S.full[st]);
+      S.mask[st] = (1 << (kTileTok / 16)) - 1;
+      mbar_expect_tx(bar, 2u * nb + (t == t0 ? (uint32_t)kQBytes : 0u));
+      if (t == t0) copy_q(p, S, st, pc.u, bar);
+      uint8_t *kbuf = S.stage + (size_t)st * kStageBytes + (size_t)(ra - t * kTileTok - 1) * kRowBytes;
+      bulk_g2s_hint(smem_addr(kbuf), kg + (size_t)(ra - 1) * kRowBytes, nb, bar, pol);
+      bulk_g2s_hint(smem_addr(kbuf + kStageBytes / 2), vg + (size_t)(ra - 1) * kRowBytes, nb, bar, pol);
     }
     return n;
   }
@@ -686,12 +716,15 @@ struct Step {
       const int st = n % kStages;
       const uint32_t bar = smem_addr(&S.full[st]);
       const bool pos_copy = pos_by_copy(p);
+      uint8_t *side = S.qbuf + (size_t)st * kAux;
+      // the chunk's coordinates (plain store, ordered before the consumers'
+      // wait by the arrive below), then the head's query row and the
+      // chunk's ring positions, into the side buffer
+      *reinterpret_cast<int4 *>(side + kInfoOff) = make_int4(bh, slot0, rows, bh / p.Hq);
       mbar_expect_tx(bar, (uint32_t)rows * kRowBytes + kRowBytes + (pos_copy ? 4u * rows : 0u));
       bulk_g2s_hint(smem_addr(S.stage + (size_t)st * kStageBytes),
                     (const uint8_t *)p.ring_q + ((size_t)bh * p.K + slot0) * kRowBytes,
                     (uint32_t)rows * kRowBytes, bar, pol);
-      // the head's query row and the chunk's ring positions, into the side buffer
-      uint8_t *side = S.qbuf + (size_t)st * kAux;
       bulk_g2s(smem_addr(side), (const uint8_t *)p.q + (size_t)((int64_t)bh * p.q_stride + p.q_offset) * sizeof(T),
                kRowBytes, bar);
       if (pos_copy)
@@ -779,10 +812,10 @@ struct Step {
   // phase M
   // ---------------------------------------------------------------------
 
-  // Squared L2 distance between the lane's 16 query elements and the row's:
-  // exact differences (bf16), squares and a pairwise tree in the lane, then
-  // the 8 lanes of the group (xor 1, 2, 4); every lane gets the sum.
-  __device__ static float row_dist(const uint8_t *row, int sub, const float2 *qv) {
+  // The lane's part of the squared L2 distance between the query and a row:
+  // exact differences of its 16 elements (bf16), squares and a pairwise tree
+  // (the 8 lanes of the group are summed by the caller).
+  __device__ static float lane_dist(const uint8_t *row, int sub, const float2 *qv) {
     float2 df[kPairs];
 #pragma unroll
     for (int c = 0; c < kNP; ++c) {
@@ -800,50 +833,27 @@ struct Step {
     t[0] = __fadd2_rn(t[0], t[2]);
     t[1] = __fadd2_rn(t[1], t[3]);
     t[0] = __fadd2_rn(t[0], t[1]);
-    float D = __fadd_rn(t[0].x, t[0].y);
-    D = __fadd_rn(D, __shfl_xor_sync(kFull, D, 1));
-    D = __fadd_rn(D, __shfl_xor_sync(kFull, D, 2));
-    D = __fadd_rn(D, __shfl_xor_sync(kFull, D, 4));
-    return D;
+    return __fadd_rn(t[0].x, t[0].y);
   }
 
   // The warp's best (distance, position) joins head bh's global minimum.
-  __device__ static void flush_best(const Smem &S, int bh, float bd, int bp) {
-#pragma unroll
-    for (int off = 8; off <= 16; off <<= 1) {
-      const float d2 = __shfl_xor_sync(kFull, bd, off);
-      const int p2 = __shfl_xor_sync(kFull, bp, off);
-      if (better(d2, p2, bd, bp)) {
-        bd = d2;
-        bp = p2;
-      }
-    }
-    if ((threadIdx.x & 31) == 0 && bp >= 1) atomicMax(&S.best[bh], pack_best(bd, bp));
-  }
-
-  // Scan match chunk j (stage use n): its rows, the head's query row and
-  // (K a multiple of 4) the rows' positions all arrive in the stage.
+  // Scan the match chunk of stage use n: its rows, the head's query row, the
+  // chunk's coordinates and (K a multiple of 4) the rows' positions all
+  // arrive in the stage.  Each lane sums (a-b)^2 of its 16 elements of the
+  // group's kRPG rows; a reduce-scatter over the group's 8 lanes (xor 4, 2,
+  // then 1) leaves lanes 2k, 2k+1 with row k's distance (three pairwise
+  // levels, as in row_dist); the warp's best then joins the head's minimum.
   __device__ static void match_chunk(const StepParams &p, const Smem &S, uint32_t n, int j, int grp, int sub,
                                      unsigned long long &wait_ns) {
-    const int cph = chunks_per_head(p.K);
-    const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
-    const int cnt = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
-    const int b = bh / p.Hq;
+    static_assert(kRPG == 4 || kRPG == 2, "rows per lane group");
     const bool pos_copy = pos_by_copy(p);
-    int pk[kRPG];
-    if (!pos_copy) {
-      const int32_t *rp = p.ring_pos + (int64_t)b * p.K + slot0;
-#pragma unroll
-      for (int k = 0; k < kRPG; ++k) {
-        const int i = grp + 32 * k;
-        pk[k] = __ldg(rp + (i < cnt ? i : cnt - 1));
-      }
-    }
-    const int64_t m = S.X[b];  // the request's length, tabled before the match
-    int pos_lo = 1, pos_hi = 0;
-    if (len_ok(p, m)) {
-      pos_lo = m - p.K > 1 ? (int)(m - p.K) : 1;
-      pos_hi = (int)(m - 1);
+    const int kk = (sub >> (3 - kLogRPG)) & (kRPG - 1);  // the row this lane finishes
+    const int i_mine = grp + 32 * kk;
+    int pk_mine = 0;
+    if (!pos_copy) {  // positions from global memory, before the wait
+      const int cph = chunks_per_head(p.K);
+      const int slot0 = (j % cph) * kMatchRows, cnt = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
+      pk_mine = __ldg(p.ring_pos + (int64_t)((j / cph) / p.Hq) * p.K + slot0 + (i_mine < cnt ? i_mine : cnt - 1));
     }
     const bool timed = threadIdx.x == 0 && p.trace;
     const unsigned long long tw = timed ? globaltimer() : 0ull;
@@ -853,41 +863,61 @@ struct Step {
     const int st = n % kStages;
     const uint8_t *rows = S.stage + (size_t)st * kStageBytes;
     const uint8_t *side = S.qbuf + (size_t)st * kAux;
+    const int4 info = *reinterpret_cast<const int4 *>(side + kInfoOff);  // bh, slot0, rows, b
+    const int bh = info.x, cnt = info.z;
     float2 qv[kPairs];
 #pragma unroll
     for (int cc = 0; cc < kNP; ++cc)
       unpack16x2<T>(*reinterpret_cast<const uint4 *>(side + cc * 128 + sub * 16), qv + cc * (kPer / 2));
-    if (pos_copy) {
-      const int32_t *sp = reinterpret_cast<const int32_t *>(side + kRowBytes);
-#pragma unroll
-      for (int k = 0; k < kRPG; ++k) {
-        const int i = grp + 32 * k;
-        pk[k] = sp[i < cnt ? i : cnt - 1];
-      }
-    }
-    // all of the group's rows at once (independent chains), then a tree;
-    // rows past the chunk read stale stage bytes and are not considered
-    float D[kRPG];
-    int ps[kRPG];
+    if (pos_copy) pk_mine = reinterpret_cast<const int32_t *>(side + kRowBytes)[i_mine < cnt ? i_mine : cnt - 1];
+    const int64_t m = S.X[info.w];  // the request's length, tabled before the match
+    // the lane's partial sums of the group's rows (rows past the chunk read
+    // stale stage bytes and are discarded below)
+    float v[kRPG];
 #pragma unroll
     for (int k = 0; k < kRPG; ++k) {
       const int i = grp + 32 * k;
-      const int ri = i < cnt ? i : cnt - 1;
-      D[k] = row_dist(rows + (size_t)ri * kRowBytes, sub, qv);
-      const bool valid = ok && i < cnt && pk[k] >= pos_lo && pk[k] <= pos_hi;
-      ps[k] = valid ? pk[k] : -1;
-      D[k] = valid ? D[k] : INFINITY;
+      v[k] = lane_dist(rows + (size_t)(i < cnt ? i : cnt - 1) * kRowBytes, sub, qv);
     }
+    // reduce-scatter: level xor 4 keeps half the rows, xor 2 (kRPG == 4)
+    // the next half, xor 1 finishes the sum
 #pragma unroll
-    for (int w = 1; w < kRPG; w <<= 1)
+    for (int lev = 0; lev < kLogRPG; ++lev) {
+      const int off = 4 >> lev;
+      const bool up = (threadIdx.x & off) != 0;
+      const int half = kRPG >> (lev + 1);
 #pragma unroll
-      for (int k = 0; k + w < kRPG; k += 2 * w)
-        if (better(D[k + w], ps[k + w], D[k], ps[k])) {
-          D[k] = D[k + w];
-          ps[k] = ps[k + w];
+      for (int i = 0; i < kRPG / 2; ++i) {
+        if (i < half) {
+          const float send = up ? v[i] : v[i + half];
+          const float keep = up ? v[i + half] : v[i];
+          v[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, off));
         }
+      }
+    }
+    float D = v[0];
+#pragma unroll
+    for (int lev = kLogRPG; lev < 3; ++lev) D = __fadd_rn(D, __shfl_xor_sync(kFull, D, 4 >> lev));
+    int pos_lo = 1, pos_hi = 0;
+    if (len_ok(p, m)) {
+      pos_lo = m - p.K > 1 ? (int)(m - p.K) : 1;
+      pos_hi = (int)(m - 1);
+    }
+    const bool valid = ok && i_mine < cnt && pk_mine >= pos_lo && pk_mine <= pos_hi;
+    int bp = valid ? pk_mine : -1;
+    D = valid ? D : INFINITY;
     release(S, n);
-    flush_best(S, bh, D[0], ps[0]);
+    // the warp's best: lanes 2k and 2k+1 agree, so xor 2 and up
+#pragma unroll
+    for (int off = 8 / kRPG; off <= 16; off <<= 1) {
+      const float d2 = __shfl_xor_sync(kFull, D, off);
+      const int p2 = __shfl_xor_sync(kFull, bp, off);
+      if (better(d2, p2, D, bp)) {
+        D = d2;
+        bp = p2;
+      }
+    }
+    if ((threadIdx.x & 31) == 0 && bp >= 1) atomicMax(&S.best[bh], pack_best(D, bp));
   }
 
   // Match chunks i0 .. i1-1 of this CTA (chunk i is j = c + i*P), from stage
