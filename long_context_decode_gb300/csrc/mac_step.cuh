@@ -1662,10 +1662,14 @@ struct Step {
   // has, so no grid barrier is needed before the merges).  A long-band
   // piece of a two-level unit counts in its CTA group.  A decode step's tail
   // pieces are not counted: they all finish before the grid barrier, which
-  // orders them before every merge.
+  // orders them before every merge (so a short band completes its unit).
   __device__ static int piece_count(const StepParams &p, const Smem &S, int u, int ph, bool is_short, int *k) {
     const bool decode = p.mode == MODE_DECODE;
     if (decode && ph == 0) return 0;
+    // a short band is its unit's only band piece, and a decode step's tail
+    // pieces all finished before the grid barrier: its CTA merges the unit
+    // without counting
+    if (decode && is_short) return 2;
     *k = blockIdx.x / kGroupCtas;
     __threadfence();  // this thread's part of the partial, before the count
     consumer_sync();
