@@ -402,7 +402,7 @@ struct Step {
   // non-empty counts and every long unit's CTA run) by all consumer threads
   // while the producer copies the short pieces.
   static constexpr int kShortBand = 128;
-  static constexpr int kPieceCost = 128;  // fixed cost of a piece (and its merge), in tokens
+  static constexpr int kPieceCost = 384;  // fixed cost of a piece and its merge, in tokens
   __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
     const int64_t n = seg_len(p, S, 1, u);
     return n > 0 && n <= *S.short_max;
