@@ -314,15 +314,22 @@ struct Step {
   // exclusive prefix of the tail lengths, the CTA spans, their non-empty
   // counts and every unit's CTA run.  With at most as many units as CTAs,
   // unit u owns the CTAs [u*P/U, (u+1)*P/U) and its tail is cut evenly among
-  // them, so no CTA meets two units (a second piece would double its fixed
-  // costs), and everything but the prefix has a closed form; with more
-  // units the tails, laid end to end, are cut into equal spans.
+  // the first k' of them, k' = min(its CTAs, length / kMinSpan rounded up),
+  // so no CTA meets two units (a second piece would double its fixed costs)
+  // nor gets a sliver, and everything but the prefix has a closed form; with
+  // more units the tails, laid end to end, are cut into equal spans.
+  static constexpr int kMinSpan = 64;  // tokens: a piece worth its fixed cost
+  __device__ static int tail_ctas(int64_t len, int k) {
+    if (len <= 0) return 0;
+    const int64_t want = (len + kMinSpan - 1) / kMinSpan;
+    return want < k ? (int)want : k;
+  }
   __device__ static void layout_tails(const StepParams &p, const Smem &S) {
     int64_t *off = S.offA;
     const int U = p.B * p.Hkv, tid = threadIdx.x, P = gridDim.x;
     const bool aligned = U <= P;
     // prefix of (length << 9 | non-empty spans of the unit's CTAs); a
-    // unit's k <= P <= 256 CTAs hold min(k, length) non-empty spans
+    // unit's k' <= P <= 256 used CTAs all hold non-empty spans
     long long carry = 0;
     for (int base = 0; base < U; base += kConsumers) {
       const int u = base + tid;
@@ -330,7 +337,7 @@ struct Step {
       if (u < U) {
         const long long len = seg_len(p, S, 0, u);
         const int k = aligned ? (u + 1) * P / U - u * P / U : 0;
-        x = (len << 9) | (long long)(len < k ? len : k);
+        x = (len << 9) | (long long)tail_ctas(len, k);
       }
       long long tot;
       const long long ex = block_scan(S, x, &tot);
@@ -351,14 +358,15 @@ struct Step {
       int ne = 0;
       if (c < P) {
         const int u = ((c + 1) * U - 1) / P;
-        const int a = u * P / U, k = (u + 1) * P / U - a, j = c - a;
+        const int a = u * P / U, j = c - a;
         const int64_t len = off[u + 1] - off[u];
-        const int64_t share = len < (1LL << 22) ? (int64_t)((uint32_t)len * (uint32_t)j / (uint32_t)k)
-                                                : div_s64(len * j, k);
+        const int k = tail_ctas(len, (u + 1) * P / U - a);
+        int64_t share = len;  // CTAs past the k' used ones: empty spans at the unit's end
+        if (j < k)
+          share = len < (1LL << 22) ? (int64_t)((uint32_t)len * (uint32_t)j / (uint32_t)k) : div_s64(len * j, k);
         S.spanA[c] = off[u] + share;
-        // slices 0..j-1 of the unit: all non-empty when len >= k, else one
-        // token each for len*j/k of them
-        ne = S.neA[u] + (len >= k ? j : (int)share);
+        // slices 0..j-1 of the unit: all non-empty up to the k' used ones
+        ne = S.neA[u] + (j < k ? j : k);
       }
       const int neP = (int)(carry & 511);
       consumer_sync();  // every per-unit prefix read before the per-CTA counts overwrite it
@@ -368,8 +376,8 @@ struct Step {
         S.neA[P] = neP;
       }
       for (int u = tid; u < U; u += kConsumers) {
-        const int a = u * P / U, k = (u + 1) * P / U - a;
-        S.runA[u] = off[u + 1] > off[u] ? make_short2((short)a, (short)(a + k - 1)) : make_short2(0, -1);
+        const int a = u * P / U, k = tail_ctas(off[u + 1] - off[u], (u + 1) * P / U - a);
+        S.runA[u] = k > 0 ? make_short2((short)a, (short)(a + k - 1)) : make_short2(0, -1);
       }
     } else {
       if (c <= P) S.spanA[c] = c < P ? part_of(c, total, P) : total;
@@ -522,10 +530,14 @@ struct Step {
     const int U = p.B * p.Hkv, c = threadIdx.x, P = gridDim.x;
     const int ns = *S.n_short;
     const long long tb = S.band_tot[0], tv = S.band_tot[1];
+    // the long bands use the first Pl CTAs, each with at least kMinSpan
+    // tokens of the cost axis (slivers cost a whole piece and a bigger merge)
+    const long long want = (tv + kMinSpan - 1) / kMinSpan;
+    const int Pl = want < P ? (int)(want > 0 ? want : 1) : P;
     long long cap = 0, tot;
-    if (c < P) {
+    if (c < Pl) {
       const int j0 = c * ns / P, j1 = (c + 1) * ns / P;
-      cap = part_of(c + 1, tv, P) - part_of(c, tv, P) - (S.scp[j1] - S.scp[j0]);
+      cap = part_of(c + 1, tv, Pl) - part_of(c, tv, Pl) - (S.scp[j1] - S.scp[j0]);
       cap = cap > 0 ? cap : 0;
     }
     const long long st = block_scan(S, cap, &tot);
