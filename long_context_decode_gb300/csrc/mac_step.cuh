@@ -571,6 +571,50 @@ struct Step {
     }
   }
 
+  // Paged tile `t` of piece pc with its page ids already loaded (kNoPage past
+  // the table): the rows of each 16-token page that fall in the piece, page
+  // by page; an id outside the pool is refused and reported.
+  static constexpr int32_t kNoPage = (int32_t)0x80000000;
+  __device__ static void issue_paged_tile(const StepParams &p, const Smem &S, int st, const Piece &pc, int t,
+                                          bool with_q, const int32_t *ids) {
+    constexpr int kPg = kTileTok / 16;
+    const int g = pc.u % p.Hkv;
+    uint8_t *kbuf = S.stage + (size_t)st * kStageBytes;
+    const uint32_t bar = smem_addr(&S.full[st]);
+    const int tb = t * kTileTok;
+    uint32_t bytes = with_q ? (uint32_t)kQBytes : 0u;
+    int msk = 0;
+#pragma unroll
+    for (int pg = 0; pg < kPg; ++pg) {
+      const int pa = tb + pg * 16 + 1, ra = pa > pc.lo ? pa : pc.lo, rz = pa + 15 < pc.hi ? pa + 15 : pc.hi;
+      if (ra > rz || ids[pg] == kNoPage) continue;  // (past the table: nothing to copy)
+      if (ids[pg] < 0 || ids[pg] >= p.kv.n_pages) {
+        set_status(p.ctl, MAC_DEV_BAD_PAGE);
+        continue;
+      }
+      msk |= 1 << pg;
+      bytes += 2u * (uint32_t)(rz - ra + 1) * kRowBytes;
+    }
+    S.mask[st] = msk;
+    if (bytes == 0) {
+      mbar_arrive(bar);
+      return;
+    }
+    mbar_expect_tx(bar, bytes);
+    if (with_q) copy_q(p, S, st, pc.u, bar);
+    const unsigned long long pol = l2_evict_first_policy();
+#pragma unroll
+    for (int pg = 0; pg < kPg; ++pg) {
+      if (!((msk >> pg) & 1)) continue;
+      const int pa = tb + pg * 16 + 1, ra = pa > pc.lo ? pa : pc.lo, rz = pa + 15 < pc.hi ? pa + 15 : pc.hi;
+      const size_t off = (((size_t)ids[pg] * p.Hkv + g) * 16 + (size_t)(ra - pa)) * kRowBytes;
+      const uint32_t nb = (uint32_t)(rz - ra + 1) * kRowBytes;
+      uint8_t *dst = kbuf + (size_t)(ra - tb - 1) * kRowBytes;
+      bulk_g2s_hint(smem_addr(dst), (const uint8_t *)p.kv.k + off, nb, bar, pol);
+      bulk_g2s_hint(smem_addr(dst + kStageBytes / 2), (const uint8_t *)p.kv.v + off, nb, bar, pol);
+    }
+  }
+
   // Rows of K/V tile `tile` (tokens tile*kTileTok+1 .. +kTileTok) that fall in
   // [lo, hi], each copied to its own row of the stage, so no byte outside the
   // piece is read; with_q also brings the unit's G pre-RoPE query rows.
@@ -683,12 +727,35 @@ struct Step {
   // The tiles of one piece, from stage use n on; returns the next use.
   __device__ static uint32_t copy_piece(const StepParams &p, const Smem &S, const Piece &pc, uint32_t n) {
     const int t0 = (pc.lo - 1) / kTileTok, t1 = (pc.hi - 1) / kTileTok;
-    if (PAGED || pc.u < 0 || pc.u >= p.B * p.Hkv || pc.lo < 1 || pc.hi < pc.lo || pc.hi > p.kv.capacity) {
-      // pages need a table lookup per 16 rows; a piece outside the cache is
-      // refused tile by tile
+    if (pc.u < 0 || pc.u >= p.B * p.Hkv || pc.lo < 1 || pc.hi < pc.lo || (!PAGED && pc.hi > p.kv.capacity)) {
+      // a piece outside the cache is refused tile by tile
       for (int t = t0; t <= t1; ++t, ++n) {
         if (!acquire_stage(p, S, n)) break;
         issue_tile(p, S, n % kStages, pc.u, pc.lo, pc.hi, t, t == t0);
+      }
+      return n;
+    }
+    if (PAGED) {
+      // a table lookup per 16 rows: the next tile's page ids are loaded
+      // (independent loads) before the wait for its stage
+      constexpr int kPg = kTileTok / 16;
+      const int32_t *row = p.kv.page_table + (int64_t)(pc.u / p.Hkv) * p.kv.max_pages;
+      int32_t ids[kPg], nxt[kPg];
+#pragma unroll
+      for (int pg = 0; pg < kPg; ++pg) {
+        const int64_t slot = (int64_t)t0 * kPg + pg;
+        ids[pg] = slot < p.kv.max_pages ? __ldg(row + slot) : kNoPage;
+      }
+      for (int t = t0; t <= t1; ++t, ++n) {
+#pragma unroll
+        for (int pg = 0; pg < kPg; ++pg) {
+          const int64_t slot = (int64_t)(t + 1) * kPg + pg;
+          nxt[pg] = t < t1 && slot < p.kv.max_pages ? __ldg(row + slot) : kNoPage;
+        }
+        if (!acquire_stage(p, S, n)) break;
+        issue_paged_tile(p, S, n % kStages, pc, t, t == t0, ids);
+#pragma unroll
+        for (int pg = 0; pg < kPg; ++pg) ids[pg] = nxt[pg];
       }
       return n;
     }
