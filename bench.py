@@ -238,7 +238,10 @@ def run_mac(args, rank, world, local):
     step_ctr = torch.zeros(1, dtype=torch.int64, device=dev)
     outs = torch.empty((Lc, B, Hq, d), dtype=torch.float32, device=dev)
     mpos = torch.empty((Lc, B, Hq), dtype=torch.int32, device=dev)
-    main, aux = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    main = torch.cuda.Stream(dev)
+    # the append: fused into the step kernel (no auxiliary stream), or the
+    # append kernel on an auxiliary stream after an event
+    aux = torch.cuda.Stream(dev) if args.append == "aux" else None
 
     def advance(q_src=None):
         if q_src is None:
@@ -359,6 +362,8 @@ def run_mac(args, rank, world, local):
             "l2": f"inputs larger than L2: {Lc} layer states, {kv_bytes / 2**30:.1f} GiB K/V resident, "
                   f"~{(match_bytes + attend_bytes) * Lc / 2**20:.0f} MiB read per step vs 129 MiB L2",
             "rings": f"filled by {fill} untimed decode steps from empty rings",
+            "append": ("fused into the step kernel (no auxiliary stream)" if args.append == "fused"
+                       else "append kernel on an auxiliary stream after an event"),
         },
         "us_per_layer_step": us_layer,
         "gpu_launches": 2 * K * Lc,  # step kernel + append kernel per layer step
@@ -540,6 +545,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--append", choices=["fused", "aux"], default="fused",
+                    help="rectify-append inside the step kernel, or as a kernel on an auxiliary stream")
     args = ap.parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":

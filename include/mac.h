@@ -144,10 +144,14 @@ int mac_init_rings(const mac_config *cfg, void *ring_ws, void *scratch_ws, const
  *             to m-r (the rectified summary; the band and tail are
  *             accumulated separately, so no log-domain subtraction is needed).
  * out: f32 [B][Hq][d] attention output.  match_pos: int32 [B][Hq] matched
- * position, -1 on a miss (may be NULL).  stream_aux may be NULL or equal to
- * stream_main (the append then runs on stream_main).  The next step on the
- * same ring_ws makes stream_main wait for the previous append.  A captured
- * CUDA graph must call mac_join_aux before its capture ends. */
+ * position, -1 on a miss (may be NULL).  stream_aux NULL: the step kernel
+ * writes the rings' slot itself once it has merged a head (the match has
+ * read the rings before that), so there is no second kernel and no event.
+ * stream_aux == stream_main: the append kernel runs on stream_main after the
+ * step.  Another stream: the append kernel runs there after an event, and
+ * the next step on the same ring_ws makes stream_main wait for it; a
+ * captured CUDA graph must then call mac_join_aux before its capture ends.
+ * The three give bitwise identical rings and outputs. */
 int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, const void *q_pre,
                     const int32_t *seq_len, const mac_kv *kv, float *out, int32_t *match_pos,
                     void *stream_main, void *stream_aux);

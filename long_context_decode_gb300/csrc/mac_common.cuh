@@ -102,6 +102,12 @@ struct StepParams {
   const float *ring_o;       // [B][Hq][K][d]
   const float *ring_lse;     // [B][Hq][K]
   void *stage_q;             // [B][Hq][d]: copy of the step's query for the append
+  // fused append (no auxiliary stream): the final merges write slot
+  // pos mod K of the rings themselves (null: the append kernel does)
+  int32_t *app_pos;          // [B][K]
+  void *app_q;               // [B][Hq][K][d]
+  float *app_o;              // [B][Hq][K][d]
+  float *app_lse;            // [B][Hq][K]
   float *as_o;               // [B][Hq][d]: AS_{1:m-r}
   float *as_lse;             // [B][Hq]
   int32_t *match_pos_out;    // [B][Hq] or null

@@ -345,6 +345,7 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
   cudaStream_t sm = (cudaStream_t)stream_main;
   cudaStream_t sa = stream_aux ? (cudaStream_t)stream_aux : sm;
   const bool use_aux = sa != sm;
+  const bool fused = stream_aux == nullptr;  // the step kernel appends itself
   const mac_ring_layout R = ring_layout(cfg);
   const ScratchLayout S = scratch_layout(cfg);
   uint8_t *ring = (uint8_t *)ring_ws, *scr = (uint8_t *)scratch_ws;
@@ -379,9 +380,18 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
   sp.as_lse = (float *)(ring + R.stage_lse);
   sp.match_pos_out = match_pos;
   sp.out = out;
+  if (fused) {
+    sp.app_pos = (int32_t *)(ring + R.pos);
+    sp.app_q = ring + R.q;
+    sp.app_o = (float *)(ring + R.o);
+    sp.app_lse = (float *)(ring + R.lse);
+    sp.as_o = nullptr;
+    sp.as_lse = nullptr;
+  }
   if (record_phase(0, sm) != cudaSuccess || launch_step(sp, cfg, sm) != cudaSuccess ||
       record_phase(1, sm) != cudaSuccess)
     return MAC_ERR_CUDA;
+  if (fused) return record_phase(2, sm) == cudaSuccess ? MAC_OK : MAC_ERR_CUDA;
 
   AppendParams ap = append_params(cfg, R, ring, sp);
   ap.q_src = ring + R.stage_q;

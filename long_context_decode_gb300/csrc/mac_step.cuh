@@ -1644,11 +1644,20 @@ struct Step {
         c_o = reinterpret_cast<const float4 *>(p.ring_o + slot * kHeadDim)[lane];
       }
     }
+    // the append: slot pos mod K of the head's rings (the fused append
+    // writes it here; otherwise the append kernel does, from staging)
+    const int pos = S.u_pos[u];
+    const bool app = fin && p.mode == MODE_DECODE && p.app_o && len_ok(p, pos);
+    const int64_t app_slot = (int64_t)bh * p.K + pos % p.K;
     if (fin && p.mode == MODE_DECODE && wi == kWPH - 1 && lane < kHeadDim / kPer) {
-      // the append (on the aux stream) reads the step's query from the ring
-      // workspace, so the caller may reuse its query buffer right away
-      reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * (kHeadDim / kPer) + lane] =
-          reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
+      // the step's query: into the ring (fused), or into the ring workspace's
+      // staging area for the append kernel, so the caller may reuse its
+      // query buffer right away
+      const uint4 qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
+      if (app)
+        reinterpret_cast<uint4 *>(p.app_q)[app_slot * (kHeadDim / kPer) + lane] = qv;
+      else if (!p.app_o)
+        reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * (kHeadDim / kPer) + lane] = qv;
     }
     float bm = -INFINITY, bl = 0.f, bo[4] = {0.f, 0.f, 0.f, 0.f};
     float tm = -INFINITY, tl = 0.f, to[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1710,11 +1719,22 @@ struct Step {
           dst[kHeadDim + 1] = Lsum;
         }
       } else {
-        if (p.as_o) {
+        if (p.as_o || app) {
+          // AS_{1:m-r}, normalised, with its ln-LSE: the rectified summary
+          // the ring keeps for position m
           const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-          *reinterpret_cast<float4 *>(p.as_o + (int64_t)bh * kHeadDim + lane * 4) =
-              make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-          if (lane == 0) p.as_lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+          const float4 as = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
+          const float lse = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+          if (app) {
+            *reinterpret_cast<float4 *>(p.app_o + app_slot * kHeadDim + lane * 4) = as;
+            if (lane == 0) {
+              p.app_lse[app_slot] = lse;
+              if (hh == 0 && g == 0) p.app_pos[(int64_t)b * p.K + pos % p.K] = pos;
+            }
+          } else {
+            *reinterpret_cast<float4 *>(p.as_o + (int64_t)bh * kHeadDim + lane * 4) = as;
+            if (lane == 0) p.as_lse[bh] = lse;
+          }
         }
         for (int w = 0; w < kWPH; ++w) {
           const float *s = sh + (size_t)w * 2 * kSeg + kSeg;
