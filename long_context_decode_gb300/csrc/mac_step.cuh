@@ -68,6 +68,14 @@ __device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long
   return old;
 }
 
+// A count of finished pieces: release of the partials the calling CTA wrote
+// before its consumer barrier, acquire of those the earlier counts released.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -1020,7 +1028,7 @@ struct Step {
     const int nc = p.B * p.Hq * chunks_per_head(p.K), P = gridDim.x, c = blockIdx.x;
     return c < nc ? (nc - c + P - 1) / P : 0;
   }
-  static constexpr int kEarlyChunks = 2;
+  static constexpr int kEarlyChunks = 4;
 
   // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.
   __device__ static void grid_barrier(const StepParams &p, const Smem &S) {
@@ -1649,16 +1657,14 @@ struct Step {
     const int pos = S.u_pos[u];
     const bool app = fin && p.mode == MODE_DECODE && p.app_o && len_ok(p, pos);
     const int64_t app_slot = (int64_t)bh * p.K + pos % p.K;
-    if (fin && p.mode == MODE_DECODE && wi == kWPH - 1 && lane < kHeadDim / kPer) {
-      // the step's query: into the ring (fused), or into the ring workspace's
-      // staging area for the append kernel, so the caller may reuse its
-      // query buffer right away
-      const uint4 qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
-      if (app)
-        reinterpret_cast<uint4 *>(p.app_q)[app_slot * (kHeadDim / kPer) + lane] = qv;
-      else if (!p.app_o)
-        reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * (kHeadDim / kPer) + lane] = qv;
-    }
+    // the step's query goes into the ring (fused), or into the ring
+    // workspace's staging area for the append kernel, so the caller may
+    // reuse its query buffer right away; loaded here, stored after the
+    // rounds so that its latency overlaps theirs
+    const bool q_copy = fin && p.mode == MODE_DECODE && wi == kWPH - 1 && lane < kHeadDim / kPer &&
+                        (app || !p.app_o);
+    uint4 qv = make_uint4(0u, 0u, 0u, 0u);
+    if (q_copy) qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
     float bm = -INFINITY, bl = 0.f, bo[4] = {0.f, 0.f, 0.f, 0.f};
     float tm = -INFINITY, tl = 0.f, to[4] = {0.f, 0.f, 0.f, 0.f};
     // rounds of up to kRound entries: every consumer thread copies 16-byte
@@ -1688,6 +1694,12 @@ struct Step {
           merge4(tm, tl, to, src[kHeadDim], src[kHeadDim + 1], o2);
       }
       consumer_sync();  // the staging buffer and pointers are reused
+    }
+    if (q_copy) {
+      if (app)
+        reinterpret_cast<uint4 *>(p.app_q)[app_slot * (kHeadDim / kPer) + lane] = qv;
+      else
+        reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * (kHeadDim / kPer) + lane] = qv;
     }
     float *sw = seg + ((size_t)hh * kWPH + wi) * 2 * kSeg;
     if (lane == 0) {
@@ -1770,7 +1782,8 @@ struct Step {
     // without counting
     if (decode && is_short) return 2;
     *k = blockIdx.x / kGroupCtas;
-    __threadfence();  // this thread's part of the partial, before the count
+    // the barrier orders every thread's part of the partial before thread
+    // 0's count, whose release makes them visible to the CTA that merges
     consumer_sync();
     if (threadIdx.x == 0) {
       const PieceList L = unit_list(p, S, u);
@@ -1778,10 +1791,10 @@ struct Step {
       if (ph == 1 && !is_short && L.kind == kGroupList) {
         int lo, hi;
         group_ctas(L, *k, &lo, &hi);
-        const uint32_t old = atomicAdd(&p.group_done[u + *k], 1u);
+        const uint32_t old = atom_add_acq_rel_u32(&p.group_done[u + *k], 1u);
         act = (int)(old + 1) == nonempty(S, 1, lo, hi) ? 1 : 0;
       } else {
-        const uint32_t old = atomicAdd(&p.unit_done[u], 1u);
+        const uint32_t old = atom_add_acq_rel_u32(&p.unit_done[u], 1u);
         act = (int)(old + 1) == unit_target(p, S, L) ? 2 : 0;
       }
       *S.last = act;
@@ -1796,13 +1809,14 @@ struct Step {
     const PieceList Lu = unit_list(p, S, u);
 #pragma unroll 1
     while (act) {
-      __threadfence();  // the other CTAs' partials, after their counts
+      // the other CTAs' partials are visible: thread 0's count acquired
+      // them (or the grid barrier ordered them) before a consumer barrier
       merge_unit(p, S, act == 1 ? group_list(Lu, k) : Lu, act == 1 ? k : -1);
       if (act == 2) break;
-      __threadfence();  // the group partial, before the unit count
-      consumer_sync();
+      // the group partial, ordered by the merge's closing barrier before
+      // thread 0's count releases it
       if (threadIdx.x == 0) {
-        const uint32_t old = atomicAdd(&p.unit_done[u], 1u);
+        const uint32_t old = atom_add_acq_rel_u32(&p.unit_done[u], 1u);
         *S.last = (int)(old + 1) == unit_target(p, S, Lu) ? 2 : 0;
       }
       consumer_sync();
