@@ -291,6 +291,20 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Hardware approximations (relative error about 2^-22) for normalising
+// merged states: the sum of a state is at least 1 (its largest term is
+// 2^0), so neither meets a denormal.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // bf16 pair in a 32-bit word -> two floats (element 2i is the low half).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

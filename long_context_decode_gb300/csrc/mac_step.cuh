@@ -82,6 +82,9 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   return v;
 }
 
+// The partial of an empty merge entry: zero sum and output.
+static __device__ __align__(16) float g_zero_partial[kPartStride];
+
 // 16 bytes of elements -> pairs of consecutive elements as float2.
 template <typename T>
 __device__ __forceinline__ void unpack16x2(const uint4 &u, float2 *f);
@@ -188,7 +191,6 @@ struct Step {
     int64_t *scp;       // [n_units + 1]: prefix of their costs (tokens + kPieceCost)
     short2 *runA;       // [n_units]: first and last CTA meeting the unit's tail (x > y: none)
     short2 *runB;       // [n_units]: same for its long band
-    const float **mptr; // [32]: partials a merge round stages
     int *n_short;       // their number; CTA c has entries [c*n/P, (c+1)*n/P)
     long long *scan;    // [kWarps]: block_scan's warp totals
     long long *short_max;  // longest band that is one piece
@@ -258,21 +260,25 @@ struct Step {
   __device__ static const int64_t *spans(const Smem &S, int ph) { return ph ? S.spanB : S.spanA; }
 
   // the CTA whose (non-empty) span holds global index x (x < total): the
-  // last c with span[c] <= x
+  // last c < P with span[c] <= x (span[0] = 0), by binary lifting over the
+  // P <= kMaxGrid entries: a fixed number of steps without branches
   __device__ static int cta_of(const int64_t *span, int P, int64_t x) {
-    int lo = 0, hi = P - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (span[mid] <= x) lo = mid; else hi = mid - 1;
+    int lo = 0;
+#pragma unroll
+    for (int s = kMaxGrid / 2; s >= 1; s >>= 1) {
+      const int t = lo + s;
+      if (t < P && span[t] <= x) lo = t;
     }
     return lo;
   }
-  // unit whose segment holds global index g (g < T)
+  // unit whose segment holds global index g (g < T): the last u < U with
+  // off[u] <= g, by binary lifting
   __device__ static int unit_of(const int64_t *off, int U, int64_t g) {
-    int lo = 0, hi = U - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (off[mid] <= g) lo = mid; else hi = mid - 1;
+    int lo = 0;
+#pragma unroll 1
+    for (int s = U > 1 ? 1 << (31 - __clz(U - 1)) : 0; s >= 1; s >>= 1) {
+      const int t = lo + s;
+      if (t < U && off[t] <= g) lo = t;
     }
     return lo;
   }
@@ -282,6 +288,7 @@ struct Step {
                                     int64_t g1, Piece *pc) {
     const int64_t *off = offs(S, ph);
     const int U = p.B * p.Hkv;
+#pragma unroll 1
     for (; u < U; ++u) {
       const int64_t a0 = off[u], z0 = off[u + 1];
       if (a0 >= g1) return false;
@@ -303,6 +310,7 @@ struct Step {
     int *ne = ph ? S.neB : S.neA;
     const int lane = threadIdx.x & 31, P = gridDim.x;
     int pre = 0;
+#pragma unroll 1
     for (int base = 0; base <= P; base += 32) {
       const int c = base + lane;
       const int f = c < P && span[c] < span[c + 1] ? 1 : 0;
@@ -339,6 +347,7 @@ struct Step {
     // prefix of (length << 9 | non-empty spans of the unit's CTAs); a
     // unit's k' <= P <= 256 used CTAs all hold non-empty spans
     long long carry = 0;
+#pragma unroll 1
     for (int base = 0; base < U; base += kConsumers) {
       const int u = base + tid;
       long long x = 0;
@@ -383,6 +392,7 @@ struct Step {
         S.spanA[P] = total;
         S.neA[P] = neP;
       }
+#pragma unroll 1
       for (int u = tid; u < U; u += kConsumers) {
         const int a = u * P / U, k = tail_ctas(off[u + 1] - off[u], (u + 1) * P / U - a);
         S.runA[u] = k > 0 ? make_short2((short)a, (short)(a + k - 1)) : make_short2(0, -1);
@@ -395,6 +405,7 @@ struct Step {
       const long long ef = block_scan(S, f, &tot);
       if (c < P) S.neA[c] = (int)ef;
       if (c == 0) S.neA[P] = (int)tot;
+#pragma unroll 1
       for (int u = tid; u < U; u += kConsumers) S.runA[u] = find_run(S, 0, u);
     }
     consumer_sync();
@@ -438,41 +449,52 @@ struct Step {
   __device__ static void band_units_warp(const StepParams &p, const Smem &S) {
     const int U = p.B * p.Hkv, lane = threadIdx.x & 31, P = gridDim.x;
     const bool decode = p.mode == MODE_DECODE;
+    // each unit's band start and length (a 32-bit count: m < 2^31), the
+    // length parked in shortU until the list overwrites it (entry j <= u,
+    // written after every lane of the chunk has read its own)
     long long all = 0;
+#pragma unroll 1
     for (int base = 0; base < U; base += 32) {
       const int u = base + lane;
-      long long len = 0;
+      int len = 0;
       if (u < U) {
         if (decode) {
           int st = 0x7fffffff;
+#pragma unroll
           for (int hh = 0; hh < G; ++hh) {
             const int pp = S.X[u * G + hh];  // head b*Hq + g*G + hh of unit u = b*Hkv + g
-            const int lo = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
-            st = lo < st ? lo : st;
+            st = min(st, pp >= 1 ? max(pp - p.r + 1, 1) : 1);
           }
           S.u_s[u] = st;
         }
-        len = seg_len(p, S, 1, u);
+        len = (int)seg_len(p, S, 1, u);
+        S.shortU[u] = len;
       }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) len += __shfl_xor_sync(kFull, len, o);
-      all += len;
+      // the chunk's sum from two 16-bit halves (no 32-bit overflow)
+      all += ((long long)__reduce_add_sync(kFull, (unsigned)len >> 16) << 16) +
+             __reduce_add_sync(kFull, (unsigned)len & 0xffffu);
     }
-    long long smax = all / P > kShortBand ? all / P : kShortBand;
+    int smax = kShortBand;  // max(all / P, kShortBand)
+    if (all >= (long long)(kShortBand + 1) * P) {
+      const long long q = all < 0x7fffffffLL ? (long long)((unsigned)all / (unsigned)P) : div_s64(all, P);
+      smax = q < 0x7fffffffLL ? (int)q : 0x7fffffff;
+    }
     if (smax > kShortBand) {
       int cnt = 0;
+#pragma unroll 1
       for (int base = 0; base < U; base += 32) {
         const int u = base + lane;
-        const long long len = u < U ? (long long)seg_len(p, S, 1, u) : 0;
+        const int len = u < U ? S.shortU[u] : 0;
         cnt += __popc(__ballot_sync(kFull, len > 0 && len <= smax));
       }
       if (cnt > P / 2) smax = kShortBand;
     }
     long long cb = 0, cc = 0;  // carries: long tokens, short costs
     int ns = 0;
+#pragma unroll 1
     for (int base = 0; base < U; base += 32) {
       const int u = base + lane;
-      const long long len = u < U ? (long long)seg_len(p, S, 1, u) : 0;
+      const int len = u < U ? S.shortU[u] : 0;
       const bool sh = len > 0 && len <= smax;
       long long x = sh ? 0 : len, y = sh ? len + kPieceCost : 0;
 #pragma unroll
@@ -531,11 +553,10 @@ struct Step {
     return base + xi - x;
   }
 
-  // The long-band spans (CTA c = consumer thread c), their non-empty counts
-  // and every long unit's CTA run, by all consumer threads (ends with a
-  // consumer barrier).
+  // The long-band spans (CTA c = consumer thread c), by all consumer threads
+  // (ends with a consumer barrier).
   __device__ static void band_spans_block(const StepParams &p, const Smem &S) {
-    const int U = p.B * p.Hkv, c = threadIdx.x, P = gridDim.x;
+    const int c = threadIdx.x, P = gridDim.x;
     const int ns = *S.n_short;
     const long long tb = S.band_tot[0], tv = S.band_tot[1];
     // the long bands use the first Pl CTAs, each with at least kMinSpan
@@ -552,10 +573,19 @@ struct Step {
     if (c < P) S.spanB[c] = st < tb ? st : tb;
     if (c == 0) S.spanB[P] = tb;
     consumer_sync();
+  }
+
+  // The long-band spans' non-empty counts and every long unit's CTA run, by
+  // all consumer threads (ends with a consumer barrier): only the merges
+  // read them, so they are made while the first band tiles are in flight.
+  __device__ static void band_runs_block(const StepParams &p, const Smem &S) {
+    const int U = p.B * p.Hkv, c = threadIdx.x, P = gridDim.x;
+    long long tot;
     const int f = c < P && S.spanB[c] < S.spanB[c + 1] ? 1 : 0;
     const long long ef = block_scan(S, f, &tot);
     if (c < P) S.neB[c] = (int)ef;
     if (c == 0) S.neB[P] = (int)tot;
+#pragma unroll 1
     for (int u = c; u < U; u += kConsumers)
       if (!short_band(p, S, u)) S.runB[u] = find_run(S, 1, u);
     consumer_sync();
@@ -737,6 +767,7 @@ struct Step {
     const int t0 = (pc.lo - 1) / kTileTok, t1 = (pc.hi - 1) / kTileTok;
     if (pc.u < 0 || pc.u >= p.B * p.Hkv || pc.lo < 1 || pc.hi < pc.lo || (!PAGED && pc.hi > p.kv.capacity)) {
       // a piece outside the cache is refused tile by tile
+#pragma unroll 1
       for (int t = t0; t <= t1; ++t, ++n) {
         if (!acquire_stage(p, S, n)) break;
         issue_tile(p, S, n % kStages, pc.u, pc.lo, pc.hi, t, t == t0);
@@ -754,6 +785,7 @@ struct Step {
         const int64_t slot = (int64_t)t0 * kPg + pg;
         ids[pg] = slot < p.kv.max_pages ? __ldg(row + slot) : kNoPage;
       }
+#pragma unroll 1
       for (int t = t0; t <= t1; ++t, ++n) {
 #pragma unroll
         for (int pg = 0; pg < kPg; ++pg) {
@@ -772,6 +804,7 @@ struct Step {
     const size_t unit_off = (size_t)pc.u * (size_t)p.kv.capacity * kRowBytes;
     const uint8_t *kg = (const uint8_t *)p.kv.k + unit_off, *vg = (const uint8_t *)p.kv.v + unit_off;
     const unsigned long long pol = l2_evict_first_policy();
+#pragma unroll 1
     for (int t = t0; t <= t1; ++t, ++n) {
       if (!acquire_stage(p, S, n)) break;
       const int st = n % kStages;
@@ -795,6 +828,7 @@ struct Step {
     const int P = gridDim.x;
     const int cph = chunks_per_head(p.K);
     const unsigned long long pol = l2_evict_first_policy();
+#pragma unroll 1
     for (int i = i0; i < i1; ++i, ++n) {
       if (!acquire_stage(p, S, n)) break;
       const int j = blockIdx.x + i * P;
@@ -847,6 +881,7 @@ struct Step {
     if (decode && !PAGED) {
       // the tile a recent match's band needs (a hit at m-1 starts it at
       // m-r) into L2 while the match runs, for the units u = c mod P
+#pragma unroll 1
       for (int u = blockIdx.x + lane * (int)gridDim.x; u < U; u += 32 * (int)gridDim.x) {
         const int64_t m = unit_len(p, S, u), hi = m - p.r;
         if (!len_ok(p, m) || hi < 1 || hi > p.kv.capacity) continue;
@@ -1056,6 +1091,7 @@ struct Step {
   // pieces and lay out the long bands.  Ends with a consumer barrier.
   __device__ static void decide(const StepParams &p, const Smem &S, unsigned long long *trace) {
     const int tid = threadIdx.x, n_bh = p.B * p.Hq;
+#pragma unroll 1
     for (int bh = tid; bh < n_bh; bh += kConsumers) {
       const int b = bh / p.Hq, u = b * p.Hkv + (bh % p.Hq) / G;
       const int64_t m = unit_len(p, S, u);
@@ -1096,6 +1132,7 @@ struct Step {
       __threadfence_block();
       *S.ready = 3;
     }
+    band_runs_block(p, S);
     (void)trace;
   }
 
@@ -1431,6 +1468,7 @@ struct Step {
       return true;
     }
     if (I.kind == 3) {
+#pragma unroll 1
       for (; I.it < I.end; I.it += gridDim.x) {
         const PieceList L = unit_list(p, S, I.it);
         if (band_pieces(S, L) == 0 &&
@@ -1476,25 +1514,6 @@ struct Step {
   // ---------------------------------------------------------------------
   // merges
   // ---------------------------------------------------------------------
-
-  // (M, L, O[4]) <- (M, L, O) (+) (m2, l2, o2[4]) in base-2 log domain; an
-  // empty operand (L == 0) is the identity.
-  __device__ static void merge4(float &M, float &L, float *O, float m2, float l2, const float *o2) {
-    if (l2 == 0.f) return;
-    if (L == 0.f) {
-      M = m2;
-      L = l2;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) O[i] = o2[i];
-      return;
-    }
-    const float mn = fmaxf(M, m2);
-    const float a = ex2(M - mn), c = ex2(m2 - mn);
-    L = L * a + l2 * c;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) O[i] = O[i] * a + o2[i] * c;
-    M = mn;
-  }
 
   // CTAs whose spans meet unit u's segment in phase ph: [*c0, *c1] (empty
   // when *c1 < *c0).
@@ -1569,6 +1588,7 @@ struct Step {
   __device__ static int unit_target(const StepParams &p, const Smem &S, const PieceList &L) {
     int n = 0;
     if (L.kind == kGroupList) {
+#pragma unroll 1
       for (int k = L.b0 / kGroupCtas; k <= L.b1 / kGroupCtas; ++k) {
         int lo, hi;
         group_ctas(L, k, &lo, &hi);
@@ -1602,13 +1622,15 @@ struct Step {
 
   // Merge of a unit (group < 0) or of CTA group `group` of its long band.
   // The G heads are merged concurrently: kWarps / G warps per head, each
-  // taking a contiguous segment of the list (lane l owns dims 4l..4l+3; the
-  // (m, l) pairs of up to 32 entries are loaded one per lane) and keeping
-  // two running states, band and tail.  The head's first warp then merges
-  // them in order.  A unit: the cached summary of a hit head, the band
-  // states (giving AS_{1:m-r}), the tail states (giving the output).  A
-  // group: the band states, written as a partial like a piece's.  The count
-  // the merge answered is cleared for the next launch.
+  // taking a contiguous share of the list (lane l owns dims 4l..4l+3).  A
+  // warp loads its entries straight into registers (lane j: entry j's
+  // (m, l); every lane: 4 dims of each entry), takes the maximum of each
+  // class (band, tail), then sums the rescaled entries, so no step waits on
+  // the previous one.  The head's first warp then combines the warps'
+  // states the same way.  A unit: the cached summary of a hit head with the
+  // band states (giving AS_{1:m-r}), then the tail states (giving the
+  // output).  A group: the band states, written as a partial like a
+  // piece's.  The count the merge answered is cleared for the next launch.
   __device__ static void merge_unit(const StepParams &p, const Smem &S, const PieceList &L, int group) {
     unsigned long long *trace = cta_trace(p);
     const unsigned long long t_in = trace && threadIdx.x == 0 ? globaltimer() : 0ull;
@@ -1626,76 +1648,131 @@ struct Step {
     __syncwarp();
   }
 
+  // Log-domain state (base 2) of 4 dimensions: the maximum M, the sum L and
+  // the raw output O.  A set of states combines at the largest M among its
+  // members with L > 0, each member weighted by 2^(M_i - M).
+  struct MState {
+    float M, L, O[4];
+  };
+  __device__ static MState mstate_at(float M) {
+    MState a;
+    a.M = M;
+    a.L = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a.O[i] = 0.f;
+    return a;
+  }
+  // a += w * (l, o): one member of weight w (0 for an empty member)
+  __device__ static void mstate_add(MState &a, float w, float l, const float *o) {
+    a.L = fmaf(w, l, a.L);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a.O[i] = fmaf(w, o[i], a.O[i]);
+  }
+  // the weight of a member (m, l) in a state at maximum M
+  __device__ static float mweight(float m, float l, float M) { return l > 0.f ? ex2(m - M) : 0.f; }
+
   __device__ static void merge_heads(const StepParams &p, const Smem &S, const PieceList &L, int group) {
     constexpr int kSeg = kHeadDim + 4;  // m, l, -, -, o[d]
     constexpr int kWPH = kWarps / G;    // warps per head
-    constexpr int kEntry = G * kPartStride;  // floats of one list entry (all heads)
-    constexpr int kChunks = kEntry / 4;      // its 16-byte pieces
-    constexpr int kRound = (kWarps * 4 * G * kHeadDim - G * kWPH * 2 * kSeg) / kEntry;  // entries staged at once
-    static_assert(kRound >= 8 && kRound <= 32, "merge staging");
-    float *buf = S.red_o;                        // [kRound][kEntry]
-    float *seg = S.red_o + (size_t)kRound * kEntry;  // [G][kWPH][2][kSeg]
+    constexpr int kBatch = sizeof(T) == 2 ? 6 : 5;  // entries whose outputs a warp asks for at once
+    float *seg = S.red_o;               // [G][kWPH][2][kSeg]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hh = warp / kWPH, wi = warp % kWPH;
-    const int u = L.u, b = u / p.Hkv, g = u % p.Hkv;
+    const int u = L.u, b = u / p.Hkv, g = u - b * p.Hkv;
     const int bh = b * p.Hq + g * G + hh;
     const int n = L.n, nb = L.nb;
-    const bool fin = group < 0;
-    // cached rectified summary of a hit head, fetched ahead of its use
-    float c_lse = -INFINITY;
+    const bool fin = group < 0, decode = p.mode == MODE_DECODE;
+    // Loads here are unconditional, from valid addresses (an empty entry
+    // reads a zero partial), so that no instruction waits on their data
+    // before it is used.  The cached rectified summary of a hit head:
+    bool hit = false;
+    float c_lse = 0.f;
     float4 c_o = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (fin && p.mode == MODE_DECODE && wi == 0) {
+    if (fin && decode && wi == 0) {
       const int pos = S.X[bh];
-      if (pos >= 1) {
-        const int64_t slot = (int64_t)bh * p.K + pos % p.K;
-        c_lse = p.ring_lse[slot];
-        c_o = reinterpret_cast<const float4 *>(p.ring_o + slot * kHeadDim)[lane];
-      }
+      hit = pos >= 1;
+      const int64_t slot = (int64_t)bh * p.K + (hit ? pos % p.K : 0);
+      c_lse = p.ring_lse[slot];
+      c_o = reinterpret_cast<const float4 *>(p.ring_o + slot * kHeadDim)[lane];
     }
     // the append: slot pos mod K of the head's rings (the fused append
     // writes it here; otherwise the append kernel does, from staging)
     const int pos = S.u_pos[u];
-    const bool app = fin && p.mode == MODE_DECODE && p.app_o && len_ok(p, pos);
+    const bool app = fin && decode && p.app_o && len_ok(p, pos);
     const int64_t app_slot = (int64_t)bh * p.K + pos % p.K;
     // the step's query goes into the ring (fused), or into the ring
     // workspace's staging area for the append kernel, so the caller may
     // reuse its query buffer right away; loaded here, stored after the
-    // rounds so that its latency overlaps theirs
-    const bool q_copy = fin && p.mode == MODE_DECODE && wi == kWPH - 1 && lane < kHeadDim / kPer &&
-                        (app || !p.app_o);
-    uint4 qv = make_uint4(0u, 0u, 0u, 0u);
-    if (q_copy) qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
-    float bm = -INFINITY, bl = 0.f, bo[4] = {0.f, 0.f, 0.f, 0.f};
-    float tm = -INFINITY, tl = 0.f, to[4] = {0.f, 0.f, 0.f, 0.f};
-    // rounds of up to kRound entries: every consumer thread copies 16-byte
-    // pieces of them into shared memory (one L2 round trip per round), then
-    // the warps of each head merge their share of the round in list order
-    for (int base = 0; base < n; base += kRound) {
-      const int cnt = min(kRound, n - base);
-      if (tid < cnt) S.mptr[tid] = piece_at(p, S, L, 0, base + tid);
-      consumer_sync();
-      for (int x = tid; x < cnt * kChunks; x += kConsumers) {
-        const int e = x / kChunks, q = x - e * kChunks;
-        const float *src = S.mptr[e];
-        if (src) cp_async16(smem_addr(buf + (size_t)e * kEntry + q * 4), src + q * 4);
+    // entries so that its latency overlaps theirs
+    const bool q_warp = fin && decode && wi == kWPH - 1 && (app || !p.app_o);
+    uint4 qv;
+    if (q_warp)
+      qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer +
+                                                 min(lane, kHeadDim / kPer - 1)];
+
+    // this warp's share of the list, up to 32 entries at a time (lane j:
+    // entry j), with a band state and a tail state
+    MState sb = mstate_at(-INFINITY), st = mstate_at(-INFINITY);
+    const int per = (n + kWPH - 1) / kWPH;
+    const int e0 = wi * per, e1 = min(n, e0 + per);
+#pragma unroll 1
+    for (int base = e0; base < e1; base += 32) {
+      const int cnt = min(32, e1 - base);
+      const float *src = lane < cnt ? piece_at(p, S, L, hh, base + lane) : nullptr;
+      if (!src) src = g_zero_partial;
+      const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src + kHeadDim));
+      const float m = ml.x, l = ml.y;
+      const unsigned long long sp = reinterpret_cast<unsigned long long>(src);
+      const bool band = base + lane < nb;
+      // the first batch of outputs is asked for before the maxima wait on (m, l)
+      float4 ov[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const float *pk = reinterpret_cast<const float *>(__shfl_sync(kFull, sp, k));
+        ov[k] = __ldcg(reinterpret_cast<const float4 *>(pk) + lane);
       }
-      cp_async_wait_all();
-      consumer_sync();
-      const int per = (cnt + kWPH - 1) / kWPH;
-      const int e0 = wi * per, e1 = min(cnt, e0 + per);
-      for (int e = e0; e < e1; ++e) {
-        if (!S.mptr[e]) continue;
-        const float *src = buf + (size_t)e * kEntry + hh * kPartStride;
-        const float4 o4 = *reinterpret_cast<const float4 *>(src + lane * 4);
-        const float o2[4] = {o4.x, o4.y, o4.z, o4.w};
-        if (base + e < nb)
-          merge4(bm, bl, bo, src[kHeadDim], src[kHeadDim + 1], o2);
-        else
-          merge4(tm, tl, to, src[kHeadDim], src[kHeadDim + 1], o2);
+      // the classes' maxima over the entries holding tokens; what earlier
+      // rounds summed (none in the common case) is rescaled to them
+      float mb = band && l > 0.f ? m : -INFINITY, mt = !band && l > 0.f ? m : -INFINITY;
+#pragma unroll
+      for (int o2 = 16; o2 >= 1; o2 >>= 1) {
+        mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o2));
+        mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o2));
       }
-      consumer_sync();  // the staging buffer and pointers are reused
+      const float Mb = fmaxf(sb.M, mb), Mt = fmaxf(st.M, mt);
+      const float rb = mweight(sb.M, sb.L, Mb), rt = mweight(st.M, st.L, Mt);
+      sb.L *= rb;
+      st.L *= rt;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sb.O[i] *= rb;
+        st.O[i] *= rt;
+      }
+      sb.M = Mb;
+      st.M = Mt;
+      const float w = mweight(m, l, band ? Mb : Mt);
+#pragma unroll 1
+      for (int k0 = 0; k0 < cnt; k0 += kBatch) {
+        if (k0 > 0) {
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) {
+            const float *pk = reinterpret_cast<const float *>(__shfl_sync(kFull, sp, (k0 + k) & 31));
+            ov[k] = __ldcg(reinterpret_cast<const float4 *>(pk) + lane);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int j = (k0 + k) & 31;
+          const float wk = __shfl_sync(kFull, w, j), lk = __shfl_sync(kFull, l, j);
+          const float o4[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
+          if (base + j < nb)
+            mstate_add(sb, wk, lk, o4);
+          else
+            mstate_add(st, wk, lk, o4);
+        }
+      }
     }
-    if (q_copy) {
+    if (q_warp && lane < kHeadDim / kPer) {
       if (app)
         reinterpret_cast<uint4 *>(p.app_q)[app_slot * (kHeadDim / kPer) + lane] = qv;
       else
@@ -1703,40 +1780,52 @@ struct Step {
     }
     float *sw = seg + ((size_t)hh * kWPH + wi) * 2 * kSeg;
     if (lane == 0) {
-      sw[0] = bm;
-      sw[1] = bl;
-      sw[kSeg] = tm;
-      sw[kSeg + 1] = tl;
+      sw[0] = sb.M;
+      sw[1] = sb.L;
+      sw[kSeg] = st.M;
+      sw[kSeg + 1] = st.L;
     }
-    *reinterpret_cast<float4 *>(sw + 4 + lane * 4) = make_float4(bo[0], bo[1], bo[2], bo[3]);
-    *reinterpret_cast<float4 *>(sw + kSeg + 4 + lane * 4) = make_float4(to[0], to[1], to[2], to[3]);
+    *reinterpret_cast<float4 *>(sw + 4 + lane * 4) = make_float4(sb.O[0], sb.O[1], sb.O[2], sb.O[3]);
+    *reinterpret_cast<float4 *>(sw + kSeg + 4 + lane * 4) = make_float4(st.O[0], st.O[1], st.O[2], st.O[3]);
     consumer_sync();
     if (wi == 0) {
       const float *sh = seg + (size_t)hh * kWPH * 2 * kSeg;
-      float M = -INFINITY, Lsum = 0.f, O[4] = {0.f, 0.f, 0.f, 0.f};
-      if (c_lse > -INFINITY) {
-        const float a[4] = {c_o.x, c_o.y, c_o.z, c_o.w};
-        merge4(M, Lsum, O, c_lse * kLog2e, 1.f, a);
-      }
+      // band: the cached summary (a state of sum 1 at its ln-LSE) and the
+      // warps' band states
+      const float cm = hit ? c_lse * kLog2e : -INFINITY;
+      float M = cm;
+#pragma unroll
       for (int w = 0; w < kWPH; ++w) {
-        const float *s = sh + (size_t)w * 2 * kSeg;
-        merge4(M, Lsum, O, s[0], s[1], s + 4 + lane * 4);
+        const float *x = sh + (size_t)w * 2 * kSeg;
+        if (x[1] > 0.f) M = fmaxf(M, x[0]);
+      }
+      MState a = mstate_at(M);
+      {
+        const float o4[4] = {c_o.x, c_o.y, c_o.z, c_o.w};
+        mstate_add(a, mweight(cm, hit ? 1.f : 0.f, M), hit ? 1.f : 0.f, o4);
+      }
+#pragma unroll
+      for (int w = 0; w < kWPH; ++w) {
+        const float *x = sh + (size_t)w * 2 * kSeg;
+        const float4 o4v = *reinterpret_cast<const float4 *>(x + 4 + lane * 4);
+        const float o4[4] = {o4v.x, o4v.y, o4v.z, o4v.w};
+        mstate_add(a, mweight(x[0], x[1], M), x[1], o4);
       }
       if (!fin) {
         // the group's partial: the raw state, in a piece partial's layout
         float *dst = p.part_g + ((size_t)(u + group) * G + hh) * kPartStride;
-        *reinterpret_cast<float4 *>(dst + lane * 4) = make_float4(O[0], O[1], O[2], O[3]);
+        *reinterpret_cast<float4 *>(dst + lane * 4) = make_float4(a.O[0], a.O[1], a.O[2], a.O[3]);
         if (lane == 0) {
-          dst[kHeadDim] = M;
-          dst[kHeadDim + 1] = Lsum;
+          dst[kHeadDim] = a.M;
+          dst[kHeadDim + 1] = a.L;
         }
       } else {
         if (p.as_o || app) {
           // AS_{1:m-r}, normalised, with its ln-LSE: the rectified summary
           // the ring keeps for position m
-          const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-          const float4 as = make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-          const float lse = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+          const float inv = a.L > 0.f ? rcp_approx(a.L) : 0.f;
+          const float4 as = make_float4(a.O[0] * inv, a.O[1] * inv, a.O[2] * inv, a.O[3] * inv);
+          const float lse = a.L > 0.f ? (a.M + lg2_approx(a.L)) * kLn2 : -INFINITY;
           if (app) {
             *reinterpret_cast<float4 *>(p.app_o + app_slot * kHeadDim + lane * 4) = as;
             if (lane == 0) {
@@ -1748,14 +1837,26 @@ struct Step {
             if (lane == 0) p.as_lse[bh] = lse;
           }
         }
+        // the output: the band state and the warps' tail states
+        float M2 = a.L > 0.f ? a.M : -INFINITY;
+#pragma unroll
         for (int w = 0; w < kWPH; ++w) {
-          const float *s = sh + (size_t)w * 2 * kSeg + kSeg;
-          merge4(M, Lsum, O, s[0], s[1], s + 4 + lane * 4);
+          const float *x = sh + (size_t)w * 2 * kSeg + kSeg;
+          if (x[1] > 0.f) M2 = fmaxf(M2, x[0]);
         }
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        MState t = mstate_at(M2);
+        mstate_add(t, mweight(a.M, a.L, M2), a.L, a.O);
+#pragma unroll
+        for (int w = 0; w < kWPH; ++w) {
+          const float *x = sh + (size_t)w * 2 * kSeg + kSeg;
+          const float4 o4v = *reinterpret_cast<const float4 *>(x + 4 + lane * 4);
+          const float o4[4] = {o4v.x, o4v.y, o4v.z, o4v.w};
+          mstate_add(t, mweight(x[0], x[1], M2), x[1], o4);
+        }
+        const float inv = t.L > 0.f ? rcp_approx(t.L) : 0.f;
         *reinterpret_cast<float4 *>(p.out + (int64_t)bh * kHeadDim + lane * 4) =
-            make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-        if (p.out_lse && lane == 0) p.out_lse[bh] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+            make_float4(t.O[0] * inv, t.O[1] * inv, t.O[2] * inv, t.O[3] * inv);
+        if (p.out_lse && lane == 0) p.out_lse[bh] = t.L > 0.f ? (t.M + lg2_approx(t.L)) * kLn2 : -INFINITY;
       }
     }
     if (tid == 0) {
@@ -1834,7 +1935,6 @@ struct Step {
     __shared__ int64_t s_span[2][kMaxGrid + 1];
     __shared__ int s_ne[2][kMaxGrid + 1];
     __shared__ long long s_short_max, s_band_tot[2], s_scan[kWarps];
-    __shared__ const float *s_mptr[32];
     const int n_units = p.B * p.Hkv, n_heads = p.B * p.Hq;
     Smem S;
     S.stage = smem;
@@ -1858,7 +1958,6 @@ struct Step {
     S.shortU = S.u_s + n_units;
     S.runA = reinterpret_cast<short2 *>(S.shortU + n_units);
     S.runB = S.runA + n_units;
-    S.mptr = s_mptr;
     S.n_short = &s_nshort;
     S.short_max = &s_short_max;
     S.band_tot = s_band_tot;
@@ -1901,6 +2000,7 @@ struct Step {
       return;
     }
 
+#pragma unroll 1
     for (int u = tid; u < n_units; u += kConsumers) {
       S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
       S.u_s[u] = 1;
@@ -1910,6 +2010,7 @@ struct Step {
     if (decode) {
       // every request's length, for the match (X holds the decisions only
       // after the grid barrier)
+#pragma unroll 1
       for (int b = tid; b < p.B; b += kConsumers) {
         const int64_t m = (int64_t)p.pos_base[b] + p.pos_add - p.len_sub;
         S.X[b] = m >= 1 && m <= p.max_len ? (int32_t)m : 0;
@@ -1917,6 +2018,7 @@ struct Step {
     }
     if (S.rope && p.rope_mode != MAC_ROPE_NONE) {
       // the rotation angles of every request's query (shared by its heads)
+#pragma unroll 1
       for (int i = tid; i < p.B * (kHeadDim / 2); i += kConsumers) {
         const int b = i / (kHeadDim / 2), j = i % (kHeadDim / 2);
         float c, sn;
@@ -1954,6 +2056,7 @@ struct Step {
           stamp(trace, 10);
           decide(p, S, trace);
           // nobody reads the other buffer in this launch: clear it for the next
+#pragma unroll 1
           for (int i = blockIdx.x * kConsumers + tid; i < n_bh; i += gridDim.x * kConsumers) S.best_next[i] = 0ull;
         }
         layout_bands(p, S, trace);
@@ -1969,6 +2072,7 @@ struct Step {
       while (*S.issued == 0 && clock64() - t0 < (1LL << 30)) {
       }
       const uint32_t nc = *S.issued;
+#pragma unroll 1
       for (uint32_t j = nc > (uint32_t)kStages ? nc - kStages : 0u; j < nc; ++j) {
         const uint32_t bar = smem_addr(&S.full[j % kStages]);
         const long long t1 = clock64();
@@ -1986,6 +2090,7 @@ struct Step {
         p.ctl[4] = 0;
         if (decode) atomicAdd(p.ctl + 6, 1u);
         if (*(volatile uint32_t *)p.ctl != 0)
+#pragma unroll 1
           for (int u = 0; u < n_units; ++u) p.unit_done[u] = 0;
       }
     }
