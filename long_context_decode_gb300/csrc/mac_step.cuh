@@ -400,11 +400,10 @@ struct Step {
     } else {
       if (c <= P) S.spanA[c] = c < P ? part_of(c, total, P) : total;
       consumer_sync();
-      long long tot;
-      const int f = c < P && S.spanA[c] < S.spanA[c + 1] ? 1 : 0;
-      const long long ef = block_scan(S, f, &tot);
-      if (c < P) S.neA[c] = (int)ef;
-      if (c == 0) S.neA[P] = (int)tot;
+      int tot;
+      const int ef = flag_scan(S, c < P && S.spanA[c] < S.spanA[c + 1], &tot);
+      if (c < P) S.neA[c] = ef;
+      if (c == 0) S.neA[P] = tot;
 #pragma unroll 1
       for (int u = tid; u < U; u += kConsumers) S.runA[u] = find_run(S, 0, u);
     }
@@ -430,6 +429,7 @@ struct Step {
   // while the producer copies the short pieces.
   static constexpr int kShortBand = 128;
   static constexpr int kPieceCost = 384;  // fixed cost of a piece and its merge, in tokens
+  static constexpr int kSnap = 128;       // largest move of a long-band CTA boundary, in tokens
   __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
     const int64_t n = seg_len(p, S, 1, u);
     return n > 0 && n <= *S.short_max;
@@ -528,6 +528,26 @@ struct Step {
     __syncwarp();
   }
 
+  // Exclusive prefix count of one flag per consumer thread, in thread
+  // order, and the total (both to every thread), from the warps' ballots.
+  // It holds one consumer barrier; the caller's next consumer barrier must
+  // come before the next use of the warp totals.
+  __device__ static int flag_scan(const Smem &S, bool f, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned bal = __ballot_sync(kFull, f);
+    if (lane == 0) S.scan[warp] = __popc(bal);
+    consumer_sync();
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = (int)S.scan[w];
+      base += w < warp ? v : 0;
+      tot += v;
+    }
+    *total = tot;
+    return base + __popc(bal & ((1u << lane) - 1u));
+  }
+
   // Exclusive scan of one value per consumer thread, in thread order, and
   // the total (both returned to every thread).  All consumer threads call
   // it; it holds two consumer barriers.
@@ -569,8 +589,24 @@ struct Step {
       cap = part_of(c + 1, tv, Pl) - part_of(c, tv, Pl) - (S.scp[j1] - S.scp[j0]);
       cap = cap > 0 ? cap : 0;
     }
-    const long long st = block_scan(S, cap, &tot);
-    if (c < P) S.spanB[c] = st < tb ? st : tb;
+    long long st = block_scan(S, cap, &tot);
+    st = st < tb ? st : tb;
+    // a CTA boundary within kSnap tokens (and half a share) of a long
+    // unit's boundary moves onto it: the CTAs on either side then hold one
+    // piece each instead of one of them two, a piece's fixed cost being
+    // worth more than the imbalance.  Moving every boundary to its nearest
+    // unit boundary, when near enough, keeps the boundaries in order.
+    if (c > 0 && c < P && st > 0 && st < tb) {
+      const long long share2 = part_of(1, tv, 2 * Pl), half = share2 < kSnap ? share2 : kSnap;
+      const int u = unit_of(S.offB, p.B * p.Hkv, st);
+      const long long lo = S.offB[u], hi = S.offB[u + 1];
+      if (st - lo <= hi - st) {
+        if (st - lo <= half) st = lo;
+      } else if (hi - st <= half) {
+        st = hi;
+      }
+    }
+    if (c < P) S.spanB[c] = st;
     if (c == 0) S.spanB[P] = tb;
     consumer_sync();
   }
@@ -580,11 +616,10 @@ struct Step {
   // read them, so they are made while the first band tiles are in flight.
   __device__ static void band_runs_block(const StepParams &p, const Smem &S) {
     const int U = p.B * p.Hkv, c = threadIdx.x, P = gridDim.x;
-    long long tot;
-    const int f = c < P && S.spanB[c] < S.spanB[c + 1] ? 1 : 0;
-    const long long ef = block_scan(S, f, &tot);
-    if (c < P) S.neB[c] = (int)ef;
-    if (c == 0) S.neB[P] = (int)tot;
+    int tot;
+    const int ef = flag_scan(S, c < P && S.spanB[c] < S.spanB[c + 1], &tot);
+    if (c < P) S.neB[c] = ef;
+    if (c == 0) S.neB[P] = tot;
 #pragma unroll 1
     for (int u = c; u < U; u += kConsumers)
       if (!short_band(p, S, u)) S.runB[u] = find_run(S, 1, u);
@@ -1674,7 +1709,7 @@ struct Step {
   __device__ static void merge_heads(const StepParams &p, const Smem &S, const PieceList &L, int group) {
     constexpr int kSeg = kHeadDim + 4;  // m, l, -, -, o[d]
     constexpr int kWPH = kWarps / G;    // warps per head
-    constexpr int kBatch = sizeof(T) == 2 ? 6 : 5;  // entries whose outputs a warp asks for at once
+    constexpr int kBatch = 5;  // entries whose outputs a warp asks for at once
     float *seg = S.red_o;               // [G][kWPH][2][kSeg]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hh = warp / kWPH, wi = warp % kWPH;
