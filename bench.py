@@ -366,7 +366,9 @@ def run_mac(args, rank, world, local):
                        else "append kernel on an auxiliary stream after an event"),
         },
         "us_per_layer_step": us_layer,
-        "gpu_launches": 2 * K * Lc,  # step kernel + append kernel per layer step
+        # our kernels in the timed region: the step kernel per layer step, plus
+        # the append kernel when it runs on the auxiliary stream
+        "gpu_launches": (2 if aux is not None else 1) * K * Lc,
         "roofline": {
             "bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
             "frac": achieved / hbm_peak, "traffic": ncu_traffic(dominant),
@@ -377,7 +379,10 @@ def run_mac(args, rank, world, local):
         "kernels": {
             "step_kernel": {"us": kern_s * 1e6, "bytes": dom_bytes, "match_bytes": match_bytes,
                             "attend_bytes": attend_bytes, "gbs": dom_bytes / kern_s / 1e9},
-            "append_kernel": {"us_after_step": append_s * 1e6, "write_bytes": write_bytes},
+            # the ring append: its own kernel after the step on the auxiliary
+            # stream, or written by the step kernel's final merges (fused)
+            "append": ({"kernel": "append_kernel", "us_after_step": append_s * 1e6, "write_bytes": write_bytes}
+                       if aux is not None else {"kernel": "step_kernel (fused)", "write_bytes": write_bytes}),
         },
         "step_roofline": {
             "algorithmic_read_bytes": match_bytes + attend_bytes, "write_bytes": write_bytes,
