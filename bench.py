@@ -202,7 +202,7 @@ def run_mac(args, rank, world, local):
     dist = init_group(world, "nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w0 = WORKLOADS[args.workload]
+    w0 = select_workload(args)
     Lc, K, Wm, P, E = args.layers, args.steps, args.warmup, args.profile_steps, args.e2e_steps
     fill, total, w = run_plan(w0, Wm, K, P, E)
     B, Hq, Hkv, d = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
@@ -516,11 +516,18 @@ def cpu_baseline(w0, args, budget_s=20.0):
                       f"{w0.contexts[0]}; time per request-step x {w0.batch} requests = one layer step"}
 
 
+def select_workload(args):
+    """The named workload, with its ring capacity replaced when --ring-k is given."""
+    from long_context_decode_gb300.workloads import WORKLOADS, with_ring_k
+    w0 = WORKLOADS[args.workload]
+    k = getattr(args, "ring_k", None)
+    return with_ring_k(w0, k) if k else w0
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None, rank
-    from long_context_decode_gb300.workloads import WORKLOADS
-    w0 = WORKLOADS[args.workload]
+    w0 = select_workload(args)
     t, n, threads = oracle_sample(w0, args.warmup, args.steps)
     per_layer_step = t * w0.batch
     value = 1.0 / per_layer_step
@@ -545,6 +552,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["mac", "reference"], default="mac")
     ap.add_argument("--workload", default="long-128k")
+    ap.add_argument("--ring-k", type=int, default=None,
+                    help="ring capacity K in place of the workload's (the K sweep, e.g. 512)")
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--profile-steps", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=64)

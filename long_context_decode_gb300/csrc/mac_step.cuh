@@ -429,7 +429,7 @@ struct Step {
   // while the producer copies the short pieces.
   static constexpr int kShortBand = 128;
   static constexpr int kPieceCost = 384;  // fixed cost of a piece and its merge, in tokens
-  static constexpr int kSnap = 128;       // largest move of a long-band CTA boundary, in tokens
+  static constexpr int kSnap = 192;       // largest move of a long-band CTA boundary, in tokens
   __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
     const int64_t n = seg_len(p, S, 1, u);
     return n > 0 && n <= *S.short_max;

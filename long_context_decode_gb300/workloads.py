@@ -204,6 +204,14 @@ WORKLOADS = {
 }
 
 
+def with_ring_k(w: Workload, ring_k: int) -> Workload:
+    """The same workload with another ring capacity K (the ring-size sweep)."""
+    if ring_k == w.ring_k:
+        return w
+    return w.with_(ring_k=ring_k, name=f"{w.name}-k{ring_k}",
+                   description=w.description.replace(f"K={w.ring_k}", f"K={ring_k}"))
+
+
 def shuffled_page_table(rng: np.random.Generator, batch: int, pages_per_req: int) -> np.ndarray:
     """[B, pages_per_req] physical page ids: a random permutation of all pages."""
     perm = rng.permutation(batch * pages_per_req).astype(np.int32)

@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 from harness import TOL, Problem, compare, gpu_trajectory, oracle_trajectory  # noqa: E402
 from long_context_decode_gb300 import mac  # noqa: E402
-from long_context_decode_gb300.workloads import WORKLOADS  # noqa: E402
+from long_context_decode_gb300.workloads import WORKLOADS, with_ring_k  # noqa: E402
 from oracle import mac_oracle as O  # noqa: E402
 
 
@@ -24,14 +24,17 @@ def built():
     mac.load()
 
 
-@pytest.mark.parametrize("name,steps,sample", [
-    ("llama8b-32k", 40, 12),
-    ("long-128k", 24, 12),
-    ("verylong-256k", 24, 8),
-    ("mixed-paged", 12, 12),
+@pytest.mark.parametrize("name,steps,sample,ring_k", [
+    ("llama8b-32k", 40, 12, None),
+    ("long-128k", 24, 12, None),
+    ("long-128k", 24, 12, 512),  # the ring-size sweep's K = 512
+    ("verylong-256k", 24, 8, None),
+    ("mixed-paged", 12, 12, None),
 ])
-def test_full_size_workload(name, steps, sample):
+def test_full_size_workload(name, steps, sample, ring_k):
     w = WORKLOADS[name].with_(n_steps=steps)
+    if ring_k:
+        w = with_ring_k(w, ring_k)
     P = Problem(w, device_generated=True, native_paged=w.page_size > 0)
     rng = np.random.default_rng(123)
     mask = np.zeros((w.batch, w.n_q_heads), np.uint8)
