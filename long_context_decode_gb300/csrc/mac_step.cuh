@@ -949,6 +949,31 @@ struct Step {
       *S.issued = n;
     }
     __syncwarp();
+    if (decode && !*S.abort) copy_step_queries(p, S);
+  }
+
+  // The step's queries, rows bh = c + i P: into ring slot pos mod K (the
+  // fused append; the final merge writes the slot's summary), or into the
+  // ring workspace's staging area for the append kernel, so that the caller
+  // may reuse its query buffer right away.  By the producer warp once its
+  // copies are issued: the grid barrier (before the band layout it waited
+  // for) ordered every match's ring reads before these writes.
+  __device__ static void copy_step_queries(const StepParams &p, const Smem &S) {
+    const int lane = threadIdx.x & 31;
+    constexpr int kChunks = kHeadDim / kPer;  // 16-byte pieces of a row
+#pragma unroll 1
+    for (int bh = blockIdx.x; bh < p.B * p.Hq; bh += gridDim.x) {
+      const int b = bh / p.Hq, u = b * p.Hkv + (bh - b * p.Hq) / G;
+      const int pos = S.u_pos[u];
+      const bool app = p.app_o && len_ok(p, pos);
+      if (lane < kChunks && (app || !p.app_o)) {
+        const uint4 qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
+        if (app)
+          reinterpret_cast<uint4 *>(p.app_q)[((int64_t)bh * p.K + pos % p.K) * kChunks + lane] = qv;
+        else
+          reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * kChunks + lane] = qv;
+      }
+    }
   }
 
   // Consumer side of stage use n.
@@ -1656,16 +1681,16 @@ struct Step {
   }
 
   // Merge of a unit (group < 0) or of CTA group `group` of its long band.
-  // The G heads are merged concurrently: kWarps / G warps per head, each
-  // taking a contiguous share of the list (lane l owns dims 4l..4l+3).  A
-  // warp loads its entries straight into registers (lane j: entry j's
-  // (m, l); every lane: 4 dims of each entry), takes the maximum of each
-  // class (band, tail), then sums the rescaled entries, so no step waits on
-  // the previous one.  The head's first warp then combines the warps'
-  // states the same way.  A unit: the cached summary of a hit head with the
-  // band states (giving AS_{1:m-r}), then the tail states (giving the
-  // output).  A group: the band states, written as a partial like a
-  // piece's.  The count the merge answered is cleared for the next launch.
+  // The G heads are merged concurrently by kWarps / G warps each, split by
+  // dims: every warp of a head goes through the whole list for its slice of
+  // the head's dims (lane j holds entry j's pointer, maximum and sum; up to
+  // kBatch entries' outputs are in flight at once), so a list of up to
+  // kBatch entries costs one trip to L2 and no warp waits for another.  Each class
+  // (band, tail) is summed at its maximum over the entries holding tokens.
+  // A unit: the cached summary of a hit head with the band state (giving
+  // AS_{1:m-r}), then the tail state (giving the output).  A group: the band
+  // state, written as a partial like a piece's.  The count the merge
+  // answered is cleared for the next launch.
   __device__ static void merge_unit(const StepParams &p, const Smem &S, const PieceList &L, int group) {
     unsigned long long *trace = cta_trace(p);
     const unsigned long long t_in = trace && threadIdx.x == 0 ? globaltimer() : 0ull;
@@ -1683,216 +1708,181 @@ struct Step {
     __syncwarp();
   }
 
-  // Log-domain state (base 2) of 4 dimensions: the maximum M, the sum L and
-  // the raw output O.  A set of states combines at the largest M among its
-  // members with L > 0, each member weighted by 2^(M_i - M).
-  struct MState {
-    float M, L, O[4];
-  };
-  __device__ static MState mstate_at(float M) {
-    MState a;
-    a.M = M;
-    a.L = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a.O[i] = 0.f;
-    return a;
+  // N consecutive floats of a partial or ring row (L2, not L1: written by
+  // other CTAs), and their store
+  template <int N>
+  __device__ static void load_dims(const float *src, float (&v)[N]) {
+    if constexpr (N == 2) {
+      const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+      v[0] = x.x;
+      v[1] = x.y;
+    } else {
+      v[0] = __ldcg(src);
+    }
   }
-  // a += w * (l, o): one member of weight w (0 for an empty member)
-  __device__ static void mstate_add(MState &a, float w, float l, const float *o) {
-    a.L = fmaf(w, l, a.L);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) a.O[i] = fmaf(w, o[i], a.O[i]);
+  template <int N>
+  __device__ static void store_dims(float *dst, const float (&v)[N]) {
+    if constexpr (N == 2)
+      *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
+    else
+      dst[0] = v[0];
   }
+  // Log-domain states (base 2): a set of members (m_i, l_i, o_i) combines
+  // at the largest m_i among those with l_i > 0, each weighted by
+  // 2^(m_i - M).
   // the weight of a member (m, l) in a state at maximum M
   __device__ static float mweight(float m, float l, float M) { return l > 0.f ? ex2(m - M) : 0.f; }
 
   __device__ static void merge_heads(const StepParams &p, const Smem &S, const PieceList &L, int group) {
-    constexpr int kSeg = kHeadDim + 4;  // m, l, -, -, o[d]
-    constexpr int kWPH = kWarps / G;    // warps per head
-    constexpr int kBatch = 5;  // entries whose outputs a warp asks for at once
-    float *seg = S.red_o;               // [G][kWPH][2][kSeg]
+    constexpr int kWPH = kWarps / G;         // warps per head
+    constexpr int kDW = kHeadDim / kWPH;     // dims of a head per warp
+    constexpr int kDL = kDW >= 32 ? kDW / 32 : 1;  // dims per lane
+    constexpr int kLanes = kDW / kDL;        // lanes holding dims
+    constexpr int kBatch = kDL == 2 ? 10 : 12;  // entries whose outputs a warp asks for at once
+    static_assert(kDL == 1 || kDL == 2, "dims per lane");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int hh = warp / kWPH, wi = warp % kWPH;
     const int u = L.u, b = u / p.Hkv, g = u - b * p.Hkv;
     const int bh = b * p.Hq + g * G + hh;
     const int n = L.n, nb = L.nb;
     const bool fin = group < 0, decode = p.mode == MODE_DECODE;
+    // this lane's dims of the head: [dl, dl + kDL) (lanes past kLanes hold
+    // copies of the last lane's, never written)
+    const int dl = wi * kDW + min(lane, kLanes - 1) * kDL;
+    const bool own = lane < kLanes;
     // Loads here are unconditional, from valid addresses (an empty entry
     // reads a zero partial), so that no instruction waits on their data
     // before it is used.  The cached rectified summary of a hit head:
     bool hit = false;
-    float c_lse = 0.f;
-    float4 c_o = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (fin && decode && wi == 0) {
+    float c_lse = 0.f, c_o[kDL];
+    if (fin && decode) {
       const int pos = S.X[bh];
       hit = pos >= 1;
       const int64_t slot = (int64_t)bh * p.K + (hit ? pos % p.K : 0);
       c_lse = p.ring_lse[slot];
-      c_o = reinterpret_cast<const float4 *>(p.ring_o + slot * kHeadDim)[lane];
+      load_dims<kDL>(p.ring_o + slot * kHeadDim + dl, c_o);
     }
     // the append: slot pos mod K of the head's rings (the fused append
     // writes it here; otherwise the append kernel does, from staging)
     const int pos = S.u_pos[u];
     const bool app = fin && decode && p.app_o && len_ok(p, pos);
     const int64_t app_slot = (int64_t)bh * p.K + pos % p.K;
-    // the step's query goes into the ring (fused), or into the ring
-    // workspace's staging area for the append kernel, so the caller may
-    // reuse its query buffer right away; loaded here, stored after the
-    // entries so that its latency overlaps theirs
-    const bool q_warp = fin && decode && wi == kWPH - 1 && (app || !p.app_o);
-    uint4 qv;
-    if (q_warp)
-      qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer +
-                                                 min(lane, kHeadDim / kPer - 1)];
 
-    // this warp's share of the list, up to 32 entries at a time (lane j:
-    // entry j), with a band state and a tail state
-    MState sb = mstate_at(-INFINITY), st = mstate_at(-INFINITY);
-    const int per = (n + kWPH - 1) / kWPH;
-    const int e0 = wi * per, e1 = min(n, e0 + per);
+    // The whole list for this head, 32 entries at a time (lane j: entry
+    // j's pointer, maximum and sum) and up to kBatch outputs in flight:
+    // every warp of the head goes through all entries for its dims, so no
+    // warp waits for another.  Each class (band, tail) is summed at its
+    // maximum over the entries holding tokens.
+    float Mb = -INFINITY, Lb = 0.f, Ob[kDL], Mt = -INFINITY, Lt = 0.f, Ot[kDL];
+#pragma unroll
+    for (int i = 0; i < kDL; ++i) Ob[i] = Ot[i] = 0.f;
 #pragma unroll 1
-    for (int base = e0; base < e1; base += 32) {
-      const int cnt = min(32, e1 - base);
+    for (int base = 0; base < n; base += 32) {
+      const int cnt = min(32, n - base);
       const float *src = lane < cnt ? piece_at(p, S, L, hh, base + lane) : nullptr;
       if (!src) src = g_zero_partial;
       const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src + kHeadDim));
-      const float m = ml.x, l = ml.y;
       const unsigned long long sp = reinterpret_cast<unsigned long long>(src);
-      const bool band = base + lane < nb;
-      // the first batch of outputs is asked for before the maxima wait on (m, l)
-      float4 ov[kBatch];
+      float ov[kBatch][kDL];
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        const float *pk = reinterpret_cast<const float *>(__shfl_sync(kFull, sp, k));
-        ov[k] = __ldcg(reinterpret_cast<const float4 *>(pk) + lane);
-      }
-      // the classes' maxima over the entries holding tokens; what earlier
-      // rounds summed (none in the common case) is rescaled to them
-      float mb = band && l > 0.f ? m : -INFINITY, mt = !band && l > 0.f ? m : -INFINITY;
+      for (int k = 0; k < kBatch; ++k)
+        load_dims<kDL>(reinterpret_cast<const float *>(__shfl_sync(kFull, sp, k)) + dl, ov[k]);
+      const bool band = base + lane < nb;
+      float mb = band && ml.y > 0.f ? ml.x : -INFINITY, mt = !band && ml.y > 0.f ? ml.x : -INFINITY;
 #pragma unroll
       for (int o2 = 16; o2 >= 1; o2 >>= 1) {
         mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o2));
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o2));
       }
-      const float Mb = fmaxf(sb.M, mb), Mt = fmaxf(st.M, mt);
-      const float rb = mweight(sb.M, sb.L, Mb), rt = mweight(st.M, st.L, Mt);
-      sb.L *= rb;
-      st.L *= rt;
+      // what earlier rounds summed (none in the common case), at the new maxima
+      mb = fmaxf(Mb, mb);
+      mt = fmaxf(Mt, mt);
+      const float rb = mweight(Mb, Lb, mb), rt = mweight(Mt, Lt, mt);
+      Lb *= rb;
+      Lt *= rt;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        sb.O[i] *= rb;
-        st.O[i] *= rt;
+      for (int i = 0; i < kDL; ++i) {
+        Ob[i] *= rb;
+        Ot[i] *= rt;
       }
-      sb.M = Mb;
-      st.M = Mt;
-      const float w = mweight(m, l, band ? Mb : Mt);
+      Mb = mb;
+      Mt = mt;
+      const float w = mweight(ml.x, ml.y, band ? Mb : Mt);
+      const float wb = band ? w : 0.f, wt = band ? 0.f : w;
+      float lb = wb * ml.y, lt = wt * ml.y;
+#pragma unroll
+      for (int o2 = 16; o2 >= 1; o2 >>= 1) {
+        lb += __shfl_xor_sync(kFull, lb, o2);
+        lt += __shfl_xor_sync(kFull, lt, o2);
+      }
+      Lb += lb;
+      Lt += lt;
 #pragma unroll 1
       for (int k0 = 0; k0 < cnt; k0 += kBatch) {
         if (k0 > 0) {
 #pragma unroll
-          for (int k = 0; k < kBatch; ++k) {
-            const float *pk = reinterpret_cast<const float *>(__shfl_sync(kFull, sp, (k0 + k) & 31));
-            ov[k] = __ldcg(reinterpret_cast<const float4 *>(pk) + lane);
-          }
+          for (int k = 0; k < kBatch; ++k)
+            load_dims<kDL>(reinterpret_cast<const float *>(__shfl_sync(kFull, sp, (k0 + k) & 31)) + dl, ov[k]);
         }
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
           const int j = (k0 + k) & 31;
-          const float wk = __shfl_sync(kFull, w, j), lk = __shfl_sync(kFull, l, j);
-          const float o4[4] = {ov[k].x, ov[k].y, ov[k].z, ov[k].w};
-          if (base + j < nb)
-            mstate_add(sb, wk, lk, o4);
-          else
-            mstate_add(st, wk, lk, o4);
-        }
-      }
-    }
-    if (q_warp && lane < kHeadDim / kPer) {
-      if (app)
-        reinterpret_cast<uint4 *>(p.app_q)[app_slot * (kHeadDim / kPer) + lane] = qv;
-      else
-        reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * (kHeadDim / kPer) + lane] = qv;
-    }
-    float *sw = seg + ((size_t)hh * kWPH + wi) * 2 * kSeg;
-    if (lane == 0) {
-      sw[0] = sb.M;
-      sw[1] = sb.L;
-      sw[kSeg] = st.M;
-      sw[kSeg + 1] = st.L;
-    }
-    *reinterpret_cast<float4 *>(sw + 4 + lane * 4) = make_float4(sb.O[0], sb.O[1], sb.O[2], sb.O[3]);
-    *reinterpret_cast<float4 *>(sw + kSeg + 4 + lane * 4) = make_float4(st.O[0], st.O[1], st.O[2], st.O[3]);
-    consumer_sync();
-    if (wi == 0) {
-      const float *sh = seg + (size_t)hh * kWPH * 2 * kSeg;
-      // band: the cached summary (a state of sum 1 at its ln-LSE) and the
-      // warps' band states
-      const float cm = hit ? c_lse * kLog2e : -INFINITY;
-      float M = cm;
+          const float xb = __shfl_sync(kFull, wb, j), xt = __shfl_sync(kFull, wt, j);
 #pragma unroll
-      for (int w = 0; w < kWPH; ++w) {
-        const float *x = sh + (size_t)w * 2 * kSeg;
-        if (x[1] > 0.f) M = fmaxf(M, x[0]);
-      }
-      MState a = mstate_at(M);
-      {
-        const float o4[4] = {c_o.x, c_o.y, c_o.z, c_o.w};
-        mstate_add(a, mweight(cm, hit ? 1.f : 0.f, M), hit ? 1.f : 0.f, o4);
-      }
-#pragma unroll
-      for (int w = 0; w < kWPH; ++w) {
-        const float *x = sh + (size_t)w * 2 * kSeg;
-        const float4 o4v = *reinterpret_cast<const float4 *>(x + 4 + lane * 4);
-        const float o4[4] = {o4v.x, o4v.y, o4v.z, o4v.w};
-        mstate_add(a, mweight(x[0], x[1], M), x[1], o4);
-      }
-      if (!fin) {
-        // the group's partial: the raw state, in a piece partial's layout
-        float *dst = p.part_g + ((size_t)(u + group) * G + hh) * kPartStride;
-        *reinterpret_cast<float4 *>(dst + lane * 4) = make_float4(a.O[0], a.O[1], a.O[2], a.O[3]);
-        if (lane == 0) {
-          dst[kHeadDim] = a.M;
-          dst[kHeadDim + 1] = a.L;
-        }
-      } else {
-        if (p.as_o || app) {
-          // AS_{1:m-r}, normalised, with its ln-LSE: the rectified summary
-          // the ring keeps for position m
-          const float inv = a.L > 0.f ? rcp_approx(a.L) : 0.f;
-          const float4 as = make_float4(a.O[0] * inv, a.O[1] * inv, a.O[2] * inv, a.O[3] * inv);
-          const float lse = a.L > 0.f ? (a.M + lg2_approx(a.L)) * kLn2 : -INFINITY;
-          if (app) {
-            *reinterpret_cast<float4 *>(p.app_o + app_slot * kHeadDim + lane * 4) = as;
-            if (lane == 0) {
-              p.app_lse[app_slot] = lse;
-              if (hh == 0 && g == 0) p.app_pos[(int64_t)b * p.K + pos % p.K] = pos;
-            }
-          } else {
-            *reinterpret_cast<float4 *>(p.as_o + (int64_t)bh * kHeadDim + lane * 4) = as;
-            if (lane == 0) p.as_lse[bh] = lse;
+          for (int i = 0; i < kDL; ++i) {
+            Ob[i] = fmaf(xb, ov[k][i], Ob[i]);
+            Ot[i] = fmaf(xt, ov[k][i], Ot[i]);
           }
         }
-        // the output: the band state and the warps' tail states
-        float M2 = a.L > 0.f ? a.M : -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWPH; ++w) {
-          const float *x = sh + (size_t)w * 2 * kSeg + kSeg;
-          if (x[1] > 0.f) M2 = fmaxf(M2, x[0]);
-        }
-        MState t = mstate_at(M2);
-        mstate_add(t, mweight(a.M, a.L, M2), a.L, a.O);
-#pragma unroll
-        for (int w = 0; w < kWPH; ++w) {
-          const float *x = sh + (size_t)w * 2 * kSeg + kSeg;
-          const float4 o4v = *reinterpret_cast<const float4 *>(x + 4 + lane * 4);
-          const float o4[4] = {o4v.x, o4v.y, o4v.z, o4v.w};
-          mstate_add(t, mweight(x[0], x[1], M2), x[1], o4);
-        }
-        const float inv = t.L > 0.f ? rcp_approx(t.L) : 0.f;
-        *reinterpret_cast<float4 *>(p.out + (int64_t)bh * kHeadDim + lane * 4) =
-            make_float4(t.O[0] * inv, t.O[1] * inv, t.O[2] * inv, t.O[3] * inv);
-        if (p.out_lse && lane == 0) p.out_lse[bh] = t.L > 0.f ? (t.M + lg2_approx(t.L)) * kLn2 : -INFINITY;
       }
+    }
+    // band: the cached summary (a state of sum 1 at its ln-LSE) with the
+    // band state
+    const float cm = hit ? c_lse * kLog2e : -INFINITY;
+    const float M = fmaxf(cm, Lb > 0.f ? Mb : -INFINITY);
+    const float wc = mweight(cm, hit ? 1.f : 0.f, M), wbb = mweight(Mb, Lb, M);
+    const float La = (hit ? wc : 0.f) + wbb * Lb;
+    float Oa[kDL];
+#pragma unroll
+    for (int i = 0; i < kDL; ++i) Oa[i] = (hit ? wc * c_o[i] : 0.f) + wbb * Ob[i];
+    if (!fin) {
+      // the group's partial: the raw state, in a piece partial's layout
+      float *dst = p.part_g + ((size_t)(u + group) * G + hh) * kPartStride;
+      if (own) store_dims<kDL>(dst + dl, Oa);
+      if (wi == 0 && lane == 0) {
+        dst[kHeadDim] = M;
+        dst[kHeadDim + 1] = La;
+      }
+    } else {
+      if (p.as_o || app) {
+        // AS_{1:m-r}, normalised, with its ln-LSE: the rectified summary
+        // the ring keeps for position m
+        const float inv = La > 0.f ? rcp_approx(La) : 0.f;
+        float as[kDL];
+#pragma unroll
+        for (int i = 0; i < kDL; ++i) as[i] = Oa[i] * inv;
+        const float lse = La > 0.f ? (M + lg2_approx(La)) * kLn2 : -INFINITY;
+        if (app) {
+          if (own) store_dims<kDL>(p.app_o + app_slot * kHeadDim + dl, as);
+          if (wi == 0 && lane == 0) {
+            p.app_lse[app_slot] = lse;
+            if (hh == 0 && g == 0) p.app_pos[(int64_t)b * p.K + pos % p.K] = pos;
+          }
+        } else {
+          if (own) store_dims<kDL>(p.as_o + (int64_t)bh * kHeadDim + dl, as);
+          if (wi == 0 && lane == 0) p.as_lse[bh] = lse;
+        }
+      }
+      // the output: the band state with the tail state
+      const float M2 = fmaxf(La > 0.f ? M : -INFINITY, Lt > 0.f ? Mt : -INFINITY);
+      const float wa = mweight(M, La, M2), wtt = mweight(Mt, Lt, M2);
+      const float L2 = wa * La + wtt * Lt;
+      const float inv = L2 > 0.f ? rcp_approx(L2) : 0.f;
+      float o[kDL];
+#pragma unroll
+      for (int i = 0; i < kDL; ++i) o[i] = (wa * Oa[i] + wtt * Ot[i]) * inv;
+      if (own) store_dims<kDL>(p.out + (int64_t)bh * kHeadDim + dl, o);
+      if (p.out_lse && wi == 0 && lane == 0) p.out_lse[bh] = L2 > 0.f ? (M2 + lg2_approx(L2)) * kLn2 : -INFINITY;
     }
     if (tid == 0) {
       if (fin)
