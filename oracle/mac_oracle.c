@@ -55,6 +55,8 @@ typedef struct {
   int dtype;        /* element type of the query, ring-query, K and V inputs */
   int page_size;    /* 0 = contiguous [B][Hkv][capacity][d]; else paged */
   int min_context;  /* steps with m < min_context never reuse */
+  int front_sink;   /* F: tokens [1, F] kept out of the reused summaries and
+                       attended exactly at every step (0 = none) */
 } oc_config;
 
 typedef struct {
@@ -327,16 +329,20 @@ static void step_head(void *vctx, int64_t idx) {
    * only.  A hit reuses the cached rectified summary AS_{1:p-r} of slot p;
    * the fresh range starts at p-r+1 (clamped to 1).  A miss has no cached
    * part and attends to [1, m] ([MAC] "Match (1)": fall back to full
-   * attention). */
+   * attention).  With a front sink F ([MAC] "Production version", front
+   * sink isolation) the summaries cover [F+1, .] only: the fresh range
+   * starts at F+1 at the earliest, and [1, min(F, m)] is attended exactly
+   * at every step, joining the output but never a summary. */
   double *q = (double *)malloc(sizeof(double) * (size_t)d);
   oc_rope(qt, m, d, c->rope_base, c->rope_mode, q);
-  int64_t lo = 1;
+  const int64_t F = c->front_sink;
+  int64_t lo = F + 1;
   *nM = -INFINITY;
   *nZ = 0.0;
   for (int i = 0; i < d; ++i) nS[i] = 0.0;
   if (hit) {
     lo = p - r + 1;
-    if (lo < 1) lo = 1;
+    if (lo < F + 1) lo = F + 1;
     int64_t slot = (((int64_t)b * Hq + h) * K + p % K);
     oc_merge(d, nM, nZ, nS, x->ring->sM[slot], x->ring->sZ[slot], x->ring->sS + slot * d);
   }
@@ -357,6 +363,11 @@ static void step_head(void *vctx, int64_t idx) {
   double *oS = (double *)malloc(sizeof(double) * (size_t)d);
   for (int i = 0; i < d; ++i) oS[i] = nS[i];
   oc_merge(d, &oM, &oZ, oS, tM, tZ, tS);
+  if (F > 0) {
+    /* the sink, exact at this step */
+    oc_summary(c, x->kv, b, g, q, 1, F < m ? F : m, &tM, &tZ, tS);
+    oc_merge(d, &oM, &oZ, oS, tM, tZ, tS);
+  }
   for (int i = 0; i < d; ++i) o[i] = (oZ > 0.0) ? oS[i] / oZ : 0.0;
   free(oS);
   free(bS);
@@ -508,8 +519,9 @@ static void seed_head(void *vctx, int64_t idx) {
       continue;
     }
     oc_rope(qt, p, d, c->rope_base, c->rope_mode, q);
-    oc_summary(c, x->kv, b, h / G, q, 1, p - c->band_r, &x->ring->sM[slot], &x->ring->sZ[slot],
-               x->ring->sS + slot * d);
+    /* with a front sink F, the summary leaves out [1, F] */
+    oc_summary(c, x->kv, b, h / G, q, (int64_t)c->front_sink + 1, p - c->band_r, &x->ring->sM[slot],
+               &x->ring->sZ[slot], x->ring->sS + slot * d);
   }
   free(qt);
   free(q);

@@ -36,7 +36,7 @@ class OcConfig(ctypes.Structure):
         ("tau", ctypes.c_double), ("thr_mode", ctypes.c_int),
         ("rope_base", ctypes.c_double), ("rope_mode", ctypes.c_int),
         ("dtype", ctypes.c_int), ("page_size", ctypes.c_int),
-        ("min_context", ctypes.c_int),
+        ("min_context", ctypes.c_int), ("front_sink", ctypes.c_int),
     ]
 
 
@@ -112,12 +112,13 @@ class Config:
     dtype: int = BF16
     page_size: int = 0
     min_context: int = 0
+    front_sink: int = 0  # F: [1, F] kept out of the summaries, attended exactly every step
 
     def c(self) -> OcConfig:
         return OcConfig(self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim,
                         self.ring_k, self.band_r, float(self.tau), self.thr_mode,
                         float(self.rope_base), self.rope_mode, self.dtype, self.page_size,
-                        self.min_context)
+                        self.min_context, self.front_sink)
 
 
 @dataclass

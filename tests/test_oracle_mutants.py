@@ -42,8 +42,13 @@ MUTANTS = [
     ("threshold tau*sqrt(2d) by default", [("? tau : (1.0 - tau)", "? (1.0 - tau) : tau")]),
     ("threshold not strict", [("(dmin < x->thr2)", "(dmin <= x->thr2)")]),
     ("append to the next slot", [("int64_t slot = idx * K + m % K;", "int64_t slot = idx * K + (m + 1) % K;")]),
-    ("seed summary one token too long", [("q, 1, p - c->band_r, &x->ring->sM[slot]",
-                                          "q, 1, p - c->band_r + 1, &x->ring->sM[slot]")]),
+    ("seed summary one token too long", [("front_sink + 1, p - c->band_r, &x->ring->sM[slot]",
+                                          "front_sink + 1, p - c->band_r + 1, &x->ring->sM[slot]")]),
+    ("seed summary keeps the sink", [("(int64_t)c->front_sink + 1, p - c->band_r", "1, p - c->band_r")]),
+    ("sink left out of the output", [("oc_summary(c, x->kv, b, g, q, 1, F < m ? F : m, &tM, &tZ, tS);",
+                                      "oc_summary(c, x->kv, b, g, q, 1, 0, &tM, &tZ, tS);")]),
+    ("summaries keep the sink on a miss", [("int64_t lo = F + 1;", "int64_t lo = 1;")]),
+    ("summaries keep the sink on a hit", [("if (lo < F + 1) lo = F + 1;", "if (lo < 1) lo = 1;")]),
     ("max not tracked", [("if (l > mx) mx = l;", "")]),
     ("values read from K", [("S[i] += e * load_elem(kv->v, c->dtype, row + i);",
                              "S[i] += e * load_elem(kv->k, c->dtype, row + i);")]),

@@ -379,10 +379,12 @@ def _rand_problem(seed, B=2, Hq=4, Hkv=2, d=16, cap=96, rope=O.ROPE_HALF, **kw):
     return rng, cfg, kv_f32(k, v)
 
 
-def test_miss_equals_full_attention():
+@pytest.mark.parametrize("F", [0, 2, 30])
+def test_miss_equals_full_attention(F):
     # an empty ring misses everywhere and the step is exact attention
-    # (MAC blog "Match (1)": a miss falls back to full attention)
-    rng, cfg, kv = _rand_problem(9, ring_k=8, band_r=5)
+    # (MAC blog "Match (1)": a miss falls back to full attention); a front
+    # sink only splits [1, m] into sink, band and tail
+    rng, cfg, kv = _rand_problem(9, ring_k=8, band_r=5, front_sink=F)
     for lens in ([40, 77], [3, 5], [1, 2]):
         lens = np.array(lens, np.int32)
         q = rng.standard_normal((2, 4, 16)).astype(np.float32)
@@ -408,18 +410,22 @@ def test_band_covering_context_gives_full_attention():
         np.testing.assert_allclose(res["out"], full, rtol=1e-12, atol=1e-15)
 
 
-@pytest.mark.parametrize("K,r,cycle,seeded", [
-    (8, 2, 1, True), (8, 2, 3, False), (16, 1, 5, True), (16, 7, 5, False), (4, 9, 3, True),
-    (32, 3, 11, False), (6, 4, 6, True),
+@pytest.mark.parametrize("K,r,cycle,seeded,F", [
+    (8, 2, 1, True, 0), (8, 2, 3, False, 0), (16, 1, 5, True, 0), (16, 7, 5, False, 0), (4, 9, 3, True, 0),
+    (32, 3, 11, False, 0), (6, 4, 6, True, 0),
+    (8, 2, 3, True, 4), (16, 7, 5, False, 10), (6, 4, 6, True, 25), (8, 2, 1, False, 60),
 ])
-def test_reuse_with_repeated_queries_is_exact(K, r, cycle, seeded):
+def test_reuse_with_repeated_queries_is_exact(K, r, cycle, seeded, F):
     # With RoPE off and the query at m equal to the one stored at p, the
     # logits of [1, p-r] under q_m are exactly those under q_p (delta_t = 0 in
     # MAC blog "Reuse"), so cached (+) band (+) tail must equal exact attention.
     # Queries repeat with period `cycle`; the match lands at m - cycle, so the
     # band, tail, slot addressing and chained rectified summaries are all used.
+    # With a front sink F the summaries leave out [1, F] and the sink is
+    # attended at each step ([MAC] "Production version"), so the output is
+    # still exact attention; F = 60 also exceeds the early steps' lengths.
     rng, cfg, kv = _rand_problem(11 + K + r + cycle, ring_k=K, band_r=r, rope=O.ROPE_NONE,
-                                 tau=0.99, cap=160)  # only identical queries are accepted
+                                 tau=0.99, cap=160, front_sink=F)  # only identical queries match
     B, Hq, d = cfg.batch, cfg.n_q_heads, cfg.head_dim
     pattern = rng.standard_normal((B, Hq, cycle, d)).astype(np.float32)
     L = np.array([30, 47], np.int32)
