@@ -167,18 +167,20 @@ def ncu_traffic(kernel: str):
     return rec["dram_bytes_per_launch"] if sha == rec.get("source_sha") else None
 
 
-def layer_step_bytes(w, m, mpos, ring_valid):
+def layer_step_bytes(w, m, mpos, ring_valid, front_sink=0):
     """Algorithmic bytes of one layer step from the match results:
-    (match bytes, attend bytes, writes).  m [B]; mpos [B, Hq] (-1 = miss)."""
-    B, Hq, Hkv, d, G, r = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.group, w.band_r
+    (match bytes, attend bytes, writes).  m [B]; mpos [B, Hq] (-1 = miss).
+    With a front sink F the span starts at F+1 at the earliest and the sink
+    [1, min(F, m)] is read besides."""
+    B, Hq, Hkv, d, G, r, F = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.group, w.band_r, front_sink
     es = 2
     match = sum(Hq * ring_valid[b] * d * es for b in range(B)) + B * Hq * d * es + B * w.ring_k * 4
     attend = 0
     for b in range(B):
-        lo = np.where(mpos[b] >= 1, np.maximum(1, mpos[b] - r + 1), 1)
+        lo = np.where(mpos[b] >= 1, np.maximum(F + 1, mpos[b] - r + 1), F + 1)
         for g in range(Hkv):
             s = int(lo[g * G:(g + 1) * G].min())
-            attend += (int(m[b]) - s + 1) * 2 * d * es
+            attend += (max(0, int(m[b]) - s + 1) + min(F, int(m[b]))) * 2 * d * es
             if w.page_size:
                 attend += ((int(m[b]) - s) // w.page_size + 1) * 4
         attend += int((mpos[b] >= 1).sum()) * (d + 1) * 4
@@ -224,7 +226,7 @@ def run_mac(args, rank, world, local):
     q_all = torch.stack([device_queries(w, total, dev, stream_seed=layer).permute(2, 0, 1, 3)
                          for layer in range(Lc)], dim=1).contiguous()  # [total, Lc, B, Hq, d]
     cfg = mac.config(B, Hq, Hkv, d, w.ring_k, w.band_r, w.tau, dtype=mac.MAC_BF16,
-                     page_size=w.page_size, max_context=cap)
+                     page_size=w.page_size, max_context=cap, front_sink=args.front_sink)
     ring_bytes, scratch_bytes = mac.mac_workspace_size(cfg)
     scratch = torch.zeros(scratch_bytes, dtype=torch.uint8, device=dev)
     layers = [mac.MacLayer(cfg, scratch=scratch, device=dev) for _ in range(Lc)]
@@ -323,7 +325,7 @@ def run_mac(args, rank, world, local):
         for layer in range(Lc):
             kern_ms.append(phase_ev[layer][0].elapsed_time(phase_ev[layer][1]))
             append_ms.append(phase_ev[layer][1].elapsed_time(phase_ev[layer][2]))
-            a, b_, c = layer_step_bytes(w, m, mp[layer], ring_valid)
+            a, b_, c = layer_step_bytes(w, m, mp[layer], ring_valid, args.front_sink)
             mb += a
             ab += b_
             wb += c
@@ -364,6 +366,7 @@ def run_mac(args, rank, world, local):
             "rings": f"filled by {fill} untimed decode steps from empty rings",
             "append": ("fused into the step kernel (no auxiliary stream)" if args.append == "fused"
                        else "append kernel on an auxiliary stream after an event"),
+            "front_sink": args.front_sink,
         },
         "us_per_layer_step": us_layer,
         # our kernels in the timed region: the step kernel per layer step, plus
@@ -552,6 +555,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["mac", "reference"], default="mac")
     ap.add_argument("--workload", default="long-128k")
+    ap.add_argument("--front-sink", type=int, default=0,
+                    help="front-sink isolation: tokens [1, F] out of the summaries, attended every step")
     ap.add_argument("--ring-k", type=int, default=None,
                     help="ring capacity K in place of the workload's (the K sweep, e.g. 512)")
     ap.add_argument("--layers", type=int, default=32)

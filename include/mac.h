@@ -75,6 +75,9 @@ typedef struct {
   int32_t page_size;   /* 0 = contiguous K/V; 16 = paged K/V */
   int32_t min_context; /* steps with m < min_context never reuse ([MAC] production defaults) */
   int64_t max_context; /* largest m any call will see; sizes the scratch workspace */
+  int32_t front_sink;  /* F >= 0: front-sink isolation ([MAC] "Production version"): tokens
+                          [1, F] stay out of the reused summaries (seeded and appended) and
+                          are attended exactly at every decode step; 0 = none */
 } mac_config;
 
 /* K/V cache.  Contiguous (page_size 0): k, v are [B][Hkv][capacity][d].

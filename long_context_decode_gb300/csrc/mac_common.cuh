@@ -65,6 +65,7 @@ struct ScratchLayout {
   size_t part_b;     // f32 [2*B*Hkv + kMaxGrid][G][kPartStride]: band pieces (short
                      // bands at u, long-band pieces at B*Hkv + u + c)
   size_t part_g;     // f32 [B*Hkv + kGroups][G][kPartStride]: merged CTA groups of a long band
+  size_t part_s;     // f32 [B*Hkv][G][kPartStride]: front-sink pieces
   size_t total;
 };
 
@@ -122,6 +123,11 @@ struct StepParams {
   float *part_b;             // band pieces
   uint32_t *group_done;      // [B*Hkv + kGroups]
   float *part_g;             // merged CTA groups
+  float *part_s;             // front-sink pieces, one per unit
+  // front sink F: tails and bands start at F+1 at the earliest (the reused
+  // summaries leave [1, F] out); with sink_piece, [1, min(F, m)] is also
+  // attended as an output-only piece of its unit
+  int sink_f, sink_piece;
   unsigned long long *trace;  // optional: [grid][kTracePoints] %globaltimer stamps
   // RoPE frequency j as a 64-bit fixed-point fraction of a turn per
   // position: round(w_j / (2 pi) * 2^64), w_j = base^(-2j/d)

@@ -33,6 +33,7 @@ int validate(const mac_config *c) {
   if ((int64_t)c->batch * c->n_kv_heads > kMaxUnits) return MAC_ERR_UNSUPPORTED;
   if ((int64_t)c->batch * c->n_q_heads > kMaxHeads) return MAC_ERR_UNSUPPORTED;
   if (c->max_context > 0x7fffffffLL - 1) return MAC_ERR_UNSUPPORTED;
+  if (c->front_sink < 0) return MAC_ERR_INVALID_ARG;
   return MAC_OK;
 }
 
@@ -68,6 +69,7 @@ ScratchLayout scratch_layout(const mac_config *c) {
   S.part_a = off;  off = align_up(off + slots * G * kPartStride * 4, 256);
   S.part_b = off;  off = align_up(off + (U + slots) * G * kPartStride * 4, 256);
   S.part_g = off;  off = align_up(off + (U + kGroups) * G * kPartStride * 4, 256);
+  S.part_s = off;  off = align_up(off + U * G * kPartStride * 4, 256);
   S.total = off;
   return S;
 }
@@ -161,6 +163,7 @@ StepParams step_params(const mac_config *c, const ScratchLayout &S, uint8_t *scr
   a.part_b = (float *)(scratch + S.part_b);
   a.group_done = (uint32_t *)(scratch + S.group_done);
   a.part_g = (float *)(scratch + S.part_g);
+  a.part_s = (float *)(scratch + S.part_s);
   return a;
 }
 
@@ -311,8 +314,10 @@ int mac_init_rings(const mac_config *cfg, void *ring_ws, void *scratch_ws, const
   if (!q_seed) return MAC_OK;
 
   // seed i: position p = L - n_seed + 1 + i, exact summary over [1, p - r]
-  // of R(p) q_seed[.., i, ..] (the full-attention path), then appended
+  // of R(p) q_seed[.., i, ..] (the full-attention path), then appended;
+  // with a front sink F the summary covers [F+1, p - r]
   StepParams sp = step_params(cfg, S, scr, kv, MODE_FULL);
+  sp.sink_f = cfg->front_sink;
   sp.check_len = 0;  // summary lengths p - r may be < 1 (empty summaries)
   sp.pos_base = prompt_len;
   sp.len_sub = cfg->band_r;
@@ -369,6 +374,8 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
   }
 
   StepParams sp = step_params(cfg, S, scr, kv, MODE_DECODE);
+  sp.sink_f = cfg->front_sink;
+  sp.sink_piece = cfg->front_sink > 0;
   sp.pos_base = seq_len;
   sp.q = q_pre;
   sp.ring_pos = (const int32_t *)(ring + R.pos);

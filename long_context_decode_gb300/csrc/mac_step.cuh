@@ -207,6 +207,7 @@ struct Step {
 
   struct Piece {
     int u, lo, hi;
+    int sink;  // the front sink [1, min(F, m)] of unit u (an output-only piece)
   };
 
   // Phase trace point (see mac_set_trace): thread 0 records %globaltimer.
@@ -235,16 +236,20 @@ struct Step {
   // segments, spans and pieces
   // ---------------------------------------------------------------------
 
-  // First token of unit u's segment: tails [max(1, m-r+1), m], bands [s, m-r].
+  // First token of unit u's segment: tails [max(F+1, m-r+1), m], bands
+  // [s, m-r] (F: the front sink, 0 without one).
   __device__ static int64_t seg_first(const StepParams &p, const Smem &S, int ph, int u) {
     if (ph == 1) return S.u_s[u];
     const int64_t a = unit_len(p, S, u) - p.r + 1;
-    return a > 1 ? a : 1;
+    return a > p.sink_f + 1 ? a : p.sink_f + 1;
   }
   __device__ static int64_t seg_len(const StepParams &p, const Smem &S, int ph, int u) {
     const int64_t m = unit_len(p, S, u);
     if (!len_ok(p, m)) return 0;
-    if (ph == 0) return m < p.r ? m : p.r;
+    if (ph == 0) {
+      const int64_t n = m - seg_first(p, S, 0, u) + 1;
+      return n > 0 ? n : 0;
+    }
     const int64_t n = (m - p.r) - (int64_t)S.u_s[u] + 1;
     return n > 0 ? n : 0;
   }
@@ -441,6 +446,7 @@ struct Step {
   }
   __device__ static Piece short_piece(const StepParams &p, const Smem &S, int j) {
     Piece pc;
+    pc.sink = 0;
     pc.u = S.shortU[j];
     pc.lo = S.u_s[pc.u];
     pc.hi = (int)(unit_len(p, S, pc.u) - p.r);
@@ -463,7 +469,7 @@ struct Step {
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) {
             const int pp = S.X[u * G + hh];  // head b*Hq + g*G + hh of unit u = b*Hkv + g
-            st = min(st, pp >= 1 ? max(pp - p.r + 1, 1) : 1);
+            st = min(st, pp >= 1 ? max(pp - p.r + 1, p.sink_f + 1) : p.sink_f + 1);
           }
           S.u_s[u] = st;
         }
@@ -1303,7 +1309,7 @@ struct Step {
     int lo_mine = pc.lo;                     // first token of the lane's head in this piece
     if (ph == 1 && p.mode == MODE_DECODE) {
       const int pp = S.X[b * p.Hq + g * G + hm];
-      const int lh = pp >= 1 ? (pp - p.r + 1 > 1 ? pp - p.r + 1 : 1) : 1;
+      const int lh = pp >= 1 ? max(pp - p.r + 1, p.sink_f + 1) : p.sink_f + 1;
       lo_mine = lh > lo_mine ? lh : lo_mine;
     }
     float2 o[G][kAPairs], q[G][kAPairs];
@@ -1504,7 +1510,27 @@ struct Step {
   // tail piece, before the decisions) or no piece at all (no valid length).
   struct PieceIter {
     int kind, it, end;
+    int sk, sk_end, sk_step;  // kind 0: the candidate units of the CTA's sink pieces
   };
+
+  // The front sink [1, min(F, m)] of unit u: its length (0 without a sink
+  // piece), and the CTA that attends it: with units aligned to CTAs, the
+  // first CTA of the unit's group after its tail run (the group's last when
+  // the tail takes them all), else u mod P.
+  __device__ static int sink_len(const StepParams &p, const Smem &S, int u) {
+    if (!p.sink_piece) return 0;
+    const int64_t m = unit_len(p, S, u);
+    if (!len_ok(p, m)) return 0;
+    return (int)(m < p.sink_f ? m : p.sink_f);
+  }
+  __device__ static int sink_cta(const StepParams &p, const Smem &S, int u) {
+    const int U = p.B * p.Hkv, P = gridDim.x;
+    if (U > P) return u % P;
+    const short2 run = S.runA[u];
+    const int a = u * P / U, a_next = (u + 1) * P / U;
+    const int cand = a + (run.y >= run.x ? run.y - run.x + 1 : 0);
+    return cand < a_next ? cand : a_next - 1;
+  }
   __device__ static PieceIter piece_iter(const StepParams &p, const Smem &S, int kind) {
     const int U = p.B * p.Hkv, ph = kind == 0 ? 0 : 1;
     PieceIter I;
@@ -1519,20 +1545,47 @@ struct Step {
       I.it = g0 < g1 ? unit_of(offs(S, ph), U, g0) : U;
       I.end = U;
     }
+    I.sk = I.sk_end = 0;
+    I.sk_step = 1;
+    if (kind == 0 && p.sink_piece) {
+      const int P = gridDim.x, c = blockIdx.x;
+      if (U > P) {
+        I.sk = c;
+        I.sk_end = U;
+        I.sk_step = P;
+      } else {
+        I.sk = ((c + 1) * U - 1) / P;  // the unit whose group holds CTA c
+        I.sk_end = I.sk + 1;
+      }
+    }
     return I;
   }
   __device__ static bool next_piece(const StepParams &p, const Smem &S, PieceIter &I, Piece &pc) {
+    pc.sink = 0;
     if (I.kind == 1) {
       if (I.it >= I.end) return false;
       pc = short_piece(p, S, I.it++);
       return true;
+    }
+    // kind 0: the CTA's sink pieces come before its tail pieces
+#pragma unroll 1
+    for (; I.sk < I.sk_end; I.sk += I.sk_step) {
+      const int u = I.sk, n = sink_len(p, S, u);
+      if (n > 0 && sink_cta(p, S, u) == (int)blockIdx.x) {
+        pc.u = u;
+        pc.lo = 1;
+        pc.hi = n;
+        pc.sink = 1;
+        I.sk += I.sk_step;
+        return true;
+      }
     }
     if (I.kind == 3) {
 #pragma unroll 1
       for (; I.it < I.end; I.it += gridDim.x) {
         const PieceList L = unit_list(p, S, I.it);
         if (band_pieces(S, L) == 0 &&
-            (p.mode == MODE_DECODE || nonempty(S, 0, L.ca0, L.ca0 + (L.n - L.nb) - 1) == 0)) {
+            (p.mode == MODE_DECODE || nonempty(S, 0, L.ca0, L.ca0 + L.nt - 1) == 0)) {
           pc.u = I.it;
           pc.lo = 1;
           pc.hi = 0;
@@ -1563,7 +1616,9 @@ struct Step {
       if (kind != 3) {
         const size_t slot = kind == 0 ? (size_t)(pc.u + blockIdx.x)
                                       : kind == 1 ? (size_t)pc.u : (size_t)(U + pc.u + blockIdx.x);
-        attend_piece(p, S, n, ph, pc, (ph ? p.part_b : p.part_a) + slot * G * kPartStride, first);
+        float *dst = pc.sink ? p.part_s + (size_t)pc.u * G * kPartStride
+                             : (ph ? p.part_b : p.part_a) + slot * G * kPartStride;
+        attend_piece(p, S, n, ph, pc, dst, first);
         first = false;
         act = piece_count(p, S, pc.u, ph, kind == 1, &k);
       }
@@ -1604,6 +1659,7 @@ struct Step {
   enum { kShort = 0, kCtas = 1, kGroupList = 2 };
   struct PieceList {
     int kind, nb, n;
+    int nt;      // tail entries (after the band entries; a sink entry, if any, is last)
     int b0, b1;  // the band entries' CTA range (kCtas) / the whole run (kGroupList)
     int ca0;     // first CTA of the tail run
     int u;
@@ -1624,7 +1680,8 @@ struct Step {
       L.kind = kCtas;
       L.nb = L.b1 - L.b0 + 1;
     }
-    L.n = L.nb + (ca1 - L.ca0 + 1);
+    L.nt = ca1 - L.ca0 + 1;
+    L.n = L.nb + L.nt + (sink_len(p, S, u) > 0 ? 1 : 0);
     return L;
   }
   __device__ static void group_ctas(const PieceList &L, int k, int *lo, int *hi) {
@@ -1636,6 +1693,7 @@ struct Step {
     L.kind = kCtas;
     group_ctas(U_, k, &L.b0, &L.b1);
     L.nb = L.n = L.b1 - L.b0 + 1;
+    L.nt = 0;
     return L;
   }
   // band pieces of the unit (merge inputs made by attention)
@@ -1657,7 +1715,7 @@ struct Step {
     } else {
       n = band_pieces(S, L);
     }
-    if (p.mode != MODE_DECODE) n += nonempty(S, 0, L.ca0, L.ca0 + (L.n - L.nb) - 1);
+    if (p.mode != MODE_DECODE) n += nonempty(S, 0, L.ca0, L.ca0 + L.nt - 1);
     return n;
   }
   __device__ static const float *piece_at(const StepParams &p, const Smem &S, const PieceList &L, int hh, int i) {
@@ -1675,6 +1733,7 @@ struct Step {
       if (nonempty(S, 1, lo, hi) == 0) return nullptr;
       return p.part_g + ((size_t)(u + k) * G + hh) * kPartStride;
     }
+    if (i >= L.nb + L.nt) return p.part_s + ((size_t)u * G + hh) * kPartStride;  // the sink
     const int c = L.ca0 + (i - L.nb);
     if (S.spanA[c] >= S.spanA[c + 1]) return nullptr;
     return p.part_a + ((size_t)(u + c) * G + hh) * kPartStride;
@@ -2028,7 +2087,7 @@ struct Step {
 #pragma unroll 1
     for (int u = tid; u < n_units; u += kConsumers) {
       S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
-      S.u_s[u] = 1;
+      S.u_s[u] = p.sink_f + 1;
       if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
         set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
     }

@@ -34,6 +34,7 @@ class mac_config(ctypes.Structure):
         ("tau", ctypes.c_double), ("thr_mode", ctypes.c_int32), ("rope_base", ctypes.c_double),
         ("rope_mode", ctypes.c_int32), ("dtype", ctypes.c_int32), ("page_size", ctypes.c_int32),
         ("min_context", ctypes.c_int32), ("max_context", ctypes.c_int64),
+        ("front_sink", ctypes.c_int32),
     ]
 
 
@@ -205,9 +206,10 @@ def mac_threshold_sq(cfg: mac_config) -> float:
 
 def config(batch, n_q_heads, n_kv_heads, head_dim=128, ring_k=1024, band_r=256, tau=0.6,
            thr_mode=MAC_THR_ONE_MINUS_TAU, rope_base=10000.0, rope_mode=MAC_ROPE_HALF,
-           dtype=MAC_BF16, page_size=0, min_context=0, max_context=131072) -> mac_config:
+           dtype=MAC_BF16, page_size=0, min_context=0, max_context=131072, front_sink=0) -> mac_config:
     return mac_config(batch, n_q_heads, n_kv_heads, head_dim, ring_k, band_r, float(tau), thr_mode,
-                      float(rope_base), rope_mode, dtype, page_size, min_context, int(max_context))
+                      float(rope_base), rope_mode, dtype, page_size, min_context, int(max_context),
+                      int(front_sink))
 
 
 def kv_view(k, v, page_table=None, capacity=0, max_pages=0, n_pages=0) -> mac_kv:

@@ -35,8 +35,8 @@ def test_every_declared_function_is_exported(mac):
 
 
 def test_struct_sizes_match_the_header(mac):
-    # mac_config: 6 int32, double, int32(+pad), double, 4 int32, int64 = 72 bytes
-    assert ctypes.sizeof(mac.mac_config) == 72
+    # mac_config: 6 int32, double, int32(+pad), double, 4 int32, int64, int32(+pad) = 80 bytes
+    assert ctypes.sizeof(mac.mac_config) == 80
     assert ctypes.sizeof(mac.mac_kv) == 40
     assert ctypes.sizeof(mac.mac_ring_layout) == 64
 

@@ -178,6 +178,45 @@ def test_repeated_queries_reuse_is_exact_on_gpu():
     layer.release()
 
 
+@pytest.mark.parametrize("F,seeded,paged,Hq,Hkv", [
+    (64, True, False, 8, 2), (128, False, False, 8, 2), (100, True, True, 4, 1), (3000, True, False, 8, 8),
+])
+def test_front_sink_trajectory(F, seeded, paged, Hq, Hkv):
+    # front-sink isolation ([MAC] "Production version"): the reused summaries
+    # leave out [1, F] and every step attends it exactly; F = 3000 also
+    # exceeds the shorter request's context (all sink, no summary)
+    w = W(B=2, Hq=Hq, Hkv=Hkv, ctx=(2500, 6000), K=64, r=32, steps=32, query="ar1_skew", tau=0.45,
+          seed=31)
+    P = Problem(w, n_seed=64 if seeded else 0, paged=paged)
+    gpu, st, layer = gpu_trajectory(P, w.n_steps, cfg=P.cfg(front_sink=F))
+    ref = oracle_trajectory(P, w.n_steps, front_sink=F)
+    c = compare(gpu, ref, O.threshold_sq(128, w.tau))
+    assert st == 0 and c["mismatched"] == 0 and c["max_err"] <= TOL, c
+    assert c["hits"] > 0
+    layer.release()
+
+
+def test_front_sink_repeated_queries_stay_exact():
+    # RoPE off and queries repeating with period 5: each hit reuses a summary
+    # of [F+1, p-r] and attends the sink afresh, so the output is exact
+    # attention (a sink counted twice, or dropped, would show here)
+    w = W(B=2, Hq=8, Hkv=2, ctx=(2000, 3333), K=64, r=3, tau=0.99, steps=30)
+    P = Problem(w)
+    pat = P.q[:, :, :5].copy()
+    for s in range(P.q.shape[2]):
+        P.q[:, :, s] = pat[:, :, (s - P.n_seed) % 5]
+    cfg = P.cfg(rope_mode=mac.MAC_ROPE_NONE, front_sink=128)
+    gpu, st, layer = gpu_trajectory(P, w.n_steps, cfg=cfg)
+    assert st == 0
+    for s, (out, mp) in enumerate(gpu):
+        m = P.m(s)
+        if s >= 5:
+            assert (mp == (m - 5)[:, None]).all()
+        full, _ = O.full_attention(P.ocfg(rope_mode=O.ROPE_NONE), P.q_step(s), m, P.okv())
+        assert rel_err(out, full).max() <= TOL
+    layer.release()
+
+
 # ---------------------------------------------------------------------------
 # bitwise self-consistency
 # ---------------------------------------------------------------------------
