@@ -166,7 +166,9 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
  * Uses the same chunking and merge order as a decode step in which every
  * head misses, so such a step's output is bitwise equal to this call's; a
  * missing head in a step where others hit attends the same tokens with a
- * chunking that depends on the other units' bands (equal to rounding). */
+ * chunking that depends on the other units' bands (equal to rounding).  The
+ * config's front_sink is ignored (attention over [1, m] is exact either way;
+ * with F > 0 a decode step's miss equals this call to rounding). */
 int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pre,
                        const int32_t *seq_len, const mac_kv *kv, float *out, float *lse,
                        void *stream);
