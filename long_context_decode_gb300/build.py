@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmac_gb300.so")
-SOURCES = ["mac_host.cu", "mac_append.cu", "mac_step_bf16.cu", "mac_step_f32.cu"]
+SOURCES = ["mac_host.cu", "mac_append.cu", "mac_step_bf16.cu", "mac_step_f32.cu", "mac_step_bf16_sink.cu",
+           "mac_step_f32_sink.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -154,8 +154,12 @@ struct AppendParams {
 // ---------------------------------------------------------------------------
 cudaError_t launch_step_bf16(const StepParams &p, int grid, cudaStream_t s);
 cudaError_t launch_step_f32(const StepParams &p, int grid, cudaStream_t s);
+cudaError_t launch_step_bf16_sink(const StepParams &p, int grid, cudaStream_t s);
+cudaError_t launch_step_f32_sink(const StepParams &p, int grid, cudaStream_t s);
 int step_occupancy_bf16(int G, bool paged, int B, int Hq, int Hkv, int K);
 int step_occupancy_f32(int G, bool paged, int B, int Hq, int Hkv, int K);
+int step_occupancy_bf16_sink(int G, bool paged, int B, int Hq, int Hkv, int K);
+int step_occupancy_f32_sink(int G, bool paged, int B, int Hq, int Hkv, int K);
 cudaError_t launch_append(const AppendParams &p, int dtype, cudaStream_t s);
 
 // ---------------------------------------------------------------------------

@@ -124,8 +124,14 @@ int num_sms() {
 int step_grid(const mac_config *c) {
   const int G = c->n_q_heads / c->n_kv_heads;
   const bool paged = c->page_size != 0;
-  int per_sm = c->dtype == MAC_F32 ? step_occupancy_f32(G, paged, c->batch, c->n_q_heads, c->n_kv_heads, c->ring_k)
-                                   : step_occupancy_bf16(G, paged, c->batch, c->n_q_heads, c->n_kv_heads, c->ring_k);
+  const int B = c->batch, Hq = c->n_q_heads, Hkv = c->n_kv_heads, K = c->ring_k;
+  int per_sm = c->dtype == MAC_F32 ? step_occupancy_f32(G, paged, B, Hq, Hkv, K)
+                                   : step_occupancy_bf16(G, paged, B, Hq, Hkv, K);
+  if (c->front_sink > 0) {  // the decode steps launch the sink kernels: the grid must fit both
+    const int s = c->dtype == MAC_F32 ? step_occupancy_f32_sink(G, paged, B, Hq, Hkv, K)
+                                      : step_occupancy_bf16_sink(G, paged, B, Hq, Hkv, K);
+    per_sm = s < per_sm ? s : per_sm;
+  }
   if (per_sm < 1) return 0;
   const int grid = num_sms() * per_sm;
   return grid < kMaxGrid ? grid : kMaxGrid;
@@ -238,6 +244,7 @@ cudaError_t launch_step(StepParams p, const mac_config *c, cudaStream_t s) {
   if (grid < 1) return cudaErrorInvalidValue;
   p.trace = t_trace;
   t_trace = nullptr;
+  if (p.sink_piece) return c->dtype == MAC_F32 ? launch_step_f32_sink(p, grid, s) : launch_step_bf16_sink(p, grid, s);
   return c->dtype == MAC_F32 ? launch_step_f32(p, grid, s) : launch_step_bf16(p, grid, s);
 }
 

@@ -111,7 +111,9 @@ constexpr float kMInit = -1e30f;
 constexpr float kLazy = 8.f;
 constexpr unsigned kFull = 0xffffffffu;
 
-template <typename T, int G, bool PAGED>
+// SINK: whether the kernel attends front-sink pieces (a launch with a front
+// sink uses the SINK = true kernels; the others carry none of that code)
+template <typename T, int G, bool PAGED, bool SINK>
 struct Step {
   static constexpr int kRowBytes = kHeadDim * (int)sizeof(T);
   static constexpr int kTileTok = kStageBytes / (2 * kRowBytes);  // 64 (bf16) / 32 (fp32)
@@ -1510,7 +1512,6 @@ struct Step {
   // tail piece, before the decisions) or no piece at all (no valid length).
   struct PieceIter {
     int kind, it, end;
-    int sk, sk_end, sk_step;  // kind 0: the candidate units of the CTA's sink pieces
   };
 
   // The front sink [1, min(F, m)] of unit u: its length (0 without a sink
@@ -1518,7 +1519,7 @@ struct Step {
   // first CTA of the unit's group after its tail run (the group's last when
   // the tail takes them all), else u mod P.
   __device__ static int sink_len(const StepParams &p, const Smem &S, int u) {
-    if (!p.sink_piece) return 0;
+    if (!SINK || !p.sink_piece) return 0;
     const int64_t m = unit_len(p, S, u);
     if (!len_ok(p, m)) return 0;
     return (int)(m < p.sink_f ? m : p.sink_f);
@@ -1545,18 +1546,12 @@ struct Step {
       I.it = g0 < g1 ? unit_of(offs(S, ph), U, g0) : U;
       I.end = U;
     }
-    I.sk = I.sk_end = 0;
-    I.sk_step = 1;
-    if (kind == 0 && p.sink_piece) {
+    if (SINK && kind == 0 && p.sink_piece) {
+      // the sink candidates first: units c, c + P, ..., or, with units
+      // aligned to CTAs, the one whose group holds CTA c
       const int P = gridDim.x, c = blockIdx.x;
-      if (U > P) {
-        I.sk = c;
-        I.sk_end = U;
-        I.sk_step = P;
-      } else {
-        I.sk = ((c + 1) * U - 1) / P;  // the unit whose group holds CTA c
-        I.sk_end = I.sk + 1;
-      }
+      I.end = -(I.it + 1);
+      I.it = U > P ? c : ((c + 1) * U - 1) / P;
     }
     return I;
   }
@@ -1567,18 +1562,24 @@ struct Step {
       pc = short_piece(p, S, I.it++);
       return true;
     }
-    // kind 0: the CTA's sink pieces come before its tail pieces
+    // kind 0: the CTA's sink pieces come before its tail pieces; while they
+    // are looked for, it is the candidate unit and end = -(tail start + 1)
+    if (SINK && I.end < 0) {
+      const int U = p.B * p.Hkv, P = gridDim.x;
 #pragma unroll 1
-    for (; I.sk < I.sk_end; I.sk += I.sk_step) {
-      const int u = I.sk, n = sink_len(p, S, u);
-      if (n > 0 && sink_cta(p, S, u) == (int)blockIdx.x) {
-        pc.u = u;
-        pc.lo = 1;
-        pc.hi = n;
-        pc.sink = 1;
-        I.sk += I.sk_step;
-        return true;
+      for (; I.it < U; I.it += U > P ? P : U) {
+        const int u = I.it, n = sink_len(p, S, u);
+        if (n > 0 && sink_cta(p, S, u) == (int)blockIdx.x) {
+          pc.u = u;
+          pc.lo = 1;
+          pc.hi = n;
+          pc.sink = 1;
+          I.it += U > P ? P : U;
+          return true;
+        }
       }
+      I.it = -I.end - 1;
+      I.end = U;
     }
     if (I.kind == 3) {
 #pragma unroll 1
@@ -1616,7 +1617,7 @@ struct Step {
       if (kind != 3) {
         const size_t slot = kind == 0 ? (size_t)(pc.u + blockIdx.x)
                                       : kind == 1 ? (size_t)pc.u : (size_t)(U + pc.u + blockIdx.x);
-        float *dst = pc.sink ? p.part_s + (size_t)pc.u * G * kPartStride
+        float *dst = SINK && pc.sink ? p.part_s + (size_t)pc.u * G * kPartStride
                              : (ph ? p.part_b : p.part_a) + slot * G * kPartStride;
         attend_piece(p, S, n, ph, pc, dst, first);
         first = false;
@@ -1733,7 +1734,7 @@ struct Step {
       if (nonempty(S, 1, lo, hi) == 0) return nullptr;
       return p.part_g + ((size_t)(u + k) * G + hh) * kPartStride;
     }
-    if (i >= L.nb + L.nt) return p.part_s + ((size_t)u * G + hh) * kPartStride;  // the sink
+    if (SINK && i >= L.nb + L.nt) return p.part_s + ((size_t)u * G + hh) * kPartStride;  // the sink
     const int c = L.ca0 + (i - L.nb);
     if (S.spanA[c] >= S.spanA[c + 1]) return nullptr;
     return p.part_a + ((size_t)(u + c) * G + hh) * kPartStride;
@@ -2185,9 +2186,9 @@ struct Step {
   }
 };
 
-template <typename T, int G, bool PAGED>
+template <typename T, int G, bool PAGED, bool SINK>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
-  Step<T, G, PAGED>::run(p);
+  Step<T, G, PAGED, SINK>::run(p);
 }
 
 }  // namespace mac
