@@ -200,27 +200,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of the phase of parity `parity`.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 
-// Acquire-release add on a shared-memory counter (CTA scope); returns the
-// old value.
-__device__ __forceinline__ uint32_t atom_add_acqrel_shared(uint32_t addr, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v)
-               : "memory");
-  return old;
-}
 
 // Wait for the phase of parity `parity` of an mbarrier, giving up after
 // ~2^31 clock cycles (about a second) or as soon as *abort is set; returns
@@ -235,9 +215,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   return true;
 }
 
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // 1-D bulk copy (TMA) global -> shared, completion counted in bytes on bar.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
@@ -260,14 +237,6 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uin
       : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared through L2 (both addresses
-// 16-byte aligned); cp_async_wait_all waits for this thread's copies.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
 
 // Bulk prefetch of global memory into L2 (16-byte aligned, size a
 // multiple of 16).

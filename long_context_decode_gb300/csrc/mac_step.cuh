@@ -311,28 +311,6 @@ struct Step {
     return false;
   }
 
-  // Prefix counts of the non-empty spans of phase ph, by one warp.
-  __device__ static void count_spans_warp(const Smem &S, int ph) {
-    const int64_t *span = spans(S, ph);
-    int *ne = ph ? S.neB : S.neA;
-    const int lane = threadIdx.x & 31, P = gridDim.x;
-    int pre = 0;
-#pragma unroll 1
-    for (int base = 0; base <= P; base += 32) {
-      const int c = base + lane;
-      const int f = c < P && span[c] < span[c + 1] ? 1 : 0;
-      int x = f;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += y;
-      }
-      if (c <= P) ne[c] = pre + x - f;
-      pre += __shfl_sync(kFull, x, 31);
-    }
-    __syncwarp();
-  }
-
   // Tail layout, by all consumer threads (ends with a consumer barrier): the
   // exclusive prefix of the tail lengths, the CTA spans, their non-empty
   // counts and every unit's CTA run.  With at most as many units as CTAs,
