@@ -183,7 +183,9 @@ struct Step {
     float *red_m;       // [kWarps][G]
     int32_t *X;
     int64_t *offA;      // [n_units + 1]: first global index of each unit's tail segment
-    int64_t *offB;      // [n_units + 1]: same for the long bands (short ones count 0)
+    int64_t *offB;      // [n_units + 1]: same for the long bands on their cost axis: each
+                        // long band is kLongPiece (a piece's fixed cost) + its tokens;
+                        // short ones count 0
     int64_t *spanA;     // [grid + 1]: CTA c's tail span is [spanA[c], spanA[c+1])
     int64_t *spanB;     // [grid + 1]: same for the long bands
     int *neA, *neB;     // [grid + 1]: non-empty spans among CTAs 0..c-1
@@ -299,12 +301,13 @@ struct Step {
     for (; u < U; ++u) {
       const int64_t a0 = off[u], z0 = off[u + 1];
       if (a0 >= g1) return false;
-      const int64_t a = a0 > g0 ? a0 : g0, z = z0 < g1 ? z0 : g1;
+      const int64_t r0 = ph && z0 > a0 ? a0 + kLongPiece : a0;  // the band's first real token
+      const int64_t a = r0 > g0 ? r0 : g0, z = z0 < g1 ? z0 : g1;
       if (a < z) {
         const int64_t t0 = seg_first(p, S, ph, u);
         pc->u = u;
-        pc->lo = (int)(t0 + (a - a0));
-        pc->hi = (int)(t0 + (z - a0) - 1);
+        pc->lo = (int)(t0 + (a - r0));
+        pc->hi = (int)(t0 + (z - r0) - 1);
         return true;
       }
     }
@@ -415,6 +418,12 @@ struct Step {
   static constexpr int kShortBand = 128;
   static constexpr int kPieceCost = 384;  // fixed cost of a piece and its merge, in tokens
   static constexpr int kSnap = 192;       // largest move of a long-band CTA boundary, in tokens
+  // On the long bands' cost axis each band starts with kLongPiece virtual
+  // tokens, a piece's fixed cost: a CTA whose span meets a band's start
+  // pays it, so a CTA with two pieces gets fewer tokens.  No CTA boundary
+  // falls inside that prefix or at its end (it moves to the band's start),
+  // so every non-empty span holds real tokens of each band it meets.
+  static constexpr int kLongPiece = 192;
   __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
     const int64_t n = seg_len(p, S, 1, u);
     return n > 0 && n <= *S.short_max;
@@ -482,7 +491,7 @@ struct Step {
       const int u = base + lane;
       const int len = u < U ? S.shortU[u] : 0;
       const bool sh = len > 0 && len <= smax;
-      long long x = sh ? 0 : len, y = sh ? len + kPieceCost : 0;
+      long long x = sh || len == 0 ? 0 : kLongPiece + len, y = sh ? len + kPieceCost : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const long long x2 = __shfl_up_sync(kFull, x, o), y2 = __shfl_up_sync(kFull, y, o);
@@ -508,7 +517,7 @@ struct Step {
       S.scp[0] = 0;
       *S.n_short = ns;
       *S.short_max = smax;
-      S.band_tot[0] = cb;       // long-band tokens
+      S.band_tot[0] = cb;       // long-band cost (tokens + a piece's cost per band)
       S.band_tot[1] = cb + cc;  // all cost
     }
     __syncwarp();
@@ -586,7 +595,9 @@ struct Step {
       const long long share2 = part_of(1, tv, 2 * Pl), half = share2 < kSnap ? share2 : kSnap;
       const int u = unit_of(S.offB, p.B * p.Hkv, st);
       const long long lo = S.offB[u], hi = S.offB[u + 1];
-      if (st - lo <= hi - st) {
+      if (st - lo <= kLongPiece) {
+        st = lo;  // inside or at the end of the band's cost prefix
+      } else if (st - lo <= hi - st) {
         if (st - lo <= half) st = lo;
       } else if (hi - st <= half) {
         st = hi;
