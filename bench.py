@@ -344,6 +344,32 @@ def run_mac(args, rank, world, local):
 
     peaks = measured_peaks()
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
+
+    # ---- the miss fallback as its own call: full attention over [1, m] ---
+    # (the same layer stack and current lengths; the speedup of the step
+    # over it is the method's gain on this workload)
+    full = None
+    if args.full_steps > 0:
+        g_full = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(main):
+            with torch.cuda.graph(g_full, stream=main):
+                for layer in range(Lc):
+                    mac.mac_full_attention(cfg, scratch, q_cur[0][layer], seq_cur, kvs[layer], outs[layer],
+                                           None, main)
+            g_full.replay()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(main)
+            for _ in range(args.full_steps):
+                g_full.replay()
+            f1.record(main)
+        torch.cuda.synchronize(dev)
+        full_s = f0.elapsed_time(f1) / 1e3 / (args.full_steps * Lc)
+        m_now = seq_cur.cpu().numpy().astype(np.int64)
+        full_bytes = float(sum(Hkv * int(m) * 2 * d * 2 for m in m_now) + B * Hq * d * 2)
+        full = {"us_per_layer_step": full_s * 1e6, "gbs": full_bytes / full_s / 1e9,
+                "frac": full_bytes / full_s / 1e9 / hbm_peak, "bytes_per_layer_step": full_bytes,
+                "step_speedup": full_s / (t_max / (K * Lc)), "steps": args.full_steps}
     # the step kernel (match + band/tail attention + merge) is the dominant
     # kernel; the append copies ~1/1000 of its bytes on the aux stream
     dominant = "step_kernel"
@@ -387,6 +413,7 @@ def run_mac(args, rank, world, local):
             "append": ({"kernel": "append_kernel", "us_after_step": append_s * 1e6, "write_bytes": write_bytes}
                        if aux is not None else {"kernel": "step_kernel (fused)", "write_bytes": write_bytes}),
         },
+        "full_attention": full,
         "step_roofline": {
             "algorithmic_read_bytes": match_bytes + attend_bytes, "write_bytes": write_bytes,
             "us_per_layer_step": layer_step_s * 1e6,
@@ -555,6 +582,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["mac", "reference"], default="mac")
     ap.add_argument("--workload", default="long-128k")
+    ap.add_argument("--full-steps", type=int, default=4,
+                    help="replays of the full-attention (miss fallback) layer stack timed after the step")
     ap.add_argument("--front-sink", type=int, default=0,
                     help="front-sink isolation: tokens [1, F] out of the summaries, attended every step")
     ap.add_argument("--ring-k", type=int, default=None,
