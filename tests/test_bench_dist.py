@@ -80,3 +80,31 @@ def test_reference_arm_runs_on_rank_zero_only():
 
     out, rank = bench.run_reference(Args, 1, 2)
     assert out is None and rank == 1
+
+
+def test_layer_step_bytes_counts_band_tail_and_sink():
+    # the algorithmic-bytes model: a miss reads [1, m]; a hit at p reads
+    # [p-r+1, m] plus its cached summary; a front sink F starts every span at
+    # F+1 and adds the sink [1, min(F, m)]
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    from long_context_decode_gb300.workloads import WORKLOADS
+    w = WORKLOADS["llama8b-32k"].with_(batch=1)
+    d, G, r, Hkv, Hq = w.head_dim, w.group, w.band_r, w.n_kv_heads, w.n_q_heads
+    m = np.array([10000])
+    row = 2 * d * 2  # K and V bytes per token
+    miss = np.full((1, Hq), -1)
+    hit = np.full((1, Hq), 9000)
+    _, a_miss, _ = bench.layer_step_bytes(w, m, miss, np.array([w.ring_k]))
+    _, a_hit, _ = bench.layer_step_bytes(w, m, hit, np.array([w.ring_k]))
+    assert a_miss == Hkv * 10000 * row
+    assert a_hit == Hkv * (10000 - (9000 - r + 1) + 1) * row + Hq * (d + 1) * 4
+    F = 128
+    _, s_miss, _ = bench.layer_step_bytes(w, m, miss, np.array([w.ring_k]), F)
+    _, s_hit, _ = bench.layer_step_bytes(w, m, hit, np.array([w.ring_k]), F)
+    assert s_miss == a_miss  # [F+1, m] and [1, F]: the same tokens
+    assert s_hit == a_hit + Hkv * F * row
+    # a context inside the sink: everything is sink
+    _, s_small, _ = bench.layer_step_bytes(w, np.array([100]), miss, np.array([0]), F)
+    assert s_small == Hkv * 100 * row
