@@ -178,15 +178,16 @@ def test_repeated_queries_reuse_is_exact_on_gpu():
     layer.release()
 
 
-@pytest.mark.parametrize("F,seeded,paged,Hq,Hkv", [
-    (64, True, False, 8, 2), (128, False, False, 8, 2), (100, True, True, 4, 1), (3000, True, False, 8, 8),
+@pytest.mark.parametrize("F,seeded,paged,Hq,Hkv,dtype", [
+    (64, True, False, 8, 2, BF16), (128, False, False, 8, 2, BF16), (100, True, True, 4, 1, BF16),
+    (3000, True, False, 8, 8, BF16), (96, True, False, 8, 4, F32), (40, False, True, 4, 4, F32),
 ])
-def test_front_sink_trajectory(F, seeded, paged, Hq, Hkv):
+def test_front_sink_trajectory(F, seeded, paged, Hq, Hkv, dtype):
     # front-sink isolation ([MAC] "Production version"): the reused summaries
     # leave out [1, F] and every step attends it exactly; F = 3000 also
     # exceeds the shorter request's context (all sink, no summary)
     w = W(B=2, Hq=Hq, Hkv=Hkv, ctx=(2500, 6000), K=64, r=32, steps=32, query="ar1_skew", tau=0.45,
-          seed=31)
+          seed=31, dtype=dtype)
     P = Problem(w, n_seed=64 if seeded else 0, paged=paged)
     gpu, st, layer = gpu_trajectory(P, w.n_steps, cfg=P.cfg(front_sink=F))
     ref = oracle_trajectory(P, w.n_steps, front_sink=F)
