@@ -77,7 +77,8 @@ typedef struct {
   int64_t max_context; /* largest m any call will see; sizes the scratch workspace */
   int32_t front_sink;  /* F >= 0: front-sink isolation ([MAC] "Production version"): tokens
                           [1, F] stay out of the reused summaries (seeded and appended) and
-                          are attended exactly at every decode step; 0 = none */
+                          are attended exactly at every decode step; 0 = none; negative:
+                          MAC_ERR_INVALID_ARG, above 2^30 - 1: MAC_ERR_UNSUPPORTED */
 } mac_config;
 
 /* K/V cache.  Contiguous (page_size 0): k, v are [B][Hkv][capacity][d].

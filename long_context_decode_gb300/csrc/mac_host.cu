@@ -34,6 +34,7 @@ int validate(const mac_config *c) {
   if ((int64_t)c->batch * c->n_q_heads > kMaxHeads) return MAC_ERR_UNSUPPORTED;
   if (c->max_context > 0x7fffffffLL - 1) return MAC_ERR_UNSUPPORTED;
   if (c->front_sink < 0) return MAC_ERR_INVALID_ARG;
+  if (c->front_sink > 0x3fffffff) return MAC_ERR_UNSUPPORTED;  // kept clear of 32-bit overflow
   return MAC_OK;
 }
 

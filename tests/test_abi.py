@@ -61,6 +61,8 @@ def test_workspace_sizes_and_validation(mac):
         (dict(batch=1, n_q_heads=32, n_kv_heads=8, rope_mode=9), mac.MAC_ERR_INVALID_ARG),
         (dict(batch=1, n_q_heads=32, n_kv_heads=8, rope_base=0.0), mac.MAC_ERR_INVALID_ARG),
         (dict(batch=1024, n_q_heads=32, n_kv_heads=8), mac.MAC_ERR_UNSUPPORTED),  # > 4096 units
+        (dict(batch=1, n_q_heads=32, n_kv_heads=8, front_sink=-1), mac.MAC_ERR_INVALID_ARG),
+        (dict(batch=1, n_q_heads=32, n_kv_heads=8, front_sink=1 << 30), mac.MAC_ERR_UNSUPPORTED),
     ]
     lib = mac.load()
     for kw, code in bad:
