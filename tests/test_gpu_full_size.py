@@ -24,14 +24,15 @@ def built():
     mac.load()
 
 
-@pytest.mark.parametrize("name,steps,sample,ring_k", [
-    ("llama8b-32k", 40, 12, None),
-    ("long-128k", 24, 12, None),
-    ("long-128k", 24, 12, 512),  # the ring-size sweep's K = 512
-    ("verylong-256k", 24, 8, None),
-    ("mixed-paged", 12, 12, None),
+@pytest.mark.parametrize("name,steps,sample,ring_k,sink", [
+    ("llama8b-32k", 40, 12, None, 0),
+    ("long-128k", 24, 12, None, 0),
+    ("long-128k", 24, 12, 512, 0),  # the ring-size sweep's K = 512
+    ("long-128k", 16, 8, None, 128),  # front-sink isolation, F = 128
+    ("verylong-256k", 24, 8, None, 0),
+    ("mixed-paged", 12, 12, None, 0),
 ])
-def test_full_size_workload(name, steps, sample, ring_k):
+def test_full_size_workload(name, steps, sample, ring_k, sink):
     w = WORKLOADS[name].with_(n_steps=steps)
     if ring_k:
         w = with_ring_k(w, ring_k)
@@ -40,8 +41,8 @@ def test_full_size_workload(name, steps, sample, ring_k):
     mask = np.zeros((w.batch, w.n_q_heads), np.uint8)
     flat = rng.choice(w.batch * w.n_q_heads, size=min(sample, w.batch * w.n_q_heads), replace=False)
     mask.reshape(-1)[flat] = 1
-    gpu, st, layer = gpu_trajectory(P, steps)
-    ref = oracle_trajectory(P, steps, head_mask=mask)
+    gpu, st, layer = gpu_trajectory(P, steps, cfg=P.cfg(front_sink=sink))
+    ref = oracle_trajectory(P, steps, head_mask=mask, front_sink=sink)
     c = compare(gpu, ref, O.threshold_sq(128, w.tau), head_mask=mask)
     assert st == 0
     assert c["mismatched"] == 0, c
