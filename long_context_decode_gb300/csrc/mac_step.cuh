@@ -423,7 +423,7 @@ struct Step {
   // pays it, so a CTA with two pieces gets fewer tokens.  No CTA boundary
   // falls inside that prefix or at its end (it moves to the band's start),
   // so every non-empty span holds real tokens of each band it meets.
-  static constexpr int kLongPiece = 192;
+  static constexpr int kLongPiece = 96;
   __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
     const int64_t n = seg_len(p, S, 1, u);
     return n > 0 && n <= *S.short_max;
@@ -1122,7 +1122,9 @@ struct Step {
   }
   static constexpr int kEarlyChunks = 4;
 
-  // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.
+  // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.  One
+  // thread per CTA polls without sleeping: the last arrival is seen one L2
+  // round trip after it lands.
   __device__ static void grid_barrier(const StepParams &p, const Smem &S) {
     if (threadIdx.x == 0) {
       unsigned long long *ctr = reinterpret_cast<unsigned long long *>(p.ctl + 2);
@@ -1135,7 +1137,6 @@ struct Step {
           *S.abort = 1;
           break;
         }
-        __nanosleep(32);
       }
     }
     consumer_sync();
