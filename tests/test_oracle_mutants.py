@@ -48,6 +48,8 @@ MUTANTS = [
     ("sink left out of the output", [("oc_summary(c, x->kv, b, g, q, 1, F < m ? F : m, &tM, &tZ, tS);",
                                       "oc_summary(c, x->kv, b, g, q, 1, 0, &tM, &tZ, tS);")]),
     ("summaries keep the sink on a miss", [("int64_t lo = F + 1;", "int64_t lo = 1;")]),
+    ("front sink ignored everywhere", [("const int64_t F = c->front_sink;", "const int64_t F = 0;"),
+                                       ("(int64_t)c->front_sink + 1, p - c->band_r", "1, p - c->band_r")]),
     ("summaries keep the sink on a hit", [("if (lo < F + 1) lo = F + 1;", "if (lo < 1) lo = 1;")]),
     ("max not tracked", [("if (l > mx) mx = l;", "")]),
     ("values read from K", [("S[i] += e * load_elem(kv->v, c->dtype, row + i);",

@@ -449,6 +449,32 @@ def test_reuse_with_repeated_queries_is_exact(K, r, cycle, seeded, F):
     assert hits >= 20
 
 
+@pytest.mark.parametrize("rope", [O.ROPE_NONE, O.ROPE_HALF, O.ROPE_INTERLEAVED])
+def test_front_sink_covering_the_reused_prefix_gives_exact_attention(rope):
+    # Front-sink isolation ([MAC] "Production version"): the reused summaries
+    # cover [F+1, p-r] only and the sink [1, F] is attended afresh at every
+    # step.  When F >= p - r for every hit, no reused summary holds a token,
+    # so each step is exact attention under its own query although the
+    # queries differ from step to step and every head hits.  An oracle that
+    # dropped F would reuse the summary of [1, p-r] made with q_p.
+    rng, cfg, kv = _rand_problem(13, ring_k=4, band_r=3, tau=-10.0, rope=rope, front_sink=40)
+    B, Hq, d = cfg.batch, cfg.n_q_heads, cfg.head_dim
+    L = np.array([35, 38], np.int32)
+    ring = O.Ring(cfg)
+    O.seed_rings(cfg, ring, rng.standard_normal((B, Hq, 4, d)).astype(np.float32), L, kv)
+    band_tokens = 0
+    for step in range(6):
+        m = (L + 1 + step).astype(np.int32)
+        assert (m - 1 <= 40 + 3).all()  # every candidate p <= m-1 has p - r <= F
+        q = rng.standard_normal((B, Hq, d)).astype(np.float32)
+        res = O.decode_step(cfg, ring, q, m, kv)
+        assert (res["match_pos"] >= 1).all() and (res["match_pos"] - 3 >= 1).all()
+        full, _ = O.full_attention(cfg, q, m, kv)
+        np.testing.assert_allclose(res["out"], full, rtol=1e-11, atol=1e-14)
+        band_tokens += int(np.maximum(0, m - 3 - 40).sum())
+    assert band_tokens > 0  # the band [F+1, m-r] is attended at least once
+
+
 def test_seed_positions_and_slots():
     rng, cfg, kv = _rand_problem(12, ring_k=8, band_r=3)
     L = np.array([5, 40], np.int32)
