@@ -258,6 +258,13 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
 }
 
+// Barrier `id` (2..15) of `n` consumer threads (whole warps), after
+// reconverging the warp.
+__device__ __forceinline__ void named_sync(int id, int n) {
+  __syncwarp();
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // __syncthreads() after reconverging the warp (same reason).
 __device__ __forceinline__ void block_sync() {
   __syncwarp();

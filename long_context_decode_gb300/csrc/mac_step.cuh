@@ -1913,6 +1913,11 @@ struct Step {
         for (int i = 0; i < kDL; ++i) as[i] = Oa[i] * inv;
         const float lse = La > 0.f ? (M + lg2_approx(La)) * kLn2 : -INFINITY;
         if (app) {
+          // a match at p = m - K reads the slot the append overwrites: every
+          // warp of the head has read the cached summary's LSE before the
+          // first warp stores the new one (each lane rewrites only the dims
+          // it read itself)
+          named_sync(2 + hh, kWPH * 32);
           if (own) store_dims<kDL>(p.app_o + app_slot * kHeadDim + dl, as);
           if (wi == 0 && lane == 0) {
             p.app_lse[app_slot] = lse;

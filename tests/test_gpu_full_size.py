@@ -49,3 +49,38 @@ def test_full_size_workload(name, steps, sample, ring_k, sink):
     assert c["max_err"] <= TOL, c
     assert c["hits"] > 0
     layer.release()
+
+
+@pytest.mark.parametrize("query,tau,rope", [
+    ("clustered", 0.6, mac.MAC_ROPE_HALF),
+    ("ar1_skew", 0.45, mac.MAC_ROPE_HALF),
+    ("clustered", 0.6, mac.MAC_ROPE_INTERLEAVED),
+])
+def test_full_rings_several_match_chunks(query, tau, rope):
+    # The ring state the benchmark times: K = 1024 valid candidates per head
+    # from the first step on (seeded rings), i.e. 8 match chunks of 128 rows
+    # per head dealt to 8 different CTAs whose minima meet in one atomic
+    # per head; chunks whose ring positions start past slot 0; decode steps
+    # overwriting the oldest slots (wraparound).  Batch, heads, K and r of the
+    # 4 x 128K workload at shorter, ragged contexts, so the oracle can seed
+    # the sampled heads' summaries.  Every decision every step; outputs of the
+    # sampled heads.
+    w = WORKLOADS["long-128k"].with_(contexts=[6000, 9001, 12345, 7777], n_steps=40, query=query,
+                                     tau=tau)
+    P = Problem(w, n_seed=w.ring_k, device_generated=True)
+    rng = np.random.default_rng(7)
+    mask = np.zeros((w.batch, w.n_q_heads), np.uint8)
+    mask.reshape(-1)[rng.choice(w.batch * w.n_q_heads, size=12, replace=False)] = 1
+    orope = {mac.MAC_ROPE_HALF: O.ROPE_HALF, mac.MAC_ROPE_INTERLEAVED: O.ROPE_INTERLEAVED}[rope]
+    gpu, st, layer = gpu_trajectory(P, w.n_steps, cfg=P.cfg(rope_mode=rope))
+    ref = oracle_trajectory(P, w.n_steps, head_mask=mask, rope_mode=orope)
+    c = compare(gpu, ref, O.threshold_sq(128, w.tau), head_mask=mask)
+    assert st == 0
+    assert c["mismatched"] == 0, c
+    assert c["max_err"] <= TOL, c
+    assert c["hits"] > 0
+    # matches reach back across the whole ring (several chunks per head)
+    far = sum(int(((r["match_pos"] >= 1) & (P.m(s)[:, None] - r["match_pos"] > 128)).sum())
+              for s, r in enumerate(ref))
+    assert far > 0
+    layer.release()

@@ -178,6 +178,36 @@ def test_repeated_queries_reuse_is_exact_on_gpu():
     layer.release()
 
 
+@pytest.mark.parametrize("K", [64, 200])
+def test_match_at_the_oldest_candidate_fused_and_aux(K):
+    # Queries repeat with period exactly K (RoPE off, tau = 0.99: only an
+    # identical query matches), so every hit lands on p = m - K, whose ring
+    # slot is the one the step appends to (m mod K).  The fused append (no
+    # auxiliary stream) must read the cached summary before overwriting it;
+    # both paths must equal exact attention, the oracle, and each other.
+    w = W(B=2, Hq=8, Hkv=2, ctx=(2000, 3333), K=K, r=3, tau=0.99, steps=40)
+    P = Problem(w, n_seed=K)
+    pat = P.q[:, :, :K].copy()
+    for i in range(P.q.shape[2]):
+        P.q[:, :, i] = pat[:, :, i % K]
+    cfg = P.cfg(rope_mode=mac.MAC_ROPE_NONE)
+    fused, st_f, lf = gpu_trajectory(P, w.n_steps, cfg=cfg)
+    aux, st_a, la = gpu_trajectory(P, w.n_steps, cfg=cfg, aux=True)
+    assert st_f == 0 and st_a == 0
+    ocfg = P.ocfg(rope_mode=O.ROPE_NONE)
+    for s, ((of, pf), (oa, pa)) in enumerate(zip(fused, aux)):
+        m = P.m(s)
+        assert (pf == (m - K)[:, None]).all()
+        assert np.array_equal(pf, pa) and np.array_equal(of, oa)
+        full, _ = O.full_attention(ocfg, P.q_step(s), m, P.okv())
+        assert rel_err(of, full).max() <= TOL
+    ref = oracle_trajectory(P, w.n_steps, rope_mode=O.ROPE_NONE)
+    c = compare(fused, ref, O.threshold_sq(128, w.tau))
+    assert c["mismatched"] == 0 and c["max_err"] <= TOL, c
+    lf.release()
+    la.release()
+
+
 @pytest.mark.parametrize("F,seeded,paged,Hq,Hkv,dtype", [
     (64, True, False, 8, 2, BF16), (128, False, False, 8, 2, BF16), (100, True, True, 4, 1, BF16),
     (3000, True, False, 8, 8, BF16), (96, True, False, 8, 4, F32), (40, False, True, 4, 4, F32),
