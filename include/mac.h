@@ -174,8 +174,8 @@ int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pr
                        const int32_t *seq_len, const mac_kv *kv, float *out, float *lse,
                        void *stream);
 
-/* Largest scratch workspace mac_full_attention_noalloc can use (4 MiB). */
-#define MAC_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+/* Largest scratch workspace mac_full_attention_noalloc can use (16 MiB). */
+#define MAC_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
 /* mac_full_attention without a caller-provided scratch workspace.  (The
  * pages have no counterpart; this is a packaging variant.)  For callers that

@@ -20,52 +20,77 @@ namespace mac {
 // work decomposition constants
 // ---------------------------------------------------------------------------
 constexpr int kHeadDim = 128;           // supported head dimension
-constexpr int kConsumers = 256;         // consumer threads per CTA (8 warps) ...
-constexpr int kThreads = kConsumers + 32;  // ... plus one producer warp
-constexpr int kWarps = kConsumers / 32;  // consumer warps
-constexpr int kStages = 4;              // stage buffers in the TMA ring
-constexpr int kStageBytes = 32768;      // bytes per stage (K+V tile, or ring rows)
+constexpr int kWarps = 8;               // warps per CTA; each feeds and drains its own stage ring
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;              // stages in each warp's ring
+constexpr int kStageBytes = 8192;       // bytes per stage: a K/V tile, or ring rows
+constexpr int kItemStages = 2;          // stages per independent work item (a window tile, a match chunk)
 constexpr int kPartStride = kHeadDim + 4;  // floats per (piece, head) partial: o[d], m, l, 0, 0
 constexpr int kMaxUnits = 1024;         // B * Hkv
 constexpr int kMaxHeads = 4096;         // B * Hq
 constexpr int kMaxGrid = 256;           // CTAs of the step grid (one per SM)
 constexpr int kGroupCtas = 16;          // CTAs per merge group of a long band
 constexpr int kGroups = kMaxGrid / kGroupCtas;
-constexpr int kRopeTab = 16;            // requests whose RoPE angles are tabulated per CTA
+constexpr int kMinSpan = 64;            // fewest long-band tokens worth a CTA
 constexpr int kTracePoints = MAC_TRACE_POINTS;  // timestamps per CTA in a phase trace
 constexpr size_t kMaxSmem = 232448;     // dynamic shared memory per CTA (227 KiB)
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Tokens of K/V per window tile (one work item): two stages of K and V rows.
+__host__ __device__ constexpr int tile_tokens(int elem_bytes) {
+  return kItemStages * kStageBytes / (2 * kHeadDim * elem_bytes);
+}
+// Ring rows per match item.
+__host__ __device__ constexpr int item_rows(int elem_bytes) {
+  return kItemStages * kStageBytes / (kHeadDim * elem_bytes);
+}
+
+// The tiles every unit (request, KV head) attends before the decisions,
+// each with its own partial summary: nbw tiles of the band window, cut
+// backwards from m - r (it holds every band a hit can need), ntt tiles of
+// the tail cut forwards from m - r + 1, and nsk tiles of the front sink.
+struct TileCounts {
+  int nbw, ntt, nsk, nt;
+};
+__host__ __device__ inline TileCounts tile_counts(int K, int r, int64_t max_context, int sink_tokens,
+                                                  int elem_bytes) {
+  const int T = tile_tokens(elem_bytes);
+  const int64_t rr = r < max_context ? r : max_context;
+  const int64_t ss = sink_tokens < max_context ? sink_tokens : max_context;
+  TileCounts c;
+  c.nbw = (K + T - 1) / T;
+  c.ntt = (int)((rr + T - 1) / T);
+  c.nsk = (int)((ss + T - 1) / T);
+  c.nt = c.nbw + c.ntt + c.nsk;
+  return c;
+}
+
 // ---------------------------------------------------------------------------
 // scratch workspace (shared by the kernels of one stream)
 // ---------------------------------------------------------------------------
-// The tail tokens of all units, laid end to end in unit order, are split
-// into one contiguous span per CTA, and so are the long bands; a CTA's span
-// meets a few units, each meeting is a piece with its own partial summary.
-// Piece (unit u, CTA c) goes to slot u + c: the CTAs meeting a unit form a
-// run that starts at or after the last CTA of the previous unit, so the
-// slots of different pieces never coincide and B*Hkv + grid - 1 suffice.
-// A short band is one piece, in band slot u; long-band pieces follow at
-// B*Hkv + u + c.  A long band run over more than kGroupCtas CTAs is merged
-// in two levels: CTA group k = c / kGroupCtas first, into group slot u + k
-// (unique for the same reason), then the groups.
-// The per-head minima are double-buffered: decode launch k combines into
-// buffer k & 1 and clears the other for launch k + 1, so no launch has to
-// wait for every CTA to finish reading before clearing.
+// Window tile t of unit u leaves its partial in part_w slot u * nt + t.
+// The long bands (the part of [1, m] before the window, attended only for
+// units with a missing head) are laid end to end and cut into one span
+// per CTA; the CTA meeting unit u leaves its piece's partial in part_c slot
+// u + c (the CTAs meeting a unit form a run starting at or after the last
+// CTA of the previous unit, so these never coincide).  A run over more than
+// kGroupCtas CTAs is merged in two levels: CTA group k = c / kGroupCtas
+// first, into part_g slot u + k.  part_x holds each CTA's per-warp states
+// while it combines them.  The per-head minima are double-buffered: decode
+// launch k combines into buffer k & 1 and clears the other for launch k + 1.
 struct ScratchLayout {
   size_t ctl;        // uint32[64]: [0] status word, [2..3] grid-barrier counter (u64),
                      // [4] CTAs of the running launch finished (the last resets
                      // it), [6] decode launch count
   size_t best;       // uint64 [2][B][Hq]: ~(dist bits << 32 | ~pos) of the best candidate, 0 = none
-  size_t unit_done;  // uint32 [B*Hkv]: pieces (or groups) of the unit finished in this launch
-  size_t group_done; // uint32 [B*Hkv + kGroups]: long-band pieces finished per (unit, CTA group)
-  size_t part_a;     // f32 [B*Hkv + kMaxGrid][G][kPartStride]: tail pieces
-  size_t part_b;     // f32 [2*B*Hkv + kMaxGrid][G][kPartStride]: band pieces (short
-                     // bands at u, long-band pieces at B*Hkv + u + c)
-  size_t part_g;     // f32 [B*Hkv + kGroups][G][kPartStride]: merged CTA groups of a long band
-  size_t part_s;     // f32 [B*Hkv][G][kPartStride]: front-sink pieces
+  size_t unit_done;  // uint32 [B*Hkv]: long-band entries (CTA pieces or groups) finished
+  size_t group_done; // uint32 [B*Hkv + kGroups]: CTA pieces finished per (unit, CTA group)
+  size_t part_w;     // f32 [B*Hkv][nt][G][kPartStride]: window, tail and sink tiles
+  size_t part_c;     // f32 [B*Hkv + kMaxGrid][G][kPartStride]: long-band CTA pieces
+  size_t part_g;     // f32 [B*Hkv + kGroups][G][kPartStride]: merged CTA groups
+  size_t part_x;     // f32 [kMaxGrid][kWarps][G][kPartStride]: warp states of a CTA piece
   size_t total;
 };
 
@@ -97,14 +122,15 @@ struct StepParams {
   KvView kv;
   const void *q;             // query of (b, h) at element (b*Hq + h) * q_stride + q_offset
   int64_t q_stride, q_offset;
+  TileCounts tc;             // window tiles per unit (the scratch is sized for these)
   // decode only
   const int32_t *ring_pos;   // [B][K]
   const void *ring_q;        // [B][Hq][K][d]
   const float *ring_o;       // [B][Hq][K][d]
   const float *ring_lse;     // [B][Hq][K]
   void *stage_q;             // [B][Hq][d]: copy of the step's query for the append
-  // fused append (no auxiliary stream): the final merges write slot
-  // pos mod K of the rings themselves (null: the append kernel does)
+  // fused append (no auxiliary stream): the merges write slot pos mod K of
+  // the rings themselves (null: the append kernel does)
   int32_t *app_pos;          // [B][K]
   void *app_q;               // [B][Hq][K][d]
   float *app_o;              // [B][Hq][K][d]
@@ -119,14 +145,11 @@ struct StepParams {
   uint32_t *ctl;
   unsigned long long *best;  // [2][B*Hq]
   uint32_t *unit_done;       // [B*Hkv]
-  float *part_a;             // tail pieces
-  float *part_b;             // band pieces
   uint32_t *group_done;      // [B*Hkv + kGroups]
-  float *part_g;             // merged CTA groups
-  float *part_s;             // front-sink pieces, one per unit
-  // front sink F: tails and bands start at F+1 at the earliest (the reused
+  float *part_w, *part_c, *part_g, *part_x;
+  // front sink F: every summary starts at F+1 at the earliest (the reused
   // summaries leave [1, F] out); with sink_piece, [1, min(F, m)] is also
-  // attended as an output-only piece of its unit
+  // attended as output-only tiles of its unit
   int sink_f, sink_piece;
   unsigned long long *trace;  // optional: [grid][kTracePoints] %globaltimer stamps
   // RoPE frequency j as a 64-bit fixed-point fraction of a turn per
@@ -152,14 +175,18 @@ struct AppendParams {
 // ---------------------------------------------------------------------------
 // launchers (defined in the .cu files)
 // ---------------------------------------------------------------------------
-cudaError_t launch_step_bf16(const StepParams &p, int grid, cudaStream_t s);
-cudaError_t launch_step_f32(const StepParams &p, int grid, cudaStream_t s);
-cudaError_t launch_step_bf16_sink(const StepParams &p, int grid, cudaStream_t s);
-cudaError_t launch_step_f32_sink(const StepParams &p, int grid, cudaStream_t s);
-int step_occupancy_bf16(int G, bool paged, int B, int Hq, int Hkv, int K);
-int step_occupancy_f32(int G, bool paged, int B, int Hq, int Hkv, int K);
-int step_occupancy_bf16_sink(int G, bool paged, int B, int Hq, int Hkv, int K);
-int step_occupancy_f32_sink(int G, bool paged, int B, int Hq, int Hkv, int K);
+#define MAC_DECLARE_STEP(TN, G)                                                  \
+  cudaError_t launch_step_##TN##_g##G(const StepParams &p, int grid, cudaStream_t s); \
+  int step_occupancy_##TN##_g##G(bool paged, int U, int B);
+MAC_DECLARE_STEP(bf16, 1)
+MAC_DECLARE_STEP(bf16, 2)
+MAC_DECLARE_STEP(bf16, 4)
+MAC_DECLARE_STEP(bf16, 8)
+MAC_DECLARE_STEP(f32, 1)
+MAC_DECLARE_STEP(f32, 2)
+MAC_DECLARE_STEP(f32, 4)
+MAC_DECLARE_STEP(f32, 8)
+#undef MAC_DECLARE_STEP
 cudaError_t launch_append(const AppendParams &p, int dtype, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
@@ -250,16 +277,9 @@ __device__ __forceinline__ unsigned long long l2_evict_first_policy() {
   return pol;
 }
 
-// Barrier of the CTA's consumer threads (all of them).  bar.sync counts
-// whole warps, so each warp first reconverges: a lane still inside a
-// single-lane region must not be counted as arrived.
-__device__ __forceinline__ void consumer_sync() {
-  __syncwarp();
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
-}
-
-// Barrier `id` (2..15) of `n` consumer threads (whole warps), after
-// reconverging the warp.
+// Barrier `id` (1..15) of `n` threads (whole warps), after reconverging the
+// warp: bar.sync counts whole warps, so a lane still inside a single-lane
+// region must not be counted as arrived.
 __device__ __forceinline__ void named_sync(int id, int n) {
   __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -269,6 +289,12 @@ __device__ __forceinline__ void named_sync(int id, int n) {
 __device__ __forceinline__ void block_sync() {
   __syncwarp();
   __syncthreads();
+}
+
+// Orders this thread's earlier shared-memory accesses (generic proxy)
+// before its later bulk copies into shared memory (async proxy).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ float ex2(float x) {

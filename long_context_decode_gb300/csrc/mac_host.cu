@@ -24,7 +24,7 @@ int validate(const mac_config *c) {
     return MAC_ERR_INVALID_ARG;
   if (c->n_q_heads % c->n_kv_heads != 0) return MAC_ERR_INVALID_ARG;
   const int G = c->n_q_heads / c->n_kv_heads;
-  if (G != 1 && G != 2 && G != 4) return MAC_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return MAC_ERR_UNSUPPORTED;
   if (c->head_dim != kHeadDim) return MAC_ERR_UNSUPPORTED;
   if (c->dtype != MAC_BF16 && c->dtype != MAC_F32) return MAC_ERR_INVALID_ARG;
   if (c->page_size != 0 && c->page_size != 16) return MAC_ERR_UNSUPPORTED;
@@ -54,23 +54,30 @@ mac_ring_layout ring_layout(const mac_config *c) {
   return L;
 }
 
-// Everything before part_a must start at zero (the status word, the
+// Tiles per unit of a launch: window and tail, plus the front sink when the
+// launch attends it (decode steps with F > 0).
+TileCounts launch_tiles(const mac_config *c, bool sink_piece) {
+  return tile_counts(c->ring_k, c->band_r, c->max_context, sink_piece ? c->front_sink : 0, elem_size(c));
+}
+
+// Everything before part_w must start at zero (the status word, the
 // counters, the per-head minima and the per-unit piece counts); the
 // partials need no clearing.  A clean launch leaves it so for the next one.
 ScratchLayout scratch_layout(const mac_config *c) {
   const size_t B = c->batch, H = c->n_q_heads, U = (size_t)c->batch * c->n_kv_heads;
   const size_t G = c->n_q_heads / c->n_kv_heads;
-  const size_t slots = U + kMaxGrid;
+  const size_t part = G * kPartStride * 4;  // bytes of one (piece, all heads) partial
+  const size_t nt = (size_t)launch_tiles(c, true).nt;
   ScratchLayout S;
   size_t off = 0;
-  S.ctl = off;     off = align_up(off + 64 * 4, 256);
-  S.best = off;    off = align_up(off + 2 * B * H * 8, 256);
-  S.unit_done = off;  off = align_up(off + U * 4, 256);
+  S.ctl = off;         off = align_up(off + 64 * 4, 256);
+  S.best = off;        off = align_up(off + 2 * B * H * 8, 256);
+  S.unit_done = off;   off = align_up(off + U * 4, 256);
   S.group_done = off;  off = align_up(off + (U + kGroups) * 4, 256);
-  S.part_a = off;  off = align_up(off + slots * G * kPartStride * 4, 256);
-  S.part_b = off;  off = align_up(off + (U + slots) * G * kPartStride * 4, 256);
-  S.part_g = off;  off = align_up(off + (U + kGroups) * G * kPartStride * 4, 256);
-  S.part_s = off;  off = align_up(off + U * G * kPartStride * 4, 256);
+  S.part_w = off;      off = align_up(off + U * nt * part, 256);
+  S.part_c = off;      off = align_up(off + (U + kMaxGrid) * part, 256);
+  S.part_g = off;      off = align_up(off + (U + kGroups) * part, 256);
+  S.part_x = off;      off = align_up(off + (size_t)kMaxGrid * kWarps * part, 256);
   S.total = off;
   return S;
 }
@@ -120,19 +127,22 @@ int num_sms() {
   return n;
 }
 
+int step_occupancy(const mac_config *c) {
+  const int G = c->n_q_heads / c->n_kv_heads, U = c->batch * c->n_kv_heads;
+  const bool paged = c->page_size != 0, f32 = c->dtype == MAC_F32;
+  switch (G) {
+    case 1: return f32 ? step_occupancy_f32_g1(paged, U, c->batch) : step_occupancy_bf16_g1(paged, U, c->batch);
+    case 2: return f32 ? step_occupancy_f32_g2(paged, U, c->batch) : step_occupancy_bf16_g2(paged, U, c->batch);
+    case 4: return f32 ? step_occupancy_f32_g4(paged, U, c->batch) : step_occupancy_bf16_g4(paged, U, c->batch);
+    case 8: return f32 ? step_occupancy_f32_g8(paged, U, c->batch) : step_occupancy_bf16_g8(paged, U, c->batch);
+    default: return 0;
+  }
+}
+
 // Persistent grid: as many CTAs as can be resident at once (one per SM), at
 // most kMaxGrid (the partial slots are sized for that many).
 int step_grid(const mac_config *c) {
-  const int G = c->n_q_heads / c->n_kv_heads;
-  const bool paged = c->page_size != 0;
-  const int B = c->batch, Hq = c->n_q_heads, Hkv = c->n_kv_heads, K = c->ring_k;
-  int per_sm = c->dtype == MAC_F32 ? step_occupancy_f32(G, paged, B, Hq, Hkv, K)
-                                   : step_occupancy_bf16(G, paged, B, Hq, Hkv, K);
-  if (c->front_sink > 0) {  // the decode steps launch the sink kernels: the grid must fit both
-    const int s = c->dtype == MAC_F32 ? step_occupancy_f32_sink(G, paged, B, Hq, Hkv, K)
-                                      : step_occupancy_bf16_sink(G, paged, B, Hq, Hkv, K);
-    per_sm = s < per_sm ? s : per_sm;
-  }
+  const int per_sm = step_occupancy(c);
   if (per_sm < 1) return 0;
   const int grid = num_sms() * per_sm;
   return grid < kMaxGrid ? grid : kMaxGrid;
@@ -166,11 +176,12 @@ StepParams step_params(const mac_config *c, const ScratchLayout &S, uint8_t *scr
   a.ctl = (uint32_t *)(scratch + S.ctl);
   a.best = (unsigned long long *)(scratch + S.best);
   a.unit_done = (uint32_t *)(scratch + S.unit_done);
-  a.part_a = (float *)(scratch + S.part_a);
-  a.part_b = (float *)(scratch + S.part_b);
   a.group_done = (uint32_t *)(scratch + S.group_done);
+  a.part_w = (float *)(scratch + S.part_w);
+  a.part_c = (float *)(scratch + S.part_c);
   a.part_g = (float *)(scratch + S.part_g);
-  a.part_s = (float *)(scratch + S.part_s);
+  a.part_x = (float *)(scratch + S.part_x);
+  a.tc = launch_tiles(c, false);
   return a;
 }
 
@@ -245,8 +256,15 @@ cudaError_t launch_step(StepParams p, const mac_config *c, cudaStream_t s) {
   if (grid < 1) return cudaErrorInvalidValue;
   p.trace = t_trace;
   t_trace = nullptr;
-  if (p.sink_piece) return c->dtype == MAC_F32 ? launch_step_f32_sink(p, grid, s) : launch_step_bf16_sink(p, grid, s);
-  return c->dtype == MAC_F32 ? launch_step_f32(p, grid, s) : launch_step_bf16(p, grid, s);
+  p.tc = launch_tiles(c, p.sink_piece != 0);
+  const bool f32 = c->dtype == MAC_F32;
+  switch (p.G) {
+    case 1: return f32 ? launch_step_f32_g1(p, grid, s) : launch_step_bf16_g1(p, grid, s);
+    case 2: return f32 ? launch_step_f32_g2(p, grid, s) : launch_step_bf16_g2(p, grid, s);
+    case 4: return f32 ? launch_step_f32_g4(p, grid, s) : launch_step_bf16_g4(p, grid, s);
+    case 8: return f32 ? launch_step_f32_g8(p, grid, s) : launch_step_bf16_g8(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Inside a stream capture the record becomes an event-record node of the
@@ -312,7 +330,7 @@ int mac_init_rings(const mac_config *cfg, void *ring_ws, void *scratch_ws, const
   const ScratchLayout S = scratch_layout(cfg);
   uint8_t *ring = (uint8_t *)ring_ws, *scr = (uint8_t *)scratch_ws;
   if (cudaMemsetAsync(ring + R.pos, 0, (size_t)cfg->batch * cfg->ring_k * 4, s) != cudaSuccess ||
-      cudaMemsetAsync(scr, 0, S.part_a, s) != cudaSuccess)
+      cudaMemsetAsync(scr, 0, S.part_w, s) != cudaSuccess)
     return MAC_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -457,7 +475,7 @@ int mac_full_attention_noalloc(const mac_config *cfg, const void *q_pre, const i
   if (!scratch) return MAC_ERR_CUDA;
   // the previous call left its counters and status in the array: clear the
   // control part (everything before the partials) on this call's stream
-  if (cudaMemsetAsync(scratch, 0, scratch_layout(cfg).part_a, (cudaStream_t)stream) != cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, scratch_layout(cfg).part_w, (cudaStream_t)stream) != cudaSuccess)
     return MAC_ERR_CUDA;
   return mac_full_attention(cfg, scratch, q_pre, seq_len, kv, out, lse, stream);
 }

@@ -1,0 +1,4 @@
+// Step-kernel instantiations: f32 K/V and queries, 4 query head(s) per KV head.
+#include "mac_step_launch.cuh"
+
+MAC_STEP_UNIT(float, f32, 4)

@@ -1,5 +1,5 @@
-// Launch helpers of the step kernel, instantiated once per element type and
-// front-sink variant in mac_step_{bf16,f32}{,_sink}.cu (one translation unit
+// Launch helpers of the step kernel, instantiated per element type and GQA
+// group size in mac_step_{bf16,f32}_g{1,2,4,8}.cu (one translation unit
 // each, so the builds run in parallel).
 #pragma once
 
@@ -7,10 +7,10 @@
 
 namespace mac {
 
-template <typename T, int G, bool PAGED, bool SINK>
-static cudaError_t prepare_step(int B, int Hq, int Hkv, int K, size_t *smem) {
-  using S = Step<T, G, PAGED, SINK>;
-  *smem = S::smem_bytes(B, Hq, Hkv, K);
+template <typename T, int G, bool PAGED>
+static cudaError_t prepare_step(int U, int B, size_t *smem) {
+  using S = Step<T, G, PAGED>;
+  *smem = S::smem_bytes(U, B);
   static size_t limit[64] = {0};  // per device: dynamic shared memory limit set on the kernel
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -20,11 +20,11 @@ static cudaError_t prepare_step(int B, int Hq, int Hkv, int K, size_t *smem) {
     int optin = 0;
     cudaFuncAttributes fa;
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
-        (e = cudaFuncGetAttributes(&fa, step_kernel<T, G, PAGED, SINK>)) != cudaSuccess)
+        (e = cudaFuncGetAttributes(&fa, step_kernel<T, G, PAGED>)) != cudaSuccess)
       return e;
     size_t dyn = (size_t)optin - fa.sharedSizeBytes;
     if (dyn > kMaxSmem) dyn = kMaxSmem;
-    e = cudaFuncSetAttribute(step_kernel<T, G, PAGED, SINK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    e = cudaFuncSetAttribute(step_kernel<T, G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
     if (e != cudaSuccess) return e;
     limit[dev] = dyn;
   }
@@ -33,11 +33,11 @@ static cudaError_t prepare_step(int B, int Hq, int Hkv, int K, size_t *smem) {
 }
 
 // Cooperative launch: the grid (one CTA per SM) is guaranteed co-resident,
-// which the grid barriers of the step rely on.
-template <typename T, int G, bool PAGED, bool SINK>
+// which the grid barrier and the long-band counts of the step rely on.
+template <typename T, int G, bool PAGED>
 static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) {
   size_t smem = 0;
-  cudaError_t e = prepare_step<T, G, PAGED, SINK>(p.B, p.Hq, p.Hkv, p.K, &smem);
+  cudaError_t e = prepare_step<T, G, PAGED>(p.B * p.Hkv, p.B, &smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -49,39 +49,28 @@ static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_kernel<T, G, PAGED, SINK>, p);
+  return cudaLaunchKernelEx(&cfg, step_kernel<T, G, PAGED>, p);
 }
 
-template <typename T, int G, bool PAGED, bool SINK>
-static int occupancy_g(int B, int Hq, int Hkv, int K) {
+template <typename T, int G, bool PAGED>
+static int occupancy_g(int U, int B) {
   size_t smem = 0;
-  if (prepare_step<T, G, PAGED, SINK>(B, Hq, Hkv, K, &smem) != cudaSuccess) return 0;
+  if (prepare_step<T, G, PAGED>(U, B, &smem) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<T, G, PAGED, SINK>, kThreads, smem) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<T, G, PAGED>, kThreads, smem) != cudaSuccess)
     return 0;
   return n;
 }
 
-template <typename T, bool SINK>
-static cudaError_t launch_step_t(const StepParams &p, int grid, cudaStream_t s) {
-  const bool paged = p.kv.paged != 0;
-  switch (p.G) {
-    case 1: return paged ? launch_step_g<T, 1, true, SINK>(p, grid, s) : launch_step_g<T, 1, false, SINK>(p, grid, s);
-    case 2: return paged ? launch_step_g<T, 2, true, SINK>(p, grid, s) : launch_step_g<T, 2, false, SINK>(p, grid, s);
-    case 4: return paged ? launch_step_g<T, 4, true, SINK>(p, grid, s) : launch_step_g<T, 4, false, SINK>(p, grid, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <typename T, bool SINK>
-static int occupancy_t(int G, bool paged, int B, int Hq, int Hkv, int K) {
-  switch (G) {
-    case 1: return paged ? occupancy_g<T, 1, true, SINK>(B, Hq, Hkv, K) : occupancy_g<T, 1, false, SINK>(B, Hq, Hkv, K);
-    case 2: return paged ? occupancy_g<T, 2, true, SINK>(B, Hq, Hkv, K) : occupancy_g<T, 2, false, SINK>(B, Hq, Hkv, K);
-    case 4: return paged ? occupancy_g<T, 4, true, SINK>(B, Hq, Hkv, K) : occupancy_g<T, 4, false, SINK>(B, Hq, Hkv, K);
-    default: return 0;
-  }
-}
-
 }  // namespace mac
+
+// One translation unit: element type T (name TN) and group size G.
+#define MAC_STEP_UNIT(T, TN, G)                                                                         \
+  namespace mac {                                                                                       \
+  cudaError_t launch_step_##TN##_g##G(const StepParams &p, int grid, cudaStream_t s) {                  \
+    return p.kv.paged ? launch_step_g<T, G, true>(p, grid, s) : launch_step_g<T, G, false>(p, grid, s); \
+  }                                                                                                     \
+  int step_occupancy_##TN##_g##G(bool paged, int U, int B) {                                            \
+    return paged ? occupancy_g<T, G, true>(U, B) : occupancy_g<T, G, false>(U, B);                     \
+  }                                                                                                     \
+  }

@@ -52,7 +52,7 @@ def test_workspace_sizes_and_validation(mac):
     bad = [
         (dict(batch=0, n_q_heads=32, n_kv_heads=8), mac.MAC_ERR_INVALID_ARG),
         (dict(batch=1, n_q_heads=30, n_kv_heads=8), mac.MAC_ERR_INVALID_ARG),
-        (dict(batch=1, n_q_heads=32, n_kv_heads=4), mac.MAC_ERR_UNSUPPORTED),  # GQA 8
+        (dict(batch=1, n_q_heads=32, n_kv_heads=2), mac.MAC_ERR_UNSUPPORTED),  # GQA 16
         (dict(batch=1, n_q_heads=32, n_kv_heads=8, head_dim=64), mac.MAC_ERR_UNSUPPORTED),
         (dict(batch=1, n_q_heads=32, n_kv_heads=8, page_size=8), mac.MAC_ERR_UNSUPPORTED),
         (dict(batch=1, n_q_heads=32, n_kv_heads=8, band_r=-1), mac.MAC_ERR_INVALID_ARG),

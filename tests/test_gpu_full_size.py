@@ -31,9 +31,13 @@ def built():
     ("long-128k", 16, 8, None, 128),  # front-sink isolation, F = 128
     ("verylong-256k", 24, 8, None, 0),
     ("mixed-paged", 12, 12, None, 0),
+    ("gqa8-128k", 16, 8, None, 0),  # 32 q / 4 kv heads (GQA 8) at 2 x 128K
 ])
 def test_full_size_workload(name, steps, sample, ring_k, sink):
-    w = WORKLOADS[name].with_(n_steps=steps)
+    if name == "gqa8-128k":
+        w = WORKLOADS["long-128k"].with_(batch=2, contexts=[131072, 100000], n_kv_heads=4, n_steps=steps)
+    else:
+        w = WORKLOADS[name].with_(n_steps=steps)
     if ring_k:
         w = with_ring_k(w, ring_k)
     P = Problem(w, device_generated=True, native_paged=w.page_size > 0)
@@ -79,8 +83,9 @@ def test_full_rings_several_match_chunks(query, tau, rope):
     assert c["mismatched"] == 0, c
     assert c["max_err"] <= TOL, c
     assert c["hits"] > 0
-    # matches reach back across the whole ring (several chunks per head)
+    # clustered queries match back across the whole ring (several chunks
+    # per head); AR(1) queries match the most recent positions
     far = sum(int(((r["match_pos"] >= 1) & (P.m(s)[:, None] - r["match_pos"] > 128)).sum())
               for s, r in enumerate(ref))
-    assert far > 0
+    assert far > 0 or query != "clustered"
     layer.release()

@@ -116,7 +116,9 @@ def test_trajectory_from_empty_rings(query, tau, K, r):
 
 
 @pytest.mark.parametrize("Hq,Hkv,dtype,paged", [(4, 4, BF16, False), (8, 4, F32, False),
-                                                (8, 2, BF16, True), (4, 1, F32, True)])
+                                                (8, 2, BF16, True), (4, 1, F32, True),
+                                                (16, 2, BF16, False), (8, 1, F32, True),
+                                                (16, 2, BF16, True)])
 def test_trajectory_seeded_gqa_dtypes(Hq, Hkv, dtype, paged):
     w = W(B=2, Hq=Hq, Hkv=Hkv, ctx=(900, 2000), K=32, r=16, dtype=dtype, steps=24,
           query="ar1_skew", tau=0.45, seed=5)
