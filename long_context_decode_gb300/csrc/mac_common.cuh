@@ -78,15 +78,16 @@ __host__ __device__ inline TileCounts tile_counts(int K, int r, int64_t max_cont
 // CTA of the previous unit, so these never coincide).  A run over more than
 // kGroupCtas CTAs is merged in two levels: CTA group k = c / kGroupCtas
 // first, into part_g slot u + k.  part_x holds each CTA's per-warp states
-// while it combines them.  The per-head minima are double-buffered: decode
-// launch k combines into buffer k & 1 and clears the other for launch k + 1.
+// while it combines them.  The per-head minima and the long-band counts are
+// double-buffered: launch k (counted in ctl[6]) uses buffer k & 1 and clears
+// the other for launch k + 1, so no count has to be reset by its readers.
 struct ScratchLayout {
   size_t ctl;        // uint32[64]: [0] status word, [2..3] grid-barrier counter (u64),
                      // [4] CTAs of the running launch finished (the last resets
-                     // it), [6] decode launch count
+                     // it), [6] launch count
   size_t best;       // uint64 [2][B][Hq]: ~(dist bits << 32 | ~pos) of the best candidate, 0 = none
-  size_t unit_done;  // uint32 [B*Hkv]: long-band entries (CTA pieces or groups) finished
-  size_t group_done; // uint32 [B*Hkv + kGroups]: CTA pieces finished per (unit, CTA group)
+  size_t unit_done;  // uint32 [2][B*Hkv]: long-band entries (CTA pieces or groups) finished
+  size_t group_done; // uint32 [2][B*Hkv + kGroups]: CTA pieces finished per (unit, CTA group)
   size_t part_w;     // f32 [B*Hkv][nt][G][kPartStride]: window, tail and sink tiles
   size_t part_c;     // f32 [B*Hkv + kMaxGrid][G][kPartStride]: long-band CTA pieces
   size_t part_g;     // f32 [B*Hkv + kGroups][G][kPartStride]: merged CTA groups
@@ -123,6 +124,7 @@ struct StepParams {
   const void *q;             // query of (b, h) at element (b*Hq + h) * q_stride + q_offset
   int64_t q_stride, q_offset;
   TileCounts tc;             // window tiles per unit (the scratch is sized for these)
+  int qslot;                 // bytes of each warp's query slot in shared memory (0: none, load from global)
   // decode only
   const int32_t *ring_pos;   // [B][K]
   const void *ring_q;        // [B][Hq][K][d]

@@ -72,8 +72,8 @@ ScratchLayout scratch_layout(const mac_config *c) {
   size_t off = 0;
   S.ctl = off;         off = align_up(off + 64 * 4, 256);
   S.best = off;        off = align_up(off + 2 * B * H * 8, 256);
-  S.unit_done = off;   off = align_up(off + U * 4, 256);
-  S.group_done = off;  off = align_up(off + (U + kGroups) * 4, 256);
+  S.unit_done = off;   off = align_up(off + 2 * U * 4, 256);
+  S.group_done = off;  off = align_up(off + 2 * (U + kGroups) * 4, 256);
   S.part_w = off;      off = align_up(off + U * nt * part, 256);
   S.part_c = off;      off = align_up(off + (U + kMaxGrid) * part, 256);
   S.part_g = off;      off = align_up(off + (U + kGroups) * part, 256);

@@ -168,9 +168,13 @@ struct Step {
   __host__ __device__ static size_t off_rope(int U) {
     return (kOffUnits + 8 * (size_t)(U + 1) + 4 * (size_t)U + 15) / 16 * 16;
   }
-  __host__ __device__ static size_t smem_bytes(int U, int B) {
+  __host__ __device__ static size_t off_slot(int U, int B) {
     return off_rope(U) + (B <= kRopeTab ? 8 * (size_t)B * (kHeadDim / 2) : 0);
   }
+  __host__ __device__ static size_t smem_bytes(int U, int B) { return off_slot(U, B); }
+  // bytes of a warp's slot: a window tile's G query rows, or a match item's
+  // query row and ring positions
+  static constexpr int kSlot = (G * kRow > kRow + kIR * 4 ? G * kRow : kRow + kIR * 4);
 
   struct Smem {
     uint8_t *stage;     // [kWarps][kStages][kStageBytes]
@@ -185,8 +189,11 @@ struct Step {
     int *Pl;            // CTAs the long bands are cut over
     unsigned long long *best, *best_next;
     volatile uint32_t *flag;
-    int *dec;           // [kOwnMax][G]: decisions of the units this CTA owns
+    int *dec;           // [kOwnMax]: decisions of the heads this CTA owns
+    uint32_t *unit_done, *group_done;            // this launch's long-band counts
+    uint32_t *unit_done_next, *group_done_next;  // cleared here for the next launch
     float2 *rope;       // [B][d/2] cos, sin of the query angles (B <= kRopeTab), or null
+    uint8_t *qslot;     // [kWarps][p.qslot]: each warp's copy of its next item's query rows, or null
   };
 
   // One warp's ring: stage uses are numbered; use n sits in stage n % kStages.
@@ -523,7 +530,10 @@ struct Step {
   // R(pos) q~ * log2(e)/sqrt(d) of the G heads of unit u, the lane's dims
   // [8 sub, 8 sub + 8) (explicit roundings keep the result identical
   // wherever it is computed).
-  __device__ static void load_query(const StepParams &p, const Smem &S, int u, float2 (&q)[G][kAPairs]) {
+  // The unit's query rows: from global memory, or (slot) from a warp's
+  // shared-memory copy holding the G rows back to back.
+  __device__ static void load_query(const StepParams &p, const Smem &S, int u, float2 (&q)[G][kAPairs],
+                                    const uint8_t *slot = nullptr) {
     const int lane = lane_id(), sub = lane & 15;
     const int b = u / p.Hkv, g = u - b * p.Hkv;
     const int64_t pos = qpos(p, b);
@@ -545,19 +555,22 @@ struct Step {
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
       const int64_t e0 = ((int64_t)b * p.Hq + g * G + hh) * p.q_stride + p.q_offset;
-      const T *row = reinterpret_cast<const T *>(p.q) + e0;
+      const T *row = slot ? reinterpret_cast<const T *>(slot + hh * kRow) : reinterpret_cast<const T *>(p.q) + e0;
+      auto ld = [&](const T *ptr, int c) -> uint4 {
+        return slot ? reinterpret_cast<const uint4 *>(ptr)[c] : __ldg(reinterpret_cast<const uint4 *>(ptr) + c);
+      };
       float x[8], y[8];
 #pragma unroll
       for (int c = 0; c < kALoads; ++c) {
         float2 f[kAPairs / kALoads];
-        unpack16x2<T>(__ldg(reinterpret_cast<const uint4 *>(row + d0) + c), f);
+        unpack16x2<T>(ld(row + d0, c), f);
 #pragma unroll
         for (int i = 0; i < kAPairs / kALoads; ++i) {
           x[c * 8 / kALoads + 2 * i] = f[i].x;
           x[c * 8 / kALoads + 2 * i + 1] = f[i].y;
         }
         if (half) {
-          unpack16x2<T>(__ldg(reinterpret_cast<const uint4 *>(row + dp) + c), f);
+          unpack16x2<T>(ld(row + dp, c), f);
 #pragma unroll
           for (int i = 0; i < kAPairs / kALoads; ++i) {
             y[c * 8 / kALoads + 2 * i] = f[i].x;
@@ -683,13 +696,13 @@ struct Step {
     const int64_t nw = n_window_items(p);
     if (i >= n_items(p)) return it;
     if (i < nw) {
-      const int u = (int)(i / p.tc.nt), t = (int)(i - (int64_t)u * p.tc.nt);
+      const int u = (int)((uint32_t)i / (uint32_t)p.tc.nt), t = (int)i - u * p.tc.nt;
       it.kind = 1;
       it.u = u;
       tile_range(p, S.um[u], t, &it.lo, &it.hi);
     } else {
       const int cph = match_cph(p);
-      const int mi = (int)(i - nw), bh = mi / cph;
+      const int mi = (int)(i - nw), bh = (int)((uint32_t)mi / (uint32_t)cph);
       it.kind = 2;
       it.u = bh;
       it.lo = (mi - bh * cph) * kIR;
@@ -734,6 +747,38 @@ struct Step {
     if (ptr) asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
   }
 
+  __device__ static void cp_async16(uint8_t *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+  }
+  // Ring positions come with a match item's slot when their chunks are whole 16-byte pieces.
+  __device__ static bool pos_in_slot(const StepParams &p, const Item &it) {
+    return (p.K & 3) == 0 && ((it.hi - it.lo) & 3) == 0;
+  }
+  // Asynchronous copy, into the warp's slot, of what item `it` needs at its
+  // start: the unit's G query rows (a window tile), or the head's query row
+  // and the item's ring positions (a match item).
+  __device__ static void fill_slot(const StepParams &p, const Item &it, uint8_t *slot) {
+    constexpr int kRC = kRow / 16;  // 16-byte chunks per row
+    const int lane = lane_id();
+    const uint8_t *q = (const uint8_t *)p.q;
+    if (it.kind == 1 && it.lo <= it.hi) {
+      const int b = it.u / p.Hkv, g = it.u - b * p.Hkv;
+#pragma unroll 1
+      for (int c = lane; c < G * kRC; c += 32) {
+        const int hh = c / kRC, k = c - hh * kRC;
+        cp_async16(slot + c * 16, q + (((int64_t)b * p.Hq + g * G + hh) * p.q_stride + p.q_offset) * kES + k * 16);
+      }
+    } else if (it.kind == 2) {
+      const uint8_t *row = q + ((int64_t)it.u * p.q_stride + p.q_offset) * kES;
+      if (lane < kRC) cp_async16(slot + lane * 16, row + lane * 16);
+      if (pos_in_slot(p, it)) {
+        const int32_t *pos = p.ring_pos + (int64_t)(it.u / p.Hq) * p.K + it.lo;
+        for (int c = lane; c < (it.hi - it.lo) / 4; c += 32) cp_async16(slot + kRow + c * 16, pos + 4 * c);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+
   __device__ static void phase_a(const StepParams &p, const Smem &S, Ring &R) {
     const int lane = lane_id(), w = warp_id(), P = gridDim.x, NW = P * kWarps;
     const int gw = w * P + blockIdx.x;
@@ -753,6 +798,8 @@ struct Step {
       }
       return true;
     };
+    uint8_t *slot = S.qslot ? S.qslot + (size_t)w * p.qslot : nullptr;
+    if (slot) fill_slot(p, item_at(p, S, gw), slot);
     Desc nx;
     nx.kind = -1;
     nx.u = nx.a = nx.cnt = 0;
@@ -767,27 +814,55 @@ struct Step {
     Att A;
     float2 q[G][kAPairs];
     float2 qlo[4], qhi[4];
+    Item ci = item_at(p, S, gw);
 #pragma unroll 1
-    for (Item ci = item_at(p, S, gw); ci.kind >= 0 && !*S.abort; ci = item_at(p, S, ci.i + NW)) {
+    while (ci.kind >= 0 && !*S.abort) {
       if (tr) tc0 = globaltimer();
       float bd = INFINITY;
       int bp = -1, pos_lo = 1, pos_hi = 0;
+      int pks[kItemStages];
+#pragma unroll
+      for (int s2 = 0; s2 < kItemStages; ++s2) pks[s2] = 0;
+      if (slot) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();
+      }
       if (ci.kind == 1) {
         att_init(A);
-        if (ci.lo <= ci.hi) load_query(p, S, ci.u, q);
+        if (ci.lo <= ci.hi) load_query(p, S, ci.u, q, slot);
       } else {
-        // the head's query row (both halves of the lane's dims) and its window of candidates
+        // the head's query row (both halves of the lane's dims), its window
+        // of candidates and the positions of the rows this lane finishes
         const int bh = ci.u, b = bh / p.Hq;
-        const T *row = reinterpret_cast<const T *>(p.q) + (int64_t)bh * p.q_stride + p.q_offset;
+        const T *row = slot ? reinterpret_cast<const T *>(slot)
+                            : reinterpret_cast<const T *>(p.q) + (int64_t)bh * p.q_stride + p.q_offset;
 #pragma unroll
         for (int c = 0; c < kHalfLoads; ++c) {
-          unpack16x2<T>(__ldg(reinterpret_cast<const uint4 *>(row + (lane & 7) * 8) + c), qlo + c * (4 / kHalfLoads));
-          unpack16x2<T>(__ldg(reinterpret_cast<const uint4 *>(row + kHeadDim / 2 + (lane & 7) * 8) + c),
-                        qhi + c * (4 / kHalfLoads));
+          const uint4 *lo4 = reinterpret_cast<const uint4 *>(row + (lane & 7) * 8) + c;
+          const uint4 *hi4 = reinterpret_cast<const uint4 *>(row + kHeadDim / 2 + (lane & 7) * 8) + c;
+          unpack16x2<T>(slot ? *lo4 : __ldg(lo4), qlo + c * (4 / kHalfLoads));
+          unpack16x2<T>(slot ? *hi4 : __ldg(hi4), qhi + c * (4 / kHalfLoads));
         }
         const int m = S.um[b * p.Hkv];
         pos_lo = m > 0 ? max(1, m - p.K) : 1;
         pos_hi = m > 0 ? m - 1 : 0;
+        const int cnt = ci.hi - ci.lo, r = match_row(lane);
+#pragma unroll
+        for (int s2 = 0; s2 < kItemStages; ++s2) {
+          const int k = s2 * kStRows + r;
+          if (k < cnt) {
+            if (slot && pos_in_slot(p, ci))
+              pks[s2] = reinterpret_cast<const int32_t *>(slot + kRow)[k];
+            else
+              pks[s2] = __ldg(p.ring_pos + (int64_t)b * p.K + ci.lo + k);
+          }
+        }
+      }
+      // the slot is free: the next item's copy overlaps this one
+      const Item nxt = item_at(p, S, ci.i + NW);
+      if (slot) {
+        __syncwarp();
+        fill_slot(p, nxt, slot);
       }
       if (tr) {
         const unsigned long long t = globaltimer();
@@ -798,10 +873,8 @@ struct Step {
       for (int s = 0; s < kItemStages; ++s) {
         const Desc d = stage_desc(ci, s);
         int pk = 0;
-        if (d.kind == 2) {  // position of the row this lane finishes
-          const int r = match_row(lane);
-          pk = __ldg(p.ring_pos + (int64_t)(d.u / p.Hq) * p.K + d.a + (r < d.cnt ? r : d.cnt - 1));
-        }
+#pragma unroll
+        for (int s2 = 0; s2 < kItemStages; ++s2) pk = s2 == s ? pks[s2] : pk;
         const uint32_t n = R.used;
         const bool ok = wait_stage(p, S, R, n);
         if (tr) {
@@ -846,7 +919,9 @@ struct Step {
         if (lane == 0 && bp >= 1) atomicMax(&S.best[ci.u], pack_best(bd, bp));
       }
       if (tr) t_end += globaltimer() - tc0;
+      ci = nxt;
     }
+    if (slot) asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (tr) {
       tr[8] = t_wait;
       tr[9] = t_item;
@@ -901,9 +976,10 @@ struct Step {
     return base + xi - x;
   }
 
-  // Units owned (merged) by this CTA: u with floor(u P / U) == c (U <= P),
-  // or u = c, c + P, ... (U > P); own_index: the unit's rank among them, -1
-  // when not owned here or beyond the kOwnMax whose decisions are kept.
+  // Heads owned (merged) by this CTA, out of N: bh with floor(bh P / N) == c
+  // (N <= P), or bh = c, c + P, ... (N > P); own_index: the head's rank among
+  // them, -1 when not owned here or beyond the kOwnMax whose decisions are
+  // kept.
   static constexpr int kOwnMax = 16;
   __device__ static void own_range(int U, int *u0, int *u_end, int *step) {
     const int P = gridDim.x, c = blockIdx.x;
@@ -931,12 +1007,12 @@ struct Step {
       if (u < U) {
         bool miss = p.mode != MODE_DECODE;
         const int b = u / p.Hkv, g = u - b * p.Hkv;
-        const int k = own_index(U, u);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
-          const int pos = decision(p, S, b * p.Hq + g * G + hh);
+          const int bh = b * p.Hq + g * G + hh, pos = decision(p, S, bh);
+          const int k = own_index(p.B * p.Hq, bh);
           miss |= pos < 1;
-          if (k >= 0) S.dec[k * G + hh] = pos;
+          if (k >= 0) S.dec[k] = pos;
         }
         x = long_len(p, S, u, miss);
       }
@@ -1026,7 +1102,8 @@ struct Step {
       dst[0] = v[0];
   }
   // the weight of a member (m, l) in a state at maximum M
-  __device__ static float mweight(float m, float l, float M) { return l > 0.f ? ex2(m - M) : 0.f; }
+  // (a member with nothing in it, l == 0 or m == -inf, weighs 0)
+  __device__ static float mweight(float m, float l, float M) { return l > 0.f && m > -INFINITY ? ex2(m - M) : 0.f; }
 
   // A log-domain state (base 2) over this lane's dims: maximum, sum, weighted values.
   struct Cls {
@@ -1142,31 +1219,114 @@ struct Step {
     att_finish(A, S.bd, hh);
   }
 
-  // The merge of head hh of unit u (by the head's warps, this warp's dims):
-  // AS = [cached] (+) [boundary] (+) band tiles [0, nbt) (+) long-band
-  // entries, then the output AS (+) tail tiles (+) sink tiles; the rectified
-  // summary AS_{1:m-r} goes to the ring slot of position m (fused append) or
-  // to the staging area for the append kernel.  With a boundary piece
-  // [bd_lo, bd_hi], the head's first warp attends it (its stages were issued
-  // from ring use bd_n0 on) while the list is merged.
-  __device__ static void merge_head(const StepParams &p, const Smem &S, Ring &R, int u, int hh, int pos, int nbt,
-                                    bool has_bd, int bd_lo, int bd_hi, uint32_t bd_n0, int c0, int c1) {
-    const int lane = lane_id(), wi = warp_id() % kWPH;
-    const int b = u / p.Hkv, g = u - b * p.Hkv, bh = b * p.Hq + g * G + hh;
-    const int dl = wi * kDW + min(lane, kLanes - 1) * kDL;
-    const bool own = lane < kLanes, decode = p.mode == MODE_DECODE;
-    const bool hit = pos >= 1;
-    // the cached rectified summary of a hit (a state of sum 1 at its ln-LSE)
-    float c_lse = 0.f, c_o[kDL];
-#pragma unroll
-    for (int i = 0; i < kDL; ++i) c_o[i] = 0.f;
-    if (hit) {
-      const int64_t slot = (int64_t)bh * p.K + pos % p.K;
-      c_lse = __ldcg(p.ring_lse + slot);
-      load_dims<kDL>(p.ring_o + slot * kHeadDim + dl, c_o);
+  // ---------------------------------------------------------------------
+  // phase B
+  // ---------------------------------------------------------------------
+  // The owner's merge of one head bh by all the CTA's warps: before the long
+  // bands (pass 0) a hit or a miss of a unit without a long band, after them
+  // (pass 1) a miss of a unit with one.  AS = [cached] (+) [boundary] (+)
+  // band tiles [0, nbt) (+) long-band entries; the output AS (+) tail tiles
+  // (+) sink tiles; the rectified summary AS_{1:m-r} goes to the ring slot
+  // of position m (fused append) or to the staging area.  Warp w sums list
+  // entries w, w + 8, ... (4 dims per lane) per class; the CTA then combines
+  // the warps' states in a fixed order.  A hit whose band starts inside a
+  // window tile has a boundary piece, attended by warp 0 (its copies are
+  // issued first, so they land while the list is loaded).  pos: the head's
+  // decision (-2: not known yet).  All threads call it.
+  struct St {
+    float M, L, O[4];
+  };
+  __device__ static void st_join(St &a, float xm, float xl, const float4 &xo) {
+    const float M = fmaxf(a.L > 0.f ? a.M : -INFINITY, xl > 0.f ? xm : -INFINITY);
+    const float wa = mweight(a.M, a.L, M), wx = mweight(xm, xl, M);
+    a.L = wa * a.L + wx * xl;
+    a.O[0] = wa * a.O[0] + wx * xo.x;
+    a.O[1] = wa * a.O[1] + wx * xo.y;
+    a.O[2] = wa * a.O[2] + wx * xo.z;
+    a.O[3] = wa * a.O[3] + wx * xo.w;
+    a.M = M;
+  }
+  __device__ static void merge_one(const StepParams &p, const Smem &S, Ring &R, int bh, bool long_pass, int pos) {
+    const int b = bh / p.Hq, h = bh - b * p.Hq, g = h / G, hh = h - g * G, u = b * p.Hkv + g;
+    const int lane = lane_id(), w = warp_id(), tid = threadIdx.x;
+    const bool decode = p.mode == MODE_DECODE;
+    if (pos == -2) pos = decision(p, S, bh);
+    int c0, c1;
+    long_run(S, u, &c0, &c1);
+    const bool late = pos < 1 && c1 >= c0;
+    if (late != long_pass) return;
+    const int m = S.um[u];
+    if (m <= 0) {
+      // a length outside the cache: zero output, no append
+      if (tid < kHeadDim) p.out[(int64_t)bh * kHeadDim + tid] = 0.f;
+      if (tid == 0) {
+        if (p.out_lse) p.out_lse[bh] = -INFINITY;
+        if (p.match_pos_out) p.match_pos_out[bh] = -1;
+      }
+      block_sync();
+      return;
+    }
+    int nbt = p.tc.nbw, lo = 0, thi = -1;
+    bool has_bd = false;
+    if (pos >= 1) {
+      lo = max(lb(p), pos - p.r + 1);
+      if (lo > m - p.r) {
+        nbt = 0;
+      } else {
+        const int j = (m - p.r - lo) / kTT;
+        int tlo;
+        tile_range(p, m, j, &tlo, &thi);
+        nbt = lo == tlo ? j + 1 : j;
+        has_bd = lo != tlo && !*S.abort;
+      }
+      c0 = 0;
+      c1 = -1;
+    }
+    unsigned long long *tr = p.trace && lane == 0 && w <= 1 ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
+    if (tr && w == 0) tr[18] = globaltimer();
+    if (p.trace && w == 2 && lane == 0) {
+      // latency probe: a partial's first line, another line of it, the query row
+      unsigned long long *t2 = p.trace + (size_t)blockIdx.x * kTracePoints;
+      const float *e0 = p.part_w + (size_t)u * p.tc.nt * G * kPartStride;
+      unsigned long long a = globaltimer();
+      float x = __ldcg(e0 + 64);
+      if (x == 123.f) t2[31] = 1;
+      unsigned long long b2 = globaltimer();
+      float y = __ldcg(e0 + 96 + (x == 1.f));
+      if (y == 123.f) t2[31] = 1;
+      unsigned long long c2 = globaltimer();
+      float z = __ldcg(reinterpret_cast<const float *>(p.q) + (int64_t)bh * 64);
+      if (z == 123.f) t2[31] = 1;
+      unsigned long long d2 = globaltimer();
+      t2[20] = b2 - a;
+      t2[21] = c2 - b2;
+      t2[22] = d2 - c2;
+    }
+    const uint32_t n0 = R.issued;
+    if (has_bd && w == 0) {
+      int32_t id[2];
+#pragma unroll 1
+      for (int a = lo; a <= thi; a += kStTok) {
+        Desc d;
+        d.kind = 1;
+        d.u = u;
+        d.a = a;
+        d.cnt = min(thi - a + 1, kStTok);
+        load_ids(p, d, id);
+        issue(p, R, d, id);
+      }
+    }
+    // the cached rectified summary of a hit (a state of sum 1 at its ln-LSE), by warp 1
+    const int64_t cslot = (int64_t)bh * p.K + (pos >= 1 ? pos % p.K : 0);
+    float c_lse = 0.f;
+    float4 c_o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (pos >= 1 && w == 1) {
+      c_lse = __ldcg(p.ring_lse + cslot);
+      c_o = __ldcg(reinterpret_cast<const float4 *>(p.ring_o + cslot * kHeadDim) + lane);
     }
     const int nl = long_entries(c0, c1);
     const int nt = p.tc.ntt + (p.sink_piece ? p.tc.nsk : 0);
+    const int n = nbt + nl + nt, nb = nbt + nl;
     const float *tiles = p.part_w + (size_t)u * p.tc.nt * G * kPartStride + hh * kPartStride;
     auto entry = [&](int i) -> const float * {
       if (i < nbt) return tiles + (size_t)i * G * kPartStride;
@@ -1175,126 +1335,104 @@ struct Step {
       i -= nl;
       return tiles + (size_t)(p.tc.nbw + i) * G * kPartStride;
     };
-    Cls band, tail;
-    merge_list(nbt + nl + nt, nbt + nl, entry, dl, band, tail);
-    if (hit) join(band, c_lse * kLog2e, 1.f, c_o);
-    if (has_bd) {
-      if (wi == 0) boundary_piece(p, S, R, u, hh, bd_lo, bd_hi, bd_n0);
-      named_sync(1 + hh, kWPH * 32);  // the boundary state is in S.bd[hh]
-      float x[kDL];
+    St band, tail;
+    band.M = tail.M = -INFINITY;
+    band.L = tail.L = 0.f;
 #pragma unroll
-      for (int i = 0; i < kDL; ++i) x[i] = S.bd[hh * kPartStride + dl + i];
-      join(band, S.bd[hh * kPartStride + kHeadDim], S.bd[hh * kPartStride + kHeadDim + 1], x);
-    }
-    if (decode) {
-      const int64_t qp = qpos(p, b);
-      const bool app = p.app_o && len_ok(p, qp);
-      // AS_{1:m-r}, normalised, with its ln-LSE: the rectified summary the
-      // ring keeps for position m
-      const float inv = band.L > 0.f ? rcp_approx(band.L) : 0.f;
-      float as[kDL];
-#pragma unroll
-      for (int i = 0; i < kDL; ++i) as[i] = band.O[i] * inv;
-      const float lse = band.L > 0.f ? (band.M + lg2_approx(band.L)) * kLn2 : -INFINITY;
-      const int64_t slot = (int64_t)bh * p.K + qp % p.K;
-      constexpr int kChunks = kHeadDim / kPer;
-      uint4 qv = make_uint4(0, 0, 0, 0);
-      if (wi == 0 && lane < kChunks)
-        qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
-      if (app) {
-        // a match at p = m - K read the slot the append overwrites: every
-        // warp of the head has read the cached summary before any stores
-        named_sync(1 + hh, kWPH * 32);
-        if (own) store_dims<kDL>(p.app_o + slot * kHeadDim + dl, as);
-        if (wi == 0) {
-          if (lane == 0) {
-            p.app_lse[slot] = lse;
-            if (hh == 0 && g == 0) p.app_pos[(int64_t)b * p.K + qp % p.K] = (int32_t)qp;
-          }
-          if (lane < kChunks) reinterpret_cast<uint4 *>(p.app_q)[slot * kChunks + lane] = qv;
-        }
-      } else if (p.as_o) {
-        if (own) store_dims<kDL>(p.as_o + (int64_t)bh * kHeadDim + dl, as);
-        if (wi == 0) {
-          if (lane == 0) p.as_lse[bh] = lse;
-          if (lane < kChunks) reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * kChunks + lane] = qv;
-        }
-      }
-      if (wi == 0 && lane == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
-    }
-    // the output: AS with the tail (and the sink)
-    join(band, tail.M, tail.L, tail.O);
-    const float inv = band.L > 0.f ? rcp_approx(band.L) : 0.f;
-    float o[kDL];
-#pragma unroll
-    for (int i = 0; i < kDL; ++i) o[i] = band.O[i] * inv;
-    if (own) store_dims<kDL>(p.out + (int64_t)bh * kHeadDim + dl, o);
-    if (p.out_lse && wi == 0 && lane == 0)
-      p.out_lse[bh] = band.L > 0.f ? (band.M + lg2_approx(band.L)) * kLn2 : -INFINITY;
-  }
-
-  // ---------------------------------------------------------------------
-  // phase B
-  // ---------------------------------------------------------------------
-  // The owner's merges of unit u's heads, one head per kWPH warps: before
-  // the long bands (pass 0) every head but the misses of a unit with a long
-  // band, after them (pass 1) those misses.  A hit whose band starts inside
-  // a window tile has a boundary piece; its copies are issued first, so they
-  // land while the list is merged.  dec: the unit's decisions (or null).
-  __device__ static void merge_unit(const StepParams &p, const Smem &S, Ring &R, int u, bool long_pass,
-                                    const int *dec) {
-    const int b = u / p.Hkv, g = u - b * p.Hkv;
-    const int hh = warp_id() / kWPH, wi = warp_id() % kWPH, bh = b * p.Hq + g * G + hh;
-    const int pos = dec ? dec[hh] : decision(p, S, bh);
-    int c0, c1;
-    long_run(S, u, &c0, &c1);
-    const bool late = pos < 1 && c1 >= c0;
-    const int m = S.um[u];
-    if (late == long_pass && m > 0) {
-      int nbt = p.tc.nbw, lo = 0, thi = -1;
-      bool has_bd = false;
-      uint32_t n0 = R.issued;
-      if (pos >= 1) {
-        lo = max(lb(p), pos - p.r + 1);
-        if (lo > m - p.r) {
-          nbt = 0;
-        } else {
-          const int j = (m - p.r - lo) / kTT;
-          int tlo;
-          tile_range(p, m, j, &tlo, &thi);
-          nbt = lo == tlo ? j + 1 : j;
-          has_bd = lo != tlo && !*S.abort;
-        }
-        if (has_bd && wi == 0) {
-          int32_t id[2];
+    for (int i = 0; i < 4; ++i) band.O[i] = tail.O[i] = 0.f;
+    constexpr int kE = 8;  // entries a warp has in flight
 #pragma unroll 1
-          for (int a = lo; a <= thi; a += kStTok) {
-            Desc d;
-            d.kind = 1;
-            d.u = u;
-            d.a = a;
-            d.cnt = min(thi - a + 1, kStTok);
-            load_ids(p, d, id);
-            issue(p, R, d, id);
-          }
-        }
-        c0 = 0;
-        c1 = -1;
-      }
-      merge_head(p, S, R, u, hh, pos, nbt, has_bd, lo, thi, n0, c0, c1);
-    } else if (late == long_pass) {
-      // a length outside the cache: zero output, no append
-      const int dl = wi * kDW + min(lane_id(), kLanes - 1) * kDL;
-      float z[kDL];
+    for (int i0 = w; i0 < n; i0 += kWarps * kE) {
+      float2 ml[kE];
+      float4 ov[kE];
 #pragma unroll
-      for (int i = 0; i < kDL; ++i) z[i] = 0.f;
-      if (lane_id() < kLanes) store_dims<kDL>(p.out + (int64_t)bh * kHeadDim + dl, z);
-      if (wi == 0 && lane_id() == 0) {
-        if (p.out_lse) p.out_lse[bh] = -INFINITY;
-        if (p.match_pos_out) p.match_pos_out[bh] = -1;
+      for (int e = 0; e < kE; ++e) {
+        const int i = i0 + e * kWarps;
+        const float *src = i < n ? entry(i) : g_zero_partial;
+        ml[e] = __ldcg(reinterpret_cast<const float2 *>(src + kHeadDim));
+        ov[e] = __ldcg(reinterpret_cast<const float4 *>(src) + lane);
+      }
+#pragma unroll
+      for (int e = 0; e < kE; ++e) {
+        const int i = i0 + e * kWarps;
+        if (i < nb) st_join(band, ml[e].x, ml[e].y, ov[e]);
+        else if (i < n) st_join(tail, ml[e].x, ml[e].y, ov[e]);
       }
     }
+    if (pos >= 1 && w == 1) st_join(band, c_lse * kLog2e, 1.f, c_o);
+    if (tr) tr[w == 0 ? 13 : 19] = globaltimer();
+    if (has_bd && w == 0) {
+      boundary_piece(p, S, R, u, hh, lo, thi, n0);
+      __syncwarp();
+      const float *x = S.bd + hh * kPartStride;
+      st_join(band, x[kHeadDim], x[kHeadDim + 1], reinterpret_cast<const float4 *>(x)[lane]);
+    }
+    // the warps' states, in warp 7's idle stage ring
+    float *red = reinterpret_cast<float *>(S.stage + (size_t)7 * kStages * kStageBytes);
+#pragma unroll
+    for (int cls = 0; cls < 2; ++cls) {
+      const St &st = cls ? tail : band;
+      float *d = red + (w * 2 + cls) * kPartStride;
+      reinterpret_cast<float4 *>(d)[lane] = make_float4(st.O[0], st.O[1], st.O[2], st.O[3]);
+      if (lane == 0) *reinterpret_cast<float2 *>(d + kHeadDim) = make_float2(st.M, st.L);
+    }
+    if (tr && w == 0) tr[14] = globaltimer();
     block_sync();
+    if (tr && w == 0) tr[15] = globaltimer();
+    if (tid < kHeadDim) {
+      float MB = -INFINITY, MT = -INFINITY;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) {
+        const float *bs = red + (ww * 2) * kPartStride, *ts = bs + kPartStride;
+        if (bs[kHeadDim + 1] > 0.f) MB = fmaxf(MB, bs[kHeadDim]);
+        if (ts[kHeadDim + 1] > 0.f) MT = fmaxf(MT, ts[kHeadDim]);
+      }
+      float LB = 0.f, OB = 0.f, LT = 0.f, OT = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) {
+        const float *bs = red + (ww * 2) * kPartStride, *ts = bs + kPartStride;
+        const float wb = mweight(bs[kHeadDim], bs[kHeadDim + 1], MB), wt = mweight(ts[kHeadDim], ts[kHeadDim + 1], MT);
+        LB += wb * bs[kHeadDim + 1];
+        OB = fmaf(wb, bs[tid], OB);
+        LT += wt * ts[kHeadDim + 1];
+        OT = fmaf(wt, ts[tid], OT);
+      }
+      const int64_t qp = qpos(p, b);
+      if (decode) {
+        // AS_{1:m-r}, normalised, with its ln-LSE: the rectified summary
+        // the ring keeps for position m
+        const float as = LB > 0.f ? OB * rcp_approx(LB) : 0.f;
+        const float lse = LB > 0.f ? (MB + lg2_approx(LB)) * kLn2 : -INFINITY;
+        const int64_t slot = (int64_t)bh * p.K + qp % p.K;
+        if (p.app_o && len_ok(p, qp)) {
+          p.app_o[slot * kHeadDim + tid] = as;
+          if (tid == 0) {
+            p.app_lse[slot] = lse;
+            if (h == 0) p.app_pos[(int64_t)b * p.K + qp % p.K] = (int32_t)qp;
+          }
+        } else if (p.as_o) {
+          p.as_o[(int64_t)bh * kHeadDim + tid] = as;
+          if (tid == 0) p.as_lse[bh] = lse;
+        }
+        if (tid == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
+      }
+      // the output: AS with the tail (and the sink)
+      const float M2 = fmaxf(LB > 0.f ? MB : -INFINITY, LT > 0.f ? MT : -INFINITY);
+      const float wa = mweight(MB, LB, M2), wt = mweight(MT, LT, M2);
+      const float L2 = wa * LB + wt * LT;
+      p.out[(int64_t)bh * kHeadDim + tid] = L2 > 0.f ? (wa * OB + wt * OT) * rcp_approx(L2) : 0.f;
+      if (tid == 0 && p.out_lse) p.out_lse[bh] = L2 > 0.f ? (M2 + lg2_approx(L2)) * kLn2 : -INFINITY;
+    } else if (decode && tid < kHeadDim + kHeadDim / kPer) {
+      // the step's query, for the ring (fused append) or the append kernel
+      const int64_t qp = qpos(p, b);
+      const int c = tid - kHeadDim;
+      const uint4 qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + c];
+      if (p.app_o && len_ok(p, qp))
+        reinterpret_cast<uint4 *>(p.app_q)[((int64_t)bh * p.K + qp % p.K) * (kHeadDim / kPer) + c] = qv;
+      else if (p.as_o)
+        reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * (kHeadDim / kPer) + c] = qv;
+    }
+    block_sync();  // the combine area is free again
   }
 
   // The long bands: this CTA's span, piece by piece (one per unit it
@@ -1437,10 +1575,10 @@ struct Step {
         int act = 0;
         if (grouped(c0, c1)) {
           const int a0 = max(c0, k * kGroupCtas), z0 = min(c1, k * kGroupCtas + kGroupCtas - 1);
-          const uint32_t old = atom_add_acq_rel_u32(p.group_done + u + k, 1u);
+          const uint32_t old = atom_add_acq_rel_u32(S.group_done + u + k, 1u);
           act = (int)old + 1 == z0 - a0 + 1 ? 1 : 0;
         } else {
-          atom_add_acq_rel_u32(p.unit_done + u, 1u);
+          atom_add_acq_rel_u32(S.unit_done + u, 1u);
         }
         *S.flag = act;
       }
@@ -1450,8 +1588,7 @@ struct Step {
         merge_group(p, u, c0, c1, k);
         block_sync();
         if (threadIdx.x == 0) {
-          p.group_done[u + k] = 0;
-          atom_add_acq_rel_u32(p.unit_done + u, 1u);
+          atom_add_acq_rel_u32(S.unit_done + u, 1u);
         }
       }
       // the next piece
@@ -1467,7 +1604,7 @@ struct Step {
       long_run(S, u, &c0, &c1);
       const uint32_t target = (uint32_t)long_entries(c0, c1);
       const long long t0 = clock64();
-      while (ld_acquire_u32(p.unit_done + u) < target) {
+      while (ld_acquire_u32(S.unit_done + u) < target) {
         if (*S.abort) break;
         if (clock64() - t0 > (1LL << 31)) {
           set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
@@ -1510,7 +1647,7 @@ struct Step {
     __shared__ uint32_t s_flag;
     __shared__ int64_t s_T;
     __shared__ long long s_scan[kWarps];
-    __shared__ int s_dec[kOwnMax * G];
+    __shared__ int s_dec[kOwnMax];
     const int U = n_units(p), tid = threadIdx.x, w = warp_id();
     Smem S;
     S.stage = smem;
@@ -1526,6 +1663,7 @@ struct Step {
     S.flag = &s_flag;
     S.dec = s_dec;
     S.rope = p.B <= kRopeTab && p.rope_mode != MAC_ROPE_NONE ? reinterpret_cast<float2 *>(smem + off_rope(U)) : nullptr;
+    S.qslot = p.qslot ? smem + off_slot(U, p.B) : nullptr;
     const bool decode = p.mode == MODE_DECODE;
     if (p.trace && tid == 0) p.trace[(size_t)blockIdx.x * kTracePoints + 16] = (unsigned long long)clock64();
     stamp(p, 0);
@@ -1533,7 +1671,7 @@ struct Step {
     if (tid == 0) {
       s_abort = 0;
       // decode launches alternate between the two buffers of minima
-      s_par = decode ? (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u) : 0;
+      s_par = (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u);
     }
     mbar_fence_init();
     if (S.rope) {
@@ -1556,6 +1694,10 @@ struct Step {
     block_sync();
     S.best = p.best + (size_t)s_par * p.B * p.Hq;
     S.best_next = p.best + (size_t)(s_par ^ 1) * p.B * p.Hq;
+    S.unit_done = p.unit_done + (size_t)s_par * U;
+    S.unit_done_next = p.unit_done + (size_t)(s_par ^ 1) * U;
+    S.group_done = p.group_done + (size_t)s_par * (U + kGroups);
+    S.group_done_next = p.group_done + (size_t)(s_par ^ 1) * (U + kGroups);
     Ring R;
     R.buf = smem + (size_t)w * kStages * kStageBytes;
     R.bar0 = smem_addr(&S.full[w * kStages]);
@@ -1566,54 +1708,58 @@ struct Step {
     stamp(p, 1);
     grid_barrier(p, S);  // the minima of every head are final, the window tiles written
     stamp(p, 2);
-    if (decode) {
-      // nobody reads the other buffer in this launch: clear it for the next
+    {
+      // nobody reads the other buffers in this launch: clear them for the next
+      const int i0 = blockIdx.x * kThreads + tid, di = gridDim.x * kThreads;
 #pragma unroll 1
-      for (int i = blockIdx.x * kThreads + tid; i < p.B * p.Hq; i += gridDim.x * kThreads) S.best_next[i] = 0ull;
+      for (int i = i0; i < p.B * p.Hq; i += di) S.best_next[i] = 0ull;
+#pragma unroll 1
+      for (int i = i0; i < U; i += di) S.unit_done_next[i] = 0u;
+#pragma unroll 1
+      for (int i = i0; i < U + kGroups; i += di) S.group_done_next[i] = 0u;
     }
     layout_long(p, S);
     stamp(p, 3);
-    int u0, u_end, step;
-    own_range(U, &u0, &u_end, &step);
+    const int NH = p.B * p.Hq;
+    int h0, h_end, hstep;
+    own_range(NH, &h0, &h_end, &hstep);
     if (!*S.abort)
 #pragma unroll 1
-      for (int u = u0; u < u_end; u += step) {
-        const int k = (u - u0) / step;
-        merge_unit(p, S, R, u, false, k < kOwnMax ? S.dec + k * G : nullptr);
+      for (int bh = h0; bh < h_end; bh += hstep) {
+        const int k = (bh - h0) / hstep;
+        merge_one(p, S, R, bh, false, k < kOwnMax ? S.dec[k] : -2);
       }
     stamp(p, 4);
     if (!*S.abort) long_bands(p, S, R);
     stamp(p, 5);
 #pragma unroll 1
-    for (int u = u0; u < u_end; u += step) {
+    for (int bh = h0; bh < h_end; bh += hstep) {
+      const int k = (bh - h0) / hstep;
+      const int pos = k < kOwnMax ? S.dec[k] : decision(p, S, bh);
+      const int u = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / G;
       int c0, c1;
       long_run(S, u, &c0, &c1);
-      if (c1 < c0 || *S.abort) continue;
+      if (c1 < c0 || pos >= 1 || *S.abort) continue;
       wait_long(p, S, u);
       if (*S.abort) continue;
-      const int k = (u - u0) / step;
-      merge_unit(p, S, R, u, true, k < kOwnMax ? S.dec + k * G : nullptr);
-      if (tid == 0) p.unit_done[u] = 0;
+      merge_one(p, S, R, bh, true, pos);
     }
     stamp(p, 6);
     drain(R);
     block_sync();
     if (tid == 0) {
-      // the last CTA to finish advances the decode launch count; after a
-      // failed launch it also clears the counts the merges may have left
+      // the last CTA to finish advances the launch count (which selects the
+      // buffers of minima and counts the next launch uses)
       __threadfence();
       const uint32_t old = atomicAdd(p.ctl + 4, 1u);
       if (old == gridDim.x - 1) {
         p.ctl[4] = 0;
-        if (decode) atomicAdd(p.ctl + 6, 1u);
-        if (*(volatile uint32_t *)p.ctl != 0) {
-#pragma unroll 1
-          for (int u = 0; u < U; ++u) p.unit_done[u] = 0;
-#pragma unroll 1
-          for (int i = 0; i < U + kGroups; ++i) p.group_done[i] = 0;
-        }
+        atomicAdd(p.ctl + 6, 1u);
       }
-      if (p.trace) p.trace[(size_t)blockIdx.x * kTracePoints + 17] = (unsigned long long)clock64();
+      if (p.trace) {
+        p.trace[(size_t)blockIdx.x * kTracePoints + 17] = (unsigned long long)clock64();
+        p.trace[(size_t)blockIdx.x * kTracePoints + 7] = globaltimer();
+      }
     }
   }
 };

@@ -7,15 +7,21 @@
 
 namespace mac {
 
+// per device: the dynamic shared memory limit set on the kernel (0: not yet)
+template <typename T, int G, bool PAGED>
+static size_t &step_smem_limit(int dev) {
+  static size_t limit[64] = {0};
+  return limit[dev];
+}
+
 template <typename T, int G, bool PAGED>
 static cudaError_t prepare_step(int U, int B, size_t *smem) {
   using S = Step<T, G, PAGED>;
   *smem = S::smem_bytes(U, B);
-  static size_t limit[64] = {0};  // per device: dynamic shared memory limit set on the kernel
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && limit[dev] == 0) {
+  if (dev < 64 && step_smem_limit<T, G, PAGED>(dev) == 0) {
     // the opt-in maximum per block, less the kernel's static shared memory
     int optin = 0;
     cudaFuncAttributes fa;
@@ -26,19 +32,27 @@ static cudaError_t prepare_step(int U, int B, size_t *smem) {
     if (dyn > kMaxSmem) dyn = kMaxSmem;
     e = cudaFuncSetAttribute(step_kernel<T, G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
     if (e != cudaSuccess) return e;
-    limit[dev] = dyn;
+    step_smem_limit<T, G, PAGED>(dev) = dyn;
   }
-  if (dev < 64 && *smem > limit[dev]) return cudaErrorInvalidValue;
+  if (dev < 64 && *smem > step_smem_limit<T, G, PAGED>(dev)) return cudaErrorInvalidValue;
   return cudaSuccess;
 }
 
 // Cooperative launch: the grid (one CTA per SM) is guaranteed co-resident,
 // which the grid barrier and the long-band counts of the step rely on.
 template <typename T, int G, bool PAGED>
-static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) {
+static cudaError_t launch_step_g(const StepParams &p_in, int grid, cudaStream_t s) {
+  using S = Step<T, G, PAGED>;
   size_t smem = 0;
-  cudaError_t e = prepare_step<T, G, PAGED>(p.B * p.Hkv, p.B, &smem);
+  cudaError_t e = prepare_step<T, G, PAGED>(p_in.B * p_in.Hkv, p_in.B, &smem);
   if (e != cudaSuccess) return e;
+  // the warps' query slots, where shared memory allows them
+  StepParams p = p_in;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t with_slots = smem + (size_t)kWarps * S::kSlot;
+  p.qslot = dev < 64 && with_slots <= step_smem_limit<T, G, PAGED>(dev) ? S::kSlot : 0;
+  if (p.qslot) smem = with_slots;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
