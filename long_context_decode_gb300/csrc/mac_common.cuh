@@ -124,7 +124,7 @@ struct StepParams {
   const void *q;             // query of (b, h) at element (b*Hq + h) * q_stride + q_offset
   int64_t q_stride, q_offset;
   TileCounts tc;             // window tiles per unit (the scratch is sized for these)
-  int qslot;                 // bytes of each warp's query slot in shared memory (0: none, load from global)
+  int qslot;                 // the warps' query entries fit in shared memory (0: queries read from global memory)
   // decode only
   const int32_t *ring_pos;   // [B][K]
   const void *ring_q;        // [B][Hq][K][d]

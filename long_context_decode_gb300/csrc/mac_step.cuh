@@ -158,8 +158,8 @@ struct Step {
   // dynamic shared memory layout
   static constexpr size_t kOffBar = (size_t)kWarps * kStages * kStageBytes;
   static constexpr size_t kOffMask = kOffBar + 8 * kWarps * kStages;      // int [kWarps][kStages]
-  static constexpr size_t kOffBd = kOffMask + 4 * kWarps * kStages;       // f32 [G][kPartStride]
-  static constexpr size_t kOffUnits = kOffBd + 4 * (size_t)G * kPartStride;
+  static constexpr size_t kOffBd = kOffMask + 4 * kWarps * kStages;       // f32 [kWarps][kPartStride]
+  static constexpr size_t kOffUnits = kOffBd + 4 * (size_t)kWarps * kPartStride;
   static_assert(kOffBar % 8 == 0 && kOffBd % 16 == 0 && kOffUnits % 16 == 0, "alignment");
   // + the long-band offsets (int64 [U + 1]) and unit lengths (int32 [U]),
   // then, for at most kRopeTab requests, the cos and sin of every request's
@@ -168,19 +168,26 @@ struct Step {
   __host__ __device__ static size_t off_rope(int U) {
     return (kOffUnits + 8 * (size_t)(U + 1) + 4 * (size_t)U + 15) / 16 * 16;
   }
-  __host__ __device__ static size_t off_slot(int U, int B) {
+  // + each stage's ring positions (a match stage's rows: int32 [kStRows]),
+  // then (when there is room) each warp's two query entries: a unit's G
+  // query rows or a head's, copied with the first stage of an item whose
+  // query differs from the item before
+  static constexpr int kPosBytes = kStRows * 4;
+  static constexpr int kQE = G * kRow;
+  static constexpr int kQBuf = kWarps * 2 * kQE;
+  __host__ __device__ static size_t off_pside(int U, int B) {
     return off_rope(U) + (B <= kRopeTab ? 8 * (size_t)B * (kHeadDim / 2) : 0);
   }
-  __host__ __device__ static size_t smem_bytes(int U, int B) { return off_slot(U, B); }
-  // bytes of a warp's slot: a window tile's G query rows, or a match item's
-  // query row and ring positions
-  static constexpr int kSlot = (G * kRow > kRow + kIR * 4 ? G * kRow : kRow + kIR * 4);
+  __host__ __device__ static size_t off_qbuf(int U, int B) {
+    return off_pside(U, B) + (size_t)kWarps * kStages * kPosBytes;
+  }
+  __host__ __device__ static size_t smem_bytes(int U, int B) { return off_qbuf(U, B); }
 
   struct Smem {
     uint8_t *stage;     // [kWarps][kStages][kStageBytes]
     uint64_t *full;     // [kWarps][kStages]: the stage's copy has landed
     int *rows;          // [kWarps][kStages]: rows of the stage that were copied (bit mask)
-    float *bd;          // [G][kPartStride]: boundary pieces of the unit being merged
+    float *bd;          // [kWarps][kPartStride]: boundary pieces of a batch of owned heads
     int64_t *off;       // [U + 1]: long-band offsets (units end to end)
     int32_t *um;        // [U]: the unit's length m (0: not a valid length)
     long long *scan;    // [kWarps]
@@ -193,7 +200,8 @@ struct Step {
     uint32_t *unit_done, *group_done;            // this launch's long-band counts
     uint32_t *unit_done_next, *group_done_next;  // cleared here for the next launch
     float2 *rope;       // [B][d/2] cos, sin of the query angles (B <= kRopeTab), or null
-    uint8_t *qslot;     // [kWarps][p.qslot]: each warp's copy of its next item's query rows, or null
+    uint8_t *pside;     // [kWarps][kStages][kPosBytes]: ring positions of match stages
+    uint8_t *qbuf;      // [kWarps][2][kQE]: query entries, or null (queries read from global memory)
   };
 
   // One warp's ring: stage uses are numbered; use n sits in stage n % kStages.
@@ -201,13 +209,18 @@ struct Step {
     uint8_t *buf;       // this warp's kStages stages
     uint32_t bar0;      // shared address of its first full barrier
     int *rows;
+    uint8_t *pside;     // this warp's stage position buffers
+    uint8_t *qbuf;      // this warp's two query entries (or null)
     uint32_t issued, used;
   };
 
   // What one stage use holds: K/V rows [a, a + cnt) of unit u (kind 1), or
   // ring rows [a, a + cnt) of head u (kind 2); kind 0: nothing; -1: the end.
   struct Desc {
-    int kind, u, a, cnt;
+    int kind = -1, u = 0, a = 0, cnt = 0;
+    int qe = -1;   // >= 0: also copy the item's query (unit u's G rows; head u's for kind 2) into entry qe
+    int pc = 0;    // a match stage whose ring positions come into its position buffer
+    int keep = 0;  // K/V rows kept in L2 (read again by a boundary piece)
   };
 
   __device__ static int lane_id() { return threadIdx.x & 31; }
@@ -264,6 +277,27 @@ struct Step {
     if (s1 != s0 && s1 < p.kv.max_pages) id[1] = __ldg(row + s1);
   }
 
+  // The query copy that rides with a stage: bytes, and its issue.
+  __device__ static uint32_t query_bytes(const Desc &d, const Ring &R) {
+    return d.qe >= 0 && R.qbuf ? (d.kind == 2 ? (uint32_t)kRow : (uint32_t)kQE) : 0u;
+  }
+  __device__ static void issue_query(const StepParams &p, const Ring &R, const Desc &d, uint32_t bar) {
+    uint8_t *dst = R.qbuf + (size_t)d.qe * kQE;
+    const uint8_t *q = (const uint8_t *)p.q;
+    if (d.kind == 2) {
+      bulk_g2s(smem_addr(dst), q + ((int64_t)d.u * p.q_stride + p.q_offset) * kES, kRow, bar);
+      return;
+    }
+    const int b = d.u / p.Hkv, g = d.u - b * p.Hkv;
+    const int64_t bh0 = (int64_t)b * p.Hq + g * G;
+    if (p.q_stride == kHeadDim && p.q_offset == 0) {  // the unit's G rows are contiguous
+      bulk_g2s(smem_addr(dst), q + bh0 * kRow, kQE, bar);
+    } else {
+      for (int hh = 0; hh < G; ++hh)
+        bulk_g2s(smem_addr(dst + hh * kRow), q + ((bh0 + hh) * p.q_stride + p.q_offset) * kES, kRow, bar);
+    }
+  }
+
   // Lane 0: the copies of the next stage use (every lane calls it).
   __device__ static void issue(const StepParams &p, Ring &R, const Desc &d, const int32_t (&id)[2]) {
     const uint32_t n = R.issued++;
@@ -271,57 +305,65 @@ struct Step {
     uint8_t *buf = stage_buf(R, n);
     const uint32_t bar = stage_bar(R, n);
     int *rows = R.rows + n % kStages;
-    if (d.kind == 2) {  // ring rows of head d.u
+    const uint32_t qb = query_bytes(d, R);
+    if (d.kind == 2) {  // ring rows of head d.u (and their positions)
       const uint32_t bytes = (uint32_t)d.cnt * kRow;
       *rows = (1 << d.cnt) - 1;
-      mbar_expect_tx(bar, bytes);
+      mbar_expect_tx(bar, bytes + qb + (d.pc ? 4u * d.cnt : 0u));
+      if (qb) issue_query(p, R, d, bar);
+      if (d.pc)
+        bulk_g2s(smem_addr(R.pside + (size_t)(n % kStages) * kPosBytes),
+                 p.ring_pos + (int64_t)(d.u / p.Hq) * p.K + d.a, 4u * d.cnt, bar);
       bulk_g2s_hint(smem_addr(buf), (const uint8_t *)p.ring_q + ((size_t)d.u * p.K + d.a) * kRow, bytes, bar,
                     l2_evict_first_policy());
       return;
     }
-    if (d.kind != 1 || d.cnt <= 0) {
-      *rows = 0;
-      mbar_arrive(bar);
-      return;
-    }
     const int g = d.u % p.Hkv;
-    if (!PAGED) {
-      if (d.a < 1 || d.a + d.cnt - 1 > p.kv.capacity || d.u >= p.B * p.Hkv) {
-        set_status(p.ctl, MAC_DEV_BAD_COPY);
-        *rows = 0;
-        mbar_arrive(bar);
-        return;
-      }
-      const size_t off = ((size_t)d.u * (size_t)p.kv.capacity + (size_t)(d.a - 1)) * kRow;
-      const uint32_t bytes = (uint32_t)d.cnt * kRow;
-      *rows = (1 << d.cnt) - 1;
-      mbar_expect_tx(bar, 2 * bytes);
-      const unsigned long long pol = l2_evict_first_policy();
-      bulk_g2s_hint(smem_addr(buf), (const uint8_t *)p.kv.k + off, bytes, bar, pol);
-      bulk_g2s_hint(smem_addr(buf + kStageBytes / 2), (const uint8_t *)p.kv.v + off, bytes, bar, pol);
-      return;
-    }
-    // paged: rows of the first page, then of the second
-    const int n0 = min(d.cnt, 16 - ((d.a - 1) & 15));
     int msk = 0;
     uint32_t bytes = 0;
+    bool ok = d.kind == 1 && d.cnt > 0;
+    if (ok && !PAGED && (d.a < 1 || d.a + d.cnt - 1 > p.kv.capacity || d.u >= p.B * p.Hkv)) {
+      set_status(p.ctl, MAC_DEV_BAD_COPY);
+      ok = false;
+    }
+    const int n0 = ok ? min(d.cnt, 16 - ((d.a - 1) & 15)) : 0;  // rows of the first page (paged)
+    if (ok && !PAGED) {
+      msk = (1 << d.cnt) - 1;
+      bytes = 2u * (uint32_t)d.cnt * kRow;
+    } else if (ok) {
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int cnt = s ? d.cnt - n0 : n0;
-      if (cnt <= 0 || id[s] == kNoPage) continue;
-      if (id[s] < 0 || id[s] >= p.kv.n_pages) {
-        set_status(p.ctl, MAC_DEV_BAD_PAGE);
-        continue;
+      for (int s = 0; s < 2; ++s) {
+        const int cnt = s ? d.cnt - n0 : n0;
+        if (cnt <= 0 || id[s] == kNoPage) continue;
+        if (id[s] < 0 || id[s] >= p.kv.n_pages) {
+          set_status(p.ctl, MAC_DEV_BAD_PAGE);
+          continue;
+        }
+        msk |= s ? ((1 << d.cnt) - 1) & ~((1 << n0) - 1) : (1 << n0) - 1;
+        bytes += 2u * (uint32_t)cnt * kRow;
       }
-      msk |= s ? ((1 << d.cnt) - 1) & ~((1 << n0) - 1) : (1 << n0) - 1;
-      bytes += 2u * (uint32_t)cnt * kRow;
     }
     *rows = msk;
-    if (bytes == 0) {
+    if (bytes + qb == 0) {
       mbar_arrive(bar);
       return;
     }
-    mbar_expect_tx(bar, bytes);
+    mbar_expect_tx(bar, bytes + qb);
+    if (qb) issue_query(p, R, d, bar);
+    if (bytes == 0) return;
+    if (!PAGED) {
+      const size_t off = ((size_t)d.u * (size_t)p.kv.capacity + (size_t)(d.a - 1)) * kRow;
+      const uint32_t nb = (uint32_t)d.cnt * kRow;
+      if (d.keep) {
+        bulk_g2s(smem_addr(buf), (const uint8_t *)p.kv.k + off, nb, bar);
+        bulk_g2s(smem_addr(buf + kStageBytes / 2), (const uint8_t *)p.kv.v + off, nb, bar);
+      } else {
+        const unsigned long long pol = l2_evict_first_policy();
+        bulk_g2s_hint(smem_addr(buf), (const uint8_t *)p.kv.k + off, nb, bar, pol);
+        bulk_g2s_hint(smem_addr(buf + kStageBytes / 2), (const uint8_t *)p.kv.v + off, nb, bar, pol);
+      }
+      return;
+    }
     const unsigned long long pol = l2_evict_first_policy();
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
@@ -491,7 +533,7 @@ struct Step {
 
   // The warp's state -> one partial summary per head at dst ([G][kPartStride]):
   // the two half-warps brought to a common maximum and summed.  only >= 0:
-  // write that head's slot alone.
+  // that head's partial alone, at dst.
   __device__ static void att_finish(Att &A, float *dst, int only = -1) {
     const int lane = lane_id(), sub = lane & 15, hw = lane >> 4;
     const int idx = sub >> kAPlain, hm = idx % G;
@@ -518,90 +560,72 @@ struct Step {
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
         if (only >= 0 && hh != only) continue;
-        float *o = dst + hh * kPartStride + sub * 8;
+        float *o = dst + (only >= 0 ? 0 : hh * kPartStride) + sub * 8;
         *reinterpret_cast<float4 *>(o) = make_float4(A.o[hh][0].x, A.o[hh][0].y, A.o[hh][1].x, A.o[hh][1].y);
         *reinterpret_cast<float4 *>(o + 4) = make_float4(A.o[hh][2].x, A.o[hh][2].y, A.o[hh][3].x, A.o[hh][3].y);
       }
       if ((sub & ((1 << kAPlain) - 1)) == 0 && idx < G && (only < 0 || hm == only))  // one lane per head
-        *reinterpret_cast<float2 *>(dst + hm * kPartStride + kHeadDim) = make_float2(Mm, L);
+        *reinterpret_cast<float2 *>(dst + (only >= 0 ? 0 : hm * kPartStride) + kHeadDim) = make_float2(Mm, L);
     }
   }
 
   // R(pos) q~ * log2(e)/sqrt(d) of the G heads of unit u, the lane's dims
   // [8 sub, 8 sub + 8) (explicit roundings keep the result identical
   // wherever it is computed).
-  // The unit's query rows: from global memory, or (slot) from a warp's
-  // shared-memory copy holding the G rows back to back.
+  // R(pos) q~ * log2(e)/sqrt(d) of the G heads of unit u, the lane's dims
+  // [8 sub, 8 sub + 8), from the query rows in global memory or (qe) in a
+  // warp's query entry holding the G rows back to back.  Every pair (a, b)
+  // of a 2x2 rotation becomes a' = a cos - b sin, b' = b cos + a sin; a lane
+  // computes its own dims x from its partner dims y with signed sines (the
+  // explicit roundings keep the result identical wherever it is computed).
   __device__ static void load_query(const StepParams &p, const Smem &S, int u, float2 (&q)[G][kAPairs],
-                                    const uint8_t *slot = nullptr) {
+                                    const uint8_t *qe = nullptr) {
     const int lane = lane_id(), sub = lane & 15;
     const int b = u / p.Hkv, g = u - b * p.Hkv;
-    const int64_t pos = qpos(p, b);
     const bool half = p.rope_mode == MAC_ROPE_HALF, none = p.rope_mode == MAC_ROPE_NONE;
     const int d0 = sub * 8, dp = (d0 + kHeadDim / 2) & (kHeadDim - 1);  // own dims, partner dims (half mode)
-    float2 cs[8];
+    float c[8], sn[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) cs[i] = make_float2(1.f, 0.f);
-    if (!none) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = half ? (d0 + i) & (kHeadDim / 2 - 1) : (d0 + i) >> 1;
-        if (S.rope) cs[i] = S.rope[b * (kHeadDim / 2) + j];
-        else if (half || (i & 1) == 0) rope_angle(pos, p.rope_f[j], &cs[i].x, &cs[i].y);
-        else cs[i] = cs[i - 1];
+    for (int i = 0; i < 8; ++i) {
+      // half: pair (j, j + d/2), own dims below d/2 are a; interleaved: pair (2j, 2j + 1)
+      const int j = half ? (d0 + i) & (kHeadDim / 2 - 1) : (d0 + i) >> 1;
+      float2 cs = make_float2(1.f, 0.f);
+      if (!none) {
+        if (S.rope) cs = S.rope[b * (kHeadDim / 2) + j];
+        else rope_angle(qpos(p, b), p.rope_f[j], &cs.x, &cs.y);
       }
+      const bool is_a = half ? d0 < kHeadDim / 2 : (i & 1) == 0;
+      c[i] = cs.x;
+      sn[i] = is_a ? -cs.y : cs.y;
     }
     bool bad = false;
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
       const int64_t e0 = ((int64_t)b * p.Hq + g * G + hh) * p.q_stride + p.q_offset;
-      const T *row = slot ? reinterpret_cast<const T *>(slot + hh * kRow) : reinterpret_cast<const T *>(p.q) + e0;
-      auto ld = [&](const T *ptr, int c) -> uint4 {
-        return slot ? reinterpret_cast<const uint4 *>(ptr)[c] : __ldg(reinterpret_cast<const uint4 *>(ptr) + c);
-      };
+      const T *row = qe ? reinterpret_cast<const T *>(qe + hh * kRow) : reinterpret_cast<const T *>(p.q) + e0;
       float x[8], y[8];
 #pragma unroll
-      for (int c = 0; c < kALoads; ++c) {
-        float2 f[kAPairs / kALoads];
-        unpack16x2<T>(ld(row + d0, c), f);
+      for (int k = 0; k < kALoads; ++k) {
+        float2 f[kAPairs / kALoads], h[kAPairs / kALoads];
+        const uint4 *o4 = reinterpret_cast<const uint4 *>(row + d0) + k;
+        const uint4 *p4 = reinterpret_cast<const uint4 *>(row + dp) + k;
+        unpack16x2<T>(qe ? *o4 : __ldg(o4), f);
+        unpack16x2<T>(half ? (qe ? *p4 : __ldg(p4)) : make_uint4(0, 0, 0, 0), h);
 #pragma unroll
         for (int i = 0; i < kAPairs / kALoads; ++i) {
-          x[c * 8 / kALoads + 2 * i] = f[i].x;
-          x[c * 8 / kALoads + 2 * i + 1] = f[i].y;
-        }
-        if (half) {
-          unpack16x2<T>(ld(row + dp, c), f);
-#pragma unroll
-          for (int i = 0; i < kAPairs / kALoads; ++i) {
-            y[c * 8 / kALoads + 2 * i] = f[i].x;
-            y[c * 8 / kALoads + 2 * i + 1] = f[i].y;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < kAPairs / kALoads; ++i) {
-            y[c * 8 / kALoads + 2 * i] = 0.f;
-            y[c * 8 / kALoads + 2 * i + 1] = 0.f;
-          }
+          x[k * 8 / kALoads + 2 * i] = f[i].x;
+          x[k * 8 / kALoads + 2 * i + 1] = f[i].y;
+          y[k * 8 / kALoads + 2 * i] = h[i].x;
+          y[k * 8 / kALoads + 2 * i + 1] = h[i].y;
         }
       }
       float r[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         bad |= !isfinite(x[i]);
-        if (none) {
-          r[i] = __fmul_rn(x[i], p.q_scale);
-        } else if (half) {
-          // pair (j, j + d/2): the lower dim is a, the upper b
-          const bool lower = d0 < kHeadDim / 2;
-          const float a = lower ? x[i] : y[i], bb = lower ? y[i] : x[i];
-          r[i] = lower ? __fmul_rn(__fsub_rn(__fmul_rn(a, cs[i].x), __fmul_rn(bb, cs[i].y)), p.q_scale)
-                       : __fmul_rn(__fadd_rn(__fmul_rn(bb, cs[i].x), __fmul_rn(a, cs[i].y)), p.q_scale);
-        } else {
-          // pair (2j, 2j + 1) within the lane's dims
-          const float a = x[i & ~1], bb = x[i | 1];
-          r[i] = (i & 1) == 0 ? __fmul_rn(__fsub_rn(__fmul_rn(a, cs[i].x), __fmul_rn(bb, cs[i].y)), p.q_scale)
-                              : __fmul_rn(__fadd_rn(__fmul_rn(bb, cs[i].x), __fmul_rn(a, cs[i].y)), p.q_scale);
-        }
+        const float yy = half ? y[i] : none ? 0.f : x[i ^ 1];
+        r[i] = none ? __fmul_rn(x[i], p.q_scale)
+                    : __fmul_rn(__fadd_rn(__fmul_rn(x[i], c[i]), __fmul_rn(yy, sn[i])), p.q_scale);
       }
 #pragma unroll
       for (int i = 0; i < kAPairs; ++i) q[hh][i] = make_float2(r[2 * i], r[2 * i + 1]);
@@ -681,20 +705,28 @@ struct Step {
   __device__ static int64_t n_items(const StepParams &p) {
     return n_window_items(p) + (p.mode == MODE_DECODE ? (int64_t)p.B * p.Hq * match_cph(p) : 0);
   }
-  // One phase-A item: a window tile (kind 1: unit u, tokens [lo, hi]) or a
-  // match item (kind 2: head u, ring rows [lo, hi)); kind -1: past the end.
+  // One streamed item: a window tile (kind 1: unit u, tokens [lo, hi], all
+  // heads), a match item (kind 2: head u, ring rows [lo, hi)), or a boundary
+  // piece (kind 3: unit u, tokens [lo, hi] for head hm alone, into the
+  // warp's slot of S.bd); kind -1: none.
   struct Item {
     int64_t i;
-    int kind, u, lo, hi;
+    int kind, u, lo, hi, hm;
   };
-  __device__ static Item item_at(const StepParams &p, const Smem &S, int64_t i) {
+  __device__ static Item no_item() {
     Item it;
-    it.i = i;
+    it.i = 0;
     it.kind = -1;
-    it.u = it.lo = 0;
+    it.u = it.lo = it.hm = 0;
     it.hi = -1;
+    return it;
+  }
+  // phase-A item i: the window tiles of every unit, then the match items
+  __device__ static Item item_a(const StepParams &p, const Smem &S, int64_t i) {
+    Item it = no_item();
+    it.i = i;
     const int64_t nw = n_window_items(p);
-    if (i >= n_items(p)) return it;
+    if (i < 0 || i >= n_items(p)) return it;
     if (i < nw) {
       const int u = (int)((uint32_t)i / (uint32_t)p.tc.nt), t = (int)i - u * p.tc.nt;
       it.kind = 1;
@@ -710,201 +742,184 @@ struct Step {
     }
     return it;
   }
+  // The boundary piece of owned head k (none when the head misses or its
+  // band starts on a tile boundary): the band [lo, m - r] of a hit at p
+  // starts at lo = p - r + 1 inside band tile j; the piece is [lo, end of
+  // tile j] for that head alone.  *nbt: the band tiles the head takes whole.
+  __device__ static Item boundary_item(const StepParams &p, const Smem &S, int bh, int pos, int *nbt) {
+    Item it = no_item();
+    const int b = bh / p.Hq, h = bh - b * p.Hq, g = h / G, u = b * p.Hkv + g;
+    const int m = S.um[u];
+    *nbt = p.tc.nbw;
+    if (pos < 1 || m <= 0) return it;
+    const int lo = max(lb(p), pos - p.r + 1);
+    if (lo > m - p.r) {
+      *nbt = 0;
+      return it;
+    }
+    const int j = (m - p.r - lo) / kTT;
+    int tlo, thi;
+    tile_range(p, m, j, &tlo, &thi);
+    *nbt = lo == tlo ? j + 1 : j;
+    if (lo == tlo) return it;
+    it.kind = 3;
+    it.u = u;
+    it.lo = lo;
+    it.hi = thi;
+    it.hm = h - g * G;
+    return it;
+  }
   // stage s of an item
-  __device__ static Desc stage_desc(const Item &it, int s) {
+  __device__ static Desc stage_desc(const StepParams &p, const Item &it, int s) {
     Desc d;
-    d.kind = it.kind;
+    d.kind = it.kind == 2 ? 2 : 1;
     d.u = it.u;
-    if (it.kind == 1) {
+    if (it.kind != 2) {
       d.a = it.lo + s * kStTok;
       d.cnt = min(it.hi - d.a + 1, kStTok);
+      d.keep = it.kind == 1;
     } else {
       d.a = it.lo + s * kStRows;
       d.cnt = min(it.hi - d.a, kStRows);
       if (d.cnt <= 0) d.kind = 0;
+      d.pc = d.kind == 2 && (p.K & 3) == 0 && (d.cnt & 3) == 0;
     }
     return d;
   }
-  // Ask L1 for what the item's first stage will need besides the stage:
-  // the query rows (and, for a match item, the ring positions).
-  __device__ static void prefetch_item(const StepParams &p, const Item &it) {
-    constexpr int kLines = kRow / 128;  // 128-byte lines per row
-    const int lane = lane_id();
-    const uint8_t *q = (const uint8_t *)p.q;
-    const uint8_t *ptr = nullptr;
-    if (it.kind == 1) {
-      const int b = it.u / p.Hkv, g = it.u - b * p.Hkv;
-      if (lane < G * kLines && it.lo <= it.hi) {
-        const int hh = lane / kLines;
-        ptr = q + (((int64_t)b * p.Hq + g * G + hh) * p.q_stride + p.q_offset) * kES + (lane % kLines) * 128;
-      }
-    } else if (it.kind == 2) {
-      if (lane < kLines)
-        ptr = q + ((int64_t)it.u * p.q_stride + p.q_offset) * kES + lane * 128;
-      else if (lane < kLines + 2 && (lane - kLines) * 128 < (it.hi - it.lo) * 4)
-        ptr = (const uint8_t *)(p.ring_pos + (int64_t)(it.u / p.Hq) * p.K + it.lo) + (lane - kLines) * 128;
-    }
-    if (ptr) asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr));
-  }
+  // the query an item needs: its unit (window, boundary) or head (match)
+  __device__ static int query_key(const Item &it) { return it.kind == 2 ? -1 - it.u : it.u; }
 
-  __device__ static void cp_async16(uint8_t *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-  }
-  // Ring positions come with a match item's slot when their chunks are whole 16-byte pieces.
-  __device__ static bool pos_in_slot(const StepParams &p, const Item &it) {
-    return (p.K & 3) == 0 && ((it.hi - it.lo) & 3) == 0;
-  }
-  // Asynchronous copy, into the warp's slot, of what item `it` needs at its
-  // start: the unit's G query rows (a window tile), or the head's query row
-  // and the item's ring positions (a match item).
-  __device__ static void fill_slot(const StepParams &p, const Item &it, uint8_t *slot) {
-    constexpr int kRC = kRow / 16;  // 16-byte chunks per row
-    const int lane = lane_id();
-    const uint8_t *q = (const uint8_t *)p.q;
-    if (it.kind == 1 && it.lo <= it.hi) {
-      const int b = it.u / p.Hkv, g = it.u - b * p.Hkv;
-#pragma unroll 1
-      for (int c = lane; c < G * kRC; c += 32) {
-        const int hh = c / kRC, k = c - hh * kRC;
-        cp_async16(slot + c * 16, q + (((int64_t)b * p.Hq + g * G + hh) * p.q_stride + p.q_offset) * kES + k * 16);
-      }
-    } else if (it.kind == 2) {
-      const uint8_t *row = q + ((int64_t)it.u * p.q_stride + p.q_offset) * kES;
-      if (lane < kRC) cp_async16(slot + lane * 16, row + lane * 16);
-      if (pos_in_slot(p, it)) {
-        const int32_t *pos = p.ring_pos + (int64_t)(it.u / p.Hq) * p.K + it.lo;
-        for (int c = lane; c < (it.hi - it.lo) / 4; c += 32) cp_async16(slot + kRow + c * 16, pos + 4 * c);
-      }
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  }
-
-  __device__ static void phase_a(const StepParams &p, const Smem &S, Ring &R) {
+  // The streaming loop of one round, one copy of the per-stage code for all
+  // rounds: round 0 streams this warp's contiguous share of the phase-A
+  // items; round r >= 1 the boundary piece of owned head (r-1) kWarps + w.
+  // One iteration per stage; the copies run up to kStages stages ahead.
+  // Consecutive items of a warp mostly share their query; an item whose
+  // query differs from the one before brings it along with its first stage
+  // (into the warp's next query entry), so the loop waits on nothing but its
+  // stages.  Without query entries (no room in shared memory) the query is
+  // read from global memory.
+  __device__ static void stream(const StepParams &p, const Smem &S, Ring &R, int rnd, int h0, int hstep, int nown) {
     const int lane = lane_id(), w = warp_id(), P = gridDim.x, NW = P * kWarps;
     const int gw = w * P + blockIdx.x;
-    unsigned long long *tr = p.trace && w == 0 && lane == 0 ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
-    unsigned long long t_wait = 0, t_item = 0, t_proc = 0, t_end = 0, tc0 = 0;
+    int64_t i_beg = 0, i_end = 0;
+    if (rnd == 0) {
+      const int64_t na = n_items(p);
+      i_beg = (int64_t)(((unsigned long long)gw * (unsigned long long)na) / (unsigned)NW);
+      i_end = (int64_t)(((unsigned long long)(gw + 1) * (unsigned long long)na) / (unsigned)NW);
+    } else {
+      const int k = (rnd - 1) * kWarps + w;
+      i_end = k < nown ? 1 : 0;
+    }
+    auto get = [&](int64_t i) -> Item {
+      if (i >= i_end) return no_item();
+      if (rnd == 0) return item_a(p, S, i);
+      const int k = (rnd - 1) * kWarps + w, bh = h0 + k * hstep;
+      int nbt;
+      Item it = boundary_item(p, S, bh, k < kOwnMax ? S.dec[k] : decision(p, S, bh), &nbt);
+      it.i = i;
+      return it;
+    };
     int32_t id[2];
-    // the fetch side runs up to kStages stages ahead of the consumer
-    Item fi = item_at(p, S, gw);
-    int fs = 0;
-    auto fetch_next = [&](Desc &d) -> bool {
-      if (fi.kind < 0) return false;
-      if (fs == 0) prefetch_item(p, fi);
-      d = stage_desc(fi, fs);
+    // fetch side: the next stage to copy; it attaches the query of each
+    // item whose query differs from the last
+    Item fi = get(i_beg);
+    int fs = 0, f_key = 0x7fffffff, f_e = 1;
+    Desc nx;
+    bool have_nx = false;
+    auto fetch_next = [&]() {
+      have_nx = fi.kind >= 0;
+      if (!have_nx) return;
+      nx = stage_desc(p, fi, fs);
+      if (fs == 0 && query_key(fi) != f_key) {
+        f_key = query_key(fi);
+        f_e ^= 1;
+        nx.qe = f_e;
+      }
       if (++fs == kItemStages) {
         fs = 0;
-        fi = item_at(p, S, fi.i + NW);
+        fi = get(fi.i + 1);
       }
-      return true;
-    };
-    uint8_t *slot = S.qslot ? S.qslot + (size_t)w * p.qslot : nullptr;
-    if (slot) fill_slot(p, item_at(p, S, gw), slot);
-    Desc nx;
-    nx.kind = -1;
-    nx.u = nx.a = nx.cnt = 0;
-#pragma unroll 1
-    for (int j = 0; j < kStages; ++j) {
-      if (!fetch_next(nx)) break;
       load_ids(p, nx, id);
-      issue(p, R, nx, id);
-    }
-    bool have_nx = fetch_next(nx);
-    if (have_nx) load_ids(p, nx, id);
+    };
+    fetch_next();
     Att A;
     float2 q[G][kAPairs];
     float2 qlo[4], qhi[4];
-    Item ci = item_at(p, S, gw);
+    float bd = INFINITY;
+    int bp = -1, pos_lo = 1, pos_hi = 0;
+    int c_key = 0x7fffffff, c_e = 1;  // the query in registers, its entry
+    Item ci = get(i_beg);
+    int cs = 0;  // the stage of ci to consume
 #pragma unroll 1
-    while (ci.kind >= 0 && !*S.abort) {
-      if (tr) tc0 = globaltimer();
-      float bd = INFINITY;
-      int bp = -1, pos_lo = 1, pos_hi = 0;
-      int pks[kItemStages];
-#pragma unroll
-      for (int s2 = 0; s2 < kItemStages; ++s2) pks[s2] = 0;
-      if (slot) {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncwarp();
+    for (;;) {
+      // keep kStages copies in flight
+#pragma unroll 1
+      while (have_nx && R.issued - R.used < (uint32_t)kStages) {
+        issue(p, R, nx, id);
+        fetch_next();
       }
-      if (ci.kind == 1) {
-        att_init(A);
-        if (ci.lo <= ci.hi) load_query(p, S, ci.u, q, slot);
-      } else {
-        // the head's query row (both halves of the lane's dims), its window
-        // of candidates and the positions of the rows this lane finishes
-        const int bh = ci.u, b = bh / p.Hq;
-        const T *row = slot ? reinterpret_cast<const T *>(slot)
-                            : reinterpret_cast<const T *>(p.q) + (int64_t)bh * p.q_stride + p.q_offset;
-#pragma unroll
-        for (int c = 0; c < kHalfLoads; ++c) {
-          const uint4 *lo4 = reinterpret_cast<const uint4 *>(row + (lane & 7) * 8) + c;
-          const uint4 *hi4 = reinterpret_cast<const uint4 *>(row + kHeadDim / 2 + (lane & 7) * 8) + c;
-          unpack16x2<T>(slot ? *lo4 : __ldg(lo4), qlo + c * (4 / kHalfLoads));
-          unpack16x2<T>(slot ? *hi4 : __ldg(hi4), qhi + c * (4 / kHalfLoads));
+      if (ci.kind < 0 || *S.abort) break;
+      if (cs == 0) {
+        if (ci.kind == 2) {
+          const int m = S.um[(ci.u / p.Hq) * p.Hkv];
+          pos_lo = m > 0 ? max(1, m - p.K) : 1;
+          pos_hi = m > 0 ? m - 1 : 0;
+          bd = INFINITY;
+          bp = -1;
+        } else {
+          att_init(A);
         }
-        const int m = S.um[b * p.Hkv];
-        pos_lo = m > 0 ? max(1, m - p.K) : 1;
-        pos_hi = m > 0 ? m - 1 : 0;
-        const int cnt = ci.hi - ci.lo, r = match_row(lane);
+      }
+      const Desc d = stage_desc(p, ci, cs);
+      const int r = match_row(lane);
+      int pk = 0;
+      if (d.kind == 2 && !d.pc)  // the position of the row this lane finishes, read directly
+        pk = __ldg(p.ring_pos + (int64_t)(d.u / p.Hq) * p.K + d.a + (r < d.cnt ? r : d.cnt - 1));
+      const uint32_t n = R.used;
+      const bool ok = wait_stage(p, S, R, n);
+      const int key = query_key(ci);
+      if (cs == 0 && key != c_key) {
+        // the item's query came with its first stage (or is read directly)
+        c_e ^= 1;
+        c_key = key;
+        const uint8_t *qe = R.qbuf ? R.qbuf + (size_t)c_e * kQE : nullptr;
+        if (ci.kind != 2) {
+          load_query(p, S, ci.u, q, qe);
+        } else {
+          const T *row = qe ? reinterpret_cast<const T *>(qe)
+                            : reinterpret_cast<const T *>(p.q) + (int64_t)ci.u * p.q_stride + p.q_offset;
 #pragma unroll
-        for (int s2 = 0; s2 < kItemStages; ++s2) {
-          const int k = s2 * kStRows + r;
-          if (k < cnt) {
-            if (slot && pos_in_slot(p, ci))
-              pks[s2] = reinterpret_cast<const int32_t *>(slot + kRow)[k];
-            else
-              pks[s2] = __ldg(p.ring_pos + (int64_t)b * p.K + ci.lo + k);
+          for (int c = 0; c < kHalfLoads; ++c) {
+            const uint4 *lo4 = reinterpret_cast<const uint4 *>(row + (lane & 7) * 8) + c;
+            const uint4 *hi4 = reinterpret_cast<const uint4 *>(row + kHeadDim / 2 + (lane & 7) * 8) + c;
+            unpack16x2<T>(qe ? *lo4 : __ldg(lo4), qlo + c * (4 / kHalfLoads));
+            unpack16x2<T>(qe ? *hi4 : __ldg(hi4), qhi + c * (4 / kHalfLoads));
           }
         }
       }
-      // the slot is free: the next item's copy overlaps this one
-      const Item nxt = item_at(p, S, ci.i + NW);
-      if (slot) {
-        __syncwarp();
-        fill_slot(p, nxt, slot);
-      }
-      if (tr) {
-        const unsigned long long t = globaltimer();
-        t_item += t - tc0;
-        tc0 = t;
-      }
-#pragma unroll 1
-      for (int s = 0; s < kItemStages; ++s) {
-        const Desc d = stage_desc(ci, s);
-        int pk = 0;
-#pragma unroll
-        for (int s2 = 0; s2 < kItemStages; ++s2) pk = s2 == s ? pks[s2] : pk;
-        const uint32_t n = R.used;
-        const bool ok = wait_stage(p, S, R, n);
-        if (tr) {
-          const unsigned long long t = globaltimer();
-          t_wait += t - tc0;
-          tc0 = t;
-        }
-        if (ok) {
-          const uint8_t *buf = stage_buf(R, n);
-          if (d.kind == 1 && d.cnt > 0)
-            att_stage(A, q, buf, d.a, R.rows[n % kStages], d.a, d.a + d.cnt - 1);
-          else if (d.kind == 2)
-            match_stage(buf, d.cnt, qlo, qhi, pk, pos_lo, pos_hi, bd, bp);
-        }
-        R.used++;
-        done_with_stage();
-        if (have_nx) {
-          issue(p, R, nx, id);
-          have_nx = fetch_next(nx);
-          if (have_nx) load_ids(p, nx, id);
-        }
-        if (tr) {
-          const unsigned long long t = globaltimer();
-          t_proc += t - tc0;
-          tc0 = t;
+      if (ok) {
+        const uint8_t *buf = stage_buf(R, n);
+        if (d.kind == 1 && d.cnt > 0) {
+          // a boundary piece counts for its head alone
+          const int hm = ((lane & 15) >> kAPlain) % G;
+          const bool mine = ci.kind != 3 || hm == ci.hm;
+          att_stage(A, q, buf, d.a, R.rows[n % kStages], mine ? d.a : 1, mine ? d.a + d.cnt - 1 : 0);
+        } else if (d.kind == 2) {
+          if (d.pc)
+            pk = reinterpret_cast<const int32_t *>(R.pside + (size_t)(n % kStages) * kPosBytes)[r < d.cnt ? r : d.cnt - 1];
+          match_stage(buf, d.cnt, qlo, qhi, pk, pos_lo, pos_hi, bd, bp);
         }
       }
+      R.used++;
+      done_with_stage();
+      if (++cs < kItemStages) continue;
+      // the item is done
+      cs = 0;
       if (ci.kind == 1) {
         const int u = ci.u, t = (int)(ci.i - (int64_t)u * p.tc.nt);
         att_finish(A, p.part_w + ((size_t)u * p.tc.nt + t) * G * kPartStride);
+      } else if (ci.kind == 3) {
+        att_finish(A, S.bd + (size_t)w * kPartStride, ci.hm);
       } else {
         // the warp's best joins the head's minimum
 #pragma unroll
@@ -918,16 +933,7 @@ struct Step {
         }
         if (lane == 0 && bp >= 1) atomicMax(&S.best[ci.u], pack_best(bd, bp));
       }
-      if (tr) t_end += globaltimer() - tc0;
-      ci = nxt;
-    }
-    if (slot) asm volatile("cp.async.wait_group 0;" ::: "memory");
-    if (tr) {
-      tr[8] = t_wait;
-      tr[9] = t_item;
-      tr[10] = t_proc;
-      tr[11] = t_end;
-      tr[12] = R.used;
+      ci = get(ci.i + 1);
     }
   }
 
@@ -1117,7 +1123,7 @@ struct Step {
   // once, so a list of up to kBatch entries costs one trip to L2.
   template <class F>
   __device__ static void merge_list(int n, int nb, F entry, int dl, Cls &band, Cls &tail) {
-    constexpr int kBatch = kDL == 4 ? 16 : 32;
+    constexpr int kBatch = 8;
     const int lane = lane_id();
     band.M = tail.M = -INFINITY;
     band.L = tail.L = 0.f;
@@ -1198,30 +1204,6 @@ struct Step {
     a.M = M;
   }
 
-  // The boundary piece of head hh of unit u: tokens [lo, hi] (one window
-  // tile from lo on), whose stages this warp issued from ring use n0 on,
-  // attended for head hh alone into S.bd[hh].
-  __device__ static void boundary_piece(const StepParams &p, const Smem &S, Ring &R, int u, int hh, int lo, int hi,
-                                        uint32_t n0) {
-    Att A;
-    att_init(A);
-    float2 q[G][kAPairs];
-    load_query(p, S, u, q);
-    const int hm = ((lane_id() & 15) >> kAPlain) % G;
-    int a = lo;
-#pragma unroll 1
-    for (uint32_t n = n0; n < R.issued; ++n, a += kStTok) {
-      if (wait_stage(p, S, R, n))
-        att_stage(A, q, stage_buf(R, n), a, R.rows[n % kStages], hm == hh ? lo : 1, hm == hh ? hi : 0);
-      R.used++;
-      done_with_stage();
-    }
-    att_finish(A, S.bd, hh);
-  }
-
-  // ---------------------------------------------------------------------
-  // phase B
-  // ---------------------------------------------------------------------
   // The owner's merge of one head bh by all the CTA's warps: before the long
   // bands (pass 0) a hit or a miss of a unit without a long band, after them
   // (pass 1) a miss of a unit with one.  AS = [cached] (+) [boundary] (+)
@@ -1230,9 +1212,9 @@ struct Step {
   // of position m (fused append) or to the staging area.  Warp w sums list
   // entries w, w + 8, ... (4 dims per lane) per class; the CTA then combines
   // the warps' states in a fixed order.  A hit whose band starts inside a
-  // window tile has a boundary piece, attended by warp 0 (its copies are
-  // issued first, so they land while the list is loaded).  pos: the head's
-  // decision (-2: not known yet).  All threads call it.
+  // window tile has a boundary piece, streamed before the merge into warp
+  // bd_w's slot of S.bd.  pos: the head's decision (-2: not known yet).
+  // All threads call it.
   struct St {
     float M, L, O[4];
   };
@@ -1246,7 +1228,7 @@ struct Step {
     a.O[3] = wa * a.O[3] + wx * xo.w;
     a.M = M;
   }
-  __device__ static void merge_one(const StepParams &p, const Smem &S, Ring &R, int bh, bool long_pass, int pos) {
+  __device__ static void merge_one(const StepParams &p, const Smem &S, int bh, bool long_pass, int pos, int bd_w) {
     const int b = bh / p.Hq, h = bh - b * p.Hq, g = h / G, hh = h - g * G, u = b * p.Hkv + g;
     const int lane = lane_id(), w = warp_id(), tid = threadIdx.x;
     const bool decode = p.mode == MODE_DECODE;
@@ -1266,56 +1248,16 @@ struct Step {
       block_sync();
       return;
     }
-    int nbt = p.tc.nbw, lo = 0, thi = -1;
-    bool has_bd = false;
+    int nbt;
+    const bool has_bd = boundary_item(p, S, bh, pos, &nbt).kind == 3 && !long_pass;
     if (pos >= 1) {
-      lo = max(lb(p), pos - p.r + 1);
-      if (lo > m - p.r) {
-        nbt = 0;
-      } else {
-        const int j = (m - p.r - lo) / kTT;
-        int tlo;
-        tile_range(p, m, j, &tlo, &thi);
-        nbt = lo == tlo ? j + 1 : j;
-        has_bd = lo != tlo && !*S.abort;
-      }
       c0 = 0;
       c1 = -1;
+    } else {
+      nbt = p.tc.nbw;
     }
     unsigned long long *tr = p.trace && lane == 0 && w <= 1 ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
     if (tr && w == 0) tr[18] = globaltimer();
-    if (p.trace && w == 2 && lane == 0) {
-      // latency probe: a partial's first line, another line of it, the query row
-      unsigned long long *t2 = p.trace + (size_t)blockIdx.x * kTracePoints;
-      const float *e0 = p.part_w + (size_t)u * p.tc.nt * G * kPartStride;
-      unsigned long long a = globaltimer();
-      float x = __ldcg(e0 + 64);
-      if (x == 123.f) t2[31] = 1;
-      unsigned long long b2 = globaltimer();
-      float y = __ldcg(e0 + 96 + (x == 1.f));
-      if (y == 123.f) t2[31] = 1;
-      unsigned long long c2 = globaltimer();
-      float z = __ldcg(reinterpret_cast<const float *>(p.q) + (int64_t)bh * 64);
-      if (z == 123.f) t2[31] = 1;
-      unsigned long long d2 = globaltimer();
-      t2[20] = b2 - a;
-      t2[21] = c2 - b2;
-      t2[22] = d2 - c2;
-    }
-    const uint32_t n0 = R.issued;
-    if (has_bd && w == 0) {
-      int32_t id[2];
-#pragma unroll 1
-      for (int a = lo; a <= thi; a += kStTok) {
-        Desc d;
-        d.kind = 1;
-        d.u = u;
-        d.a = a;
-        d.cnt = min(thi - a + 1, kStTok);
-        load_ids(p, d, id);
-        issue(p, R, d, id);
-      }
-    }
     // the cached rectified summary of a hit (a state of sum 1 at its ln-LSE), by warp 1
     const int64_t cslot = (int64_t)bh * p.K + (pos >= 1 ? pos % p.K : 0);
     float c_lse = 0.f;
@@ -1362,9 +1304,7 @@ struct Step {
     if (pos >= 1 && w == 1) st_join(band, c_lse * kLog2e, 1.f, c_o);
     if (tr) tr[w == 0 ? 13 : 19] = globaltimer();
     if (has_bd && w == 0) {
-      boundary_piece(p, S, R, u, hh, lo, thi, n0);
-      __syncwarp();
-      const float *x = S.bd + hh * kPartStride;
+      const float *x = S.bd + (size_t)bd_w * kPartStride;
       st_join(band, x[kHeadDim], x[kHeadDim + 1], reinterpret_cast<const float4 *>(x)[lane]);
     }
     // the warps' states, in warp 7's idle stage ring
@@ -1563,8 +1503,7 @@ struct Step {
         }
       }
       att_finish(A, p.part_x + ((size_t)c * kWarps + warp_id()) * G * kPartStride);
-      __threadfence();  // the warp states are read back by the other threads of the CTA
-      block_sync();
+      block_sync();  // the warp states are read back (from L2) by the other threads of the CTA
       combine_warps(p, u);
       block_sync();
       // count the piece: in its CTA group (two-level) or in the unit
@@ -1597,14 +1536,11 @@ struct Step {
     }
   }
 
-  // Wait (bounded) until unit u's long-band entries are all in.
-  __device__ static void wait_long(const StepParams &p, const Smem &S, int u) {
+  // Wait (bounded, thread 0 for the CTA) until a count reaches target.
+  __device__ static void wait_count(const StepParams &p, const Smem &S, const uint32_t *ctr, uint32_t target) {
     if (threadIdx.x == 0) {
-      int c0, c1;
-      long_run(S, u, &c0, &c1);
-      const uint32_t target = (uint32_t)long_entries(c0, c1);
       const long long t0 = clock64();
-      while (ld_acquire_u32(S.unit_done + u) < target) {
+      while (ld_acquire_u32(ctr) < target) {
         if (*S.abort) break;
         if (clock64() - t0 > (1LL << 31)) {
           set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
@@ -1614,6 +1550,12 @@ struct Step {
       }
     }
     block_sync();
+  }
+  // Wait until unit u's long-band entries are all in.
+  __device__ static void wait_long(const StepParams &p, const Smem &S, int u) {
+    int c0, c1;
+    long_run(S, u, &c0, &c1);
+    wait_count(p, S, S.unit_done + u, (uint32_t)long_entries(c0, c1));
   }
 
   // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.
@@ -1663,8 +1605,8 @@ struct Step {
     S.flag = &s_flag;
     S.dec = s_dec;
     S.rope = p.B <= kRopeTab && p.rope_mode != MAC_ROPE_NONE ? reinterpret_cast<float2 *>(smem + off_rope(U)) : nullptr;
-    S.qslot = p.qslot ? smem + off_slot(U, p.B) : nullptr;
-    const bool decode = p.mode == MODE_DECODE;
+    S.pside = smem + off_pside(U, p.B);
+    S.qbuf = p.qslot ? smem + off_qbuf(U, p.B) : nullptr;
     if (p.trace && tid == 0) p.trace[(size_t)blockIdx.x * kTracePoints + 16] = (unsigned long long)clock64();
     stamp(p, 0);
     if (tid < kWarps * kStages) mbar_init(smem_addr(&S.full[tid]), 1);
@@ -1702,33 +1644,47 @@ struct Step {
     R.buf = smem + (size_t)w * kStages * kStageBytes;
     R.bar0 = smem_addr(&S.full[w * kStages]);
     R.rows = S.rows + w * kStages;
+    R.pside = S.pside + (size_t)w * kStages * kPosBytes;
+    R.qbuf = S.qbuf ? S.qbuf + (size_t)w * 2 * kQE : nullptr;
     R.issued = R.used = 0;
 
-    phase_a(p, S, R);
-    stamp(p, 1);
-    grid_barrier(p, S);  // the minima of every head are final, the window tiles written
-    stamp(p, 2);
-    {
-      // nobody reads the other buffers in this launch: clear them for the next
-      const int i0 = blockIdx.x * kThreads + tid, di = gridDim.x * kThreads;
-#pragma unroll 1
-      for (int i = i0; i < p.B * p.Hq; i += di) S.best_next[i] = 0ull;
-#pragma unroll 1
-      for (int i = i0; i < U; i += di) S.unit_done_next[i] = 0u;
-#pragma unroll 1
-      for (int i = i0; i < U + kGroups; i += di) S.group_done_next[i] = 0u;
-    }
-    layout_long(p, S);
-    stamp(p, 3);
+    // owned heads, merged by this CTA
     const int NH = p.B * p.Hq;
     int h0, h_end, hstep;
     own_range(NH, &h0, &h_end, &hstep);
-    if (!*S.abort)
+    const int nown = h_end > h0 ? (h_end - h0 + hstep - 1) / hstep : 0;
+    const int nrnd = 1 + max(1, (nown + kWarps - 1) / kWarps);
+    // round 0: phase A; round r >= 1: the boundary pieces of owned heads
+    // (r-1) kWarps .. r kWarps - 1, then their merges.  One call site of the
+    // streaming loop for all rounds.
 #pragma unroll 1
-      for (int bh = h0; bh < h_end; bh += hstep) {
-        const int k = (bh - h0) / hstep;
-        merge_one(p, S, R, bh, false, k < kOwnMax ? S.dec[k] : -2);
+    for (int rnd = 0; rnd < nrnd; ++rnd) {
+      if (rnd == 1) {
+        stamp(p, 1);
+        grid_barrier(p, S);  // the minima of every head are final, the window tiles written
+        stamp(p, 2);
+        {
+          // nobody reads the other buffers in this launch: clear them for the next
+          const int i0 = blockIdx.x * kThreads + tid, di = gridDim.x * kThreads;
+#pragma unroll 1
+          for (int i = i0; i < p.B * p.Hq; i += di) S.best_next[i] = 0ull;
+#pragma unroll 1
+          for (int i = i0; i < U; i += di) S.unit_done_next[i] = 0u;
+#pragma unroll 1
+          for (int i = i0; i < U + kGroups; i += di) S.group_done_next[i] = 0u;
+        }
+        layout_long(p, S);
+        stamp(p, 3);
       }
+      if (*S.abort && rnd > 0) continue;
+      stream(p, S, R, rnd, h0, hstep, nown);
+      if (rnd > 0) {
+        block_sync();  // the batch's boundary states are in S.bd
+#pragma unroll 1
+        for (int k = (rnd - 1) * kWarps; k < min(nown, rnd * kWarps) && !*S.abort; ++k)
+          merge_one(p, S, h0 + k * hstep, false, k < kOwnMax ? S.dec[k] : -2, k - (rnd - 1) * kWarps);
+      }
+    }
     stamp(p, 4);
     if (!*S.abort) long_bands(p, S, R);
     stamp(p, 5);
@@ -1742,7 +1698,7 @@ struct Step {
       if (c1 < c0 || pos >= 1 || *S.abort) continue;
       wait_long(p, S, u);
       if (*S.abort) continue;
-      merge_one(p, S, R, bh, true, pos);
+      merge_one(p, S, bh, true, pos, 0);
     }
     stamp(p, 6);
     drain(R);

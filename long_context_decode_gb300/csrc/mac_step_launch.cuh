@@ -46,13 +46,13 @@ static cudaError_t launch_step_g(const StepParams &p_in, int grid, cudaStream_t 
   size_t smem = 0;
   cudaError_t e = prepare_step<T, G, PAGED>(p_in.B * p_in.Hkv, p_in.B, &smem);
   if (e != cudaSuccess) return e;
-  // the warps' query slots, where shared memory allows them
+  // the warps' query entries, where shared memory allows them
   StepParams p = p_in;
   int dev = 0;
   cudaGetDevice(&dev);
-  const size_t with_slots = smem + (size_t)kWarps * S::kSlot;
-  p.qslot = dev < 64 && with_slots <= step_smem_limit<T, G, PAGED>(dev) ? S::kSlot : 0;
-  if (p.qslot) smem = with_slots;
+  const size_t with_q = smem + (size_t)S::kQBuf;
+  p.qslot = dev < 64 && with_q <= step_smem_limit<T, G, PAGED>(dev) ? 1 : 0;
+  if (p.qslot) smem = with_q;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
