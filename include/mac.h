@@ -63,7 +63,7 @@ enum { MAC_ROPE_HALF = 0, MAC_ROPE_INTERLEAVED = 1, MAC_ROPE_NONE = 2 };
 typedef struct {
   int32_t batch;       /* B: request slots */
   int32_t n_q_heads;   /* Hq */
-  int32_t n_kv_heads;  /* Hkv; Hq/Hkv in {1, 2, 4} */
+  int32_t n_kv_heads;  /* Hkv; Hq/Hkv in {1, 2, 4, 8} */
   int32_t head_dim;    /* d; 128 */
   int32_t ring_k;      /* K: ring capacity = candidate window [m-K, m-1] ([MAC] "Match (3)") */
   int32_t band_r;      /* r: rectification band ([MAC] "Amend"); r >= 0 */
@@ -182,7 +182,7 @@ int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pr
  * cannot allocate device memory: code whose device memory is owned by
  * another allocator it may not call into, code that must not trigger the
  * device-wide synchronisation cudaMalloc can cause, or code running under a
- * fixed memory budget decided at start-up.  The scratch lives in a 4 MiB
+ * fixed memory budget decided at start-up.  The scratch lives in a 16 MiB
  * array compiled into this library (MAC_NOALLOC_SCRATCH_BYTES); every GPU
  * that loads the library holds that array until the process exits.
  *   - Same arguments and results as mac_full_attention, minus scratch_ws.
@@ -244,6 +244,15 @@ int mac_set_phase_events(void *before_step, void *after_step, void *after_append
  *   26/27 producer: short-band list seen / long-band layout published
  *   28/29 time spent waiting for match chunks (ns) / match chunks scanned
  *   30/31 producer: first match copies issued / tail layout seen
+ * Configurations with Hq/Hkv = 8 run the ring kernel (every warp feeds its
+ * own stage ring; no producer warp), whose stamps are:
+ *    0 start            1 warp 0's window tiles and match items done
+ *    2 after the grid barrier         3 decisions and long bands laid out
+ *    4 boundary pieces and hit merges done   5 long bands done
+ *    6 end              7 the CTA's exit
+ *   13/19 warps 0 / 1: owner merge's list read   14/15 owner merge's
+ *         states written / combined  18 owner merge start
+ *   16/17 the SM's clock64() at start / end
  * Stamps of phases a launch does not run are left as they were.  The buffer
  * must hold MAC_TRACE_POINTS * (number of SMs) uint64.  The hook clears
  * itself. */

@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmac_gb300.so")
-SOURCES = ["mac_host.cu", "mac_append.cu"] + [f"mac_step_{t}_g{g}.cu" for t in ("bf16", "f32") for g in (1, 2, 4, 8)]
+SOURCES = ["mac_host.cu", "mac_append.cu", "mac_step_bf16.cu", "mac_step_f32.cu", "mac_step_bf16_sink.cu",
+           "mac_step_f32_sink.cu", "mac_ring_bf16_g8.cu", "mac_ring_f32_g8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -20,23 +20,36 @@ namespace mac {
 // work decomposition constants
 // ---------------------------------------------------------------------------
 constexpr int kHeadDim = 128;           // supported head dimension
-constexpr int kWarps = 8;               // warps per CTA; each feeds and drains its own stage ring
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;              // stages in each warp's ring
-constexpr int kStageBytes = 8192;       // bytes per stage: a K/V tile, or ring rows
-constexpr int kItemStages = 2;          // stages per independent work item (a window tile, a match chunk)
+constexpr int kConsumers = 256;         // span kernel: consumer threads per CTA (8 warps) ...
+constexpr int kThreads = kConsumers + 32;  // ... plus one producer warp
+constexpr int kWarps = kConsumers / 32;  // consumer warps
+constexpr int kStages = 4;              // stage buffers in the span kernel's TMA ring
+constexpr int kStageBytes = 32768;      // bytes per stage (K+V tile, or ring rows)
 constexpr int kPartStride = kHeadDim + 4;  // floats per (piece, head) partial: o[d], m, l, 0, 0
 constexpr int kMaxUnits = 1024;         // B * Hkv
 constexpr int kMaxHeads = 4096;         // B * Hq
 constexpr int kMaxGrid = 256;           // CTAs of the step grid (one per SM)
 constexpr int kGroupCtas = 16;          // CTAs per merge group of a long band
 constexpr int kGroups = kMaxGrid / kGroupCtas;
-constexpr int kMinSpan = 64;            // fewest long-band tokens worth a CTA
+constexpr int kRopeTab = 16;            // requests whose RoPE angles are tabulated per CTA
 constexpr int kTracePoints = MAC_TRACE_POINTS;  // timestamps per CTA in a phase trace
 constexpr size_t kMaxSmem = 232448;     // dynamic shared memory per CTA (227 KiB)
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+
+// The ring kernel (GQA 8: eight query heads per K/V tile) has its own
+// decomposition: every warp feeds and drains a private ring of small stages.
+struct TileCounts {
+  int nbw, ntt, nsk, nt;
+};
+namespace ring {
+constexpr int kWarps = 8;               // warps per CTA; each feeds and drains its own stage ring
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;              // stages in each warp's ring
+constexpr int kStageBytes = 8192;       // bytes per stage: a K/V tile, or ring rows
+constexpr int kItemStages = 2;          // stages per independent work item (a window tile, a match chunk)
+constexpr int kMinSpan = 64;            // fewest long-band tokens worth a CTA
 
 // Tokens of K/V per window tile (one work item): two stages of K and V rows.
 __host__ __device__ constexpr int tile_tokens(int elem_bytes) {
@@ -51,9 +64,6 @@ __host__ __device__ constexpr int item_rows(int elem_bytes) {
 // each with its own partial summary: nbw tiles of the band window, cut
 // backwards from m - r (it holds every band a hit can need), ntt tiles of
 // the tail cut forwards from m - r + 1, and nsk tiles of the front sink.
-struct TileCounts {
-  int nbw, ntt, nsk, nt;
-};
 __host__ __device__ inline TileCounts tile_counts(int K, int r, int64_t max_context, int sink_tokens,
                                                   int elem_bytes) {
   const int T = tile_tokens(elem_bytes);
@@ -66,32 +76,51 @@ __host__ __device__ inline TileCounts tile_counts(int K, int r, int64_t max_cont
   c.nt = c.nbw + c.ntt + c.nsk;
   return c;
 }
+}  // namespace ring
 
 // ---------------------------------------------------------------------------
 // scratch workspace (shared by the kernels of one stream)
 // ---------------------------------------------------------------------------
-// Window tile t of unit u leaves its partial in part_w slot u * nt + t.
-// The long bands (the part of [1, m] before the window, attended only for
-// units with a missing head) are laid end to end and cut into one span
-// per CTA; the CTA meeting unit u leaves its piece's partial in part_c slot
-// u + c (the CTAs meeting a unit form a run starting at or after the last
-// CTA of the previous unit, so these never coincide).  A run over more than
+// Span kernel (G <= 4): the tail tokens of all units, laid end to end in
+// unit order, are split into one contiguous span per CTA, and so are the
+// long bands; a CTA's span meets a few units, each meeting is a piece with
+// its own partial summary.  Piece (unit u, CTA c) goes to slot u + c: the
+// CTAs meeting a unit form a run that starts at or after the last CTA of
+// the previous unit, so the slots of different pieces never coincide and
+// B*Hkv + grid - 1 suffice.  A short band is one piece, in band slot u;
+// long-band pieces follow at B*Hkv + u + c.  A long band run over more than
 // kGroupCtas CTAs is merged in two levels: CTA group k = c / kGroupCtas
-// first, into part_g slot u + k.  part_x holds each CTA's per-warp states
-// while it combines them.  The per-head minima and the long-band counts are
-// double-buffered: launch k (counted in ctl[6]) uses buffer k & 1 and clears
-// the other for launch k + 1, so no count has to be reset by its readers.
+// first, into group slot u + k (unique for the same reason), then the
+// groups.  The per-head minima are double-buffered: decode launch k
+// combines into buffer k & 1 and clears the other for launch k + 1.
+//
+// Ring kernel (G = 8): window tile t of unit u leaves its partial in part_w
+// slot u * nt + t; the long bands are cut over the CTAs as above, the CTA
+// meeting unit u leaving its piece in part_c slot u + c, merged per CTA
+// group into part_g; part_x holds each CTA's per-warp states while it
+// combines them.  Its minima and long-band counts are double-buffered the
+// same way.
+//
+// Everything before `parts` starts at zero and a clean launch leaves it so.
 struct ScratchLayout {
   size_t ctl;        // uint32[64]: [0] status word, [2..3] grid-barrier counter (u64),
                      // [4] CTAs of the running launch finished (the last resets
-                     // it), [6] launch count
+                     // it), [6] decode launch count
   size_t best;       // uint64 [2][B][Hq]: ~(dist bits << 32 | ~pos) of the best candidate, 0 = none
-  size_t unit_done;  // uint32 [2][B*Hkv]: long-band entries (CTA pieces or groups) finished
-  size_t group_done; // uint32 [2][B*Hkv + kGroups]: CTA pieces finished per (unit, CTA group)
+  size_t unit_done;  // uint32 [2][B*Hkv]: pieces (or groups) of the unit finished
+  size_t group_done; // uint32 [2][B*Hkv + kGroups]: long-band pieces finished per (unit, CTA group)
+  size_t parts;      // first partial (nothing from here on needs clearing)
+  // span kernel
+  size_t part_a;     // f32 [B*Hkv + kMaxGrid][G][kPartStride]: tail pieces
+  size_t part_b;     // f32 [2*B*Hkv + kMaxGrid][G][kPartStride]: band pieces (short
+                     // bands at u, long-band pieces at B*Hkv + u + c)
+  size_t part_s;     // f32 [B*Hkv][G][kPartStride]: front-sink pieces
+  // both
+  size_t part_g;     // f32 [B*Hkv + kGroups][G][kPartStride]: merged CTA groups of a long band
+  // ring kernel
   size_t part_w;     // f32 [B*Hkv][nt][G][kPartStride]: window, tail and sink tiles
   size_t part_c;     // f32 [B*Hkv + kMaxGrid][G][kPartStride]: long-band CTA pieces
-  size_t part_g;     // f32 [B*Hkv + kGroups][G][kPartStride]: merged CTA groups
-  size_t part_x;     // f32 [kMaxGrid][kWarps][G][kPartStride]: warp states of a CTA piece
+  size_t part_x;     // f32 [kMaxGrid][ring::kWarps][G][kPartStride]: warp states of a CTA piece
   size_t total;
 };
 
@@ -123,8 +152,8 @@ struct StepParams {
   KvView kv;
   const void *q;             // query of (b, h) at element (b*Hq + h) * q_stride + q_offset
   int64_t q_stride, q_offset;
-  TileCounts tc;             // window tiles per unit (the scratch is sized for these)
-  int qslot;                 // the warps' query entries fit in shared memory (0: queries read from global memory)
+  TileCounts tc;             // ring kernel: window tiles per unit (the scratch is sized for these)
+  int qslot;                 // ring kernel: the warps' query entries fit in shared memory (0: read from global memory)
   // decode only
   const int32_t *ring_pos;   // [B][K]
   const void *ring_q;        // [B][Hq][K][d]
@@ -146,12 +175,14 @@ struct StepParams {
   // scratch
   uint32_t *ctl;
   unsigned long long *best;  // [2][B*Hq]
-  uint32_t *unit_done;       // [B*Hkv]
-  uint32_t *group_done;      // [B*Hkv + kGroups]
-  float *part_w, *part_c, *part_g, *part_x;
+  uint32_t *unit_done;       // [2][B*Hkv] (the span kernel uses the first half)
+  uint32_t *group_done;      // [2][B*Hkv + kGroups]
+  float *part_a, *part_b, *part_s;    // span kernel: tail, band and front-sink pieces
+  float *part_w, *part_c, *part_x;    // ring kernel: window tiles, long-band pieces, warp states
+  float *part_g;                      // merged CTA groups
   // front sink F: every summary starts at F+1 at the earliest (the reused
   // summaries leave [1, F] out); with sink_piece, [1, min(F, m)] is also
-  // attended as output-only tiles of its unit
+  // attended as output only
   int sink_f, sink_piece;
   unsigned long long *trace;  // optional: [grid][kTracePoints] %globaltimer stamps
   // RoPE frequency j as a 64-bit fixed-point fraction of a turn per
@@ -177,18 +208,22 @@ struct AppendParams {
 // ---------------------------------------------------------------------------
 // launchers (defined in the .cu files)
 // ---------------------------------------------------------------------------
-#define MAC_DECLARE_STEP(TN, G)                                                  \
-  cudaError_t launch_step_##TN##_g##G(const StepParams &p, int grid, cudaStream_t s); \
-  int step_occupancy_##TN##_g##G(bool paged, int U, int B);
-MAC_DECLARE_STEP(bf16, 1)
-MAC_DECLARE_STEP(bf16, 2)
-MAC_DECLARE_STEP(bf16, 4)
-MAC_DECLARE_STEP(bf16, 8)
-MAC_DECLARE_STEP(f32, 1)
-MAC_DECLARE_STEP(f32, 2)
-MAC_DECLARE_STEP(f32, 4)
-MAC_DECLARE_STEP(f32, 8)
-#undef MAC_DECLARE_STEP
+// span kernel, G in {1, 2, 4}
+cudaError_t launch_step_bf16(const StepParams &p, int grid, cudaStream_t s);
+cudaError_t launch_step_f32(const StepParams &p, int grid, cudaStream_t s);
+cudaError_t launch_step_bf16_sink(const StepParams &p, int grid, cudaStream_t s);
+cudaError_t launch_step_f32_sink(const StepParams &p, int grid, cudaStream_t s);
+int step_occupancy_bf16(int G, bool paged, int B, int Hq, int Hkv, int K);
+int step_occupancy_f32(int G, bool paged, int B, int Hq, int Hkv, int K);
+int step_occupancy_bf16_sink(int G, bool paged, int B, int Hq, int Hkv, int K);
+int step_occupancy_f32_sink(int G, bool paged, int B, int Hq, int Hkv, int K);
+// ring kernel, G = 8
+namespace ring {
+cudaError_t launch_bf16_g8(const StepParams &p, int grid, cudaStream_t s);
+cudaError_t launch_f32_g8(const StepParams &p, int grid, cudaStream_t s);
+int occupancy_bf16_g8(bool paged, int U, int B);
+int occupancy_f32_g8(bool paged, int U, int B);
+}  // namespace ring
 cudaError_t launch_append(const AppendParams &p, int dtype, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
@@ -279,9 +314,16 @@ __device__ __forceinline__ unsigned long long l2_evict_first_policy() {
   return pol;
 }
 
+// Barrier of the span kernel's consumer threads (all of them).  bar.sync
+// counts whole warps, so each warp first reconverges: a lane still inside a
+// single-lane region must not be counted as arrived.
+__device__ __forceinline__ void consumer_sync() {
+  __syncwarp();
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
 // Barrier `id` (1..15) of `n` threads (whole warps), after reconverging the
-// warp: bar.sync counts whole warps, so a lane still inside a single-lane
-// region must not be counted as arrived.
+// warp (same reason).
 __device__ __forceinline__ void named_sync(int id, int n) {
   __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");

@@ -54,30 +54,43 @@ mac_ring_layout ring_layout(const mac_config *c) {
   return L;
 }
 
-// Tiles per unit of a launch: window and tail, plus the front sink when the
-// launch attends it (decode steps with F > 0).
+// The step kernel of a configuration: the span kernel for GQA groups of up
+// to four query heads, the ring kernel for groups of eight.
+bool ring_kernel(const mac_config *c) { return c->n_q_heads / c->n_kv_heads == 8; }
+
+// Ring kernel: tiles per unit of a launch (window and tail, plus the front
+// sink when the launch attends it: decode steps with F > 0).
 TileCounts launch_tiles(const mac_config *c, bool sink_piece) {
-  return tile_counts(c->ring_k, c->band_r, c->max_context, sink_piece ? c->front_sink : 0, elem_size(c));
+  return ring::tile_counts(c->ring_k, c->band_r, c->max_context, sink_piece ? c->front_sink : 0, elem_size(c));
 }
 
-// Everything before part_w must start at zero (the status word, the
+// Everything before `parts` must start at zero (the status word, the
 // counters, the per-head minima and the per-unit piece counts); the
 // partials need no clearing.  A clean launch leaves it so for the next one.
 ScratchLayout scratch_layout(const mac_config *c) {
   const size_t B = c->batch, H = c->n_q_heads, U = (size_t)c->batch * c->n_kv_heads;
   const size_t G = c->n_q_heads / c->n_kv_heads;
   const size_t part = G * kPartStride * 4;  // bytes of one (piece, all heads) partial
-  const size_t nt = (size_t)launch_tiles(c, true).nt;
-  ScratchLayout S;
+  ScratchLayout S = {};
   size_t off = 0;
   S.ctl = off;         off = align_up(off + 64 * 4, 256);
   S.best = off;        off = align_up(off + 2 * B * H * 8, 256);
   S.unit_done = off;   off = align_up(off + 2 * U * 4, 256);
   S.group_done = off;  off = align_up(off + 2 * (U + kGroups) * 4, 256);
-  S.part_w = off;      off = align_up(off + U * nt * part, 256);
-  S.part_c = off;      off = align_up(off + (U + kMaxGrid) * part, 256);
-  S.part_g = off;      off = align_up(off + (U + kGroups) * part, 256);
-  S.part_x = off;      off = align_up(off + (size_t)kMaxGrid * kWarps * part, 256);
+  S.parts = off;
+  if (ring_kernel(c)) {
+    const size_t nt = (size_t)launch_tiles(c, true).nt;
+    S.part_w = off;    off = align_up(off + U * nt * part, 256);
+    S.part_c = off;    off = align_up(off + (U + kMaxGrid) * part, 256);
+    S.part_g = off;    off = align_up(off + (U + kGroups) * part, 256);
+    S.part_x = off;    off = align_up(off + (size_t)kMaxGrid * ring::kWarps * part, 256);
+  } else {
+    const size_t slots = U + kMaxGrid;
+    S.part_a = off;    off = align_up(off + slots * part, 256);
+    S.part_b = off;    off = align_up(off + (U + slots) * part, 256);
+    S.part_g = off;    off = align_up(off + (U + kGroups) * part, 256);
+    S.part_s = off;    off = align_up(off + U * part, 256);
+  }
   S.total = off;
   return S;
 }
@@ -130,13 +143,14 @@ int num_sms() {
 int step_occupancy(const mac_config *c) {
   const int G = c->n_q_heads / c->n_kv_heads, U = c->batch * c->n_kv_heads;
   const bool paged = c->page_size != 0, f32 = c->dtype == MAC_F32;
-  switch (G) {
-    case 1: return f32 ? step_occupancy_f32_g1(paged, U, c->batch) : step_occupancy_bf16_g1(paged, U, c->batch);
-    case 2: return f32 ? step_occupancy_f32_g2(paged, U, c->batch) : step_occupancy_bf16_g2(paged, U, c->batch);
-    case 4: return f32 ? step_occupancy_f32_g4(paged, U, c->batch) : step_occupancy_bf16_g4(paged, U, c->batch);
-    case 8: return f32 ? step_occupancy_f32_g8(paged, U, c->batch) : step_occupancy_bf16_g8(paged, U, c->batch);
-    default: return 0;
+  if (ring_kernel(c)) return f32 ? ring::occupancy_f32_g8(paged, U, c->batch) : ring::occupancy_bf16_g8(paged, U, c->batch);
+  const int B = c->batch, Hq = c->n_q_heads, Hkv = c->n_kv_heads, K = c->ring_k;
+  int per_sm = f32 ? step_occupancy_f32(G, paged, B, Hq, Hkv, K) : step_occupancy_bf16(G, paged, B, Hq, Hkv, K);
+  if (c->front_sink > 0) {  // the decode steps launch the sink kernels: the grid must fit both
+    const int s = f32 ? step_occupancy_f32_sink(G, paged, B, Hq, Hkv, K) : step_occupancy_bf16_sink(G, paged, B, Hq, Hkv, K);
+    per_sm = s < per_sm ? s : per_sm;
   }
+  return per_sm;
 }
 
 // Persistent grid: as many CTAs as can be resident at once (one per SM), at
@@ -177,10 +191,16 @@ StepParams step_params(const mac_config *c, const ScratchLayout &S, uint8_t *scr
   a.best = (unsigned long long *)(scratch + S.best);
   a.unit_done = (uint32_t *)(scratch + S.unit_done);
   a.group_done = (uint32_t *)(scratch + S.group_done);
-  a.part_w = (float *)(scratch + S.part_w);
-  a.part_c = (float *)(scratch + S.part_c);
   a.part_g = (float *)(scratch + S.part_g);
-  a.part_x = (float *)(scratch + S.part_x);
+  if (ring_kernel(c)) {
+    a.part_w = (float *)(scratch + S.part_w);
+    a.part_c = (float *)(scratch + S.part_c);
+    a.part_x = (float *)(scratch + S.part_x);
+  } else {
+    a.part_a = (float *)(scratch + S.part_a);
+    a.part_b = (float *)(scratch + S.part_b);
+    a.part_s = (float *)(scratch + S.part_s);
+  }
   a.tc = launch_tiles(c, false);
   return a;
 }
@@ -256,15 +276,13 @@ cudaError_t launch_step(StepParams p, const mac_config *c, cudaStream_t s) {
   if (grid < 1) return cudaErrorInvalidValue;
   p.trace = t_trace;
   t_trace = nullptr;
-  p.tc = launch_tiles(c, p.sink_piece != 0);
   const bool f32 = c->dtype == MAC_F32;
-  switch (p.G) {
-    case 1: return f32 ? launch_step_f32_g1(p, grid, s) : launch_step_bf16_g1(p, grid, s);
-    case 2: return f32 ? launch_step_f32_g2(p, grid, s) : launch_step_bf16_g2(p, grid, s);
-    case 4: return f32 ? launch_step_f32_g4(p, grid, s) : launch_step_bf16_g4(p, grid, s);
-    case 8: return f32 ? launch_step_f32_g8(p, grid, s) : launch_step_bf16_g8(p, grid, s);
-    default: return cudaErrorInvalidValue;
+  if (ring_kernel(c)) {
+    p.tc = launch_tiles(c, p.sink_piece != 0);
+    return f32 ? ring::launch_f32_g8(p, grid, s) : ring::launch_bf16_g8(p, grid, s);
   }
+  if (p.sink_piece) return f32 ? launch_step_f32_sink(p, grid, s) : launch_step_bf16_sink(p, grid, s);
+  return f32 ? launch_step_f32(p, grid, s) : launch_step_bf16(p, grid, s);
 }
 
 // Inside a stream capture the record becomes an event-record node of the
@@ -330,7 +348,7 @@ int mac_init_rings(const mac_config *cfg, void *ring_ws, void *scratch_ws, const
   const ScratchLayout S = scratch_layout(cfg);
   uint8_t *ring = (uint8_t *)ring_ws, *scr = (uint8_t *)scratch_ws;
   if (cudaMemsetAsync(ring + R.pos, 0, (size_t)cfg->batch * cfg->ring_k * 4, s) != cudaSuccess ||
-      cudaMemsetAsync(scr, 0, S.part_w, s) != cudaSuccess)
+      cudaMemsetAsync(scr, 0, S.parts, s) != cudaSuccess)
     return MAC_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -475,7 +493,7 @@ int mac_full_attention_noalloc(const mac_config *cfg, const void *q_pre, const i
   if (!scratch) return MAC_ERR_CUDA;
   // the previous call left its counters and status in the array: clear the
   // control part (everything before the partials) on this call's stream
-  if (cudaMemsetAsync(scratch, 0, scratch_layout(cfg).part_w, (cudaStream_t)stream) != cudaSuccess)
+  if (cudaMemsetAsync(scratch, 0, scratch_layout(cfg).parts, (cudaStream_t)stream) != cudaSuccess)
     return MAC_ERR_CUDA;
   return mac_full_attention(cfg, scratch, q_pre, seq_len, kv, out, lse, stream);
 }

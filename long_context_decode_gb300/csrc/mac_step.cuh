@@ -1,50 +1,50 @@
-// mac_step.cuh -- one persistent kernel per decode step (cooperative launch,
-// one CTA of eight warps per SM).  Every warp feeds and drains its own ring
-// of shared-memory stages: its first lane issues the 1-D bulk (TMA) copies a
-// few stages ahead of the stage the warp is working on, so the streaming
-// phases hold no CTA barrier.
+// mac_step.cuh -- the span kernel: one persistent kernel per decode step
+// (cooperative launch, one CTA per SM) for GQA groups of up to four query
+// heads (groups of eight run the ring kernel, mac_ring.cuh): eight consumer
+// warps and one producer warp.
 //
-//   Phase A -- work that needs no decision, as independent 16 KB items dealt
-//   round-robin to all warps of the grid:
-//     * match items ([MAC] "Match (2)"/"Match (3)", K1): 64 rows of one
-//       head's pre-RoPE query ring.  Eight lanes share a row; each sums
-//       (a-b)^2 of its 16 elements (a-b of two bf16 values is exact in fp32)
-//       as two pairwise trees, one per half of the dims; the eight lanes
-//       finish each half's tree with shuffles and the distance is the sum of
-//       the halves: at most 8 roundings of non-negative terms.  The pages'
-//       expansion |a|^2+|b|^2-2a.b cancels badly for close pairs and is not
-//       used.  The warp's best (distance, position) joins the head's minimum
-//       through a 64-bit atomic max of a packed key, a total order (smaller
-//       distance, then the more recent position), so the result does not
-//       depend on scheduling.
-//     * window tiles ([MAC] "Complete", K2): every unit (request, KV head)
-//       attends the last K + r tokens before the decisions exist, as tiles of
-//       32 tokens cut backwards from m - r (the band window: a hit at
-//       p >= m - K needs the band [p - r + 1, m - r], which lies in it) and
-//       forwards from m - r + 1 (the tail), plus the front sink when there is
-//       one.  Each tile leaves one partial summary per head (running max,
-//       sum, weighted values; base-2 log domain); a GQA group loads each K/V
-//       tile once for its G query heads.
-//   Grid barrier; the minima become decisions ([MAC] K1: hit iff the
-//   smallest squared distance is strictly below thr^2).
-//   Phase B:
-//     * hits: the band of a hit at p starts at lo = p - r + 1, inside one
-//       window tile; the unit's owner CTA re-attends that tile from lo on
-//       for the head (its later tiles are whole), then merges the cached
-//       rectified summary of [1, p - r], the boundary piece and the band
-//       tiles into AS_{1:m-r}, and that with the tail into the output
-//       ([MAC] "Decomposable attention", "Amend"; [ACSP] log-sum-exp merge).
-//     * misses ([MAC] "Match (1)": exact attention): the rest of [1, m]
-//       before the window (the long band) of every unit with a missing head,
-//       laid end to end and cut into one span per CTA; the eight warps of a
-//       CTA take its stages round-robin and combine their states per unit;
-//       the CTAs' pieces are merged per group of kGroupCtas CTAs by the last
-//       to finish, and the owner merges the groups with the window tiles.
-//   Full attention (and ring seeding) run the same kernel with every head
-//   missing and no match, so a decode step whose heads all miss is bitwise
-//   equal to full attention.
+//   Phase M (Match, [MAC] "Match (2)"/"Match (3)", K1): the pre-RoPE query
+//   rings of all (request, head) pairs form B*Hq*K rows, cut into chunks of at
+//   most a stage (never across heads) dealt round-robin to the CTAs, so every
+//   CTA reads every part of the memory.  Eight lanes share a row; each sums
+//   (a-b)^2 of its 16 elements in a pairwise tree (a-b of two bf16 values is
+//   exact in fp32) and the eight finish the tree with shuffles, so a distance
+//   carries at most 8 roundings of non-negative terms.  The pages' expansion
+//   |a|^2+|b|^2-2a.b cancels badly for close pairs and is not used.  Each warp
+//   combines its rows' best (distance, position) into the head's minimum with
+//   a 64-bit atomic max of a packed key, a total order (smaller distance, then
+//   more recent position), so the result does not depend on scheduling.
 //
-// Every wait is bounded and reports MAC_DEV_WAIT_TIMEOUT instead of hanging.
+//   Complete (K2), tail pieces: the last r tokens of every unit, which every
+//   head attends whatever the match decides, so they run before the
+//   decisions exist (their tiles are copied during the match).
+//
+//   Grid barrier; every CTA turns the minima into decisions ([MAC] K1: hit
+//   iff the smallest squared distance is strictly below thr^2) and lays out
+//   the band [s, m-r] of every unit (request, kv head), s = the first token
+//   any head of the unit needs (p-r+1 for a hit at p, 1 for a miss).  Band
+//   pieces follow; a head whose band starts after s masks the tokens before
+//   its own start ([MAC] "GQA intra-group skew").
+//
+//   Merge: the CTA that finishes a unit's last piece (a count per unit)
+//   merges, per head, the cached rectified summary of a hit, the band
+//   pieces in token order (giving AS_{1:m-r}) and then the tail pieces
+//   (giving the output); a unit without band pieces is merged after the
+//   decisions by one CTA chosen by its index.
+//
+// Work balance ("span-balanced" flash decode): the tail tokens of all units
+// are laid end to end and cut into one contiguous span per CTA, and so are
+// the band tokens; a span meets a few units, and each meeting (a piece)
+// leaves one partial summary (running max, sum, weighted values; base-2 log
+// domain, [MAC] "Complete").  A GQA group loads each K/V tile once for its G
+// query heads.  Full attention (and ring seeding) run the same pieces with
+// s = 1 and no match, so a decode step whose heads all miss is bitwise equal
+// to full attention.
+//
+// Streaming: one ring of kStages shared-memory stages filled with 1-D TMA
+// bulk copies by the producer warp (full/empty mbarriers) and drained by the
+// consumer warps.  Every wait is bounded and reports MAC_DEV_WAIT_TIMEOUT
+// instead of hanging.
 #pragma once
 
 #include "mac_common.cuh"
@@ -71,7 +71,7 @@ __device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long
 }
 
 // A count of finished pieces: release of the partials the calling CTA wrote
-// before its barrier, acquire of those the earlier counts released.
+// before its consumer barrier, acquire of those the earlier counts released.
 __device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t *p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -81,12 +81,6 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t *p, uint32_t v
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -109,6 +103,7 @@ __device__ __forceinline__ void unpack16x2<float>(const uint4 &u, float2 *f) {
   f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
 }
 
+
 constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x >> 1); }
 
 // Running maxima start here (finite, so that empty states never produce
@@ -117,307 +112,1129 @@ constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x >> 1); }
 constexpr float kMInit = -1e30f;
 constexpr float kLazy = 8.f;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int32_t kNoPage = (int32_t)0x80000000;
 
-template <typename T, int G, bool PAGED>
+// SINK: whether the kernel attends front-sink pieces (a launch with a front
+// sink uses the SINK = true kernels; the others carry none of that code)
+template <typename T, int G, bool PAGED, bool SINK>
 struct Step {
-  static constexpr int kES = (int)sizeof(T);
-  static constexpr int kRow = kHeadDim * kES;                 // bytes of a K, V or ring row
-  static constexpr int kStTok = kStageBytes / (2 * kRow);     // K/V tokens per stage: 16 / 8
-  static constexpr int kTT = kStTok * kItemStages;            // tokens per window tile: 32 / 16
-  static constexpr int kStRows = kStageBytes / kRow;          // ring rows per stage: 32 / 16
-  static constexpr int kIR = kStRows * kItemStages;           // ring rows per match item
-  static constexpr int kPer = 16 / kES;                       // elements per 16-byte load
-  // match: 8 lanes per row, lane `sub` owns dims [8 sub, 8 sub + 8) of
-  // each half of the row; kMRG rows per lane group of a stage
-  static constexpr int kHalfLoads = 8 / kPer;                 // 16-byte loads per half: 1 / 2
-  static constexpr int kMRG = kStRows / 4;                    // 8 / 4
-  static constexpr int kLogMRG = ilog2c(kMRG);
-  // attention: a half-warp per token, lane `sub` (0..15) owns dims
-  // [8 sub, 8 sub + 8) of the query and the weighted values; kATPG tokens
-  // per half-warp per pass, one score per lane after a reduce-scatter
-  static constexpr int kATPG = G <= 4 ? 4 : 2;
-  static constexpr int kPassTok = 2 * kATPG;
-  static constexpr int kPasses = kStTok / kPassTok;
-  static constexpr int kAV = kATPG * G;
-  static constexpr int kAScat = ilog2c(kAV);
-  static constexpr int kAPlain = 4 - kAScat;
+  static constexpr int kRowBytes = kHeadDim * (int)sizeof(T);
+  static constexpr int kTileTok = kStageBytes / (2 * kRowBytes);  // 64 (bf16) / 32 (fp32)
+  static constexpr int kMatchRows = kStageBytes / kRowBytes;      // ring rows per stage
+  static constexpr int kRPG = kMatchRows / 32;                    // rows per lane group per match chunk
+  static constexpr int kLogRPG = ilog2c(kRPG);
+  static constexpr int kPer = 16 / (int)sizeof(T);                // elements per 16-byte piece
+  static constexpr int kNP = 16 / kPer;                           // pieces per lane (16 dims)
+  static constexpr int kPairs = 8;                                // float2 pairs per lane (16 dims)
+  // attention: a half-warp (16 lanes, 8 dims each) per token; kAGroups
+  // half-warps per CTA, kATPG tokens each per tile
+  static constexpr int kAGroups = kWarps * 2;
+  static constexpr int kATPG = kTileTok / kAGroups;               // 4 (bf16) / 2 (fp32)
+  static constexpr int kAPairs = 4;                               // float2 pairs per lane (8 dims)
+  static constexpr int kALoads = 8 * (int)sizeof(T) / 16;         // 16-byte loads per lane and row
+  static constexpr int kAV = kATPG * G;                           // scores of a half-warp per tile
+  static constexpr int kAScat = ilog2c(kAV);                      // reduce-scatter levels
+  static constexpr int kAPlain = 4 - kAScat;                      // plain butterfly levels after them
   static constexpr int kLogG = ilog2c(G);
   static constexpr int kLogATPG = ilog2c(kATPG);
-  static constexpr int kAPairs = 4;                           // float2 per lane and head
-  static constexpr int kALoads = 8 * kES / 16;                // 16-byte loads per lane and row
-  // merges: kWPH warps per head, each owning kDW dims (kDL per lane)
-  static constexpr int kWPH = kWarps / G;
-  static constexpr int kDW = kHeadDim / kWPH;
-  static constexpr int kDL = kDW >= 32 ? kDW / 32 : 1;
-  static constexpr int kLanes = kDW / kDL;
+  static constexpr int kQBytes = G * kRowBytes;
+  // per-stage side buffer: a tile's G query rows, or a match chunk's query
+  // row, ring positions and chunk coordinates (int4 at kInfoOff)
+  static constexpr int kInfoOff = kRowBytes + 4 * kMatchRows;
+  static constexpr int kAux = (kQBytes > kInfoOff + 16 ? kQBytes : kInfoOff + 16);
+  static constexpr int kOutPer = (G * kHeadDim + kConsumers - 1) / kConsumers;
   static_assert(kAV <= 16 && kAV >= 2, "one score per lane of a half-warp at most");
-  static_assert(kPasses >= 1 && kPasses * kPassTok == kStTok, "passes per stage");
-  static_assert(kStTok <= 16, "a stage meets at most two 16-token pages");
 
   // dynamic shared memory layout
-  static constexpr size_t kOffBar = (size_t)kWarps * kStages * kStageBytes;
-  static constexpr size_t kOffMask = kOffBar + 8 * kWarps * kStages;      // int [kWarps][kStages]
-  static constexpr size_t kOffBd = kOffMask + 4 * kWarps * kStages;       // f32 [kWarps][kPartStride]
-  static constexpr size_t kOffUnits = kOffBd + 4 * (size_t)kWarps * kPartStride;
-  static_assert(kOffBar % 8 == 0 && kOffBd % 16 == 0 && kOffUnits % 16 == 0, "alignment");
-  // + the long-band offsets (int64 [U + 1]) and unit lengths (int32 [U]),
-  // then, for at most kRopeTab requests, the cos and sin of every request's
-  // query rotation angles (float2 [B][d/2])
-  static constexpr int kRopeTab = 16;
-  __host__ __device__ static size_t off_rope(int U) {
-    return (kOffUnits + 8 * (size_t)(U + 1) + 4 * (size_t)U + 15) / 16 * 16;
+  static constexpr size_t kOffQ = (size_t)kStages * kStageBytes;
+  static constexpr size_t kOffBar = kOffQ + (size_t)kStages * kAux;       // full[kStages], empty[kStages]
+  static constexpr size_t kOffQrot = kOffBar + 128;                        // [G][d] f32
+  static constexpr size_t kOffRedO = kOffQrot + 4 * (size_t)G * kHeadDim;  // [kWarps][4][G][d]
+  static constexpr size_t kOffRedL = kOffRedO + 4 * (size_t)kWarps * 4 * G * kHeadDim;
+  static constexpr size_t kOffRedM = kOffRedL + 4 * (size_t)kWarps * 4 * G;
+  static constexpr size_t kOffX = kOffRedM + 4 * (size_t)kWarps * G;
+  static_assert(kOffBar % 8 == 0 && kOffX % 8 == 0, "alignment");
+
+  // X: the matched position of every head (-1: miss)
+  __host__ __device__ static int x_ints(int B, int Hq, int K) { (void)K; return B * Hq; }
+  __host__ __device__ static size_t off_units(int B, int Hq, int K) {
+    return (kOffX + 4 * (size_t)x_ints(B, Hq, K) + 7) / 8 * 8;
   }
-  // + each stage's ring positions (a match stage's rows: int32 [kStRows]),
-  // then (when there is room) each warp's two query entries: a unit's G
-  // query rows or a head's, copied with the first stage of an item whose
-  // query differs from the item before
-  static constexpr int kPosBytes = kStRows * 4;
-  static constexpr int kQE = G * kRow;
-  static constexpr int kQBuf = kWarps * 2 * kQE;
-  __host__ __device__ static size_t off_pside(int U, int B) {
-    return off_rope(U) + (B <= kRopeTab ? 8 * (size_t)B * (kHeadDim / 2) : 0);
+  // + offsets of the tail and long-band segments and the short-band cost
+  // prefix (int64, n_units + 1 each), query position, band start and the
+  // short-band list (int32) and the tail and band CTA runs (short2) of every
+  // unit, then the RoPE cos/sin table of every request when there are at
+  // most kRopeTab of them
+  __host__ __device__ static size_t off_rope(int B, int Hq, int Hkv, int K) {
+    const size_t U = (size_t)B * Hkv;
+    return (off_units(B, Hq, K) + 24 * (U + 1) + 20 * U + 7) / 8 * 8;
   }
-  __host__ __device__ static size_t off_qbuf(int U, int B) {
-    return off_pside(U, B) + (size_t)kWarps * kStages * kPosBytes;
+  __host__ __device__ static size_t smem_bytes(int B, int Hq, int Hkv, int K) {
+    const size_t tab = B <= kRopeTab ? 8 * (size_t)B * (kHeadDim / 2) : 0;
+    return off_rope(B, Hq, Hkv, K) + tab;
   }
-  __host__ __device__ static size_t smem_bytes(int U, int B) { return off_qbuf(U, B); }
 
   struct Smem {
-    uint8_t *stage;     // [kWarps][kStages][kStageBytes]
-    uint64_t *full;     // [kWarps][kStages]: the stage's copy has landed
-    int *rows;          // [kWarps][kStages]: rows of the stage that were copied (bit mask)
-    float *bd;          // [kWarps][kPartStride]: boundary pieces of a batch of owned heads
-    int64_t *off;       // [U + 1]: long-band offsets (units end to end)
-    int32_t *um;        // [U]: the unit's length m (0: not a valid length)
-    long long *scan;    // [kWarps]
+    uint8_t *stage;     // [kStages][kStageBytes]
+    uint8_t *qbuf;      // [kStages][kAux]: pre-RoPE query rows of a piece's unit, or a
+                        // match chunk's query row and ring positions
+    uint64_t *full;     // [kStages]: the stage's copy has landed
+    uint64_t *empty;    // [kStages]: every consumer warp is done with the stage
+    float *qrot;        // [G][d]: rotated, scaled query of the current piece
+    float *red_o;       // [kWarps][4][G][d]
+    float *red_l;       // [kWarps * 4][G]
+    float *red_m;       // [kWarps][G]
+    int32_t *X;
+    int64_t *offA;      // [n_units + 1]: first global index of each unit's tail segment
+    int64_t *offB;      // [n_units + 1]: same for the long bands on their cost axis: each
+                        // long band is kLongPiece (a piece's fixed cost) + its tokens;
+                        // short ones count 0
+    int64_t *spanA;     // [grid + 1]: CTA c's tail span is [spanA[c], spanA[c+1])
+    int64_t *spanB;     // [grid + 1]: same for the long bands
+    int *neA, *neB;     // [grid + 1]: non-empty spans among CTAs 0..c-1
+    int32_t *u_pos;     // [n_units]: position of the unit's query (RoPE angle pos - 1)
+    int32_t *u_s;       // [n_units]: first band token of the unit
+    int32_t *shortU;    // [n_units]: the units with a short band, in unit order
+    int64_t *scp;       // [n_units + 1]: prefix of their costs (tokens + kPieceCost)
+    short2 *runA;       // [n_units]: first and last CTA meeting the unit's tail (x > y: none)
+    short2 *runB;       // [n_units]: same for its long band
+    int *n_short;       // their number; CTA c has entries [c*n/P, (c+1)*n/P)
+    long long *scan;    // [kWarps]: block_scan's warp totals
+    long long *short_max;  // longest band that is one piece
+    long long *band_tot;   // [2]: long-band tokens, their cost plus the short pieces'
+    float2 *rope;       // [B][d/2]: cos, sin of the query's rotation angles (B <= kRopeTab), or null
+    int *mask;          // [kStages]: valid 16-token pages of the tile in the stage
     volatile int *abort;
-    int64_t *ntok;      // long-band tokens in all
-    int *Pl;            // CTAs the long bands are cut over
-    unsigned long long *best, *best_next;
-    volatile uint32_t *flag;
-    int *dec;           // [kOwnMax]: decisions of the heads this CTA owns
-    uint32_t *unit_done, *group_done;            // this launch's long-band counts
-    uint32_t *unit_done_next, *group_done_next;  // cleared here for the next launch
-    float2 *rope;       // [B][d/2] cos, sin of the query angles (B <= kRopeTab), or null
-    uint8_t *pside;     // [kWarps][kStages][kPosBytes]: ring positions of match stages
-    uint8_t *qbuf;      // [kWarps][2][kQE]: query entries, or null (queries read from global memory)
+    volatile int *ready;  // layouts known to the producer: 1 tails (and bands in full mode), 2 bands
+    volatile uint32_t *issued;  // uses the producer copied (published at its end)
+    unsigned long long *best;   // this launch's per-head minima (decode)
+    unsigned long long *best_next;  // cleared here for the next decode launch
+    volatile int *last;         // this CTA finished the last piece of a unit
   };
 
-  // One warp's ring: stage uses are numbered; use n sits in stage n % kStages.
-  struct Ring {
-    uint8_t *buf;       // this warp's kStages stages
-    uint32_t bar0;      // shared address of its first full barrier
-    int *rows;
-    uint8_t *pside;     // this warp's stage position buffers
-    uint8_t *qbuf;      // this warp's two query entries (or null)
-    uint32_t issued, used;
+  struct Piece {
+    int u, lo, hi;
+    int sink;  // the front sink [1, min(F, m)] of unit u (an output-only piece)
   };
 
-  // What one stage use holds: K/V rows [a, a + cnt) of unit u (kind 1), or
-  // ring rows [a, a + cnt) of head u (kind 2); kind 0: nothing; -1: the end.
-  struct Desc {
-    int kind = -1, u = 0, a = 0, cnt = 0;
-    int qe = -1;   // >= 0: also copy the item's query (unit u's G rows; head u's for kind 2) into entry qe
-    int pc = 0;    // a match stage whose ring positions come into its position buffer
-    int keep = 0;  // K/V rows kept in L2 (read again by a boundary piece)
-  };
+  // Phase trace point (see mac_set_trace): thread 0 records %globaltimer.
+  // Like every region run by one thread, it ends with the warp reconverged
+  // before the barriers and shuffles that follow.
+  __device__ static void stamp(unsigned long long *trace, int k) {
+    if (trace && threadIdx.x == 0) trace[k] = globaltimer();
+    __syncwarp();
+  }
+  __device__ static unsigned long long *cta_trace(const StepParams &p) {
+    return p.trace ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
+  }
 
-  __device__ static int lane_id() { return threadIdx.x & 31; }
-  __device__ static int warp_id() { return threadIdx.x >> 5; }
+  // Lane `sub` (0..7) of a token's 8-lane group owns 16 dimensions: piece c
+  // covers dims [c*8*kPer + sub*kPer, +kPer), so each group reads 128
+  // contiguous bytes of a row per piece (no shared-memory bank conflicts).
+  __device__ static int piece_dim(int c, int sub) { return c * 8 * kPer + sub * kPer; }
 
-  // ---------------------------------------------------------------------
-  // unit geometry
-  // ---------------------------------------------------------------------
-  // lb: the first token a summary covers (F + 1; 1 for full attention).
-  __device__ static int lb(const StepParams &p) { return p.sink_f + 1; }
+  // the lengths the scratch and the cache hold
   __device__ static bool len_ok(const StepParams &p, int64_t m) { return m >= 1 && m <= p.max_len; }
-  // window start: the earliest band start a hit can have
-  __device__ static int win_start(const StepParams &p, int m) { return max(lb(p), m - p.r - p.K + 1); }
-  __device__ static int tail_start(const StepParams &p, int m) { return max(lb(p), m - p.r + 1); }
-  // Tile t of a unit of length m (0 when invalid): tokens [*lo, *hi] (empty when *lo > *hi).
-  __device__ static void tile_range(const StepParams &p, int m, int t, int *lo, int *hi) {
-    *lo = 1;
-    *hi = 0;
-    if (m <= 0) return;
-    if (t < p.tc.nbw) {
-      const int h = m - p.r - kTT * t;
-      *hi = h;
-      *lo = max(win_start(p, m), h - kTT + 1);
-    } else if (t < p.tc.nbw + p.tc.ntt) {
-      const int l = tail_start(p, m) + kTT * (t - p.tc.nbw);
-      *lo = l;
-      *hi = min(m, l + kTT - 1);
-    } else if (p.sink_piece) {
-      const int l = 1 + kTT * (t - p.tc.nbw - p.tc.ntt);
-      *lo = l;
-      *hi = min(min(p.sink_f, m), l + kTT - 1);
-    }
+  __device__ static int64_t unit_len(const StepParams &p, const Smem &S, int u) {
+    return (int64_t)S.u_pos[u] - p.len_sub;
   }
-  // the request's query position (RoPE angle pos - 1)
-  __device__ static int64_t qpos(const StepParams &p, int b) { return (int64_t)p.pos_base[b] + p.pos_add; }
 
   // ---------------------------------------------------------------------
-  // copies
+  // segments, spans and pieces
   // ---------------------------------------------------------------------
-  __device__ static uint8_t *stage_buf(const Ring &R, uint32_t n) {
-    return R.buf + (size_t)(n % kStages) * kStageBytes;
-  }
-  __device__ static uint32_t stage_bar(const Ring &R, uint32_t n) { return R.bar0 + 8 * (n % kStages); }
 
-  // Page ids of the (at most two) pages a K/V stage meets, loaded ahead of
-  // its copy (kNoPage: none).
-  __device__ static void load_ids(const StepParams &p, const Desc &d, int32_t (&id)[2]) {
-    id[0] = id[1] = kNoPage;
-    if (!PAGED || d.kind != 1 || d.cnt <= 0 || lane_id() != 0 || d.u < 0 || d.u >= p.B * p.Hkv) return;
-    const int b = d.u / p.Hkv;
-    const int s0 = (d.a - 1) >> 4, s1 = (d.a + d.cnt - 2) >> 4;
-    const int32_t *row = p.kv.page_table + (int64_t)b * p.kv.max_pages;
-    if (s0 >= 0 && s0 < p.kv.max_pages) id[0] = __ldg(row + s0);
-    if (s1 != s0 && s1 < p.kv.max_pages) id[1] = __ldg(row + s1);
+  // First token of unit u's segment: tails [max(F+1, m-r+1), m], bands
+  // [s, m-r] (F: the front sink, 0 without one).
+  __device__ static int64_t seg_first(const StepParams &p, const Smem &S, int ph, int u) {
+    if (ph == 1) return S.u_s[u];
+    const int64_t a = unit_len(p, S, u) - p.r + 1;
+    return a > p.sink_f + 1 ? a : p.sink_f + 1;
   }
-
-  // The query copy that rides with a stage: bytes, and its issue.
-  __device__ static uint32_t query_bytes(const Desc &d, const Ring &R) {
-    return d.qe >= 0 && R.qbuf ? (d.kind == 2 ? (uint32_t)kRow : (uint32_t)kQE) : 0u;
-  }
-  __device__ static void issue_query(const StepParams &p, const Ring &R, const Desc &d, uint32_t bar) {
-    uint8_t *dst = R.qbuf + (size_t)d.qe * kQE;
-    const uint8_t *q = (const uint8_t *)p.q;
-    if (d.kind == 2) {
-      bulk_g2s(smem_addr(dst), q + ((int64_t)d.u * p.q_stride + p.q_offset) * kES, kRow, bar);
-      return;
+  __device__ static int64_t seg_len(const StepParams &p, const Smem &S, int ph, int u) {
+    const int64_t m = unit_len(p, S, u);
+    if (!len_ok(p, m)) return 0;
+    if (ph == 0) {
+      const int64_t n = m - seg_first(p, S, 0, u) + 1;
+      return n > 0 ? n : 0;
     }
-    const int b = d.u / p.Hkv, g = d.u - b * p.Hkv;
-    const int64_t bh0 = (int64_t)b * p.Hq + g * G;
-    if (p.q_stride == kHeadDim && p.q_offset == 0) {  // the unit's G rows are contiguous
-      bulk_g2s(smem_addr(dst), q + bh0 * kRow, kQE, bar);
-    } else {
-      for (int hh = 0; hh < G; ++hh)
-        bulk_g2s(smem_addr(dst + hh * kRow), q + ((bh0 + hh) * p.q_stride + p.q_offset) * kES, kRow, bar);
-    }
+    const int64_t n = (m - p.r) - (int64_t)S.u_s[u] + 1;
+    return n > 0 ? n : 0;
   }
 
-  // Lane 0: the copies of the next stage use (every lane calls it).
-  __device__ static void issue(const StepParams &p, Ring &R, const Desc &d, const int32_t (&id)[2]) {
-    const uint32_t n = R.issued++;
-    if (lane_id() != 0) return;
-    uint8_t *buf = stage_buf(R, n);
-    const uint32_t bar = stage_bar(R, n);
-    int *rows = R.rows + n % kStages;
-    const uint32_t qb = query_bytes(d, R);
-    if (d.kind == 2) {  // ring rows of head d.u (and their positions)
-      const uint32_t bytes = (uint32_t)d.cnt * kRow;
-      *rows = (1 << d.cnt) - 1;
-      mbar_expect_tx(bar, bytes + qb + (d.pc ? 4u * d.cnt : 0u));
-      if (qb) issue_query(p, R, d, bar);
-      if (d.pc)
-        bulk_g2s(smem_addr(R.pside + (size_t)(n % kStages) * kPosBytes),
-                 p.ring_pos + (int64_t)(d.u / p.Hq) * p.K + d.a, 4u * d.cnt, bar);
-      bulk_g2s_hint(smem_addr(buf), (const uint8_t *)p.ring_q + ((size_t)d.u * p.K + d.a) * kRow, bytes, bar,
-                    l2_evict_first_policy());
-      return;
-    }
-    const int g = d.u % p.Hkv;
-    int msk = 0;
-    uint32_t bytes = 0;
-    bool ok = d.kind == 1 && d.cnt > 0;
-    if (ok && !PAGED && (d.a < 1 || d.a + d.cnt - 1 > p.kv.capacity || d.u >= p.B * p.Hkv)) {
-      set_status(p.ctl, MAC_DEV_BAD_COPY);
-      ok = false;
-    }
-    const int n0 = ok ? min(d.cnt, 16 - ((d.a - 1) & 15)) : 0;  // rows of the first page (paged)
-    if (ok && !PAGED) {
-      msk = (1 << d.cnt) - 1;
-      bytes = 2u * (uint32_t)d.cnt * kRow;
-    } else if (ok) {
+  __device__ static const int64_t *offs(const Smem &S, int ph) { return ph ? S.offB : S.offA; }
+
+  // c * total / P, in 32-bit arithmetic whenever the product fits (the
+  // common case: 64-bit division is a long serial routine)
+  __device__ static int64_t part_of(int c, int64_t total, int P) {
+    if (total < (1LL << 23)) return (int64_t)((uint32_t)c * (uint32_t)total / (uint32_t)P);
+    return div_s64((int64_t)c * total, P);
+  }
+  __device__ static const int64_t *spans(const Smem &S, int ph) { return ph ? S.spanB : S.spanA; }
+
+  // the CTA whose (non-empty) span holds global index x (x < total): the
+  // last c < P with span[c] <= x (span[0] = 0), by binary lifting over the
+  // P <= kMaxGrid entries: a fixed number of steps without branches
+  __device__ static int cta_of(const int64_t *span, int P, int64_t x) {
+    int lo = 0;
 #pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int cnt = s ? d.cnt - n0 : n0;
-        if (cnt <= 0 || id[s] == kNoPage) continue;
-        if (id[s] < 0 || id[s] >= p.kv.n_pages) {
-          set_status(p.ctl, MAC_DEV_BAD_PAGE);
-          continue;
-        }
-        msk |= s ? ((1 << d.cnt) - 1) & ~((1 << n0) - 1) : (1 << n0) - 1;
-        bytes += 2u * (uint32_t)cnt * kRow;
+    for (int s = kMaxGrid / 2; s >= 1; s >>= 1) {
+      const int t = lo + s;
+      if (t < P && span[t] <= x) lo = t;
+    }
+    return lo;
+  }
+  // unit whose segment holds global index g (g < T): the last u < U with
+  // off[u] <= g, by binary lifting
+  __device__ static int unit_of(const int64_t *off, int U, int64_t g) {
+    int lo = 0;
+#pragma unroll 1
+    for (int s = U > 1 ? 1 << (31 - __clz(U - 1)) : 0; s >= 1; s >>= 1) {
+      const int t = lo + s;
+      if (t < U && off[t] <= g) lo = t;
+    }
+    return lo;
+  }
+
+  // The first piece of span [g0, g1) at unit >= u; false when none is left.
+  __device__ static bool find_piece(const StepParams &p, const Smem &S, int ph, int u, int64_t g0,
+                                    int64_t g1, Piece *pc) {
+    const int64_t *off = offs(S, ph);
+    const int U = p.B * p.Hkv;
+#pragma unroll 1
+    for (; u < U; ++u) {
+      const int64_t a0 = off[u], z0 = off[u + 1];
+      if (a0 >= g1) return false;
+      const int64_t r0 = ph && z0 > a0 ? a0 + kLongPiece : a0;  // the band's first real token
+      const int64_t a = r0 > g0 ? r0 : g0, z = z0 < g1 ? z0 : g1;
+      if (a < z) {
+        const int64_t t0 = seg_first(p, S, ph, u);
+        pc->u = u;
+        pc->lo = (int)(t0 + (a - r0));
+        pc->hi = (int)(t0 + (z - r0) - 1);
+        return true;
       }
     }
-    *rows = msk;
-    if (bytes + qb == 0) {
+    return false;
+  }
+
+  // Tail layout, by all consumer threads (ends with a consumer barrier): the
+  // exclusive prefix of the tail lengths, the CTA spans, their non-empty
+  // counts and every unit's CTA run.  With at most as many units as CTAs,
+  // unit u owns the CTAs [u*P/U, (u+1)*P/U) and its tail is cut evenly among
+  // the first k' of them, k' = min(its CTAs, length / kMinSpan rounded up),
+  // so no CTA meets two units (a second piece would double its fixed costs)
+  // nor gets a sliver, and everything but the prefix has a closed form; with
+  // more units the tails, laid end to end, are cut into equal spans.
+  static constexpr int kMinSpan = 64;  // tokens: a piece worth its fixed cost
+  __device__ static int tail_ctas(int64_t len, int k) {
+    if (len <= 0) return 0;
+    const int64_t want = (len + kMinSpan - 1) / kMinSpan;
+    return want < k ? (int)want : k;
+  }
+  __device__ static void layout_tails(const StepParams &p, const Smem &S) {
+    int64_t *off = S.offA;
+    const int U = p.B * p.Hkv, tid = threadIdx.x, P = gridDim.x;
+    const bool aligned = U <= P;
+    // prefix of (length << 9 | non-empty spans of the unit's CTAs); a
+    // unit's k' <= P <= 256 used CTAs all hold non-empty spans
+    long long carry = 0;
+#pragma unroll 1
+    for (int base = 0; base < U; base += kConsumers) {
+      const int u = base + tid;
+      long long x = 0;
+      if (u < U) {
+        const long long len = seg_len(p, S, 0, u);
+        const int k = aligned ? (u + 1) * P / U - u * P / U : 0;
+        x = (len << 9) | (long long)tail_ctas(len, k);
+      }
+      long long tot;
+      const long long ex = block_scan(S, x, &tot);
+      if (u < U) {
+        off[u + 1] = (carry + ex + x) >> 9;
+        if (aligned) S.neA[u + 1] = (int)((carry + ex + x) & 511);  // per-unit prefix, per-CTA below
+      }
+      carry += tot;
+    }
+    const int64_t total = carry >> 9;
+    if (tid == 0) {
+      off[0] = 0;
+      if (aligned) S.neA[0] = 0;
+    }
+    consumer_sync();
+    const int c = tid;  // P <= kMaxGrid = kConsumers: one CTA per thread (CTA P by thread 0)
+    if (aligned) {
+      int ne = 0;
+      if (c < P) {
+        const int u = ((c + 1) * U - 1) / P;
+        const int a = u * P / U, j = c - a;
+        const int64_t len = off[u + 1] - off[u];
+        const int k = tail_ctas(len, (u + 1) * P / U - a);
+        int64_t share = len;  // CTAs past the k' used ones: empty spans at the unit's end
+        if (j < k)
+          share = len < (1LL << 22) ? (int64_t)((uint32_t)len * (uint32_t)j / (uint32_t)k) : div_s64(len * j, k);
+        S.spanA[c] = off[u] + share;
+        // slices 0..j-1 of the unit: all non-empty up to the k' used ones
+        ne = S.neA[u] + (j < k ? j : k);
+      }
+      const int neP = (int)(carry & 511);
+      consumer_sync();  // every per-unit prefix read before the per-CTA counts overwrite it
+      if (c < P) S.neA[c] = ne;
+      if (c == 0) {
+        S.spanA[P] = total;
+        S.neA[P] = neP;
+      }
+#pragma unroll 1
+      for (int u = tid; u < U; u += kConsumers) {
+        const int a = u * P / U, k = tail_ctas(off[u + 1] - off[u], (u + 1) * P / U - a);
+        S.runA[u] = k > 0 ? make_short2((short)a, (short)(a + k - 1)) : make_short2(0, -1);
+      }
+    } else {
+      if (c <= P) S.spanA[c] = c < P ? part_of(c, total, P) : total;
+      consumer_sync();
+      int tot;
+      const int ef = flag_scan(S, c < P && S.spanA[c] < S.spanA[c + 1], &tot);
+      if (c < P) S.neA[c] = ef;
+      if (c == 0) S.neA[P] = tot;
+#pragma unroll 1
+      for (int u = tid; u < U; u += kConsumers) S.runA[u] = find_run(S, 0, u);
+    }
+    consumer_sync();
+  }
+
+  // Band layout.  A band of at most max(kShortBand, all band tokens / P)
+  // tokens (a hit whose match is recent: the common case) is one piece on
+  // its own, since splitting it would cost more merges than it saves -- as
+  // long as at most P/2 units qualify, else the bound is kShortBand (many
+  // whole units dealt by count would give some CTAs two where spans give
+  // each its exact share).  These short bands are dealt out in unit order,
+  // CTA c taking list entries [c*n/P, (c+1)*n/P).  The long bands (misses,
+  // old matches) are laid end to end and cut into CTA spans: the token
+  // count of all bands plus kPieceCost per short piece is split evenly over
+  // the CTAs, and each CTA's span is its share less its short pieces' cost.
+  // So neither a run of short bands nor a long band piles up on a CTA.
+  //
+  // Two parts, each by one warp: band_units_warp (band starts, the short
+  // list, long-band offsets) right after the decisions, so that the short
+  // pieces can start; band_spans_block (the long-band spans, their
+  // non-empty counts and every long unit's CTA run) by all consumer threads
+  // while the producer copies the short pieces.
+  static constexpr int kShortBand = 128;
+  static constexpr int kPieceCost = 384;  // fixed cost of a piece and its merge, in tokens
+  static constexpr int kSnap = 192;       // largest move of a long-band CTA boundary, in tokens
+  // On the long bands' cost axis each band starts with kLongPiece virtual
+  // tokens, a piece's fixed cost: a CTA whose span meets a band's start
+  // pays it, so a CTA with two pieces gets fewer tokens.  No CTA boundary
+  // falls inside that prefix or at its end (it moves to the band's start),
+  // so every non-empty span holds real tokens of each band it meets.
+  static constexpr int kLongPiece = 96;
+  __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
+    const int64_t n = seg_len(p, S, 1, u);
+    return n > 0 && n <= *S.short_max;
+  }
+  __device__ static void short_range(const Smem &S, int *j0, int *j1) {
+    const int ns = *S.n_short, c = blockIdx.x, P = gridDim.x;
+    *j0 = c * ns / P;
+    *j1 = (c + 1) * ns / P;
+  }
+  __device__ static Piece short_piece(const StepParams &p, const Smem &S, int j) {
+    Piece pc;
+    pc.sink = 0;
+    pc.u = S.shortU[j];
+    pc.lo = S.u_s[pc.u];
+    pc.hi = (int)(unit_len(p, S, pc.u) - p.r);
+    return pc;
+  }
+  __device__ static void band_units_warp(const StepParams &p, const Smem &S) {
+    const int U = p.B * p.Hkv, lane = threadIdx.x & 31, P = gridDim.x;
+    const bool decode = p.mode == MODE_DECODE;
+    // each unit's band start and length (a 32-bit count: m < 2^31), the
+    // length parked in shortU until the list overwrites it (entry j <= u,
+    // written after every lane of the chunk has read its own)
+    long long all = 0;
+#pragma unroll 1
+    for (int base = 0; base < U; base += 32) {
+      const int u = base + lane;
+      int len = 0;
+      if (u < U) {
+        if (decode) {
+          int st = 0x7fffffff;
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) {
+            const int pp = S.X[u * G + hh];  // head b*Hq + g*G + hh of unit u = b*Hkv + g
+            st = min(st, pp >= 1 ? max(pp - p.r + 1, p.sink_f + 1) : p.sink_f + 1);
+          }
+          S.u_s[u] = st;
+        }
+        len = (int)seg_len(p, S, 1, u);
+        S.shortU[u] = len;
+      }
+      // the chunk's sum from two 16-bit halves (no 32-bit overflow)
+      all += ((long long)__reduce_add_sync(kFull, (unsigned)len >> 16) << 16) +
+             __reduce_add_sync(kFull, (unsigned)len & 0xffffu);
+    }
+    int smax = kShortBand;  // max(all / P, kShortBand)
+    if (all >= (long long)(kShortBand + 1) * P) {
+      const long long q = all < 0x7fffffffLL ? (long long)((unsigned)all / (unsigned)P) : div_s64(all, P);
+      smax = q < 0x7fffffffLL ? (int)q : 0x7fffffff;
+    }
+    if (smax > kShortBand) {
+      int cnt = 0;
+#pragma unroll 1
+      for (int base = 0; base < U; base += 32) {
+        const int u = base + lane;
+        const int len = u < U ? S.shortU[u] : 0;
+        cnt += __popc(__ballot_sync(kFull, len > 0 && len <= smax));
+      }
+      if (cnt > P / 2) smax = kShortBand;
+    }
+    long long cb = 0, cc = 0;  // carries: long tokens, short costs
+    int ns = 0;
+#pragma unroll 1
+    for (int base = 0; base < U; base += 32) {
+      const int u = base + lane;
+      const int len = u < U ? S.shortU[u] : 0;
+      const bool sh = len > 0 && len <= smax;
+      long long x = sh || len == 0 ? 0 : kLongPiece + len, y = sh ? len + kPieceCost : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long x2 = __shfl_up_sync(kFull, x, o), y2 = __shfl_up_sync(kFull, y, o);
+        if (lane >= o) {
+          x += x2;
+          y += y2;
+        }
+      }
+      const unsigned bal = __ballot_sync(kFull, sh);
+      if (u < U) S.offB[u + 1] = cb + x;
+      if (sh) {
+        const int j = ns + __popc(bal & ((1u << lane) - 1u));
+        S.shortU[j] = u;
+        S.scp[j + 1] = cc + y;
+        S.runB[u] = make_short2(0, -1);
+      }
+      cb += __shfl_sync(kFull, x, 31);
+      cc += __shfl_sync(kFull, y, 31);
+      ns += __popc(bal);
+    }
+    if (lane == 0) {
+      S.offB[0] = 0;
+      S.scp[0] = 0;
+      *S.n_short = ns;
+      *S.short_max = smax;
+      S.band_tot[0] = cb;       // long-band cost (tokens + a piece's cost per band)
+      S.band_tot[1] = cb + cc;  // all cost
+    }
+    __syncwarp();
+  }
+
+  // Exclusive prefix count of one flag per consumer thread, in thread
+  // order, and the total (both to every thread), from the warps' ballots.
+  // It holds one consumer barrier; the caller's next consumer barrier must
+  // come before the next use of the warp totals.
+  __device__ static int flag_scan(const Smem &S, bool f, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned bal = __ballot_sync(kFull, f);
+    if (lane == 0) S.scan[warp] = __popc(bal);
+    consumer_sync();
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = (int)S.scan[w];
+      base += w < warp ? v : 0;
+      tot += v;
+    }
+    *total = tot;
+    return base + __popc(bal & ((1u << lane) - 1u));
+  }
+
+  // Exclusive scan of one value per consumer thread, in thread order, and
+  // the total (both returned to every thread).  All consumer threads call
+  // it; it holds two consumer barriers.
+  __device__ static long long block_scan(const Smem &S, long long x, long long *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(kFull, xi, o);
+      if (lane >= o) xi += y;
+    }
+    if (lane == 31) S.scan[warp] = xi;
+    consumer_sync();
+    long long base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const long long v = S.scan[w];
+      base += w < warp ? v : 0;
+      tot += v;
+    }
+    consumer_sync();
+    *total = tot;
+    return base + xi - x;
+  }
+
+  // The long-band spans (CTA c = consumer thread c), by all consumer threads
+  // (ends with a consumer barrier).
+  __device__ static void band_spans_block(const StepParams &p, const Smem &S) {
+    const int c = threadIdx.x, P = gridDim.x;
+    const int ns = *S.n_short;
+    const long long tb = S.band_tot[0], tv = S.band_tot[1];
+    // the long bands use the first Pl CTAs, each with at least kMinSpan
+    // tokens of the cost axis (slivers cost a whole piece and a bigger merge)
+    const long long want = (tv + kMinSpan - 1) / kMinSpan;
+    const int Pl = want < P ? (int)(want > 0 ? want : 1) : P;
+    long long cap = 0, tot;
+    if (c < Pl) {
+      const int j0 = c * ns / P, j1 = (c + 1) * ns / P;
+      cap = part_of(c + 1, tv, Pl) - part_of(c, tv, Pl) - (S.scp[j1] - S.scp[j0]);
+      cap = cap > 0 ? cap : 0;
+    }
+    long long st = block_scan(S, cap, &tot);
+    st = st < tb ? st : tb;
+    // a CTA boundary within kSnap tokens (and half a share) of a long
+    // unit's boundary moves onto it: the CTAs on either side then hold one
+    // piece each instead of one of them two, a piece's fixed cost being
+    // worth more than the imbalance.  Moving every boundary to its nearest
+    // unit boundary, when near enough, keeps the boundaries in order.
+    if (c > 0 && c < P && st > 0 && st < tb) {
+      const long long share2 = part_of(1, tv, 2 * Pl), half = share2 < kSnap ? share2 : kSnap;
+      const int u = unit_of(S.offB, p.B * p.Hkv, st);
+      const long long lo = S.offB[u], hi = S.offB[u + 1];
+      if (st - lo <= kLongPiece) {
+        st = lo;  // inside or at the end of the band's cost prefix
+      } else if (st - lo <= hi - st) {
+        if (st - lo <= half) st = lo;
+      } else if (hi - st <= half) {
+        st = hi;
+      }
+    }
+    if (c < P) S.spanB[c] = st;
+    if (c == 0) S.spanB[P] = tb;
+    consumer_sync();
+  }
+
+  // The long-band spans' non-empty counts and every long unit's CTA run, by
+  // all consumer threads (ends with a consumer barrier): only the merges
+  // read them, so they are made while the first band tiles are in flight.
+  __device__ static void band_runs_block(const StepParams &p, const Smem &S) {
+    const int U = p.B * p.Hkv, c = threadIdx.x, P = gridDim.x;
+    int tot;
+    const int ef = flag_scan(S, c < P && S.spanB[c] < S.spanB[c + 1], &tot);
+    if (c < P) S.neB[c] = ef;
+    if (c == 0) S.neB[P] = tot;
+#pragma unroll 1
+    for (int u = c; u < U; u += kConsumers)
+      if (!short_band(p, S, u)) S.runB[u] = find_run(S, 1, u);
+    consumer_sync();
+  }
+
+  // ---------------------------------------------------------------------
+  // producer
+  // ---------------------------------------------------------------------
+
+  // The G pre-RoPE query rows of unit u's heads into stage st's side buffer.
+  __device__ static void copy_q(const StepParams &p, const Smem &S, int st, int u, uint32_t bar) {
+    const uint8_t *q = (const uint8_t *)p.q;
+    const int b = u / p.Hkv, g = u % p.Hkv;
+    const int64_t bh0 = (int64_t)b * p.Hq + g * G;
+    if (p.q_stride == kHeadDim && p.q_offset == 0) {  // the group's G rows are contiguous
+      bulk_g2s(smem_addr(S.qbuf + (size_t)st * kAux), q + (size_t)bh0 * kRowBytes, kQBytes, bar);
+    } else {
+      for (int hh = 0; hh < G; ++hh)
+        bulk_g2s(smem_addr(S.qbuf + (size_t)st * kAux + hh * kRowBytes),
+                 q + (size_t)((bh0 + hh) * p.q_stride + p.q_offset) * sizeof(T), kRowBytes, bar);
+    }
+  }
+
+  // Paged tile `t` of piece pc with its page ids already loaded (kNoPage past
+  // the table): the rows of each 16-token page that fall in the piece, page
+  // by page; an id outside the pool is refused and reported.
+  static constexpr int32_t kNoPage = (int32_t)0x80000000;
+  __device__ static void issue_paged_tile(const StepParams &p, const Smem &S, int st, const Piece &pc, int t,
+                                          bool with_q, const int32_t *ids) {
+    constexpr int kPg = kTileTok / 16;
+    const int g = pc.u % p.Hkv;
+    uint8_t *kbuf = S.stage + (size_t)st * kStageBytes;
+    const uint32_t bar = smem_addr(&S.full[st]);
+    const int tb = t * kTileTok;
+    uint32_t bytes = with_q ? (uint32_t)kQBytes : 0u;
+    int msk = 0;
+#pragma unroll
+    for (int pg = 0; pg < kPg; ++pg) {
+      const int pa = tb + pg * 16 + 1, ra = pa > pc.lo ? pa : pc.lo, rz = pa + 15 < pc.hi ? pa + 15 : pc.hi;
+      if (ra > rz || ids[pg] == kNoPage) continue;  // (past the table: nothing to copy)
+      if (ids[pg] < 0 || ids[pg] >= p.kv.n_pages) {
+        set_status(p.ctl, MAC_DEV_BAD_PAGE);
+        continue;
+      }
+      msk |= 1 << pg;
+      bytes += 2u * (uint32_t)(rz - ra + 1) * kRowBytes;
+    }
+    S.mask[st] = msk;
+    if (bytes == 0) {
       mbar_arrive(bar);
       return;
     }
-    mbar_expect_tx(bar, bytes + qb);
-    if (qb) issue_query(p, R, d, bar);
-    if (bytes == 0) return;
-    if (!PAGED) {
-      const size_t off = ((size_t)d.u * (size_t)p.kv.capacity + (size_t)(d.a - 1)) * kRow;
-      const uint32_t nb = (uint32_t)d.cnt * kRow;
-      if (d.keep) {
-        bulk_g2s(smem_addr(buf), (const uint8_t *)p.kv.k + off, nb, bar);
-        bulk_g2s(smem_addr(buf + kStageBytes / 2), (const uint8_t *)p.kv.v + off, nb, bar);
-      } else {
-        const unsigned long long pol = l2_evict_first_policy();
-        bulk_g2s_hint(smem_addr(buf), (const uint8_t *)p.kv.k + off, nb, bar, pol);
-        bulk_g2s_hint(smem_addr(buf + kStageBytes / 2), (const uint8_t *)p.kv.v + off, nb, bar, pol);
-      }
-      return;
-    }
+    mbar_expect_tx(bar, bytes);
+    if (with_q) copy_q(p, S, st, pc.u, bar);
     const unsigned long long pol = l2_evict_first_policy();
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      const int cnt = s ? d.cnt - n0 : n0;
-      if (cnt <= 0 || !((msk >> (s ? n0 : 0)) & 1)) continue;
-      const int t0 = s ? d.a + n0 : d.a;  // first token of the segment
-      const size_t off = (((size_t)id[s] * p.Hkv + g) * 16 + (size_t)((t0 - 1) & 15)) * kRow;
-      uint8_t *dst = buf + (size_t)(t0 - d.a) * kRow;
-      bulk_g2s_hint(smem_addr(dst), (const uint8_t *)p.kv.k + off, (uint32_t)cnt * kRow, bar, pol);
-      bulk_g2s_hint(smem_addr(dst + kStageBytes / 2), (const uint8_t *)p.kv.v + off, (uint32_t)cnt * kRow, bar,
-                    pol);
+    for (int pg = 0; pg < kPg; ++pg) {
+      if (!((msk >> pg) & 1)) continue;
+      const int pa = tb + pg * 16 + 1, ra = pa > pc.lo ? pa : pc.lo, rz = pa + 15 < pc.hi ? pa + 15 : pc.hi;
+      const size_t off = (((size_t)ids[pg] * p.Hkv + g) * 16 + (size_t)(ra - pa)) * kRowBytes;
+      const uint32_t nb = (uint32_t)(rz - ra + 1) * kRowBytes;
+      uint8_t *dst = kbuf + (size_t)(ra - tb - 1) * kRowBytes;
+      bulk_g2s_hint(smem_addr(dst), (const uint8_t *)p.kv.k + off, nb, bar, pol);
+      bulk_g2s_hint(smem_addr(dst + kStageBytes / 2), (const uint8_t *)p.kv.v + off, nb, bar, pol);
     }
   }
 
-  // Wait for stage use n to land (bounded).
-  __device__ static bool wait_stage(const StepParams &p, const Smem &S, const Ring &R, uint32_t n) {
-    const bool ok = mbar_wait_bounded(stage_bar(R, n), (n / kStages) & 1u, S.abort);
+  // Rows of K/V tile `tile` (tokens tile*kTileTok+1 .. +kTileTok) that fall in
+  // [lo, hi], each copied to its own row of the stage, so no byte outside the
+  // piece is read; with_q also brings the unit's G pre-RoPE query rows.
+  __device__ static void issue_tile(const StepParams &p, const Smem &S, int st, int u, int lo,
+                                    int hi, int64_t tile, bool with_q) {
+    if (u < 0 || u >= p.B * p.Hkv) {
+      set_status(p.ctl, MAC_DEV_BAD_COPY);
+      S.mask[st] = 0;
+      mbar_arrive(smem_addr(&S.full[st]));
+      return;
+    }
+    const int b = u / p.Hkv, g = u % p.Hkv;
+    uint8_t *kbuf = S.stage + (size_t)st * kStageBytes;
+    uint8_t *vbuf = kbuf + kStageBytes / 2;
+    const uint32_t bar = smem_addr(&S.full[st]);
+    const int64_t t0 = tile * kTileTok;
+    uint32_t bytes = with_q ? (uint32_t)kQBytes : 0u;
+    int msk = 0;
+    int64_t ra[kTileTok / 16], rz[kTileTok / 16];
+    int32_t pid[kTileTok / 16];
+    if (!PAGED) {
+      msk = (1 << (kTileTok / 16)) - 1;
+      ra[0] = t0 + 1 > lo ? t0 + 1 : lo;
+      rz[0] = t0 + kTileTok < hi ? t0 + kTileTok : hi;
+      // the schedule only issues tiles that meet [lo, hi] inside the cache;
+      // anything else is refused rather than copied
+      if (ra[0] > rz[0] || ra[0] < 1 || rz[0] > p.kv.capacity || u < 0 || u >= p.B * p.Hkv) {
+        set_status(p.ctl, MAC_DEV_BAD_COPY);
+        msk = 0;
+        with_q = false;
+        bytes = 0;
+      } else {
+        bytes += 2u * (uint32_t)(rz[0] - ra[0] + 1) * kRowBytes;
+      }
+    } else {
+      for (int pg = 0; pg < kTileTok / 16; ++pg) {
+        const int64_t slot = tile * (kTileTok / 16) + pg;
+        const int64_t pa = t0 + pg * 16 + 1, pz = pa + 15;
+        ra[pg] = pa > lo ? pa : lo;
+        rz[pg] = pz < hi ? pz : hi;
+        pid[pg] = -1;
+        if (ra[pg] > rz[pg] || slot >= p.kv.max_pages) continue;
+        const int32_t id = p.kv.page_table[(int64_t)b * p.kv.max_pages + slot];
+        if (id < 0 || id >= p.kv.n_pages) {
+          set_status(p.ctl, MAC_DEV_BAD_PAGE);
+          continue;
+        }
+        pid[pg] = id;
+        msk |= 1 << pg;
+        bytes += 2u * (uint32_t)(rz[pg] - ra[pg] + 1) * kRowBytes;
+      }
+    }
+    S.mask[st] = msk;
+    if (bytes == 0) {
+      mbar_arrive(bar);
+      return;
+    }
+    mbar_expect_tx(bar, bytes);
+    if (with_q) copy_q(p, S, st, u, bar);
+    const unsigned long long pol = l2_evict_first_policy();
+    if (!PAGED) {
+      if (msk == 0) return;
+      const size_t off = (((size_t)b * p.Hkv + g) * (size_t)p.kv.capacity + (size_t)(ra[0] - 1)) * kRowBytes;
+      const uint32_t n = (uint32_t)(rz[0] - ra[0] + 1) * kRowBytes;
+      const uint32_t dst = (uint32_t)(ra[0] - t0 - 1) * kRowBytes;
+      bulk_g2s_hint(smem_addr(kbuf + dst), (const uint8_t *)p.kv.k + off, n, bar, pol);
+      bulk_g2s_hint(smem_addr(vbuf + dst), (const uint8_t *)p.kv.v + off, n, bar, pol);
+    } else {
+      for (int pg = 0; pg < kTileTok / 16; ++pg) {
+        if (pid[pg] < 0) continue;
+        const size_t off = (((size_t)pid[pg] * p.Hkv + g) * 16 + (size_t)((ra[pg] - 1) % 16)) * kRowBytes;
+        const uint32_t n = (uint32_t)(rz[pg] - ra[pg] + 1) * kRowBytes;
+        const uint32_t dst = (uint32_t)(ra[pg] - t0 - 1) * kRowBytes;
+        bulk_g2s_hint(smem_addr(kbuf + dst), (const uint8_t *)p.kv.k + off, n, bar, pol);
+        bulk_g2s_hint(smem_addr(vbuf + dst), (const uint8_t *)p.kv.v + off, n, bar, pol);
+      }
+    }
+  }
+
+  // Match chunk j: head j / cph, rows [(j % cph) * kMatchRows, +rows) of its
+  // ring, cph = chunks per head (chunks never cross heads).
+  __device__ static int chunks_per_head(int K) { return (K + kMatchRows - 1) / kMatchRows; }
+
+  // Bounded spin of the producer lane on a shared flag set by a consumer.
+  __device__ static bool wait_ready(const StepParams &p, const Smem &S, int level) {
+    const long long t0 = clock64();
+    while (*S.ready < level) {
+      if (*S.abort) return false;
+      if (clock64() - t0 > (1LL << 31)) {
+        set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
+        *S.abort = 1;
+        return false;
+      }
+      __nanosleep(64);  // leave the issue slots to the warp doing the work
+    }
+    __threadfence_block();
+    return true;
+  }
+
+  // Producer lane: wait for stage use n to be free, then arm its full barrier.
+  __device__ static bool acquire_stage(const StepParams &p, const Smem &S, uint32_t n) {
+    if (!mbar_wait_bounded(smem_addr(&S.empty[n % kStages]), ((n / kStages) & 1u) ^ 1u, S.abort)) {
+      if (!*S.abort) set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
+      *S.abort = 1;
+      return false;
+    }
+    return true;
+  }
+
+  // The tiles of one piece, from stage use n on; returns the next use.
+  __device__ static uint32_t copy_piece(const StepParams &p, const Smem &S, const Piece &pc, uint32_t n) {
+    const int t0 = (pc.lo - 1) / kTileTok, t1 = (pc.hi - 1) / kTileTok;
+    if (pc.u < 0 || pc.u >= p.B * p.Hkv || pc.lo < 1 || pc.hi < pc.lo || (!PAGED && pc.hi > p.kv.capacity)) {
+      // a piece outside the cache is refused tile by tile
+#pragma unroll 1
+      for (int t = t0; t <= t1; ++t, ++n) {
+        if (!acquire_stage(p, S, n)) break;
+        issue_tile(p, S, n % kStages, pc.u, pc.lo, pc.hi, t, t == t0);
+      }
+      return n;
+    }
+    if (PAGED) {
+      // a table lookup per 16 rows: the next tile's page ids are loaded
+      // (independent loads) before the wait for its stage
+      constexpr int kPg = kTileTok / 16;
+      const int32_t *row = p.kv.page_table + (int64_t)(pc.u / p.Hkv) * p.kv.max_pages;
+      int32_t ids[kPg], nxt[kPg];
+#pragma unroll
+      for (int pg = 0; pg < kPg; ++pg) {
+        const int64_t slot = (int64_t)t0 * kPg + pg;
+        ids[pg] = slot < p.kv.max_pages ? __ldg(row + slot) : kNoPage;
+      }
+#pragma unroll 1
+      for (int t = t0; t <= t1; ++t, ++n) {
+#pragma unroll
+        for (int pg = 0; pg < kPg; ++pg) {
+          const int64_t slot = (int64_t)(t + 1) * kPg + pg;
+          nxt[pg] = t < t1 && slot < p.kv.max_pages ? __ldg(row + slot) : kNoPage;
+        }
+        if (!acquire_stage(p, S, n)) break;
+        issue_paged_tile(p, S, n % kStages, pc, t, t == t0, ids);
+#pragma unroll
+        for (int pg = 0; pg < kPg; ++pg) ids[pg] = nxt[pg];
+      }
+      return n;
+    }
+    // contiguous cache, a piece inside it: checked once, then each tile is
+    // two row ranges (the unit's K and V rows are contiguous)
+    const size_t unit_off = (size_t)pc.u * (size_t)p.kv.capacity * kRowBytes;
+    const uint8_t *kg = (const uint8_t *)p.kv.k + unit_off, *vg = (const uint8_t *)p.kv.v + unit_off;
+    const unsigned long long pol = l2_evict_first_policy();
+#pragma unroll 1
+    for (int t = t0; t <= t1; ++t, ++n) {
+      if (!acquire_stage(p, S, n)) break;
+      const int st = n % kStages;
+      const int ra = t * kTileTok + 1 > pc.lo ? t * kTileTok + 1 : pc.lo;
+      const int rz = t * kTileTok + kTileTok < pc.hi ? t * kTileTok + kTileTok : pc.hi;
+      const uint32_t nb = (uint32_t)(rz - ra + 1) * kRowBytes;
+      const uint32_t bar = smem_addr(&S.full[st]);
+      S.mask[st] = (1 << (kTileTok / 16)) - 1;
+      mbar_expect_tx(bar, 2u * nb + (t == t0 ? (uint32_t)kQBytes : 0u));
+      if (t == t0) copy_q(p, S, st, pc.u, bar);
+      uint8_t *kbuf = S.stage + (size_t)st * kStageBytes + (size_t)(ra - t * kTileTok - 1) * kRowBytes;
+      bulk_g2s_hint(smem_addr(kbuf), kg + (size_t)(ra - 1) * kRowBytes, nb, bar, pol);
+      bulk_g2s_hint(smem_addr(kbuf + kStageBytes / 2), vg + (size_t)(ra - 1) * kRowBytes, nb, bar, pol);
+    }
+    return n;
+  }
+
+  // Match chunks i0 .. i1-1 of this CTA (chunk i is j = c + i*P) into stage
+  // uses n, n+1, ...; returns the next use.
+  __device__ static uint32_t copy_match(const StepParams &p, const Smem &S, uint32_t n, int i0, int i1) {
+    const int P = gridDim.x;
+    const int cph = chunks_per_head(p.K);
+    const unsigned long long pol = l2_evict_first_policy();
+#pragma unroll 1
+    for (int i = i0; i < i1; ++i, ++n) {
+      if (!acquire_stage(p, S, n)) break;
+      const int j = blockIdx.x + i * P;
+      const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
+      const int rows = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
+      const int st = n % kStages;
+      const uint32_t bar = smem_addr(&S.full[st]);
+      const bool pos_copy = pos_by_copy(p);
+      uint8_t *side = S.qbuf + (size_t)st * kAux;
+      // the chunk's coordinates (plain store, ordered before the consumers'
+      // wait by the arrive below), then the head's query row and the
+      // chunk's ring positions, into the side buffer
+      *reinterpret_cast<int4 *>(side + kInfoOff) = make_int4(bh, slot0, rows, bh / p.Hq);
+      mbar_expect_tx(bar, (uint32_t)rows * kRowBytes + kRowBytes + (pos_copy ? 4u * rows : 0u));
+      bulk_g2s_hint(smem_addr(S.stage + (size_t)st * kStageBytes),
+                    (const uint8_t *)p.ring_q + ((size_t)bh * p.K + slot0) * kRowBytes,
+                    (uint32_t)rows * kRowBytes, bar, pol);
+      bulk_g2s(smem_addr(side), (const uint8_t *)p.q + (size_t)((int64_t)bh * p.q_stride + p.q_offset) * sizeof(T),
+               kRowBytes, bar);
+      if (pos_copy)
+        bulk_g2s(smem_addr(side + kRowBytes), p.ring_pos + (size_t)(bh / p.Hq) * p.K + slot0, 4u * rows, bar);
+    }
+    return n;
+  }
+  // Ring positions come with the chunk when their rows are 16-byte aligned.
+  __device__ static bool pos_by_copy(const StepParams &p) { return (p.K & 3) == 0; }
+
+  // The producer warp: a copy engine.  Its first lane starts the first match
+  // copies (they need nothing but the parameters), then copies the tail
+  // tiles and the rest of the match chunks once the consumers publish the
+  // unit positions and the tail layout, the short pieces once they publish
+  // the short-band list, and the long-band pieces once they publish the
+  // long-band spans.  Every copy goes in the order the consumers use the
+  // stages: kEarlyChunks match chunks, tail pieces, the other match chunks,
+  // short pieces, long-band pieces.
+  __device__ static void producer_warp(const StepParams &p, const Smem &S) {
+    const int lane = threadIdx.x & 31, U = p.B * p.Hkv;
+    unsigned long long *tr = lane == 0 ? cta_trace(p) : nullptr;
+    const bool decode = p.mode == MODE_DECODE;
+    uint32_t n = 0;
+    const int nchunks = decode ? match_chunks(p) : 0;
+    const int early = nchunks < kEarlyChunks ? nchunks : kEarlyChunks;
+    if (lane == 0) {
+      n = copy_match(p, S, 0, 0, early);
+      if (tr) tr[30] = globaltimer();
+      if (!wait_ready(p, S, 1)) *S.abort = 1;  // unit positions and tail layout
+      if (tr) tr[31] = globaltimer();
+    }
+    __syncwarp();
+    if (decode && !PAGED) {
+      // the tile a recent match's band needs (a hit at m-1 starts it at
+      // m-r) into L2 while the match runs, for the units u = c mod P
+#pragma unroll 1
+      for (int u = blockIdx.x + lane * (int)gridDim.x; u < U; u += 32 * (int)gridDim.x) {
+        const int64_t m = unit_len(p, S, u), hi = m - p.r;
+        if (!len_ok(p, m) || hi < 1 || hi > p.kv.capacity) continue;
+        const int64_t lo = hi - kTileTok + 1 > 1 ? hi - kTileTok + 1 : 1;
+        const size_t off = ((size_t)u * (size_t)p.kv.capacity + (size_t)(lo - 1)) * kRowBytes;
+        const uint32_t bytes = (uint32_t)(hi - lo + 1) * kRowBytes;
+        bulk_prefetch_l2((const uint8_t *)p.kv.k + off, bytes);
+        bulk_prefetch_l2((const uint8_t *)p.kv.v + off, bytes);
+      }
+    }
+    if (lane == 0) {
+      // tails (the unit layout is known), the rest of the match, then the
+      // short bands and the long bands as their layouts are published
+#pragma unroll 1
+      for (int kind = 0; kind < 3 && !*S.abort; ++kind) {
+        if (kind == 1) {
+          n = copy_match(p, S, n, early, nchunks);
+          if (!wait_ready(p, S, 2)) break;
+          if (tr) tr[26] = globaltimer();
+        } else if (kind == 2) {
+          if (tr) tr[9] = globaltimer();
+          if (!wait_ready(p, S, 3)) break;
+          if (tr) tr[27] = globaltimer();
+        }
+        PieceIter I = piece_iter(p, S, kind);
+        Piece pc;
+        while (!*S.abort && next_piece(p, S, I, pc)) n = copy_piece(p, S, pc, n);
+      }
+      __threadfence_block();
+      *S.issued = n;
+    }
+    __syncwarp();
+    if (decode && !*S.abort) copy_step_queries(p, S);
+  }
+
+  // The step's queries, rows bh = c + i P: into ring slot pos mod K (the
+  // fused append; the final merge writes the slot's summary), or into the
+  // ring workspace's staging area for the append kernel, so that the caller
+  // may reuse its query buffer right away.  By the producer warp once its
+  // copies are issued: the grid barrier (before the band layout it waited
+  // for) ordered every match's ring reads before these writes.
+  __device__ static void copy_step_queries(const StepParams &p, const Smem &S) {
+    const int lane = threadIdx.x & 31;
+    constexpr int kChunks = kHeadDim / kPer;  // 16-byte pieces of a row
+#pragma unroll 1
+    for (int bh = blockIdx.x; bh < p.B * p.Hq; bh += gridDim.x) {
+      const int b = bh / p.Hq, u = b * p.Hkv + (bh - b * p.Hq) / G;
+      const int pos = S.u_pos[u];
+      const bool app = p.app_o && len_ok(p, pos);
+      if (lane < kChunks && (app || !p.app_o)) {
+        const uint4 qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + lane];
+        if (app)
+          reinterpret_cast<uint4 *>(p.app_q)[((int64_t)bh * p.K + pos % p.K) * kChunks + lane] = qv;
+        else
+          reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * kChunks + lane] = qv;
+      }
+    }
+  }
+
+  // Consumer side of stage use n.
+  __device__ static bool wait_use(const StepParams &p, const Smem &S, uint32_t n) {
+    const bool ok = mbar_wait_bounded(smem_addr(&S.full[n % kStages]), (n / kStages) & 1u, S.abort);
     if (!ok && !*S.abort) {
       set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
       *S.abort = 1;
     }
     return ok;
   }
-  // The warp is done reading its oldest stage: its buffer may be refilled.
-  __device__ static void done_with_stage() {
+  __device__ static void release(const Smem &S, uint32_t n) {
     __syncwarp();
-    fence_proxy_async();
-  }
-  // Before the CTA exits: the copies this warp issued have landed (bounded).
-  __device__ static void drain(const Ring &R) {
-    for (uint32_t n = R.used; n < R.issued; ++n) {
-      const long long t0 = clock64();
-      while (!mbar_try_wait(stage_bar(R, n), (n / kStages) & 1u) && clock64() - t0 < (1LL << 30)) {
-      }
-    }
+    if ((threadIdx.x & 31) == 0) mbar_arrive(smem_addr(&S.empty[n % kStages]));
   }
 
   // ---------------------------------------------------------------------
-  // attention of a stage
+  // phase M
   // ---------------------------------------------------------------------
-  struct Att {
-    float2 o[G][kAPairs];
-    float mrun[G];
-    float m_mine, l_mine;
-  };
-  __device__ static void att_init(Att &A) {
+
+  // The lane's part of the squared L2 distance between the query and a row:
+  // exact differences of its 16 elements (bf16), squares and a pairwise tree
+  // (the 8 lanes of the group are summed by the caller).
+  __device__ static float lane_dist(const uint8_t *row, int sub, const float2 *qv) {
+    float2 df[kPairs];
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      A.mrun[hh] = kMInit;
+    for (int c = 0; c < kNP; ++c) {
+      float2 e2[kPer / 2];
+      unpack16x2<T>(*reinterpret_cast<const uint4 *>(row + c * 128 + sub * 16), e2);
 #pragma unroll
-      for (int i = 0; i < kAPairs; ++i) A.o[hh][i] = make_float2(0.f, 0.f);
+      for (int k = 0; k < kPer / 2; ++k) {
+        const float2 q = qv[c * (kPer / 2) + k];
+        df[c * (kPer / 2) + k] = __fadd2_rn(q, make_float2(-e2[k].x, -e2[k].y));
+      }
     }
-    A.m_mine = kMInit;
-    A.l_mine = 0.f;
+    float2 t[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) t[k] = __ffma2_rn(df[k + 4], df[k + 4], __fmul2_rn(df[k], df[k]));
+    t[0] = __fadd2_rn(t[0], t[2]);
+    t[1] = __fadd2_rn(t[1], t[3]);
+    t[0] = __fadd2_rn(t[0], t[1]);
+    return __fadd_rn(t[0].x, t[0].y);
+  }
+
+  // The warp's best (distance, position) joins head bh's global minimum.
+  // Scan the match chunk of stage use n: its rows, the head's query row, the
+  // chunk's coordinates and (K a multiple of 4) the rows' positions all
+  // arrive in the stage.  Each lane sums (a-b)^2 of its 16 elements of the
+  // group's kRPG rows; a reduce-scatter over the group's 8 lanes (xor 4, 2,
+  // then 1) leaves lanes 2k, 2k+1 with row k's distance (three pairwise
+  // levels, as in row_dist); the warp's best then joins the head's minimum.
+  __device__ static void match_chunk(const StepParams &p, const Smem &S, uint32_t n, int j, int grp, int sub,
+                                     unsigned long long &wait_ns) {
+    static_assert(kRPG == 4 || kRPG == 2, "rows per lane group");
+    const bool pos_copy = pos_by_copy(p);
+    const int kk = (sub >> (3 - kLogRPG)) & (kRPG - 1);  // the row this lane finishes
+    const int i_mine = grp + 32 * kk;
+    int pk_mine = 0;
+    if (!pos_copy) {  // positions from global memory, before the wait
+      const int cph = chunks_per_head(p.K);
+      const int slot0 = (j % cph) * kMatchRows, cnt = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
+      pk_mine = __ldg(p.ring_pos + (int64_t)((j / cph) / p.Hq) * p.K + slot0 + (i_mine < cnt ? i_mine : cnt - 1));
+    }
+    const bool timed = threadIdx.x == 0 && p.trace;
+    const unsigned long long tw = timed ? globaltimer() : 0ull;
+    const bool ok = wait_use(p, S, n);
+    if (timed) wait_ns += globaltimer() - tw;
+    if (n == 0) stamp(cta_trace(p), 8);
+    const int st = n % kStages;
+    const uint8_t *rows = S.stage + (size_t)st * kStageBytes;
+    const uint8_t *side = S.qbuf + (size_t)st * kAux;
+    const int4 info = *reinterpret_cast<const int4 *>(side + kInfoOff);  // bh, slot0, rows, b
+    const int bh = info.x, cnt = info.z;
+    float2 qv[kPairs];
+#pragma unroll
+    for (int cc = 0; cc < kNP; ++cc)
+      unpack16x2<T>(*reinterpret_cast<const uint4 *>(side + cc * 128 + sub * 16), qv + cc * (kPer / 2));
+    if (pos_copy) pk_mine = reinterpret_cast<const int32_t *>(side + kRowBytes)[i_mine < cnt ? i_mine : cnt - 1];
+    const int64_t m = S.X[info.w];  // the request's length, tabled before the match
+    // the lane's partial sums of the group's rows (rows past the chunk read
+    // stale stage bytes and are discarded below)
+    float v[kRPG];
+#pragma unroll
+    for (int k = 0; k < kRPG; ++k) {
+      const int i = grp + 32 * k;
+      v[k] = lane_dist(rows + (size_t)(i < cnt ? i : cnt - 1) * kRowBytes, sub, qv);
+    }
+    // reduce-scatter: level xor 4 keeps half the rows, xor 2 (kRPG == 4)
+    // the next half, xor 1 finishes the sum
+#pragma unroll
+    for (int lev = 0; lev < kLogRPG; ++lev) {
+      const int off = 4 >> lev;
+      const bool up = (threadIdx.x & off) != 0;
+      const int half = kRPG >> (lev + 1);
+#pragma unroll
+      for (int i = 0; i < kRPG / 2; ++i) {
+        if (i < half) {
+          const float send = up ? v[i] : v[i + half];
+          const float keep = up ? v[i + half] : v[i];
+          v[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, off));
+        }
+      }
+    }
+    float D = v[0];
+#pragma unroll
+    for (int lev = kLogRPG; lev < 3; ++lev) D = __fadd_rn(D, __shfl_xor_sync(kFull, D, 4 >> lev));
+    int pos_lo = 1, pos_hi = 0;
+    if (len_ok(p, m)) {
+      pos_lo = m - p.K > 1 ? (int)(m - p.K) : 1;
+      pos_hi = (int)(m - 1);
+    }
+    const bool valid = ok && i_mine < cnt && pk_mine >= pos_lo && pk_mine <= pos_hi;
+    int bp = valid ? pk_mine : -1;
+    D = valid ? D : INFINITY;
+    release(S, n);
+    // the warp's best: lanes 2k and 2k+1 agree, so xor 2 and up
+#pragma unroll
+    for (int off = 8 / kRPG; off <= 16; off <<= 1) {
+      const float d2 = __shfl_xor_sync(kFull, D, off);
+      const int p2 = __shfl_xor_sync(kFull, bp, off);
+      if (better(d2, p2, D, bp)) {
+        D = d2;
+        bp = p2;
+      }
+    }
+    if ((threadIdx.x & 31) == 0 && bp >= 1) atomicMax(&S.best[bh], pack_best(D, bp));
+  }
+
+  // Match chunks i0 .. i1-1 of this CTA (chunk i is j = c + i*P), from stage
+  // use n on.
+  __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n, int i0, int i1) {
+    const int P = gridDim.x;
+    const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31, sub = lane & 7;
+    const int grp = warp * 4 + (lane >> 3);  // row group: rows grp, grp + 32, ... of a chunk
+    unsigned long long wait_ns = 0;
+#pragma unroll 1
+    for (int i = i0; i < i1; ++i) match_chunk(p, S, n++, blockIdx.x + i * P, grp, sub, wait_ns);
+    unsigned long long *tr = threadIdx.x == 0 ? cta_trace(p) : nullptr;
+    if (tr) {
+      tr[28] += wait_ns;
+      tr[29] += (unsigned long long)(i1 > i0 ? i1 - i0 : 0);
+    }
+  }
+
+  // Match chunks of this CTA, and how many come before its tail pieces.
+  __device__ static int match_chunks(const StepParams &p) {
+    const int nc = p.B * p.Hq * chunks_per_head(p.K), P = gridDim.x, c = blockIdx.x;
+    return c < nc ? (nc - c + P - 1) / P : 0;
+  }
+  static constexpr int kEarlyChunks = 4;
+
+  // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.  One
+  // thread per CTA polls without sleeping: the last arrival is seen one L2
+  // round trip after it lands.
+  __device__ static void grid_barrier(const StepParams &p, const Smem &S) {
+    if (threadIdx.x == 0) {
+      unsigned long long *ctr = reinterpret_cast<unsigned long long *>(p.ctl + 2);
+      const unsigned long long old = atom_add_release_u64(ctr, 1ull);
+      const unsigned long long target = old - old % gridDim.x + gridDim.x;
+      const long long t0 = clock64();
+      while (ld_acquire_u64(ctr) < target) {
+        if (clock64() - t0 > (1LL << 31)) {
+          set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
+          *S.abort = 1;
+          break;
+        }
+      }
+    }
+    consumer_sync();
+  }
+
+  // Decisions of every head from the combined minima (one head per consumer
+  // thread); the cached summaries of the hits are asked into L2 for the
+  // merges; then, by warp 0, every unit's band start and the short-band list
+  // (every CTA computes the same), after which the producer may copy short
+  // pieces and lay out the long bands.  Ends with a consumer barrier.
+  __device__ static void decide(const StepParams &p, const Smem &S, unsigned long long *trace) {
+    const int tid = threadIdx.x, n_bh = p.B * p.Hq;
+#pragma unroll 1
+    for (int bh = tid; bh < n_bh; bh += kConsumers) {
+      const int b = bh / p.Hq, u = b * p.Hkv + (bh % p.Hq) / G;
+      const int64_t m = unit_len(p, S, u);
+      const unsigned long long inv = __ldcg(&S.best[bh]);
+      int pos = -1;
+      if (inv != 0ull && len_ok(p, m) && m >= p.min_context) {
+        const unsigned long long key = ~inv;
+        const float d = __uint_as_float((uint32_t)(key >> 32));
+        if (d < p.thr2) pos = (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+      }
+      S.X[bh] = pos;
+      if (blockIdx.x == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
+      if (pos >= 1 && bh % gridDim.x == blockIdx.x) {
+        const int64_t slot = (int64_t)bh * p.K + pos % p.K;
+        for (int k = 0; k < kHeadDim * 4; k += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(p.ring_o + slot * kHeadDim + k / 4));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.ring_lse + slot));
+      }
+    }
+    consumer_sync();
+    stamp(trace, 5);
+  }
+
+  // Every unit's band start and the short-band list (warp 0), after which
+  // the producer may copy short pieces, then the long-band spans (all
+  // consumer threads), after which it may copy long-band pieces.  Ends with
+  // a consumer barrier.
+  __device__ static void layout_bands(const StepParams &p, const Smem &S, unsigned long long *trace) {
+    if (threadIdx.x < 32) {
+      band_units_warp(p, S);
+      __threadfence_block();
+      if (threadIdx.x == 0) *S.ready = 2;
+      __syncwarp();
+    }
+    consumer_sync();
+    band_spans_block(p, S);
+    if (threadIdx.x == 0) {
+      __threadfence_block();
+      *S.ready = 3;
+    }
+    band_runs_block(p, S);
+    (void)trace;
+  }
+
+  // ---------------------------------------------------------------------
+  // attention over the CTA's pieces
+  // ---------------------------------------------------------------------
+
+
+  // cos, sin of rotation angle j of request b at position pos: from the
+  // CTA's table when there is one, else computed here.
+  __device__ static float2 rope_cs(const StepParams &p, const Smem &S, int b, int64_t pos, int j) {
+    if (S.rope) return S.rope[b * (kHeadDim / 2) + j];
+    float c, sn;
+    rope_angle(pos, p.rope_f[j], &c, &sn);
+    return make_float2(c, sn);
+  }
+
+  __device__ static void rotate_pair(float a, float b, float2 cs, float scale, float *ra, float *rb) {
+    *ra = __fmul_rn(__fsub_rn(__fmul_rn(a, cs.x), __fmul_rn(b, cs.y)), scale);
+    *rb = __fmul_rn(__fadd_rn(__fmul_rn(b, cs.x), __fmul_rn(a, cs.y)), scale);
+  }
+
+  // R(pos) q~ * log2(e)/sqrt(d) of the piece's G heads into shared memory,
+  // from the pre-RoPE rows that came with its first tile: one rotation pair
+  // per consumer thread (explicit roundings keep the result identical
+  // wherever it is computed).  Ends with a consumer barrier.
+  __device__ static void rotate_query(const StepParams &p, const Smem &S, int st, int b, int64_t pos) {
+    const int half = kHeadDim / 2;
+    const bool inter = p.rope_mode == MAC_ROPE_INTERLEAVED;
+    for (int i = threadIdx.x; i < G * half; i += kConsumers) {
+      const int hh = i / half, j = i % half;
+      const int ia = inter ? 2 * j : j, ib = inter ? 2 * j + 1 : j + half;
+      const void *row = S.qbuf + (size_t)st * kAux + hh * kRowBytes;
+      const float a = elem_f32<T>(row, ia), bb = elem_f32<T>(row, ib);
+      const float2 cs = p.rope_mode == MAC_ROPE_NONE ? make_float2(1.f, 0.f) : rope_cs(p, S, b, pos, j);
+      float ra, rb;
+      rotate_pair(a, bb, cs, p.q_scale, &ra, &rb);
+      S.qrot[hh * kHeadDim + ia] = ra;
+      S.qrot[hh * kHeadDim + ib] = rb;
+      if (!(isfinite(a) && isfinite(bb))) set_status(p.ctl, MAC_DEV_NONFINITE_Q);
+    }
+    consumer_sync();
   }
 
   // v[i] (i = token slot * G + head, partial dot products of the lane's 8
@@ -443,6 +1260,7 @@ struct Step {
     for (int lev = kAScat; lev < 4; ++lev) s += __shfl_xor_sync(kFull, s, 8 >> lev);
     return s;
   }
+
   // max / sum over the lanes of the half-warp whose score slots hold the
   // same head (the token bits of the slot index)
   __device__ static float head_max(float x) {
@@ -456,25 +1274,78 @@ struct Step {
     return x;
   }
 
-  // One stage: rows 0..kStTok-1 hold tokens a, a+1, ... (K in the first half
-  // of the stage, V in the second; `rows` marks the rows actually copied).
-  // The lane's score slot counts for its head only within [lo_m, hi_m].
-  __device__ static void att_stage(Att &A, const float2 (&q)[G][kAPairs], const uint8_t *buf, int a, int rows,
-                                   int lo_m, int hi_m) {
-    const int lane = lane_id(), sub = lane & 15, hw = lane >> 4;
-    const int idx = sub >> kAPlain, ti = idx / G;
-    const uint8_t *kb = buf, *vb = buf + kStageBytes / 2;
-#pragma unroll 1
-    for (int ps = 0; ps < kPasses; ++ps) {
+  // the lane's 8 dims (d = 8 sub .. 8 sub + 7) of row `row`
+  __device__ static void row_dims(const uint8_t *base, int row, int sub, float2 (&f)[kAPairs]) {
+#pragma unroll
+    for (int c = 0; c < kALoads; ++c)
+      unpack16x2<T>(*reinterpret_cast<const uint4 *>(base + row * kRowBytes + sub * 8 * (int)sizeof(T) + c * 16),
+                    f + c * (kAPairs / kALoads));
+  }
+
+  // One piece: tokens [pc.lo, pc.hi] of unit pc.u for its G heads; the
+  // piece's partial summary goes to dst ([G][kPartStride]).  A half-warp
+  // takes one token of a kATPG-token slot of every tile; lane `sub` owns
+  // dims 8 sub .. 8 sub + 7 of the rotated query (held in registers for the
+  // whole piece) and of the weighted values.
+  __device__ static void attend_piece(const StepParams &p, const Smem &S, uint32_t &n, int ph,
+                                      const Piece &pc, float *dst, bool first_piece) {
+    unsigned long long *trace = first_piece ? cta_trace(p) : nullptr;
+    unsigned long long *tr_all = ph == 1 && threadIdx.x == 0 ? cta_trace(p) : nullptr;
+    if (tr_all) {
+      tr_all[22] += (unsigned long long)(pc.hi - pc.lo + 1);
+      tr_all[23] += 1;
+    }
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, sub = lane & 15;
+    const int grp = warp * 2 + (lane >> 4);  // this half-warp: rows grp, grp + 16, ... of a tile
+    const int idx = sub >> kAPlain;          // this lane's score slot
+    const int ti = idx / G, hm = idx % G;    // its token (of the group's kATPG) and head
+    const int b = pc.u / p.Hkv, g = pc.u % p.Hkv;
+    int lo_mine = pc.lo;                     // first token of the lane's head in this piece
+    if (ph == 1 && p.mode == MODE_DECODE) {
+      const int pp = S.X[b * p.Hq + g * G + hm];
+      const int lh = pp >= 1 ? max(pp - p.r + 1, p.sink_f + 1) : p.sink_f + 1;
+      lo_mine = lh > lo_mine ? lh : lo_mine;
+    }
+    float2 o[G][kAPairs], q[G][kAPairs];
+    float mrun[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+      mrun[hh] = kMInit;
+#pragma unroll
+      for (int i = 0; i < kAPairs; ++i) o[hh][i] = make_float2(0.f, 0.f);
+    }
+    float m_mine = kMInit, l_mine = 0.f;
+    unsigned long long wait_ns = 0;  // traced band waits (kept in a register)
+
+    const int64_t tile0 = (pc.lo - 1) / kTileTok;
+    const int ntiles = (int)((pc.hi - 1) / kTileTok - tile0 + 1);
+    for (int k = 0; k < ntiles; ++k, ++n) {
+      const int st = n % kStages;
+      const unsigned long long tw = tr_all ? globaltimer() : 0ull;
+      const bool ok = wait_use(p, S, n);
+      if (tr_all) wait_ns += globaltimer() - tw;
+      if (k == 0) {
+        stamp(trace, ph ? 13 : 11);
+        rotate_query(p, S, st, b, S.u_pos[pc.u]);
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          const float4 x0 = *reinterpret_cast<const float4 *>(S.qrot + hh * kHeadDim + sub * 8);
+          const float4 x1 = *reinterpret_cast<const float4 *>(S.qrot + hh * kHeadDim + sub * 8 + 4);
+          q[hh][0] = make_float2(x0.x, x0.y);
+          q[hh][1] = make_float2(x0.z, x0.w);
+          q[hh][2] = make_float2(x1.x, x1.y);
+          q[hh][3] = make_float2(x1.z, x1.w);
+        }
+      }
+      const uint8_t *kb = S.stage + (size_t)st * kStageBytes;
+      const uint8_t *vb = kb + kStageBytes / 2;
+      const int t0 = (int)((tile0 + k) * kTileTok);
+      // partial scores of the group's kATPG tokens for the G heads
       float v[kAV];
 #pragma unroll
       for (int tt = 0; tt < kATPG; ++tt) {
-        const int row = ps * kPassTok + tt * 2 + hw;
         float2 kf[kAPairs];
-#pragma unroll
-        for (int c = 0; c < kALoads; ++c)
-          unpack16x2<T>(*reinterpret_cast<const uint4 *>(kb + row * kRow + sub * 8 * kES + c * 16),
-                        kf + c * (kAPairs / kALoads));
+        row_dims(kb, tt * kAGroups + grp, sub, kf);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
           float2 acc = __fmul2_rn(q[hh][0], kf[0]);
@@ -484,39 +1355,46 @@ struct Step {
         }
       }
       float s = reduce_scores(v, lane);
-      const int row_m = ps * kPassTok + ti * 2 + hw, t_m = a + row_m;
-      const bool valid = ((rows >> row_m) & 1) && t_m >= lo_m && t_m <= hi_m;
+      const int row_m = ti * kAGroups + grp;
+      const int t_m = t0 + row_m + 1;
+      const bool valid = ok && t_m >= lo_mine && t_m <= pc.hi && ((S.mask[st] >> (row_m >> 4)) & 1);
       s = valid ? s : -INFINITY;
-      // lazy running max (per half-warp and head): raised only when a score
+      // lazy running max (per group and head): raised only when a score
       // exceeds it by kLazy
       const float mt = head_max(s);
-      if (__any_sync(kFull, mt > A.m_mine + kLazy)) {
-        const float mn_mine = fmaxf(A.m_mine, mt);
+      if (__any_sync(kFull, mt > m_mine + kLazy)) {
+        const float mn_mine = fmaxf(m_mine, mt);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
           const float mn = __shfl_sync(kFull, mn_mine, (lane & 16) | (hh << kAPlain));
-          const float f = ex2(A.mrun[hh] - mn);
+          const float f = ex2(mrun[hh] - mn);
           const float2 f2 = make_float2(f, f);
 #pragma unroll
-          for (int i = 0; i < kAPairs; ++i) A.o[hh][i] = __fmul2_rn(A.o[hh][i], f2);
-          A.mrun[hh] = mn;
+          for (int i = 0; i < kAPairs; ++i) o[hh][i] = __fmul2_rn(o[hh][i], f2);
+          mrun[hh] = mn;
         }
-        A.l_mine *= ex2(A.m_mine - mn_mine);
-        A.m_mine = mn_mine;
+        l_mine *= ex2(m_mine - mn_mine);
+        m_mine = mn_mine;
       }
-      const float w = ex2(s - A.m_mine);
-      A.l_mine += w;
+      const float w = ex2(s - m_mine);
+      l_mine += w;
+      // rows the piece did not copy hold stale bytes, possibly NaN patterns,
+      // and 0 * NaN is NaN: in a partly covered tile they are zeroed
+      const int msk = S.mask[st];
+      const bool whole = t0 + 1 >= pc.lo && t0 + kTileTok <= pc.hi && msk == (1 << (kTileTok / 16)) - 1;
 #pragma unroll
       for (int tt = 0; tt < kATPG; ++tt) {
-        const int row = ps * kPassTok + tt * 2 + hw;
+        const int row = tt * kAGroups + grp;
         uint4 raw[kALoads];
 #pragma unroll
         for (int c = 0; c < kALoads; ++c)
-          raw[c] = *reinterpret_cast<const uint4 *>(vb + row * kRow + sub * 8 * kES + c * 16);
-        // rows not copied hold stale bytes, possibly NaN patterns (0 * NaN is NaN)
-        const uint32_t vm = ((rows >> row) & 1) ? ~0u : 0u;
+          raw[c] = *reinterpret_cast<const uint4 *>(vb + row * kRowBytes + sub * 8 * (int)sizeof(T) + c * 16);
+        if (!whole) {
+          const int t = t0 + row + 1;
+          const uint32_t vm = (t >= pc.lo && t <= pc.hi && ((msk >> (row >> 4)) & 1)) ? ~0u : 0u;
 #pragma unroll
-        for (int c = 0; c < kALoads; ++c) raw[c] = make_uint4(raw[c].x & vm, raw[c].y & vm, raw[c].z & vm, raw[c].w & vm);
+          for (int c = 0; c < kALoads; ++c) raw[c] = make_uint4(raw[c].x & vm, raw[c].y & vm, raw[c].z & vm, raw[c].w & vm);
+        }
         float2 vf[kAPairs];
 #pragma unroll
         for (int c = 0; c < kALoads; ++c) unpack16x2<T>(raw[c], vf + c * (kAPairs / kALoads));
@@ -525,572 +1403,368 @@ struct Step {
           const float wv = __shfl_sync(kFull, w, (lane & 16) | ((tt * G + hh) << kAPlain));
           const float2 w2 = make_float2(wv, wv);
 #pragma unroll
-          for (int i = 0; i < kAPairs; ++i) A.o[hh][i] = __ffma2_rn(w2, vf[i], A.o[hh][i]);
+          for (int i = 0; i < kAPairs; ++i) o[hh][i] = __ffma2_rn(w2, vf[i], o[hh][i]);
         }
       }
+      release(S, n);
     }
+    stamp(trace, ph ? 14 : 12);
+    if (tr_all) {
+      tr_all[24] = globaltimer();
+      tr_all[25] += wait_ns;
+    }
+    epilogue(p, S, o, mrun, m_mine, l_mine, dst);
+    if (ph == 1) stamp(trace, 15);
   }
 
-  // The warp's state -> one partial summary per head at dst ([G][kPartStride]):
-  // the two half-warps brought to a common maximum and summed.  only >= 0:
-  // that head's partial alone, at dst.
-  __device__ static void att_finish(Att &A, float *dst, int only = -1) {
-    const int lane = lane_id(), sub = lane & 15, hw = lane >> 4;
-    const int idx = sub >> kAPlain, hm = idx % G;
-    const float l_grp = head_sum(A.l_mine);  // this half-warp's sum for head hm
-    float M[G];
+  // The CTA's kAGroups half-warp states -> one partial summary per head:
+  // common maximum, every group rescaled to it, then summed in a fixed order
+  // through shared memory.
+  __device__ static void epilogue(const StepParams &p, const Smem &S, float2 (&o)[G][kAPairs],
+                                  const float (&mrun)[G], float m_mine, float l_mine, float *dst) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, sub = lane & 15;
+    const int grp = warp * 2 + (lane >> 4);
+    const int idx = sub >> kAPlain, ti = idx / G, hm = idx % G;
+    const float l_grp = head_sum(l_mine);  // the group's sum for head hm (all its token slots)
+    float mw[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) mw[hh] = fmaxf(mrun[hh], __shfl_xor_sync(kFull, mrun[hh], 16));
+    if (lane == 0)
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) S.red_m[warp * G + hh] = mw[hh];
+    consumer_sync();
+    float mc[G];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
-      M[hh] = fmaxf(A.mrun[hh], __shfl_xor_sync(kFull, A.mrun[hh], 16));
-      const float f = ex2(A.mrun[hh] - M[hh]);
+      mc[hh] = S.red_m[hh];
 #pragma unroll
-      for (int i = 0; i < kAPairs; ++i) {
-        float2 x = __fmul2_rn(A.o[hh][i], make_float2(f, f));
-        x.x += __shfl_xor_sync(kFull, x.x, 16);
-        x.y += __shfl_xor_sync(kFull, x.y, 16);
-        A.o[hh][i] = x;
-      }
+      for (int w = 1; w < kWarps; ++w) mc[hh] = fmaxf(mc[hh], S.red_m[w * G + hh]);
     }
-    float Mm = M[0];
 #pragma unroll
-    for (int hh = 1; hh < G; ++hh) Mm = hm == hh ? M[hh] : Mm;
-    float L = l_grp * ex2(A.m_mine - Mm);
-    L += __shfl_xor_sync(kFull, L, 16);
-    if (hw == 0) {
+    for (int hh = 0; hh < G; ++hh) {
+      const float f = ex2(mrun[hh] - mc[hh]);
+      const float2 f2 = make_float2(f, f);
+#pragma unroll
+      for (int i = 0; i < kAPairs; ++i) o[hh][i] = __fmul2_rn(o[hh][i], f2);
+    }
+    if (ti == 0 && (sub & ((1 << kAPlain) - 1)) == 0) {
+      float mcm = mc[0];
+#pragma unroll
+      for (int hh = 1; hh < G; ++hh) mcm = hm == hh ? mc[hh] : mcm;
+      S.red_l[grp * G + hm] = l_grp * ex2(m_mine - mcm);
+    }
+    {
+      float *wr = S.red_o + (size_t)grp * G * kHeadDim + sub * 8;
 #pragma unroll
       for (int hh = 0; hh < G; ++hh) {
-        if (only >= 0 && hh != only) continue;
-        float *o = dst + (only >= 0 ? 0 : hh * kPartStride) + sub * 8;
-        *reinterpret_cast<float4 *>(o) = make_float4(A.o[hh][0].x, A.o[hh][0].y, A.o[hh][1].x, A.o[hh][1].y);
-        *reinterpret_cast<float4 *>(o + 4) = make_float4(A.o[hh][2].x, A.o[hh][2].y, A.o[hh][3].x, A.o[hh][3].y);
+        *reinterpret_cast<float4 *>(wr + hh * kHeadDim) = make_float4(o[hh][0].x, o[hh][0].y, o[hh][1].x, o[hh][1].y);
+        *reinterpret_cast<float4 *>(wr + hh * kHeadDim + 4) = make_float4(o[hh][2].x, o[hh][2].y, o[hh][3].x, o[hh][3].y);
       }
-      if ((sub & ((1 << kAPlain) - 1)) == 0 && idx < G && (only < 0 || hm == only))  // one lane per head
-        *reinterpret_cast<float2 *>(dst + (only >= 0 ? 0 : hm * kPartStride) + kHeadDim) = make_float2(Mm, L);
     }
-  }
-
-  // R(pos) q~ * log2(e)/sqrt(d) of the G heads of unit u, the lane's dims
-  // [8 sub, 8 sub + 8) (explicit roundings keep the result identical
-  // wherever it is computed).
-  // R(pos) q~ * log2(e)/sqrt(d) of the G heads of unit u, the lane's dims
-  // [8 sub, 8 sub + 8), from the query rows in global memory or (qe) in a
-  // warp's query entry holding the G rows back to back.  Every pair (a, b)
-  // of a 2x2 rotation becomes a' = a cos - b sin, b' = b cos + a sin; a lane
-  // computes its own dims x from its partner dims y with signed sines (the
-  // explicit roundings keep the result identical wherever it is computed).
-  __device__ static void load_query(const StepParams &p, const Smem &S, int u, float2 (&q)[G][kAPairs],
-                                    const uint8_t *qe = nullptr) {
-    const int lane = lane_id(), sub = lane & 15;
-    const int b = u / p.Hkv, g = u - b * p.Hkv;
-    const bool half = p.rope_mode == MAC_ROPE_HALF, none = p.rope_mode == MAC_ROPE_NONE;
-    const int d0 = sub * 8, dp = (d0 + kHeadDim / 2) & (kHeadDim - 1);  // own dims, partner dims (half mode)
-    float c[8], sn[8];
+    consumer_sync();
+    // each output element: the kAGroups group states in a fixed order (the
+    // next piece's epilogue writes these buffers only after its first
+    // barrier, which every thread reaches after these reads)
+    float acc[kOutPer];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      // half: pair (j, j + d/2), own dims below d/2 are a; interleaved: pair (2j, 2j + 1)
-      const int j = half ? (d0 + i) & (kHeadDim / 2 - 1) : (d0 + i) >> 1;
-      float2 cs = make_float2(1.f, 0.f);
-      if (!none) {
-        if (S.rope) cs = S.rope[b * (kHeadDim / 2) + j];
-        else rope_angle(qpos(p, b), p.rope_f[j], &cs.x, &cs.y);
+    for (int j = 0; j < kOutPer; ++j) {
+      acc[j] = 0.f;
+      const int e = tid + j * kConsumers;
+      if (e < G * kHeadDim) {
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w2 = 0; w2 < kAGroups; ++w2) part[w2 & 3] += S.red_o[(size_t)w2 * G * kHeadDim + e];
+        acc[j] = (part[0] + part[1]) + (part[2] + part[3]);
       }
-      const bool is_a = half ? d0 < kHeadDim / 2 : (i & 1) == 0;
-      c[i] = cs.x;
-      sn[i] = is_a ? -cs.y : cs.y;
     }
-    bool bad = false;
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      const int64_t e0 = ((int64_t)b * p.Hq + g * G + hh) * p.q_stride + p.q_offset;
-      const T *row = qe ? reinterpret_cast<const T *>(qe + hh * kRow) : reinterpret_cast<const T *>(p.q) + e0;
-      float x[8], y[8];
-#pragma unroll
-      for (int k = 0; k < kALoads; ++k) {
-        float2 f[kAPairs / kALoads], h[kAPairs / kALoads];
-        const uint4 *o4 = reinterpret_cast<const uint4 *>(row + d0) + k;
-        const uint4 *p4 = reinterpret_cast<const uint4 *>(row + dp) + k;
-        unpack16x2<T>(qe ? *o4 : __ldg(o4), f);
-        unpack16x2<T>(half ? (qe ? *p4 : __ldg(p4)) : make_uint4(0, 0, 0, 0), h);
-#pragma unroll
-        for (int i = 0; i < kAPairs / kALoads; ++i) {
-          x[k * 8 / kALoads + 2 * i] = f[i].x;
-          x[k * 8 / kALoads + 2 * i + 1] = f[i].y;
-          y[k * 8 / kALoads + 2 * i] = h[i].x;
-          y[k * 8 / kALoads + 2 * i + 1] = h[i].y;
-        }
-      }
-      float r[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        bad |= !isfinite(x[i]);
-        const float yy = half ? y[i] : none ? 0.f : x[i ^ 1];
-        r[i] = none ? __fmul_rn(x[i], p.q_scale)
-                    : __fmul_rn(__fadd_rn(__fmul_rn(x[i], c[i]), __fmul_rn(yy, sn[i])), p.q_scale);
-      }
-#pragma unroll
-      for (int i = 0; i < kAPairs; ++i) q[hh][i] = make_float2(r[2 * i], r[2 * i + 1]);
+    for (int j = 0; j < kOutPer; ++j) {
+      const int e = tid + j * kConsumers;
+      if (e < G * kHeadDim) dst[(e / kHeadDim) * kPartStride + e % kHeadDim] = acc[j];
     }
-    if (bad) set_status(p.ctl, MAC_DEV_NONFINITE_Q);
-  }
-
-  // ---------------------------------------------------------------------
-  // match
-  // ---------------------------------------------------------------------
-  // The squared distance over the lane's 8 dims of one half of a row (exact
-  // bf16 differences, squares summed in a pairwise tree).
-  __device__ static float half_dist(const float2 (&qv)[4], const uint8_t *src) {
-    float2 e[4];
+    if (warp == 0) {
+      // lane i < kAGroups holds group i's sums; butterfly over the groups
 #pragma unroll
-    for (int c = 0; c < kHalfLoads; ++c)
-      unpack16x2<T>(*reinterpret_cast<const uint4 *>(src + c * 16), e + c * (4 / kHalfLoads));
-    float2 df[4];
+      for (int hh = 0; hh < G; ++hh) {
+        float L = lane < kAGroups ? S.red_l[lane * G + hh] : 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) df[k] = __fadd2_rn(qv[k], make_float2(-e[k].x, -e[k].y));
-    const float2 t0 = __ffma2_rn(df[2], df[2], __fmul2_rn(df[0], df[0]));
-    const float2 t1 = __ffma2_rn(df[3], df[3], __fmul2_rn(df[1], df[1]));
-    const float2 t = __fadd2_rn(t0, t1);
-    return __fadd_rn(t.x, t.y);
-  }
-  // v[k]: this lane's part of row k of its group -> the lane's row total
-  // (row sub >> (3 - kLogMRG)): reduce-scatter over the 8 lanes, then plain
-  // butterflies (a pairwise tree of the 8 lanes' parts).
-  __device__ static float group_reduce(float (&v)[kMRG]) {
-#pragma unroll
-    for (int lev = 0; lev < kLogMRG; ++lev) {
-      const int off = 4 >> lev;
-      const bool up = (threadIdx.x & off) != 0;
-      const int half = kMRG >> (lev + 1);
-#pragma unroll
-      for (int i = 0; i < kMRG / 2; ++i) {
-        if (i < half) {
-          const float send = up ? v[i] : v[i + half];
-          const float keep = up ? v[i + half] : v[i];
-          v[i] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, off));
+        for (int o2 = kAGroups / 2; o2 >= 1; o2 >>= 1) L += __shfl_xor_sync(kFull, L, o2);
+        if (lane == hh) {
+          dst[hh * kPartStride + kHeadDim] = mc[hh];
+          dst[hh * kPartStride + kHeadDim + 1] = L;
         }
       }
     }
-    float D = v[0];
-#pragma unroll
-    for (int lev = kLogMRG; lev < 3; ++lev) D = __fadd_rn(D, __shfl_xor_sync(kFull, D, 4 >> lev));
-    return D;
-  }
-  // the stage row whose distance this lane finishes
-  __device__ static int match_row(int lane) { return (lane >> 3) + 4 * (((lane & 7) >> (3 - kLogMRG)) & (kMRG - 1)); }
-  // One stage of ring rows (cnt of them): the lane's candidate (distance,
-  // position pk) joins its running best.
-  __device__ static void match_stage(const uint8_t *buf, int cnt, const float2 (&qlo)[4], const float2 (&qhi)[4],
-                                     int pk, int pos_lo, int pos_hi, float &bd, int &bp) {
-    const int lane = lane_id(), grp = lane >> 3, sub = lane & 7;
-    float lo[kMRG], hi[kMRG];
-#pragma unroll
-    for (int k = 0; k < kMRG; ++k) {
-      const int r = grp + 4 * k;
-      const uint8_t *row = buf + (size_t)(r < cnt ? r : cnt - 1) * kRow;
-      lo[k] = half_dist(qlo, row + sub * 8 * kES);
-      hi[k] = half_dist(qhi, row + kRow / 2 + sub * 8 * kES);
-    }
-    const float D = __fadd_rn(group_reduce(lo), group_reduce(hi));
-    if (match_row(lane) < cnt && pk >= pos_lo && pk <= pos_hi && better(D, pk, bd, bp)) {
-      bd = D;
-      bp = pk;
-    }
   }
 
-  // ---------------------------------------------------------------------
-  // phase A: window tiles and match items, round-robin over all warps
-  // ---------------------------------------------------------------------
-  __device__ static int n_units(const StepParams &p) { return p.B * p.Hkv; }
-  __device__ static int match_cph(const StepParams &p) { return (p.K + kIR - 1) / kIR; }
-  __device__ static int64_t n_window_items(const StepParams &p) { return (int64_t)n_units(p) * p.tc.nt; }
-  __device__ static int64_t n_items(const StepParams &p) {
-    return n_window_items(p) + (p.mode == MODE_DECODE ? (int64_t)p.B * p.Hq * match_cph(p) : 0);
-  }
-  // One streamed item: a window tile (kind 1: unit u, tokens [lo, hi], all
-  // heads), a match item (kind 2: head u, ring rows [lo, hi)), or a boundary
-  // piece (kind 3: unit u, tokens [lo, hi] for head hm alone, into the
-  // warp's slot of S.bd); kind -1: none.
-  struct Item {
-    int64_t i;
-    int kind, u, lo, hi, hm;
+  // The CTA's pieces of one kind, in the order both the producer and the
+  // consumers walk them: 0 its tail span, 1 its short bands, 2 its
+  // long-band span; kind 3 lists (without attention) the units u = c mod P
+  // whose merge no band piece triggers: no band piece (the last piece was a
+  // tail piece, before the decisions) or no piece at all (no valid length).
+  struct PieceIter {
+    int kind, it, end;
   };
-  __device__ static Item no_item() {
-    Item it;
-    it.i = 0;
-    it.kind = -1;
-    it.u = it.lo = it.hm = 0;
-    it.hi = -1;
-    return it;
+
+  // The front sink [1, min(F, m)] of unit u: its length (0 without a sink
+  // piece), and the CTA that attends it: with units aligned to CTAs, the
+  // first CTA of the unit's group after its tail run (the group's last when
+  // the tail takes them all), else u mod P.
+  __device__ static int sink_len(const StepParams &p, const Smem &S, int u) {
+    if (!SINK || !p.sink_piece) return 0;
+    const int64_t m = unit_len(p, S, u);
+    if (!len_ok(p, m)) return 0;
+    return (int)(m < p.sink_f ? m : p.sink_f);
   }
-  // phase-A item i: the window tiles of every unit, then the match items
-  __device__ static Item item_a(const StepParams &p, const Smem &S, int64_t i) {
-    Item it = no_item();
-    it.i = i;
-    const int64_t nw = n_window_items(p);
-    if (i < 0 || i >= n_items(p)) return it;
-    if (i < nw) {
-      const int u = (int)((uint32_t)i / (uint32_t)p.tc.nt), t = (int)i - u * p.tc.nt;
-      it.kind = 1;
-      it.u = u;
-      tile_range(p, S.um[u], t, &it.lo, &it.hi);
+  __device__ static int sink_cta(const StepParams &p, const Smem &S, int u) {
+    const int U = p.B * p.Hkv, P = gridDim.x;
+    if (U > P) return u % P;
+    const short2 run = S.runA[u];
+    const int a = u * P / U, a_next = (u + 1) * P / U;
+    const int cand = a + (run.y >= run.x ? run.y - run.x + 1 : 0);
+    return cand < a_next ? cand : a_next - 1;
+  }
+  __device__ static PieceIter piece_iter(const StepParams &p, const Smem &S, int kind) {
+    const int U = p.B * p.Hkv, ph = kind == 0 ? 0 : 1;
+    PieceIter I;
+    I.kind = kind;
+    if (kind == 1) {
+      short_range(S, &I.it, &I.end);
+    } else if (kind == 3) {
+      I.it = blockIdx.x;
+      I.end = U;
     } else {
-      const int cph = match_cph(p);
-      const int mi = (int)(i - nw), bh = (int)((uint32_t)mi / (uint32_t)cph);
-      it.kind = 2;
-      it.u = bh;
-      it.lo = (mi - bh * cph) * kIR;
-      it.hi = min(p.K, it.lo + kIR);
+      const int64_t g0 = spans(S, ph)[blockIdx.x], g1 = spans(S, ph)[blockIdx.x + 1];
+      I.it = g0 < g1 ? unit_of(offs(S, ph), U, g0) : U;
+      I.end = U;
     }
-    return it;
+    if (SINK && kind == 0 && p.sink_piece) {
+      // the sink candidates first: units c, c + P, ..., or, with units
+      // aligned to CTAs, the one whose group holds CTA c
+      const int P = gridDim.x, c = blockIdx.x;
+      I.end = -(I.it + 1);
+      I.it = U > P ? c : ((c + 1) * U - 1) / P;
+    }
+    return I;
   }
-  // The boundary piece of owned head k (none when the head misses or its
-  // band starts on a tile boundary): the band [lo, m - r] of a hit at p
-  // starts at lo = p - r + 1 inside band tile j; the piece is [lo, end of
-  // tile j] for that head alone.  *nbt: the band tiles the head takes whole.
-  __device__ static Item boundary_item(const StepParams &p, const Smem &S, int bh, int pos, int *nbt) {
-    Item it = no_item();
-    const int b = bh / p.Hq, h = bh - b * p.Hq, g = h / G, u = b * p.Hkv + g;
-    const int m = S.um[u];
-    *nbt = p.tc.nbw;
-    if (pos < 1 || m <= 0) return it;
-    const int lo = max(lb(p), pos - p.r + 1);
-    if (lo > m - p.r) {
-      *nbt = 0;
-      return it;
+  __device__ static bool next_piece(const StepParams &p, const Smem &S, PieceIter &I, Piece &pc) {
+    pc.sink = 0;
+    if (I.kind == 1) {
+      if (I.it >= I.end) return false;
+      pc = short_piece(p, S, I.it++);
+      return true;
     }
-    const int j = (m - p.r - lo) / kTT;
-    int tlo, thi;
-    tile_range(p, m, j, &tlo, &thi);
-    *nbt = lo == tlo ? j + 1 : j;
-    if (lo == tlo) return it;
-    it.kind = 3;
-    it.u = u;
-    it.lo = lo;
-    it.hi = thi;
-    it.hm = h - g * G;
-    return it;
-  }
-  // stage s of an item
-  __device__ static Desc stage_desc(const StepParams &p, const Item &it, int s) {
-    Desc d;
-    d.kind = it.kind == 2 ? 2 : 1;
-    d.u = it.u;
-    if (it.kind != 2) {
-      d.a = it.lo + s * kStTok;
-      d.cnt = min(it.hi - d.a + 1, kStTok);
-      d.keep = it.kind == 1;
-    } else {
-      d.a = it.lo + s * kStRows;
-      d.cnt = min(it.hi - d.a, kStRows);
-      if (d.cnt <= 0) d.kind = 0;
-      d.pc = d.kind == 2 && (p.K & 3) == 0 && (d.cnt & 3) == 0;
-    }
-    return d;
-  }
-  // the query an item needs: its unit (window, boundary) or head (match)
-  __device__ static int query_key(const Item &it) { return it.kind == 2 ? -1 - it.u : it.u; }
-
-  // The streaming loop of one round, one copy of the per-stage code for all
-  // rounds: round 0 streams this warp's contiguous share of the phase-A
-  // items; round r >= 1 the boundary piece of owned head (r-1) kWarps + w.
-  // One iteration per stage; the copies run up to kStages stages ahead.
-  // Consecutive items of a warp mostly share their query; an item whose
-  // query differs from the one before brings it along with its first stage
-  // (into the warp's next query entry), so the loop waits on nothing but its
-  // stages.  Without query entries (no room in shared memory) the query is
-  // read from global memory.
-  __device__ static void stream(const StepParams &p, const Smem &S, Ring &R, int rnd, int h0, int hstep, int nown) {
-    const int lane = lane_id(), w = warp_id(), P = gridDim.x, NW = P * kWarps;
-    const int gw = w * P + blockIdx.x;
-    int64_t i_beg = 0, i_end = 0;
-    if (rnd == 0) {
-      const int64_t na = n_items(p);
-      i_beg = (int64_t)(((unsigned long long)gw * (unsigned long long)na) / (unsigned)NW);
-      i_end = (int64_t)(((unsigned long long)(gw + 1) * (unsigned long long)na) / (unsigned)NW);
-    } else {
-      const int k = (rnd - 1) * kWarps + w;
-      i_end = k < nown ? 1 : 0;
-    }
-    auto get = [&](int64_t i) -> Item {
-      if (i >= i_end) return no_item();
-      if (rnd == 0) return item_a(p, S, i);
-      const int k = (rnd - 1) * kWarps + w, bh = h0 + k * hstep;
-      int nbt;
-      Item it = boundary_item(p, S, bh, k < kOwnMax ? S.dec[k] : decision(p, S, bh), &nbt);
-      it.i = i;
-      return it;
-    };
-    int32_t id[2];
-    // fetch side: the next stage to copy; it attaches the query of each
-    // item whose query differs from the last
-    Item fi = get(i_beg);
-    int fs = 0, f_key = 0x7fffffff, f_e = 1;
-    Desc nx;
-    bool have_nx = false;
-    auto fetch_next = [&]() {
-      have_nx = fi.kind >= 0;
-      if (!have_nx) return;
-      nx = stage_desc(p, fi, fs);
-      if (fs == 0 && query_key(fi) != f_key) {
-        f_key = query_key(fi);
-        f_e ^= 1;
-        nx.qe = f_e;
-      }
-      if (++fs == kItemStages) {
-        fs = 0;
-        fi = get(fi.i + 1);
-      }
-      load_ids(p, nx, id);
-    };
-    fetch_next();
-    Att A;
-    float2 q[G][kAPairs];
-    float2 qlo[4], qhi[4];
-    float bd = INFINITY;
-    int bp = -1, pos_lo = 1, pos_hi = 0;
-    int c_key = 0x7fffffff, c_e = 1;  // the query in registers, its entry
-    Item ci = get(i_beg);
-    int cs = 0;  // the stage of ci to consume
+    // kind 0: the CTA's sink pieces come before its tail pieces; while they
+    // are looked for, it is the candidate unit and end = -(tail start + 1)
+    if (SINK && I.end < 0) {
+      const int U = p.B * p.Hkv, P = gridDim.x;
 #pragma unroll 1
-    for (;;) {
-      // keep kStages copies in flight
+      for (; I.it < U; I.it += U > P ? P : U) {
+        const int u = I.it, n = sink_len(p, S, u);
+        if (n > 0 && sink_cta(p, S, u) == (int)blockIdx.x) {
+          pc.u = u;
+          pc.lo = 1;
+          pc.hi = n;
+          pc.sink = 1;
+          I.it += U > P ? P : U;
+          return true;
+        }
+      }
+      I.it = -I.end - 1;
+      I.end = U;
+    }
+    if (I.kind == 3) {
 #pragma unroll 1
-      while (have_nx && R.issued - R.used < (uint32_t)kStages) {
-        issue(p, R, nx, id);
-        fetch_next();
-      }
-      if (ci.kind < 0 || *S.abort) break;
-      if (cs == 0) {
-        if (ci.kind == 2) {
-          const int m = S.um[(ci.u / p.Hq) * p.Hkv];
-          pos_lo = m > 0 ? max(1, m - p.K) : 1;
-          pos_hi = m > 0 ? m - 1 : 0;
-          bd = INFINITY;
-          bp = -1;
-        } else {
-          att_init(A);
+      for (; I.it < I.end; I.it += gridDim.x) {
+        const PieceList L = unit_list(p, S, I.it);
+        if (band_pieces(S, L) == 0 &&
+            (p.mode == MODE_DECODE || nonempty(S, 0, L.ca0, L.ca0 + L.nt - 1) == 0)) {
+          pc.u = I.it;
+          pc.lo = 1;
+          pc.hi = 0;
+          I.it += gridDim.x;
+          return true;
         }
       }
-      const Desc d = stage_desc(p, ci, cs);
-      const int r = match_row(lane);
-      int pk = 0;
-      if (d.kind == 2 && !d.pc)  // the position of the row this lane finishes, read directly
-        pk = __ldg(p.ring_pos + (int64_t)(d.u / p.Hq) * p.K + d.a + (r < d.cnt ? r : d.cnt - 1));
-      const uint32_t n = R.used;
-      const bool ok = wait_stage(p, S, R, n);
-      const int key = query_key(ci);
-      if (cs == 0 && key != c_key) {
-        // the item's query came with its first stage (or is read directly)
-        c_e ^= 1;
-        c_key = key;
-        const uint8_t *qe = R.qbuf ? R.qbuf + (size_t)c_e * kQE : nullptr;
-        if (ci.kind != 2) {
-          load_query(p, S, ci.u, q, qe);
-        } else {
-          const T *row = qe ? reinterpret_cast<const T *>(qe)
-                            : reinterpret_cast<const T *>(p.q) + (int64_t)ci.u * p.q_stride + p.q_offset;
-#pragma unroll
-          for (int c = 0; c < kHalfLoads; ++c) {
-            const uint4 *lo4 = reinterpret_cast<const uint4 *>(row + (lane & 7) * 8) + c;
-            const uint4 *hi4 = reinterpret_cast<const uint4 *>(row + kHeadDim / 2 + (lane & 7) * 8) + c;
-            unpack16x2<T>(qe ? *lo4 : __ldg(lo4), qlo + c * (4 / kHalfLoads));
-            unpack16x2<T>(qe ? *hi4 : __ldg(hi4), qhi + c * (4 / kHalfLoads));
-          }
-        }
-      }
-      if (ok) {
-        const uint8_t *buf = stage_buf(R, n);
-        if (d.kind == 1 && d.cnt > 0) {
-          // a boundary piece counts for its head alone
-          const int hm = ((lane & 15) >> kAPlain) % G;
-          const bool mine = ci.kind != 3 || hm == ci.hm;
-          att_stage(A, q, buf, d.a, R.rows[n % kStages], mine ? d.a : 1, mine ? d.a + d.cnt - 1 : 0);
-        } else if (d.kind == 2) {
-          if (d.pc)
-            pk = reinterpret_cast<const int32_t *>(R.pside + (size_t)(n % kStages) * kPosBytes)[r < d.cnt ? r : d.cnt - 1];
-          match_stage(buf, d.cnt, qlo, qhi, pk, pos_lo, pos_hi, bd, bp);
-        }
-      }
-      R.used++;
-      done_with_stage();
-      if (++cs < kItemStages) continue;
-      // the item is done
-      cs = 0;
-      if (ci.kind == 1) {
-        const int u = ci.u, t = (int)(ci.i - (int64_t)u * p.tc.nt);
-        att_finish(A, p.part_w + ((size_t)u * p.tc.nt + t) * G * kPartStride);
-      } else if (ci.kind == 3) {
-        att_finish(A, S.bd + (size_t)w * kPartStride, ci.hm);
-      } else {
-        // the warp's best joins the head's minimum
-#pragma unroll
-        for (int off = 1; off <= 16; off <<= 1) {
-          const float d2 = __shfl_xor_sync(kFull, bd, off);
-          const int p2 = __shfl_xor_sync(kFull, bp, off);
-          if (better(d2, p2, bd, bp)) {
-            bd = d2;
-            bp = p2;
-          }
-        }
-        if (lane == 0 && bp >= 1) atomicMax(&S.best[ci.u], pack_best(bd, bp));
-      }
-      ci = get(ci.i + 1);
+      return false;
     }
+    const int ph = I.kind == 0 ? 0 : 1;
+    if (!find_piece(p, S, ph, I.it, spans(S, ph)[blockIdx.x], spans(S, ph)[blockIdx.x + 1], &pc)) return false;
+    I.it = pc.u + 1;
+    return true;
   }
 
-  // ---------------------------------------------------------------------
-  // decisions and the long-band layout
-  // ---------------------------------------------------------------------
-  // The decision of head bh: the matched position, or -1 (miss).
-  __device__ static int decision(const StepParams &p, const Smem &S, int bh) {
-    if (p.mode != MODE_DECODE) return -1;
-    const int m = S.um[(bh / p.Hq) * p.Hkv];
-    const unsigned long long inv = __ldcg(&S.best[bh]);
-    if (inv == 0ull || m <= 0 || m < p.min_context) return -1;
-    const unsigned long long key = ~inv;
-    const float d = __uint_as_float((uint32_t)(key >> 32));
-    return d < p.thr2 ? (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull)) : -1;
-  }
-  // Long-band length of unit u: tokens [lb, win_start - 1] of a unit with a
-  // missing head.
-  __device__ static int64_t long_len(const StepParams &p, const Smem &S, int u, bool miss) {
-    const int m = S.um[u];
-    if (m <= 0 || !miss) return 0;
-    return max(0, win_start(p, m) - lb(p));
-  }
-
-  // Exclusive scan of one value per thread, in thread order, and the total.
-  // All threads call it; it holds two barriers.
-  __device__ static long long block_scan(const Smem &S, long long x, long long *total) {
-    const int lane = lane_id(), warp = warp_id();
-    long long xi = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(kFull, xi, o);
-      if (lane >= o) xi += y;
-    }
-    if (lane == 31) S.scan[warp] = xi;
-    block_sync();
-    long long base = 0, tot = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const long long v = S.scan[w];
-      base += w < warp ? v : 0;
-      tot += v;
-    }
-    block_sync();
-    *total = tot;
-    return base + xi - x;
-  }
-
-  // Heads owned (merged) by this CTA, out of N: bh with floor(bh P / N) == c
-  // (N <= P), or bh = c, c + P, ... (N > P); own_index: the head's rank among
-  // them, -1 when not owned here or beyond the kOwnMax whose decisions are
-  // kept.
-  static constexpr int kOwnMax = 16;
-  __device__ static void own_range(int U, int *u0, int *u_end, int *step) {
-    const int P = gridDim.x, c = blockIdx.x;
-    *u0 = U <= P ? (c * U + P - 1) / P : c;
-    *u_end = U <= P ? ((c + 1) * U + P - 1) / P : U;
-    *step = U <= P ? 1 : P;
-  }
-  __device__ static int own_index(int U, int u) {
-    int u0, u_end, step;
-    own_range(U, &u0, &u_end, &step);
-    if (u < u0 || u >= u_end || (u - u0) % step != 0) return -1;
-    const int k = (u - u0) / step;
-    return k < kOwnMax ? k : -1;
-  }
-
-  // Every unit's long-band offset (units end to end) and the number of CTAs
-  // they are cut over; the same in every CTA.  Ends with a barrier.
-  __device__ static void layout_long(const StepParams &p, const Smem &S) {
-    const int U = n_units(p);
-    long long carry = 0;
+  // The consumers' side: attention of each piece, its count, and the merges
+  // it completes (one call site each, so the code is inlined once).
+  __device__ static void attend_kind(const StepParams &p, const Smem &S, uint32_t &n, int kind) {
+    const int U = p.B * p.Hkv, ph = kind == 0 ? 0 : 1;
+    PieceIter I = piece_iter(p, S, kind);
+    int j0, j1;
+    short_range(S, &j0, &j1);
+    bool first = kind != 2 || j1 == j0;  // the CTA's first band piece is traced
+    Piece pc;
 #pragma unroll 1
-    for (int base = 0; base < U; base += kThreads) {
-      const int u = base + threadIdx.x;
-      long long x = 0;
-      if (u < U) {
-        bool miss = p.mode != MODE_DECODE;
-        const int b = u / p.Hkv, g = u - b * p.Hkv;
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const int bh = b * p.Hq + g * G + hh, pos = decision(p, S, bh);
-          const int k = own_index(p.B * p.Hq, bh);
-          miss |= pos < 1;
-          if (k >= 0) S.dec[k] = pos;
-        }
-        x = long_len(p, S, u, miss);
+    while (next_piece(p, S, I, pc)) {
+      int act = 2, k = 0;
+      if (kind != 3) {
+        const size_t slot = kind == 0 ? (size_t)(pc.u + blockIdx.x)
+                                      : kind == 1 ? (size_t)pc.u : (size_t)(U + pc.u + blockIdx.x);
+        float *dst = SINK && pc.sink ? p.part_s + (size_t)pc.u * G * kPartStride
+                             : (ph ? p.part_b : p.part_a) + slot * G * kPartStride;
+        attend_piece(p, S, n, ph, pc, dst, first);
+        first = false;
+        act = piece_count(p, S, pc.u, ph, kind == 1, &k);
       }
-      long long tot;
-      const long long ex = block_scan(S, x, &tot);
-      if (u < U) S.off[u + 1] = carry + ex + x;
-      carry += tot;
+      if (act) merge_chain(p, S, pc.u, act, k);
     }
-    if (threadIdx.x == 0) {
-      S.off[0] = 0;
-      *S.ntok = carry;
-      const long long want = (carry + kMinSpan - 1) / kMinSpan;
-      *S.Pl = carry > 0 ? (int)(want < (long long)gridDim.x ? want : (long long)gridDim.x) : 0;
-    }
-    block_sync();
-  }
-  // span of CTA c on the long-band axis: [span(c), span(c + 1)) (c < Pl)
-  __device__ static int64_t span(const Smem &S, int c) {
-    const int64_t tot = *S.ntok;
-    const int Pl = *S.Pl;
-    return c >= Pl ? tot : (int64_t)(((unsigned long long)c * (unsigned long long)tot) / (unsigned long long)Pl);
-  }
-  // the CTA whose span holds long-band index x (0 <= x < T): the largest c
-  // with span(c) <= x
-  __device__ static int cta_of(const Smem &S, int64_t x) {
-    return (int)((((unsigned long long)x + 1) * (unsigned long long)*S.Pl - 1) / (unsigned long long)*S.ntok);
-  }
-  // the last unit u with off[u] <= x
-  __device__ static int unit_of(const StepParams &p, const Smem &S, int64_t x) {
-    const int U = n_units(p);
-    int lo = 0;
-#pragma unroll 1
-    for (int s = U > 1 ? 1 << (31 - __clz(U - 1)) : 0; s >= 1; s >>= 1) {
-      const int t = lo + s;
-      if (t < U && S.off[t] <= x) lo = t;
-    }
-    return lo;
-  }
-  // unit u's CTA run [*c0, *c1] (empty: *c1 < *c0)
-  __device__ static void long_run(const Smem &S, int u, int *c0, int *c1) {
-    const int64_t a = S.off[u], z = S.off[u + 1];
-    if (z <= a) {
-      *c0 = 0;
-      *c1 = -1;
-      return;
-    }
-    *c0 = cta_of(S, a);
-    *c1 = cta_of(S, z - 1);
-  }
-  // long-band entries of unit u's merge: CTA pieces, or CTA groups
-  __device__ static bool grouped(int c0, int c1) { return c1 - c0 + 1 > kGroupCtas; }
-  __device__ static int long_entries(int c0, int c1) {
-    if (c1 < c0) return 0;
-    return grouped(c0, c1) ? c1 / kGroupCtas - c0 / kGroupCtas + 1 : c1 - c0 + 1;
-  }
-  __device__ static const float *long_entry(const StepParams &p, int u, int c0, int c1, int i, int hh) {
-    if (grouped(c0, c1)) return p.part_g + ((size_t)(u + c0 / kGroupCtas + i) * G + hh) * kPartStride;
-    return p.part_c + ((size_t)(u + c0 + i) * G + hh) * kPartStride;
   }
 
   // ---------------------------------------------------------------------
   // merges
   // ---------------------------------------------------------------------
+
+  // CTAs whose spans meet unit u's segment in phase ph: [*c0, *c1] (empty
+  // when *c1 < *c0).
+  __device__ static void seg_ctas(const Smem &S, int ph, int u, int *c0, int *c1) {
+    const short2 r = (ph ? S.runB : S.runA)[u];
+    *c0 = r.x;
+    *c1 = r.y;
+  }
+  // the run of unit u in phase ph, from the offsets and spans
+  __device__ static short2 find_run(const Smem &S, int ph, int u) {
+    const int64_t *off = offs(S, ph), *span = spans(S, ph);
+    if (off[u + 1] <= off[u]) return make_short2(0, -1);
+    return make_short2((short)cta_of(span, gridDim.x, off[u]), (short)cta_of(span, gridDim.x, off[u + 1] - 1));
+  }
+
+  // Non-empty spans of phase ph among CTAs [c0, c1].
+  __device__ static int nonempty(const Smem &S, int ph, int c0, int c1) {
+    if (c1 < c0) return 0;
+    const int *ne = ph ? S.neB : S.neA;
+    return ne[c1 + 1] - ne[c0];
+  }
+
+  // The partials a merge reads, in order: nb band entries, then (for a unit)
+  // one per CTA of its tail run.  Band entries: the short piece, one per CTA
+  // of the long-band run, or, for a run over more than kGroupCtas CTAs, one
+  // per CTA group (merged first, each by the CTA that finishes the group's
+  // last piece).  A group merge lists the run's CTAs in group k.
+  enum { kShort = 0, kCtas = 1, kGroupList = 2 };
+  struct PieceList {
+    int kind, nb, n;
+    int nt;      // tail entries (after the band entries; a sink entry, if any, is last)
+    int b0, b1;  // the band entries' CTA range (kCtas) / the whole run (kGroupList)
+    int ca0;     // first CTA of the tail run
+    int u;
+  };
+  __device__ static PieceList unit_list(const StepParams &p, const Smem &S, int u) {
+    PieceList L;
+    int ca1;
+    L.u = u;
+    seg_ctas(S, 1, u, &L.b0, &L.b1);
+    seg_ctas(S, 0, u, &L.ca0, &ca1);
+    if (short_band(p, S, u)) {
+      L.kind = kShort;
+      L.nb = 1;
+    } else if (L.b1 - L.b0 + 1 > kGroupCtas) {
+      L.kind = kGroupList;
+      L.nb = L.b1 / kGroupCtas - L.b0 / kGroupCtas + 1;
+    } else {
+      L.kind = kCtas;
+      L.nb = L.b1 - L.b0 + 1;
+    }
+    L.nt = ca1 - L.ca0 + 1;
+    L.n = L.nb + L.nt + (sink_len(p, S, u) > 0 ? 1 : 0);
+    return L;
+  }
+  __device__ static void group_ctas(const PieceList &L, int k, int *lo, int *hi) {
+    *lo = max(L.b0, k * kGroupCtas);
+    *hi = min(L.b1, k * kGroupCtas + kGroupCtas - 1);
+  }
+  __device__ static PieceList group_list(const PieceList &U_, int k) {
+    PieceList L = U_;
+    L.kind = kCtas;
+    group_ctas(U_, k, &L.b0, &L.b1);
+    L.nb = L.n = L.b1 - L.b0 + 1;
+    L.nt = 0;
+    return L;
+  }
+  // band pieces of the unit (merge inputs made by attention)
+  __device__ static int band_pieces(const Smem &S, const PieceList &L) {
+    return L.kind == kShort ? 1 : nonempty(S, 1, L.b0, L.b1);
+  }
+  // what the unit's count must reach: its band entries that exist (pieces,
+  // or groups with a piece) and, without a grid barrier before the bands,
+  // its tail pieces
+  __device__ static int unit_target(const StepParams &p, const Smem &S, const PieceList &L) {
+    int n = 0;
+    if (L.kind == kGroupList) {
+#pragma unroll 1
+      for (int k = L.b0 / kGroupCtas; k <= L.b1 / kGroupCtas; ++k) {
+        int lo, hi;
+        group_ctas(L, k, &lo, &hi);
+        n += nonempty(S, 1, lo, hi) > 0;
+      }
+    } else {
+      n = band_pieces(S, L);
+    }
+    if (p.mode != MODE_DECODE) n += nonempty(S, 0, L.ca0, L.ca0 + L.nt - 1);
+    return n;
+  }
+  __device__ static const float *piece_at(const StepParams &p, const Smem &S, const PieceList &L, int hh, int i) {
+    const int U = p.B * p.Hkv, u = L.u;
+    if (i < L.nb) {
+      if (L.kind == kShort) return p.part_b + ((size_t)u * G + hh) * kPartStride;
+      if (L.kind == kCtas) {
+        const int c = L.b0 + i;
+        if (S.spanB[c] >= S.spanB[c + 1]) return nullptr;
+        return p.part_b + ((size_t)(U + u + c) * G + hh) * kPartStride;
+      }
+      const int k = L.b0 / kGroupCtas + i;
+      int lo, hi;
+      group_ctas(L, k, &lo, &hi);
+      if (nonempty(S, 1, lo, hi) == 0) return nullptr;
+      return p.part_g + ((size_t)(u + k) * G + hh) * kPartStride;
+    }
+    if (SINK && i >= L.nb + L.nt) return p.part_s + ((size_t)u * G + hh) * kPartStride;  // the sink
+    const int c = L.ca0 + (i - L.nb);
+    if (S.spanA[c] >= S.spanA[c + 1]) return nullptr;
+    return p.part_a + ((size_t)(u + c) * G + hh) * kPartStride;
+  }
+
+  // Merge of a unit (group < 0) or of CTA group `group` of its long band.
+  // The G heads are merged concurrently by kWarps / G warps each, split by
+  // dims: every warp of a head goes through the whole list for its slice of
+  // the head's dims (lane j holds entry j's pointer, maximum and sum; up to
+  // kBatch entries' outputs are in flight at once), so a list of up to
+  // kBatch entries costs one trip to L2 and no warp waits for another.  Each class
+  // (band, tail) is summed at its maximum over the entries holding tokens.
+  // A unit: the cached summary of a hit head with the band state (giving
+  // AS_{1:m-r}), then the tail state (giving the output).  A group: the band
+  // state, written as a partial like a piece's.  The count the merge
+  // answered is cleared for the next launch.
+  __device__ static void merge_unit(const StepParams &p, const Smem &S, const PieceList &L, int group) {
+    unsigned long long *trace = cta_trace(p);
+    const unsigned long long t_in = trace && threadIdx.x == 0 ? globaltimer() : 0ull;
+    merge_heads(p, S, L, group);
+    if (trace && threadIdx.x == 0) {
+      // merge statistics: total time, count, longest merge and its entries
+      const unsigned long long dt = globaltimer() - t_in;
+      trace[18] += dt;
+      trace[19] += 1;
+      if (dt > trace[20]) {
+        trace[20] = dt;
+        trace[21] = (unsigned long long)L.n;
+      }
+    }
+    __syncwarp();
+  }
+
+  // N consecutive floats of a partial or ring row (L2, not L1: written by
+  // other CTAs), and their store
   template <int N>
   __device__ static void load_dims(const float *src, float (&v)[N]) {
-    if constexpr (N == 4) {
-      const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
-      v[0] = x.x;
-      v[1] = x.y;
-      v[2] = x.z;
-      v[3] = x.w;
-    } else if constexpr (N == 2) {
+    if constexpr (N == 2) {
       const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
       v[0] = x.x;
       v[1] = x.y;
@@ -1100,39 +1774,64 @@ struct Step {
   }
   template <int N>
   __device__ static void store_dims(float *dst, const float (&v)[N]) {
-    if constexpr (N == 4)
-      *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-    else if constexpr (N == 2)
+    if constexpr (N == 2)
       *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
     else
       dst[0] = v[0];
   }
+  // Log-domain states (base 2): a set of members (m_i, l_i, o_i) combines
+  // at the largest m_i among those with l_i > 0, each weighted by
+  // 2^(m_i - M).
   // the weight of a member (m, l) in a state at maximum M
-  // (a member with nothing in it, l == 0 or m == -inf, weighs 0)
-  __device__ static float mweight(float m, float l, float M) { return l > 0.f && m > -INFINITY ? ex2(m - M) : 0.f; }
+  __device__ static float mweight(float m, float l, float M) { return l > 0.f ? ex2(m - M) : 0.f; }
 
-  // A log-domain state (base 2) over this lane's dims: maximum, sum, weighted values.
-  struct Cls {
-    float M, L, O[kDL];
-  };
-  // The states of one head's list for this lane's dims [dl, dl + kDL):
-  // entries 0..n-1 (entry(i) -> partial, or null: empty), the first nb of
-  // the band class, the rest of the tail class.  Each class is summed at its
-  // maximum over the entries holding tokens.  Lane j holds entry j's
-  // pointer, maximum and sum; up to kBatch entries' outputs are in flight at
-  // once, so a list of up to kBatch entries costs one trip to L2.
-  template <class F>
-  __device__ static void merge_list(int n, int nb, F entry, int dl, Cls &band, Cls &tail) {
-    constexpr int kBatch = 8;
-    const int lane = lane_id();
-    band.M = tail.M = -INFINITY;
-    band.L = tail.L = 0.f;
+  __device__ static void merge_heads(const StepParams &p, const Smem &S, const PieceList &L, int group) {
+    constexpr int kWPH = kWarps / G;         // warps per head
+    constexpr int kDW = kHeadDim / kWPH;     // dims of a head per warp
+    constexpr int kDL = kDW >= 32 ? kDW / 32 : 1;  // dims per lane
+    constexpr int kLanes = kDW / kDL;        // lanes holding dims
+    constexpr int kBatch = kDL == 2 ? 10 : 12;  // entries whose outputs a warp asks for at once
+    static_assert(kDL == 1 || kDL == 2, "dims per lane");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int hh = warp / kWPH, wi = warp % kWPH;
+    const int u = L.u, b = u / p.Hkv, g = u - b * p.Hkv;
+    const int bh = b * p.Hq + g * G + hh;
+    const int n = L.n, nb = L.nb;
+    const bool fin = group < 0, decode = p.mode == MODE_DECODE;
+    // this lane's dims of the head: [dl, dl + kDL) (lanes past kLanes hold
+    // copies of the last lane's, never written)
+    const int dl = wi * kDW + min(lane, kLanes - 1) * kDL;
+    const bool own = lane < kLanes;
+    // Loads here are unconditional, from valid addresses (an empty entry
+    // reads a zero partial), so that no instruction waits on their data
+    // before it is used.  The cached rectified summary of a hit head:
+    bool hit = false;
+    float c_lse = 0.f, c_o[kDL];
+    if (fin && decode) {
+      const int pos = S.X[bh];
+      hit = pos >= 1;
+      const int64_t slot = (int64_t)bh * p.K + (hit ? pos % p.K : 0);
+      c_lse = p.ring_lse[slot];
+      load_dims<kDL>(p.ring_o + slot * kHeadDim + dl, c_o);
+    }
+    // the append: slot pos mod K of the head's rings (the fused append
+    // writes it here; otherwise the append kernel does, from staging)
+    const int pos = S.u_pos[u];
+    const bool app = fin && decode && p.app_o && len_ok(p, pos);
+    const int64_t app_slot = (int64_t)bh * p.K + pos % p.K;
+
+    // The whole list for this head, 32 entries at a time (lane j: entry
+    // j's pointer, maximum and sum) and up to kBatch outputs in flight:
+    // every warp of the head goes through all entries for its dims, so no
+    // warp waits for another.  Each class (band, tail) is summed at its
+    // maximum over the entries holding tokens.
+    float Mb = -INFINITY, Lb = 0.f, Ob[kDL], Mt = -INFINITY, Lt = 0.f, Ot[kDL];
 #pragma unroll
-    for (int i = 0; i < kDL; ++i) band.O[i] = tail.O[i] = 0.f;
+    for (int i = 0; i < kDL; ++i) Ob[i] = Ot[i] = 0.f;
 #pragma unroll 1
     for (int base = 0; base < n; base += 32) {
       const int cnt = min(32, n - base);
-      const float *src = lane < cnt ? entry(base + lane) : nullptr;
+      const float *src = lane < cnt ? piece_at(p, S, L, hh, base + lane) : nullptr;
       if (!src) src = g_zero_partial;
       const float2 ml = __ldcg(reinterpret_cast<const float2 *>(src + kHeadDim));
       const unsigned long long sp = reinterpret_cast<unsigned long long>(src);
@@ -1140,36 +1839,36 @@ struct Step {
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
         load_dims<kDL>(reinterpret_cast<const float *>(__shfl_sync(kFull, sp, k)) + dl, ov[k]);
-      const bool isb = base + lane < nb;
-      float mb = isb && ml.y > 0.f ? ml.x : -INFINITY, mt = !isb && ml.y > 0.f ? ml.x : -INFINITY;
+      const bool band = base + lane < nb;
+      float mb = band && ml.y > 0.f ? ml.x : -INFINITY, mt = !band && ml.y > 0.f ? ml.x : -INFINITY;
 #pragma unroll
       for (int o2 = 16; o2 >= 1; o2 >>= 1) {
         mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o2));
         mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, o2));
       }
-      // what earlier rounds summed, at the new maxima
-      mb = fmaxf(band.M, mb);
-      mt = fmaxf(tail.M, mt);
-      const float rb = mweight(band.M, band.L, mb), rt = mweight(tail.M, tail.L, mt);
-      band.L *= rb;
-      tail.L *= rt;
+      // what earlier rounds summed (none in the common case), at the new maxima
+      mb = fmaxf(Mb, mb);
+      mt = fmaxf(Mt, mt);
+      const float rb = mweight(Mb, Lb, mb), rt = mweight(Mt, Lt, mt);
+      Lb *= rb;
+      Lt *= rt;
 #pragma unroll
       for (int i = 0; i < kDL; ++i) {
-        band.O[i] *= rb;
-        tail.O[i] *= rt;
+        Ob[i] *= rb;
+        Ot[i] *= rt;
       }
-      band.M = mb;
-      tail.M = mt;
-      const float wgt = mweight(ml.x, ml.y, isb ? band.M : tail.M);
-      const float wb = isb ? wgt : 0.f, wt = isb ? 0.f : wgt;
-      float lbs = wb * ml.y, lts = wt * ml.y;
+      Mb = mb;
+      Mt = mt;
+      const float w = mweight(ml.x, ml.y, band ? Mb : Mt);
+      const float wb = band ? w : 0.f, wt = band ? 0.f : w;
+      float lb = wb * ml.y, lt = wt * ml.y;
 #pragma unroll
       for (int o2 = 16; o2 >= 1; o2 >>= 1) {
-        lbs += __shfl_xor_sync(kFull, lbs, o2);
-        lts += __shfl_xor_sync(kFull, lts, o2);
+        lb += __shfl_xor_sync(kFull, lb, o2);
+        lt += __shfl_xor_sync(kFull, lt, o2);
       }
-      band.L += lbs;
-      tail.L += lts;
+      Lb += lb;
+      Lt += lt;
 #pragma unroll 1
       for (int k0 = 0; k0 < cnt; k0 += kBatch) {
         if (k0 > 0) {
@@ -1179,550 +1878,314 @@ struct Step {
         }
 #pragma unroll
         for (int k = 0; k < kBatch; ++k) {
-          // past the round's entries the batch wraps onto lanes already summed
           const int j = (k0 + k) & 31;
-          const bool in = k0 + k < cnt;
-          float xb = __shfl_sync(kFull, wb, j), xt = __shfl_sync(kFull, wt, j);
-          xb = in ? xb : 0.f;
-          xt = in ? xt : 0.f;
+          const float xb = __shfl_sync(kFull, wb, j), xt = __shfl_sync(kFull, wt, j);
 #pragma unroll
           for (int i = 0; i < kDL; ++i) {
-            band.O[i] = fmaf(xb, ov[k][i], band.O[i]);
-            tail.O[i] = fmaf(xt, ov[k][i], tail.O[i]);
+            Ob[i] = fmaf(xb, ov[k][i], Ob[i]);
+            Ot[i] = fmaf(xt, ov[k][i], Ot[i]);
           }
         }
       }
     }
-  }
-  // a (+)= x, each state at its own maximum
-  __device__ static void join(Cls &a, float xm, float xl, const float (&xo)[kDL]) {
-    const float M = fmaxf(a.L > 0.f ? a.M : -INFINITY, xl > 0.f ? xm : -INFINITY);
-    const float wa = mweight(a.M, a.L, M), wx = mweight(xm, xl, M);
-    a.L = wa * a.L + wx * xl;
+    // band: the cached summary (a state of sum 1 at its ln-LSE) with the
+    // band state
+    const float cm = hit ? c_lse * kLog2e : -INFINITY;
+    const float M = fmaxf(cm, Lb > 0.f ? Mb : -INFINITY);
+    const float wc = mweight(cm, hit ? 1.f : 0.f, M), wbb = mweight(Mb, Lb, M);
+    const float La = (hit ? wc : 0.f) + wbb * Lb;
+    float Oa[kDL];
 #pragma unroll
-    for (int i = 0; i < kDL; ++i) a.O[i] = wa * a.O[i] + wx * xo[i];
-    a.M = M;
-  }
-
-  // The owner's merge of one head bh by all the CTA's warps: before the long
-  // bands (pass 0) a hit or a miss of a unit without a long band, after them
-  // (pass 1) a miss of a unit with one.  AS = [cached] (+) [boundary] (+)
-  // band tiles [0, nbt) (+) long-band entries; the output AS (+) tail tiles
-  // (+) sink tiles; the rectified summary AS_{1:m-r} goes to the ring slot
-  // of position m (fused append) or to the staging area.  Warp w sums list
-  // entries w, w + 8, ... (4 dims per lane) per class; the CTA then combines
-  // the warps' states in a fixed order.  A hit whose band starts inside a
-  // window tile has a boundary piece, streamed before the merge into warp
-  // bd_w's slot of S.bd.  pos: the head's decision (-2: not known yet).
-  // All threads call it.
-  struct St {
-    float M, L, O[4];
-  };
-  __device__ static void st_join(St &a, float xm, float xl, const float4 &xo) {
-    const float M = fmaxf(a.L > 0.f ? a.M : -INFINITY, xl > 0.f ? xm : -INFINITY);
-    const float wa = mweight(a.M, a.L, M), wx = mweight(xm, xl, M);
-    a.L = wa * a.L + wx * xl;
-    a.O[0] = wa * a.O[0] + wx * xo.x;
-    a.O[1] = wa * a.O[1] + wx * xo.y;
-    a.O[2] = wa * a.O[2] + wx * xo.z;
-    a.O[3] = wa * a.O[3] + wx * xo.w;
-    a.M = M;
-  }
-  __device__ static void merge_one(const StepParams &p, const Smem &S, int bh, bool long_pass, int pos, int bd_w) {
-    const int b = bh / p.Hq, h = bh - b * p.Hq, g = h / G, hh = h - g * G, u = b * p.Hkv + g;
-    const int lane = lane_id(), w = warp_id(), tid = threadIdx.x;
-    const bool decode = p.mode == MODE_DECODE;
-    if (pos == -2) pos = decision(p, S, bh);
-    int c0, c1;
-    long_run(S, u, &c0, &c1);
-    const bool late = pos < 1 && c1 >= c0;
-    if (late != long_pass) return;
-    const int m = S.um[u];
-    if (m <= 0) {
-      // a length outside the cache: zero output, no append
-      if (tid < kHeadDim) p.out[(int64_t)bh * kHeadDim + tid] = 0.f;
-      if (tid == 0) {
-        if (p.out_lse) p.out_lse[bh] = -INFINITY;
-        if (p.match_pos_out) p.match_pos_out[bh] = -1;
+    for (int i = 0; i < kDL; ++i) Oa[i] = (hit ? wc * c_o[i] : 0.f) + wbb * Ob[i];
+    if (!fin) {
+      // the group's partial: the raw state, in a piece partial's layout
+      float *dst = p.part_g + ((size_t)(u + group) * G + hh) * kPartStride;
+      if (own) store_dims<kDL>(dst + dl, Oa);
+      if (wi == 0 && lane == 0) {
+        dst[kHeadDim] = M;
+        dst[kHeadDim + 1] = La;
       }
-      block_sync();
-      return;
-    }
-    int nbt;
-    const bool has_bd = boundary_item(p, S, bh, pos, &nbt).kind == 3 && !long_pass;
-    if (pos >= 1) {
-      c0 = 0;
-      c1 = -1;
     } else {
-      nbt = p.tc.nbw;
-    }
-    unsigned long long *tr = p.trace && lane == 0 && w <= 1 ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
-    if (tr && w == 0) tr[18] = globaltimer();
-    // the cached rectified summary of a hit (a state of sum 1 at its ln-LSE), by warp 1
-    const int64_t cslot = (int64_t)bh * p.K + (pos >= 1 ? pos % p.K : 0);
-    float c_lse = 0.f;
-    float4 c_o = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (pos >= 1 && w == 1) {
-      c_lse = __ldcg(p.ring_lse + cslot);
-      c_o = __ldcg(reinterpret_cast<const float4 *>(p.ring_o + cslot * kHeadDim) + lane);
-    }
-    const int nl = long_entries(c0, c1);
-    const int nt = p.tc.ntt + (p.sink_piece ? p.tc.nsk : 0);
-    const int n = nbt + nl + nt, nb = nbt + nl;
-    const float *tiles = p.part_w + (size_t)u * p.tc.nt * G * kPartStride + hh * kPartStride;
-    auto entry = [&](int i) -> const float * {
-      if (i < nbt) return tiles + (size_t)i * G * kPartStride;
-      i -= nbt;
-      if (i < nl) return long_entry(p, u, c0, c1, i, hh);
-      i -= nl;
-      return tiles + (size_t)(p.tc.nbw + i) * G * kPartStride;
-    };
-    St band, tail;
-    band.M = tail.M = -INFINITY;
-    band.L = tail.L = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) band.O[i] = tail.O[i] = 0.f;
-    constexpr int kE = 8;  // entries a warp has in flight
-#pragma unroll 1
-    for (int i0 = w; i0 < n; i0 += kWarps * kE) {
-      float2 ml[kE];
-      float4 ov[kE];
-#pragma unroll
-      for (int e = 0; e < kE; ++e) {
-        const int i = i0 + e * kWarps;
-        const float *src = i < n ? entry(i) : g_zero_partial;
-        ml[e] = __ldcg(reinterpret_cast<const float2 *>(src + kHeadDim));
-        ov[e] = __ldcg(reinterpret_cast<const float4 *>(src) + lane);
-      }
-#pragma unroll
-      for (int e = 0; e < kE; ++e) {
-        const int i = i0 + e * kWarps;
-        if (i < nb) st_join(band, ml[e].x, ml[e].y, ov[e]);
-        else if (i < n) st_join(tail, ml[e].x, ml[e].y, ov[e]);
-      }
-    }
-    if (pos >= 1 && w == 1) st_join(band, c_lse * kLog2e, 1.f, c_o);
-    if (tr) tr[w == 0 ? 13 : 19] = globaltimer();
-    if (has_bd && w == 0) {
-      const float *x = S.bd + (size_t)bd_w * kPartStride;
-      st_join(band, x[kHeadDim], x[kHeadDim + 1], reinterpret_cast<const float4 *>(x)[lane]);
-    }
-    // the warps' states, in warp 7's idle stage ring
-    float *red = reinterpret_cast<float *>(S.stage + (size_t)7 * kStages * kStageBytes);
-#pragma unroll
-    for (int cls = 0; cls < 2; ++cls) {
-      const St &st = cls ? tail : band;
-      float *d = red + (w * 2 + cls) * kPartStride;
-      reinterpret_cast<float4 *>(d)[lane] = make_float4(st.O[0], st.O[1], st.O[2], st.O[3]);
-      if (lane == 0) *reinterpret_cast<float2 *>(d + kHeadDim) = make_float2(st.M, st.L);
-    }
-    if (tr && w == 0) tr[14] = globaltimer();
-    block_sync();
-    if (tr && w == 0) tr[15] = globaltimer();
-    if (tid < kHeadDim) {
-      float MB = -INFINITY, MT = -INFINITY;
-#pragma unroll
-      for (int ww = 0; ww < kWarps; ++ww) {
-        const float *bs = red + (ww * 2) * kPartStride, *ts = bs + kPartStride;
-        if (bs[kHeadDim + 1] > 0.f) MB = fmaxf(MB, bs[kHeadDim]);
-        if (ts[kHeadDim + 1] > 0.f) MT = fmaxf(MT, ts[kHeadDim]);
-      }
-      float LB = 0.f, OB = 0.f, LT = 0.f, OT = 0.f;
-#pragma unroll
-      for (int ww = 0; ww < kWarps; ++ww) {
-        const float *bs = red + (ww * 2) * kPartStride, *ts = bs + kPartStride;
-        const float wb = mweight(bs[kHeadDim], bs[kHeadDim + 1], MB), wt = mweight(ts[kHeadDim], ts[kHeadDim + 1], MT);
-        LB += wb * bs[kHeadDim + 1];
-        OB = fmaf(wb, bs[tid], OB);
-        LT += wt * ts[kHeadDim + 1];
-        OT = fmaf(wt, ts[tid], OT);
-      }
-      const int64_t qp = qpos(p, b);
-      if (decode) {
+      if (p.as_o || app) {
         // AS_{1:m-r}, normalised, with its ln-LSE: the rectified summary
         // the ring keeps for position m
-        const float as = LB > 0.f ? OB * rcp_approx(LB) : 0.f;
-        const float lse = LB > 0.f ? (MB + lg2_approx(LB)) * kLn2 : -INFINITY;
-        const int64_t slot = (int64_t)bh * p.K + qp % p.K;
-        if (p.app_o && len_ok(p, qp)) {
-          p.app_o[slot * kHeadDim + tid] = as;
-          if (tid == 0) {
-            p.app_lse[slot] = lse;
-            if (h == 0) p.app_pos[(int64_t)b * p.K + qp % p.K] = (int32_t)qp;
+        const float inv = La > 0.f ? rcp_approx(La) : 0.f;
+        float as[kDL];
+#pragma unroll
+        for (int i = 0; i < kDL; ++i) as[i] = Oa[i] * inv;
+        const float lse = La > 0.f ? (M + lg2_approx(La)) * kLn2 : -INFINITY;
+        if (app) {
+          // a match at p = m - K reads the slot the append overwrites: every
+          // warp of the head has read the cached summary's LSE before the
+          // first warp stores the new one (each lane rewrites only the dims
+          // it read itself)
+          named_sync(2 + hh, kWPH * 32);
+          if (own) store_dims<kDL>(p.app_o + app_slot * kHeadDim + dl, as);
+          if (wi == 0 && lane == 0) {
+            p.app_lse[app_slot] = lse;
+            if (hh == 0 && g == 0) p.app_pos[(int64_t)b * p.K + pos % p.K] = pos;
           }
-        } else if (p.as_o) {
-          p.as_o[(int64_t)bh * kHeadDim + tid] = as;
-          if (tid == 0) p.as_lse[bh] = lse;
-        }
-        if (tid == 0 && p.match_pos_out) p.match_pos_out[bh] = pos;
-      }
-      // the output: AS with the tail (and the sink)
-      const float M2 = fmaxf(LB > 0.f ? MB : -INFINITY, LT > 0.f ? MT : -INFINITY);
-      const float wa = mweight(MB, LB, M2), wt = mweight(MT, LT, M2);
-      const float L2 = wa * LB + wt * LT;
-      p.out[(int64_t)bh * kHeadDim + tid] = L2 > 0.f ? (wa * OB + wt * OT) * rcp_approx(L2) : 0.f;
-      if (tid == 0 && p.out_lse) p.out_lse[bh] = L2 > 0.f ? (M2 + lg2_approx(L2)) * kLn2 : -INFINITY;
-    } else if (decode && tid < kHeadDim + kHeadDim / kPer) {
-      // the step's query, for the ring (fused append) or the append kernel
-      const int64_t qp = qpos(p, b);
-      const int c = tid - kHeadDim;
-      const uint4 qv = reinterpret_cast<const uint4 *>(p.q)[((int64_t)bh * p.q_stride + p.q_offset) / kPer + c];
-      if (p.app_o && len_ok(p, qp))
-        reinterpret_cast<uint4 *>(p.app_q)[((int64_t)bh * p.K + qp % p.K) * (kHeadDim / kPer) + c] = qv;
-      else if (p.as_o)
-        reinterpret_cast<uint4 *>(p.stage_q)[(int64_t)bh * (kHeadDim / kPer) + c] = qv;
-    }
-    block_sync();  // the combine area is free again
-  }
-
-  // The long bands: this CTA's span, piece by piece (one per unit it
-  // meets); the CTA's warps take the piece's stages round-robin, then
-  // combine their states into the piece's partial; pieces are counted per
-  // unit (or per CTA group, whose last CTA merges the group).
-  struct LongCur {
-    int u, lo, hi, k;  // piece: unit, tokens [lo, hi]; the warp's next stage k (tokens lo + k * kStTok ..)
-  };
-  __device__ static bool piece_at(const StepParams &p, const Smem &S, int u, int64_t g0, int64_t g1, LongCur &C) {
-    const int U = n_units(p);
-#pragma unroll 1
-    for (; u < U; ++u) {
-      const int64_t a0 = S.off[u], z0 = S.off[u + 1];
-      if (a0 >= g1) return false;
-      const int64_t a = a0 > g0 ? a0 : g0, z = z0 < g1 ? z0 : g1;
-      if (a < z) {
-        C.u = u;
-        C.lo = (int)(lb(p) + (a - a0));
-        C.hi = (int)(lb(p) + (z - a0) - 1);
-        return true;
-      }
-    }
-    return false;
-  }
-  // the next stage of this warp from cursor C (kind -1: none left)
-  __device__ static Desc long_next(const StepParams &p, const Smem &S, LongCur &C, int64_t g0, int64_t g1) {
-    Desc d;
-    d.kind = -1;
-    d.u = d.a = d.cnt = 0;
-#pragma unroll 1
-    while (C.u >= 0) {
-      const int a = C.lo + C.k * kStTok;
-      if (a <= C.hi) {
-        d.kind = 1;
-        d.u = C.u;
-        d.a = a;
-        d.cnt = min(C.hi - a + 1, kStTok);
-        C.k += kWarps;
-        return d;
-      }
-      if (!piece_at(p, S, C.u + 1, g0, g1, C)) C.u = -1;
-      C.k = warp_id();
-    }
-    return d;
-  }
-
-  // Merge of CTA group k of unit u's long band: its CTA pieces into the group
-  // partial (the raw state).
-  __device__ static void merge_group(const StepParams &p, int u, int c0, int c1, int k) {
-    const int lane = lane_id(), hh = warp_id() / kWPH, wi = warp_id() % kWPH;
-    const int dl = wi * kDW + min(lane, kLanes - 1) * kDL;
-    const int a = max(c0, k * kGroupCtas), z = min(c1, k * kGroupCtas + kGroupCtas - 1);
-    auto entry = [&](int i) -> const float * { return p.part_c + ((size_t)(u + a + i) * G + hh) * kPartStride; };
-    Cls band, tail;
-    merge_list(z - a + 1, z - a + 1, entry, dl, band, tail);
-    float *dst = p.part_g + ((size_t)(u + k) * G + hh) * kPartStride;
-    if (lane < kLanes) store_dims<kDL>(dst + dl, band.O);
-    if (wi == 0 && lane == 0) *reinterpret_cast<float2 *>(dst + kHeadDim) = make_float2(band.M, band.L);
-  }
-
-  // The CTA's combine of its warps' states of a piece of unit u: part_x ->
-  // part_c slot u + c, the warps in a fixed order.
-  __device__ static void combine_warps(const StepParams &p, int u) {
-    const int c = blockIdx.x;
-    const float *x = p.part_x + (size_t)c * kWarps * G * kPartStride;
-    float *dst = p.part_c + (size_t)(u + c) * G * kPartStride;
-#pragma unroll 1
-    for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) {
-      const int hh = e / kHeadDim, dd = e % kHeadDim;
-      float2 ml[kWarps];
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        ml[w] = __ldcg(reinterpret_cast<const float2 *>(x + (w * G + hh) * kPartStride + kHeadDim));
-        if (ml[w].y > 0.f) M = fmaxf(M, ml[w].x);
-      }
-      float L = 0.f, O = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float wt = mweight(ml[w].x, ml[w].y, M);
-        L += wt * ml[w].y;
-        O = fmaf(wt, __ldcg(x + (w * G + hh) * kPartStride + dd), O);
-      }
-      dst[hh * kPartStride + dd] = O;
-      if (dd == 0) *reinterpret_cast<float2 *>(dst + hh * kPartStride + kHeadDim) = make_float2(M, L);
-    }
-  }
-
-  __device__ static void long_bands(const StepParams &p, const Smem &S, Ring &R) {
-    const int c = blockIdx.x;
-    if (c >= *S.Pl) return;
-    const int64_t g0 = span(S, c), g1 = span(S, c + 1);
-    LongCur F, C;  // fetch and consume cursors
-    if (!piece_at(p, S, unit_of(p, S, g0), g0, g1, F)) return;
-    F.k = warp_id();
-    C = F;
-    int32_t id[2];
-    // prime
-    Desc nx = long_next(p, S, F, g0, g1);
-#pragma unroll 1
-    for (int j = 0; j < kStages && nx.kind >= 0; ++j) {
-      load_ids(p, nx, id);
-      issue(p, R, nx, id);
-      nx = long_next(p, S, F, g0, g1);
-    }
-    if (nx.kind >= 0) load_ids(p, nx, id);
-    float2 q[G][kAPairs];
-    Att A;
-#pragma unroll 1
-    while (C.u >= 0) {
-      const int u = C.u;
-      att_init(A);
-      load_query(p, S, u, q);
-#pragma unroll 1
-      for (;;) {
-        const int a = C.lo + C.k * kStTok;
-        if (a > C.hi || *S.abort) break;
-        const uint32_t n = R.used;
-        if (wait_stage(p, S, R, n)) att_stage(A, q, stage_buf(R, n), a, R.rows[n % kStages], 1, 0x7fffffff);
-        R.used++;
-        C.k += kWarps;
-        done_with_stage();
-        if (nx.kind >= 0) {
-          issue(p, R, nx, id);
-          nx = long_next(p, S, F, g0, g1);
-          if (nx.kind >= 0) load_ids(p, nx, id);
-        }
-      }
-      att_finish(A, p.part_x + ((size_t)c * kWarps + warp_id()) * G * kPartStride);
-      block_sync();  // the warp states are read back (from L2) by the other threads of the CTA
-      combine_warps(p, u);
-      block_sync();
-      // count the piece: in its CTA group (two-level) or in the unit
-      int c0, c1;
-      long_run(S, u, &c0, &c1);
-      const int k = c / kGroupCtas;
-      if (threadIdx.x == 0) {
-        int act = 0;
-        if (grouped(c0, c1)) {
-          const int a0 = max(c0, k * kGroupCtas), z0 = min(c1, k * kGroupCtas + kGroupCtas - 1);
-          const uint32_t old = atom_add_acq_rel_u32(S.group_done + u + k, 1u);
-          act = (int)old + 1 == z0 - a0 + 1 ? 1 : 0;
         } else {
-          atom_add_acq_rel_u32(S.unit_done + u, 1u);
-        }
-        *S.flag = act;
-      }
-      block_sync();
-      if (*S.flag) {
-        // the last CTA of the group merges it, then counts it in the unit
-        merge_group(p, u, c0, c1, k);
-        block_sync();
-        if (threadIdx.x == 0) {
-          atom_add_acq_rel_u32(S.unit_done + u, 1u);
+          if (own) store_dims<kDL>(p.as_o + (int64_t)bh * kHeadDim + dl, as);
+          if (wi == 0 && lane == 0) p.as_lse[bh] = lse;
         }
       }
-      // the next piece
-      if (!piece_at(p, S, u + 1, g0, g1, C)) C.u = -1;
-      C.k = warp_id();
+      // the output: the band state with the tail state
+      const float M2 = fmaxf(La > 0.f ? M : -INFINITY, Lt > 0.f ? Mt : -INFINITY);
+      const float wa = mweight(M, La, M2), wtt = mweight(Mt, Lt, M2);
+      const float L2 = wa * La + wtt * Lt;
+      const float inv = L2 > 0.f ? rcp_approx(L2) : 0.f;
+      float o[kDL];
+#pragma unroll
+      for (int i = 0; i < kDL; ++i) o[i] = (wa * Oa[i] + wtt * Ot[i]) * inv;
+      if (own) store_dims<kDL>(p.out + (int64_t)bh * kHeadDim + dl, o);
+      if (p.out_lse && wi == 0 && lane == 0) p.out_lse[bh] = L2 > 0.f ? (M2 + lg2_approx(L2)) * kLn2 : -INFINITY;
     }
+    if (tid == 0) {
+      if (fin)
+        p.unit_done[u] = 0;
+      else
+        p.group_done[u + group] = 0;
+    }
+    consumer_sync();
   }
 
-  // Wait (bounded, thread 0 for the CTA) until a count reaches target.
-  __device__ static void wait_count(const StepParams &p, const Smem &S, const uint32_t *ctr, uint32_t target) {
+  // After a piece's partial is written: count it.  Returns what the count
+  // completes: 0 nothing, 1 CTA group *k of the unit's long band (merge it
+  // first), 2 the unit (every CTA knows how many pieces each unit and group
+  // has, so no grid barrier is needed before the merges).  A long-band
+  // piece of a two-level unit counts in its CTA group.  A decode step's tail
+  // pieces are not counted: they all finish before the grid barrier, which
+  // orders them before every merge (so a short band completes its unit).
+  __device__ static int piece_count(const StepParams &p, const Smem &S, int u, int ph, bool is_short, int *k) {
+    const bool decode = p.mode == MODE_DECODE;
+    if (decode && ph == 0) return 0;
+    // a short band is its unit's only band piece, and a decode step's tail
+    // pieces all finished before the grid barrier: its CTA merges the unit
+    // without counting
+    if (decode && is_short) return 2;
+    *k = blockIdx.x / kGroupCtas;
+    // the barrier orders every thread's part of the partial before thread
+    // 0's count, whose release makes them visible to the CTA that merges
+    consumer_sync();
     if (threadIdx.x == 0) {
-      const long long t0 = clock64();
-      while (ld_acquire_u32(ctr) < target) {
-        if (*S.abort) break;
-        if (clock64() - t0 > (1LL << 31)) {
-          set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
-          *S.abort = 1;
-          break;
-        }
+      const PieceList L = unit_list(p, S, u);
+      int act = 0;
+      if (ph == 1 && !is_short && L.kind == kGroupList) {
+        int lo, hi;
+        group_ctas(L, *k, &lo, &hi);
+        const uint32_t old = atom_add_acq_rel_u32(&p.group_done[u + *k], 1u);
+        act = (int)(old + 1) == nonempty(S, 1, lo, hi) ? 1 : 0;
+      } else {
+        const uint32_t old = atom_add_acq_rel_u32(&p.unit_done[u], 1u);
+        act = (int)(old + 1) == unit_target(p, S, L) ? 2 : 0;
       }
+      *S.last = act;
     }
-    block_sync();
-  }
-  // Wait until unit u's long-band entries are all in.
-  __device__ static void wait_long(const StepParams &p, const Smem &S, int u) {
-    int c0, c1;
-    long_run(S, u, &c0, &c1);
-    wait_count(p, S, S.unit_done + u, (uint32_t)long_entries(c0, c1));
+    consumer_sync();
+    return *S.last;
   }
 
-  // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.
-  __device__ static void grid_barrier(const StepParams &p, const Smem &S) {
-    block_sync();
-    if (threadIdx.x == 0) {
-      unsigned long long *ctr = reinterpret_cast<unsigned long long *>(p.ctl + 2);
-      const unsigned long long old = atom_add_release_u64(ctr, 1ull);
-      const unsigned long long target = old - old % gridDim.x + gridDim.x;
-      const long long t0 = clock64();
-      while (ld_acquire_u64(ctr) < target) {
-        if (clock64() - t0 > (1LL << 31)) {
-          set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
-          *S.abort = 1;
-          break;
-        }
+  // The merges a count completed: group k (act 1), which then counts in the
+  // unit and may complete it, and the unit (act 2).
+  __device__ static void merge_chain(const StepParams &p, const Smem &S, int u, int act, int k) {
+    const PieceList Lu = unit_list(p, S, u);
+#pragma unroll 1
+    while (act) {
+      // the other CTAs' partials are visible: thread 0's count acquired
+      // them (or the grid barrier ordered them) before a consumer barrier
+      merge_unit(p, S, act == 1 ? group_list(Lu, k) : Lu, act == 1 ? k : -1);
+      if (act == 2) break;
+      // the group partial, ordered by the merge's closing barrier before
+      // thread 0's count releases it
+      if (threadIdx.x == 0) {
+        const uint32_t old = atom_add_acq_rel_u32(&p.unit_done[u], 1u);
+        *S.last = (int)(old + 1) == unit_target(p, S, Lu) ? 2 : 0;
       }
+      consumer_sync();
+      act = *S.last;
     }
-    block_sync();
-  }
-
-  __device__ static void stamp(const StepParams &p, int k) {
-    if (p.trace && threadIdx.x == 0) p.trace[(size_t)blockIdx.x * kTracePoints + k] = globaltimer();
   }
 
   // ---------------------------------------------------------------------
 
   __device__ static void run(const StepParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int s_abort, s_par, s_Pl;
-    __shared__ uint32_t s_flag;
-    __shared__ int64_t s_T;
-    __shared__ long long s_scan[kWarps];
-    __shared__ int s_dec[kOwnMax];
-    const int U = n_units(p), tid = threadIdx.x, w = warp_id();
+    __shared__ int s_mask[kStages];
+    __shared__ int s_abort, s_ready, s_last, s_par, s_nshort;
+    __shared__ uint32_t s_issued;
+    __shared__ int64_t s_span[2][kMaxGrid + 1];
+    __shared__ int s_ne[2][kMaxGrid + 1];
+    __shared__ long long s_short_max, s_band_tot[2], s_scan[kWarps];
+    const int n_units = p.B * p.Hkv, n_heads = p.B * p.Hq;
     Smem S;
     S.stage = smem;
+    S.qbuf = smem + kOffQ;
     S.full = reinterpret_cast<uint64_t *>(smem + kOffBar);
-    S.rows = reinterpret_cast<int *>(smem + kOffMask);
-    S.bd = reinterpret_cast<float *>(smem + kOffBd);
-    S.off = reinterpret_cast<int64_t *>(smem + kOffUnits);
-    S.um = reinterpret_cast<int32_t *>(S.off + U + 1);
+    S.empty = S.full + kStages;
+    S.qrot = reinterpret_cast<float *>(smem + kOffQrot);
+    S.red_o = reinterpret_cast<float *>(smem + kOffRedO);
+    S.red_l = reinterpret_cast<float *>(smem + kOffRedL);
+    S.red_m = reinterpret_cast<float *>(smem + kOffRedM);
+    S.X = reinterpret_cast<int32_t *>(smem + kOffX);
+    S.offA = reinterpret_cast<int64_t *>(smem + off_units(p.B, p.Hq, p.K));
+    S.offB = S.offA + (n_units + 1);
+    S.spanA = s_span[0];
+    S.spanB = s_span[1];
+    S.neA = s_ne[0];
+    S.neB = s_ne[1];
+    S.scp = S.offB + (n_units + 1);
+    S.u_pos = reinterpret_cast<int32_t *>(S.scp + (n_units + 1));
+    S.u_s = S.u_pos + n_units;
+    S.shortU = S.u_s + n_units;
+    S.runA = reinterpret_cast<short2 *>(S.shortU + n_units);
+    S.runB = S.runA + n_units;
+    S.n_short = &s_nshort;
+    S.short_max = &s_short_max;
+    S.band_tot = s_band_tot;
     S.scan = s_scan;
+    S.rope = p.B <= kRopeTab ? reinterpret_cast<float2 *>(smem + off_rope(p.B, p.Hq, p.Hkv, p.K)) : nullptr;
+    S.mask = s_mask;
     S.abort = &s_abort;
-    S.ntok = &s_T;
-    S.Pl = &s_Pl;
-    S.flag = &s_flag;
-    S.dec = s_dec;
-    S.rope = p.B <= kRopeTab && p.rope_mode != MAC_ROPE_NONE ? reinterpret_cast<float2 *>(smem + off_rope(U)) : nullptr;
-    S.pside = smem + off_pside(U, p.B);
-    S.qbuf = p.qslot ? smem + off_qbuf(U, p.B) : nullptr;
-    if (p.trace && tid == 0) p.trace[(size_t)blockIdx.x * kTracePoints + 16] = (unsigned long long)clock64();
-    stamp(p, 0);
-    if (tid < kWarps * kStages) mbar_init(smem_addr(&S.full[tid]), 1);
-    if (tid == 0) {
-      s_abort = 0;
-      // decode launches alternate between the two buffers of minima
-      s_par = (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u);
+    S.ready = &s_ready;
+    S.issued = &s_issued;
+    S.last = &s_last;
+    const bool decode = p.mode == MODE_DECODE;
+    const int tid = threadIdx.x;
+    unsigned long long *trace = tid < kConsumers ? cta_trace(p) : nullptr;
+    if (trace && tid == 0) {
+      trace[16] = (unsigned long long)clock64();
+      for (int k = 18; k < kTracePoints; ++k) trace[k] = 0;
     }
-    mbar_fence_init();
-    if (S.rope) {
+    stamp(trace, 0);
+    if (tid == 0) {
+      for (int i = 0; i < kStages; ++i) {
+        mbar_init(smem_addr(&S.full[i]), 1);
+        mbar_init(smem_addr(&S.empty[i]), kWarps);
+      }
+      s_abort = 0;
+      s_ready = 0;
+      s_issued = 0;
+      // decode launches alternate between the two buffers of minima; every
+      // CTA reads the count before the first grid barrier, and it only
+      // changes after every CTA has finished
+      s_par = decode ? (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u) : 0;
+      mbar_fence_init();
+    }
+    __syncthreads();  // the last barrier of all kThreads threads
+    const int n_bh = n_heads;
+    S.best = p.best + (size_t)s_par * n_bh;
+    S.best_next = p.best + (size_t)(s_par ^ 1) * n_bh;
+
+    if (tid >= kConsumers) {
+      producer_warp(p, S);
+      return;
+    }
+
+#pragma unroll 1
+    for (int u = tid; u < n_units; u += kConsumers) {
+      S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
+      S.u_s[u] = p.sink_f + 1;
+      if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
+        set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
+    }
+    if (decode) {
+      // every request's length, for the match (X holds the decisions only
+      // after the grid barrier)
+#pragma unroll 1
+      for (int b = tid; b < p.B; b += kConsumers) {
+        const int64_t m = (int64_t)p.pos_base[b] + p.pos_add - p.len_sub;
+        S.X[b] = m >= 1 && m <= p.max_len ? (int32_t)m : 0;
+      }
+    }
+    if (S.rope && p.rope_mode != MAC_ROPE_NONE) {
       // the rotation angles of every request's query (shared by its heads)
 #pragma unroll 1
-      for (int i = tid; i < p.B * (kHeadDim / 2); i += kThreads) {
+      for (int i = tid; i < p.B * (kHeadDim / 2); i += kConsumers) {
         const int b = i / (kHeadDim / 2), j = i % (kHeadDim / 2);
         float c, sn;
-        rope_angle(qpos(p, b), p.rope_f[j], &c, &sn);
+        rope_angle((int64_t)p.pos_base[b] + p.pos_add, p.rope_f[j], &c, &sn);
         S.rope[i] = make_float2(c, sn);
       }
     }
-#pragma unroll 1
-    for (int u = tid; u < U; u += kThreads) {
-      const int64_t m = qpos(p, u / p.Hkv) - p.len_sub;
-      const bool ok = len_ok(p, m);
-      S.um[u] = ok ? (int32_t)m : 0;
-      if (p.check_len && blockIdx.x == 0 && !ok) set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
-    }
-    block_sync();
-    S.best = p.best + (size_t)s_par * p.B * p.Hq;
-    S.best_next = p.best + (size_t)(s_par ^ 1) * p.B * p.Hq;
-    S.unit_done = p.unit_done + (size_t)s_par * U;
-    S.unit_done_next = p.unit_done + (size_t)(s_par ^ 1) * U;
-    S.group_done = p.group_done + (size_t)s_par * (U + kGroups);
-    S.group_done_next = p.group_done + (size_t)(s_par ^ 1) * (U + kGroups);
-    Ring R;
-    R.buf = smem + (size_t)w * kStages * kStageBytes;
-    R.bar0 = smem_addr(&S.full[w * kStages]);
-    R.rows = S.rows + w * kStages;
-    R.pside = S.pside + (size_t)w * kStages * kPosBytes;
-    R.qbuf = S.qbuf ? S.qbuf + (size_t)w * 2 * kQE : nullptr;
-    R.issued = R.used = 0;
-
-    // owned heads, merged by this CTA
-    const int NH = p.B * p.Hq;
-    int h0, h_end, hstep;
-    own_range(NH, &h0, &h_end, &hstep);
-    const int nown = h_end > h0 ? (h_end - h0 + hstep - 1) / hstep : 0;
-    const int nrnd = 1 + max(1, (nown + kWarps - 1) / kWarps);
-    // round 0: phase A; round r >= 1: the boundary pieces of owned heads
-    // (r-1) kWarps .. r kWarps - 1, then their merges.  One call site of the
-    // streaming loop for all rounds.
-#pragma unroll 1
-    for (int rnd = 0; rnd < nrnd; ++rnd) {
-      if (rnd == 1) {
-        stamp(p, 1);
-        grid_barrier(p, S);  // the minima of every head are final, the window tiles written
-        stamp(p, 2);
-        {
-          // nobody reads the other buffers in this launch: clear them for the next
-          const int i0 = blockIdx.x * kThreads + tid, di = gridDim.x * kThreads;
-#pragma unroll 1
-          for (int i = i0; i < p.B * p.Hq; i += di) S.best_next[i] = 0ull;
-#pragma unroll 1
-          for (int i = i0; i < U; i += di) S.unit_done_next[i] = 0u;
-#pragma unroll 1
-          for (int i = i0; i < U + kGroups; i += di) S.group_done_next[i] = 0u;
-        }
-        layout_long(p, S);
-        stamp(p, 3);
-      }
-      if (*S.abort && rnd > 0) continue;
-      stream(p, S, R, rnd, h0, hstep, nown);
-      if (rnd > 0) {
-        block_sync();  // the batch's boundary states are in S.bd
-#pragma unroll 1
-        for (int k = (rnd - 1) * kWarps; k < min(nown, rnd * kWarps) && !*S.abort; ++k)
-          merge_one(p, S, h0 + k * hstep, false, k < kOwnMax ? S.dec[k] : -2, k - (rnd - 1) * kWarps);
-      }
-    }
-    stamp(p, 4);
-    if (!*S.abort) long_bands(p, S, R);
-    stamp(p, 5);
-#pragma unroll 1
-    for (int bh = h0; bh < h_end; bh += hstep) {
-      const int k = (bh - h0) / hstep;
-      const int pos = k < kOwnMax ? S.dec[k] : decision(p, S, bh);
-      const int u = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / G;
-      int c0, c1;
-      long_run(S, u, &c0, &c1);
-      if (c1 < c0 || pos >= 1 || *S.abort) continue;
-      wait_long(p, S, u);
-      if (*S.abort) continue;
-      merge_one(p, S, bh, true, pos, 0);
-    }
-    stamp(p, 6);
-    drain(R);
-    block_sync();
+    consumer_sync();
+    layout_tails(p, S);
     if (tid == 0) {
-      // the last CTA to finish advances the launch count (which selects the
-      // buffers of minima and counts the next launch uses)
+      __threadfence_block();
+      *S.ready = 1;  // the producer may copy tail tiles
+    }
+    stamp(trace, 7);
+
+    uint32_t n = 0;  // stage uses consumed so far (every consumer counts the same sequence)
+    const int nchunks = decode ? match_chunks(p) : 0;
+    const int early = nchunks < kEarlyChunks ? nchunks : kEarlyChunks;
+    // the first match chunks, then the tail pieces (every head attends them
+    // whatever the match decides), whose fixed costs so overlap the copies
+    // of the other match chunks; full attention counts every piece at its
+    // unit, so it lays out the bands before the first piece
+    match_phase(p, S, n, 0, early);
+    // piece kinds: tails, short bands, long bands, then the merges no piece
+    // triggers; the band layout comes before the tails (full attention) or
+    // after the match and the decisions (decode): one call site
+#pragma unroll 1
+    for (int kind = 0; kind < 4; ++kind) {
+      if (kind == (decode ? 1 : 0)) {
+        if (decode) {
+          stamp(trace, 2);
+          match_phase(p, S, n, early, nchunks);
+          stamp(trace, 1);
+          grid_barrier(p, S);  // the minima of every head are final, the tail partials written
+          stamp(trace, 10);
+          decide(p, S, trace);
+          // nobody reads the other buffer in this launch: clear it for the next
+#pragma unroll 1
+          for (int i = blockIdx.x * kConsumers + tid; i < n_bh; i += gridDim.x * kConsumers) S.best_next[i] = 0ull;
+        }
+        layout_bands(p, S, trace);
+        stamp(trace, 3);
+      }
+      attend_kind(p, S, n, kind);
+    }
+    stamp(trace, 4);
+    if (tid == 0 && *S.abort) {
+      // after an abort the producer may have copies in flight into the
+      // stages: wait for them, bounded, before the CTA exits
+      const long long t0 = clock64();
+      while (*S.issued == 0 && clock64() - t0 < (1LL << 30)) {
+      }
+      const uint32_t nc = *S.issued;
+#pragma unroll 1
+      for (uint32_t j = nc > (uint32_t)kStages ? nc - kStages : 0u; j < nc; ++j) {
+        const uint32_t bar = smem_addr(&S.full[j % kStages]);
+        const long long t1 = clock64();
+        while (!mbar_try_wait(bar, (j / kStages) & 1u) && clock64() - t1 < (1LL << 30)) {
+        }
+      }
+    }
+    if (tid == 0) {
+      // the last CTA to finish advances the decode launch count; after a
+      // failed launch it also clears the piece counts the merges of that
+      // launch may have left
       __threadfence();
       const uint32_t old = atomicAdd(p.ctl + 4, 1u);
-      if (old == gridDim.x - 1) {
+      if (old == gridDim.x - 1) {  // every CTA of the launch has finished
         p.ctl[4] = 0;
-        atomicAdd(p.ctl + 6, 1u);
-      }
-      if (p.trace) {
-        p.trace[(size_t)blockIdx.x * kTracePoints + 17] = (unsigned long long)clock64();
-        p.trace[(size_t)blockIdx.x * kTracePoints + 7] = globaltimer();
+        if (decode) atomicAdd(p.ctl + 6, 1u);
+        if (*(volatile uint32_t *)p.ctl != 0)
+#pragma unroll 1
+          for (int u = 0; u < n_units; ++u) p.unit_done[u] = 0;
       }
     }
+    __syncwarp();
+    stamp(trace, 6);
+    if (trace && tid == 0) trace[17] = (unsigned long long)clock64();
+    __syncwarp();
   }
 };
 
-template <typename T, int G, bool PAGED>
+template <typename T, int G, bool PAGED, bool SINK>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
-  Step<T, G, PAGED>::run(p);
+  Step<T, G, PAGED, SINK>::run(p);
 }
 
 }  // namespace mac

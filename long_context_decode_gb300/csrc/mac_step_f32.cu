@@ -1,0 +1,11 @@
+// fp32 instantiations of the step kernel, without front-sink pieces.
+#include "mac_step_launch.cuh"
+
+namespace mac {
+cudaError_t launch_step_f32(const StepParams &p, int grid, cudaStream_t s) {
+  return launch_step_t<float, false>(p, grid, s);
+}
+int step_occupancy_f32(int G, bool paged, int B, int Hq, int Hkv, int K) {
+  return occupancy_t<float, false>(G, paged, B, Hq, Hkv, K);
+}
+}  // namespace mac

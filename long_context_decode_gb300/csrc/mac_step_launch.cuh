@@ -1,5 +1,5 @@
-// Launch helpers of the step kernel, instantiated per element type and GQA
-// group size in mac_step_{bf16,f32}_g{1,2,4,8}.cu (one translation unit
+// Launch helpers of the step kernel, instantiated once per element type and
+// front-sink variant in mac_step_{bf16,f32}{,_sink}.cu (one translation unit
 // each, so the builds run in parallel).
 #pragma once
 
@@ -7,52 +7,38 @@
 
 namespace mac {
 
-// per device: the dynamic shared memory limit set on the kernel (0: not yet)
-template <typename T, int G, bool PAGED>
-static size_t &step_smem_limit(int dev) {
-  static size_t limit[64] = {0};
-  return limit[dev];
-}
-
-template <typename T, int G, bool PAGED>
-static cudaError_t prepare_step(int U, int B, size_t *smem) {
-  using S = Step<T, G, PAGED>;
-  *smem = S::smem_bytes(U, B);
+template <typename T, int G, bool PAGED, bool SINK>
+static cudaError_t prepare_step(int B, int Hq, int Hkv, int K, size_t *smem) {
+  using S = Step<T, G, PAGED, SINK>;
+  *smem = S::smem_bytes(B, Hq, Hkv, K);
+  static size_t limit[64] = {0};  // per device: dynamic shared memory limit set on the kernel
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && step_smem_limit<T, G, PAGED>(dev) == 0) {
+  if (dev < 64 && limit[dev] == 0) {
     // the opt-in maximum per block, less the kernel's static shared memory
     int optin = 0;
     cudaFuncAttributes fa;
     if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess ||
-        (e = cudaFuncGetAttributes(&fa, step_kernel<T, G, PAGED>)) != cudaSuccess)
+        (e = cudaFuncGetAttributes(&fa, step_kernel<T, G, PAGED, SINK>)) != cudaSuccess)
       return e;
     size_t dyn = (size_t)optin - fa.sharedSizeBytes;
     if (dyn > kMaxSmem) dyn = kMaxSmem;
-    e = cudaFuncSetAttribute(step_kernel<T, G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    e = cudaFuncSetAttribute(step_kernel<T, G, PAGED, SINK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
     if (e != cudaSuccess) return e;
-    step_smem_limit<T, G, PAGED>(dev) = dyn;
+    limit[dev] = dyn;
   }
-  if (dev < 64 && *smem > step_smem_limit<T, G, PAGED>(dev)) return cudaErrorInvalidValue;
+  if (dev < 64 && *smem > limit[dev]) return cudaErrorInvalidValue;
   return cudaSuccess;
 }
 
 // Cooperative launch: the grid (one CTA per SM) is guaranteed co-resident,
-// which the grid barrier and the long-band counts of the step rely on.
-template <typename T, int G, bool PAGED>
-static cudaError_t launch_step_g(const StepParams &p_in, int grid, cudaStream_t s) {
-  using S = Step<T, G, PAGED>;
+// which the grid barriers of the step rely on.
+template <typename T, int G, bool PAGED, bool SINK>
+static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) {
   size_t smem = 0;
-  cudaError_t e = prepare_step<T, G, PAGED>(p_in.B * p_in.Hkv, p_in.B, &smem);
+  cudaError_t e = prepare_step<T, G, PAGED, SINK>(p.B, p.Hq, p.Hkv, p.K, &smem);
   if (e != cudaSuccess) return e;
-  // the warps' query entries, where shared memory allows them
-  StepParams p = p_in;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const size_t with_q = smem + (size_t)S::kQBuf;
-  p.qslot = dev < 64 && with_q <= step_smem_limit<T, G, PAGED>(dev) ? 1 : 0;
-  if (p.qslot) smem = with_q;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -63,28 +49,39 @@ static cudaError_t launch_step_g(const StepParams &p_in, int grid, cudaStream_t 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, step_kernel<T, G, PAGED>, p);
+  return cudaLaunchKernelEx(&cfg, step_kernel<T, G, PAGED, SINK>, p);
 }
 
-template <typename T, int G, bool PAGED>
-static int occupancy_g(int U, int B) {
+template <typename T, int G, bool PAGED, bool SINK>
+static int occupancy_g(int B, int Hq, int Hkv, int K) {
   size_t smem = 0;
-  if (prepare_step<T, G, PAGED>(U, B, &smem) != cudaSuccess) return 0;
+  if (prepare_step<T, G, PAGED, SINK>(B, Hq, Hkv, K, &smem) != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<T, G, PAGED>, kThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, step_kernel<T, G, PAGED, SINK>, kThreads, smem) !=
+      cudaSuccess)
     return 0;
   return n;
 }
 
-}  // namespace mac
-
-// One translation unit: element type T (name TN) and group size G.
-#define MAC_STEP_UNIT(T, TN, G)                                                                         \
-  namespace mac {                                                                                       \
-  cudaError_t launch_step_##TN##_g##G(const StepParams &p, int grid, cudaStream_t s) {                  \
-    return p.kv.paged ? launch_step_g<T, G, true>(p, grid, s) : launch_step_g<T, G, false>(p, grid, s); \
-  }                                                                                                     \
-  int step_occupancy_##TN##_g##G(bool paged, int U, int B) {                                            \
-    return paged ? occupancy_g<T, G, true>(U, B) : occupancy_g<T, G, false>(U, B);                     \
-  }                                                                                                     \
+template <typename T, bool SINK>
+static cudaError_t launch_step_t(const StepParams &p, int grid, cudaStream_t s) {
+  const bool paged = p.kv.paged != 0;
+  switch (p.G) {
+    case 1: return paged ? launch_step_g<T, 1, true, SINK>(p, grid, s) : launch_step_g<T, 1, false, SINK>(p, grid, s);
+    case 2: return paged ? launch_step_g<T, 2, true, SINK>(p, grid, s) : launch_step_g<T, 2, false, SINK>(p, grid, s);
+    case 4: return paged ? launch_step_g<T, 4, true, SINK>(p, grid, s) : launch_step_g<T, 4, false, SINK>(p, grid, s);
+    default: return cudaErrorInvalidValue;
   }
+}
+
+template <typename T, bool SINK>
+static int occupancy_t(int G, bool paged, int B, int Hq, int Hkv, int K) {
+  switch (G) {
+    case 1: return paged ? occupancy_g<T, 1, true, SINK>(B, Hq, Hkv, K) : occupancy_g<T, 1, false, SINK>(B, Hq, Hkv, K);
+    case 2: return paged ? occupancy_g<T, 2, true, SINK>(B, Hq, Hkv, K) : occupancy_g<T, 2, false, SINK>(B, Hq, Hkv, K);
+    case 4: return paged ? occupancy_g<T, 4, true, SINK>(B, Hq, Hkv, K) : occupancy_g<T, 4, false, SINK>(B, Hq, Hkv, K);
+    default: return 0;
+  }
+}
+
+}  // namespace mac

@@ -24,7 +24,7 @@ EXPORTS = ("mac_workspace_size", "mac_ring_layout_of", "mac_init_rings", "mac_de
            "mac_full_attention", "mac_full_attention_noalloc", "mac_join_aux", "mac_release_ring",
            "mac_last_status", "mac_set_phase_events", "mac_set_trace", "mac_status_string",
            "mac_threshold_sq")
-MAC_NOALLOC_SCRATCH_BYTES = 4 << 20
+MAC_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class mac_config(ctypes.Structure):

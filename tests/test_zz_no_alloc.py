@@ -75,7 +75,7 @@ def test_noalloc_matches_allocating_entry_point_on_consecutive_calls():
 
 
 def test_noalloc_rejects_configurations_beyond_the_static_array():
-    big = mac.config(256, 16, 4)  # 1024 (request, kv-head) units, GQA 4: over 4 MiB of partials
+    big = mac.config(128, 32, 4)  # 512 (request, kv-head) units at GQA 8: ~96 MiB of window-tile partials
     assert mac.mac_workspace_size(big)[1] > mac.MAC_NOALLOC_SCRATCH_BYTES
     kv = mac.mac_kv(256, 256, None, 1 << 20, 0, 0)
     rc = mac.load().mac_full_attention_noalloc(ctypes.byref(big), 256, 256, ctypes.byref(kv), 256,
