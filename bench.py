@@ -151,9 +151,11 @@ def measured_peaks():
         return {}
 
 
-def ncu_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's source changed since the counters were taken."""
+def ncu_traffic(kernel: str, bytes_per_launch: float):
+    """DRAM bytes per launch for this run's mix of launches: the committed
+    ncu capture's traffic over the algorithmic bytes of the same launches
+    (one layer state, same per-layer workload), times this run's algorithmic
+    bytes per launch; None when the kernel's source changed since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         rec = json.load(open(path))[kernel]
@@ -164,7 +166,9 @@ def ncu_traffic(kernel: str):
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     except OSError:
         return None
-    return rec["dram_bytes_per_launch"] if sha == rec.get("source_sha") else None
+    if sha != rec.get("source_sha") or "traffic_over_algorithmic" not in rec:
+        return None
+    return rec["traffic_over_algorithmic"] * bytes_per_launch
 
 
 def layer_step_bytes(w, m, mpos, ring_valid, front_sink=0):
@@ -192,19 +196,54 @@ def layer_step_bytes(w, m, mpos, ring_valid, front_sink=0):
 # the CUDA arm
 # ---------------------------------------------------------------------------
 
+# the other contexts the metric names, measured in the same default run
+EXTRA_CONTEXTS = ("llama8b-32k", "verylong-256k")
+
+
 def run_mac(args, rank, world, local):
     import torch
 
     from long_context_decode_gb300 import build as libbuild
     libbuild.build()
-    from long_context_decode_gb300 import mac
-    from long_context_decode_gb300.workloads import (WORKLOADS, device_kv, device_paged_kv,
-                                                     device_queries)
 
     dist = init_group(world, "nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w0 = select_workload(args)
+    out = measure(args, w0, dist, rank, world, dev)
+    # 32K and 256K beside the 128K line (one GPU: each is its own replica
+    # stack, measured after the main one has released its memory)
+    if (world == 1 and args.context_steps > 0 and args.workload == "long-128k" and not args.ring_k
+            and not args.front_sink):
+        from long_context_decode_gb300.workloads import WORKLOADS
+        ctx = {}
+        for name in EXTRA_CONTEXTS:
+            sub = argparse.Namespace(**vars(args))
+            sub.steps, sub.e2e_steps, sub.full_steps, sub.workload = args.context_steps, 0, 2, name
+            torch.cuda.empty_cache()
+            r = measure(sub, WORKLOADS[name], dist, rank, world, dev)
+            ctx[name] = {
+                "workload": r["config"]["workload"], "steps": sub.steps, "layers_per_step": sub.layers,
+                "us_per_layer_step": r["us_per_layer_step"], "value": r["value"], "unit": UNIT,
+                "bytes_per_launch": r["roofline"]["bytes_per_launch"], "launch_us": r["roofline"]["launch_us"],
+                "achieved_gbs": r["roofline"]["achieved"], "frac": r["roofline"]["frac"],
+                "hit_rate": r["step_roofline"]["hit_rate"], "clocks": r["clocks"],
+                "full_attention": r["full_attention"], "device_status": r["device_status"],
+            }
+        out["contexts"] = ctx
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w0, args, budget_s=args.cpu_budget)
+    return out, rank
+
+
+def measure(args, w0, dist, rank, world, dev):
+    """One workload: the timed decode steps of a stack of layer states, the
+    step kernel's roofline, the end-to-end leg and the full-attention leg."""
+    import torch
+
+    from long_context_decode_gb300 import mac
+    from long_context_decode_gb300.workloads import device_kv, device_paged_kv, device_queries
+
     Lc, K, Wm, P, E = args.layers, args.steps, args.warmup, args.profile_steps, args.e2e_steps
     fill, total, w = run_plan(w0, Wm, K, P, E)
     B, Hq, Hkv, d = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim
@@ -310,6 +349,33 @@ def run_mac(args, rank, world, local):
     t_max = max_over_ranks(dist, t_local, dev)
     status = mac.mac_last_status(cfg, scratch)
 
+    # ---- the step's own small kernels, timed alone -----------------------
+    # A timed step is the graph: the 4 PyTorch kernels of advance() (query
+    # gather, lengths, counter), then the Lc step kernels.  The same 4
+    # kernels on dummy outputs (the counter unchanged), replayed alone, give
+    # their share; the rest of the timed step, per layer, is the step
+    # kernel's time including its launch gap: a duration no longer than the
+    # timed layer step.
+    ctr_d = torch.zeros(1, dtype=torch.int64, device=dev)
+    q_d, seq_tmp_d, seq_d = torch.empty_like(q_cur), torch.empty_like(seq_tmp), torch.empty_like(seq_cur)
+    g_adv = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(main):
+        with torch.cuda.graph(g_adv, stream=main):
+            torch.index_select(q_all, 0, ctr_d, out=q_d)
+            torch.add(base, ctr_d, out=seq_tmp_d)
+            seq_d.copy_(seq_tmp_d)
+            ctr_d.add_(0)
+        g_adv.replay()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(main)
+        for _ in range(200):
+            g_adv.replay()
+        a1.record(main)
+    torch.cuda.synchronize(dev)
+    adv_s = a0.elapsed_time(a1) / 1e3 / 200
+    launch_s = max(1e-9, (t_max / K - adv_s) / Lc)
+
     # ---- profiled steps: per-kernel times and algorithmic bytes ----------
     kern_ms, append_ms, step_ms, mb, ab, wb, hits, heads = [], [], [], 0, 0, 0, 0, 0
     for _ in range(P):
@@ -373,7 +439,7 @@ def run_mac(args, rank, world, local):
     # the step kernel (match + band/tail attention + merge) is the dominant
     # kernel; the append copies ~1/1000 of its bytes on the aux stream
     dominant = "step_kernel"
-    dom_bytes, dom_s = match_bytes + attend_bytes, kern_s
+    dom_bytes, dom_s = match_bytes + attend_bytes, launch_s
     achieved = dom_bytes / dom_s / 1e9
     us_layer = t_max / (K * Lc) * 1e6
     value = whole_job_value(K * Lc, world, t_max)
@@ -400,14 +466,19 @@ def run_mac(args, rank, world, local):
         "gpu_launches": (2 if aux is not None else 1) * K * Lc,
         "roofline": {
             "bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-            "frac": achieved / hbm_peak, "traffic": ncu_traffic(dominant),
+            "frac": achieved / hbm_peak, "traffic": ncu_traffic(dominant, dom_bytes),
             "bytes_per_launch": dom_bytes, "launch_us": dom_s * 1e6,
+            "launch_us_source": "driver-timed step minus its 4 step-advance kernels (timed alone), per layer",
             "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)" if "hbm_gbs" in peaks
             else "of fallback 6.8 TB/s",
         },
         "kernels": {
-            "step_kernel": {"us": kern_s * 1e6, "bytes": dom_bytes, "match_bytes": match_bytes,
-                            "attend_bytes": attend_bytes, "gbs": dom_bytes / kern_s / 1e9},
+            "step_kernel": {"us": launch_s * 1e6, "bytes": dom_bytes, "match_bytes": match_bytes,
+                            "attend_bytes": attend_bytes, "gbs": dom_bytes / launch_s / 1e9,
+                            # the same kernel bracketed by event-record nodes in a second
+                            # graph (the nodes themselves add to it)
+                            "us_with_event_nodes": kern_s * 1e6},
+            "step_advance": {"kernels": 4, "us_per_step": adv_s * 1e6},
             # the ring append: its own kernel after the step on the auxiliary
             # stream, or written by the step kernel's final merges (fused)
             "append": ({"kernel": "append_kernel", "us_after_step": append_s * 1e6, "write_bytes": write_bytes}
@@ -416,9 +487,10 @@ def run_mac(args, rank, world, local):
         "full_attention": full,
         "step_roofline": {
             "algorithmic_read_bytes": match_bytes + attend_bytes, "write_bytes": write_bytes,
-            "us_per_layer_step": layer_step_s * 1e6,
-            "gbs": (match_bytes + attend_bytes) / layer_step_s / 1e9,
-            "frac": (match_bytes + attend_bytes) / layer_step_s / 1e9 / hbm_peak,
+            # the whole timed layer step (its share of the step-advance kernels included)
+            "us_per_layer_step": us_layer,
+            "gbs": (match_bytes + attend_bytes) / (us_layer * 1e-6) / 1e9,
+            "frac": (match_bytes + attend_bytes) / (us_layer * 1e-6) / 1e9 / hbm_peak,
             "hit_rate": hits / max(1, heads),
         },
         "clocks": clk,
@@ -426,11 +498,9 @@ def run_mac(args, rank, world, local):
         "device_status": status,
         "setup_s": setup_s,
     }
-    if world == 1 and rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w0, args, budget_s=args.cpu_budget)
     for L in layers:
         L.release()
-    return out, rank
+    return out
 
 
 def run_e2e(torch, mac, cfg, w, layers, scratch, kvs, kv_tensors, q_all, step_ctr, base, seq_cur,
@@ -503,10 +573,31 @@ def run_e2e(torch, mac, cfg, w, layers, scratch, kvs, kv_tensors, q_all, step_ct
 # the CPU oracle (baseline / reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w0, warmup, steps, budget_s=None):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the ISA)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_sample(w0, warmup, steps, budget_s=None, single_s=0.0):
     """Time the fp64 oracle on request 0 of the workload (all its heads),
     after filling its rings with ring_k untimed decode steps; returns
-    (seconds per request-step, steps timed, threads)."""
+    (seconds per request-step, steps timed, threads) and, with single_s > 0,
+    (seconds per request-step, steps timed) of further steps on one thread
+    for about single_s seconds."""
     from long_context_decode_gb300.workloads import F32, host_kv
     from oracle import mac_oracle as O
 
@@ -527,23 +618,40 @@ def oracle_sample(w0, warmup, steps, budget_s=None):
                       kv, n_threads=threads)
     times = []
     t_start = time.perf_counter()
-    for s in range(fill + warmup, fill + warmup + steps):
+    # with a one-thread leg, the threaded leg takes at most half the steps
+    n_multi = steps // 2 if single_s > 0 else steps
+    for s in range(fill + warmup, fill + warmup + n_multi):
         t0 = time.perf_counter()
         O.decode_step(cfg, ring, np.ascontiguousarray(q[:, :, s]), np.array([L + 1 + s], np.int32),
                       kv, n_threads=threads)
         times.append(time.perf_counter() - t0)
         if budget_s is not None and time.perf_counter() - t_start > budget_s:
             break
-    return float(np.mean(times)), len(times), threads
+    if single_s <= 0:
+        return float(np.mean(times)), len(times), threads
+    one = []
+    t_start = time.perf_counter()
+    for s in range(fill + warmup + len(times), fill + warmup + steps):
+        t0 = time.perf_counter()
+        O.decode_step(cfg, ring, np.ascontiguousarray(q[:, :, s]), np.array([L + 1 + s], np.int32),
+                      kv, n_threads=1)
+        one.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > single_s:
+            break
+    return float(np.mean(times)), len(times), threads, (float(np.mean(one)) if one else None), len(one)
 
 
 def cpu_baseline(w0, args, budget_s=20.0):
-    t, n, threads = oracle_sample(w0, 3, 256, budget_s=budget_s)
+    t, n, threads, t1, n1 = oracle_sample(w0, 3, 512, budget_s=budget_s, single_s=budget_s / 2)
     per_layer_step = t * w0.batch  # the oracle sample is one of the batch's requests
     return {"value": 1.0 / per_layer_step, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"fp64 C oracle, request 0 of {w0.batch} (all {w0.n_q_heads} heads), {n} decode "
-                      f"steps after {w0.ring_k}+3 untimed ring-filling steps at context "
-                      f"{w0.contexts[0]}; time per request-step x {w0.batch} requests = one layer step"}
+            "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
+            "single_thread": ({"value": 1.0 / (t1 * w0.batch), "unit": UNIT, "cores": 1, "steps": n1}
+                              if t1 else None),
+            "sample": f"fp64 C oracle, request 0 of {w0.batch} (all {w0.n_q_heads} heads, one thread per "
+                      f"head up to {threads} threads), {n} decode steps after {w0.ring_k}+3 untimed "
+                      f"ring-filling steps at context {w0.contexts[0]}, then {n1} more steps on one thread; "
+                      f"time per request-step x {w0.batch} requests = one layer step"}
 
 
 def select_workload(args):
@@ -592,6 +700,9 @@ def main():
     ap.add_argument("--profile-steps", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=64)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--context-steps", type=int, default=1000,
+                    help="timed steps of each of the 32K and 256K workloads reported beside the 128K line "
+                         "(0: skip them)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--append", choices=["fused", "aux"], default="fused",
                     help="rectify-append inside the step kernel, or as a kernel on an auxiliary stream")
