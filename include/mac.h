@@ -207,6 +207,31 @@ int mac_full_attention_noalloc(const mac_config *cfg, const void *q_pre, const i
  * separate aux stream. */
 int mac_join_aux(void *ring_ws, void *stream_main);
 
+/* Ready gate ([MAC] "Production version": request state gated so that a
+ * captured CUDA graph stays valid).  reset_flags: device int32 [B].  For
+ * every request b whose flag is non-zero, its rings start over empty: no
+ * slot holds a position any more, so its next decode step has no match
+ * candidate, misses on every head and attends [1, m] exactly, and the
+ * appends of its next steps refill the rings.  The flags are read and
+ * cleared on the device, on `stream`, after any append still pending on an
+ * auxiliary stream for ring_ws; the call can be captured into a graph and
+ * the caller sets flags between replays (a new request in a reused slot,
+ * a request whose cache was rewritten).  Returns MAC_ERR_INVALID_ARG for a
+ * null or misaligned pointer; the flags' values are not checked. */
+int mac_reset_requests(const mac_config *cfg, void *ring_ws, int32_t *reset_flags, void *stream);
+
+/* Test hook for the bounded waits (no counterpart on the pages): the next
+ * step kernel launched by the calling thread gives every wait (a stage's
+ * copy, a flag, the grid barrier, a piece count) `cycles` SM cycles instead
+ * of about a second, and, if withhold_use >= 0, never issues the copy of
+ * that stage use (per CTA in the span kernel, per warp in the ring kernel),
+ * so the wait for it runs out: the kernel sets MAC_DEV_WAIT_TIMEOUT, stops
+ * its work, lets its other copies land and returns.  The launch's outputs
+ * are then undefined; its scratch workspace must be cleared (or replaced)
+ * before the next launch.  1 <= cycles <= 2^31, withhold_use >= -1; the
+ * hook clears itself. */
+int mac_test_wait_budget(int64_t cycles, int32_t withhold_use);
+
 /* Destroy the events the library keeps for ring_ws (call before freeing it). */
 int mac_release_ring(void *ring_ws);
 

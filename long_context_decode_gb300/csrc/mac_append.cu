@@ -27,6 +27,23 @@ __global__ void __launch_bounds__(64) append_kernel(const __grid_constant__ Appe
   }
 }
 
+// The ready gate: a request whose flag is set starts over with an empty
+// ring (no slot holds a position, so its next step has no candidate, misses
+// on every head and attends [1, m] exactly; the appends then refill the
+// ring).  The flag is consumed.  One CTA per request.
+__global__ void __launch_bounds__(256) reset_kernel(int32_t *ring_pos, int32_t *flags, int K) {
+  const int b = blockIdx.x;
+  if (flags[b] == 0) return;  // the same value in every thread of the CTA
+  for (int s = threadIdx.x; s < K; s += blockDim.x) ring_pos[(int64_t)b * K + s] = 0;
+  __syncthreads();  // every thread has read the flag
+  if (threadIdx.x == 0) flags[b] = 0;
+}
+
+cudaError_t launch_reset(int32_t *ring_pos, int32_t *flags, int B, int K, cudaStream_t s) {
+  reset_kernel<<<B, 256, 0, s>>>(ring_pos, flags, K);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(const AppendParams &p, int dtype, cudaStream_t s) {
   if (dtype == MAC_BF16)
     append_kernel<uint16_t><<<p.B * p.Hq, 64, 0, s>>>(p);

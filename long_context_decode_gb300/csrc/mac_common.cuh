@@ -185,6 +185,11 @@ struct StepParams {
   // attended as output only
   int sink_f, sink_piece;
   unsigned long long *trace;  // optional: [grid][kTracePoints] %globaltimer stamps
+  // bounded waits: the budget of every wait on a copy, a flag or another CTA
+  // (cycles), and, for the run-out test only, one stage use (>= 0) whose
+  // copy is never issued
+  long long wait_limit;
+  int withhold;
   // RoPE frequency j as a 64-bit fixed-point fraction of a turn per
   // position: round(w_j / (2 pi) * 2^64), w_j = base^(-2j/d)
   unsigned long long rope_f[kHeadDim / 2];
@@ -225,6 +230,7 @@ int occupancy_bf16_g8(bool paged, int U, int B);
 int occupancy_f32_g8(bool paged, int U, int B);
 }  // namespace ring
 cudaError_t launch_append(const AppendParams &p, int dtype, cudaStream_t s);
+cudaError_t launch_reset(int32_t *ring_pos, int32_t *flags, int B, int K, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // device helpers
@@ -270,11 +276,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // ~2^31 clock cycles (about a second) or as soon as *abort is set; returns
 // false when it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  volatile int *abort) {
+                                                  volatile int *abort, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (*abort || clock64() - t0 > (1LL << 31)) return false;
+    if (*abort || clock64() - t0 > limit) return false;
   }
   return true;
 }

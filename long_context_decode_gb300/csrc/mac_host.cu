@@ -270,12 +270,21 @@ void *noalloc_scratch() {
 thread_local cudaEvent_t t_phase[3] = {nullptr, nullptr, nullptr};
 // trace buffer armed by mac_set_trace for this thread's next step kernel
 thread_local unsigned long long *t_trace = nullptr;
+// run-out test knob armed by mac_test_wait_budget for this thread's next
+// step kernel (0: the default budget)
+thread_local long long t_wait_limit = 0;
+thread_local int t_withhold = -1;
+constexpr long long kWaitLimit = 1LL << 31;  // about a second of SM cycles
 
 cudaError_t launch_step(StepParams p, const mac_config *c, cudaStream_t s) {
   const int grid = step_grid(c);
   if (grid < 1) return cudaErrorInvalidValue;
   p.trace = t_trace;
   t_trace = nullptr;
+  p.wait_limit = t_wait_limit > 0 ? t_wait_limit : kWaitLimit;
+  p.withhold = t_withhold;
+  t_wait_limit = 0;
+  t_withhold = -1;
   const bool f32 = c->dtype == MAC_F32;
   if (ring_kernel(c)) {
     p.tc = launch_tiles(c, p.sink_piece != 0);
@@ -521,6 +530,31 @@ int mac_set_phase_events(void *before_step, void *after_step, void *after_append
 int mac_set_trace(void *device_buffer) {
   t_trace = (unsigned long long *)device_buffer;
   return MAC_OK;
+}
+
+int mac_test_wait_budget(int64_t cycles, int32_t withhold_use) {
+  if (cycles < 1 || cycles > kWaitLimit || withhold_use < -1) return MAC_ERR_INVALID_ARG;
+  t_wait_limit = cycles;
+  t_withhold = withhold_use;
+  return MAC_OK;
+}
+
+int mac_reset_requests(const mac_config *cfg, void *ring_ws, int32_t *reset_flags, void *stream) {
+  int v = validate(cfg);
+  if (v != MAC_OK) return v;
+  if (!ring_ws || !reset_flags || ((uintptr_t)reset_flags & 3u) != 0) return MAC_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  {
+    // after an append still pending on an auxiliary stream for these rings
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_rings.find(ring_ws);
+    if (it != g_rings.end() && it->second.pending && it->second.capture_id == capture_id_of(s)) {
+      if (cudaStreamWaitEvent(s, it->second.aux_done, 0) != cudaSuccess) return MAC_ERR_CUDA;
+    }
+  }
+  const mac_ring_layout R = ring_layout(cfg);
+  int32_t *pos = (int32_t *)((uint8_t *)ring_ws + R.pos);
+  return launch_reset(pos, reset_flags, cfg->batch, cfg->ring_k, s) == cudaSuccess ? MAC_OK : MAC_ERR_CUDA;
 }
 
 int mac_release_ring(void *ring_ws) {

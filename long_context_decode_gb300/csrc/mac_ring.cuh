@@ -303,7 +303,7 @@ struct Step {
   // Lane 0: the copies of the next stage use (every lane calls it).
   __device__ static void issue(const StepParams &p, Ring &R, const Desc &d, const int32_t (&id)[2]) {
     const uint32_t n = R.issued++;
-    if (lane_id() != 0) return;
+    if (lane_id() != 0 || (int)n == p.withhold) return;  // the run-out test's use is never copied
     uint8_t *buf = stage_buf(R, n);
     const uint32_t bar = stage_bar(R, n);
     int *rows = R.rows + n % kStages;
@@ -382,7 +382,7 @@ struct Step {
 
   // Wait for stage use n to land (bounded).
   __device__ static bool wait_stage(const StepParams &p, const Smem &S, const Ring &R, uint32_t n) {
-    const bool ok = mbar_wait_bounded(stage_bar(R, n), (n / kStages) & 1u, S.abort);
+    const bool ok = mbar_wait_bounded(stage_bar(R, n), (n / kStages) & 1u, S.abort, p.wait_limit);
     if (!ok && !*S.abort) {
       set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
       *S.abort = 1;
@@ -395,10 +395,15 @@ struct Step {
     fence_proxy_async();
   }
   // Before the CTA exits: the copies this warp issued have landed (bounded).
-  __device__ static void drain(const Ring &R) {
+  __device__ static void drain(const StepParams &p, const Ring &R) {
+    // a copy lands within microseconds; the bound only guards a stage whose
+    // phase a withheld use shifted (the run-out test)
+    const long long lim = p.wait_limit < (1LL << 30) ? (p.wait_limit > (1LL << 20) ? p.wait_limit : (1LL << 20))
+                                                     : (1LL << 30);
     for (uint32_t n = R.used; n < R.issued; ++n) {
+      if ((int)n == p.withhold) continue;
       const long long t0 = clock64();
-      while (!mbar_try_wait(stage_bar(R, n), (n / kStages) & 1u) && clock64() - t0 < (1LL << 30)) {
+      while (!mbar_try_wait(stage_bar(R, n), (n / kStages) & 1u) && clock64() - t0 < lim) {
       }
     }
   }
@@ -1544,7 +1549,7 @@ struct Step {
       const long long t0 = clock64();
       while (ld_acquire_u32(ctr) < target) {
         if (*S.abort) break;
-        if (clock64() - t0 > (1LL << 31)) {
+        if (clock64() - t0 > p.wait_limit) {
           set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
           *S.abort = 1;
           break;
@@ -1569,7 +1574,7 @@ struct Step {
       const unsigned long long target = old - old % gridDim.x + gridDim.x;
       const long long t0 = clock64();
       while (ld_acquire_u64(ctr) < target) {
-        if (clock64() - t0 > (1LL << 31)) {
+        if (clock64() - t0 > p.wait_limit) {
           set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
           *S.abort = 1;
           break;
@@ -1703,7 +1708,7 @@ struct Step {
       merge_one(p, S, bh, true, pos, 0);
     }
     stamp(p, 6);
-    drain(R);
+    drain(p, R);
     block_sync();
     if (tid == 0) {
       // the last CTA to finish advances the launch count (which selects the

@@ -775,7 +775,7 @@ struct Step {
     const long long t0 = clock64();
     while (*S.ready < level) {
       if (*S.abort) return false;
-      if (clock64() - t0 > (1LL << 31)) {
+      if (clock64() - t0 > p.wait_limit) {
         set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
         *S.abort = 1;
         return false;
@@ -787,8 +787,18 @@ struct Step {
   }
 
   // Producer lane: wait for stage use n to be free, then arm its full barrier.
+  // The run-out test's withheld use is never copied: the producer stalls
+  // there (bounded) until the consumers' wait for it has run out.
   __device__ static bool acquire_stage(const StepParams &p, const Smem &S, uint32_t n) {
-    if (!mbar_wait_bounded(smem_addr(&S.empty[n % kStages]), ((n / kStages) & 1u) ^ 1u, S.abort)) {
+    if ((int)n == p.withhold) {
+      const long long t0 = clock64();
+      while (!*S.abort && clock64() - t0 <= 2 * p.wait_limit) {
+      }
+      if (!*S.abort) set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
+      *S.abort = 1;
+      return false;
+    }
+    if (!mbar_wait_bounded(smem_addr(&S.empty[n % kStages]), ((n / kStages) & 1u) ^ 1u, S.abort, p.wait_limit)) {
       if (!*S.abort) set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
       *S.abort = 1;
       return false;
@@ -977,7 +987,7 @@ struct Step {
 
   // Consumer side of stage use n.
   __device__ static bool wait_use(const StepParams &p, const Smem &S, uint32_t n) {
-    const bool ok = mbar_wait_bounded(smem_addr(&S.full[n % kStages]), (n / kStages) & 1u, S.abort);
+    const bool ok = mbar_wait_bounded(smem_addr(&S.full[n % kStages]), (n / kStages) & 1u, S.abort, p.wait_limit);
     if (!ok && !*S.abort) {
       set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
       *S.abort = 1;
@@ -1134,7 +1144,7 @@ struct Step {
       const unsigned long long target = old - old % gridDim.x + gridDim.x;
       const long long t0 = clock64();
       while (ld_acquire_u64(ctr) < target) {
-        if (clock64() - t0 > (1LL << 31)) {
+        if (clock64() - t0 > p.wait_limit) {
           set_status(p.ctl, MAC_DEV_WAIT_TIMEOUT);
           *S.abort = 1;
           break;

@@ -23,7 +23,7 @@ MAC_ROPE_HALF, MAC_ROPE_INTERLEAVED, MAC_ROPE_NONE = 0, 1, 2
 EXPORTS = ("mac_workspace_size", "mac_ring_layout_of", "mac_init_rings", "mac_decode_step",
            "mac_full_attention", "mac_full_attention_noalloc", "mac_join_aux", "mac_release_ring",
            "mac_last_status", "mac_set_phase_events", "mac_set_trace", "mac_status_string",
-           "mac_threshold_sq")
+           "mac_threshold_sq", "mac_reset_requests", "mac_test_wait_budget")
 MAC_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -83,6 +83,8 @@ def load() -> ctypes.CDLL:
     L.mac_last_status.argtypes = [P(mac_config), vp, P(i32), vp]
     L.mac_set_phase_events.argtypes = [vp, vp, vp]
     L.mac_set_trace.argtypes = [vp]
+    L.mac_reset_requests.argtypes = [P(mac_config), vp, vp, vp]
+    L.mac_test_wait_budget.argtypes = [i64, i32]
     L.mac_status_string.argtypes = [ctypes.c_int]
     L.mac_status_string.restype = ctypes.c_char_p
     L.mac_threshold_sq.argtypes = [P(mac_config)]
@@ -190,6 +192,20 @@ def mac_set_trace(buffer):
     """Arm the next step kernel on this thread to write per-CTA phase
     timestamps into ``buffer`` (a torch uint64/int64 tensor of >= 8 * SMs)."""
     _check(load().mac_set_trace(_ptr(buffer)), "mac_set_trace")
+
+
+def mac_reset_requests(cfg: mac_config, ring, reset_flags, stream=None):
+    """Requests whose flag (device int32 tensor [B]) is set start over with
+    empty rings: their next step misses on every head; the flags are
+    cleared on the device."""
+    _check(load().mac_reset_requests(ctypes.byref(cfg), _ptr(ring), _ptr(reset_flags), _stream(stream)),
+           "mac_reset_requests")
+
+
+def mac_test_wait_budget(cycles: int, withhold_use: int = -1):
+    """Test hook: the next step kernel on this thread gives every bounded
+    wait ``cycles`` SM cycles and never copies stage use ``withhold_use``."""
+    _check(load().mac_test_wait_budget(int(cycles), int(withhold_use)), "mac_test_wait_budget")
 
 
 def mac_status_string(code: int) -> str:

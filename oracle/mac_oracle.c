@@ -555,3 +555,16 @@ int oc_seed_rings(const oc_config *c, oc_ring *ring, const void *q_seed,
     }
   return 0;
 }
+
+/* The ready gate ([MAC] "Production version": request state that a captured
+ * graph can gate).  A request whose flag is set starts over with an empty
+ * ring: no slot holds a position, so its next decode step has no candidate,
+ * misses on every head and is exact attention, and its appends refill the
+ * ring from there.  Other requests are untouched. */
+int oc_reset_requests(const oc_config *c, oc_ring *ring, const int32_t *flags) {
+  int B = c->batch, K = c->ring_k;
+  for (int b = 0; b < B; ++b)
+    if (flags[b] != 0)
+      for (int s = 0; s < K; ++s) ring->pos[(int64_t)b * K + s] = 0;
+  return 0;
+}

@@ -88,6 +88,7 @@ def lib() -> ctypes.CDLL:
         L.oc_full_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32]
         L.oc_full_attention.restype = i32
         L.oc_seed_rings.argtypes = [vp, vp, vp, vp, i32, vp, vp, i32]
+        L.oc_reset_requests.argtypes = [vp, vp, vp]
         L.oc_seed_rings.restype = i32
         _LIB = L
     return _LIB
@@ -255,6 +256,16 @@ def seed_rings(cfg: Config, ring: Ring, q_seed: np.ndarray, prompt_len: np.ndarr
                                 ctypes.byref(k), _ptr(hm), _threads(n_threads))
     if rcode != 0:
         raise ValueError(f"oc_seed_rings returned {rcode}")
+
+
+def reset_requests(cfg: Config, ring: Ring, flags_b: np.ndarray) -> None:
+    """Requests whose flag is non-zero start over with an empty ring."""
+    f = np.ascontiguousarray(flags_b, np.int32)
+    assert f.shape == (cfg.batch,)
+    c, rc = cfg.c(), ring.c()
+    rcode = lib().oc_reset_requests(ctypes.byref(c), ctypes.byref(rc), _ptr(f))
+    if rcode != 0:
+        raise ValueError(f"oc_reset_requests returned {rcode}")
 
 
 def flags(res: dict, thr2: float, rel: float = 1e-6) -> np.ndarray:

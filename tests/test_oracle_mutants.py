@@ -60,6 +60,7 @@ MUTANTS = [
     ("hit reuses the wrong slot", [("int64_t slot = (((int64_t)b * Hq + h) * K + p % K);",
                                     "int64_t slot = (((int64_t)b * Hq + h) * K + (p + 1) % K);")]),
     ("distance drops the square", [("D += diff * diff;", "D += fabs(diff);")]),
+    ("reset leaves the ring as it was", [("for (int s = 0; s < K; ++s) ring->pos[(int64_t)b * K + s] = 0;", ";")]),
 ]
 
 

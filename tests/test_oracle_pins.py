@@ -475,6 +475,32 @@ def test_front_sink_covering_the_reused_prefix_gives_exact_attention(rope):
     assert band_tokens > 0  # the band [F+1, m-r] is attended at least once
 
 
+def test_a_reset_request_misses_at_its_next_step():
+    # Ready gate ([MAC] "Production version"): a reset request has no
+    # candidate at its next step, so every head misses and the step is exact
+    # attention; the other request is untouched, and at the step after, the
+    # reset step's own append is the request's only candidate.
+    rng, cfg, kv = _rand_problem(14, ring_k=4, band_r=3, tau=-10.0)
+    B, Hq, d = cfg.batch, cfg.n_q_heads, cfg.head_dim
+    L = np.array([30, 34], np.int32)
+    ring = O.Ring(cfg)
+    O.seed_rings(cfg, ring, rng.standard_normal((B, Hq, 4, d)).astype(np.float32), L, kv)
+    q0, q1 = (rng.standard_normal((B, Hq, d)).astype(np.float32) for _ in range(2))
+    m = (L + 1).astype(np.int32)
+    kept = ring.copy()
+    r_kept = O.decode_step(cfg, kept, q0, m, kv)
+    assert (r_kept["match_pos"] >= 1).all()  # every head would hit
+    O.reset_requests(cfg, ring, np.array([1, 0], np.int32))
+    res = O.decode_step(cfg, ring, q0, m, kv)
+    assert (res["match_pos"][0] == -1).all()
+    full, _ = O.full_attention(cfg, q0, m, kv)
+    np.testing.assert_allclose(res["out"][0], full[0], rtol=1e-11, atol=1e-14)
+    np.testing.assert_array_equal(res["match_pos"][1], r_kept["match_pos"][1])
+    np.testing.assert_array_equal(res["out"][1], r_kept["out"][1])
+    nxt = O.decode_step(cfg, ring, q1, m + 1, kv)
+    assert (nxt["match_pos"][0] == m[0]).all()
+
+
 def test_seed_positions_and_slots():
     rng, cfg, kv = _rand_problem(12, ring_k=8, band_r=3)
     L = np.array([5, 40], np.int32)
