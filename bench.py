@@ -177,7 +177,8 @@ def layer_step_bytes(w, m, mpos, ring_valid, front_sink=0):
     With a front sink F the span starts at F+1 at the earliest and the sink
     [1, min(F, m)] is read besides."""
     B, Hq, Hkv, d, G, r, F = w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.group, w.band_r, front_sink
-    es = 2
+    from long_context_decode_gb300.workloads import F32
+    es = 4 if w.dtype == F32 else 2
     match = sum(Hq * ring_valid[b] * d * es for b in range(B)) + B * Hq * d * es + B * w.ring_k * 4
     attend = 0
     for b in range(B):
@@ -242,7 +243,7 @@ def measure(args, w0, dist, rank, world, dev):
     import torch
 
     from long_context_decode_gb300 import mac
-    from long_context_decode_gb300.workloads import device_kv, device_paged_kv, device_queries
+    from long_context_decode_gb300.workloads import F32, device_kv, device_paged_kv, device_queries
 
     Lc, K, Wm, P, E = args.layers, args.steps, args.warmup, args.profile_steps, args.e2e_steps
     fill, total, w = run_plan(w0, Wm, K, P, E)
@@ -264,7 +265,8 @@ def measure(args, w0, dist, rank, world, dev):
     cap = w.capacity() if not w.page_size else kv_tensors[0][2].shape[1] * 16
     q_all = torch.stack([device_queries(w, total, dev, stream_seed=layer).permute(2, 0, 1, 3)
                          for layer in range(Lc)], dim=1).contiguous()  # [total, Lc, B, Hq, d]
-    cfg = mac.config(B, Hq, Hkv, d, w.ring_k, w.band_r, w.tau, dtype=mac.MAC_BF16,
+    es = 4 if w.dtype == F32 else 2
+    cfg = mac.config(B, Hq, Hkv, d, w.ring_k, w.band_r, w.tau, dtype=mac.MAC_F32 if w.dtype == F32 else mac.MAC_BF16,
                      page_size=w.page_size, max_context=cap, front_sink=args.front_sink)
     ring_bytes, scratch_bytes = mac.mac_workspace_size(cfg)
     scratch = torch.zeros(scratch_bytes, dtype=torch.uint8, device=dev)
@@ -432,7 +434,7 @@ def measure(args, w0, dist, rank, world, dev):
         torch.cuda.synchronize(dev)
         full_s = f0.elapsed_time(f1) / 1e3 / (args.full_steps * Lc)
         m_now = seq_cur.cpu().numpy().astype(np.int64)
-        full_bytes = float(sum(Hkv * int(m) * 2 * d * 2 for m in m_now) + B * Hq * d * 2)
+        full_bytes = float(sum(Hkv * int(m) * 2 * d * es for m in m_now) + B * Hq * d * es)
         full = {"us_per_layer_step": full_s * 1e6, "gbs": full_bytes / full_s / 1e9,
                 "frac": full_bytes / full_s / 1e9 / hbm_peak, "bytes_per_layer_step": full_bytes,
                 "step_speedup": full_s / (t_max / (K * Lc)), "steps": args.full_steps}
@@ -446,7 +448,7 @@ def measure(args, w0, dist, rank, world, dev):
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": t_max / K * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f32" if w.dtype == F32 else "bf16", "data": "synthetic",
         "impl": "mac",
         "config": {
             "workload": f"{w0.name}: {w0.description}",

@@ -115,9 +115,9 @@ def main(argv=None):
             graphs[True].replay()
         torch.cuda.synchronize()
         t = trace.view(nsm, TP).cpu().numpy().astype(np.int64)
-        misses = int((mps[NL - 1].cpu().numpy() < 0).sum())
+        miss = mps[NL - 1].cpu().numpy().reshape(B, Hkv, Hq // Hkv) < 0
         t0 = t[:, 0][t[:, 0] != 0].min()
-        row = {"missing_heads": misses}
+        row = {"missing_heads": int(miss.sum()), "missing_units": int(miss.any(-1).sum())}
         for k, name in PHASES:
             col = t[:, k]
             col = col[col != 0]
@@ -126,6 +126,19 @@ def main(argv=None):
                 row[name] = (float(np.median(c)), float(c.max()))
         clk = (t[:, 17] - t[:, 16]) / np.maximum(1, t[:, 6] - t[:, 0])
         row["sm_ghz"] = float(np.median(clk[clk > 0])) if (clk > 0).any() else None
+        # per-CTA band work: the last band piece's tiles done (stamp 24, us),
+        # time waiting for band tiles (25, ns), band tokens (22) and pieces
+        # (23), time merging (18, ns) and units merged (19)
+        has = t[:, 24] != 0
+        if has.any():
+            row["band_tiles_done_us"] = [float(np.percentile((t[has, 24] - t0) / 1e3, q)) for q in (10, 50, 90, 100)]
+        row["band_wait_us"] = [float(np.percentile(t[:, 25] / 1e3, q)) for q in (50, 90, 100)]
+        row["band_tokens"] = [float(np.percentile(t[:, 22], q)) for q in (10, 50, 90, 100)]
+        row["band_pieces"] = [float(np.percentile(t[:, 23], q)) for q in (50, 100)]
+        row["merge_us"] = [float(np.percentile(t[:, 18] / 1e3, q)) for q in (50, 90, 100)]
+        row["units_merged"] = [float(np.percentile(t[:, 19], q)) for q in (50, 100)]
+        row["longest_merge_us"] = float(t[:, 20].max() / 1e3)
+        row["longest_merge_entries"] = int(t[np.argmax(t[:, 20]), 21])
         rows.append(row)
     status = mac.mac_last_status(cfg, scratch)
 
@@ -136,8 +149,8 @@ def main(argv=None):
                        float(np.median([r[name][1] for r in sel if name in r])))
                 for _, name in PHASES if any(name in r for r in sel)}
 
-    hit = [r for r in rows if r["missing_heads"] == 0]
-    miss1 = [r for r in rows if 1 <= r["missing_heads"] <= G_of(w)]
+    hit = [r for r in rows if r["missing_units"] == 0]
+    miss1 = [r for r in rows if r["missing_units"] == 1]
     t_hit, t_miss = table(hit), table(miss1)
     print(f"# step kernel phases: {w0.name}, last of {NL} layer states, {R} traced steps "
           f"({len(hit)} all-hit, {len(miss1)} with one missing unit); device status {status}")
@@ -151,6 +164,17 @@ def main(argv=None):
         fa = (f"{a[0]:.2f}", f"{a[1]:.2f}") if a else ("-", "-")
         fb = (f"{b[0]:.2f}", f"{b[1]:.2f}") if b else ("-", "-")
         print(f"| {name} ({k}) | {fa[0]} | {fa[1]} | {fb[0]} | {fb[1]} |")
+    for label, sel in (("all hit", hit), ("one missing unit", miss1)):
+        if not sel:
+            continue
+        print()
+        print(f"{label}, per-CTA band work (medians over the steps of percentiles over the CTAs):")
+        for key in ("band_tiles_done_us", "band_wait_us", "band_tokens", "band_pieces", "merge_us", "units_merged"):
+            vals = [r[key] for r in sel if key in r]
+            if vals:
+                print(f"  {key}: " + " / ".join(f"{v:.2f}" for v in np.median(np.array(vals), 0)))
+        print(f"  longest merge: {np.median([r['longest_merge_us'] for r in sel]):.2f} us, "
+              f"{int(np.median([r['longest_merge_entries'] for r in sel]))} entries")
     ghz = [r["sm_ghz"] for r in rows if r["sm_ghz"]]
     print()
     print(f"µs since the first CTA started; medians over the steps of each class. SM clock during the "
@@ -159,11 +183,6 @@ def main(argv=None):
         json.dump(rows, open(args.json, "w"))
     for L in layers:
         L.release()
-
-
-def G_of(w):
-    """Heads of one unit: a step with one missing unit has 1..G missing heads."""
-    return w.n_q_heads // w.n_kv_heads
 
 
 if __name__ == "__main__":
