@@ -190,6 +190,9 @@ struct StepParams {
   // copy is never issued
   long long wait_limit;
   int withhold;
+  // host only: launch with programmatic stream serialization (the kernel
+  // may start before the previous one on the stream has finished)
+  int early_start;
   // RoPE frequency j as a 64-bit fixed-point fraction of a turn per
   // position: round(w_j / (2 pi) * 2^64), w_j = base^(-2j/d)
   unsigned long long rope_f[kHeadDim / 2];
@@ -340,6 +343,15 @@ __device__ __forceinline__ void block_sync() {
   __syncwarp();
   __syncthreads();
 }
+
+// Programmatic dependent launch: let the next kernel on the stream start
+// (its CTAs take SMs as this grid frees them), and wait until the previous
+// kernel on the stream has finished with its writes visible (returns at
+// once when the launch has no such dependency).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Orders this thread's earlier shared-memory accesses (generic proxy)
 // before its later bulk copies into shared memory (async proxy).

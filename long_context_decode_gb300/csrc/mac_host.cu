@@ -237,6 +237,28 @@ struct RingEvents {
 std::mutex g_mu;
 std::unordered_map<void *, RingEvents> g_rings;
 
+// The last library launch on each stream, as far as an early start of the
+// next step kernel goes: the ring a fused decode step wrote, or kNoRing
+// after full attention (which writes no ring); absent or null after
+// anything else (an append kernel, a reset, ring seeding, a step with
+// timing events), after which the next step kernel waits as usual.  A step
+// kernel's early part reads its queries, its lengths and its own layer's
+// rings, so it may start early after a step that wrote another ring.
+std::unordered_map<cudaStream_t, const void *> g_last_launch;
+const char kNoRingTag = 0;
+const void *const kNoRing = &kNoRingTag;
+
+// Records `writes` as the stream's last launch; returns whether a step
+// kernel whose early part reads ring `reads` (null: none) may start early.
+bool note_launch(cudaStream_t s, const void *reads, const void *writes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  const void *prev = nullptr;
+  auto it = g_last_launch.find(s);
+  if (it != g_last_launch.end()) prev = it->second;
+  g_last_launch[s] = writes;
+  return prev != nullptr && (reads == nullptr || prev != reads);
+}
+
 unsigned long long capture_id_of(cudaStream_t s) {
   cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
   unsigned long long id = 0;
@@ -353,6 +375,7 @@ int mac_init_rings(const mac_config *cfg, void *ring_ws, void *scratch_ws, const
     return MAC_ERR_INVALID_ARG;
   if (q_seed && (v = check_kv(cfg, kv)) != MAC_OK) return v;
   cudaStream_t s = (cudaStream_t)stream;
+  note_launch(s, nullptr, nullptr);  // seeding writes the ring: the next step waits
   const mac_ring_layout R = ring_layout(cfg);
   const ScratchLayout S = scratch_layout(cfg);
   uint8_t *ring = (uint8_t *)ring_ws, *scr = (uint8_t *)scratch_ws;
@@ -448,6 +471,10 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
     sp.as_o = nullptr;
     sp.as_lse = nullptr;
   }
+  {
+    const bool plain = fused && !t_phase[0] && !t_phase[1] && !t_phase[2];
+    sp.early_start = note_launch(sm, ring_ws, plain ? ring_ws : nullptr) && plain ? 1 : 0;
+  }
   if (record_phase(0, sm) != cudaSuccess || launch_step(sp, cfg, sm) != cudaSuccess ||
       record_phase(1, sm) != cudaSuccess)
     return MAC_ERR_CUDA;
@@ -487,6 +514,7 @@ int mac_full_attention(const mac_config *cfg, void *scratch_ws, const void *q_pr
   sp.q = q_pre;
   sp.out = out;
   sp.out_lse = lse;
+  sp.early_start = note_launch((cudaStream_t)stream, nullptr, kNoRing) ? 1 : 0;
   if (launch_step(sp, cfg, (cudaStream_t)stream) != cudaSuccess) return MAC_ERR_CUDA;
   return MAC_OK;
 }
@@ -502,6 +530,7 @@ int mac_full_attention_noalloc(const mac_config *cfg, const void *q_pre, const i
   if (!scratch) return MAC_ERR_CUDA;
   // the previous call left its counters and status in the array: clear the
   // control part (everything before the partials) on this call's stream
+  note_launch((cudaStream_t)stream, nullptr, nullptr);  // a memset comes between
   if (cudaMemsetAsync(scratch, 0, scratch_layout(cfg).parts, (cudaStream_t)stream) != cudaSuccess)
     return MAC_ERR_CUDA;
   return mac_full_attention(cfg, scratch, q_pre, seq_len, kv, out, lse, stream);
@@ -554,6 +583,7 @@ int mac_reset_requests(const mac_config *cfg, void *ring_ws, int32_t *reset_flag
   }
   const mac_ring_layout R = ring_layout(cfg);
   int32_t *pos = (int32_t *)((uint8_t *)ring_ws + R.pos);
+  note_launch(s, nullptr, nullptr);
   return launch_reset(pos, reset_flags, cfg->batch, cfg->ring_k, s) == cudaSuccess ? MAC_OK : MAC_ERR_CUDA;
 }
 

@@ -2022,7 +2022,7 @@ struct Step {
   __device__ static void run(const StepParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_mask[kStages];
-    __shared__ int s_abort, s_ready, s_last, s_par, s_nshort;
+    __shared__ int s_abort, s_ready, s_last, s_par, s_nshort, s_badlen;
     __shared__ uint32_t s_issued;
     __shared__ int64_t s_span[2][kMaxGrid + 1];
     __shared__ int s_ne[2][kMaxGrid + 1];
@@ -2076,16 +2076,17 @@ struct Step {
       s_abort = 0;
       s_ready = 0;
       s_issued = 0;
-      // decode launches alternate between the two buffers of minima; every
-      // CTA reads the count before the first grid barrier, and it only
-      // changes after every CTA has finished
-      s_par = decode ? (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u) : 0;
+      s_badlen = 0;
       mbar_fence_init();
     }
     __syncthreads();  // the last barrier of all kThreads threads
+    // The next step kernel on the stream may start its CTAs on the SMs this
+    // grid frees.  Until their dependency wait they read only inputs (this
+    // launch's queries and lengths, their own layer's rings) and write only
+    // shared memory; the host launches them early only when this launch
+    // writes none of those (a step on another ring, or full attention).
+    griddep_launch_dependents();
     const int n_bh = n_heads;
-    S.best = p.best + (size_t)s_par * n_bh;
-    S.best_next = p.best + (size_t)(s_par ^ 1) * n_bh;
 
     if (tid >= kConsumers) {
       producer_warp(p, S);
@@ -2096,8 +2097,7 @@ struct Step {
     for (int u = tid; u < n_units; u += kConsumers) {
       S.u_pos[u] = (int32_t)((int64_t)p.pos_base[u / p.Hkv] + p.pos_add);
       S.u_s[u] = p.sink_f + 1;
-      if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub))
-        set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
+      if (p.check_len && blockIdx.x == 0 && !len_ok(p, (int64_t)S.u_pos[u] - p.len_sub)) s_badlen = 1;
     }
     if (decode) {
       // every request's length, for the match (X holds the decisions only
@@ -2125,6 +2125,18 @@ struct Step {
       *S.ready = 1;  // the producer may copy tail tiles
     }
     stamp(trace, 7);
+    // From here on the scratch workspace is used: the previous kernel on the
+    // stream has finished and its writes are visible.  Decode launches
+    // alternate between the two buffers of minima; the count changes only
+    // after every CTA of a launch has finished.
+    griddep_wait();
+    if (tid == 0) {
+      s_par = decode ? (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u) : 0;
+      if (s_badlen) set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
+    }
+    consumer_sync();
+    S.best = p.best + (size_t)s_par * n_bh;
+    S.best_next = p.best + (size_t)(s_par ^ 1) * n_bh;
 
     uint32_t n = 0;  // stage uses consumed so far (every consumer counts the same sequence)
     const int nchunks = decode ? match_chunks(p) : 0;

@@ -45,8 +45,19 @@ static cudaError_t launch_step_g(const StepParams &p, int grid, cudaStream_t s) 
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (p.early_start) {
+    // An early start: the CTAs may begin on the SMs the previous step kernel
+    // frees (griddep_wait in the kernel orders everything that depends on
+    // it).  A cooperative launch would place no CTA before the whole grid
+    // fits, so this one is plain: the grid (one CTA per SM, which its shared
+    // memory enforces) is resident once the previous kernel has finished,
+    // and the grid barrier's wait is bounded should another stream hold SMs.
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, step_kernel<T, G, PAGED, SINK>, p);
