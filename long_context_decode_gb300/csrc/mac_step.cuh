@@ -207,6 +207,8 @@ struct Step {
     volatile int *ready;  // layouts known to the producer: 1 tails (and bands in full mode), 2 bands
     volatile uint32_t *issued;  // uses the producer copied (published at its end)
     unsigned long long *best;   // this launch's per-head minima (decode)
+    unsigned long long *ekey;   // [kWarps][kEarlyChunks]: the first chunks' candidates, per warp
+    int *ebh;                   // [kWarps][kEarlyChunks]: their heads
     unsigned long long *best_next;  // cleared here for the next decode launch
     volatile int *last;         // this CTA finished the last piece of a unit
   };
@@ -1034,8 +1036,10 @@ struct Step {
   // group's kRPG rows; a reduce-scatter over the group's 8 lanes (xor 4, 2,
   // then 1) leaves lanes 2k, 2k+1 with row k's distance (three pairwise
   // levels, as in row_dist); the warp's best then joins the head's minimum.
+  // The warp's best candidate of chunk j joins its head's minimum, or (slot
+  // >= 0) waits in the warp's slot of S.ekey until the minima may be used.
   __device__ static void match_chunk(const StepParams &p, const Smem &S, uint32_t n, int j, int grp, int sub,
-                                     unsigned long long &wait_ns) {
+                                     unsigned long long &wait_ns, int slot) {
     static_assert(kRPG == 4 || kRPG == 2, "rows per lane group");
     const bool pos_copy = pos_by_copy(p);
     const int kk = (sub >> (3 - kLogRPG)) & (kRPG - 1);  // the row this lane finishes
@@ -1108,18 +1112,29 @@ struct Step {
         bp = p2;
       }
     }
-    if ((threadIdx.x & 31) == 0 && bp >= 1) atomicMax(&S.best[bh], pack_best(D, bp));
+    if ((threadIdx.x & 31) == 0) {
+      const unsigned long long key = bp >= 1 ? pack_best(D, bp) : 0ull;
+      if (slot >= 0) {
+        S.ekey[slot] = key;
+        S.ebh[slot] = bh;
+      } else if (key) {
+        atomicMax(&S.best[bh], key);
+      }
+    }
   }
 
   // Match chunks i0 .. i1-1 of this CTA (chunk i is j = c + i*P), from stage
-  // use n on.
-  __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n, int i0, int i1) {
+  // use n on; with defer, the warps' candidates wait in S.ekey (the first
+  // chunks, scanned before the previous kernel on the stream has finished).
+  __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n, int i0, int i1,
+                                     bool defer = false) {
     const int P = gridDim.x;
     const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31, sub = lane & 7;
     const int grp = warp * 4 + (lane >> 3);  // row group: rows grp, grp + 32, ... of a chunk
     unsigned long long wait_ns = 0;
 #pragma unroll 1
-    for (int i = i0; i < i1; ++i) match_chunk(p, S, n++, blockIdx.x + i * P, grp, sub, wait_ns);
+    for (int i = i0; i < i1; ++i)
+      match_chunk(p, S, n++, blockIdx.x + i * P, grp, sub, wait_ns, defer ? warp * kEarlyChunks + (i - i0) : -1);
     unsigned long long *tr = threadIdx.x == 0 ? cta_trace(p) : nullptr;
     if (tr) {
       tr[28] += wait_ns;
@@ -2027,6 +2042,8 @@ struct Step {
     __shared__ int64_t s_span[2][kMaxGrid + 1];
     __shared__ int s_ne[2][kMaxGrid + 1];
     __shared__ long long s_short_max, s_band_tot[2], s_scan[kWarps];
+    __shared__ unsigned long long s_ekey[kWarps * kEarlyChunks];
+    __shared__ int s_ebh[kWarps * kEarlyChunks];
     const int n_units = p.B * p.Hkv, n_heads = p.B * p.Hq;
     Smem S;
     S.stage = smem;
@@ -2060,6 +2077,8 @@ struct Step {
     S.ready = &s_ready;
     S.issued = &s_issued;
     S.last = &s_last;
+    S.ekey = s_ekey;
+    S.ebh = s_ebh;
     const bool decode = p.mode == MODE_DECODE;
     const int tid = threadIdx.x;
     unsigned long long *trace = tid < kConsumers ? cta_trace(p) : nullptr;
@@ -2125,6 +2144,16 @@ struct Step {
       *S.ready = 1;  // the producer may copy tail tiles
     }
     stamp(trace, 7);
+    uint32_t n = 0;  // stage uses consumed so far (every consumer counts the same sequence)
+    const int nchunks = decode ? match_chunks(p) : 0;
+    const int early = nchunks < kEarlyChunks ? nchunks : kEarlyChunks;
+    // the first match chunks (their candidates held back: they may be
+    // scanned before the previous kernel on the stream has finished), then
+    // the tail pieces (every head attends them whatever the match decides),
+    // whose fixed costs so overlap the copies of the other match chunks;
+    // full attention counts every piece at its unit, so it lays out the
+    // bands before the first piece
+    match_phase(p, S, n, 0, early, true);
     // From here on the scratch workspace is used: the previous kernel on the
     // stream has finished and its writes are visible.  Decode launches
     // alternate between the two buffers of minima; the count changes only
@@ -2137,15 +2166,15 @@ struct Step {
     consumer_sync();
     S.best = p.best + (size_t)s_par * n_bh;
     S.best_next = p.best + (size_t)(s_par ^ 1) * n_bh;
-
-    uint32_t n = 0;  // stage uses consumed so far (every consumer counts the same sequence)
-    const int nchunks = decode ? match_chunks(p) : 0;
-    const int early = nchunks < kEarlyChunks ? nchunks : kEarlyChunks;
-    // the first match chunks, then the tail pieces (every head attends them
-    // whatever the match decides), whose fixed costs so overlap the copies
-    // of the other match chunks; full attention counts every piece at its
-    // unit, so it lays out the bands before the first piece
-    match_phase(p, S, n, 0, early);
+    if ((tid & 31) == 0) {
+      // the held-back candidates of the first chunks join their heads' minima
+      const int w = tid >> 5;
+#pragma unroll 1
+      for (int i = 0; i < early; ++i) {
+        const unsigned long long key = S.ekey[w * kEarlyChunks + i];
+        if (key) atomicMax(&S.best[S.ebh[w * kEarlyChunks + i]], key);
+      }
+    }
     // piece kinds: tails, short bands, long bands, then the merges no piece
     // triggers; the band layout comes before the tails (full attention) or
     // after the match and the decisions (decode): one call site
