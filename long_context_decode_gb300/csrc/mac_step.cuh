@@ -1502,6 +1502,7 @@ struct Step {
         acc[j] = (part[0] + part[1]) + (part[2] + part[3]);
       }
     }
+    griddep_wait();  // the partials live in the scratch workspace (a tail piece may come before the wait)
 #pragma unroll
     for (int j = 0; j < kOutPer; ++j) {
       const int e = tid + j * kConsumers;
@@ -2154,27 +2155,32 @@ struct Step {
     // full attention counts every piece at its unit, so it lays out the
     // bands before the first piece
     match_phase(p, S, n, 0, early, true);
-    // From here on the scratch workspace is used: the previous kernel on the
-    // stream has finished and its writes are visible.  Decode launches
-    // alternate between the two buffers of minima; the count changes only
-    // after every CTA of a launch has finished.
-    griddep_wait();
-    if (tid == 0) {
-      s_par = decode ? (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u) : 0;
-      if (s_badlen) set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
-    }
-    consumer_sync();
-    S.best = p.best + (size_t)s_par * n_bh;
-    S.best_next = p.best + (size_t)(s_par ^ 1) * n_bh;
-    if ((tid & 31) == 0) {
-      // the held-back candidates of the first chunks join their heads' minima
-      const int w = tid >> 5;
-#pragma unroll 1
-      for (int i = 0; i < early; ++i) {
-        const unsigned long long key = S.ekey[w * kEarlyChunks + i];
-        if (key) atomicMax(&S.best[S.ebh[w * kEarlyChunks + i]], key);
+    // From the dependency wait on, the scratch workspace is used: the
+    // previous kernel on the stream has finished and its writes are visible.
+    // Decode launches alternate between the two buffers of minima; the count
+    // changes only after every CTA of a launch has finished.  A decode step
+    // attends its tail pieces before the wait (their partials' stores wait
+    // for it), full attention counts its pieces and waits at once.
+    auto scratch_ready = [&]() {
+      griddep_wait();
+      if (tid == 0) {
+        s_par = decode ? (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u) : 0;
+        if (s_badlen) set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
       }
-    }
+      consumer_sync();
+      S.best = p.best + (size_t)s_par * n_bh;
+      S.best_next = p.best + (size_t)(s_par ^ 1) * n_bh;
+      if ((tid & 31) == 0) {
+        // the held-back candidates of the first chunks join their heads' minima
+        const int w = tid >> 5;
+#pragma unroll 1
+        for (int i = 0; i < early; ++i) {
+          const unsigned long long key = S.ekey[w * kEarlyChunks + i];
+          if (key) atomicMax(&S.best[S.ebh[w * kEarlyChunks + i]], key);
+        }
+      }
+    };
+    if (!decode) scratch_ready();
     // piece kinds: tails, short bands, long bands, then the merges no piece
     // triggers; the band layout comes before the tails (full attention) or
     // after the match and the decisions (decode): one call site
@@ -2183,6 +2189,7 @@ struct Step {
       if (kind == (decode ? 1 : 0)) {
         if (decode) {
           stamp(trace, 2);
+          scratch_ready();
           match_phase(p, S, n, early, nchunks);
           stamp(trace, 1);
           grid_barrier(p, S);  // the minima of every head are final, the tail partials written
