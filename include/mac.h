@@ -103,6 +103,9 @@ typedef struct {
   size_t stage_q;    /* dtype [B][Hq][d]: this step's pre-RoPE query, for the append */
   size_t stage_o;    /* f32 [B][Hq][d]: this step's AS_{1:m-r}, normalised */
   size_t stage_lse;  /* f32 [B][Hq]: its LSE */
+  size_t ctl;        /* the running step's match state (GQA groups up to 4): uint32 step
+                        count, uint32 [2] chunk counters, uint64 [2][B][Hq] per-head minima
+                        (the step count's parity selects the copy in use) */
   size_t total;      /* bytes */
 } mac_ring_layout;
 

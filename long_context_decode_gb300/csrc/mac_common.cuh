@@ -160,6 +160,10 @@ struct StepParams {
   const float *ring_o;       // [B][Hq][K][d]
   const float *ring_lse;     // [B][Hq][K]
   void *stage_q;             // [B][Hq][d]: copy of the step's query for the append
+  // the ring's match state (span kernel): [0] step count, [2 + k] chunk
+  // counter of copy k, then from word 4 the per-head minima u64 [2][B*Hq]
+  // (copy k = step count & 1 in use, the other cleared for the next step)
+  uint32_t *ring_ctl;
   // fused append (no auxiliary stream): the merges write slot pos mod K of
   // the rings themselves (null: the append kernel does)
   int32_t *app_pos;          // [B][K]

@@ -50,6 +50,7 @@ mac_ring_layout ring_layout(const mac_config *c) {
   L.stage_q = off;   off = align_up(off + B * H * d * es, 256);
   L.stage_o = off;   off = align_up(off + B * H * d * 4, 256);
   L.stage_lse = off; off = align_up(off + B * H * 4, 256);
+  L.ctl = off;       off = align_up(off + 16 + 2 * B * H * 8, 256);
   L.total = off;
   return L;
 }
@@ -380,6 +381,7 @@ int mac_init_rings(const mac_config *cfg, void *ring_ws, void *scratch_ws, const
   const ScratchLayout S = scratch_layout(cfg);
   uint8_t *ring = (uint8_t *)ring_ws, *scr = (uint8_t *)scratch_ws;
   if (cudaMemsetAsync(ring + R.pos, 0, (size_t)cfg->batch * cfg->ring_k * 4, s) != cudaSuccess ||
+      cudaMemsetAsync(ring + R.ctl, 0, R.total - R.ctl, s) != cudaSuccess ||
       cudaMemsetAsync(scr, 0, S.parts, s) != cudaSuccess)
     return MAC_ERR_CUDA;
   {
@@ -459,6 +461,7 @@ int mac_decode_step(const mac_config *cfg, void *ring_ws, void *scratch_ws, cons
   sp.ring_o = (const float *)(ring + R.o);
   sp.ring_lse = (const float *)(ring + R.lse);
   sp.stage_q = ring + R.stage_q;
+  sp.ring_ctl = (uint32_t *)(ring + R.ctl);
   sp.as_o = (float *)(ring + R.stage_o);
   sp.as_lse = (float *)(ring + R.stage_lse);
   sp.match_pos_out = match_pos;

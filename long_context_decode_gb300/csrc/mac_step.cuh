@@ -206,10 +206,7 @@ struct Step {
     volatile int *abort;
     volatile int *ready;  // layouts known to the producer: 1 tails (and bands in full mode), 2 bands
     volatile uint32_t *issued;  // uses the producer copied (published at its end)
-    unsigned long long *best;   // this launch's per-head minima (decode)
-    unsigned long long *ekey;   // [kWarps][kEarlyChunks]: the first chunks' candidates, per warp
-    int *ebh;                   // [kWarps][kEarlyChunks]: their heads
-    unsigned long long *best_next;  // cleared here for the next decode launch
+    int rpar;                   // decode: the copy of the ring's match state in use
     volatile int *last;         // this CTA finished the last piece of a unit
   };
 
@@ -868,25 +865,41 @@ struct Step {
     return n;
   }
 
-  // Match chunks i0 .. i1-1 of this CTA (chunk i is j = c + i*P) into stage
-  // uses n, n+1, ...; returns the next use.
-  __device__ static uint32_t copy_match(const StepParams &p, const Smem &S, uint32_t n, int i0, int i1) {
-    const int P = gridDim.x;
-    const int cph = chunks_per_head(p.K);
+  // The ring's match state: the step count, the chunk counter and the
+  // per-head minima of copy k (k = the step count's parity).
+  __device__ static uint32_t *chunk_counter(const StepParams &p, int k) { return p.ring_ctl + 2 + k; }
+  __device__ static unsigned long long *ring_best(const StepParams &p, int k) {
+    return reinterpret_cast<unsigned long long *>(p.ring_ctl + 4) + (size_t)k * p.B * p.Hq;
+  }
+
+  // The match chunks this CTA takes from the ring's counter (chunk j: rows
+  // [slot0, slot0 + rows) of head j / cph), each into the next stage use,
+  // then one stage use with no rows that ends the match; returns the next
+  // use.  CTAs that start earlier take more chunks.  The next chunk is taken
+  // while the current one's stage is awaited.
+  __device__ static uint32_t copy_match(const StepParams &p, const Smem &S, uint32_t n, int par) {
+    const int cph = chunks_per_head(p.K), nc = p.B * p.Hq * cph;
     const unsigned long long pol = l2_evict_first_policy();
+    uint32_t *ctr = chunk_counter(p, par);
+    int j = (int)atomicAdd(ctr, 1u);
 #pragma unroll 1
-    for (int i = i0; i < i1; ++i, ++n) {
-      if (!acquire_stage(p, S, n)) break;
-      const int j = blockIdx.x + i * P;
-      const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
-      const int rows = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
+    for (;; ++n) {
+      if (!acquire_stage(p, S, n)) return n;
       const int st = n % kStages;
       const uint32_t bar = smem_addr(&S.full[st]);
-      const bool pos_copy = pos_by_copy(p);
       uint8_t *side = S.qbuf + (size_t)st * kAux;
-      // the chunk's coordinates (plain store, ordered before the consumers'
-      // wait by the arrive below), then the head's query row and the
-      // chunk's ring positions, into the side buffer
+      if (j >= nc) {
+        // the end of the match (plain store, ordered before the consumers'
+        // wait by the arrive)
+        *reinterpret_cast<int4 *>(side + kInfoOff) = make_int4(-1, 0, 0, 0);
+        mbar_arrive(bar);
+        return n + 1;
+      }
+      const int bh = j / cph, slot0 = (j % cph) * kMatchRows;
+      const int rows = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
+      const bool pos_copy = pos_by_copy(p);
+      // the chunk's coordinates, then the head's query row and the chunk's
+      // ring positions, into the side buffer
       *reinterpret_cast<int4 *>(side + kInfoOff) = make_int4(bh, slot0, rows, bh / p.Hq);
       mbar_expect_tx(bar, (uint32_t)rows * kRowBytes + kRowBytes + (pos_copy ? 4u * rows : 0u));
       bulk_g2s_hint(smem_addr(S.stage + (size_t)st * kStageBytes),
@@ -896,29 +909,26 @@ struct Step {
                kRowBytes, bar);
       if (pos_copy)
         bulk_g2s(smem_addr(side + kRowBytes), p.ring_pos + (size_t)(bh / p.Hq) * p.K + slot0, 4u * rows, bar);
+      j = (int)atomicAdd(ctr, 1u);
     }
-    return n;
   }
   // Ring positions come with the chunk when their rows are 16-byte aligned.
   __device__ static bool pos_by_copy(const StepParams &p) { return (p.K & 3) == 0; }
 
-  // The producer warp: a copy engine.  Its first lane starts the first match
-  // copies (they need nothing but the parameters), then copies the tail
-  // tiles and the rest of the match chunks once the consumers publish the
-  // unit positions and the tail layout, the short pieces once they publish
-  // the short-band list, and the long-band pieces once they publish the
-  // long-band spans.  Every copy goes in the order the consumers use the
-  // stages: kEarlyChunks match chunks, tail pieces, the other match chunks,
-  // short pieces, long-band pieces.
+  // The producer warp: a copy engine.  Its first lane copies the match
+  // chunks it takes from the ring's counter (they need nothing but the
+  // parameters) and the use that ends the match, then the tail tiles once
+  // the consumers publish the unit positions and the tail layout, the short
+  // pieces once they publish the short-band list, and the long-band pieces
+  // once they publish the long-band spans.  Every copy goes in the order the
+  // consumers use the stages.
   __device__ static void producer_warp(const StepParams &p, const Smem &S) {
     const int lane = threadIdx.x & 31, U = p.B * p.Hkv;
     unsigned long long *tr = lane == 0 ? cta_trace(p) : nullptr;
     const bool decode = p.mode == MODE_DECODE;
     uint32_t n = 0;
-    const int nchunks = decode ? match_chunks(p) : 0;
-    const int early = nchunks < kEarlyChunks ? nchunks : kEarlyChunks;
     if (lane == 0) {
-      n = copy_match(p, S, 0, 0, early);
+      if (decode) n = copy_match(p, S, 0, S.rpar);
       if (tr) tr[30] = globaltimer();
       if (!wait_ready(p, S, 1)) *S.abort = 1;  // unit positions and tail layout
       if (tr) tr[31] = globaltimer();
@@ -939,12 +949,11 @@ struct Step {
       }
     }
     if (lane == 0) {
-      // tails (the unit layout is known), the rest of the match, then the
-      // short bands and the long bands as their layouts are published
+      // tails (the unit layout is known), then the short bands and the long
+      // bands as their layouts are published
 #pragma unroll 1
       for (int kind = 0; kind < 3 && !*S.abort; ++kind) {
         if (kind == 1) {
-          n = copy_match(p, S, n, early, nchunks);
           if (!wait_ready(p, S, 2)) break;
           if (tr) tr[26] = globaltimer();
         } else if (kind == 2) {
@@ -1036,26 +1045,25 @@ struct Step {
   // group's kRPG rows; a reduce-scatter over the group's 8 lanes (xor 4, 2,
   // then 1) leaves lanes 2k, 2k+1 with row k's distance (three pairwise
   // levels, as in row_dist); the warp's best then joins the head's minimum.
-  // The warp's best candidate of chunk j joins its head's minimum, or (slot
-  // >= 0) waits in the warp's slot of S.ekey until the minima may be used.
-  __device__ static void match_chunk(const StepParams &p, const Smem &S, uint32_t n, int j, int grp, int sub,
-                                     unsigned long long &wait_ns, int slot) {
+  // The match chunk in stage use n (false: the use that ends the match).
+  // The warp's best candidate joins its head's minimum in the ring's copy.
+  __device__ static bool match_chunk(const StepParams &p, const Smem &S, uint32_t n, int grp, int sub,
+                                     unsigned long long &wait_ns, unsigned long long *best) {
     static_assert(kRPG == 4 || kRPG == 2, "rows per lane group");
     const bool pos_copy = pos_by_copy(p);
     const int kk = (sub >> (3 - kLogRPG)) & (kRPG - 1);  // the row this lane finishes
     const int i_mine = grp + 32 * kk;
     int pk_mine = 0;
-    if (!pos_copy) {  // positions from global memory, before the wait
-      const int cph = chunks_per_head(p.K);
-      const int slot0 = (j % cph) * kMatchRows, cnt = p.K - slot0 < kMatchRows ? p.K - slot0 : kMatchRows;
-      pk_mine = __ldg(p.ring_pos + (int64_t)((j / cph) / p.Hq) * p.K + slot0 + (i_mine < cnt ? i_mine : cnt - 1));
-    }
     const bool timed = threadIdx.x == 0 && p.trace;
     const unsigned long long tw = timed ? globaltimer() : 0ull;
     const bool ok = wait_use(p, S, n);
     if (timed) wait_ns += globaltimer() - tw;
     if (n == 0) stamp(cta_trace(p), 8);
     const int st = n % kStages;
+    if (reinterpret_cast<const int4 *>(S.qbuf + (size_t)st * kAux + kInfoOff)->x < 0 || !ok) {
+      release(S, n);  // the end of the match (or an aborted wait)
+      return false;
+    }
     const uint8_t *rows = S.stage + (size_t)st * kStageBytes;
     const uint8_t *side = S.qbuf + (size_t)st * kAux;
     const int4 info = *reinterpret_cast<const int4 *>(side + kInfoOff);  // bh, slot0, rows, b
@@ -1064,7 +1072,10 @@ struct Step {
 #pragma unroll
     for (int cc = 0; cc < kNP; ++cc)
       unpack16x2<T>(*reinterpret_cast<const uint4 *>(side + cc * 128 + sub * 16), qv + cc * (kPer / 2));
-    if (pos_copy) pk_mine = reinterpret_cast<const int32_t *>(side + kRowBytes)[i_mine < cnt ? i_mine : cnt - 1];
+    if (pos_copy)
+      pk_mine = reinterpret_cast<const int32_t *>(side + kRowBytes)[i_mine < cnt ? i_mine : cnt - 1];
+    else
+      pk_mine = __ldg(p.ring_pos + (int64_t)info.w * p.K + info.y + (i_mine < cnt ? i_mine : cnt - 1));
     const int64_t m = S.X[info.w];  // the request's length, tabled before the match
     // the lane's partial sums of the group's rows (rows past the chunk read
     // stale stage bytes and are discarded below)
@@ -1112,47 +1123,36 @@ struct Step {
         bp = p2;
       }
     }
-    if ((threadIdx.x & 31) == 0) {
-      const unsigned long long key = bp >= 1 ? pack_best(D, bp) : 0ull;
-      if (slot >= 0) {
-        S.ekey[slot] = key;
-        S.ebh[slot] = bh;
-      } else if (key) {
-        atomicMax(&S.best[bh], key);
-      }
-    }
+    if ((threadIdx.x & 31) == 0 && bp >= 1) atomicMax(&best[bh], pack_best(D, bp));
+    return true;
   }
 
-  // Match chunks i0 .. i1-1 of this CTA (chunk i is j = c + i*P), from stage
-  // use n on; with defer, the warps' candidates wait in S.ekey (the first
-  // chunks, scanned before the previous kernel on the stream has finished).
-  __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n, int i0, int i1,
-                                     bool defer = false) {
-    const int P = gridDim.x;
+  // The match chunks the producer took for this CTA, from stage use n on,
+  // up to and including the use that ends the match.  Nothing here touches
+  // the scratch workspace, so it may run before the previous kernel on the
+  // stream has finished.
+  __device__ static void match_phase(const StepParams &p, const Smem &S, uint32_t &n) {
     const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31, sub = lane & 7;
     const int grp = warp * 4 + (lane >> 3);  // row group: rows grp, grp + 32, ... of a chunk
+    unsigned long long *best = ring_best(p, S.rpar);
     unsigned long long wait_ns = 0;
+    int chunks = 0;
 #pragma unroll 1
-    for (int i = i0; i < i1; ++i)
-      match_chunk(p, S, n++, blockIdx.x + i * P, grp, sub, wait_ns, defer ? warp * kEarlyChunks + (i - i0) : -1);
+    while (match_chunk(p, S, n++, grp, sub, wait_ns, best)) ++chunks;
     unsigned long long *tr = threadIdx.x == 0 ? cta_trace(p) : nullptr;
     if (tr) {
       tr[28] += wait_ns;
-      tr[29] += (unsigned long long)(i1 > i0 ? i1 - i0 : 0);
+      tr[29] += (unsigned long long)chunks;
     }
   }
-
-  // Match chunks of this CTA, and how many come before its tail pieces.
-  __device__ static int match_chunks(const StepParams &p) {
-    const int nc = p.B * p.Hq * chunks_per_head(p.K), P = gridDim.x, c = blockIdx.x;
-    return c < nc ? (nc - c + P - 1) / P : 0;
-  }
-  static constexpr int kEarlyChunks = 4;
 
   // All CTAs of the (co-resident, cooperative) grid meet; bounded wait.  One
   // thread per CTA polls without sleeping: the last arrival is seen one L2
   // round trip after it lands.
   __device__ static void grid_barrier(const StepParams &p, const Smem &S) {
+    // every consumer's earlier writes and atomics (the match minima, the
+    // tail partials) come before thread 0's release
+    consumer_sync();
     if (threadIdx.x == 0) {
       unsigned long long *ctr = reinterpret_cast<unsigned long long *>(p.ctl + 2);
       const unsigned long long old = atom_add_release_u64(ctr, 1ull);
@@ -1180,7 +1180,7 @@ struct Step {
     for (int bh = tid; bh < n_bh; bh += kConsumers) {
       const int b = bh / p.Hq, u = b * p.Hkv + (bh % p.Hq) / G;
       const int64_t m = unit_len(p, S, u);
-      const unsigned long long inv = __ldcg(&S.best[bh]);
+      const unsigned long long inv = __ldcg(&ring_best(p, S.rpar)[bh]);
       int pos = -1;
       if (inv != 0ull && len_ok(p, m) && m >= p.min_context) {
         const unsigned long long key = ~inv;
@@ -2038,13 +2038,11 @@ struct Step {
   __device__ static void run(const StepParams &p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_mask[kStages];
-    __shared__ int s_abort, s_ready, s_last, s_par, s_nshort, s_badlen;
+    __shared__ int s_abort, s_ready, s_last, s_rpar, s_nshort, s_badlen;
     __shared__ uint32_t s_issued;
     __shared__ int64_t s_span[2][kMaxGrid + 1];
     __shared__ int s_ne[2][kMaxGrid + 1];
     __shared__ long long s_short_max, s_band_tot[2], s_scan[kWarps];
-    __shared__ unsigned long long s_ekey[kWarps * kEarlyChunks];
-    __shared__ int s_ebh[kWarps * kEarlyChunks];
     const int n_units = p.B * p.Hkv, n_heads = p.B * p.Hq;
     Smem S;
     S.stage = smem;
@@ -2078,8 +2076,6 @@ struct Step {
     S.ready = &s_ready;
     S.issued = &s_issued;
     S.last = &s_last;
-    S.ekey = s_ekey;
-    S.ebh = s_ebh;
     const bool decode = p.mode == MODE_DECODE;
     const int tid = threadIdx.x;
     unsigned long long *trace = tid < kConsumers ? cta_trace(p) : nullptr;
@@ -2097,14 +2093,19 @@ struct Step {
       s_ready = 0;
       s_issued = 0;
       s_badlen = 0;
+      // the ring's match state in use: the step count's parity (the previous
+      // step on this ring has finished: it is never started early)
+      s_rpar = decode ? (int)(*(volatile uint32_t *)p.ring_ctl & 1u) : 0;
       mbar_fence_init();
     }
     __syncthreads();  // the last barrier of all kThreads threads
+    S.rpar = s_rpar;
     // The next step kernel on the stream may start its CTAs on the SMs this
     // grid frees.  Until their dependency wait they read only inputs (this
     // launch's queries and lengths, their own layer's rings) and write only
-    // shared memory; the host launches them early only when this launch
-    // writes none of those (a step on another ring, or full attention).
+    // shared memory and their own layer's ring state; the host launches them
+    // early only when this launch writes none of those (a step on another
+    // ring, or full attention).
     griddep_launch_dependents();
     const int n_bh = n_heads;
 
@@ -2146,39 +2147,20 @@ struct Step {
     }
     stamp(trace, 7);
     uint32_t n = 0;  // stage uses consumed so far (every consumer counts the same sequence)
-    const int nchunks = decode ? match_chunks(p) : 0;
-    const int early = nchunks < kEarlyChunks ? nchunks : kEarlyChunks;
-    // the first match chunks (their candidates held back: they may be
-    // scanned before the previous kernel on the stream has finished), then
-    // the tail pieces (every head attends them whatever the match decides),
-    // whose fixed costs so overlap the copies of the other match chunks;
-    // full attention counts every piece at its unit, so it lays out the
-    // bands before the first piece
-    match_phase(p, S, n, 0, early, true);
+    // The match, as many chunks as the producer took from the ring's
+    // counter, then the tail pieces (every head attends them whatever the
+    // match decides): neither needs the scratch workspace (the tail
+    // partials' stores wait for the previous kernel), so both may run while
+    // the previous kernel on the stream finishes.  Full attention counts
+    // every piece at its unit, so it lays out the bands before the first
+    // piece and waits at once.
+    if (decode) match_phase(p, S, n);
+    stamp(trace, 1);
     // From the dependency wait on, the scratch workspace is used: the
     // previous kernel on the stream has finished and its writes are visible.
-    // Decode launches alternate between the two buffers of minima; the count
-    // changes only after every CTA of a launch has finished.  A decode step
-    // attends its tail pieces before the wait (their partials' stores wait
-    // for it), full attention counts its pieces and waits at once.
     auto scratch_ready = [&]() {
       griddep_wait();
-      if (tid == 0) {
-        s_par = decode ? (int)(*(volatile uint32_t *)(p.ctl + 6) & 1u) : 0;
-        if (s_badlen) set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
-      }
-      consumer_sync();
-      S.best = p.best + (size_t)s_par * n_bh;
-      S.best_next = p.best + (size_t)(s_par ^ 1) * n_bh;
-      if ((tid & 31) == 0) {
-        // the held-back candidates of the first chunks join their heads' minima
-        const int w = tid >> 5;
-#pragma unroll 1
-        for (int i = 0; i < early; ++i) {
-          const unsigned long long key = S.ekey[w * kEarlyChunks + i];
-          if (key) atomicMax(&S.best[S.ebh[w * kEarlyChunks + i]], key);
-        }
-      }
+      if (tid == 0 && s_badlen) set_status(p.ctl, MAC_DEV_BAD_SEQ_LEN);
     };
     if (!decode) scratch_ready();
     // piece kinds: tails, short bands, long bands, then the merges no piece
@@ -2190,14 +2172,15 @@ struct Step {
         if (decode) {
           stamp(trace, 2);
           scratch_ready();
-          match_phase(p, S, n, early, nchunks);
-          stamp(trace, 1);
           grid_barrier(p, S);  // the minima of every head are final, the tail partials written
           stamp(trace, 10);
           decide(p, S, trace);
-          // nobody reads the other buffer in this launch: clear it for the next
+          // nobody uses the ring's other copy of the match state in this
+          // launch: clear it for the next step on this ring
+          unsigned long long *next = ring_best(p, S.rpar ^ 1);
 #pragma unroll 1
-          for (int i = blockIdx.x * kConsumers + tid; i < n_bh; i += gridDim.x * kConsumers) S.best_next[i] = 0ull;
+          for (int i = blockIdx.x * kConsumers + tid; i < n_bh; i += gridDim.x * kConsumers) next[i] = 0ull;
+          if (blockIdx.x == 0 && tid == 0) *chunk_counter(p, S.rpar ^ 1) = 0u;
         }
         layout_bands(p, S, trace);
         stamp(trace, 3);
@@ -2228,7 +2211,10 @@ struct Step {
       const uint32_t old = atomicAdd(p.ctl + 4, 1u);
       if (old == gridDim.x - 1) {  // every CTA of the launch has finished
         p.ctl[4] = 0;
-        if (decode) atomicAdd(p.ctl + 6, 1u);
+        if (decode) {
+          atomicAdd(p.ctl + 6, 1u);
+          *p.ring_ctl = *p.ring_ctl + 1u;  // the next step on this ring uses the other copy
+        }
         if (*(volatile uint32_t *)p.ctl != 0)
 #pragma unroll 1
           for (int u = 0; u < n_units; ++u) p.unit_done[u] = 0;

@@ -47,7 +47,7 @@ class mac_kv(ctypes.Structure):
 
 class mac_ring_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("pos", "q", "o", "lse", "stage_q", "stage_o", "stage_lse", "total")]
+                ("pos", "q", "o", "lse", "stage_q", "stage_o", "stage_lse", "ctl", "total")]
 
 
 class MacError(RuntimeError):

@@ -38,7 +38,7 @@ def test_struct_sizes_match_the_header(mac):
     # mac_config: 6 int32, double, int32(+pad), double, 4 int32, int64, int32(+pad) = 80 bytes
     assert ctypes.sizeof(mac.mac_config) == 80
     assert ctypes.sizeof(mac.mac_kv) == 40
-    assert ctypes.sizeof(mac.mac_ring_layout) == 64
+    assert ctypes.sizeof(mac.mac_ring_layout) == 72
 
 
 def test_workspace_sizes_and_validation(mac):
@@ -46,7 +46,7 @@ def test_workspace_sizes_and_validation(mac):
     ring, scratch = mac.mac_workspace_size(cfg)
     assert ring > 0 and scratch > 0
     lay = mac.mac_ring_layout_of(cfg)
-    parts = [lay.pos, lay.q, lay.o, lay.lse, lay.stage_q, lay.stage_o, lay.stage_lse, lay.total]
+    parts = [lay.pos, lay.q, lay.o, lay.lse, lay.stage_q, lay.stage_o, lay.stage_lse, lay.ctl, lay.total]
     assert parts == sorted(parts) and all(p % 256 == 0 for p in parts)
     assert lay.total == ring
     bad = [
