@@ -281,9 +281,11 @@ int mac_set_phase_events(void *before_step, void *after_step, void *after_append
  *   13/19 warps 0 / 1: owner merge's list read   14/15 owner merge's
  *         states written / combined  18 owner merge start
  *   16/17 the SM's clock64() at start / end
- * Stamps of phases a launch does not run are left as they were.  The buffer
- * must hold MAC_TRACE_POINTS * (number of SMs) uint64.  The hook clears
- * itself. */
+ * Stamps of phases a launch does not run are left as they were.  The span
+ * kernel's stamps are compiled into one instantiation only, bf16 K/V without
+ * a front sink, which the launch then runs; other span-kernel launches leave
+ * the buffer as it was.  The buffer must hold MAC_TRACE_POINTS * (number of
+ * SMs) uint64.  The hook clears itself. */
 #define MAC_TRACE_POINTS 32
 int mac_set_trace(void *device_buffer);
 

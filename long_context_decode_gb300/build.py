@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmac_gb300.so")
 SOURCES = ["mac_host.cu", "mac_append.cu", "mac_step_bf16.cu", "mac_step_f32.cu", "mac_step_bf16_sink.cu",
-           "mac_step_f32_sink.cu", "mac_ring_bf16_g8.cu", "mac_ring_f32_g8.cu"]
+           "mac_step_f32_sink.cu", "mac_step_bf16_trace.cu", "mac_ring_bf16_g8.cu", "mac_ring_f32_g8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -229,6 +229,8 @@ int step_occupancy_bf16(int G, bool paged, int B, int Hq, int Hkv, int K);
 int step_occupancy_f32(int G, bool paged, int B, int Hq, int Hkv, int K);
 int step_occupancy_bf16_sink(int G, bool paged, int B, int Hq, int Hkv, int K);
 int step_occupancy_f32_sink(int G, bool paged, int B, int Hq, int Hkv, int K);
+// the span kernel with the phase trace compiled in (bf16, no front sink)
+cudaError_t launch_step_bf16_trace(const StepParams &p, int grid, cudaStream_t s);
 // ring kernel, G = 8
 namespace ring {
 cudaError_t launch_bf16_g8(const StepParams &p, int grid, cudaStream_t s);

@@ -314,6 +314,7 @@ cudaError_t launch_step(StepParams p, const mac_config *c, cudaStream_t s) {
     return f32 ? ring::launch_f32_g8(p, grid, s) : ring::launch_bf16_g8(p, grid, s);
   }
   if (p.sink_piece) return f32 ? launch_step_f32_sink(p, grid, s) : launch_step_bf16_sink(p, grid, s);
+  if (p.trace && !f32) return launch_step_bf16_trace(p, grid, s);  // the only traced instantiation
   return f32 ? launch_step_f32(p, grid, s) : launch_step_bf16(p, grid, s);
 }
 

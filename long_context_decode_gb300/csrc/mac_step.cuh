@@ -114,8 +114,10 @@ constexpr float kLazy = 8.f;
 constexpr unsigned kFull = 0xffffffffu;
 
 // SINK: whether the kernel attends front-sink pieces (a launch with a front
-// sink uses the SINK = true kernels; the others carry none of that code)
-template <typename T, int G, bool PAGED, bool SINK>
+// sink uses the SINK = true kernels; the others carry none of that code).
+// TRACE: whether it records the phase trace (mac_set_trace); the product
+// kernels carry none of that code either.
+template <typename T, int G, bool PAGED, bool SINK, bool TRACE = false>
 struct Step {
   static constexpr int kRowBytes = kHeadDim * (int)sizeof(T);
   static constexpr int kTileTok = kStageBytes / (2 * kRowBytes);  // 64 (bf16) / 32 (fp32)
@@ -219,11 +221,14 @@ struct Step {
   // Like every region run by one thread, it ends with the warp reconverged
   // before the barriers and shuffles that follow.
   __device__ static void stamp(unsigned long long *trace, int k) {
-    if (trace && threadIdx.x == 0) trace[k] = globaltimer();
-    __syncwarp();
+    if constexpr (TRACE) {
+      if (trace && threadIdx.x == 0) trace[k] = globaltimer();
+      __syncwarp();
+    }
   }
   __device__ static unsigned long long *cta_trace(const StepParams &p) {
-    return p.trace ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
+    if constexpr (TRACE) return p.trace ? p.trace + (size_t)blockIdx.x * kTracePoints : nullptr;
+    return nullptr;
   }
 
   // Lane `sub` (0..7) of a token's 8-lane group owns 16 dimensions: piece c
@@ -1054,7 +1059,7 @@ struct Step {
     const int kk = (sub >> (3 - kLogRPG)) & (kRPG - 1);  // the row this lane finishes
     const int i_mine = grp + 32 * kk;
     int pk_mine = 0;
-    const bool timed = threadIdx.x == 0 && p.trace;
+    const bool timed = TRACE && threadIdx.x == 0 && p.trace;
     const unsigned long long tw = timed ? globaltimer() : 0ull;
     const bool ok = wait_use(p, S, n);
     if (timed) wait_ns += globaltimer() - tw;
@@ -2227,9 +2232,9 @@ struct Step {
   }
 };
 
-template <typename T, int G, bool PAGED, bool SINK>
+template <typename T, int G, bool PAGED, bool SINK, bool TRACE>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepParams p) {
-  Step<T, G, PAGED, SINK>::run(p);
+  Step<T, G, PAGED, SINK, TRACE>::run(p);
 }
 
 }  // namespace mac

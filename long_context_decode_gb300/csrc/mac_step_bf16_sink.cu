@@ -3,9 +3,9 @@
 
 namespace mac {
 cudaError_t launch_step_bf16_sink(const StepParams &p, int grid, cudaStream_t s) {
-  return launch_step_t<uint16_t, true>(p, grid, s);
+  return launch_step_t<uint16_t, true, false>(p, grid, s);
 }
 int step_occupancy_bf16_sink(int G, bool paged, int B, int Hq, int Hkv, int K) {
-  return occupancy_t<uint16_t, true>(G, paged, B, Hq, Hkv, K);
+  return occupancy_t<uint16_t, true, false>(G, paged, B, Hq, Hkv, K);
 }
 }  // namespace mac

@@ -3,9 +3,9 @@
 
 namespace mac {
 cudaError_t launch_step_f32(const StepParams &p, int grid, cudaStream_t s) {
-  return launch_step_t<float, false>(p, grid, s);
+  return launch_step_t<float, false, false>(p, grid, s);
 }
 int step_occupancy_f32(int G, bool paged, int B, int Hq, int Hkv, int K) {
-  return occupancy_t<float, false>(G, paged, B, Hq, Hkv, K);
+  return occupancy_t<float, false, false>(G, paged, B, Hq, Hkv, K);
 }
 }  // namespace mac
