@@ -2177,15 +2177,27 @@ struct Step {
         if (decode) {
           stamp(trace, 2);
           scratch_ready();
+          // the merge counts start from zero, also after a launch that
+          // failed with counts left over (no merge runs before the barrier)
+#pragma unroll 1
+          for (int i = blockIdx.x * kConsumers + tid; i < n_units + kGroups; i += gridDim.x * kConsumers) {
+            if (i < n_units) p.unit_done[i] = 0u;
+            p.group_done[i] = 0u;
+          }
           grid_barrier(p, S);  // the minima of every head are final, the tail partials written
           stamp(trace, 10);
           decide(p, S, trace);
           // nobody uses the ring's other copy of the match state in this
-          // launch: clear it for the next step on this ring
+          // launch: clear it for the next step on this ring, which uses it
+          // (every CTA read the step count before the barrier)
           unsigned long long *next = ring_best(p, S.rpar ^ 1);
 #pragma unroll 1
           for (int i = blockIdx.x * kConsumers + tid; i < n_bh; i += gridDim.x * kConsumers) next[i] = 0ull;
-          if (blockIdx.x == 0 && tid == 0) *chunk_counter(p, S.rpar ^ 1) = 0u;
+          if (blockIdx.x == 0 && tid == 0) {
+            *chunk_counter(p, S.rpar ^ 1) = 0u;
+            *p.ring_ctl = *p.ring_ctl + 1u;
+            atomicAdd(p.ctl + 6, 1u);  // decode launches
+          }
         }
         layout_bands(p, S, trace);
         stamp(trace, 3);
@@ -2208,21 +2220,21 @@ struct Step {
         }
       }
     }
-    if (tid == 0) {
-      // the last CTA to finish advances the decode launch count; after a
-      // failed launch it also clears the piece counts the merges of that
-      // launch may have left
+    if (tid == 0 && !decode) {
+      // full attention has no grid barrier before its merges: the last CTA
+      // to finish a failed launch clears the piece counts its merges may
+      // have left (a decode step clears them before its grid barrier, so
+      // its CTAs exit without waiting on a count)
       __threadfence();
       const uint32_t old = atomicAdd(p.ctl + 4, 1u);
       if (old == gridDim.x - 1) {  // every CTA of the launch has finished
         p.ctl[4] = 0;
-        if (decode) {
-          atomicAdd(p.ctl + 6, 1u);
-          *p.ring_ctl = *p.ring_ctl + 1u;  // the next step on this ring uses the other copy
-        }
-        if (*(volatile uint32_t *)p.ctl != 0)
+        if (*(volatile uint32_t *)p.ctl != 0) {
 #pragma unroll 1
           for (int u = 0; u < n_units; ++u) p.unit_done[u] = 0;
+#pragma unroll 1
+          for (int u = 0; u < n_units + kGroups; ++u) p.group_done[u] = 0;
+        }
       }
     }
     __syncwarp();
