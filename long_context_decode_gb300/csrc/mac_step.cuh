@@ -420,16 +420,18 @@ struct Step {
   // list, long-band offsets) right after the decisions, so that the short
   // pieces can start; band_spans_block (the long-band spans, their
   // non-empty counts and every long unit's CTA run) by all consumer threads
-  // while the producer copies the short pieces.
-  static constexpr int kShortBand = 128;
-  static constexpr int kPieceCost = 384;  // fixed cost of a piece and its merge, in tokens
+  // while the producer copies the short pieces.  kShortBand, kPieceCost and
+  // kLongPiece were set by timing the 4 x 128K decode step over a sweep of
+  // each (the other two in their ranges made it no faster).
+  static constexpr int kShortBand = 256;
+  static constexpr int kPieceCost = 512;  // fixed cost of a piece and its merge, in tokens
   static constexpr int kSnap = 192;       // largest move of a long-band CTA boundary, in tokens
   // On the long bands' cost axis each band starts with kLongPiece virtual
   // tokens, a piece's fixed cost: a CTA whose span meets a band's start
   // pays it, so a CTA with two pieces gets fewer tokens.  No CTA boundary
   // falls inside that prefix or at its end (it moves to the band's start),
   // so every non-empty span holds real tokens of each band it meets.
-  static constexpr int kLongPiece = 96;
+  static constexpr int kLongPiece = 256;
   __device__ static bool short_band(const StepParams &p, const Smem &S, int u) {
     const int64_t n = seg_len(p, S, 1, u);
     return n > 0 && n <= *S.short_max;
