@@ -10,11 +10,16 @@ phase trace (``mac_set_trace``): per CTA, %globaltimer stamps at the end of
 each phase.  Each replay of that graph is one traced step; the table gives,
 per phase, the median CTA's and the last CTA's time since the first CTA
 started, for steps where every head hits and for steps with one missing
-unit.  Timestamps cost a store each, so the traced kernel runs a little
-slower than the untimed one.
+unit.  The traced kernel is a separate instantiation with the stamps
+compiled in (the product kernels carry none); a stamp costs a timer read
+and a store, so it runs a little slower than the product kernel.
 
-The stamps follow the span kernel's layout (GQA groups up to 4; see
-``mac_set_trace`` in include/mac.h).
+Each class also gets the mean CTA residency (start to end): in a stack of
+layers the next kernel's CTAs take each SM as it frees up (early start), so
+the SMs stay occupied and the layer step's period is close to this mean.
+
+The stamps follow the span kernel's layout (GQA groups up to 4, bf16
+without a front sink; see ``mac_set_trace`` in include/mac.h).
 """
 from __future__ import annotations
 
@@ -26,6 +31,7 @@ import numpy as np
 
 # span kernel stamps, in phase order: (index, name)
 PHASES = [
+    (0, "start"),
     (7, "tail layout published"),
     (8, "first match chunk arrived"),
     (2, "tail pieces done"),
@@ -124,6 +130,11 @@ def main(argv=None):
             if len(col):
                 c = (col - t0) / 1e3
                 row[name] = (float(np.median(c)), float(c.max()))
+        # CTA residency: start to end of each CTA, averaged over the CTAs.  In
+        # a stack of layers the next kernel's CTAs take each SM as it frees
+        # up, so the layer step's period is close to this mean.
+        ran = (t[:, 0] != 0) & (t[:, 6] != 0)
+        row["residency_us"] = float(np.mean((t[ran, 6] - t[ran, 0]) / 1e3)) if ran.any() else None
         clk = (t[:, 17] - t[:, 16]) / np.maximum(1, t[:, 6] - t[:, 0])
         row["sm_ghz"] = float(np.median(clk[clk > 0])) if (clk > 0).any() else None
         # per-CTA band work: the last band piece's tiles done (stamp 24, us),
@@ -175,6 +186,9 @@ def main(argv=None):
                 print(f"  {key}: " + " / ".join(f"{v:.2f}" for v in np.median(np.array(vals), 0)))
         print(f"  longest merge: {np.median([r['longest_merge_us'] for r in sel]):.2f} us, "
               f"{int(np.median([r['longest_merge_entries'] for r in sel]))} entries")
+        res = [r["residency_us"] for r in sel if r["residency_us"] is not None]
+        if res:
+            print(f"  CTA residency (start to end, mean over the CTAs): {np.median(res):.2f} us")
     ghz = [r["sm_ghz"] for r in rows if r["sm_ghz"]]
     print()
     print(f"µs since the first CTA started; medians over the steps of each class. SM clock during the "
