@@ -204,7 +204,7 @@ struct Step {
     long long *short_max;  // longest band that is one piece
     long long *band_tot;   // [2]: long-band tokens, their cost plus the short pieces'
     float2 *rope;       // [B][d/2]: cos, sin of the query's rotation angles (B <= kRopeTab), or null
-    int *mask;          // [kStages]: valid 16-token pages of the tile in the stage
+    int *mask;          // [kStages]: valid 16-row groups of the tile in the stage (pages, if paged)
     volatile int *abort;
     volatile int *ready;  // layouts known to the producer: 1 tails (and bands in full mode), 2 bands
     volatile uint32_t *issued;  // uses the producer copied (published at its end)
@@ -649,21 +649,21 @@ struct Step {
     }
   }
 
-  // Paged tile `t` of piece pc with its page ids already loaded (kNoPage past
-  // the table): the rows of each 16-token page that fall in the piece, page
-  // by page; an id outside the pool is refused and reported.
+  // Paged tile of piece pc starting after token tb (a page boundary), with
+  // the ids of its kSlots page-table slots from tb / 16 on already loaded
+  // (kNoPage past the table): the rows of each 16-token page that fall in
+  // the piece, page by page; an id outside the pool is refused and reported.
   static constexpr int32_t kNoPage = (int32_t)0x80000000;
-  __device__ static void issue_paged_tile(const StepParams &p, const Smem &S, int st, const Piece &pc, int t,
+  static constexpr int kSlots = kTileTok / 16;  // pages in a tile
+  __device__ static void issue_paged_tile(const StepParams &p, const Smem &S, int st, const Piece &pc, int tb,
                                           bool with_q, const int32_t *ids) {
-    constexpr int kPg = kTileTok / 16;
     const int g = pc.u % p.Hkv;
     uint8_t *kbuf = S.stage + (size_t)st * kStageBytes;
     const uint32_t bar = smem_addr(&S.full[st]);
-    const int tb = t * kTileTok;
     uint32_t bytes = with_q ? (uint32_t)kQBytes : 0u;
     int msk = 0;
 #pragma unroll
-    for (int pg = 0; pg < kPg; ++pg) {
+    for (int pg = 0; pg < kSlots; ++pg) {
       const int pa = tb + pg * 16 + 1, ra = pa > pc.lo ? pa : pc.lo, rz = pa + 15 < pc.hi ? pa + 15 : pc.hi;
       if (ra > rz || ids[pg] == kNoPage) continue;  // (past the table: nothing to copy)
       if (ids[pg] < 0 || ids[pg] >= p.kv.n_pages) {
@@ -682,7 +682,7 @@ struct Step {
     if (with_q) copy_q(p, S, st, pc.u, bar);
     const unsigned long long pol = l2_evict_first_policy();
 #pragma unroll
-    for (int pg = 0; pg < kPg; ++pg) {
+    for (int pg = 0; pg < kSlots; ++pg) {
       if (!((msk >> pg) & 1)) continue;
       const int pa = tb + pg * 16 + 1, ra = pa > pc.lo ? pa : pc.lo, rz = pa + 15 < pc.hi ? pa + 15 : pc.hi;
       const size_t off = (((size_t)ids[pg] * p.Hkv + g) * 16 + (size_t)(ra - pa)) * kRowBytes;
@@ -690,85 +690,6 @@ struct Step {
       uint8_t *dst = kbuf + (size_t)(ra - tb - 1) * kRowBytes;
       bulk_g2s_hint(smem_addr(dst), (const uint8_t *)p.kv.k + off, nb, bar, pol);
       bulk_g2s_hint(smem_addr(dst + kStageBytes / 2), (const uint8_t *)p.kv.v + off, nb, bar, pol);
-    }
-  }
-
-  // Rows of K/V tile `tile` (tokens tile*kTileTok+1 .. +kTileTok) that fall in
-  // [lo, hi], each copied to its own row of the stage, so no byte outside the
-  // piece is read; with_q also brings the unit's G pre-RoPE query rows.
-  __device__ static void issue_tile(const StepParams &p, const Smem &S, int st, int u, int lo,
-                                    int hi, int64_t tile, bool with_q) {
-    if (u < 0 || u >= p.B * p.Hkv) {
-      set_status(p.ctl, MAC_DEV_BAD_COPY);
-      S.mask[st] = 0;
-      mbar_arrive(smem_addr(&S.full[st]));
-      return;
-    }
-    const int b = u / p.Hkv, g = u % p.Hkv;
-    uint8_t *kbuf = S.stage + (size_t)st * kStageBytes;
-    uint8_t *vbuf = kbuf + kStageBytes / 2;
-    const uint32_t bar = smem_addr(&S.full[st]);
-    const int64_t t0 = tile * kTileTok;
-    uint32_t bytes = with_q ? (uint32_t)kQBytes : 0u;
-    int msk = 0;
-    int64_t ra[kTileTok / 16], rz[kTileTok / 16];
-    int32_t pid[kTileTok / 16];
-    if (!PAGED) {
-      msk = (1 << (kTileTok / 16)) - 1;
-      ra[0] = t0 + 1 > lo ? t0 + 1 : lo;
-      rz[0] = t0 + kTileTok < hi ? t0 + kTileTok : hi;
-      // the schedule only issues tiles that meet [lo, hi] inside the cache;
-      // anything else is refused rather than copied
-      if (ra[0] > rz[0] || ra[0] < 1 || rz[0] > p.kv.capacity || u < 0 || u >= p.B * p.Hkv) {
-        set_status(p.ctl, MAC_DEV_BAD_COPY);
-        msk = 0;
-        with_q = false;
-        bytes = 0;
-      } else {
-        bytes += 2u * (uint32_t)(rz[0] - ra[0] + 1) * kRowBytes;
-      }
-    } else {
-      for (int pg = 0; pg < kTileTok / 16; ++pg) {
-        const int64_t slot = tile * (kTileTok / 16) + pg;
-        const int64_t pa = t0 + pg * 16 + 1, pz = pa + 15;
-        ra[pg] = pa > lo ? pa : lo;
-        rz[pg] = pz < hi ? pz : hi;
-        pid[pg] = -1;
-        if (ra[pg] > rz[pg] || slot >= p.kv.max_pages) continue;
-        const int32_t id = p.kv.page_table[(int64_t)b * p.kv.max_pages + slot];
-        if (id < 0 || id >= p.kv.n_pages) {
-          set_status(p.ctl, MAC_DEV_BAD_PAGE);
-          continue;
-        }
-        pid[pg] = id;
-        msk |= 1 << pg;
-        bytes += 2u * (uint32_t)(rz[pg] - ra[pg] + 1) * kRowBytes;
-      }
-    }
-    S.mask[st] = msk;
-    if (bytes == 0) {
-      mbar_arrive(bar);
-      return;
-    }
-    mbar_expect_tx(bar, bytes);
-    if (with_q) copy_q(p, S, st, u, bar);
-    const unsigned long long pol = l2_evict_first_policy();
-    if (!PAGED) {
-      if (msk == 0) return;
-      const size_t off = (((size_t)b * p.Hkv + g) * (size_t)p.kv.capacity + (size_t)(ra[0] - 1)) * kRowBytes;
-      const uint32_t n = (uint32_t)(rz[0] - ra[0] + 1) * kRowBytes;
-      const uint32_t dst = (uint32_t)(ra[0] - t0 - 1) * kRowBytes;
-      bulk_g2s_hint(smem_addr(kbuf + dst), (const uint8_t *)p.kv.k + off, n, bar, pol);
-      bulk_g2s_hint(smem_addr(vbuf + dst), (const uint8_t *)p.kv.v + off, n, bar, pol);
-    } else {
-      for (int pg = 0; pg < kTileTok / 16; ++pg) {
-        if (pid[pg] < 0) continue;
-        const size_t off = (((size_t)pid[pg] * p.Hkv + g) * 16 + (size_t)((ra[pg] - 1) % 16)) * kRowBytes;
-        const uint32_t n = (uint32_t)(rz[pg] - ra[pg] + 1) * kRowBytes;
-        const uint32_t dst = (uint32_t)(ra[pg] - t0 - 1) * kRowBytes;
-        bulk_g2s_hint(smem_addr(kbuf + dst), (const uint8_t *)p.kv.k + off, n, bar, pol);
-        bulk_g2s_hint(smem_addr(vbuf + dst), (const uint8_t *)p.kv.v + off, n, bar, pol);
-      }
     }
   }
 
@@ -812,40 +733,54 @@ struct Step {
     return true;
   }
 
+  // A piece's tiles, the same for the producer and the consumers: tile k
+  // holds tokens tile_base + 1 .. tile_base + kTileTok.  In a contiguous
+  // cache the first starts at the piece's first token, so a piece of
+  // kTileTok tokens is one tile wherever it starts; in a paged cache it
+  // starts with the page holding that token, so every tile is whole pages
+  // (a page split between two tiles would cost a copy in each).
+  __device__ static int tile_start(const Piece &pc) { return PAGED ? (pc.lo - 1) / 16 * 16 : pc.lo - 1; }
+  __device__ static int tile_count(const Piece &pc) {
+    return pc.hi >= pc.lo ? (pc.hi - 1 - tile_start(pc)) / kTileTok + 1 : 0;
+  }
+  __device__ static int tile_base(const Piece &pc, int k) { return tile_start(pc) + k * kTileTok; }
+
   // The tiles of one piece, from stage use n on; returns the next use.
   __device__ static uint32_t copy_piece(const StepParams &p, const Smem &S, const Piece &pc, uint32_t n) {
-    const int t0 = (pc.lo - 1) / kTileTok, t1 = (pc.hi - 1) / kTileTok;
+    const int nt = tile_count(pc);
     if (pc.u < 0 || pc.u >= p.B * p.Hkv || pc.lo < 1 || pc.hi < pc.lo || (!PAGED && pc.hi > p.kv.capacity)) {
-      // a piece outside the cache is refused tile by tile
+      // a piece outside the cache is refused tile by tile: nothing is
+      // copied and no row of its stages counts
 #pragma unroll 1
-      for (int t = t0; t <= t1; ++t, ++n) {
+      for (int k = 0; k < nt; ++k, ++n) {
         if (!acquire_stage(p, S, n)) break;
-        issue_tile(p, S, n % kStages, pc.u, pc.lo, pc.hi, t, t == t0);
+        set_status(p.ctl, MAC_DEV_BAD_COPY);
+        S.mask[n % kStages] = 0;
+        mbar_arrive(smem_addr(&S.full[n % kStages]));
       }
       return n;
     }
     if (PAGED) {
       // a table lookup per 16 rows: the next tile's page ids are loaded
       // (independent loads) before the wait for its stage
-      constexpr int kPg = kTileTok / 16;
       const int32_t *row = p.kv.page_table + (int64_t)(pc.u / p.Hkv) * p.kv.max_pages;
-      int32_t ids[kPg], nxt[kPg];
+      int32_t ids[kSlots], nxt[kSlots];
 #pragma unroll
-      for (int pg = 0; pg < kPg; ++pg) {
-        const int64_t slot = (int64_t)t0 * kPg + pg;
-        ids[pg] = slot < p.kv.max_pages ? __ldg(row + slot) : kNoPage;
+      for (int i = 0; i < kSlots; ++i) {
+        const int64_t slot = (int64_t)(tile_base(pc, 0) / 16) + i;
+        ids[i] = slot < p.kv.max_pages ? __ldg(row + slot) : kNoPage;
       }
 #pragma unroll 1
-      for (int t = t0; t <= t1; ++t, ++n) {
+      for (int k = 0; k < nt; ++k, ++n) {
 #pragma unroll
-        for (int pg = 0; pg < kPg; ++pg) {
-          const int64_t slot = (int64_t)(t + 1) * kPg + pg;
-          nxt[pg] = t < t1 && slot < p.kv.max_pages ? __ldg(row + slot) : kNoPage;
+        for (int i = 0; i < kSlots; ++i) {
+          const int64_t slot = (int64_t)(tile_base(pc, k + 1) / 16) + i;
+          nxt[i] = k + 1 < nt && slot < p.kv.max_pages ? __ldg(row + slot) : kNoPage;
         }
         if (!acquire_stage(p, S, n)) break;
-        issue_paged_tile(p, S, n % kStages, pc, t, t == t0, ids);
+        issue_paged_tile(p, S, n % kStages, pc, tile_base(pc, k), k == 0, ids);
 #pragma unroll
-        for (int pg = 0; pg < kPg; ++pg) ids[pg] = nxt[pg];
+        for (int i = 0; i < kSlots; ++i) ids[i] = nxt[i];
       }
       return n;
     }
@@ -855,17 +790,17 @@ struct Step {
     const uint8_t *kg = (const uint8_t *)p.kv.k + unit_off, *vg = (const uint8_t *)p.kv.v + unit_off;
     const unsigned long long pol = l2_evict_first_policy();
 #pragma unroll 1
-    for (int t = t0; t <= t1; ++t, ++n) {
+    for (int k = 0; k < nt; ++k, ++n) {
       if (!acquire_stage(p, S, n)) break;
       const int st = n % kStages;
-      const int ra = t * kTileTok + 1 > pc.lo ? t * kTileTok + 1 : pc.lo;
-      const int rz = t * kTileTok + kTileTok < pc.hi ? t * kTileTok + kTileTok : pc.hi;
+      const int ra = tile_base(pc, k) + 1;  // the stage's first row
+      const int rz = ra + kTileTok - 1 < pc.hi ? ra + kTileTok - 1 : pc.hi;
       const uint32_t nb = (uint32_t)(rz - ra + 1) * kRowBytes;
       const uint32_t bar = smem_addr(&S.full[st]);
-      S.mask[st] = (1 << (kTileTok / 16)) - 1;
-      mbar_expect_tx(bar, 2u * nb + (t == t0 ? (uint32_t)kQBytes : 0u));
-      if (t == t0) copy_q(p, S, st, pc.u, bar);
-      uint8_t *kbuf = S.stage + (size_t)st * kStageBytes + (size_t)(ra - t * kTileTok - 1) * kRowBytes;
+      S.mask[st] = (1 << (kTileTok / 16)) - 1;  // (rows past pc.hi are excluded by position)
+      mbar_expect_tx(bar, 2u * nb + (k == 0 ? (uint32_t)kQBytes : 0u));
+      if (k == 0) copy_q(p, S, st, pc.u, bar);
+      uint8_t *kbuf = S.stage + (size_t)st * kStageBytes;
       bulk_g2s_hint(smem_addr(kbuf), kg + (size_t)(ra - 1) * kRowBytes, nb, bar, pol);
       bulk_g2s_hint(smem_addr(kbuf + kStageBytes / 2), vg + (size_t)(ra - 1) * kRowBytes, nb, bar, pol);
     }
@@ -1349,8 +1284,7 @@ struct Step {
     float m_mine = kMInit, l_mine = 0.f;
     unsigned long long wait_ns = 0;  // traced band waits (kept in a register)
 
-    const int64_t tile0 = (pc.lo - 1) / kTileTok;
-    const int ntiles = (int)((pc.hi - 1) / kTileTok - tile0 + 1);
+    const int ntiles = tile_count(pc);
     for (int k = 0; k < ntiles; ++k, ++n) {
       const int st = n % kStages;
       const unsigned long long tw = tr_all ? globaltimer() : 0ull;
@@ -1371,7 +1305,7 @@ struct Step {
       }
       const uint8_t *kb = S.stage + (size_t)st * kStageBytes;
       const uint8_t *vb = kb + kStageBytes / 2;
-      const int t0 = (int)((tile0 + k) * kTileTok);
+      const int t0 = tile_base(pc, k);  // stage row i holds token t0 + 1 + i
       // partial scores of the group's kATPG tokens for the G heads
       float v[kAV];
 #pragma unroll
@@ -1389,7 +1323,10 @@ struct Step {
       float s = reduce_scores(v, lane);
       const int row_m = ti * kAGroups + grp;
       const int t_m = t0 + row_m + 1;
-      const bool valid = ok && t_m >= lo_mine && t_m <= pc.hi && ((S.mask[st] >> (row_m >> 4)) & 1);
+      // a contiguous tile holds the piece's tokens from its first row on (or
+      // nothing, for a refused piece); a paged tile the pages its mask lists
+      const int msk = S.mask[st];
+      const bool valid = ok && t_m >= lo_mine && t_m <= pc.hi && (PAGED ? ((msk >> (row_m >> 4)) & 1) != 0 : msk != 0);
       s = valid ? s : -INFINITY;
       // lazy running max (per group and head): raised only when a score
       // exceeds it by kLazy
@@ -1412,8 +1349,8 @@ struct Step {
       l_mine += w;
       // rows the piece did not copy hold stale bytes, possibly NaN patterns,
       // and 0 * NaN is NaN: in a partly covered tile they are zeroed
-      const int msk = S.mask[st];
-      const bool whole = t0 + 1 >= pc.lo && t0 + kTileTok <= pc.hi && msk == (1 << (kTileTok / 16)) - 1;
+      const bool whole = t0 + kTileTok <= pc.hi &&
+                         (PAGED ? t0 + 1 >= pc.lo && msk == (1 << (kTileTok / 16)) - 1 : msk != 0);
 #pragma unroll
       for (int tt = 0; tt < kATPG; ++tt) {
         const int row = tt * kAGroups + grp;
@@ -1423,7 +1360,8 @@ struct Step {
           raw[c] = *reinterpret_cast<const uint4 *>(vb + row * kRowBytes + sub * 8 * (int)sizeof(T) + c * 16);
         if (!whole) {
           const int t = t0 + row + 1;
-          const uint32_t vm = (t >= pc.lo && t <= pc.hi && ((msk >> (row >> 4)) & 1)) ? ~0u : 0u;
+          const uint32_t vm =
+              (PAGED ? t >= pc.lo && t <= pc.hi && ((msk >> (row >> 4)) & 1) != 0 : t <= pc.hi && msk != 0) ? ~0u : 0u;
 #pragma unroll
           for (int c = 0; c < kALoads; ++c) raw[c] = make_uint4(raw[c].x & vm, raw[c].y & vm, raw[c].z & vm, raw[c].w & vm);
         }

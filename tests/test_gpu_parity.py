@@ -268,14 +268,18 @@ def test_miss_path_bitwise_equals_full_attention():
     layer.release()
 
 
-def test_paged_bitwise_equals_contiguous():
+def test_paged_equals_contiguous():
+    # The same cache, contiguous and paged: identical decisions, and outputs
+    # that differ only in summation order (a contiguous tile starts at its
+    # piece's first token, a paged one at that token's page), far inside
+    # the parity tolerance.
     w = W(B=2, Hq=8, Hkv=2, ctx=(1000, 2500), K=64, r=32, steps=20, query="ar1_skew", tau=0.45)
     a, st_a, la = gpu_trajectory(Problem(w, n_seed=64), w.n_steps)
     b, st_b, lb = gpu_trajectory(Problem(w, n_seed=64, paged=True), w.n_steps)
     assert st_a == 0 and st_b == 0
     for (oa, pa), (ob, pb) in zip(a, b):
         assert np.array_equal(pa, pb)
-        assert np.array_equal(oa, ob)
+        assert rel_err(oa, ob).max() <= 1e-5
     la.release()
     lb.release()
 
