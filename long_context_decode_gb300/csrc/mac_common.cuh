@@ -91,8 +91,10 @@ __host__ __device__ inline TileCounts tile_counts(int K, int r, int64_t max_cont
 // long-band pieces follow at B*Hkv + u + c.  A long band run over more than
 // kGroupCtas CTAs is merged in two levels: CTA group k = c / kGroupCtas
 // first, into group slot u + k (unique for the same reason), then the
-// groups.  The per-head minima are double-buffered: decode launch k
-// combines into buffer k & 1 and clears the other for launch k + 1.
+// groups.  The per-head minima and the match's chunk counter live in the
+// ring workspace (its match state), double-buffered by the ring's step
+// count: step k on a ring combines into copy k & 1 and clears the other for
+// step k + 1, so a step needs nothing from the scratch before its match.
 //
 // Ring kernel (G = 8): window tile t of unit u leaves its partial in part_w
 // slot u * nt + t; the long bands are cut over the CTAs as above, the CTA
@@ -104,9 +106,11 @@ __host__ __device__ inline TileCounts tile_counts(int K, int r, int64_t max_cont
 // Everything before `parts` starts at zero and a clean launch leaves it so.
 struct ScratchLayout {
   size_t ctl;        // uint32[64]: [0] status word, [2..3] grid-barrier counter (u64),
-                     // [4] CTAs of the running launch finished (the last resets
-                     // it), [6] decode launch count
+                     // [4] CTAs of the running launch finished (full attention
+                     // and the ring kernel; the last resets it), [6] decode
+                     // launch count
   size_t best;       // uint64 [2][B][Hq]: ~(dist bits << 32 | ~pos) of the best candidate, 0 = none
+                     // (ring kernel; the span kernel keeps its minima in the ring workspace)
   size_t unit_done;  // uint32 [2][B*Hkv]: pieces (or groups) of the unit finished
   size_t group_done; // uint32 [2][B*Hkv + kGroups]: long-band pieces finished per (unit, CTA group)
   size_t parts;      // first partial (nothing from here on needs clearing)

@@ -324,14 +324,15 @@ struct Step {
   // exclusive prefix of the tail lengths, the CTA spans, their non-empty
   // counts and every unit's CTA run.  With at most as many units as CTAs,
   // unit u owns the CTAs [u*P/U, (u+1)*P/U) and its tail is cut evenly among
-  // the first k' of them, k' = min(its CTAs, length / kMinSpan rounded up),
+  // the first k' of them, k' = min(its CTAs, length / kMinTail rounded up),
   // so no CTA meets two units (a second piece would double its fixed costs)
   // nor gets a sliver, and everything but the prefix has a closed form; with
   // more units the tails, laid end to end, are cut into equal spans.
-  static constexpr int kMinSpan = 64;  // tokens: a piece worth its fixed cost
+  static constexpr int kMinTail = 64;  // tokens: a tail piece worth its fixed cost
+  static constexpr int kMinSpan = 64;  // tokens: a long-band span worth its fixed cost
   __device__ static int tail_ctas(int64_t len, int k) {
     if (len <= 0) return 0;
-    const int64_t want = (len + kMinSpan - 1) / kMinSpan;
+    const int64_t want = (len + kMinTail - 1) / kMinTail;
     return want < k ? (int)want : k;
   }
   __device__ static void layout_tails(const StepParams &p, const Smem &S) {
