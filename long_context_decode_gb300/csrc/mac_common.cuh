@@ -418,6 +418,14 @@ __device__ __forceinline__ void rope_angle(int64_t pos, unsigned long long f, fl
   __sincosf(a, s, c);
 }
 
+// b - c for a bf16 b (its bits) and an f32 c, rounded once to f32 (the
+// mixed-precision subtraction of sm_100 and later)
+__device__ __forceinline__ float bf16_minus_f32(uint16_t b, float c) {
+  float d;
+  asm("sub.rn.f32.bf16 %0, %1, %2;" : "=f"(d) : "h"(b), "f"(c));
+  return d;
+}
+
 template <typename T>
 __device__ __forceinline__ float elem_f32(const void *base, int64_t i);
 template <>

@@ -964,12 +964,26 @@ struct Step {
     float2 df[kPairs];
 #pragma unroll
     for (int c = 0; c < kNP; ++c) {
-      float2 e2[kPer / 2];
-      unpack16x2<T>(*reinterpret_cast<const uint4 *>(row + c * 128 + sub * 16), e2);
+      const uint4 raw = *reinterpret_cast<const uint4 *>(row + c * 128 + sub * 16);
+      if constexpr (sizeof(T) == 2) {
+        // b - q straight from the bf16 element (one mixed-precision
+        // subtraction each, exact widening then one rounding): the negation
+        // of the difference, which squares to the same value
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int k = 0; k < kPer / 2; ++k) {
-        const float2 q = qv[c * (kPer / 2) + k];
-        df[c * (kPer / 2) + k] = __fadd2_rn(q, make_float2(-e2[k].x, -e2[k].y));
+        for (int k = 0; k < 4; ++k) {
+          const float2 q = qv[c * 4 + k];
+          df[c * 4 + k] = make_float2(bf16_minus_f32((uint16_t)(w[k] & 0xffffu), q.x),
+                                      bf16_minus_f32((uint16_t)(w[k] >> 16), q.y));
+        }
+      } else {
+        float2 e2[kPer / 2];
+        unpack16x2<T>(raw, e2);
+#pragma unroll
+        for (int k = 0; k < kPer / 2; ++k) {
+          const float2 q = qv[c * (kPer / 2) + k];
+          df[c * (kPer / 2) + k] = __fadd2_rn(q, make_float2(-e2[k].x, -e2[k].y));
+        }
       }
     }
     float2 t[4];
