@@ -646,13 +646,24 @@ struct Step {
   // The squared distance over the lane's 8 dims of one half of a row (exact
   // bf16 differences, squares summed in a pairwise tree).
   __device__ static float half_dist(const float2 (&qv)[4], const uint8_t *src) {
-    float2 e[4];
-#pragma unroll
-    for (int c = 0; c < kHalfLoads; ++c)
-      unpack16x2<T>(*reinterpret_cast<const uint4 *>(src + c * 16), e + c * (4 / kHalfLoads));
     float2 df[4];
+    if constexpr (sizeof(T) == 2) {
+      // b - q straight from the bf16 element (one mixed-precision
+      // subtraction each): the negation of the difference, same square
+      const uint4 raw = *reinterpret_cast<const uint4 *>(src);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) df[k] = __fadd2_rn(qv[k], make_float2(-e[k].x, -e[k].y));
+      for (int k = 0; k < 4; ++k)
+        df[k] = make_float2(bf16_minus_f32((uint16_t)(w[k] & 0xffffu), qv[k].x),
+                            bf16_minus_f32((uint16_t)(w[k] >> 16), qv[k].y));
+    } else {
+      float2 e[4];
+#pragma unroll
+      for (int c = 0; c < kHalfLoads; ++c)
+        unpack16x2<T>(*reinterpret_cast<const uint4 *>(src + c * 16), e + c * (4 / kHalfLoads));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) df[k] = __fadd2_rn(qv[k], make_float2(-e[k].x, -e[k].y));
+    }
     const float2 t0 = __ffma2_rn(df[2], df[2], __fmul2_rn(df[0], df[0]));
     const float2 t1 = __ffma2_rn(df[3], df[3], __fmul2_rn(df[1], df[1]));
     const float2 t = __fadd2_rn(t0, t1);
