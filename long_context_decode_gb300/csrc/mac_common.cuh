@@ -106,9 +106,8 @@ __host__ __device__ inline TileCounts tile_counts(int K, int r, int64_t max_cont
 // Everything before `parts` starts at zero and a clean launch leaves it so.
 struct ScratchLayout {
   size_t ctl;        // uint32[64]: [0] status word, [2..3] grid-barrier counter (u64),
-                     // [4] CTAs of the running launch finished (full attention
-                     // and the ring kernel; the last resets it), [6] decode
-                     // launch count
+                     // [4] CTAs of the running launch finished (ring kernel;
+                     // the last resets it), [6] decode launch count
   size_t best;       // uint64 [2][B][Hq]: ~(dist bits << 32 | ~pos) of the best candidate, 0 = none
                      // (ring kernel; the span kernel keeps its minima in the ring workspace)
   size_t unit_done;  // uint32 [2][B*Hkv]: pieces (or groups) of the unit finished

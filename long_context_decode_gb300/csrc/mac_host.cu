@@ -313,6 +313,15 @@ cudaError_t launch_step(StepParams p, const mac_config *c, cudaStream_t s) {
     p.tc = launch_tiles(c, p.sink_piece != 0);
     return f32 ? ring::launch_f32_g8(p, grid, s) : ring::launch_bf16_g8(p, grid, s);
   }
+  if (p.mode == MODE_FULL) {
+    // Full attention counts pieces into its merges without a grid barrier
+    // before them, so it cannot clear counts a failed launch left behind
+    // (a decode step clears them before its barrier): they are cleared
+    // here, ahead of it on the stream.
+    const ScratchLayout S = scratch_layout(c);
+    const cudaError_t e = cudaMemsetAsync(p.unit_done, 0, S.parts - S.unit_done, s);
+    if (e != cudaSuccess) return e;
+  }
   if (p.sink_piece) return f32 ? launch_step_f32_sink(p, grid, s) : launch_step_bf16_sink(p, grid, s);
   if (p.trace && !f32) return launch_step_bf16_trace(p, grid, s);  // the only traced instantiation
   return f32 ? launch_step_f32(p, grid, s) : launch_step_bf16(p, grid, s);

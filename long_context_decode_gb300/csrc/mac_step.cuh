@@ -2133,7 +2133,8 @@ struct Step {
           stamp(trace, 2);
           scratch_ready();
           // the merge counts start from zero, also after a launch that
-          // failed with counts left over (no merge runs before the barrier)
+          // failed with counts left over (no merge runs before the barrier;
+          // the host clears them ahead of a full-attention launch)
 #pragma unroll 1
           for (int i = blockIdx.x * kConsumers + tid; i < n_units + kGroups; i += gridDim.x * kConsumers) {
             if (i < n_units) p.unit_done[i] = 0u;
@@ -2172,23 +2173,6 @@ struct Step {
         const uint32_t bar = smem_addr(&S.full[j % kStages]);
         const long long t1 = clock64();
         while (!mbar_try_wait(bar, (j / kStages) & 1u) && clock64() - t1 < (1LL << 30)) {
-        }
-      }
-    }
-    if (tid == 0 && !decode) {
-      // full attention has no grid barrier before its merges: the last CTA
-      // to finish a failed launch clears the piece counts its merges may
-      // have left (a decode step clears them before its grid barrier, so
-      // its CTAs exit without waiting on a count)
-      __threadfence();
-      const uint32_t old = atomicAdd(p.ctl + 4, 1u);
-      if (old == gridDim.x - 1) {  // every CTA of the launch has finished
-        p.ctl[4] = 0;
-        if (*(volatile uint32_t *)p.ctl != 0) {
-#pragma unroll 1
-          for (int u = 0; u < n_units; ++u) p.unit_done[u] = 0;
-#pragma unroll 1
-          for (int u = 0; u < n_units + kGroups; ++u) p.group_done[u] = 0;
         }
       }
     }

@@ -129,3 +129,39 @@ def test_a_withheld_stage_runs_the_wait_out(Hq, Hkv, mode):
         O.seed_rings(ocfg, ring, P.q_seed(), P.L, okv)
         ref = O.decode_step(ocfg, ring, P.q_step(0), P.m(0), okv)["out"]
     assert rel_err(res, ref).max() <= TOL
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 2)])
+@pytest.mark.parametrize("first", ["decode", "full"])
+def test_full_attention_after_a_failed_launch_on_the_same_scratch(Hq, Hkv, first):
+    # A launch that fails (a withheld stage runs its wait out) may leave
+    # merge counts behind in the scratch.  Full attention on the same
+    # scratch, with no reset in between and the status left unread, must
+    # still be exact: its counts start from zero.
+    w = W(Hq=Hq, Hkv=Hkv, steps=1)
+    P = Problem(w, n_seed=w.ring_k)
+    cfg = P.cfg()
+    kv = P.kv()
+    B, H, d = w.batch, w.n_q_heads, w.head_dim
+    q = to_dev(P.q_step(0), P.dev)
+    m = torch.from_numpy(P.m(0)).to(P.dev)
+    layer = mac.MacLayer(cfg, device=P.dev)
+    mac.mac_init_rings(cfg, layer.ring, layer.scratch, to_dev(P.q_seed(), P.dev),
+                       torch.from_numpy(P.L).to(P.dev), P.n_seed, kv)
+    torch.cuda.synchronize()
+    out = torch.empty(B, H, d, device=P.dev)
+    mp = torch.empty(B, H, dtype=torch.int32, device=P.dev)
+    mac.mac_test_wait_budget(1 << 16, 1)
+    if first == "decode":
+        mac.mac_decode_step(cfg, layer.ring, layer.scratch, q, m, kv, out, mp, None, None)
+    else:
+        mac.mac_full_attention(cfg, layer.scratch, q, m, kv, out, None)
+    torch.cuda.synchronize()
+    out2 = torch.empty(B, H, d, device=P.dev)
+    mac.mac_full_attention(cfg, layer.scratch, q, m, kv, out2, None)
+    torch.cuda.synchronize()
+    status = mac.mac_last_status(cfg, layer.scratch)
+    assert status & mac.MAC_DEV_WAIT_TIMEOUT, status  # the failed launch's report, still unread
+    ref, _ = O.full_attention(P.ocfg(), P.q_step(0), P.m(0), P.okv())
+    assert rel_err(out2.double().cpu().numpy(), ref).max() <= TOL
+    layer.release()
