@@ -510,12 +510,14 @@ struct Step {
         }
       }
       const unsigned bal = __ballot_sync(kFull, sh);
-      if (u < U) S.offB[u + 1] = cb + x;
+      if (u < U) {
+        S.offB[u + 1] = cb + x;
+        S.runB[u] = make_short2(0, -1);  // no CTA run (band_runs_block marks the long bands')
+      }
       if (sh) {
         const int j = ns + __popc(bal & ((1u << lane) - 1u));
         S.shortU[j] = u;
         S.scp[j + 1] = cc + y;
-        S.runB[u] = make_short2(0, -1);
       }
       cb += __shfl_sync(kFull, x, 31);
       cc += __shfl_sync(kFull, y, 31);
@@ -626,9 +628,20 @@ struct Step {
     const int ef = flag_scan(S, c < P && S.spanB[c] < S.spanB[c + 1], &tot);
     if (c < P) S.neB[c] = ef;
     if (c == 0) S.neB[P] = tot;
+    // Every long band's run, scattered from the non-empty spans: span c
+    // holds global index x iff span[c] <= x < span[c+1] (the CTA cta_of
+    // finds), so CTA c's thread marks the bands whose segment starts or ends
+    // in its span -- each start and each end lies in exactly one.  One
+    // search over the units per thread replaces two over the CTAs per band.
+    if (c < P && S.spanB[c] < S.spanB[c + 1]) {
+      const int64_t a = S.spanB[c], z = S.spanB[c + 1], *off = S.offB;
 #pragma unroll 1
-    for (int u = c; u < U; u += kConsumers)
-      if (!short_band(p, S, u)) S.runB[u] = find_run(S, 1, u);
+      for (int u = unit_of(off, U, a); u < U && off[u] < z; ++u) {
+        if (off[u + 1] <= off[u]) continue;  // no long band
+        if (off[u] >= a) S.runB[u].x = (short)c;
+        if (off[u + 1] - 1 < z) S.runB[u].y = (short)c;
+      }
+    }
     consumer_sync();
   }
 
