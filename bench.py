@@ -215,7 +215,7 @@ def run_mac(args, rank, world, local):
     # 32K and 256K beside the 128K line (one GPU: each is its own replica
     # stack, measured after the main one has released its memory)
     if (world == 1 and args.context_steps > 0 and args.workload == "long-128k" and not args.ring_k
-            and not args.front_sink):
+            and not args.front_sink and not args.kv_heads):
         from long_context_decode_gb300.workloads import WORKLOADS
         ctx = {}
         for name in EXTRA_CONTEXTS:
@@ -693,11 +693,14 @@ def cpu_baseline(w0, args, budget_s=20.0):
 
 
 def select_workload(args):
-    """The named workload, with its ring capacity replaced when --ring-k is given."""
-    from long_context_decode_gb300.workloads import WORKLOADS, with_ring_k
+    """The named workload, with its ring capacity replaced when --ring-k is
+    given and its KV-head count when --kv-heads is."""
+    from long_context_decode_gb300.workloads import WORKLOADS, with_kv_heads, with_ring_k
     w0 = WORKLOADS[args.workload]
     k = getattr(args, "ring_k", None)
-    return with_ring_k(w0, k) if k else w0
+    w0 = with_ring_k(w0, k) if k else w0
+    hkv = getattr(args, "kv_heads", None)
+    return with_kv_heads(w0, hkv) if hkv else w0
 
 
 def run_reference(args, rank, world):
@@ -734,6 +737,9 @@ def main():
                     help="front-sink isolation: tokens [1, F] out of the summaries, attended every step")
     ap.add_argument("--ring-k", type=int, default=None,
                     help="ring capacity K in place of the workload's (the K sweep, e.g. 512)")
+    ap.add_argument("--kv-heads", type=int, default=None,
+                    help="KV heads in place of the workload's (another GQA group size; 4 with 32 query heads "
+                         "runs the GQA-8 kernel)")
     ap.add_argument("--layers", type=int, default=32)
     ap.add_argument("--profile-steps", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=64)

@@ -212,6 +212,18 @@ def with_ring_k(w: Workload, ring_k: int) -> Workload:
                    description=w.description.replace(f"K={w.ring_k}", f"K={ring_k}"))
 
 
+def with_kv_heads(w: Workload, n_kv_heads: int) -> Workload:
+    """The same workload with another number of KV heads (another GQA group
+    size: 32q/4kv runs the GQA-8 path)."""
+    if n_kv_heads == w.n_kv_heads:
+        return w
+    if n_kv_heads < 1 or w.n_q_heads % n_kv_heads:
+        raise ValueError(f"{n_kv_heads} KV heads do not divide {w.n_q_heads} query heads")
+    return w.with_(n_kv_heads=n_kv_heads, name=f"{w.name}-kv{n_kv_heads}",
+                   description=w.description.replace(f"{w.n_q_heads}q/{w.n_kv_heads}kv",
+                                                     f"{w.n_q_heads}q/{n_kv_heads}kv"))
+
+
 def shuffled_page_table(rng: np.random.Generator, batch: int, pages_per_req: int) -> np.ndarray:
     """[B, pages_per_req] physical page ids: a random permutation of all pages."""
     perm = rng.permutation(batch * pages_per_req).astype(np.int32)
